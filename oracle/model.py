@@ -1,0 +1,232 @@
+"""ORACLE — test infrastructure only.  Python model of the paged pool, its
+free list, the per-request page tables and the per-token transaction.
+
+Sources restated here:
+
+* "Incremental Serving", section "Request flow": ``begin_token()`` reserves the
+  next logical position; every layer calls ``append_and_attend(q, k, v)`` with
+  [1, H, 1, d_h] tensors; ``commit_token()`` makes the position visible; after a
+  failure ``abort_token()`` leaves the visible length unchanged.
+* Same page, section "Paged KV-cache layout": per layer, key and value pages
+  [physical_page, head, page_offset, head_width]; a request owns a logical page
+  table; one physical page id addresses the matching page in every layer; pages
+  are leased lazily as a sequence grows and returned on reset or destroy; page
+  size 16 by default; a block count of 0 sizes the pool for one maximum-length
+  context.
+* "38 · Cached generation", sections "Bind one decoder to its model-wide cache"
+  and "Assemble model-wide tolerance, work, generation, reset, and exact error
+  evidence": every layer advances together; work counters advance only when a
+  token commits (cache appends = layers per token, cached attention-score
+  values = lanes x retained length per token); reset clears length and work;
+  a rejected operation leaves the state unchanged.
+
+Readings where the sources are silent (each also listed in the design notes):
+
+* free list: FIFO queue initialised to a Fisher-Yates shuffle of 0..pages-1
+  driven by SplitMix64(seed), swap index ``next() mod (i + 1)`` for i from
+  pages-1 down to 1; lease pops the front, release pushes the request's pages
+  to the back in logical order;
+* ``abort_token`` returns a page leased by its ``begin_token`` to the front of
+  the free list, so the pool is exactly as before ``begin_token``;
+* the new row is written into its slot by ``append_and_attend``; it is visible
+  only once committed because readers stop at the visible length;
+* ``begin_token`` at ``max_context`` reports capacity exhaustion.
+"""
+from __future__ import annotations
+
+import collections
+
+import numpy as np
+
+from . import F32, paged_decode_attention, append as _append
+
+MASK64 = (1 << 64) - 1
+
+
+class Status:
+    OK = 0
+    INVALID_ARGUMENT = 1
+    OUT_OF_PAGES = 2
+    CAPACITY_EXCEEDED = 3
+    BAD_STATE = 4
+
+
+class OracleError(Exception):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def _splitmix64(seed: int):
+    """SplitMix64 (Steele, Lea & Flood 2014): state += golden gamma, then mix."""
+    state = seed & MASK64
+    while True:
+        state = (state + 0x9E3779B97F4A7C15) & MASK64
+        z = state
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+        yield z ^ (z >> 31)
+
+
+def shuffled_pages(n: int, seed: int) -> list:
+    """Fisher-Yates shuffle of 0..n-1 with SplitMix64(seed)."""
+    a = list(range(n))
+    g = _splitmix64(seed)
+    for i in range(n - 1, 0, -1):
+        j = next(g) % (i + 1)
+        a[i], a[j] = a[j], a[i]
+    return a
+
+
+def cached_score_cells(lanes: int, retained_lengths) -> int:
+    """Score values formed by cached decode: lanes x t for each retained length t
+    ("38 · Cached generation", "Count attention-score cells, not total runtime")."""
+    return sum(lanes * t for t in retained_lengths)
+
+
+class OraclePool:
+    """Per-layer K/V pools [pages, H, P, D] (storage dtype) plus a FIFO free list."""
+
+    def __init__(self, layers: int, pages: int, heads: int, head_dim: int, page_size: int = 16,
+                 dtype: int = F32, max_context: int = 0, seed: int = 0, storage: bool = True):
+        if layers < 1 or heads < 1 or head_dim < 1 or page_size < 1 or max_context < 1 or pages < 0:
+            raise OracleError(Status.INVALID_ARGUMENT, "bad pool geometry")
+        if pages == 0:
+            pages = -(-max_context // page_size)       # one maximum-length context
+        self.layers, self.pages, self.H, self.D, self.P = layers, pages, heads, head_dim, page_size
+        self.dtype, self.max_context = dtype, max_context
+        self.max_pages_per_request = -(-max_context // page_size)
+        self.free = collections.deque(shuffled_pages(pages, seed))
+        sd = np.float32 if dtype == F32 else np.uint16
+        if storage:
+            self.k = np.zeros((layers, pages, heads, page_size, head_dim), dtype=sd)
+            self.v = np.zeros_like(self.k)
+        else:
+            self.k = self.v = None
+        self.requests = []
+
+    def bytes(self) -> int:
+        """Device bytes of the K and V pools: 2 * layers * pages * P * H * D * element size."""
+        es = 4 if self.dtype == F32 else 2
+        return 2 * self.layers * self.pages * self.P * self.H * self.D * es
+
+    def request(self) -> "OracleRequest":
+        r = OracleRequest(self)
+        self.requests.append(r)
+        return r
+
+
+class OracleRequest:
+    """One request: logical page table, visible length, pending token, counters."""
+
+    def __init__(self, pool: OraclePool):
+        self.pool = pool
+        self.table = []
+        self.length = 0
+        self.pending = None             # dict(pos, leased, appended:set) while a token is open
+        self.committed_tokens = 0
+        self.cache_appends = 0
+        self.score_cells = 0
+
+    # -- leasing ---------------------------------------------------------------
+    def lease_pages(self, n: int) -> None:
+        p = self.pool
+        if self.pending is not None:
+            raise OracleError(Status.BAD_STATE, "token pending")
+        if n < 0:
+            raise OracleError(Status.INVALID_ARGUMENT, "negative count")
+        if len(self.table) + n > p.max_pages_per_request:
+            raise OracleError(Status.CAPACITY_EXCEEDED, "beyond one maximum-length context")
+        if n > len(p.free):
+            raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
+        for _ in range(n):
+            self.table.append(p.free.popleft())
+
+    def release_pages(self) -> None:
+        """Reset: every page back to the pool (logical order), length and work zeroed."""
+        if self.pending is not None:
+            raise OracleError(Status.BAD_STATE, "token pending")
+        self.pool.free.extend(self.table)
+        self.table = []
+        self.length = 0
+        self.committed_tokens = self.cache_appends = self.score_cells = 0
+
+    def destroy(self) -> None:
+        if self.pending is not None:
+            self.abort_token()
+        self.release_pages()
+        self.pool.requests.remove(self)
+
+    # -- the transaction ------------------------------------------------------
+    def begin_token(self) -> int:
+        p = self.pool
+        if self.pending is not None:
+            raise OracleError(Status.BAD_STATE, "token already pending")
+        if self.length >= p.max_context:
+            raise OracleError(Status.CAPACITY_EXCEEDED, "maximum context reached")
+        leased = None
+        if self.length // p.P >= len(self.table):
+            if not p.free:
+                raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
+            leased = p.free.popleft()
+            self.table.append(leased)
+        self.pending = dict(pos=self.length, leased=leased, appended=set())
+        return self.length
+
+    def append_and_attend(self, layer: int, q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                          compute: bool = True):
+        """q [H, D] fp32; k, v [H, D] storage dtype.  Returns out [H, D] fp64 (or None)."""
+        p = self.pool
+        if self.pending is None:
+            raise OracleError(Status.BAD_STATE, "no token pending")
+        if not 0 <= layer < p.layers:
+            raise OracleError(Status.INVALID_ARGUMENT, "layer out of range")
+        if layer in self.pending["appended"]:
+            raise OracleError(Status.BAD_STATE, "layer already appended for this token")
+        t = self.pending["pos"] + 1
+        tables = np.asarray(self.table, dtype=np.int32)[None, :]
+        lens = np.asarray([t], dtype=np.int32)
+        kp, vp = p.k[layer], p.v[layer]
+        if compute:
+            out = paged_decode_attention(kp, vp, q[None], k[None], v[None], tables, lens, p.dtype)[0]
+        else:
+            _append(kp, vp, k[None], v[None], tables, lens, p.dtype)
+            out = None
+        self.pending["appended"].add(layer)
+        return out
+
+    def commit_token(self) -> None:
+        p = self.pool
+        if self.pending is None:
+            raise OracleError(Status.BAD_STATE, "no token pending")
+        if len(self.pending["appended"]) != p.layers:
+            raise OracleError(Status.BAD_STATE, "not every layer appended")
+        t = self.pending["pos"] + 1
+        self.length = t
+        self.committed_tokens += 1
+        self.cache_appends += p.layers
+        self.score_cells += p.layers * p.H * t
+        self.pending = None
+
+    def abort_token(self) -> None:
+        if self.pending is None:
+            raise OracleError(Status.BAD_STATE, "no token pending")
+        if self.pending["leased"] is not None:
+            page = self.table.pop()
+            assert page == self.pending["leased"]
+            self.pool.free.appendleft(page)
+        self.pending = None
+
+
+def complete_prefix_score_cells(lanes: int, lengths) -> int:
+    """Dense causal score grid cells rebuilt by complete-prefix replay: lanes x t^2 each."""
+    return sum(lanes * t * t for t in lengths)
+
+
+def bytes_per_session(layers: int, heads: int, head_dim: int, positions: int, elem_bytes: int) -> int:
+    """KV-cache bytes of one session: 2 * L * H * d_h * S * element size."""
+    return 2 * layers * heads * head_dim * positions * elem_bytes
+
+
+__all__ = ["Status", "OracleError", "OraclePool", "OracleRequest", "shuffled_pages",
+           "cached_score_cells", "complete_prefix_score_cells", "bytes_per_session"]

@@ -1,0 +1,78 @@
+"""Pin sensitivity: plant plausible mistakes in copies of the oracle (CPU only)
+and check that the pins reject every one of them."""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import F32, BF16
+from tests._helpers import PagedCase, dense_causal_last_row, to_f64
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attention.c")
+
+MUTANTS = {
+    "scale_dropped": ("const double scale = 1.0 / sqrt((double)D);", "const double scale = 1.0;"),
+    "scale_squared": ("const double scale = 1.0 / sqrt((double)D);", "const double scale = 1.0 / D;"),
+    "new_key_excluded": ("seq_lens[b], h, scores,", "seq_lens[b] - 1 + (seq_lens[b] == 1), h, scores,"),
+    "slot_index": ("int64_t off = pool_offset(page, h, j % P, H, P, D);",
+                   "int64_t off = pool_offset(page, h, (j + 1) % P, H, P, D);"),
+    "page_index": ("int64_t page = table[j / P];\n        if", "int64_t page = table[j / (P + 1)];\n        if"),
+    "k_for_v": ("mix += scores[j] * load_elem(v_pool,", "mix += scores[j] * load_elem(k_pool,"),
+    "no_normalise": ("scores[j] /= sum;", "scores[j] /= 1.0;"),
+    "no_max_shift_sign": ("scores[j] = exp(scores[j] - m);", "scores[j] = exp(m - scores[j]);"),
+    "append_slot": ("pool_offset(page, h, pos % P, H, P, D);", "pool_offset(page, h, (pos + 1) % P, H, P, D);"),
+    "first_table_row": ("tables + (int64_t)b * max_pages, seq_lens[b]", "tables, seq_lens[b]"),
+    "layout_transposed": ("return ((page * H + head) * P + slot) * (int64_t)D;",
+                          "return ((page * P + slot) * H + head) * (int64_t)D;"),
+    "bf16_shift": ("<< 16;   /* bf16", "<< 15;   /* bf16"),
+    "head_of_query": ("q + lane * D,", "q + (int64_t)b * H * D,"),
+}
+
+
+def _pins_pass(lib) -> bool:
+    """The pins of test_oracle_pins, run against one library."""
+    try:
+        for lens, H, D, P, dtype in [([5, 17, 33], 2, 2, 16, F32), ([31, 48, 2], 2, 8, 16, BF16),
+                                     ([1], 2, 4, 16, F32)]:
+            case = PagedCase(lens, H, D, P, dtype, seed=11)
+            kp, vp = case.k_pool.copy(), case.v_pool.copy()
+            out = oracle.paged_decode_attention(kp, vp, case.q, case.k_new, case.v_new,
+                                                case.tables, case.seq_lens, dtype, library=lib)
+            for b in range(case.B):
+                pg, slot = case.tables[b, (lens[b] - 1) // P], (lens[b] - 1) % P
+                if not np.array_equal(kp[pg, :, slot], case.k_new[b]):
+                    return False
+                for h in range(H):
+                    lane = b * H + h
+                    ref, _ = dense_causal_last_row(case.query_rows(b, h), to_f64(case.K[lane], dtype),
+                                                   to_f64(case.V[lane], dtype))
+                    if not np.allclose(out[b, h], ref, rtol=0, atol=1e-12):
+                        return False
+    except (ValueError, FloatingPointError):
+        return False
+    return True
+
+
+def _compile(tmp_path, name, text):
+    src = tmp_path / f"{name}.c"
+    src.write_text(text)
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", str(src), "-o", str(so), "-lm"],
+                   check=True, capture_output=True)
+    return oracle.load(str(so))
+
+
+def test_unmutated_copy_passes(tmp_path):
+    assert _pins_pass(_compile(tmp_path, "clean", open(SRC).read()))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(tmp_path, name):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not found exactly once"
+    lib = _compile(tmp_path, name, text.replace(old, new))
+    with np.errstate(all="ignore"):
+        assert not _pins_pass(lib), f"pins accepted mutant {name}"
