@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Paged decode attention benchmark (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+
+A step is one pass of the whole decode path over one batch: the plan, the
+fused append + split attention kernel and the split merge, for every request
+of the workload (one layer).  Inputs are synthetic and seeded; the K/V history
+is resident in HBM before timing starts.  The default workload is the
+long-context batch: 16 requests x 131072 tokens, H=8, d_h=128, bf16 pages of
+16 tokens (8.6 GB of K/V per step, far larger than L2, so no flush is needed).
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (the
+only other place this script runs the oracle), one bounded sample per step.
+For N > 1 (torchrun), every rank runs its own replica of the workload (weak
+scaling, no data-path collective); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of 8 TB/s) and decode tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- workload --
+
+def make_workload(name: str, rank: int = 0):
+    from synth import workloads
+    w = workloads.REGISTRY[name]()
+    w.seed += 1000 * rank          # each replica draws its own values
+    return w
+
+
+def describe(w) -> str:
+    st = "fp32" if w.elem_bytes == 4 else "bf16"
+    if w.name == "long":
+        return (f"long context: {w.B} requests x {int(w.seq_lens[0])} tokens, H={w.H}, d_h={w.D}, "
+                f"{st} pages of {w.P}")
+    if w.name.startswith("batched"):
+        return (f"batched decode: {w.B} requests, t ~ U[1,4096], H={w.H}, d_h={w.D}, {st}, "
+                f"pool of {w.pool_pages} shuffled pages")
+    if w.name == "ragged":
+        return (f"ragged fragmented pool: {w.B} requests, lognormal(ln 512, 1) lengths, H={w.H}, "
+                f"d_h={w.D}, {st}, {w.pool_pages}-page pool after {w.churn_cycles} lease/release cycles")
+    return w.name
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes one step must move: retained history K and V rows, the new rows read
+    and written, q and out, page-table entries and lengths."""
+    lens = w.seq_lens.astype(np.int64)
+    es = w.elem_bytes
+    hist = int((lens - 1).sum()) * w.H * w.D * 2 * es
+    new_rows = w.B * w.H * w.D * es * 2 * 2
+    q_out = w.B * w.H * w.D * 4 * 2
+    tables = int(w.n_pages.sum()) * 4 + w.B * 4
+    return hist + new_rows + q_out + tables
+
+
+# ---------------------------------------------------------------- ranks --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """Largest value of x over all ranks (timing only; no data-path exchange)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+# --------------------------------------------------------------- clocks --
+
+CLOCK_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+                "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, kept by timestamp."""
+
+    def __init__(self, device_index: int = 0):
+        self.proc = None
+        try:
+            import torch
+            ident = ["-i", "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)]
+        except Exception:
+            ident = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(CLOCK_FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "20", *ident], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        self.samples = []
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != len(CLOCK_FIELDS):
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                self.samples.append(dict(t=ts, sm=float(f[1]), sm_max=float(f[2]), fields=f))
+            except ValueError:
+                continue
+
+    def summary(self, t0: float, t1: float) -> dict:
+        win = [s for s in self.samples if t0 <= s["t"] <= t1]
+        note = "samples inside the timed region"
+        if not win:
+            win = self.samples
+            note = "no sample fell inside the timed region; all samples of the run"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in win for n, v in zip(names, s["fields"][5:9]) if v == "Active"})
+        return {"sm_mhz": float(np.median([s["sm"] for s in win])),
+                "sm_max_mhz": max(s["sm_max"] for s in win), "reasons": reasons,
+                "samples": len(win), "note": note}
+
+
+# -------------------------------------------------------------- roofline --
+
+def measured_peak_hbm():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    with open(DECODE_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the split kernel from a committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha256") != decode_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ the GPU arm --
+
+def setup_device(w, torch):
+    """Pool, tables from the library's allocator, history in HBM, step inputs on device."""
+    import paged_kv_cache_decode_gb300 as pkv
+    from synth.device import fill_history, step_inputs, to_device
+    from synth.workloads import churn_ops, LEASE
+
+    pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "f32" if w.elem_bytes == 4 else "bf16",
+                    w.max_context, w.seed)
+    reqs = [pool.request() for _ in range(w.B)]
+    for r_i, kind, cnt in (churn_ops(w) if w.churn_cycles else []):
+        try:
+            reqs[r_i].lease_pages(cnt) if kind == LEASE else reqs[r_i].release_pages()
+        except pkv.PkvError:
+            pass
+    for b, r in enumerate(reqs):
+        r.release_pages()
+        r.lease_pages(int(w.n_pages[b]))
+    max_pages = int(w.n_pages.max())
+    tables = np.full((w.B, max_pages), -1, dtype=np.int32)
+    for b, r in enumerate(reqs):
+        t = r.page_table()
+        tables[b, :len(t)] = t
+    k_pages, v_pages = pool.kv_pages(0)
+    fill_history(k_pages, v_pages, w, tables, 0)
+    q, k_new, v_new = step_inputs(w, 0)
+    host = dict(q=q, k=k_new, v=v_new, tables=tables, lens=w.seq_lens.astype(np.int32))
+    dev = dict(q=to_device(q), k=to_device(k_new), v=to_device(v_new),
+               tables=torch.from_numpy(tables).cuda(), lens=torch.from_numpy(host["lens"]).cuda())
+    max_seq_len = int(w.seq_lens.max())
+    ws = pool.workspace(w.B, max_seq_len)
+    out = torch.empty((w.B, w.H, w.D), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    return pool, reqs, host, dev, ws, out, max_seq_len
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    rank, world = dist_init("nccl")
+    w = make_workload(args.workload, rank)
+    pool, reqs, host, dev, ws, out, max_seq_len = setup_device(w, torch)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pool.paged_decode_attention(0, dev["q"], dev["k"], dev["v"], dev["tables"], dev["lens"],
+                                    max_seq_len, out=out, workspace=ws)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pool.check_device_status() == 0
+
+    K = args.steps
+    evb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    eva = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        pool.set_timing_events(evb[i], eva[i])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    pool.set_timing_events(None, None)
+    step_ms = start.elapsed_time(end) / K
+    kernel_ms = float(np.mean([b.elapsed_time(a) for b, a in zip(evb, eva)]))
+    step_ms_max = max_over_ranks(step_ms, "cuda")
+
+    # end to end: host buffers in pinned memory, copies inside the timed region
+    hp = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()
+          if k in ("q", "tables", "lens")}
+    for k in ("k", "v"):
+        t = torch.from_numpy(host[k])
+        hp[k] = (t.view(torch.int16) if host[k].dtype == np.uint16 else t).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    dk = dev["k"].view(torch.int16) if dev["k"].dtype == torch.bfloat16 else dev["k"]
+    dv = dev["v"].view(torch.int16) if dev["v"].dtype == torch.bfloat16 else dev["v"]
+    h2d = sum(x.numel() * x.element_size() for x in hp.values())
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        dev["q"].copy_(hp["q"], non_blocking=True)
+        dk.copy_(hp["k"], non_blocking=True)
+        dv.copy_(hp["v"], non_blocking=True)
+        dev["tables"].copy_(hp["tables"], non_blocking=True)
+        dev["lens"].copy_(hp["lens"], non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, "cuda")
+    assert pool.check_device_status() == 0
+    if sampler:
+        sampler.stop()
+
+    alg = algorithmic_bytes(w)
+    line = None
+    if rank == 0:
+        peak, peak_kind = measured_peak_hbm()
+        achieved = alg / (kernel_ms * 1e-3) / 1e9
+        value = world * alg / (step_ms_max * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.elem_bytes == 2 else "f32", "data": "synthetic",
+            "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
+                       "head_dim": w.D, "page_size": w.P, "pool_pages": w.pool_pages,
+                       "seq_len_max": int(w.seq_lens.max()), "tokens_retained": int(w.seq_lens.sum()),
+                       "storage": "bf16" if w.elem_bytes == 2 else "fp32", "accumulate": "fp32",
+                       "alg_bytes_per_step": alg,
+                       "l2": f"inputs larger than L2 ({alg / 1e9:.2f} GB per step, no flush)"
+                             if alg > 129e6 else "inputs smaller than L2 (cache-warm)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "tokens_per_s": round(world * w.B / (step_ms_max * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": measured_traffic(w.name),
+                         "kernel": f"split_decode_kernel<{'bf16' if w.elem_bytes == 2 else 'f32'},{w.D}>",
+                         "kernel_ms": round(kernel_ms, 5), "peak_kind": peak_kind + " (hbm_gbs copy)"},
+            "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": K * 3,
+            "clocks": sampler.summary(t0, t1) if sampler else None,
+        }
+    pool.close()
+    return line, w
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample(w, requests, threads=0):
+    """Host pool holding the given requests' pages (compact ids), the step's inputs
+    for them, and a callable that runs the oracle once."""
+    import oracle
+    import synth
+    from synth import KHIST, VHIST, F32
+    from synth.device import step_inputs
+    q, k_new, v_new = step_inputs(w, 0)
+    npg = [int(w.n_pages[b]) for b in requests]
+    total = sum(npg)
+    sd = np.float32 if w.elem_bytes == 4 else np.uint16
+    kp = np.empty((total, w.H, w.P, w.D), dtype=sd)
+    vp = np.empty_like(kp)
+    tab = np.full((len(requests), max(npg)), -1, dtype=np.int32)
+    off = 0
+    for i, (b, n) in enumerate(zip(requests, npg)):
+        t = int(w.seq_lens[b])
+        tab[i, :n] = np.arange(off, off + n, dtype=np.int32)
+        synth.history_pages(w.seed, KHIST, 0, b, n, w.H, w.P, w.D, t - 1, w.dtype, kp[off:off + n])
+        synth.history_pages(w.seed, VHIST, 0, b, n, w.H, w.P, w.D, t - 1, w.dtype, vp[off:off + n])
+        off += n
+    lens = w.seq_lens[requests].astype(np.int32)
+    dt = F32 if w.elem_bytes == 4 else 1
+
+    def run():
+        return oracle.paged_decode_attention(kp, vp, q[requests], k_new[requests], v_new[requests],
+                                             tab, lens, dt, threads=threads)
+    sample_bytes = int((lens.astype(np.int64) - 1).sum()) * w.H * w.D * 2 * w.elem_bytes
+    return run, sample_bytes, lens
+
+
+def sample_requests(w, target_tokens: int):
+    """Requests 0, 1, ... until their retained tokens reach target_tokens."""
+    out, tok = [], 0
+    for b in range(w.B):
+        out.append(b)
+        tok += int(w.seq_lens[b])
+        if tok >= target_tokens:
+            break
+    return out
+
+
+def cpu_baseline(w, target_tokens=4 * 131072):
+    import oracle
+    reqs = sample_requests(w, target_tokens)
+    run, sbytes, lens = oracle_sample(w, reqs)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": round(sbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{len(reqs)} of {w.B} requests ({len(reqs) * w.H} lanes, "
+                      f"{int(lens.sum())} tokens), fp64 C oracle, one pass, {dt:.2f} s",
+            "tokens_per_s": round(len(reqs) / dt, 3)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None, None
+    import oracle
+    w = make_workload(args.workload, 0)
+    reqs = sample_requests(w, 1)                       # one request per step
+    run, sbytes, lens = oracle_sample(w, reqs)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = round(sbytes / dt / 1e9, 4)
+    sample = (f"each step: request 0 of {w.B} ({w.H} lanes x {int(lens[0])} tokens), "
+              f"fp64 C oracle on the host cores")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
+                   "head_dim": w.D, "page_size": w.P},
+        "tokens_per_s": round(len(reqs) / dt, 3),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line, w
+
+
+# ------------------------------------------------------------------ main --
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="long")
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    import __graft_entry__
+    __graft_entry__.build()
+    if args.impl == "reference":
+        line, _ = run_reference(args)
+    else:
+        line, w = run_gpu(args)
+        rank, world, _ = dist_env()
+        if line is not None and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

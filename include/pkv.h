@@ -1,0 +1,280 @@
+/*
+ * pkv — paged KV-cache decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libpkv.so.  Plain pointers and sizes only.
+ *
+ * Sources the operations follow (page title, section):
+ *   [SERVE-FLOW]   "Incremental Serving", section "Request flow".
+ *   [SERVE-PAGED]  "Incremental Serving", section "Paged KV-cache layout".
+ *   [SERVE-CABI]   "Incremental Serving", section "Stable C and Python sessions".
+ *   [CACHED-MIX]   "38 · Cached generation", section "Prepare every block, then
+ *                  commit every cache together" (function incremental_mixture,
+ *                  and the prepared-ticket commit).
+ *   [CACHED-BIND]  "38 · Cached generation", section "Bind one decoder to its
+ *                  model-wide cache, then advance every block coherently".
+ *   [CACHED-CELLS] "38 · Cached generation", section "Count attention-score
+ *                  cells, not total runtime".
+ *   [ROLLOUT-KV]   "Rollout Serving, Caching, and Batching", KV-cache memory formula.
+ *
+ * Conventions (all entry points):
+ *   - Every call returns a pkv_status.  PKV_OK is 0.  A call that returns an
+ *     error has changed no state ([CACHED-BIND]: rejected operations leave the
+ *     committed state unchanged).  pkv_last_error() then describes the failure
+ *     (thread-local, valid until the next call on the same thread).
+ *   - Handles are opaque.  A pool owns its device K/V storage; requests point at
+ *     their pool, and a pool cannot be destroyed while requests are alive.
+ *   - Not thread-safe: calls that touch the same pool must be serialised by the
+ *     caller ([SERVE-CABI]: the raw C ABI requires external synchronisation).
+ *   - Device work is asynchronous on the caller's stream (a cudaStream_t passed
+ *     as void*; NULL is the legacy default stream).  No entry point
+ *     synchronises except pkv_check_device_status.  The caller's current CUDA
+ *     device must be the device the pool was created on.
+ *   - Device-side faults are never raised by trapping: a kernel that meets an
+ *     out-of-range length or page id, or a wait that runs out, sets a bit in the
+ *     pool's device error word, skips the bad access and returns;
+ *     pkv_check_device_status reports it.
+ *
+ * Layout ([SERVE-PAGED]): per layer, key pages and value pages are each
+ *   [physical_page][head][page_offset][head_width]  (row-major, storage dtype)
+ * and one physical page id addresses the matching K and V page in every layer.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkv_pool pkv_pool;
+typedef struct pkv_request pkv_request;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARGUMENT = 1,   /* bad pointer, size, layer, shape */
+    PKV_ERR_OUT_OF_PAGES = 2,       /* the pool has no free page left */
+    PKV_ERR_CAPACITY_EXCEEDED = 3,  /* request at its maximum context ([SERVE-CABI]) */
+    PKV_ERR_BAD_STATE = 4,          /* call out of order (token pending / not pending, ...) */
+    PKV_ERR_OUT_OF_MEMORY = 5,      /* host or device allocation failed */
+    PKV_ERR_CUDA = 6,               /* a CUDA runtime call failed */
+    PKV_ERR_DEVICE_CHECK = 7,       /* a kernel flagged bad input (see pkv_check_device_status) */
+    PKV_ERR_NO_STORAGE = 8,         /* bookkeeping-only pool has no device storage */
+    PKV_ERR_UNSUPPORTED = 9         /* geometry the kernels do not implement */
+} pkv_status;
+
+typedef enum pkv_dtype {
+    PKV_F32 = 0,    /* 4-byte IEEE float */
+    PKV_BF16 = 1    /* 2-byte bfloat16 (upper half of an IEEE float) */
+} pkv_dtype;
+
+/* pkv_pool_create flags */
+#define PKV_POOL_HOST_ONLY 1u   /* bookkeeping only: free list, tables, transactions; no device
+                                   storage, so append/attend entry points return PKV_ERR_NO_STORAGE */
+
+/* bits of the device error word */
+#define PKV_DEVERR_SEQ_LEN 1u   /* a seq_len < 1, > max_seq_len, or needing > max_pages pages */
+#define PKV_DEVERR_PAGE_ID 2u   /* a page-table entry outside [0, pages) */
+#define PKV_DEVERR_TIMEOUT 4u   /* a bounded wait for an async copy ran out */
+
+/* Work counters of one request ([CACHED-BIND] work counters; [CACHED-CELLS]).
+ * They advance only when a token commits; reset (release) zeroes them. */
+typedef struct pkv_counters {
+    int64_t committed_tokens;   /* tokens made visible by pkv_commit_token */
+    int64_t cache_appends;      /* layers x committed tokens */
+    int64_t score_cells;        /* sum over committed tokens of layers x heads x t */
+} pkv_counters;
+
+/* ---------------------------------------------------------------- pool -- */
+
+/*
+ * Create a paged pool ([SERVE-PAGED]).
+ *   layers, heads, head_dim: geometry of every request served from the pool.
+ *   pages:       physical pages per layer; 0 = enough pages for one
+ *                maximum-length context, ceil(max_context / page_size)
+ *                ([SERVE-PAGED]: a block count of 0 sizes one full context).
+ *   page_size:   tokens per page; the sources' default is 16.  Kernels require a
+ *                multiple of 16 (a contiguous one-page-per-request layout uses
+ *                page_size = max_context rounded up to 16).
+ *   dtype:       storage dtype of K and V (PKV_F32 or PKV_BF16).
+ *   max_context: largest retained length of one request (>= 1).
+ *   seed:        free-list order: a FIFO queue initialised to a Fisher-Yates
+ *                shuffle of 0..pages-1 driven by SplitMix64(seed), swap index
+ *                next() mod (i + 1) for i = pages-1 down to 1.
+ *   flags:       0, or PKV_POOL_HOST_ONLY.
+ * Supported by the kernels: head_dim a power of two, 2 <= head_dim <= 128 for
+ * PKV_F32 and <= 256 for PKV_BF16 (else PKV_ERR_UNSUPPORTED, unless HOST_ONLY).
+ * Device storage is 2 * layers * pages * page_size * heads * head_dim * element
+ * size bytes ([ROLLOUT-KV]), zero-filled; the pool also allocates a 4-byte
+ * device error word.  On success *out receives the handle.
+ */
+int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page_size, int dtype,
+                    int64_t max_context, uint64_t seed, unsigned flags, pkv_pool** out);
+
+/* Free the pool and its device storage.  PKV_ERR_BAD_STATE while any request
+ * created from it is alive.  NULL is accepted. */
+int pkv_pool_destroy(pkv_pool* pool);
+
+/* Device base addresses of one layer's key and value pages (layout above).
+ * Owned by the pool; valid until pkv_pool_destroy.  NO_STORAGE for host-only pools. */
+int pkv_pool_kv_ptr(const pkv_pool* pool, int layer, void** k_pages, void** v_pages);
+
+/* Bytes of device K/V storage (2 * layers * pages * page_size * heads * head_dim * es). */
+int pkv_pool_bytes(const pkv_pool* pool, uint64_t* bytes);
+
+/* Physical pages per layer, and how many are currently free. */
+int pkv_pool_pages(const pkv_pool* pool, int64_t* pages, int64_t* free_pages);
+
+/* Copy the free list, front first, into host_out[0 .. cap); *n receives its
+ * length (the copy is truncated to cap). */
+int pkv_pool_free_list(const pkv_pool* pool, int32_t* host_out, int64_t cap, int64_t* n);
+
+/* ------------------------------------------------------------- requests -- */
+
+/* New empty request (length 0, no pages) drawing pages from `pool`. */
+int pkv_request_create(pkv_pool* pool, pkv_request** out);
+
+/* Abort a pending token if any, return every page to the pool, free the
+ * request ([SERVE-PAGED]: pages go back when a request is destroyed).  NULL ok. */
+int pkv_request_destroy(pkv_request* req);
+
+/*
+ * Lease n more pages now, appended to the request's logical page table in the
+ * order they leave the free list's front.  Pages are otherwise leased lazily
+ * by pkv_begin_token ([SERVE-PAGED]).  All or nothing: OUT_OF_PAGES if fewer
+ * than n are free, CAPACITY_EXCEEDED if the table would pass
+ * ceil(max_context / page_size), BAD_STATE while a token is pending.
+ */
+int pkv_lease_pages(pkv_request* req, int64_t n);
+
+/* Reset: push every page to the back of the free list in logical order, set
+ * the visible length to 0 and zero the counters ([SERVE-PAGED]; [CACHED-BIND]
+ * reset).  BAD_STATE while a token is pending. */
+int pkv_release_pages(pkv_request* req);
+
+/* Visible (committed) length. */
+int pkv_request_length(const pkv_request* req, int64_t* visible_len);
+
+/* Copy the logical page table (physical ids) into host_out[0 .. cap); *n_pages
+ * receives its length. */
+int pkv_request_page_table(const pkv_request* req, int32_t* host_out, int64_t cap,
+                           int64_t* n_pages);
+
+/* Counters of the request. */
+int pkv_request_counters(const pkv_request* req, pkv_counters* out);
+
+/* ---------------------------------------------------------- transaction -- */
+
+/*
+ * Reserve the next logical position ([SERVE-FLOW] step 1).  *position receives
+ * it (= the visible length).  If that position starts a page the request does
+ * not hold yet, one page is leased from the free list's front.
+ * BAD_STATE if a token is already pending; CAPACITY_EXCEEDED at max_context;
+ * OUT_OF_PAGES if a page is needed and none is free.
+ */
+int pkv_begin_token(pkv_request* req, int64_t* position);
+
+/*
+ * One layer's step for the pending token ([SERVE-FLOW] step 2): store the
+ * new key and value rows at the pending position of `layer`'s pools, then
+ * attend the newest query over all t = position + 1 retained keys of that
+ * layer, the new one included ([CACHED-MIX]: scores q.k / sqrt(head_dim),
+ * stable softmax, weighted sum of values).
+ *   q   [heads][head_dim] fp32, device
+ *   k,v [heads][head_dim] storage dtype, device
+ *   out [heads][head_dim] fp32, device (the [1,H,1,d_h] attention context)
+ *   stream: cudaStream_t
+ * Call once per layer per pending token; BAD_STATE if none is pending or the
+ * layer already ran for it.  The new row is written into the page at once but
+ * is visible to later tokens only after pkv_commit_token.
+ * Enqueues at most one 4-byte host-to-device copy of a newly leased page-table
+ * entry and two kernels on `stream`; returns without waiting.
+ */
+int pkv_append_and_attend(pkv_request* req, int layer, const float* q, const void* k,
+                          const void* v, float* out, void* stream);
+
+/* Make the pending position visible ([SERVE-FLOW] step 3).  BAD_STATE unless a
+ * token is pending and every layer ran pkv_append_and_attend for it exactly
+ * once ([CACHED-BIND]: all layers advance together).  Counters advance by
+ * layers (appends) and layers x heads x t (score cells). */
+int pkv_commit_token(pkv_request* req);
+
+/* Drop the pending token ([SERVE-FLOW] step 4): the visible length stays, and a
+ * page leased by its pkv_begin_token goes back to the front of the free list,
+ * so table and free list are exactly as before pkv_begin_token.  Rows already
+ * written for it stay in the page, unreachable, and are overwritten by the
+ * retry.  BAD_STATE if no token is pending. */
+int pkv_abort_token(pkv_request* req);
+
+/* -------------------------------------------------------------- batched -- */
+
+/*
+ * Device scratch bytes that pkv_paged_decode_attention needs for `batch`
+ * requests of at most max_seq_len tokens (split partial results and the
+ * per-request tile prefix).  Depends on the pool's geometry and device.
+ */
+int pkv_workspace_size(const pkv_pool* pool, int batch, int64_t max_seq_len, size_t* bytes);
+
+/*
+ * Batched paged decode attention for one layer ([SERVE-PAGED] layout and
+ * page table; [CACHED-MIX] arithmetic).  For every request b with retained
+ * length t_b = seq_lens[b] (new token included, >= 1):
+ *   1. store k_new[b], v_new[b] at logical position t_b - 1, i.e. physical page
+ *      page_tables[b][(t_b - 1) / page_size], slot (t_b - 1) % page_size;
+ *   2. for each head h:
+ *      out[b][h] = sum_j softmax_j(q[b][h] . K_j / sqrt(head_dim)) V_j, over the
+ *      t_b keys K_j = K[page_tables[b][j / page_size]][h][j % page_size].
+ *   q            [batch][heads][head_dim] fp32, device
+ *   k_new, v_new [batch][heads][head_dim] storage dtype, device
+ *   page_tables  [batch][max_pages] int32, device (entries past ceil(t_b/page_size) unread)
+ *   seq_lens     [batch] int32, device
+ *   max_seq_len  host bound on every seq_lens entry (sizes the launch)
+ *   out          [batch][heads][head_dim] fp32, device
+ *   workspace    device scratch of >= pkv_workspace_size bytes (caller owned,
+ *                16-byte aligned, contents need no initialisation)
+ * Stateless over bookkeeping: the caller owns lengths and tables.  Bad
+ * lengths or page ids found on the device set the pool's error word; the
+ * affected request's rows of `out` are then unspecified.  Enqueues three kernels
+ * on `stream` and returns without waiting.  Calls whose device work can overlap
+ * must use different workspaces.
+ */
+int pkv_paged_decode_attention(pkv_pool* pool, int layer, int batch, const float* q,
+                               const void* k_new, const void* v_new, const int32_t* page_tables,
+                               int max_pages, const int32_t* seq_lens, int64_t max_seq_len,
+                               float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------- tracing -- */
+
+/*
+ * Kernel timing hook.  When `before` and `after` are non-NULL cudaEvent_t
+ * handles, every later pkv_append_and_attend / pkv_paged_decode_attention on
+ * this pool records `before` on its stream immediately before the split
+ * (attention) kernel and `after` immediately after it, so
+ * cudaEventElapsedTime(before, after) is that kernel's device time.  NULL,
+ * NULL turns the hook off.  The events stay owned by the caller.
+ */
+int pkv_pool_set_timing_events(pkv_pool* pool, void* before, void* after);
+
+/* -------------------------------------------------------------- status -- */
+
+/* Synchronise the device, then read and clear the pool's device error word.
+ * *bits (may be NULL) receives the PKV_DEVERR_* bits.  Returns
+ * PKV_ERR_DEVICE_CHECK if any bit was set, PKV_ERR_CUDA if the device reports a
+ * CUDA error. */
+int pkv_check_device_status(pkv_pool* pool, uint32_t* bits);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* Name of a status code. */
+const char* pkv_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

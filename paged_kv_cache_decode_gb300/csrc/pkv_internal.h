@@ -1,0 +1,64 @@
+// Internal interface between the host library (pool.cpp) and the kernels
+// (decode.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+constexpr int kTile = 16;          // key rows staged and processed as one unit
+constexpr int kSplitWarps = 4;     // warps per CTA of the split kernel; each warp is one worker
+
+// One launch of the decode path for one layer.
+struct DecodeArgs {
+    int dtype;               // PKV_F32 / PKV_BF16
+    int B, H, D, P;          // requests, heads, head width, page size (multiple of kTile)
+    const float* q;          // [B][H][D]
+    const void* k_new;       // [B][H][D] storage dtype
+    const void* v_new;
+    void* k_pages;           // this layer's pools, [pages][H][P][D]
+    void* v_pages;
+    int64_t n_pages;
+    const int32_t* tables;   // [B][max_pages]
+    int max_pages;
+    const int32_t* seq_lens; // [B] device; nullptr => single request of length single_t
+    int64_t single_t;
+    int64_t max_seq_len;
+    float* out;              // [B][H][D]
+    void* workspace;
+    size_t workspace_bytes;
+    int workers;             // workers of this launch (split-kernel warps)
+    unsigned* dev_error;
+    cudaEvent_t ev_before;   // optional: recorded around the split kernel
+    cudaEvent_t ev_after;
+};
+
+// Byte offsets of the scratch areas inside a workspace.
+struct WorkspaceLayout {
+    size_t req_prefix;   // int64 [B + 1]: tiles-per-lane prefix over requests
+    size_t worker_req;   // int32 [workers]: request holding each worker's first tile
+    size_t part_ml;      // float2 [B*H + workers]: (running max in log2 units, sum)
+    size_t part_o;       // float [B*H + workers][D]: unnormalised partial outputs
+    size_t total;
+};
+
+WorkspaceLayout workspace_layout(int B, int H, int D, int workers);
+
+// Workers one launch uses: the pool's resident worker count, capped by the
+// number of tiles the launch can hold (B * H * ceil(max_seq_len / kTile)).
+int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len);
+
+// Resident split-kernel warps per SM x SMs for this geometry on the current
+// device; 0 if the geometry is not implemented.
+int resident_workers(int dtype, int D, int num_sms);
+
+// True if the kernels implement (dtype, D).
+bool decode_supported(int dtype, int D);
+
+// Enqueue plan (batched only), split and merge kernels on `stream`.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

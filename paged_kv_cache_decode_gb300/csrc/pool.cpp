@@ -1,0 +1,570 @@
+// Host side of libpkv: the paged pool, its free list, per-request page tables,
+// the begin / append / commit / abort transaction and the C ABI.
+//
+// Sources: "Incremental Serving", sections "Request flow" (the per-token
+// transaction), "Paged KV-cache layout" (pools, page table, lazy leasing,
+// default page size 16, block count 0 = one full context) and "Stable C and
+// Python sessions" (opaque handles, capacity exhaustion reported, external
+// synchronisation); "38 · Cached generation", sections "Bind one decoder to its
+// model-wide cache" and "Assemble model-wide ... evidence" (all layers advance
+// together, counters advance on commit, reset zeroes them, rejected operations
+// change nothing).
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+int ok() {
+    g_last_error.clear();
+    return PKV_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// SplitMix64 (Steele, Lea & Flood 2014).
+struct SplitMix64 {
+    uint64_t state;
+    uint64_t next() {
+        uint64_t z = (state += 0x9e3779b97f4a7c15ull);
+        z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+        z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+        return z ^ (z >> 31);
+    }
+};
+
+}  // namespace
+
+struct pkv_pool {
+    int layers = 0, heads = 0, head_dim = 0, page_size = 0, dtype = 0;
+    int64_t pages = 0, max_context = 0, max_pages_per_request = 0;
+    bool host_only = false;
+    std::deque<int32_t> free_list;     // front = next page to lease
+    void* k_base = nullptr;            // [layers][pages][H][P][D]
+    void* v_base = nullptr;
+    size_t layer_bytes = 0;
+    unsigned* dev_error = nullptr;
+    int device = -1;
+    int workers = 0;                   // resident split-kernel warps on the device
+    int64_t live_requests = 0;
+    cudaEvent_t ev_before = nullptr;   // optional split-kernel timing events
+    cudaEvent_t ev_after = nullptr;
+};
+
+struct pkv_request {
+    pkv_pool* pool = nullptr;
+    std::vector<int32_t> table;        // logical page -> physical page
+    int64_t length = 0;                // visible (committed) length
+    bool pending = false;
+    int64_t position = 0;              // pending position
+    bool leased_by_begin = false;
+    std::vector<uint8_t> appended;     // per layer, for the pending token
+    int appended_count = 0;
+    pkv_counters counters{};
+    int32_t* dev_table = nullptr;      // device copy, max_pages_per_request entries
+    int64_t dev_dirty_from = 0;        // entries [dev_dirty_from, table.size()) not on the device
+    void* dev_workspace = nullptr;
+    size_t workspace_bytes = 0;
+    int workspace_workers = 0;
+};
+
+namespace {
+
+int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+void mark_dirty(pkv_request* r, int64_t from) {
+    if (from < r->dev_dirty_from) r->dev_dirty_from = from;
+}
+
+int check_device(const pkv_pool* p) {
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (cur != p->device)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "current device %d is not the pool's device %d", cur,
+                    p->device);
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_version(void) { return 10000; }
+
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARGUMENT: return "PKV_ERR_INVALID_ARGUMENT";
+        case PKV_ERR_OUT_OF_PAGES: return "PKV_ERR_OUT_OF_PAGES";
+        case PKV_ERR_CAPACITY_EXCEEDED: return "PKV_ERR_CAPACITY_EXCEEDED";
+        case PKV_ERR_BAD_STATE: return "PKV_ERR_BAD_STATE";
+        case PKV_ERR_OUT_OF_MEMORY: return "PKV_ERR_OUT_OF_MEMORY";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK";
+        case PKV_ERR_NO_STORAGE: return "PKV_ERR_NO_STORAGE";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        default: return "PKV_ERR_UNKNOWN";
+    }
+}
+
+int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page_size, int dtype,
+                    int64_t max_context, uint64_t seed, unsigned flags, pkv_pool** out) {
+    if (!out) return fail(PKV_ERR_INVALID_ARGUMENT, "out is NULL");
+    *out = nullptr;
+    if (layers < 1 || heads < 1 || head_dim < 1 || page_size < 1 || max_context < 1 || pages < 0)
+        return fail(PKV_ERR_INVALID_ARGUMENT,
+                    "bad geometry: layers=%d heads=%d head_dim=%d page_size=%d max_context=%lld "
+                    "pages=%lld",
+                    layers, heads, head_dim, page_size, (long long)max_context, (long long)pages);
+    if (dtype != PKV_F32 && dtype != PKV_BF16)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "dtype %d is neither PKV_F32 nor PKV_BF16", dtype);
+    if (flags & ~PKV_POOL_HOST_ONLY) return fail(PKV_ERR_INVALID_ARGUMENT, "unknown flags");
+    const bool host_only = (flags & PKV_POOL_HOST_ONLY) != 0;
+    const int64_t per_request = (max_context + page_size - 1) / page_size;
+    if (pages == 0) pages = per_request;
+    if (pages > INT32_MAX || per_request > INT32_MAX)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "page ids must fit in int32");
+    if (!host_only) {
+        if (page_size % pkv::kTile != 0)
+            return fail(PKV_ERR_UNSUPPORTED, "page_size %d is not a multiple of %d", page_size,
+                        pkv::kTile);
+        if (!pkv::decode_supported(dtype, head_dim))
+            return fail(PKV_ERR_UNSUPPORTED,
+                        "head_dim %d not implemented (powers of two, 2..128 fp32, 2..256 bf16)",
+                        head_dim);
+    }
+
+    pkv_pool* p = new (std::nothrow) pkv_pool;
+    if (!p) return fail(PKV_ERR_OUT_OF_MEMORY, "host allocation failed");
+    p->layers = layers;
+    p->heads = heads;
+    p->head_dim = head_dim;
+    p->page_size = page_size;
+    p->dtype = dtype;
+    p->pages = pages;
+    p->max_context = max_context;
+    p->max_pages_per_request = per_request;
+    p->host_only = host_only;
+
+    // free list: Fisher-Yates shuffle of 0..pages-1 with SplitMix64(seed)
+    std::vector<int32_t> order((size_t)pages);
+    for (int64_t i = 0; i < pages; ++i) order[(size_t)i] = (int32_t)i;
+    SplitMix64 rng{seed};
+    for (int64_t i = pages - 1; i > 0; --i) {
+        const int64_t j = (int64_t)(rng.next() % (uint64_t)(i + 1));
+        std::swap(order[(size_t)i], order[(size_t)j]);
+    }
+    p->free_list.assign(order.begin(), order.end());
+
+    if (!host_only) {
+        cudaError_t e = cudaGetDevice(&p->device);
+        int sms = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+        if (e != cudaSuccess) {
+            delete p;
+            return cuda_fail(e, "device query");
+        }
+        p->workers = pkv::resident_workers(dtype, head_dim, sms);
+        if (p->workers <= 0) {
+            delete p;
+            return fail(PKV_ERR_CUDA, "split kernel cannot be resident on this device");
+        }
+        p->layer_bytes = (size_t)pages * page_size * heads * head_dim * elem_bytes(dtype);
+        const size_t total = p->layer_bytes * (size_t)layers;
+        if ((e = cudaMalloc(&p->k_base, total)) != cudaSuccess ||
+            (e = cudaMalloc(&p->v_base, total)) != cudaSuccess ||
+            (e = cudaMalloc(&p->dev_error, sizeof(unsigned))) != cudaSuccess) {
+            cudaFree(p->k_base);
+            cudaFree(p->v_base);
+            cudaFree(p->dev_error);
+            delete p;
+            cudaGetLastError();
+            return fail(PKV_ERR_OUT_OF_MEMORY, "cudaMalloc of 2 x %zu bytes: %s", total,
+                        cudaGetErrorString(e));
+        }
+        if ((e = cudaMemset(p->k_base, 0, total)) != cudaSuccess ||
+            (e = cudaMemset(p->v_base, 0, total)) != cudaSuccess ||
+            (e = cudaMemset(p->dev_error, 0, sizeof(unsigned))) != cudaSuccess ||
+            (e = cudaDeviceSynchronize()) != cudaSuccess) {
+            cudaFree(p->k_base);
+            cudaFree(p->v_base);
+            cudaFree(p->dev_error);
+            delete p;
+            return cuda_fail(e, "zero-fill pool");
+        }
+    }
+    *out = p;
+    return ok();
+}
+
+int pkv_pool_destroy(pkv_pool* p) {
+    if (!p) return ok();
+    if (p->live_requests != 0)
+        return fail(PKV_ERR_BAD_STATE, "%lld requests still use the pool",
+                    (long long)p->live_requests);
+    if (!p->host_only) {
+        cudaFree(p->k_base);
+        cudaFree(p->v_base);
+        cudaFree(p->dev_error);
+    }
+    delete p;
+    return ok();
+}
+
+int pkv_pool_kv_ptr(const pkv_pool* p, int layer, void** k_pages, void** v_pages) {
+    if (!p || !k_pages || !v_pages) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    if (layer < 0 || layer >= p->layers)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    *k_pages = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)layer;
+    *v_pages = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)layer;
+    return ok();
+}
+
+int pkv_pool_bytes(const pkv_pool* p, uint64_t* bytes) {
+    if (!p || !bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    *bytes = 2ull * (uint64_t)p->layers * (uint64_t)p->pages * (uint64_t)p->page_size *
+             (uint64_t)p->heads * (uint64_t)p->head_dim * (uint64_t)elem_bytes(p->dtype);
+    return ok();
+}
+
+int pkv_pool_pages(const pkv_pool* p, int64_t* pages, int64_t* free_pages) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if (pages) *pages = p->pages;
+    if (free_pages) *free_pages = (int64_t)p->free_list.size();
+    return ok();
+}
+
+int pkv_pool_free_list(const pkv_pool* p, int32_t* host_out, int64_t cap, int64_t* n) {
+    if (!p || !n || cap < 0 || (cap > 0 && !host_out))
+        return fail(PKV_ERR_INVALID_ARGUMENT, "bad argument");
+    *n = (int64_t)p->free_list.size();
+    int64_t i = 0;
+    for (auto it = p->free_list.begin(); it != p->free_list.end() && i < cap; ++it) host_out[i++] = *it;
+    return ok();
+}
+
+int pkv_request_create(pkv_pool* p, pkv_request** out) {
+    if (!p || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    *out = nullptr;
+    pkv_request* r = new (std::nothrow) pkv_request;
+    if (!r) return fail(PKV_ERR_OUT_OF_MEMORY, "host allocation failed");
+    r->pool = p;
+    r->appended.assign((size_t)p->layers, 0);
+    r->table.reserve((size_t)p->max_pages_per_request);
+    if (!p->host_only) {
+        int rc = check_device(p);
+        if (rc != PKV_OK) {
+            delete r;
+            return rc;
+        }
+        r->workspace_workers =
+            pkv::launch_workers(p->workers, 1, p->heads, p->max_context);
+        r->workspace_bytes =
+            pkv::workspace_layout(1, p->heads, p->head_dim, r->workspace_workers).total;
+        cudaError_t e = cudaMalloc(&r->dev_table, sizeof(int32_t) * (size_t)p->max_pages_per_request);
+        if (e == cudaSuccess) e = cudaMalloc(&r->dev_workspace, r->workspace_bytes);
+        if (e != cudaSuccess) {
+            cudaFree(r->dev_table);
+            cudaFree(r->dev_workspace);
+            delete r;
+            cudaGetLastError();
+            return fail(PKV_ERR_OUT_OF_MEMORY, "cudaMalloc for request: %s", cudaGetErrorString(e));
+        }
+    }
+    ++p->live_requests;
+    *out = r;
+    return ok();
+}
+
+int pkv_request_destroy(pkv_request* r) {
+    if (!r) return ok();
+    pkv_pool* p = r->pool;
+    if (r->pending) pkv_abort_token(r);
+    for (int32_t pg : r->table) p->free_list.push_back(pg);
+    if (!p->host_only) {
+        cudaFree(r->dev_table);
+        cudaFree(r->dev_workspace);
+    }
+    --p->live_requests;
+    delete r;
+    return ok();
+}
+
+int pkv_lease_pages(pkv_request* r, int64_t n) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    pkv_pool* p = r->pool;
+    if (r->pending) return fail(PKV_ERR_BAD_STATE, "a token is pending");
+    if (n < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "negative page count %lld", (long long)n);
+    if ((int64_t)r->table.size() + n > p->max_pages_per_request)
+        return fail(PKV_ERR_CAPACITY_EXCEEDED,
+                    "%lld + %lld pages exceed one maximum-length context (%lld pages)",
+                    (long long)r->table.size(), (long long)n, (long long)p->max_pages_per_request);
+    if (n > (int64_t)p->free_list.size())
+        return fail(PKV_ERR_OUT_OF_PAGES, "%lld pages requested, %lld free", (long long)n,
+                    (long long)p->free_list.size());
+    mark_dirty(r, (int64_t)r->table.size());
+    for (int64_t i = 0; i < n; ++i) {
+        r->table.push_back(p->free_list.front());
+        p->free_list.pop_front();
+    }
+    return ok();
+}
+
+int pkv_release_pages(pkv_request* r) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    if (r->pending) return fail(PKV_ERR_BAD_STATE, "a token is pending");
+    for (int32_t pg : r->table) r->pool->free_list.push_back(pg);
+    r->table.clear();
+    r->length = 0;
+    r->counters = pkv_counters{};
+    r->dev_dirty_from = 0;
+    return ok();
+}
+
+int pkv_request_length(const pkv_request* r, int64_t* visible_len) {
+    if (!r || !visible_len) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    *visible_len = r->length;
+    return ok();
+}
+
+int pkv_request_page_table(const pkv_request* r, int32_t* host_out, int64_t cap, int64_t* n_pages) {
+    if (!r || !n_pages || cap < 0 || (cap > 0 && !host_out))
+        return fail(PKV_ERR_INVALID_ARGUMENT, "bad argument");
+    *n_pages = (int64_t)r->table.size();
+    const int64_t n = *n_pages < cap ? *n_pages : cap;
+    if (n > 0) std::memcpy(host_out, r->table.data(), sizeof(int32_t) * (size_t)n);
+    return ok();
+}
+
+int pkv_request_counters(const pkv_request* r, pkv_counters* out) {
+    if (!r || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    *out = r->counters;
+    return ok();
+}
+
+int pkv_begin_token(pkv_request* r, int64_t* position) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    pkv_pool* p = r->pool;
+    if (r->pending) return fail(PKV_ERR_BAD_STATE, "a token is already pending");
+    if (r->length >= p->max_context)
+        return fail(PKV_ERR_CAPACITY_EXCEEDED, "request is at its maximum context %lld",
+                    (long long)p->max_context);
+    bool lease = r->length / p->page_size >= (int64_t)r->table.size();
+    if (lease && p->free_list.empty()) return fail(PKV_ERR_OUT_OF_PAGES, "no free page");
+    if (lease) {
+        mark_dirty(r, (int64_t)r->table.size());
+        r->table.push_back(p->free_list.front());
+        p->free_list.pop_front();
+    }
+    r->pending = true;
+    r->position = r->length;
+    r->leased_by_begin = lease;
+    std::fill(r->appended.begin(), r->appended.end(), 0);
+    r->appended_count = 0;
+    if (position) *position = r->position;
+    return ok();
+}
+
+int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void* k, const void* v,
+                          float* out, void* stream) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    pkv_pool* p = r->pool;
+    if (!q || !k || !v || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL tensor pointer");
+    if (layer < 0 || layer >= p->layers)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
+    if (r->appended[(size_t)layer]) return fail(PKV_ERR_BAD_STATE, "layer %d already ran", layer);
+    int rc = check_device(p);
+    if (rc != PKV_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t n = (int64_t)r->table.size();
+    if (r->dev_dirty_from < n) {
+        cudaError_t e = cudaMemcpyAsync(r->dev_table + r->dev_dirty_from,
+                                        r->table.data() + r->dev_dirty_from,
+                                        sizeof(int32_t) * (size_t)(n - r->dev_dirty_from),
+                                        cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "page-table upload");
+        r->dev_dirty_from = n;
+    }
+    pkv::DecodeArgs a{};
+    a.dtype = p->dtype;
+    a.B = 1;
+    a.H = p->heads;
+    a.D = p->head_dim;
+    a.P = p->page_size;
+    a.q = q;
+    a.k_new = k;
+    a.v_new = v;
+    void *kp, *vp;
+    pkv_pool_kv_ptr(p, layer, &kp, &vp);
+    a.k_pages = kp;
+    a.v_pages = vp;
+    a.n_pages = p->pages;
+    a.tables = r->dev_table;
+    a.max_pages = (int)p->max_pages_per_request;
+    a.seq_lens = nullptr;
+    a.single_t = r->position + 1;
+    a.max_seq_len = r->position + 1;
+    a.out = out;
+    a.workspace = r->dev_workspace;
+    a.workspace_bytes = r->workspace_bytes;
+    a.workers = pkv::launch_workers(r->workspace_workers, 1, p->heads, r->position + 1);
+    a.dev_error = p->dev_error;
+    a.ev_before = p->ev_before;
+    a.ev_after = p->ev_after;
+    cudaError_t e = pkv::launch_decode(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    r->appended[(size_t)layer] = 1;
+    ++r->appended_count;
+    return ok();
+}
+
+int pkv_commit_token(pkv_request* r) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    pkv_pool* p = r->pool;
+    if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
+    if (r->appended_count != p->layers)
+        return fail(PKV_ERR_BAD_STATE, "%d of %d layers appended", r->appended_count, p->layers);
+    const int64_t t = r->position + 1;
+    r->length = t;
+    r->counters.committed_tokens += 1;
+    r->counters.cache_appends += p->layers;
+    r->counters.score_cells += (int64_t)p->layers * p->heads * t;
+    r->pending = false;
+    r->leased_by_begin = false;
+    return ok();
+}
+
+int pkv_abort_token(pkv_request* r) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
+    if (r->leased_by_begin) {
+        r->pool->free_list.push_front(r->table.back());
+        r->table.pop_back();
+        mark_dirty(r, (int64_t)r->table.size());
+    }
+    r->pending = false;
+    r->leased_by_begin = false;
+    return ok();
+}
+
+int pkv_workspace_size(const pkv_pool* p, int batch, int64_t max_seq_len, size_t* bytes) {
+    if (!p || !bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    if (batch < 0 || max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "bad batch or length");
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    const int w = pkv::launch_workers(p->workers, batch, p->heads, max_seq_len);
+    *bytes = pkv::workspace_layout(batch, p->heads, p->head_dim, w).total;
+    return ok();
+}
+
+int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q,
+                               const void* k_new, const void* v_new, const int32_t* page_tables,
+                               int max_pages, const int32_t* seq_lens, int64_t max_seq_len,
+                               float* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    if (layer < 0 || layer >= p->layers)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (batch < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch");
+    if (batch == 0) return ok();
+    if (!q || !k_new || !v_new || !page_tables || !seq_lens || !out || !workspace)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
+    if (max_pages < 1 || max_seq_len < 1)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+    const int w = pkv::launch_workers(p->workers, batch, p->heads, max_seq_len);
+    const size_t need = pkv::workspace_layout(batch, p->heads, p->head_dim, w).total;
+    if (workspace_bytes < need)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need);
+    int rc = check_device(p);
+    if (rc != PKV_OK) return rc;
+    pkv::DecodeArgs a{};
+    a.dtype = p->dtype;
+    a.B = batch;
+    a.H = p->heads;
+    a.D = p->head_dim;
+    a.P = p->page_size;
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    void *kp, *vp;
+    pkv_pool_kv_ptr(p, layer, &kp, &vp);
+    a.k_pages = kp;
+    a.v_pages = vp;
+    a.n_pages = p->pages;
+    a.tables = page_tables;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.single_t = 0;
+    a.max_seq_len = max_seq_len;
+    a.out = out;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.workers = w;
+    a.dev_error = p->dev_error;
+    a.ev_before = p->ev_before;
+    a.ev_after = p->ev_after;
+    cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ok();
+}
+
+int pkv_pool_set_timing_events(pkv_pool* p, void* before, void* after) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if ((before == nullptr) != (after == nullptr))
+        return fail(PKV_ERR_INVALID_ARGUMENT, "give both events or neither");
+    p->ev_before = static_cast<cudaEvent_t>(before);
+    p->ev_after = static_cast<cudaEvent_t>(after);
+    return ok();
+}
+
+int pkv_check_device_status(pkv_pool* p, uint32_t* bits) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if (bits) *bits = 0;
+    if (p->host_only) return ok();
+    int rc = check_device(p);
+    if (rc != PKV_OK) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned word = 0;
+    if ((e = cudaMemcpy(&word, p->dev_error, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "read device error word");
+    if (word != 0 && (e = cudaMemset(p->dev_error, 0, sizeof word)) != cudaSuccess)
+        return cuda_fail(e, "clear device error word");
+    if (bits) *bits = word;
+    if (word != 0) return fail(PKV_ERR_DEVICE_CHECK, "device error bits 0x%x", word);
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+"""Move seeded synthetic inputs onto the device.
+
+Input plumbing for the GPU tests and the benchmark: builds q / k_new / v_new of a
+batched step and copies request history into pool pages through given page
+tables.  Holds no attention arithmetic and does not import the product
+package: callers pass torch views of the pool pages.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import F32, KHIST, VHIST, Q, rows, history_pages
+from .workloads import Workload
+
+TORCH_STORAGE = {F32: torch.float32, 1: torch.bfloat16}
+
+
+def step_inputs(w: Workload, layer: int = 0):
+    """Host arrays of one batched step: q [B,H,D] fp32, k_new / v_new [B,H,D] storage
+    dtype (token t_b - 1 of each request's key / value sequence)."""
+    B, H, D = w.B, w.H, w.D
+    sd = np.float32 if w.dtype == F32 else np.uint16
+    q = np.empty((B, H, D), np.float32)
+    k = np.empty((B, H, D), sd)
+    v = np.empty((B, H, D), sd)
+    for b in range(B):
+        t = int(w.seq_lens[b])
+        for h in range(H):
+            q[b, h] = rows(w.seed, Q, layer, b, h, t - 1, 1, D, F32)[0]
+            k[b, h] = rows(w.seed, KHIST, layer, b, h, t - 1, 1, D, w.dtype)[0]
+            v[b, h] = rows(w.seed, VHIST, layer, b, h, t - 1, 1, D, w.dtype)[0]
+    return q, k, v
+
+
+def to_device(x: np.ndarray, dtype: int | None = None, device="cuda") -> torch.Tensor:
+    """numpy -> torch on the device; uint16 arrays are bf16 bit patterns."""
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if x.dtype == np.uint16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t.to(device)
+
+
+def fill_history(k_pages: torch.Tensor, v_pages: torch.Tensor, w: Workload, tables: np.ndarray,
+                 layer: int = 0, requests=None) -> int:
+    """Write tokens 0 .. t_b - 2 of every request into its pages (slot t_b - 1 is left
+    for the step's own append).  k_pages / v_pages: [pages, H, P, D] device views of
+    one layer.  Returns the bytes written."""
+    P, H, D = w.P, w.H, w.D
+    written = 0
+    reqs = range(w.B) if requests is None else requests
+    for b in reqs:
+        t = int(w.seq_lens[b])
+        n = (t + P - 1) // P
+        idx = torch.from_numpy(np.ascontiguousarray(tables[b, :n], dtype=np.int64)).to(k_pages.device)
+        for kind, dst in ((KHIST, k_pages), (VHIST, v_pages)):
+            host = history_pages(w.seed, kind, layer, b, n, H, P, D, t - 1, w.dtype)
+            dev = to_device(host, w.dtype, k_pages.device)
+            dst.index_copy_(0, idx, dev)
+            written += host.nbytes
+    return written

@@ -1,0 +1,147 @@
+"""GPU-test helpers: run one batched step through the C ABI and the same step
+through the oracle, on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_decode_gb300 as pkv
+import synth
+from oracle.model import OraclePool
+from synth import F32, BF16, KHIST, VHIST
+from synth.device import fill_history, step_inputs, to_device
+from synth.workloads import Workload, churn_ops, LEASE
+
+FP32_ATOL = 1e-5        # max abs error, fp32 storage
+BF16_RTOL = 5e-3        # normwise per (request, head) row, bf16 storage
+
+
+def dtype_name(dtype: int) -> str:
+    return "f32" if dtype == F32 else "bf16"
+
+
+def check_close(out: np.ndarray, ref: np.ndarray, dtype: int, what: str = "") -> float:
+    """Assert the parity bar; return the error measure."""
+    out = np.asarray(out, dtype=np.float64)
+    assert np.isfinite(out).all(), f"{what}: non-finite output"
+    if dtype == F32:
+        err = float(np.abs(out - ref).max()) if out.size else 0.0
+        assert err <= FP32_ATOL, f"{what}: max abs error {err:.3e} > {FP32_ATOL}"
+        return err
+    num = np.abs(out - ref).max(axis=-1)
+    den = np.maximum(np.abs(ref).max(axis=-1), 1e-6)
+    err = float((num / den).max()) if out.size else 0.0
+    assert err <= BF16_RTOL, f"{what}: normwise relative error {err:.3e} > {BF16_RTOL}"
+    return err
+
+
+class BatchedRun:
+    """Pool + tables from the library's allocator (mirrored by the oracle model),
+    history written into the pages, one batched step run on the device."""
+
+    def __init__(self, w: Workload, layer: int = 0, max_seq_len=None, page_table_pad=0,
+                 stream=None):
+        self.w = w
+        self.layer = layer
+        self.pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dtype_name(w.dtype),
+                             w.max_context, w.seed)
+        self.opool = OraclePool(w.layers, w.pool_pages, w.H, w.D, w.P, w.dtype,
+                                max_context=w.max_context, seed=w.seed, storage=False)
+        self.reqs = [self.pool.request() for _ in range(w.B)]
+        self.oreqs = [self.opool.request() for _ in range(w.B)]
+        for r_i, kind, cnt in churn_ops(w) if w.churn_cycles else []:
+            for side, reqs in ((0, self.reqs), (1, self.oreqs)):
+                try:
+                    if kind == LEASE:
+                        reqs[r_i].lease_pages(cnt)
+                    else:
+                        reqs[r_i].release_pages()
+                except (pkv.PkvError, oracle.OracleError):
+                    pass
+        for b in range(w.B):
+            n = int(w.n_pages[b])
+            self.reqs[b].release_pages()
+            self.reqs[b].lease_pages(n)
+            self.oreqs[b].release_pages()
+            self.oreqs[b].lease_pages(n)
+        self.max_pages = int(w.n_pages.max()) + page_table_pad
+        self.tables = np.full((w.B, self.max_pages), -1, dtype=np.int32)
+        self.otables = np.full((w.B, self.max_pages), -1, dtype=np.int32)
+        for b in range(w.B):
+            t = self.reqs[b].page_table()
+            self.tables[b, :len(t)] = t
+            self.otables[b, :len(self.oreqs[b].table)] = self.oreqs[b].table
+        self.k_pages, self.v_pages = self.pool.kv_pages(layer)
+        fill_history(self.k_pages, self.v_pages, w, self.tables, layer)
+        self.q, self.k_new, self.v_new = step_inputs(w, layer)
+        self.max_seq_len = int(max_seq_len or w.seq_lens.max())
+        self.dev = dict(q=to_device(self.q), k=to_device(self.k_new), v=to_device(self.v_new),
+                        tables=torch.from_numpy(self.tables).cuda(),
+                        lens=torch.from_numpy(w.seq_lens.astype(np.int32)).cuda())
+        self.out = torch.full((w.B, w.H, w.D), float("nan"), device="cuda")
+        self.ws = self.pool.workspace(w.B, self.max_seq_len)
+        self.stream = stream
+
+    def run(self):
+        d = self.dev
+        self.pool.paged_decode_attention(self.layer, d["q"], d["k"], d["v"], d["tables"], d["lens"],
+                                         self.max_seq_len, out=self.out, workspace=self.ws,
+                                         stream=self.stream)
+        return self.out
+
+    def oracle_out(self, requests=None, heads=None) -> dict:
+        """Oracle output of the given requests (all by default) on a compact host pool
+        holding only their pages; tables are the oracle model's own."""
+        w = self.w
+        requests = list(range(w.B)) if requests is None else list(requests)
+        heads = list(range(w.H)) if heads is None else list(heads)
+        npg = [int(w.n_pages[b]) for b in requests]
+        compact = {}
+        for b, n in zip(requests, npg):
+            for pg in self.otables[b, :n]:
+                compact.setdefault(int(pg), len(compact))
+        sd = np.float32 if w.dtype == F32 else np.uint16
+        kp = np.zeros((len(compact), w.H, w.P, w.D), dtype=sd)
+        vp = np.zeros_like(kp)
+        ctab = np.full((len(requests), max(npg)), -1, dtype=np.int32)
+        for i, (b, n) in enumerate(zip(requests, npg)):
+            ids = np.array([compact[int(pg)] for pg in self.otables[b, :n]], dtype=np.int64)
+            ctab[i, :n] = ids
+            t = int(w.seq_lens[b])
+            kp[ids] = synth.history_pages(w.seed, KHIST, self.layer, b, n, w.H, w.P, w.D, t - 1, w.dtype)
+            vp[ids] = synth.history_pages(w.seed, VHIST, self.layer, b, n, w.H, w.P, w.D, t - 1, w.dtype)
+        lanes = [i * w.H + h for i in range(len(requests)) for h in heads]
+        ref = oracle.paged_decode_attention(kp, vp, self.q[requests], self.k_new[requests],
+                                            self.v_new[requests], ctab,
+                                            w.seq_lens[requests].astype(np.int32), w.dtype,
+                                            lanes=lanes)
+        return {(b, h): ref[i, h] for i, b in enumerate(requests) for h in heads}
+
+    def appended_rows(self, b: int):
+        """Device bytes of slot t_b - 1 of request b (K and V, all heads)."""
+        t = int(self.w.seq_lens[b])
+        pg = int(self.tables[b, (t - 1) // self.w.P])
+        slot = (t - 1) % self.w.P
+        k = self.k_pages[pg, :, slot].cpu()
+        v = self.v_pages[pg, :, slot].cpu()
+        if self.w.dtype == BF16:
+            k, v = k.view(torch.int16).numpy().view(np.uint16), v.view(torch.int16).numpy().view(np.uint16)
+        else:
+            k, v = k.numpy(), v.numpy()
+        return k, v
+
+    def close(self):
+        self.pool.close()
+
+
+def make_workload(name, seq_lens, H, D, P=16, dtype=F32, pool_pages=None, seed=0, layers=1,
+                  max_context=None, churn=0) -> Workload:
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    n = (seq_lens.astype(np.int64) + P - 1) // P
+    if pool_pages is None:
+        pool_pages = int(n.sum()) + 7
+    if max_context is None:
+        max_context = int(max(seq_lens.max(), 1))
+    return Workload(name, len(seq_lens), layers, H, D, P, dtype, int(pool_pages), int(max_context),
+                    seed, seq_lens, churn_cycles=churn)

@@ -1,0 +1,282 @@
+"""CUDA path vs the fp64 oracle, through the C ABI, on the same seeded inputs.
+
+Bar: bit-exact page tables, visible lengths and appended K/V bytes; max abs
+error <= 1e-5 for fp32 storage; normwise relative error per (request, head)
+row <= 5e-3 for bf16 storage (fp32 accumulation on the device).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_decode_gb300 as pkv
+import synth
+from oracle.model import OraclePool
+from synth import F32, BF16, KHIST, VHIST, Q, workloads
+from synth.device import to_device
+from tests._gpu import BatchedRun, check_close, make_workload, dtype_name, FP32_ATOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _host(t: torch.Tensor, dtype: int) -> np.ndarray:
+    t = t.cpu()
+    if dtype == BF16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+# ------------------------------------------------------------ transactional --
+
+def _lane_tensors(seed, layer, H, pos, D, dtype, kseed=None):
+    kseed = seed if kseed is None else kseed
+    q = synth.lane_rows(seed, Q, layer, 0, H, pos, D, F32)
+    k = synth.lane_rows(kseed, KHIST, layer, 0, H, pos, D, dtype)
+    v = synth.lane_rows(kseed, VHIST, layer, 0, H, pos, D, dtype)
+    return q, k, v
+
+
+def _serial(layers, H, D, dtype, pool_pages, max_context, steps, seed, abort_at=None,
+            check_at=None, P=16):
+    """Serial begin / append x layers / commit on the library and on the oracle model."""
+    pool = pkv.Pool(layers, pool_pages, H, D, P, dtype_name(dtype), max_context, seed)
+    req = pool.request()
+    opool = OraclePool(layers, pool_pages, H, D, P, dtype, max_context=max_context, seed=seed)
+    oreq = opool.request()
+    errs = []
+    for t in range(1, steps + 1):
+        pos = req.begin_token()
+        assert pos == oreq.begin_token() == t - 1
+        if abort_at is not None and t == abort_at:
+            for layer in range(layers - 1):
+                q, k, v = _lane_tensors(seed, layer, H, pos, D, dtype, kseed=seed + 99)
+                req.append_and_attend(layer, to_device(q), to_device(k),
+                                      to_device(v))
+                oreq.append_and_attend(layer, q, k, v, compute=False)
+            req.abort_token()
+            oreq.abort_token()
+            assert req.length == oreq.length == t - 1
+            assert req.page_table() == oreq.table
+            assert pool.free_list() == list(opool.free)
+            assert req.begin_token() == oreq.begin_token() == pos
+        compute = check_at is None or t in check_at
+        for layer in range(layers):
+            q, k, v = _lane_tensors(seed, layer, H, pos, D, dtype)
+            out = req.append_and_attend(layer, to_device(q), to_device(k),
+                                        to_device(v))
+            ref = oreq.append_and_attend(layer, q, k, v, compute=compute)
+            if compute:
+                errs.append(check_close(out.cpu().numpy(), ref, dtype, f"t={t} layer={layer}"))
+        req.commit_token()
+        oreq.commit_token()
+        assert req.length == oreq.length == t
+        assert req.page_table() == oreq.table
+    assert pool.free_list() == list(opool.free)
+    # every byte of the request's pages, in every layer, equals the oracle's pool
+    used = torch.tensor(req.page_table(), dtype=torch.int64)
+    for layer in range(layers):
+        kd, vd = pool.kv_pages(layer)
+        assert _host(kd[used.cuda()], dtype).tobytes() == opool.k[layer][used.numpy()].tobytes()
+        assert _host(vd[used.cuda()], dtype).tobytes() == opool.v[layer][used.numpy()].tobytes()
+    assert pool.check_device_status() == 0
+    c = req.counters()
+    assert c == {"committed_tokens": oreq.committed_tokens, "cache_appends": oreq.cache_appends,
+                 "score_cells": oreq.score_cells}
+    pool.close()
+    return c, errs
+
+
+def test_tiny_fixture_with_abort_and_retry():
+    """1 request, 2 layers, H=2, d_h=2, pages of 16, pool of 4 pages, t = 1..4, abort at t=3."""
+    w = workloads.tiny()
+    c, errs = _serial(w.layers, w.H, w.D, F32, w.pool_pages, w.max_context, 4, w.seed, abort_at=3)
+    assert c["score_cells"] == 4 * (1 + 2 + 3 + 4)
+    assert c["cache_appends"] == 2 * 4
+
+
+def test_tiny_fixture_counts_match_printed_values():
+    c, _ = _serial(2, 2, 2, F32, 4, 64, 3, 0)
+    assert c["score_cells"] == 24 and c["cache_appends"] == 6
+
+
+@pytest.mark.parametrize("t", [128, 512, 2048])
+def test_single_request_serial(t):
+    """12 layers, H=12, d_h=64, fp32, 4096-page shuffled pool, serial appends to t."""
+    checks = {1, 2, 15, 16, 17, 33, t // 2, t - 1, t}
+    _, errs = _serial(12, 12, 64, F32, 4096, 2048, t, 1, check_at=checks)
+    assert max(errs) <= FP32_ATOL
+
+
+def test_serial_bf16_and_page_size_32():
+    _serial(3, 4, 128, BF16, 64, 200, 70, 5, abort_at=33, P=32)
+
+
+# ------------------------------------------------------------------ batched --
+
+def _batched_check(w, requests=None, heads=None, **kw):
+    run = BatchedRun(w, **kw)
+    try:
+        assert run.tables.tolist() == run.otables.tolist()
+        out = run.run().cpu().numpy()
+        assert run.pool.check_device_status() == 0
+        ref = run.oracle_out(requests, heads)
+        got = np.stack([out[b, h] for (b, h) in ref])
+        exp = np.stack(list(ref.values()))
+        err = check_close(got, exp, w.dtype, w.name)
+        reqs = range(w.B) if requests is None else requests
+        for b in reqs:
+            k, v = run.appended_rows(b)
+            assert k.tobytes() == run.k_new[b].tobytes() and v.tobytes() == run.v_new[b].tobytes()
+        return run, err
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_batched_decode_full_config(dtype):
+    """64 requests, H=32, d_h=128, t ~ U{1..4096}, 32768-page shuffled pool: every lane."""
+    _batched_check(workloads.batched(dtype))
+
+
+def test_ragged_fragmented_pool_sampled():
+    """256 requests, lognormal lengths, 600k-page pool after 10k lease/release cycles:
+    the longest, the shortest and 30 random requests, all heads."""
+    w = workloads.ragged()
+    order = np.argsort(w.seq_lens)
+    rng = np.random.default_rng(0)
+    sample = sorted(set([int(order[0]), int(order[-1]), int(order[len(order) // 2])] +
+                        rng.choice(w.B, 30, replace=False).tolist()))
+    _batched_check(w, requests=sample)
+
+
+def test_long_context_sampled():
+    """16 requests x 131072 tokens, H=8, d_h=128, bf16: 3 requests, all heads."""
+    _batched_check(workloads.long_context(), requests=[0, 7, 15])
+
+
+# --------------------------------------------------------------- edge cases --
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_ragged_tails_and_single_tokens(dtype):
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 47, 48, 49, 1, 64, 255, 256, 257]
+    _batched_check(make_workload("tails", lens, 3, 64, dtype=dtype, seed=3))
+
+
+def test_all_single_token_requests():
+    w = make_workload("ones", [1] * 37, 4, 32, dtype=BF16, seed=4)
+    run, _ = _batched_check(w)
+
+
+@pytest.mark.parametrize("D,dtype", [(2, F32), (4, F32), (8, F32), (16, BF16), (32, F32),
+                                     (64, BF16), (128, F32), (256, BF16), (2, BF16)])
+def test_head_widths(D, dtype):
+    _batched_check(make_workload(f"d{D}", [1, 40, 100, 16, 77], 2, D, dtype=dtype, seed=D))
+
+
+@pytest.mark.parametrize("P", [32, 64])
+def test_page_sizes(P):
+    _batched_check(make_workload(f"p{P}", [1, 31, 33, 64, 65, 200], 2, 64, P=P, dtype=F32, seed=P))
+
+
+def test_contiguous_single_page_layout_equals_paged():
+    """One max-context page per request (page_size = max_context) gives the paged result."""
+    lens = [37, 256, 5, 129]
+    a = BatchedRun(make_workload("paged", lens, 2, 64, P=16, dtype=F32, seed=8))
+    b = BatchedRun(make_workload("contig", lens, 2, 64, P=256, dtype=F32, seed=8, max_context=256))
+    try:
+        assert b.tables.shape[1] == 1
+        oa, ob = a.run().cpu().numpy(), b.run().cpu().numpy()
+        assert np.abs(oa - ob).max() <= 2e-6
+        ref = a.oracle_out()
+        check_close(np.stack([ob[k] for k in ref]), np.stack(list(ref.values())), F32, "contig")
+    finally:
+        a.close()
+        b.close()
+
+
+def test_more_workers_than_tiles():
+    """A loose max_seq_len gives far more workers than tiles (empty workers)."""
+    _batched_check(make_workload("few", [40, 3], 1, 64, dtype=F32, seed=9, max_context=8192),
+                   max_seq_len=8192)
+
+
+def test_wide_page_table_rows_and_side_stream():
+    s = torch.cuda.Stream()
+    w = make_workload("stream", [300, 20, 1000], 4, 128, dtype=BF16, seed=10)
+    with torch.cuda.stream(s):
+        _batched_check(w, page_table_pad=5, stream=s)
+    torch.cuda.synchronize()
+
+
+def test_repeated_calls_are_deterministic():
+    w = make_workload("rep", [1000, 17, 4000, 2], 8, 128, dtype=BF16, seed=11)
+    run = BatchedRun(w)
+    try:
+        a = run.run().clone()
+        b = run.run().clone()
+        assert torch.equal(a, b)
+    finally:
+        run.close()
+
+
+def test_bad_lengths_and_page_ids_set_error_bits():
+    w = make_workload("bad", [20, 50, 7], 2, 64, dtype=F32, seed=12)
+    run = BatchedRun(w)
+    try:
+        good = run.run().cpu().numpy()
+        assert run.pool.check_device_status() == 0
+        lens = run.dev["lens"].clone()
+        run.dev["lens"][0] = 0                       # t < 1
+        run.run()
+        assert run.pool.device_status_bits() & pkv.PKV_DEVERR_SEQ_LEN
+        run.dev["lens"].copy_(lens)
+        run.dev["lens"][1] = run.max_seq_len + 1     # t > max_seq_len
+        run.run()
+        assert run.pool.device_status_bits() & pkv.PKV_DEVERR_SEQ_LEN
+        run.dev["lens"].copy_(lens)
+        saved = run.dev["tables"][1, 1].item()
+        run.dev["tables"][1, 1] = run.pool.pages     # page id out of range
+        out = run.run().cpu().numpy()
+        assert run.pool.device_status_bits() & pkv.PKV_DEVERR_PAGE_ID
+        assert np.array_equal(out[0], good[0]) and np.array_equal(out[2], good[2])
+        run.dev["tables"][1, 1] = saved
+        out = run.run().cpu().numpy()
+        assert run.pool.check_device_status() == 0
+        assert np.abs(out - good).max() == 0
+    finally:
+        run.close()
+
+
+def test_argument_errors_change_nothing():
+    w = make_workload("args", [10, 20], 2, 64, dtype=F32, seed=13)
+    run = BatchedRun(w)
+    try:
+        d = run.dev
+        import ctypes
+        st = pkv.lib.pkv_paged_decode_attention(
+            run.pool.handle, 0, 2, ctypes.c_void_p(d["q"].data_ptr()), ctypes.c_void_p(d["k"].data_ptr()),
+            ctypes.c_void_p(d["v"].data_ptr()), ctypes.c_void_p(d["tables"].data_ptr()),
+            d["tables"].shape[1], ctypes.c_void_p(d["lens"].data_ptr()), 20,
+            ctypes.c_void_p(run.out.data_ptr()), ctypes.c_void_p(run.ws.data_ptr()), 16, None)
+        assert st == pkv.PKV_ERR_INVALID_ARGUMENT
+        st = pkv.lib.pkv_paged_decode_attention(run.pool.handle, 0, 0, None, None, None, None, 1,
+                                                None, 1, None, None, 0, None)
+        assert st == pkv.PKV_OK
+        st = pkv.lib.pkv_paged_decode_attention(run.pool.handle, 1, 2, None, None, None, None, 1,
+                                                None, 1, None, None, 0, None)
+        assert st == pkv.PKV_ERR_INVALID_ARGUMENT
+        assert torch.isnan(run.out).all()
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.Pool(1, 4, 2, 96, 16, "bf16", 64)
+        assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.Pool(1, 4, 2, 64, 8, "bf16", 64)
+        assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+    finally:
+        run.close()

@@ -1,0 +1,164 @@
+"""Host bookkeeping of the library against the oracle's pool model, bit-exact
+(CPU only: bookkeeping-only pools, no device storage)."""
+import numpy as np
+import pytest
+
+import paged_kv_cache_decode_gb300 as pkv
+from oracle.model import OraclePool, OracleError, Status, shuffled_pages
+from synth import F32, BF16, workloads
+from tests.conftest import read_golden
+
+
+def host_pool(layers=1, pages=64, heads=2, head_dim=4, page_size=16, dtype="f32",
+              max_context=1024, seed=0):
+    return pkv.Pool(layers, pages, heads, head_dim, page_size, dtype, max_context, seed,
+                    host_only=True)
+
+
+@pytest.mark.parametrize("pages,seed", [(1, 0), (4, 0), (4096, 1), (32768, 2), (1000, 2**63 + 5)])
+def test_free_list_matches_oracle_shuffle(pages, seed):
+    with host_pool(pages=pages, seed=seed, max_context=16 * pages) as p:
+        assert p.free_list() == shuffled_pages(pages, seed)
+
+
+def test_zero_pages_sizes_one_full_context():
+    with host_pool(pages=0, max_context=100) as p:
+        assert p.pages == 7
+
+
+def test_pool_bytes_worked_example():
+    g = read_golden("pages_counts.txt")
+    with pkv.Pool(32, 512, 16, 64, 16, "bf16", 8192, host_only=True) as p:
+        assert p.bytes() == g["kv_bytes_L32_H16_dh64_S8192_2byte"]
+
+
+def _apply(op, req, oreq):
+    """Run one operation on both sides; return the status of each."""
+    name, arg = op
+    st_lib = pkv.PKV_OK
+    st_orc = Status.OK
+    try:
+        getattr(req, name)(*arg)
+    except pkv.PkvError as e:
+        st_lib = e.status
+    try:
+        getattr(oreq, name)(*arg)
+    except OracleError as e:
+        st_orc = e.status
+    return st_lib, st_orc
+
+
+def test_lease_release_begin_abort_sequences_match_oracle():
+    rng = np.random.default_rng(7)
+    P, pages, maxc = 16, 40, 16 * 12
+    with host_pool(pages=pages, max_context=maxc, seed=9) as p:
+        op_ = OraclePool(1, pages, 2, 4, P, F32, max_context=maxc, seed=9, storage=False)
+        reqs = [p.request() for _ in range(4)]
+        oreqs = [op_.request() for _ in range(4)]
+        for step in range(3000):
+            i = int(rng.integers(0, 4))
+            r, o = reqs[i], oreqs[i]
+            kind = int(rng.integers(0, 5))
+            if kind == 0:
+                op = ("lease_pages", (int(rng.integers(-1, 6)),))
+            elif kind == 1:
+                op = ("release_pages", ())
+            elif kind == 2:
+                op = ("begin_token", ())
+            else:
+                op = ("abort_token", ())
+            a, b = _apply(op, r, o)
+            assert a == b, (step, op, a, b)
+            assert r.page_table() == o.table
+            assert r.length == o.length
+        assert p.free_list() == list(op_.free)
+
+
+def test_rejected_calls_change_nothing():
+    with host_pool(pages=3, max_context=32, seed=1) as p:
+        r = p.request()
+        snap = lambda: (r.page_table(), r.length, p.free_list())
+        s0 = snap()
+        for fn, st in [(r.commit_token, pkv.PKV_ERR_BAD_STATE), (r.abort_token, pkv.PKV_ERR_BAD_STATE),
+                       (lambda: r.lease_pages(3), pkv.PKV_ERR_CAPACITY_EXCEEDED),
+                       (lambda: r.lease_pages(-2), pkv.PKV_ERR_INVALID_ARGUMENT)]:
+            with pytest.raises(pkv.PkvError) as e:
+                fn()
+            assert e.value.status == st and snap() == s0
+        assert r.begin_token() == 0
+        s1 = snap()
+        for fn, st in [(r.begin_token, pkv.PKV_ERR_BAD_STATE), (r.release_pages, pkv.PKV_ERR_BAD_STATE),
+                       (lambda: r.lease_pages(1), pkv.PKV_ERR_BAD_STATE),
+                       (r.commit_token, pkv.PKV_ERR_BAD_STATE)]:
+            with pytest.raises(pkv.PkvError) as e:
+                fn()
+            assert e.value.status == st and snap() == s1
+        import torch
+        z = torch.zeros(2, 4)
+        with pytest.raises(ValueError):          # host tensors are refused by the binding
+            r.append_and_attend(0, z, z, z)
+        r.abort_token()
+        assert snap() == s0
+        # pool exhaustion
+        r.lease_pages(2)
+        other = p.request()
+        other.lease_pages(1)
+        with pytest.raises(pkv.PkvError) as e:
+            p.request().lease_pages(1)
+        assert e.value.status == pkv.PKV_ERR_OUT_OF_PAGES
+
+
+def test_append_on_host_only_pool_reports_no_storage():
+    import ctypes
+    with host_pool() as p:
+        r = p.request()
+        r.begin_token()
+        st = pkv.lib.pkv_append_and_attend(r.handle, 0, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                           ctypes.c_void_p(16), ctypes.c_void_p(16), None)
+        assert st == pkv.PKV_ERR_NO_STORAGE
+        with pytest.raises(pkv.PkvError):
+            p.kv_pages(0)
+        assert st == pkv.PKV_ERR_NO_STORAGE
+
+
+def test_pool_destroy_refused_while_requests_live():
+    p = host_pool()
+    r = p.request()
+    st = pkv.lib.pkv_pool_destroy(p.handle)
+    assert st == pkv.PKV_ERR_BAD_STATE
+    r.close()
+    p.close()
+
+
+def test_destroy_returns_pages():
+    with host_pool(pages=10, seed=4) as p:
+        r = p.request()
+        r.lease_pages(4)
+        r.begin_token()
+        r.close()
+        assert p.free_pages == 10
+
+
+def test_ragged_churn_tables_match_oracle():
+    """The fragmented-pool recipe: 10k seeded lease/release cycles, then every request
+    leases exactly its pages.  Page tables and free list are bit-identical."""
+    w = workloads.ragged()
+    ops = workloads.churn_ops(w)
+    with pkv.Pool(1, w.pool_pages, w.H, w.D, w.P, "bf16", w.max_context, w.seed,
+                  host_only=True) as p:
+        op_ = OraclePool(1, w.pool_pages, w.H, w.D, w.P, BF16, max_context=w.max_context,
+                         seed=w.seed, storage=False)
+        reqs = [p.request() for _ in range(w.B)]
+        oreqs = [op_.request() for _ in range(w.B)]
+        for r_i, kind, cnt in ops:
+            op = ("lease_pages", (cnt,)) if kind == workloads.LEASE else ("release_pages", ())
+            a, b = _apply(op, reqs[r_i], oreqs[r_i])
+            assert a == b
+        for b in range(w.B):
+            _apply(("release_pages", ()), reqs[b], oreqs[b])
+            _apply(("lease_pages", (int(w.n_pages[b]),)), reqs[b], oreqs[b])
+        for r, o in zip(reqs, oreqs):
+            assert r.page_table() == o.table
+        assert p.free_list() == list(op_.free)
+        used = sorted(x for r in reqs for x in r.page_table())
+        assert len(used) == len(set(used)) == int(w.n_pages.sum())
