@@ -42,10 +42,18 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ---------------------------------------------------------------- workload --
 
-def make_workload(name: str, rank: int = 0):
+def make_workload(name: str, rank: int = 0, requests: int = 0):
+    """The named workload; ``requests`` > 0 keeps only its first requests (small
+    profiling captures; the long-context pool shrinks to match)."""
     from synth import workloads
     w = workloads.REGISTRY[name]()
     w.seed += 1000 * rank          # each replica draws its own values
+    if 0 < requests < w.B:
+        w.B = requests
+        w.seq_lens = w.seq_lens[:requests].copy()
+        if w.name == "long":
+            w.pool_pages = int(w.n_pages.sum())
+        w.name += f"_first{requests}"
     return w
 
 
@@ -240,7 +248,7 @@ def run_gpu(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     rank, world = dist_init("nccl")
-    w = make_workload(args.workload, rank)
+    w = make_workload(args.workload, rank, args.requests)
     pool, reqs, host, dev, ws, out, max_seq_len = setup_device(w, torch)
     stream = torch.cuda.current_stream()
 
@@ -392,9 +400,11 @@ def sample_requests(w, target_tokens: int):
     return out
 
 
-def cpu_baseline(w, target_tokens=4 * 131072):
+def cpu_baseline(w, lane_tokens=1 << 24):
+    """The oracle on the whole step, or on its first requests up to ``lane_tokens``
+    retained (lane, token) pairs (~10-30 s of CPU work on 16 cores)."""
     import oracle
-    reqs = sample_requests(w, target_tokens)
+    reqs = sample_requests(w, max(1, lane_tokens // w.H))
     run, sbytes, lens = oracle_sample(w, reqs)
     t0 = time.perf_counter()
     run()
@@ -411,7 +421,7 @@ def run_reference(args):
     if rank != 0:
         return None, None
     import oracle
-    w = make_workload(args.workload, 0)
+    w = make_workload(args.workload, 0, args.requests)
     reqs = sample_requests(w, 1)                       # one request per step
     run, sbytes, lens = oracle_sample(w, reqs)
     for _ in range(args.warmup):
@@ -448,6 +458,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="long")
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="keep only the first N requests (small profiling captures)")
     return ap.parse_args(argv)
 
 
