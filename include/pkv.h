@@ -244,6 +244,39 @@ int pkv_paged_decode_attention(pkv_pool* pool, int layer, int batch, const float
                                int max_pages, const int32_t* seq_lens, int64_t max_seq_len,
                                float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Bytes of the fixed device array that pkv_paged_decode_attention_static uses
+ * as scratch (8 MiB).  Every GPU that loads libpkv.so holds it until exit.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * pkv_paged_decode_attention without a workspace argument and without any
+ * allocation.  The source pages have no counterpart to this call: it exists for
+ * callers that cannot allocate device memory themselves, such as code embedded
+ * in an application that has already reserved the GPU's memory for its own
+ * arena and lends no allocator, or code that must not call cudaMalloc /
+ * cudaFree on a latency-critical path because those calls can synchronise the
+ * device.  Arguments, layout and results are those of
+ * pkv_paged_decode_attention.
+ *
+ * Scratch is a file-scope device array of PKV_STATIC_SCRATCH_BYTES inside the
+ * library.  The call makes no cudaMalloc, cudaFree or other allocating call.
+ * The first call on a device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress; make that first call before any
+ * stream capture.  A batch whose scratch need (pkv_workspace_size) exceeds
+ * PKV_STATIC_SCRATCH_BYTES is rejected with PKV_ERR_INVALID_ARGUMENT and
+ * changes nothing.  All calls on a device share the array and it keeps the last
+ * call's contents (no part of it needs to start at zero); calls whose device
+ * work can overlap race on it and must be serialised by the caller, for
+ * instance by issuing them on one stream.
+ */
+int pkv_paged_decode_attention_static(pkv_pool* pool, int layer, int batch, const float* q,
+                                      const void* k_new, const void* v_new,
+                                      const int32_t* page_tables, int max_pages,
+                                      const int32_t* seq_lens, int64_t max_seq_len, float* out,
+                                      void* stream);
+
 /* ------------------------------------------------------------- tracing -- */
 
 /*

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 
-SOURCES = ["decode.cu", "pool.cpp"]
+SOURCES = ["decode.cu", "pool.cpp", "static_scratch.cu"]
 HEADERS = [os.path.join(CSRC, "pkv_internal.h"), os.path.join(INCLUDE, "pkv.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+struct pkv_pool;
+
 namespace pkv {
 
 constexpr int kTile = 16;          // key rows staged and processed as one unit
@@ -60,5 +62,16 @@ bool decode_supported(int dtype, int D);
 
 // Enqueue plan (batched only), split and merge kernels on `stream`.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Record a failed call in the thread's last-error message; returns `status`.
+int record_error(int status, const char* fmt, ...);
+
+// Validate the arguments of a batched call and fill `a` (all but the
+// workspace); `*workspace_bytes` receives the scratch the launch needs.
+// Returns PKV_OK (with a.B == 0 for an empty batch) or a recorded error.
+int prepare_batched(pkv_pool* pool, int layer, int batch, const float* q, const void* k_new,
+                    const void* v_new, const int32_t* page_tables, int max_pages,
+                    const int32_t* seq_lens, int64_t max_seq_len, float* out, DecodeArgs* a,
+                    size_t* workspace_bytes);
 
 }  // namespace pkv

@@ -568,3 +568,60 @@ int pkv_check_device_status(pkv_pool* p, uint32_t* bits) {
 }
 
 }  // extern "C"
+
+namespace pkv {
+
+int record_error(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+int prepare_batched(pkv_pool* p, int layer, int batch, const float* q, const void* k_new,
+                    const void* v_new, const int32_t* page_tables, int max_pages,
+                    const int32_t* seq_lens, int64_t max_seq_len, float* out, DecodeArgs* a,
+                    size_t* workspace_bytes) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    if (layer < 0 || layer >= p->layers)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (batch < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch");
+    *a = DecodeArgs{};
+    *workspace_bytes = 0;
+    if (batch == 0) return ok();
+    if (!q || !k_new || !v_new || !page_tables || !seq_lens || !out)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
+    if (max_pages < 1 || max_seq_len < 1)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
+    int rc = check_device(p);
+    if (rc != PKV_OK) return rc;
+    const int w = launch_workers(p->workers, batch, p->heads, max_seq_len);
+    *workspace_bytes = workspace_layout(batch, p->heads, p->head_dim, w).total;
+    a->dtype = p->dtype;
+    a->B = batch;
+    a->H = p->heads;
+    a->D = p->head_dim;
+    a->P = p->page_size;
+    a->q = q;
+    a->k_new = k_new;
+    a->v_new = v_new;
+    a->k_pages = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)layer;
+    a->v_pages = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)layer;
+    a->n_pages = p->pages;
+    a->tables = page_tables;
+    a->max_pages = max_pages;
+    a->seq_lens = seq_lens;
+    a->max_seq_len = max_seq_len;
+    a->out = out;
+    a->workers = w;
+    a->dev_error = p->dev_error;
+    a->ev_before = p->ev_before;
+    a->ev_after = p->ev_after;
+    return ok();
+}
+
+}  // namespace pkv
