@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention: achieved HBM GB/s (% of 8 TB/s) and decode tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "decode.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -194,16 +194,21 @@ def decode_source_hash() -> str:
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per launch of the split kernel from a committed ncu summary, or None
-    when the kernel source changed since the counters were taken."""
+    """DRAM bytes per launch of the split kernel from the committed ncu summary
+    profiles/traffic_split_decode_<workload>.txt, or None when there is none or
+    the kernel source changed since the counters were taken."""
+    rec = {}
     try:
-        with open(TRAFFIC_FILE) as f:
-            rec = json.load(f).get(workload)
-    except (OSError, ValueError):
+        with open(os.path.join(TRAFFIC_DIR, f"traffic_split_decode_{workload}.txt")) as f:
+            for line in f:
+                line = line.split("#", 1)[0].split()
+                if len(line) == 2:
+                    rec[line[0]] = line[1]
+    except OSError:
         return None
-    if not rec or rec.get("source_sha256") != decode_source_hash():
+    if rec.get("source_sha256") != decode_source_hash() or "dram_bytes_per_launch" not in rec:
         return None
-    return rec.get("dram_bytes_per_launch")
+    return int(rec["dram_bytes_per_launch"])
 
 
 # ------------------------------------------------------------ the GPU arm --
