@@ -23,9 +23,14 @@
 //
 // A lane that a single worker covers completely is finished by that worker.
 // Otherwise each worker covering part of it writes a partial (m, l, o[d_h])
-// into slot lane + worker of the workspace (slots never collide: see
-// merge_kernel), and the merge kernel combines them:
+// into slot lane + worker of the workspace and bumps the lane's counter; the
+// last of the lane's workers to arrive merges the partials:
 //     out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s.
+// Tile x belongs to worker floor(((x + 1) W - 1) / T), the inverse of
+// begin(w) = floor(w T / W); slots never collide across lanes because the
+// first worker of lane i + 1 is at least the last worker of lane i.  A small
+// plan kernel runs first (lengths, tile prefix, worker table, counters); the
+// split kernel is launched as its programmatic dependent.
 //
 // The append is fused into the worker that owns the lane's last tile: once that
 // tile's copy has landed it overwrites row t_b - 1 of the staged tile with
@@ -71,8 +76,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+#ifndef PKV_WAIT_HINT_NS
+#define PKV_WAIT_HINT_NS 0         // suspend-time hint of one try_wait (0: hardware default)
+#endif
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
+#if PKV_WAIT_HINT_NS > 0
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(PKV_WAIT_HINT_NS)
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -80,6 +98,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "=r"(done)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
+#endif
     return done != 0;
 }
 
@@ -106,9 +125,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+#ifndef PKV_L2_EVICT_FIRST
+#define PKV_L2_EVICT_FIRST 1       // stream K/V with an L2 evict-first policy
+#endif
+
+__device__ __forceinline__ uint64_t l2_stream_policy() {
     uint64_t pol;
+#if PKV_L2_EVICT_FIRST
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+#else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+#endif
     return pol;
 }
 
@@ -120,6 +147,16 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching now / wait until the previous kernel's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------- element access --
@@ -138,31 +175,38 @@ struct Storage;
 
 template <>
 struct Storage<float> {
-    static constexpr int dtype = PKV_F32;
+    // N elements -> N/2 float pairs
     template <int N>
-    __device__ __forceinline__ static void to_float(const void* bits, float* out) {
-        const float* f = reinterpret_cast<const float*>(bits);
+    __device__ __forceinline__ static void to_float2(const void* bits, float2* out) {
+        const float2* f = reinterpret_cast<const float2*>(bits);
 #pragma unroll
-        for (int i = 0; i < N; ++i) out[i] = f[i];
+        for (int i = 0; i < N / 2; ++i) out[i] = f[i];
     }
 };
 
 template <>
 struct Storage<__nv_bfloat16> {
-    static constexpr int dtype = PKV_BF16;
     // bf16 is the upper half of an fp32: element 2i is the low half of word i.
     template <int N>
-    __device__ __forceinline__ static void to_float(const void* bits, float* out) {
+    __device__ __forceinline__ static void to_float2(const void* bits, float2* out) {
         const uint32_t* w = reinterpret_cast<const uint32_t*>(bits);
 #pragma unroll
-        for (int i = 0; i < N / 2; ++i) {
-            out[2 * i] = __uint_as_float(w[i] << 16);
-            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
+        for (int i = 0; i < N / 2; ++i)
+            out[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
     }
 };
 
-// Warp geometry of one tile for storage type T and head width D.
+#ifndef PKV_SM_SMEM_BUDGET
+#define PKV_SM_SMEM_BUDGET 131072  // stage-ring bytes of one split CTA (one CTA per SM)
+#endif
+
+// Warp geometry of one 16-row tile for storage type T and head width D, and
+// the CTA shape.  TPR lanes share one row (VEC elements each, one 16-byte
+// vector at most); RPI rows are read per warp step.  After the dot products, a
+// transposed shuffle reduction leaves lane l holding the full score of row
+// ((l % TPR) >> 1) * RPI + l / TPR (lanes l and l ^ 1 hold the same row when
+// TPR >= 2), so each lane takes one exp2 per tile.  One CTA per SM: WARPS
+// workers, each with STAGES tiles in flight, within the shared-memory budget.
 template <typename T, int D>
 struct Geo {
     static constexpr int ES = sizeof(T);
@@ -170,16 +214,26 @@ struct Geo {
     static constexpr int VBYTES = VEC * ES;                    // 16, 8 or 4
     static constexpr int TPR = D / VEC;                        // lanes sharing one row
     static constexpr int RPI = 32 / TPR;                       // rows per warp step
-    static constexpr int ITERS = (kTile + RPI - 1) / RPI;      // warp steps per tile
+    static constexpr int ITERS = TPR >= 2 ? TPR / 2 : 1;       // warp steps per tile
+    static constexpr int DUP = TPR >= 2 ? 2 : 1;               // lanes holding each score
+    static constexpr int HALVING_ROUNDS = ITERS == 16 ? 4 : ITERS == 8 ? 3 : ITERS == 4 ? 2
+                                        : ITERS == 2 ? 1 : 0;  // log2(ITERS)
     static constexpr int TILE_BYTES = kTile * D * ES;          // K (or V) rows of one tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int BUDGET = 24 * 1024;                   // shared memory per worker
-    static constexpr int STAGES_RAW = BUDGET / STAGE_BYTES;
+    static constexpr int STAGES_AT_WARPS = PKV_SM_SMEM_BUDGET / (kSplitWarps * STAGE_BYTES);
+    static constexpr int WARPS = STAGES_AT_WARPS >= 2
+        ? kSplitWarps : (PKV_SM_SMEM_BUDGET / (2 * STAGE_BYTES) > 0 ? PKV_SM_SMEM_BUDGET / (2 * STAGE_BYTES) : 1);
+    static constexpr int STAGES_RAW = PKV_SM_SMEM_BUDGET / (WARPS * STAGE_BYTES);
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES;
-    static constexpr int CTA_SMEM = kSplitWarps * WARP_SMEM + kSplitWarps * STAGES * 8;
-    static_assert(D % VEC == 0 && TPR <= 32 && (TPR & (TPR - 1)) == 0, "unsupported head width");
+    // per warp: stage buffers, then per stage an mbarrier (8 B) and the staged page id (4 B)
+    static constexpr int CTA_SMEM = WARPS * (WARP_SMEM + STAGES * 12);
+    static constexpr int DPL = D >= 32 ? D / 32 : 1;           // features per lane when merging
+    static_assert(D % VEC == 0 && VEC % 2 == 0, "unsupported head width");
+    static_assert(TPR <= 32 && (TPR & (TPR - 1)) == 0, "unsupported head width");
+    static_assert(RPI * ITERS >= kTile, "a warp step pattern must cover the tile");
     static_assert(TILE_BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
+    static_assert(WARPS >= 1 && WARPS <= 32 && CTA_SMEM <= 227 * 1024, "CTA does not fit an SM");
 };
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
@@ -197,25 +251,18 @@ struct KParams {
     int max_pages;
     const int32_t* seq_lens;    // nullptr: one request of length single_t
     int64_t single_t;
-    int64_t single_tiles;
     int64_t max_seq_len;
     int B, H, P, tiles_per_page;
     float qscale;               // log2(e) / sqrt(D)
     float* out;
-    int64_t* req_prefix;
-    int32_t* worker_req;
+    int64_t* req_prefix;        // [B + 1] tiles-per-lane prefix (plan kernel)
+    int32_t* worker_req;        // [W] request of each worker's first tile (plan kernel)
+    int32_t* lane_cnt;          // [B * H] partials deposited per split lane (zeroed by plan)
     float2* part_ml;
     float* part_o;
     int W;
     unsigned* err;
 };
-
-// Tiles-per-lane prefix over requests (written by plan_kernel; closed form for
-// a single request).
-__device__ __forceinline__ int64_t req_prefix_at(const KParams& p, int b) {
-    if (p.seq_lens == nullptr) return b == 0 ? 0 : p.single_tiles;
-    return __ldg(p.req_prefix + b);
-}
 
 __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
@@ -224,20 +271,25 @@ __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
 // ----------------------------------------------------------- plan kernel --
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemRequests = 2048;   // prefix kept in shared memory up to this batch
 
 // Validates lengths, writes the per-request tile prefix and the first request
-// of every worker.  One CTA.
+// of every worker, and zeroes the per-lane partial counters.  One CTA.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
+    pdl_launch_dependents();   // the split grid may launch now; it waits for our writes
     __shared__ int64_t warp_sums[kPlanThreads / 32];
     __shared__ int64_t carry_s;
+    __shared__ int64_t pre_s[kPlanSmemRequests + 1];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const bool in_smem = p.B <= kPlanSmemRequests;
     if (tid == 0) carry_s = 0;
+    for (int64_t i = tid; i < (int64_t)p.B * p.H; i += kPlanThreads) p.lane_cnt[i] = 0;
     __syncthreads();
     for (int base = 0; base < p.B; base += kPlanThreads) {
         const int i = base + tid;
         int64_t n = 0;
         if (i < p.B) {
-            const int64_t t = p.seq_lens[i];
+            const int64_t t = seq_len_at(p, i);
             const int64_t pages = (t + p.P - 1) / p.P;
             if (t < 1 || t > p.max_seq_len || pages > p.max_pages) {
                 atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
@@ -265,21 +317,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
         __syncthreads();
         const int64_t carry = carry_s;
         const int64_t before = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - n;
-        if (i < p.B) p.req_prefix[i] = carry + before;
+        if (i < p.B) {
+            p.req_prefix[i] = carry + before;
+            if (in_smem) pre_s[i] = carry + before;
+        }
         __syncthreads();
         if (tid == 0) carry_s = carry + warp_sums[kPlanThreads / 32 - 1];
         __syncthreads();
     }
     const int64_t total = carry_s;
-    if (tid == 0) p.req_prefix[p.B] = total;
+    if (tid == 0) {
+        p.req_prefix[p.B] = total;
+        if (in_smem) pre_s[p.B] = total;
+    }
     __syncthreads();
     const int64_t T = (int64_t)p.H * total;
+    const int64_t* pre = in_smem ? pre_s : p.req_prefix;
     for (int w = tid; w < p.W; w += kPlanThreads) {
         const int64_t x = ((int64_t)w * T) / p.W;
         int lo = 0, hi = p.B - 1;   // largest b with H * prefix[b] <= x
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)p.H * p.req_prefix[mid] <= x) lo = mid; else hi = mid - 1;
+            if ((int64_t)p.H * pre[mid] <= x) lo = mid; else hi = mid - 1;
         }
         p.worker_req[w] = lo;
     }
@@ -287,26 +346,37 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
 
 // ---------------------------------------------------------- split kernel --
 
-// Position of a worker inside the flattened (request, head, tile) sequence.
+// Position of a worker inside the flattened (request, head, tile) sequence,
+// with the tile's page-table index and first slot tracked incrementally.
 struct Cursor {
     int b, h;
-    int64_t tile;      // tile within the lane
-    int64_t n;         // tiles of this lane
-    int64_t first;     // H * prefix[b]
+    int tile;          // tile within the lane
+    int n;             // tiles of this lane
+    int page_idx;      // logical page of the tile
+    int slot0;         // first slot of the tile within its page
+    int64_t first;     // flattened index of tile 0 of head 0 of request b
 };
 
 __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
-    if (++c.tile < c.n) return;
+    ++c.tile;
+    c.slot0 += kTile;
+    if (c.slot0 == p.P) {
+        c.slot0 = 0;
+        ++c.page_idx;
+    }
+    if (c.tile < c.n) return;
     c.tile = 0;
+    c.page_idx = 0;
+    c.slot0 = 0;
     if (++c.h < p.H) return;
     c.h = 0;
     // next request with at least one tile
-    int64_t pre = req_prefix_at(p, c.b + 1);
+    int64_t pre = __ldg(p.req_prefix + c.b + 1);
     while (c.b + 1 < p.B) {
         ++c.b;
-        const int64_t nxt = req_prefix_at(p, c.b + 1);
+        const int64_t nxt = __ldg(p.req_prefix + c.b + 1);
         if (nxt > pre) {
-            c.n = nxt - pre;
+            c.n = (int)(nxt - pre);
             c.first = (int64_t)p.H * pre;
             return;
         }
@@ -315,66 +385,119 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
     c.b = p.B;   // past the end; never dereferenced
 }
 
-template <typename T, int D>
-__device__ __forceinline__ int64_t tile_offset(const KParams& p, const Cursor& c, int32_t page) {
-    const int64_t slot0 = (c.tile % p.tiles_per_page) * kTile;
-    return (((int64_t)page * p.H + c.h) * p.P + slot0) * D;
+// Worker that owns flattened tile x: the inverse of begin(w) = floor(w T / W).
+__device__ __forceinline__ int64_t worker_of(int64_t x, int64_t T, int W) {
+    return ((x + 1) * W - 1) / T;
 }
 
-__device__ __forceinline__ int32_t tile_page(const KParams& p, const Cursor& c) {
-    return __ldg(p.tables + (int64_t)c.b * p.max_pages + c.tile / p.tiles_per_page);
+// Combine the partials of lane `lane_id`, deposited by workers w_lo..w_hi
+// (those owning at least one tile) in slots lane_id + w, into out.  One warp:
+// lane j takes partials j, j + 32, ... for the maximum and the weights
+// 2^(m_w - M); the weighted sum of the o vectors then runs 32 partials at a
+// time with each weight broadcast by shuffle, so the loads of consecutive
+// partials are independent.  Partials are read from L2 (other SMs wrote them
+// during this kernel).
+template <int D, int DPL>
+__device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, int64_t w_lo,
+                                           int64_t w_hi, int64_t T_all, int lane) {
+    auto owns_tiles = [&](int64_t w) { return (w * T_all) / p.W != ((w + 1) * T_all) / p.W; };
+    const int cnt = (int)(w_hi - w_lo + 1);
+    const int64_t slot0 = lane_id + w_lo;
+    float M = -INFINITY;
+    for (int j = lane; j < cnt; j += 32)
+        if (owns_tiles(w_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[slot0 + j]).x);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    float acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+    const bool has_features = lane * DPL < D;
+    for (int base = 0; base < cnt; base += 32) {
+        float wgt = 0.f;
+        if (base + lane < cnt && owns_tiles(w_lo + base + lane)) {
+            const float2 ml = __ldcg(&p.part_ml[slot0 + base + lane]);
+            wgt = exp2f(ml.x - M);
+            L = fmaf(ml.y, wgt, L);
+        }
+        const int nj = cnt - base < 32 ? cnt - base : 32;
+#pragma unroll 8
+        for (int j = 0; j < nj; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wgt, j);
+            if (has_features && wj != 0.f) {
+                const float* op = p.part_o + (slot0 + base + j) * D + lane * DPL;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc[i] = fmaf(wj, __ldcg(op + i), acc[i]);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (!has_features) return;
+    const float inv = 1.f / L;
+    float* out = p.out + lane_id * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kSplitWarps * 32)
+__global__ void __launch_bounds__(Geo<T, D>::WARPS * 32, 1)
 split_decode_kernel(const KParams p) {
     using G = Geo<T, D>;
     using VT = typename VecBits<G::VBYTES>::type;
+    constexpr int NV = G::VEC / 2;   // float pairs per lane vector
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t w = (int64_t)blockIdx.x * kSplitWarps + warp;
+    const int64_t w = (int64_t)blockIdx.x * G::WARPS + warp;
     if (w >= p.W) return;
 
-    // this worker's tiles: [begin, end) of the flattened sequence
-    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
-    const int64_t begin = (w * T_all) / p.W;
-    const int64_t end = ((w + 1) * T_all) / p.W;
-    const int64_t n_work = end - begin;
-    if (n_work <= 0) return;
-
     unsigned char* ring = smem + warp * G::WARP_SMEM;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSplitWarps * G::WARP_SMEM) + warp * G::STAGES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::WARPS * G::WARP_SMEM) + warp * G::STAGES;
+    int32_t* stage_page = reinterpret_cast<int32_t*>(smem + G::WARPS * (G::WARP_SMEM + G::STAGES * 8)) +
+                          warp * G::STAGES;
     if (lane == 0) {
         for (int s = 0; s < G::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
     __syncwarp();
+    const uint64_t policy = l2_stream_policy();
+
+    pdl_wait_primary();   // the plan kernel's prefix, worker table and counters
+
+    // this worker's tiles: [begin, end) of the flattened sequence
+    const int64_t T_all = (int64_t)p.H * __ldg(p.req_prefix + p.B);
+    const int64_t begin = (w * T_all) / p.W;
+    const int64_t end = ((w + 1) * T_all) / p.W;
+    const int n_work = (int)(end - begin);
+    if (n_work <= 0) return;
 
     Cursor cur;
     {
-        const int b0 = p.seq_lens == nullptr ? 0 : __ldg(p.worker_req + w);
-        const int64_t pre = req_prefix_at(p, b0);
+        const int b0 = __ldg(p.worker_req + w);
+        const int64_t pre = __ldg(p.req_prefix + b0);
         cur.b = b0;
-        cur.n = req_prefix_at(p, b0 + 1) - pre;
+        cur.n = (int)(__ldg(p.req_prefix + b0 + 1) - pre);
         cur.first = (int64_t)p.H * pre;
         const int64_t local = begin - cur.first;
         cur.h = (int)(local / cur.n);
-        cur.tile = local % cur.n;
+        cur.tile = (int)(local % cur.n);
+        cur.page_idx = cur.tile / p.tiles_per_page;
+        cur.slot0 = (cur.tile - cur.page_idx * p.tiles_per_page) * kTile;
     }
     Cursor prod = cur;
-    const uint64_t policy = l2_evict_first_policy();
 
     // Producer step (lane 0): stage tile `prod` into stage s.
     auto issue = [&](int s) {
         if (lane != 0) return;
-        const int32_t page = tile_page(p, prod);
+        const int32_t page = __ldg(p.tables + (int64_t)prod.b * p.max_pages + prod.page_idx);
+        stage_page[s] = page;
         if (page < 0 || page >= p.n_pages) {
             atomicOr(p.err, PKV_DEVERR_PAGE_ID);
             mbar_arrive(&bars[s]);
             return;
         }
-        const int64_t off = tile_offset<T, D>(p, prod, page);
+        const int64_t off = (((int64_t)page * p.H + prod.h) * p.P + prod.slot0) * D;
         unsigned char* dst = ring + s * G::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[s], G::STAGE_BYTES);
         bulk_copy_g2s(dst, static_cast<const T*>(p.k_pages) + off, G::TILE_BYTES, &bars[s], policy);
@@ -382,7 +505,7 @@ split_decode_kernel(const KParams p) {
                       &bars[s], policy);
     };
 
-    const int prologue = n_work < G::STAGES ? (int)n_work : G::STAGES;
+    const int prologue = n_work < G::STAGES ? n_work : G::STAGES;
     for (int s = 0; s < prologue; ++s) {
         issue(s);
         cursor_advance(prod, p);
@@ -390,25 +513,28 @@ split_decode_kernel(const KParams p) {
 
     const int rg = lane / G::TPR;             // row group of this lane
     const int col = (lane % G::TPR) * G::VEC; // first feature of this lane
+    const int it_own = (lane % G::TPR) >> 1;  // warp step of the row this lane scores
+    const int row_own = it_own * G::RPI + rg;
 
-    float qv[G::VEC];
-    float o[G::VEC];
+    float2 qv[NV];
+    float2 o[NV];
     float m = -INFINITY, l = 0.f;
-    int64_t piece_first = 0, t_b = 0;
+    int piece_first = 0, t_b = 0;
+    int s = 0;
+    uint32_t parity = 0;
 
-    for (int64_t k = 0; k < n_work; ++k) {
-        const int s = (int)(k % G::STAGES);
-        const uint32_t parity = (uint32_t)((k / G::STAGES) & 1);
+    for (int k = 0; k < n_work; ++k) {
         const int64_t lane_id = (int64_t)cur.b * p.H + cur.h;
 
         if (k == 0 || cur.tile == 0) {   // a new lane piece starts
             piece_first = cur.tile;
-            t_b = seq_len_at(p, cur.b);
-            const float* qp = p.q + lane_id * D + col;
+            t_b = (int)seq_len_at(p, cur.b);
+            const float2* qp = reinterpret_cast<const float2*>(p.q + lane_id * D + col);
 #pragma unroll
-            for (int v = 0; v < G::VEC; ++v) {
-                qv[v] = qp[v] * p.qscale;
-                o[v] = 0.f;
+            for (int v = 0; v < NV; ++v) {
+                const float2 qq = qp[v];
+                qv[v] = make_float2(qq.x * p.qscale, qq.y * p.qscale);
+                o[v] = make_float2(0.f, 0.f);
             }
             m = -INFINITY;
             l = 0.f;
@@ -417,19 +543,26 @@ split_decode_kernel(const KParams p) {
         if (!mbar_wait_bounded(&bars[s], parity, kWaitLimitNs)) {
             if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
             // let the copies already issued land before the shared memory goes away
-            const int64_t last = (k + G::STAGES - 1 < n_work - 1) ? k + G::STAGES - 1 : n_work - 1;
-            for (int64_t j = k + 1; j <= last; ++j)
-                mbar_wait_bounded(&bars[j % G::STAGES], (uint32_t)((j / G::STAGES) & 1), kWaitLimitNs);
+            const int last = (k + G::STAGES - 1 < n_work - 1) ? k + G::STAGES - 1 : n_work - 1;
+            int s2 = s;
+            uint32_t par2 = parity;
+            for (int j = k + 1; j <= last; ++j) {
+                if (++s2 == G::STAGES) {
+                    s2 = 0;
+                    par2 ^= 1u;
+                }
+                mbar_wait_bounded(&bars[s2], par2, kWaitLimitNs);
+            }
             return;
         }
 
         T* Ks = reinterpret_cast<T*>(ring + s * G::STAGE_BYTES);
         T* Vs = Ks + kTile * D;
-        const int32_t page = tile_page(p, cur);
+        const int32_t page = stage_page[s];
         const bool page_ok = page >= 0 && page < p.n_pages;
         const bool last_tile = cur.tile == cur.n - 1;
-        const int64_t rem = t_b - cur.tile * kTile;
-        const int rows = !page_ok ? 0 : (rem < kTile ? (int)rem : kTile);
+        const int rem = t_b - cur.tile * kTile;
+        const int rows = !page_ok ? 0 : (rem < kTile ? rem : kTile);
 
         if (last_tile && page_ok) {
             // fused append: row t_b - 1 comes from k_new / v_new, into the tile and the page
@@ -440,7 +573,8 @@ split_decode_kernel(const KParams p) {
                 const VT vb = *reinterpret_cast<const VT*>(static_cast<const T*>(p.v_new) + src);
                 *reinterpret_cast<VT*>(Ks + r * D + col) = kb;
                 *reinterpret_cast<VT*>(Vs + r * D + col) = vb;
-                const int64_t dst = tile_offset<T, D>(p, cur, page) + (int64_t)r * D + col;
+                const int64_t dst =
+                    (((int64_t)page * p.H + cur.h) * p.P + cur.slot0 + r) * D + col;
                 *reinterpret_cast<VT*>(static_cast<T*>(p.k_pages) + dst) = kb;
                 *reinterpret_cast<VT*>(static_cast<T*>(p.v_pages) + dst) = vb;
             }
@@ -448,52 +582,60 @@ split_decode_kernel(const KParams p) {
         }
 
         if (rows > 0) {
+            // partial dot products of this lane's features for its ITERS rows
             float sc[G::ITERS];
 #pragma unroll
             for (int it = 0; it < G::ITERS; ++it) {
                 const int row = it * G::RPI + rg;
-                float acc = 0.f;
+                float2 acc = make_float2(0.f, 0.f);
                 if (row < kTile) {
-                    float kf[G::VEC];
+                    float2 kf[NV];
                     const VT kb = *reinterpret_cast<const VT*>(Ks + row * D + col);
-                    Storage<T>::template to_float<G::VEC>(&kb, kf);
+                    Storage<T>::template to_float2<G::VEC>(&kb, kf);
 #pragma unroll
-                    for (int v = 0; v < G::VEC; ++v) acc = fmaf(qv[v], kf[v], acc);
+                    for (int v = 0; v < NV; ++v) acc = __ffma2_rn(qv[v], kf[v], acc);
                 }
-                sc[it] = acc;
+                sc[it] = acc.x + acc.y;
             }
+            // transposed reduction over the TPR lanes of a row: each round halves
+            // the values a lane keeps, the last round adds lane pairs
 #pragma unroll
-            for (int it = 0; it < G::ITERS; ++it) {
+            for (int r = 0; r < G::HALVING_ROUNDS; ++r) {
+                const int half = G::ITERS >> (r + 1);   // lane offset of this round = 2 * half
+                const bool upper = (lane & (2 * half)) != 0;
 #pragma unroll
-                for (int off = G::TPR / 2; off >= 1; off >>= 1)
-                    sc[it] += __shfl_xor_sync(0xffffffffu, sc[it], off);
+                for (int i = 0; i < half; ++i) {
+                    const float send = upper ? sc[i] : sc[i + half];
+                    const float keep = upper ? sc[i + half] : sc[i];
+                    sc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * half);
+                }
             }
-            float tmax = -INFINITY;
+            if (G::TPR >= 2) sc[0] += __shfl_xor_sync(0xffffffffu, sc[0], 1);
+            const float s_own = row_own < rows ? sc[0] : -INFINITY;
+            float tmax = s_own;
 #pragma unroll
-            for (int it = 0; it < G::ITERS; ++it) {
-                const int row = it * G::RPI + rg;
-                if (row >= rows) sc[it] = -INFINITY;
-                tmax = fmaxf(tmax, sc[it]);
-            }
-#pragma unroll
-            for (int off = G::TPR; off < 32; off <<= 1)
+            for (int off = 16; off >= 1; off >>= 1)
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
             const float m_new = fmaxf(m, tmax);
             const float alpha = exp2f(m - m_new);
-            l *= alpha;
+            const float p_own = exp2f(s_own - m_new);
+            l = fmaf(l, alpha, p_own);
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int v = 0; v < G::VEC; ++v) o[v] *= alpha;
+            for (int v = 0; v < NV; ++v) o[v] = __fmul2_rn(o[v], a2);
 #pragma unroll
             for (int it = 0; it < G::ITERS; ++it) {
                 const int row = it * G::RPI + rg;
+                const float pw = G::TPR >= 2
+                    ? __shfl_sync(0xffffffffu, p_own, (lane & ~(G::TPR - 1)) | (it << 1))
+                    : p_own;
                 if (row < rows) {
-                    const float pw = exp2f(sc[it] - m_new);
-                    l += pw;
-                    float vf[G::VEC];
+                    float2 vf[NV];
                     const VT vb = *reinterpret_cast<const VT*>(Vs + row * D + col);
-                    Storage<T>::template to_float<G::VEC>(&vb, vf);
+                    Storage<T>::template to_float2<G::VEC>(&vb, vf);
+                    const float2 p2 = make_float2(pw, pw);
 #pragma unroll
-                    for (int v = 0; v < G::VEC; ++v) o[v] = fmaf(pw, vf[v], o[v]);
+                    for (int v = 0; v < NV; ++v) o[v] = __ffma2_rn(p2, vf[v], o[v]);
                 }
             }
             m = m_new;
@@ -506,96 +648,69 @@ split_decode_kernel(const KParams p) {
             issue(s);
             cursor_advance(prod, p);
         }
+        if (++s == G::STAGES) {
+            s = 0;
+            parity ^= 1u;
+        }
 
         if (last_tile || k == n_work - 1) {
-            // close the lane piece: sum the row groups
+            // close the lane piece: sum the lanes' shares of l, and o over row groups
             float lt = l;
 #pragma unroll
-            for (int off = G::TPR; off < 32; off <<= 1) {
-                lt += __shfl_xor_sync(0xffffffffu, lt, off);
+            for (int off = 16; off >= 1; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+            lt *= 1.f / G::DUP;
 #pragma unroll
-                for (int v = 0; v < G::VEC; ++v) o[v] += __shfl_xor_sync(0xffffffffu, o[v], off);
+            for (int off = G::TPR; off < 32; off <<= 1) {
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    o[v].x += __shfl_xor_sync(0xffffffffu, o[v].x, off);
+                    o[v].y += __shfl_xor_sync(0xffffffffu, o[v].y, off);
+                }
             }
             if (piece_first == 0 && last_tile) {
                 if (lane < G::TPR) {
                     const float inv = 1.f / lt;
-                    float* op = p.out + lane_id * D + col;
+                    float2* op = reinterpret_cast<float2*>(p.out + lane_id * D + col);
 #pragma unroll
-                    for (int v = 0; v < G::VEC; ++v) op[v] = o[v] * inv;
+                    for (int v = 0; v < NV; ++v) op[v] = make_float2(o[v].x * inv, o[v].y * inv);
                 }
             } else {
+                // deposit the partial; the last of the lane's workers to arrive merges
                 const int64_t slot = lane_id + w;
                 if (lane < G::TPR) {
-                    float* op = p.part_o + slot * D + col;
+                    float2* op = reinterpret_cast<float2*>(p.part_o + slot * D + col);
 #pragma unroll
-                    for (int v = 0; v < G::VEC; ++v) op[v] = o[v];
+                    for (int v = 0; v < NV; ++v) op[v] = o[v];
                 }
                 if (lane == 0) p.part_ml[slot] = make_float2(m, lt);
+                __threadfence();
+                __syncwarp();
+                const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // lane's first tile
+                const int64_t w_lo = worker_of(A, T_all, p.W);
+                const int64_t w_hi = worker_of(A + cur.n - 1, T_all, p.W);
+                int need;
+                if (T_all >= p.W) {
+                    need = (int)(w_hi - w_lo + 1);   // no worker is empty
+                } else {
+                    int c = 0;
+                    for (int64_t x = w_lo + lane; x <= w_hi; x += 32)
+                        c += (x * T_all) / p.W != ((x + 1) * T_all) / p.W;
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                    need = c;
+                }
+                int arrived = 0;
+                if (lane == 0) arrived = atomicAdd(&p.lane_cnt[lane_id], 1) + 1;
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == need) {
+                    __threadfence();
+                    merge_lane<D, G::DPL>(p, lane_id, w_lo, w_hi, T_all, lane);
+                }
+                __syncwarp();
             }
         }
         cursor_advance(cur, p);
     }
-}
-
-// ---------------------------------------------------------- merge kernel --
-
-constexpr int kMergeWarps = 8;
-
-// One warp per lane.  Lane (b, h) covers flattened tiles [A, A + n); tile x
-// belongs to worker floor(((x + 1) W - 1) / T) (the inverse of
-// begin(w) = floor(w T / W)).  A lane covered by one worker is already final.
-// When T < W some workers own no tile; those between the lane's first and last
-// worker wrote nothing and are skipped.  Partial slots lane + w are disjoint
-// across lanes because the first worker of lane i + 1 is at least the last
-// worker of lane i.
-template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const KParams p) {
-    constexpr int DPL = D >= 32 ? D / 32 : 1;   // features per lane
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t lane_id = (int64_t)blockIdx.x * kMergeWarps + warp;
-    if (lane_id >= (int64_t)p.B * p.H) return;
-    const int b = (int)(lane_id / p.H), h = (int)(lane_id % p.H);
-    const int64_t pre = req_prefix_at(p, b);
-    const int64_t n = req_prefix_at(p, b + 1) - pre;
-    if (n <= 0) return;
-    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
-    const int64_t A = (int64_t)p.H * pre + (int64_t)h * n;
-    const int64_t w_lo = ((A + 1) * p.W - 1) / T_all;
-    const int64_t w_hi = ((A + n) * p.W - 1) / T_all;
-    if (w_lo == w_hi) return;
-
-    auto owns_tiles = [&](int64_t w) { return (w * T_all) / p.W != ((w + 1) * T_all) / p.W; };
-    float M = -INFINITY;
-    for (int64_t w = w_lo + lane; w <= w_hi; w += 32)
-        if (owns_tiles(w)) M = fmaxf(M, p.part_ml[lane_id + w].x);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
-    float L = 0.f;
-    for (int64_t w = w_lo + lane; w <= w_hi; w += 32) {
-        if (!owns_tiles(w)) continue;
-        const float2 ml = p.part_ml[lane_id + w];
-        L += ml.y * exp2f(ml.x - M);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-
-    if (lane * DPL >= D) return;
-    float acc[DPL];
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    for (int64_t w = w_lo; w <= w_hi; ++w) {
-        if (!owns_tiles(w)) continue;
-        const int64_t slot = lane_id + w;
-        const float sc = exp2f(p.part_ml[slot].x - M);
-        const float* op = p.part_o + slot * D + lane * DPL;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(sc, op[i], acc[i]);
-    }
-    const float inv = 1.f / L;
-    float* out = p.out + lane_id * D + lane * DPL;
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
 
 // ------------------------------------------------------------------ host --
@@ -609,6 +724,8 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers) {
     off = align_up(off + sizeof(int64_t) * ((size_t)B + 1), 256);
     L.worker_req = off;
     off = align_up(off + sizeof(int32_t) * (size_t)workers, 256);
+    L.lane_cnt = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)B * H, 256);
     const size_t slots = (size_t)B * H + (size_t)workers;
     L.part_ml = off;
     off = align_up(off + sizeof(float2) * slots, 256);
@@ -624,11 +741,8 @@ int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len) {
 }
 
 template <typename T, int D>
-static int split_smem() { return Geo<T, D>::CTA_SMEM; }
-
-template <typename T, int D>
 static cudaError_t prepare_split() {
-    static bool done = false;   // per instantiation; attribute is per device-function
+    static bool done = false;   // per instantiation
     if (done) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<T, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -642,29 +756,33 @@ static int resident_workers_t(int num_sms) {
     if (prepare_split<T, D>() != cudaSuccess) return 0;
     int blocks = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_kernel<T, D>,
-                                                      kSplitWarps * 32, Geo<T, D>::CTA_SMEM) !=
+                                                      Geo<T, D>::WARPS * 32, Geo<T, D>::CTA_SMEM) !=
         cudaSuccess)
         return 0;
-    return blocks * num_sms * kSplitWarps;
+    return blocks * num_sms * Geo<T, D>::WARPS;
 }
 
 template <typename T, int D>
 static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream) {
+    using G = Geo<T, D>;
     cudaError_t e = prepare_split<T, D>();
     if (e != cudaSuccess) return e;
-    if (a.seq_lens != nullptr) {
-        plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    const int grid = (p.W + kSplitWarps - 1) / kSplitWarps;
-    if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
-    split_decode_kernel<T, D><<<grid, kSplitWarps * 32, Geo<T, D>::CTA_SMEM, stream>>>(p);
+    plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((p.W + G::WARPS - 1) / G::WARPS));
+    cfg.blockDim = dim3(G::WARPS * 32);
+    cfg.dynamicSmemBytes = G::CTA_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D>, p)) != cudaSuccess) return e;
     if (a.ev_after && (e = cudaEventRecord(a.ev_after, stream)) != cudaSuccess) return e;
-    const int64_t lanes = (int64_t)p.B * p.H;
-    const int mgrid = (int)((lanes + kMergeWarps - 1) / kMergeWarps);
-    merge_kernel<D><<<mgrid, kMergeWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 #define PKV_FOR_EACH_D(X, T) X(T, 2) X(T, 4) X(T, 8) X(T, 16) X(T, 32) X(T, 64) X(T, 128)
@@ -701,7 +819,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.max_pages = a.max_pages;
     p.seq_lens = a.seq_lens;
     p.single_t = a.single_t;
-    p.single_tiles = (a.single_t + kTile - 1) / kTile;
     p.max_seq_len = a.max_seq_len;
     p.B = a.B;
     p.H = a.H;
@@ -713,6 +830,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     p.req_prefix = reinterpret_cast<int64_t*>(ws + L.req_prefix);
     p.worker_req = reinterpret_cast<int32_t*>(ws + L.worker_req);
+    p.lane_cnt = reinterpret_cast<int32_t*>(ws + L.lane_cnt);
     p.part_ml = reinterpret_cast<float2*>(ws + L.part_ml);
     p.part_o = reinterpret_cast<float*>(ws + L.part_o);
     p.W = a.workers;

@@ -11,8 +11,13 @@ struct pkv_pool;
 
 namespace pkv {
 
+// Tuning constants of the split kernel (compile-time; overridable with -D for sweeps).
+#ifndef PKV_SPLIT_WARPS
+#define PKV_SPLIT_WARPS 8          // warps per CTA (one CTA per SM); each warp is one worker
+#endif
+
 constexpr int kTile = 16;          // key rows staged and processed as one unit
-constexpr int kSplitWarps = 4;     // warps per CTA of the split kernel; each warp is one worker
+constexpr int kSplitWarps = PKV_SPLIT_WARPS;
 
 // One launch of the decode path for one layer.
 struct DecodeArgs {
@@ -42,6 +47,7 @@ struct DecodeArgs {
 struct WorkspaceLayout {
     size_t req_prefix;   // int64 [B + 1]: tiles-per-lane prefix over requests
     size_t worker_req;   // int32 [workers]: request holding each worker's first tile
+    size_t lane_cnt;     // int32 [B*H]: partials deposited per lane (zeroed by the plan kernel)
     size_t part_ml;      // float2 [B*H + workers]: (running max in log2 units, sum)
     size_t part_o;       // float [B*H + workers][D]: unnormalised partial outputs
     size_t total;
@@ -60,7 +66,7 @@ int resident_workers(int dtype, int D, int num_sms);
 // True if the kernels implement (dtype, D).
 bool decode_supported(int dtype, int D);
 
-// Enqueue plan (batched only), split and merge kernels on `stream`.
+// Enqueue the plan and split kernels on `stream`.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Record a failed call in the thread's last-error message; returns `status`.
