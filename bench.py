@@ -368,6 +368,153 @@ def run_gpu(args):
     return line, w
 
 
+# ------------------------------------------- the GPU arm, one request --
+
+def token_bytes(w, t: int) -> int:
+    """Algorithmic bytes of one token at retained length t through every layer."""
+    es = w.elem_bytes
+    per_layer = ((t - 1) * w.H * w.D * 2 * es + w.H * w.D * es * 2 * 2 + w.H * w.D * 4 * 2
+                 + ((t + w.P - 1) // w.P) * 4)
+    return w.layers * per_layer
+
+
+def run_gpu_serial(args):
+    """Single request through the transactional API: history built by serial
+    begin / append x layers / commit up to t - 1; each timed step is one token at
+    retained length t: begin_token, append_and_attend on every layer, abort_token
+    (so every step sees the same t; commit is the same O(1) host update)."""
+    import torch
+    import paged_kv_cache_decode_gb300 as pkv
+    import synth
+    from synth import KHIST, VHIST, Q, F32
+    from synth.device import to_device
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    rank, world = dist_init("nccl")
+    w = make_workload(args.workload, rank)
+    t = int(w.seq_lens[0])
+    dt = "f32" if w.elem_bytes == 4 else "bf16"
+    pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dt, w.max_context, w.seed)
+    req = pool.request()
+    out = torch.empty((w.H, w.D), dtype=torch.float32, device="cuda")
+
+    def layer_inputs(pos):
+        return [(to_device(synth.lane_rows(w.seed, Q, l, 0, w.H, pos, w.D, F32)),
+                 to_device(synth.lane_rows(w.seed, KHIST, l, 0, w.H, pos, w.D, w.dtype)),
+                 to_device(synth.lane_rows(w.seed, VHIST, l, 0, w.H, pos, w.D, w.dtype)))
+                for l in range(w.layers)]
+
+    for pos in range(t - 1):                      # history, untimed
+        req.begin_token()
+        for l, (q, k, v) in enumerate(layer_inputs(pos)):
+            req.append_and_attend(l, q, k, v, out)
+        req.commit_token()
+    torch.cuda.synchronize()
+    assert req.length == t - 1 and pool.check_device_status() == 0
+    inputs = layer_inputs(t - 1)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        req.begin_token()
+        for l, (q, k, v) in enumerate(inputs):
+            req.append_and_attend(l, q, k, v, out)
+        req.abort_token()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(K):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    tok_ms = max_over_ranks(start.elapsed_time(end) / K, "cuda")
+    # split kernel of one layer, alone
+    evb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    eva = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        pool.set_timing_events(evb[i], eva[i])
+        req.begin_token()
+        req.append_and_attend(0, *inputs[0], out)
+        req.abort_token()
+    torch.cuda.synchronize()
+    pool.set_timing_events(None, None)
+    kernel_ms = float(np.mean([b.elapsed_time(a) for b, a in zip(evb, eva)]))
+    # end to end: every layer's q, k, v copied in from pinned host memory, out copied back
+    hin = [tuple(x.cpu().pin_memory() for x in layer) for layer in inputs]
+    hout = torch.empty((w.layers, w.H, w.D), dtype=torch.float32).pin_memory()
+    outs = torch.empty((w.layers, w.H, w.D), dtype=torch.float32, device="cuda")
+
+    def e2e_step():
+        req.begin_token()
+        for l, ((hq, hk, hv), (q, k, v)) in enumerate(zip(hin, inputs)):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            req.append_and_attend(l, q, k, v, outs[l])
+        hout.copy_(outs, non_blocking=True)
+        req.abort_token()
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, "cuda")
+    assert pool.check_device_status() == 0
+    if sampler:
+        sampler.stop()
+    alg = token_bytes(w, t)
+    layer_alg = alg // w.layers
+    h2d = sum(x.numel() * x.element_size() for layer in hin for x in layer)
+    line = None
+    if rank == 0:
+        peak, peak_kind = measured_peak_hbm()
+        achieved = layer_alg / (kernel_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(world * alg / (tok_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(tok_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.elem_bytes == 2 else "f32", "data": "synthetic",
+            "config": {"workload": (f"single request: {w.layers} layers, H={w.H}, d_h={w.D}, "
+                                    f"retained length t={t}, pool of {w.pool_pages} shuffled pages; "
+                                    "a step is one token through every layer (transactional API)"),
+                       "name": w.name, "layers": w.layers, "heads": w.H, "head_dim": w.D,
+                       "page_size": w.P, "seq_len": t, "alg_bytes_per_step": alg,
+                       "l2": f"{layer_alg / 1e6:.1f} MB per layer, {alg / 1e6:.0f} MB per token, no flush: "
+                             + ("every layer's history fits in the 129 MB L2 between tokens"
+                                if alg <= 129e6 else "larger than the 129 MB L2"),
+                       "parallelism": f"replicas x{world}"},
+            "us_per_token": round(tok_ms * 1e3, 2),
+            "tokens_per_s": round(world / (tok_ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": f"split_decode_kernel<{'bf16' if w.elem_bytes == 2 else 'f32'},{w.D}>",
+                         "kernel_ms": round(kernel_ms, 5), "peak_kind": peak_kind + " (hbm_gbs copy)",
+                         "note": "one layer's split kernel; latency-bound at this size"},
+            "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": hout.numel() * 4},
+            "gpu_launches": K * w.layers * 2,
+            "clocks": sampler.summary(t0, t1) if sampler else None,
+        }
+    pool.close()
+    return line, w
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(w, requests, threads=0):
@@ -484,7 +631,7 @@ def main(argv=None):
     if args.impl == "reference":
         line, _ = run_reference(args)
     else:
-        line, w = run_gpu(args)
+        line, w = (run_gpu_serial if args.workload.startswith("single") else run_gpu)(args)
         rank, world, _ = dist_env()
         if line is not None and world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)

@@ -257,7 +257,8 @@ struct KParams {
     float* out;
     int64_t* req_prefix;        // [B + 1] tiles-per-lane prefix (plan kernel)
     int32_t* worker_req;        // [W] request of each worker's first tile (plan kernel)
-    int32_t* lane_cnt;          // [B * H] partials deposited per split lane (zeroed by plan)
+    unsigned long long* lane_cnt;  // [B * H] partials deposited per split lane
+    uint32_t epoch;             // 0: counters zeroed by the plan kernel; else the call's epoch
     float2* part_ml;
     float* part_o;
     int W;
@@ -266,6 +267,13 @@ struct KParams {
 
 __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
+}
+
+// Tiles-per-lane prefix over requests: closed form for a single request (no
+// dependence on the plan kernel), else the plan kernel's table.
+__device__ __forceinline__ int64_t req_prefix_at(const KParams& p, int b) {
+    if (p.seq_lens == nullptr) return b == 0 ? 0 : (p.single_t + kTile - 1) / kTile;
+    return __ldg(p.req_prefix + b);
 }
 
 // ----------------------------------------------------------- plan kernel --
@@ -283,7 +291,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const bool in_smem = p.B <= kPlanSmemRequests;
     if (tid == 0) carry_s = 0;
-    for (int64_t i = tid; i < (int64_t)p.B * p.H; i += kPlanThreads) p.lane_cnt[i] = 0;
+    for (int64_t i = tid; i < (int64_t)p.B * p.H; i += kPlanThreads) p.lane_cnt[i] = 0ull;
     __syncthreads();
     for (int base = 0; base < p.B; base += kPlanThreads) {
         const int i = base + tid;
@@ -371,10 +379,10 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
     if (++c.h < p.H) return;
     c.h = 0;
     // next request with at least one tile
-    int64_t pre = __ldg(p.req_prefix + c.b + 1);
+    int64_t pre = req_prefix_at(p, c.b + 1);
     while (c.b + 1 < p.B) {
         ++c.b;
-        const int64_t nxt = __ldg(p.req_prefix + c.b + 1);
+        const int64_t nxt = req_prefix_at(p, c.b + 1);
         if (nxt > pre) {
             c.n = (int)(nxt - pre);
             c.first = (int64_t)p.H * pre;
@@ -424,10 +432,14 @@ __device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, in
 #pragma unroll 8
         for (int j = 0; j < nj; ++j) {
             const float wj = __shfl_sync(0xffffffffu, wgt, j);
-            if (has_features && wj != 0.f) {
+            if (has_features) {
+                // slots of workers that own no tile hold stale data: weight 0, value dropped
                 const float* op = p.part_o + (slot0 + base + j) * D + lane * DPL;
 #pragma unroll
-                for (int i = 0; i < DPL; ++i) acc[i] = fmaf(wj, __ldcg(op + i), acc[i]);
+                for (int i = 0; i < DPL; ++i) {
+                    const float v = __ldcg(op + i);
+                    acc[i] = wj != 0.f ? fmaf(wj, v, acc[i]) : acc[i];
+                }
             }
         }
     }
@@ -463,10 +475,18 @@ split_decode_kernel(const KParams p) {
     __syncwarp();
     const uint64_t policy = l2_stream_policy();
 
-    pdl_wait_primary();   // the plan kernel's prefix, worker table and counters
+    // The plan kernel's prefix and worker table are needed now for a batch.  A
+    // single request's partition is closed-form and its lane counters carry an
+    // epoch, so it runs without a plan kernel.
+    const bool batched = p.seq_lens != nullptr;
+    bool plan_seen = false;
+    if (batched) {
+        pdl_wait_primary();
+        plan_seen = true;
+    }
 
     // this worker's tiles: [begin, end) of the flattened sequence
-    const int64_t T_all = (int64_t)p.H * __ldg(p.req_prefix + p.B);
+    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
     const int64_t begin = (w * T_all) / p.W;
     const int64_t end = ((w + 1) * T_all) / p.W;
     const int n_work = (int)(end - begin);
@@ -474,10 +494,10 @@ split_decode_kernel(const KParams p) {
 
     Cursor cur;
     {
-        const int b0 = __ldg(p.worker_req + w);
-        const int64_t pre = __ldg(p.req_prefix + b0);
+        const int b0 = batched ? __ldg(p.worker_req + w) : 0;
+        const int64_t pre = req_prefix_at(p, b0);
         cur.b = b0;
-        cur.n = (int)(__ldg(p.req_prefix + b0 + 1) - pre);
+        cur.n = (int)(req_prefix_at(p, b0 + 1) - pre);
         cur.first = (int64_t)p.H * pre;
         const int64_t local = begin - cur.first;
         cur.h = (int)(local / cur.n);
@@ -700,7 +720,21 @@ split_decode_kernel(const KParams p) {
                     need = c;
                 }
                 int arrived = 0;
-                if (lane == 0) arrived = atomicAdd(&p.lane_cnt[lane_id], 1) + 1;
+                if (p.epoch == 0) {
+                    // counters zeroed by the plan kernel of this call
+                    if (!plan_seen) {
+                        pdl_wait_primary();
+                        plan_seen = true;
+                    }
+                    if (lane == 0) arrived = (int)atomicAdd(&p.lane_cnt[lane_id], 1ull) + 1;
+                } else if (lane == 0) {
+                    // counter = epoch << 32 | count, epochs increasing from call to
+                    // call: the max resets a counter left by an earlier call (never
+                    // one of this call, whose value is at least epoch << 32), then add
+                    unsigned long long* c = &p.lane_cnt[lane_id];
+                    atomicMax(c, (unsigned long long)p.epoch << 32);
+                    arrived = (int)((atomicAdd(c, 1ull) & 0xffffffffull) + 1);
+                }
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
                     __threadfence();
@@ -720,12 +754,14 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 WorkspaceLayout workspace_layout(int B, int H, int D, int workers) {
     WorkspaceLayout L{};
     size_t off = 0;
+    // lane counters first: their place must not depend on the worker count,
+    // because epoch-tagged counters persist from one call to the next
+    L.lane_cnt = off;
+    off = align_up(off + sizeof(unsigned long long) * (size_t)B * H, 256);
     L.req_prefix = off;
     off = align_up(off + sizeof(int64_t) * ((size_t)B + 1), 256);
     L.worker_req = off;
     off = align_up(off + sizeof(int32_t) * (size_t)workers, 256);
-    L.lane_cnt = off;
-    off = align_up(off + sizeof(int32_t) * (size_t)B * H, 256);
     const size_t slots = (size_t)B * H + (size_t)workers;
     L.part_ml = off;
     off = align_up(off + sizeof(float2) * slots, 256);
@@ -735,9 +771,14 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers) {
     return L;
 }
 
+#ifndef PKV_MIN_TILES_PER_WORKER
+#define PKV_MIN_TILES_PER_WORKER 4   // below this much work a worker's fixed costs dominate
+#endif
+
 int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len) {
     const int64_t tiles = (int64_t)B * H * ((max_seq_len + kTile - 1) / kTile);
-    return (int)(tiles < pool_workers ? (tiles < 1 ? 1 : tiles) : pool_workers);
+    const int64_t want = (tiles + PKV_MIN_TILES_PER_WORKER - 1) / PKV_MIN_TILES_PER_WORKER;
+    return (int)(want < pool_workers ? (want < 1 ? 1 : want) : pool_workers);
 }
 
 template <typename T, int D>
@@ -767,19 +808,23 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     using G = Geo<T, D>;
     cudaError_t e = prepare_split<T, D>();
     if (e != cudaSuccess) return e;
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (p.epoch == 0) {   // a single request with epoch counters needs no plan
+        plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)((p.W + G::WARPS - 1) / G::WARPS));
     cfg.blockDim = dim3(G::WARPS * 32);
     cfg.dynamicSmemBytes = G::CTA_SMEM;
     cfg.stream = stream;
+    // dependent launch only behind this call's own plan kernel; with epoch
+    // counters the kernel follows whatever came before in plain stream order
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.epoch == 0 ? 1 : 0;
     if ((e = cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D>, p)) != cudaSuccess) return e;
     if (a.ev_after && (e = cudaEventRecord(a.ev_after, stream)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -830,7 +875,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     p.req_prefix = reinterpret_cast<int64_t*>(ws + L.req_prefix);
     p.worker_req = reinterpret_cast<int32_t*>(ws + L.worker_req);
-    p.lane_cnt = reinterpret_cast<int32_t*>(ws + L.lane_cnt);
+    p.lane_cnt = reinterpret_cast<unsigned long long*>(ws + L.lane_cnt);
+    p.epoch = a.epoch;
     p.part_ml = reinterpret_cast<float2*>(ws + L.part_ml);
     p.part_o = reinterpret_cast<float*>(ws + L.part_o);
     p.W = a.workers;

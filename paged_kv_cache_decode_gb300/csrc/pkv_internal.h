@@ -41,13 +41,15 @@ struct DecodeArgs {
     unsigned* dev_error;
     cudaEvent_t ev_before;   // optional: recorded around the split kernel
     cudaEvent_t ev_after;
+    uint32_t epoch;          // single request only: nonzero call epoch of the lane counters
+                             // (no plan kernel; the workspace's counters started at zero)
 };
 
 // Byte offsets of the scratch areas inside a workspace.
 struct WorkspaceLayout {
     size_t req_prefix;   // int64 [B + 1]: tiles-per-lane prefix over requests
     size_t worker_req;   // int32 [workers]: request holding each worker's first tile
-    size_t lane_cnt;     // int32 [B*H]: partials deposited per lane (zeroed by the plan kernel)
+    size_t lane_cnt;     // uint64 [B*H]: partials deposited per lane (plan-zeroed or epoch-tagged)
     size_t part_ml;      // float2 [B*H + workers]: (running max in log2 units, sum)
     size_t part_o;       // float [B*H + workers][D]: unnormalised partial outputs
     size_t total;

@@ -90,6 +90,7 @@ struct pkv_request {
     void* dev_workspace = nullptr;
     size_t workspace_bytes = 0;
     int workspace_workers = 0;
+    uint32_t epoch = 0;                // calls made on dev_workspace (lane-counter epochs)
 };
 
 namespace {
@@ -291,6 +292,7 @@ int pkv_request_create(pkv_pool* p, pkv_request** out) {
             pkv::workspace_layout(1, p->heads, p->head_dim, r->workspace_workers).total;
         cudaError_t e = cudaMalloc(&r->dev_table, sizeof(int32_t) * (size_t)p->max_pages_per_request);
         if (e == cudaSuccess) e = cudaMalloc(&r->dev_workspace, r->workspace_bytes);
+        if (e == cudaSuccess) e = cudaMemset(r->dev_workspace, 0, r->workspace_bytes);
         if (e != cudaSuccess) {
             cudaFree(r->dev_table);
             cudaFree(r->dev_workspace);
@@ -441,8 +443,16 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
+    if (r->epoch == UINT32_MAX) {
+        // epochs must increase: after 2^32 - 1 calls start over from zeroed counters
+        cudaError_t z = cudaMemsetAsync(r->dev_workspace, 0, r->workspace_bytes, s);
+        if (z != cudaSuccess) return cuda_fail(z, "workspace reset");
+        r->epoch = 0;
+    }
+    a.epoch = r->epoch + 1;
     cudaError_t e = pkv::launch_decode(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    r->epoch = a.epoch;
     r->appended[(size_t)layer] = 1;
     ++r->appended_count;
     return ok();
