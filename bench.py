@@ -65,6 +65,9 @@ def describe(w) -> str:
     if w.name.startswith("batched"):
         return (f"batched decode: {w.B} requests, t ~ U[1,4096], H={w.H}, d_h={w.D}, {st}, "
                 f"pool of {w.pool_pages} shuffled pages")
+    if w.name.startswith("gqa"):
+        return (f"grouped-query decode: {w.B} requests, t ~ U[1,{w.max_context}], {w.H} KV heads x "
+                f"{w.group} query heads each, d_h={w.D}, {st}, pool of {w.pool_pages} shuffled pages")
     if w.name == "ragged":
         return (f"ragged fragmented pool: {w.B} requests, lognormal(ln 512, 1) lengths, H={w.H}, "
                 f"d_h={w.D}, {st}, {w.pool_pages}-page pool after {w.churn_cycles} lease/release cycles")
@@ -76,9 +79,9 @@ def algorithmic_bytes(w) -> int:
     and written, q and out, page-table entries and lengths."""
     lens = w.seq_lens.astype(np.int64)
     es = w.elem_bytes
-    hist = int((lens - 1).sum()) * w.H * w.D * 2 * es
+    hist = int((lens - 1).sum()) * w.H * w.D * 2 * es          # H = KV heads
     new_rows = w.B * w.H * w.D * es * 2 * 2
-    q_out = w.B * w.H * w.D * 4 * 2
+    q_out = w.B * w.HQ * w.D * 4 * 2                             # query heads
     tables = int(w.n_pages.sum()) * 4 + w.B * 4
     return hist + new_rows + q_out + tables
 
@@ -220,7 +223,7 @@ def setup_device(w, torch):
     from synth.workloads import churn_ops, LEASE
 
     pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "f32" if w.elem_bytes == 4 else "bf16",
-                    w.max_context, w.seed)
+                    w.max_context, w.seed, query_heads=w.HQ)
     reqs = [pool.request() for _ in range(w.B)]
     for r_i, kind, cnt in (churn_ops(w) if w.churn_cycles else []):
         try:
@@ -243,7 +246,7 @@ def setup_device(w, torch):
                tables=torch.from_numpy(tables).cuda(), lens=torch.from_numpy(host["lens"]).cuda())
     max_seq_len = int(w.seq_lens.max())
     ws = pool.workspace(w.B, max_seq_len)
-    out = torch.empty((w.B, w.H, w.D), dtype=torch.float32, device="cuda")
+    out = torch.empty((w.B, w.HQ, w.D), dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
     return pool, reqs, host, dev, ws, out, max_seq_len
 
@@ -344,7 +347,8 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.elem_bytes == 2 else "f32", "data": "synthetic",
             "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
-                       "head_dim": w.D, "page_size": w.P, "pool_pages": w.pool_pages,
+                       "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P,
+                       "pool_pages": w.pool_pages,
                        "seq_len_max": int(w.seq_lens.max()), "tokens_retained": int(w.seq_lens.sum()),
                        "storage": "bf16" if w.elem_bytes == 2 else "fp32", "accumulate": "fp32",
                        "alg_bytes_per_step": alg,
@@ -502,7 +506,7 @@ def run_gpu_serial(args):
             "tokens_per_s": round(world / (tok_ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": f"split_decode_kernel<{'bf16' if w.elem_bytes == 2 else 'f32'},{w.D}>",
+                         "kernel": f"split_decode_kernel<{'bf16' if w.elem_bytes == 2 else 'f32'},{w.D},{w.group}>",
                          "kernel_ms": round(kernel_ms, 5), "peak_kind": peak_kind + " (hbm_gbs copy)",
                          "note": "one layer's split kernel; latency-bound at this size"},
             "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
@@ -543,7 +547,7 @@ def oracle_sample(w, requests, threads=0):
 
     def run():
         return oracle.paged_decode_attention(kp, vp, q[requests], k_new[requests], v_new[requests],
-                                             tab, lens, dt, threads=threads)
+                                             tab, lens, dt, threads=threads, group=w.group)
     sample_bytes = int((lens.astype(np.int64) - 1).sum()) * w.H * w.D * 2 * w.elem_bytes
     return run, sample_bytes, lens
 

@@ -14,7 +14,9 @@
  *                  model-wide cache, then advance every block coherently".
  *   [CACHED-CELLS] "38 · Cached generation", section "Count attention-score
  *                  cells, not total runtime".
- *   [ROLLOUT-KV]   "Rollout Serving, Caching, and Batching", KV-cache memory formula.
+ *   [ROLLOUT-KV]   "Rollout Serving, Caching, and Batching", KV-cache memory formula
+ *                  (and its note that grouped-query or multi-query attention has
+ *                  fewer KV heads than query heads).
  *
  * Conventions (all entry points):
  *   - Every call returns a pkv_status.  PKV_OK is 0.  A call that returns an
@@ -83,10 +85,36 @@ typedef enum pkv_dtype {
 typedef struct pkv_counters {
     int64_t committed_tokens;   /* tokens made visible by pkv_commit_token */
     int64_t cache_appends;      /* layers x committed tokens */
-    int64_t score_cells;        /* sum over committed tokens of layers x heads x t */
+    int64_t score_cells;        /* sum over committed tokens of layers x query_heads x t */
 } pkv_counters;
 
 /* ---------------------------------------------------------------- pool -- */
+
+/*
+ * Pool geometry for pkv_pool_create_ex.  pkv_pool_options_init fills the
+ * defaults: 1 layer, pages 0, 1 KV head, query_heads 0, head_dim 128,
+ * page_size 16, PKV_BF16, max_context 4096, seed 0, flags 0.
+ *   kv_heads:    heads stored in every page (the K/V layout's head axis).
+ *   query_heads: heads of the query and of the output; 0 means kv_heads.  A
+ *                multiple of kv_heads: query head q reads KV head
+ *                q / (query_heads / kv_heads) (grouped-query attention,
+ *                [ROLLOUT-KV]; kv_heads == 1 is multi-query attention).
+ * The other fields are those of pkv_pool_create.
+ */
+typedef struct pkv_pool_options {
+    int layers;
+    int64_t pages;
+    int kv_heads;
+    int query_heads;
+    int head_dim;
+    int page_size;
+    int dtype;
+    int64_t max_context;
+    uint64_t seed;
+    unsigned flags;
+} pkv_pool_options;
+
+int pkv_pool_options_init(pkv_pool_options* options);
 
 /*
  * Create a paged pool ([SERVE-PAGED]).
@@ -105,12 +133,21 @@ typedef struct pkv_counters {
  *   flags:       0, or PKV_POOL_HOST_ONLY.
  * Supported by the kernels: head_dim a power of two, 2 <= head_dim <= 128 for
  * PKV_F32 and <= 256 for PKV_BF16 (else PKV_ERR_UNSUPPORTED, unless HOST_ONLY).
+ * Equivalent to pkv_pool_create_ex with kv_heads = query_heads = heads.
  * Device storage is 2 * layers * pages * page_size * heads * head_dim * element
  * size bytes ([ROLLOUT-KV]), zero-filled; the pool also allocates a 4-byte
  * device error word.  On success *out receives the handle.
  */
 int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page_size, int dtype,
                     int64_t max_context, uint64_t seed, unsigned flags, pkv_pool** out);
+
+/* Create a pool from options (see pkv_pool_options).  Grouped-query pools
+ * (query_heads = G x kv_heads) are implemented for G in {2, 4, 8} at head_dim 64
+ * and 128 (else PKV_ERR_UNSUPPORTED, unless HOST_ONLY). */
+int pkv_pool_create_ex(const pkv_pool_options* options, pkv_pool** out);
+
+/* KV heads stored per page and heads of the query (either pointer may be NULL). */
+int pkv_pool_heads(const pkv_pool* pool, int* kv_heads, int* query_heads);
 
 /* Free the pool and its device storage.  PKV_ERR_BAD_STATE while any request
  * created from it is alive.  NULL is accepted. */
@@ -181,9 +218,9 @@ int pkv_begin_token(pkv_request* req, int64_t* position);
  * attend the newest query over all t = position + 1 retained keys of that
  * layer, the new one included ([CACHED-MIX]: scores q.k / sqrt(head_dim),
  * stable softmax, weighted sum of values).
- *   q   [heads][head_dim] fp32, device
- *   k,v [heads][head_dim] storage dtype, device
- *   out [heads][head_dim] fp32, device (the [1,H,1,d_h] attention context)
+ *   q   [query_heads][head_dim] fp32, device
+ *   k,v [kv_heads][head_dim] storage dtype, device
+ *   out [query_heads][head_dim] fp32, device (the [1,H,1,d_h] attention context)
  *   stream: cudaStream_t
  * Call once per layer per pending token; BAD_STATE if none is pending or the
  * layer already ran for it.  The new row is written into the page at once but
@@ -197,7 +234,7 @@ int pkv_append_and_attend(pkv_request* req, int layer, const float* q, const voi
 /* Make the pending position visible ([SERVE-FLOW] step 3).  BAD_STATE unless a
  * token is pending and every layer ran pkv_append_and_attend for it exactly
  * once ([CACHED-BIND]: all layers advance together).  Counters advance by
- * layers (appends) and layers x heads x t (score cells). */
+ * layers (appends) and layers x query_heads x t (score cells). */
 int pkv_commit_token(pkv_request* req);
 
 /* Drop the pending token ([SERVE-FLOW] step 4): the visible length stays, and a
@@ -222,15 +259,15 @@ int pkv_workspace_size(const pkv_pool* pool, int batch, int64_t max_seq_len, siz
  * length t_b = seq_lens[b] (new token included, >= 1):
  *   1. store k_new[b], v_new[b] at logical position t_b - 1, i.e. physical page
  *      page_tables[b][(t_b - 1) / page_size], slot (t_b - 1) % page_size;
- *   2. for each head h:
- *      out[b][h] = sum_j softmax_j(q[b][h] . K_j / sqrt(head_dim)) V_j, over the
+ *   2. for each query head q (KV head h = q / (query_heads / kv_heads)):
+ *      out[b][q] = sum_j softmax_j(q[b][q] . K_j / sqrt(head_dim)) V_j, over the
  *      t_b keys K_j = K[page_tables[b][j / page_size]][h][j % page_size].
- *   q            [batch][heads][head_dim] fp32, device
- *   k_new, v_new [batch][heads][head_dim] storage dtype, device
+ *   q            [batch][query_heads][head_dim] fp32, device
+ *   k_new, v_new [batch][kv_heads][head_dim] storage dtype, device
  *   page_tables  [batch][max_pages] int32, device (entries past ceil(t_b/page_size) unread)
  *   seq_lens     [batch] int32, device
  *   max_seq_len  host bound on every seq_lens entry (sizes the launch)
- *   out          [batch][heads][head_dim] fp32, device
+ *   out          [batch][query_heads][head_dim] fp32, device
  *   workspace    device scratch of >= pkv_workspace_size bytes (caller owned,
  *                16-byte aligned, contents need no initialisation)
  * Stateless over bookkeeping: the caller owns lengths and tables.  Bad

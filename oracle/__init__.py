@@ -62,6 +62,9 @@ def load(path: str):
     L.orc_paged_decode_attention.restype = i32
     L.orc_paged_decode_attention.argtypes = [i32, i32, i32, i32, i32, vp, vp, i64, vp, vp,
                                              vp, vp, i32, vp, vp, vp, i64, i32]
+    L.orc_paged_decode_attention_gqa.restype = i32
+    L.orc_paged_decode_attention_gqa.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, i64, vp, vp,
+                                                 vp, vp, i32, vp, vp, vp, i64, i32]
     L.orc_max_threads.restype = i32
     return L
 
@@ -85,14 +88,15 @@ def _check_pool(pool: np.ndarray, dtype: int):
 def paged_decode_attention(k_pool: np.ndarray, v_pool: np.ndarray, q: np.ndarray,
                            k_new: np.ndarray, v_new: np.ndarray, tables: np.ndarray,
                            seq_lens: np.ndarray, dtype: int = F32, lanes=None,
-                           threads: int = 0, library=None) -> np.ndarray:
+                           threads: int = 0, library=None, group: int = 1) -> np.ndarray:
     """Append the new rows, then fp64 attention of each lane's newest query.
 
     k_pool, v_pool: one layer, [pages, H, P, D] storage dtype (fp32 or bf16 bits as
-    uint16); modified in place by the append.  q [B, H, D] fp32; k_new, v_new
+    uint16); modified in place by the append.  q [B, H*group, D] fp32; k_new, v_new
     [B, H, D] storage dtype; tables [B, max_pages] int32; seq_lens [B] int32 (t_b,
-    new token included).  Returns out [B, H, D] fp64 (lanes not listed in ``lanes``
-    are left zero).  ``library``: an alternative loaded oracle library (tests only).
+    new token included).  Query head qh reads KV head qh // group.  Returns out
+    [B, H*group, D] fp64 (query lanes b*H*group + qh not listed in ``lanes`` are
+    left zero).  ``library``: an alternative loaded oracle library (tests only).
     """
     _check_pool(k_pool, dtype)
     _check_pool(v_pool, dtype)
@@ -100,7 +104,7 @@ def paged_decode_attention(k_pool: np.ndarray, v_pool: np.ndarray, q: np.ndarray
     assert v_pool.shape == k_pool.shape
     q = np.ascontiguousarray(q, dtype=np.float32)
     B = q.shape[0]
-    assert q.shape == (B, H, D)
+    assert q.shape == (B, H * group, D)
     k_new = np.ascontiguousarray(k_new, dtype=_storage_dtype(dtype))
     v_new = np.ascontiguousarray(v_new, dtype=_storage_dtype(dtype))
     assert k_new.shape == (B, H, D) and v_new.shape == (B, H, D)
@@ -108,13 +112,18 @@ def paged_decode_attention(k_pool: np.ndarray, v_pool: np.ndarray, q: np.ndarray
     assert tables.ndim == 2 and tables.shape[0] == B
     seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     assert seq_lens.shape == (B,)
-    out = np.zeros((B, H, D), dtype=np.float64)
+    out = np.zeros((B, H * group, D), dtype=np.float64)
     lane_arr = None
     n_lanes = 0
     if lanes is not None:
         lane_arr = np.ascontiguousarray(lanes, dtype=np.int64)
         n_lanes = lane_arr.size
-    rc = (library or lib()).orc_paged_decode_attention(
+    L = library or lib()
+    if group == 1:
+        call = lambda *a: L.orc_paged_decode_attention(*a)           # noqa: E731
+    else:
+        call = lambda B_, H_, *a: L.orc_paged_decode_attention_gqa(B_, H_, group, *a)  # noqa: E731
+    rc = call(
         B, H, D, P, dtype, k_pool.ctypes.data, v_pool.ctypes.data, n_pages, q.ctypes.data,
         k_new.ctypes.data, v_new.ctypes.data, tables.ctypes.data, tables.shape[1],
         seq_lens.ctypes.data, out.ctypes.data,

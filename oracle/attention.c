@@ -32,6 +32,12 @@
  * t_b counts the new token ("38 · Cached generation", section "Keep retained
  * length and final length separate": t is the number of keys read by the one
  * newest cached query).  q is fp32, widened to fp64.  Output is fp64.
+ *
+ * Grouped-query attention ("Rollout Serving, Caching, and Batching", KV-cache
+ * memory formula: grouped-query or multi-query attention has fewer KV heads
+ * than query heads): with `group` query heads per KV head, query head qh reads
+ * the keys and values of KV head qh / group.  group = 1 is ordinary multi-head
+ * attention.
  */
 #include <stdint.h>
 #include <string.h>
@@ -112,26 +118,29 @@ static int lane_attention(int H, int D, int P, int dtype, const void* k_pool, co
 
 /*
  * Batched paged decode attention, steps 1-5.
- *   q        [B][H][D] fp32
+ *   H        KV heads; the query has H * group heads
+ *   q        [B][H*group][D] fp32
  *   k_new    [B][H][D] storage dtype; v_new likewise
  *   tables   [B][max_pages] int32 physical page ids
  *   seq_lens [B] retained lengths t_b including the new token (>= 1)
  *   k_pool / v_pool: one layer, [n_pages][H][P][D] storage dtype (modified by step 1)
- *   out      [B][H][D] fp64
- *   lanes    optional list of n_lanes lane ids (b*H + h) to compute; NULL = all.
- *            Step 1 always runs for every request.
+ *   out      [B][H*group][D] fp64
+ *   lanes    optional list of n_lanes query lanes (b*H*group + qh) to compute;
+ *            NULL = all.  Step 1 always runs for every request.
  *   threads  OpenMP threads for the lane loop (<= 0: library default)
  * Returns 0 on success, -1 on an out-of-range length or page id.
  */
-int orc_paged_decode_attention(int B, int H, int D, int P, int dtype, void* k_pool, void* v_pool,
-                               int64_t n_pages, const float* q, const void* k_new,
-                               const void* v_new, const int32_t* tables, int max_pages,
-                               const int32_t* seq_lens, double* out, const int64_t* lanes,
-                               int64_t n_lanes, int threads) {
+int orc_paged_decode_attention_gqa(int B, int H, int group, int D, int P, int dtype, void* k_pool,
+                                   void* v_pool, int64_t n_pages, const float* q,
+                                   const void* k_new, const void* v_new, const int32_t* tables,
+                                   int max_pages, const int32_t* seq_lens, double* out,
+                                   const int64_t* lanes, int64_t n_lanes, int threads) {
+    if (group < 1) return -1;
     int rc = orc_append(B, H, D, P, dtype, k_pool, v_pool, n_pages, k_new, v_new, tables,
                         max_pages, seq_lens);
     if (rc != 0) return rc;
-    int64_t total = lanes ? n_lanes : (int64_t)B * H;
+    const int HQ = H * group;
+    int64_t total = lanes ? n_lanes : (int64_t)B * HQ;
     int64_t t_max = 1;
     for (int b = 0; b < B; ++b) if (seq_lens[b] > t_max) t_max = seq_lens[b];
     int bad = 0;
@@ -149,15 +158,26 @@ int orc_paged_decode_attention(int B, int H, int D, int P, int dtype, void* k_po
         for (int64_t i = 0; i < total; ++i) {
             if (!scores) continue;
             int64_t lane = lanes ? lanes[i] : i;
-            int b = (int)(lane / H), h = (int)(lane % H);
+            int b = (int)(lane / HQ), qh = (int)(lane % HQ);
             if (lane_attention(H, D, P, dtype, k_pool, v_pool, n_pages, q + lane * D,
-                               tables + (int64_t)b * max_pages, seq_lens[b], h, scores,
-                               out + lane * D) != 0)
+                               tables + (int64_t)b * max_pages, seq_lens[b], qh / group,
+                               scores, out + lane * D) != 0)
                 bad = 1;
         }
         free(scores);
     }
     return bad ? -1 : 0;
+}
+
+/* Multi-head attention: one query head per KV head. */
+int orc_paged_decode_attention(int B, int H, int D, int P, int dtype, void* k_pool, void* v_pool,
+                               int64_t n_pages, const float* q, const void* k_new,
+                               const void* v_new, const int32_t* tables, int max_pages,
+                               const int32_t* seq_lens, double* out, const int64_t* lanes,
+                               int64_t n_lanes, int threads) {
+    return orc_paged_decode_attention_gqa(B, H, 1, D, P, dtype, k_pool, v_pool, n_pages, q, k_new,
+                                          v_new, tables, max_pages, seq_lens, out, lanes, n_lanes,
+                                          threads);
 }
 
 /* Threads the lane loop would use by default. */

@@ -88,9 +88,16 @@ class OraclePool:
     """Per-layer K/V pools [pages, H, P, D] (storage dtype) plus a FIFO free list."""
 
     def __init__(self, layers: int, pages: int, heads: int, head_dim: int, page_size: int = 16,
-                 dtype: int = F32, max_context: int = 0, seed: int = 0, storage: bool = True):
+                 dtype: int = F32, max_context: int = 0, seed: int = 0, storage: bool = True,
+                 query_heads: int = 0):
+        """heads: KV heads stored per page; query_heads: heads of the query (0 = heads),
+        a multiple of heads (grouped-query attention)."""
         if layers < 1 or heads < 1 or head_dim < 1 or page_size < 1 or max_context < 1 or pages < 0:
             raise OracleError(Status.INVALID_ARGUMENT, "bad pool geometry")
+        query_heads = query_heads or heads
+        if query_heads % heads:
+            raise OracleError(Status.INVALID_ARGUMENT, "query heads not a multiple of KV heads")
+        self.HQ, self.group = query_heads, query_heads // heads
         if pages == 0:
             pages = -(-max_context // page_size)       # one maximum-length context
         self.layers, self.pages, self.H, self.D, self.P = layers, pages, heads, head_dim, page_size
@@ -175,7 +182,7 @@ class OracleRequest:
 
     def append_and_attend(self, layer: int, q: np.ndarray, k: np.ndarray, v: np.ndarray,
                           compute: bool = True):
-        """q [H, D] fp32; k, v [H, D] storage dtype.  Returns out [H, D] fp64 (or None)."""
+        """q [HQ, D] fp32; k, v [H, D] storage dtype.  Returns out [HQ, D] fp64 (or None)."""
         p = self.pool
         if self.pending is None:
             raise OracleError(Status.BAD_STATE, "no token pending")
@@ -188,7 +195,8 @@ class OracleRequest:
         lens = np.asarray([t], dtype=np.int32)
         kp, vp = p.k[layer], p.v[layer]
         if compute:
-            out = paged_decode_attention(kp, vp, q[None], k[None], v[None], tables, lens, p.dtype)[0]
+            out = paged_decode_attention(kp, vp, q[None], k[None], v[None], tables, lens, p.dtype,
+                                         group=p.group)[0]
         else:
             _append(kp, vp, k[None], v[None], tables, lens, p.dtype)
             out = None
@@ -205,7 +213,7 @@ class OracleRequest:
         self.length = t
         self.committed_tokens += 1
         self.cache_appends += p.layers
-        self.score_cells += p.layers * p.H * t
+        self.score_cells += p.layers * p.HQ * t
         self.pending = None
 
     def abort_token(self) -> None:

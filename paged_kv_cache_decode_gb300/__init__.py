@@ -25,7 +25,7 @@ import ctypes
 import torch
 
 from .binding import (  # noqa: F401
-    lib, check, PkvError, pkv_counters, LIB_PATH,
+    lib, check, PkvError, pkv_counters, pkv_pool_options, LIB_PATH,
     PKV_OK, PKV_ERR_INVALID_ARGUMENT, PKV_ERR_OUT_OF_PAGES, PKV_ERR_CAPACITY_EXCEEDED,
     PKV_ERR_BAD_STATE, PKV_ERR_OUT_OF_MEMORY, PKV_ERR_CUDA, PKV_ERR_DEVICE_CHECK,
     PKV_ERR_NO_STORAGE, PKV_ERR_UNSUPPORTED, PKV_F32, PKV_BF16, PKV_POOL_HOST_ONLY,
@@ -81,19 +81,28 @@ class _DeviceArray:
 
 
 class Pool:
-    """A paged K/V pool: per layer, key and value pages [pages, heads, page_size, head_dim]."""
+    """A paged K/V pool: per layer, key and value pages [pages, heads, page_size, head_dim].
+
+    ``heads`` is the number of KV heads stored per page; ``query_heads`` (default:
+    ``heads``) the heads of the query and output, a multiple of ``heads``
+    (grouped-query attention)."""
 
     def __init__(self, layers: int, pages: int, heads: int, head_dim: int, page_size: int = 16,
-                 dtype="f32", max_context: int = 4096, seed: int = 0, host_only: bool = False):
+                 dtype="f32", max_context: int = 4096, seed: int = 0, host_only: bool = False,
+                 query_heads: int = 0):
         self.layers, self.heads, self.head_dim, self.page_size = layers, heads, head_dim, page_size
+        self.query_heads = query_heads or heads
         self.dtype = _dtype_code(dtype)
         self.torch_dtype = _TORCH_DTYPE[self.dtype]
         self.max_context = max_context
         self.host_only = host_only
+        o = pkv_pool_options()
+        check(lib.pkv_pool_options_init(ctypes.byref(o)), "pkv_pool_options_init")
+        o.layers, o.pages, o.kv_heads, o.query_heads = layers, pages, heads, self.query_heads
+        o.head_dim, o.page_size, o.dtype, o.max_context = head_dim, page_size, self.dtype, max_context
+        o.seed, o.flags = seed & ((1 << 64) - 1), PKV_POOL_HOST_ONLY if host_only else 0
         h = ctypes.c_void_p()
-        check(lib.pkv_pool_create(layers, pages, heads, head_dim, page_size, self.dtype, max_context,
-                                  seed & ((1 << 64) - 1), PKV_POOL_HOST_ONLY if host_only else 0,
-                                  ctypes.byref(h)), "pkv_pool_create")
+        check(lib.pkv_pool_create_ex(ctypes.byref(o), ctypes.byref(h)), "pkv_pool_create_ex")
         self._h = h
         self.pages = self.page_info()[0]
         self.max_pages_per_request = -(-max_context // page_size)
@@ -163,9 +172,9 @@ class Pool:
     def paged_decode_attention(self, layer: int, q, k_new, v_new, page_tables, seq_lens,
                                max_seq_len: int, out=None, workspace=None, stream=None):
         B = q.shape[0]
-        H, D = self.heads, self.head_dim
+        H, HQ, D = self.heads, self.query_heads, self.head_dim
         if out is None:
-            out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
+            out = torch.empty((B, HQ, D), dtype=torch.float32, device=q.device)
         if workspace is None:
             key = (B, max_seq_len)
             if key not in self._ws:
@@ -175,12 +184,12 @@ class Pool:
             raise ValueError("page_tables must be [batch, max_pages]")
         check(lib.pkv_paged_decode_attention(
             self.handle, layer, B,
-            _dev(q, "q", torch.float32, (B, H, D)),
+            _dev(q, "q", torch.float32, (B, HQ, D)),
             _dev(k_new, "k_new", self.torch_dtype, (B, H, D)),
             _dev(v_new, "v_new", self.torch_dtype, (B, H, D)),
             _dev(page_tables, "page_tables", torch.int32, None), page_tables.shape[1],
             _dev(seq_lens, "seq_lens", torch.int32, (B,)), int(max_seq_len),
-            _dev(out, "out", torch.float32, (B, H, D)),
+            _dev(out, "out", torch.float32, (B, HQ, D)),
             _dev(workspace, "workspace", torch.uint8, None), workspace.numel(),
             _stream_ptr(stream)), "pkv_paged_decode_attention")
         return out
@@ -277,15 +286,17 @@ class Request:
         return pos.value
 
     def append_and_attend(self, layer: int, q, k, v, out=None, stream=None):
-        """q [H, d_h] fp32; k, v [H, d_h] storage dtype; returns out [H, d_h] fp32."""
+        """q [query_heads, d_h] fp32; k, v [heads, d_h] storage dtype; returns out
+        [query_heads, d_h] fp32."""
         p = self.pool
-        shape = (p.heads, p.head_dim)
+        qshape = (p.query_heads, p.head_dim)
+        kshape = (p.heads, p.head_dim)
         if out is None:
-            out = torch.empty(shape, dtype=torch.float32, device=q.device)
+            out = torch.empty(qshape, dtype=torch.float32, device=q.device)
         check(lib.pkv_append_and_attend(
-            self.handle, layer, _dev(q, "q", torch.float32, shape),
-            _dev(k, "k", p.torch_dtype, shape), _dev(v, "v", p.torch_dtype, shape),
-            _dev(out, "out", torch.float32, shape), _stream_ptr(stream)), "pkv_append_and_attend")
+            self.handle, layer, _dev(q, "q", torch.float32, qshape),
+            _dev(k, "k", p.torch_dtype, kshape), _dev(v, "v", p.torch_dtype, kshape),
+            _dev(out, "out", torch.float32, qshape), _stream_ptr(stream)), "pkv_append_and_attend")
         return out
 
     def commit_token(self) -> None:
@@ -305,8 +316,9 @@ class Request:
 # --------------------------------------------------------- C-ABI names --
 
 def pool_create(layers, pages, heads, head_dim, page_size=16, dtype="f32", max_context=4096,
-                seed=0, host_only=False) -> Pool:
-    return Pool(layers, pages, heads, head_dim, page_size, dtype, max_context, seed, host_only)
+                seed=0, host_only=False, query_heads=0) -> Pool:
+    return Pool(layers, pages, heads, head_dim, page_size, dtype, max_context, seed, host_only,
+                query_heads)
 
 
 def pool_destroy(pool: Pool) -> None:

@@ -36,6 +36,14 @@ PKV_DEVERR_TIMEOUT = 4
 LIB_PATH = _build.LIB
 
 
+class pkv_pool_options(ctypes.Structure):
+    _fields_ = [("layers", ctypes.c_int), ("pages", ctypes.c_int64), ("kv_heads", ctypes.c_int),
+                ("query_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("page_size", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("max_context", ctypes.c_int64), ("seed", ctypes.c_uint64),
+                ("flags", ctypes.c_uint)]
+
+
 class pkv_counters(ctypes.Structure):
     _fields_ = [("committed_tokens", ctypes.c_int64), ("cache_appends", ctypes.c_int64),
                 ("score_cells", ctypes.c_int64)]
@@ -48,6 +56,9 @@ _P = ctypes.POINTER
 # name -> argtypes (restype int unless listed in _RESTYPE)
 SIGNATURES = {
     "pkv_pool_create": [_i, _i64, _i, _i, _i, _i, _i64, _u64, ctypes.c_uint, _P(_vp)],
+    "pkv_pool_options_init": [_P(pkv_pool_options)],
+    "pkv_pool_create_ex": [_P(pkv_pool_options), _P(_vp)],
+    "pkv_pool_heads": [_vp, _P(_i), _P(_i)],
     "pkv_pool_destroy": [_vp],
     "pkv_pool_kv_ptr": [_vp, _i, _P(_vp), _P(_vp)],
     "pkv_pool_bytes": [_vp, _P(_u64)],

@@ -398,22 +398,22 @@ __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t T, int W) {
     return ((x + 1) * W - 1) / T;
 }
 
-// Combine the partials of lane `lane_id`, deposited by workers w_lo..w_hi
-// (those owning at least one tile) in slots lane_id + w, into out.  One warp:
-// lane j takes partials j, j + 32, ... for the maximum and the weights
-// 2^(m_w - M); the weighted sum of the o vectors then runs 32 partials at a
-// time with each weight broadcast by shuffle, so the loads of consecutive
+// Combine the partials of query g of KV lane `lane_id`, deposited by workers
+// w_lo..w_hi (those owning at least one tile) in slots lane_id + w, into out.
+// One warp: lane j takes partials j, j + 32, ... for the maximum and the
+// weights 2^(m_w - M); the weighted sum of the o vectors then runs 32 partials
+// at a time with each weight broadcast by shuffle, so the loads of consecutive
 // partials are independent.  Partials are read from L2 (other SMs wrote them
 // during this kernel).
-template <int D, int DPL>
-__device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, int64_t w_lo,
-                                           int64_t w_hi, int64_t T_all, int lane) {
+template <int D, int DPL, int G>
+__device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, int g, int64_t w_lo,
+                                            int64_t w_hi, int64_t T_all, int lane) {
     auto owns_tiles = [&](int64_t w) { return (w * T_all) / p.W != ((w + 1) * T_all) / p.W; };
     const int cnt = (int)(w_hi - w_lo + 1);
     const int64_t slot0 = lane_id + w_lo;
     float M = -INFINITY;
     for (int j = lane; j < cnt; j += 32)
-        if (owns_tiles(w_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[slot0 + j]).x);
+        if (owns_tiles(w_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + j) * G + g]).x);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
@@ -424,7 +424,7 @@ __device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, in
     for (int base = 0; base < cnt; base += 32) {
         float wgt = 0.f;
         if (base + lane < cnt && owns_tiles(w_lo + base + lane)) {
-            const float2 ml = __ldcg(&p.part_ml[slot0 + base + lane]);
+            const float2 ml = __ldcg(&p.part_ml[(slot0 + base + lane) * G + g]);
             wgt = exp2f(ml.x - M);
             L = fmaf(ml.y, wgt, L);
         }
@@ -434,7 +434,7 @@ __device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, in
             const float wj = __shfl_sync(0xffffffffu, wgt, j);
             if (has_features) {
                 // slots of workers that own no tile hold stale data: weight 0, value dropped
-                const float* op = p.part_o + (slot0 + base + j) * D + lane * DPL;
+                const float* op = p.part_o + ((slot0 + base + j) * G + g) * D + lane * DPL;
 #pragma unroll
                 for (int i = 0; i < DPL; ++i) {
                     const float v = __ldcg(op + i);
@@ -447,29 +447,33 @@ __device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, in
     for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     if (!has_features) return;
     const float inv = 1.f / L;
-    float* out = p.out + lane_id * D + lane * DPL;
+    float* out = p.out + (lane_id * G + g) * D + lane * DPL;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
 
-template <typename T, int D>
+// One worker (warp) of the split kernel.  A lane here is a (request, KV head)
+// pair; its G query heads (grouped-query attention, G = 1 for multi-head) share
+// every staged K/V tile: query head h*G + g of request b reads KV head h.
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(Geo<T, D>::WARPS * 32, 1)
 split_decode_kernel(const KParams p) {
-    using G = Geo<T, D>;
-    using VT = typename VecBits<G::VBYTES>::type;
-    constexpr int NV = G::VEC / 2;   // float pairs per lane vector
+    using Gm = Geo<T, D>;
+    using VT = typename VecBits<Gm::VBYTES>::type;
+    constexpr int NV = Gm::VEC / 2;   // float pairs per lane vector
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t w = (int64_t)blockIdx.x * G::WARPS + warp;
+    const int64_t w = (int64_t)blockIdx.x * Gm::WARPS + warp;
     if (w >= p.W) return;
 
-    unsigned char* ring = smem + warp * G::WARP_SMEM;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::WARPS * G::WARP_SMEM) + warp * G::STAGES;
-    int32_t* stage_page = reinterpret_cast<int32_t*>(smem + G::WARPS * (G::WARP_SMEM + G::STAGES * 8)) +
-                          warp * G::STAGES;
+    unsigned char* ring = smem + warp * Gm::WARP_SMEM;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::WARPS * Gm::WARP_SMEM) + warp * Gm::STAGES;
+    int32_t* stage_page =
+        reinterpret_cast<int32_t*>(smem + Gm::WARPS * (Gm::WARP_SMEM + Gm::STAGES * 8)) +
+        warp * Gm::STAGES;
     if (lane == 0) {
-        for (int s = 0; s < G::STAGES; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < Gm::STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
     __syncwarp();
@@ -518,27 +522,27 @@ split_decode_kernel(const KParams p) {
             return;
         }
         const int64_t off = (((int64_t)page * p.H + prod.h) * p.P + prod.slot0) * D;
-        unsigned char* dst = ring + s * G::STAGE_BYTES;
-        mbar_arrive_expect_tx(&bars[s], G::STAGE_BYTES);
-        bulk_copy_g2s(dst, static_cast<const T*>(p.k_pages) + off, G::TILE_BYTES, &bars[s], policy);
-        bulk_copy_g2s(dst + G::TILE_BYTES, static_cast<const T*>(p.v_pages) + off, G::TILE_BYTES,
+        unsigned char* dst = ring + s * Gm::STAGE_BYTES;
+        mbar_arrive_expect_tx(&bars[s], Gm::STAGE_BYTES);
+        bulk_copy_g2s(dst, static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES, &bars[s], policy);
+        bulk_copy_g2s(dst + Gm::TILE_BYTES, static_cast<const T*>(p.v_pages) + off, Gm::TILE_BYTES,
                       &bars[s], policy);
     };
 
-    const int prologue = n_work < G::STAGES ? n_work : G::STAGES;
+    const int prologue = n_work < Gm::STAGES ? n_work : Gm::STAGES;
     for (int s = 0; s < prologue; ++s) {
         issue(s);
         cursor_advance(prod, p);
     }
 
-    const int rg = lane / G::TPR;             // row group of this lane
-    const int col = (lane % G::TPR) * G::VEC; // first feature of this lane
-    const int it_own = (lane % G::TPR) >> 1;  // warp step of the row this lane scores
-    const int row_own = it_own * G::RPI + rg;
+    const int rg = lane / Gm::TPR;             // row group of this lane
+    const int col = (lane % Gm::TPR) * Gm::VEC; // first feature of this lane
+    const int it_own = (lane % Gm::TPR) >> 1;  // warp step of the row this lane scores
+    const int row_own = it_own * Gm::RPI + rg;
 
-    float2 qv[NV];
-    float2 o[NV];
-    float m = -INFINITY, l = 0.f;
+    float2 qv[G][NV];
+    float2 o[G][NV];
+    float m[G], l[G];
     int piece_first = 0, t_b = 0;
     int s = 0;
     uint32_t parity = 0;
@@ -549,25 +553,28 @@ split_decode_kernel(const KParams p) {
         if (k == 0 || cur.tile == 0) {   // a new lane piece starts
             piece_first = cur.tile;
             t_b = (int)seq_len_at(p, cur.b);
-            const float2* qp = reinterpret_cast<const float2*>(p.q + lane_id * D + col);
 #pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                const float2 qq = qp[v];
-                qv[v] = make_float2(qq.x * p.qscale, qq.y * p.qscale);
-                o[v] = make_float2(0.f, 0.f);
+            for (int g = 0; g < G; ++g) {
+                const float2* qp = reinterpret_cast<const float2*>(p.q + (lane_id * G + g) * D + col);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const float2 qq = qp[v];
+                    qv[g][v] = make_float2(qq.x * p.qscale, qq.y * p.qscale);
+                    o[g][v] = make_float2(0.f, 0.f);
+                }
+                m[g] = -INFINITY;
+                l[g] = 0.f;
             }
-            m = -INFINITY;
-            l = 0.f;
         }
 
         if (!mbar_wait_bounded(&bars[s], parity, kWaitLimitNs)) {
             if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
             // let the copies already issued land before the shared memory goes away
-            const int last = (k + G::STAGES - 1 < n_work - 1) ? k + G::STAGES - 1 : n_work - 1;
+            const int last = (k + Gm::STAGES - 1 < n_work - 1) ? k + Gm::STAGES - 1 : n_work - 1;
             int s2 = s;
             uint32_t par2 = parity;
             for (int j = k + 1; j <= last; ++j) {
-                if (++s2 == G::STAGES) {
+                if (++s2 == Gm::STAGES) {
                     s2 = 0;
                     par2 ^= 1u;
                 }
@@ -576,7 +583,7 @@ split_decode_kernel(const KParams p) {
             return;
         }
 
-        T* Ks = reinterpret_cast<T*>(ring + s * G::STAGE_BYTES);
+        T* Ks = reinterpret_cast<T*>(ring + s * Gm::STAGE_BYTES);
         T* Vs = Ks + kTile * D;
         const int32_t page = stage_page[s];
         const bool page_ok = page >= 0 && page < p.n_pages;
@@ -587,7 +594,7 @@ split_decode_kernel(const KParams p) {
         if (last_tile && page_ok) {
             // fused append: row t_b - 1 comes from k_new / v_new, into the tile and the page
             const int r = rows - 1;
-            if (lane < G::TPR) {
+            if (lane < Gm::TPR) {
                 const int64_t src = lane_id * D + col;
                 const VT kb = *reinterpret_cast<const VT*>(static_cast<const T*>(p.k_new) + src);
                 const VT vb = *reinterpret_cast<const VT*>(static_cast<const T*>(p.v_new) + src);
@@ -602,107 +609,140 @@ split_decode_kernel(const KParams p) {
         }
 
         if (rows > 0) {
-            // partial dot products of this lane's features for its ITERS rows
-            float sc[G::ITERS];
+            // partial dot products of this lane's features for its ITERS rows, per query
+            float sc[G][Gm::ITERS];
 #pragma unroll
-            for (int it = 0; it < G::ITERS; ++it) {
-                const int row = it * G::RPI + rg;
-                float2 acc = make_float2(0.f, 0.f);
+            for (int it = 0; it < Gm::ITERS; ++it) {
+                const int row = it * Gm::RPI + rg;
+                float2 kf[NV];
                 if (row < kTile) {
-                    float2 kf[NV];
                     const VT kb = *reinterpret_cast<const VT*>(Ks + row * D + col);
-                    Storage<T>::template to_float2<G::VEC>(&kb, kf);
+                    Storage<T>::template to_float2<Gm::VEC>(&kb, kf);
+                } else {
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) acc = __ffma2_rn(qv[v], kf[v], acc);
+                    for (int v = 0; v < NV; ++v) kf[v] = make_float2(0.f, 0.f);
                 }
-                sc[it] = acc.x + acc.y;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) acc = __ffma2_rn(qv[g][v], kf[v], acc);
+                    sc[g][it] = acc.x + acc.y;
+                }
             }
             // transposed reduction over the TPR lanes of a row: each round halves
             // the values a lane keeps, the last round adds lane pairs
 #pragma unroll
-            for (int r = 0; r < G::HALVING_ROUNDS; ++r) {
-                const int half = G::ITERS >> (r + 1);   // lane offset of this round = 2 * half
-                const bool upper = (lane & (2 * half)) != 0;
+            for (int g = 0; g < G; ++g) {
 #pragma unroll
-                for (int i = 0; i < half; ++i) {
-                    const float send = upper ? sc[i] : sc[i + half];
-                    const float keep = upper ? sc[i + half] : sc[i];
-                    sc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * half);
+                for (int r = 0; r < Gm::HALVING_ROUNDS; ++r) {
+                    const int half = Gm::ITERS >> (r + 1);   // lane offset of this round = 2 * half
+                    const bool upper = (lane & (2 * half)) != 0;
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        const float send = upper ? sc[g][i] : sc[g][i + half];
+                        const float keep = upper ? sc[g][i + half] : sc[g][i];
+                        sc[g][i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * half);
+                    }
                 }
+                if (Gm::TPR >= 2) sc[g][0] += __shfl_xor_sync(0xffffffffu, sc[g][0], 1);
             }
-            if (G::TPR >= 2) sc[0] += __shfl_xor_sync(0xffffffffu, sc[0], 1);
-            const float s_own = row_own < rows ? sc[0] : -INFINITY;
-            float tmax = s_own;
+            float p_own[G];
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-            const float m_new = fmaxf(m, tmax);
-            const float alpha = exp2f(m - m_new);
-            const float p_own = exp2f(s_own - m_new);
-            l = fmaf(l, alpha, p_own);
-            const float2 a2 = make_float2(alpha, alpha);
+            for (int g = 0; g < G; ++g) {
+                const float s_own = row_own < rows ? sc[g][0] : -INFINITY;
+                float tmax = s_own;
 #pragma unroll
-            for (int v = 0; v < NV; ++v) o[v] = __fmul2_rn(o[v], a2);
+                for (int off = 16; off >= 1; off >>= 1)
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+                const float m_new = fmaxf(m[g], tmax);
+                const float alpha = exp2f(m[g] - m_new);
+                p_own[g] = exp2f(s_own - m_new);
+                l[g] = fmaf(l[g], alpha, p_own[g]);
+                const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int it = 0; it < G::ITERS; ++it) {
-                const int row = it * G::RPI + rg;
-                const float pw = G::TPR >= 2
-                    ? __shfl_sync(0xffffffffu, p_own, (lane & ~(G::TPR - 1)) | (it << 1))
-                    : p_own;
+                for (int v = 0; v < NV; ++v) o[g][v] = __fmul2_rn(o[g][v], a2);
+                m[g] = m_new;
+            }
+#pragma unroll
+            for (int it = 0; it < Gm::ITERS; ++it) {
+                const int row = it * Gm::RPI + rg;
+                float pw[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    pw[g] = Gm::TPR >= 2
+                        ? __shfl_sync(0xffffffffu, p_own[g], (lane & ~(Gm::TPR - 1)) | (it << 1))
+                        : p_own[g];
                 if (row < rows) {
                     float2 vf[NV];
                     const VT vb = *reinterpret_cast<const VT*>(Vs + row * D + col);
-                    Storage<T>::template to_float2<G::VEC>(&vb, vf);
-                    const float2 p2 = make_float2(pw, pw);
+                    Storage<T>::template to_float2<Gm::VEC>(&vb, vf);
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) o[v] = __ffma2_rn(p2, vf[v], o[v]);
+                    for (int g = 0; g < G; ++g) {
+                        const float2 p2 = make_float2(pw[g], pw[g]);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) o[g][v] = __ffma2_rn(p2, vf[v], o[g][v]);
+                    }
                 }
             }
-            m = m_new;
         }
 
         // the stage is free again: hand it to the copy engine for tile k + STAGES
         fence_proxy_async_smem();
         __syncwarp();
-        if (k + G::STAGES < n_work) {
+        if (k + Gm::STAGES < n_work) {
             issue(s);
             cursor_advance(prod, p);
         }
-        if (++s == G::STAGES) {
+        if (++s == Gm::STAGES) {
             s = 0;
             parity ^= 1u;
         }
 
         if (last_tile || k == n_work - 1) {
             // close the lane piece: sum the lanes' shares of l, and o over row groups
-            float lt = l;
+            float lt[G];
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
-            lt *= 1.f / G::DUP;
+            for (int g = 0; g < G; ++g) {
+                lt[g] = l[g];
 #pragma unroll
-            for (int off = G::TPR; off < 32; off <<= 1) {
+                for (int off = 16; off >= 1; off >>= 1) lt[g] += __shfl_xor_sync(0xffffffffu, lt[g], off);
+                lt[g] *= 1.f / Gm::DUP;
 #pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    o[v].x += __shfl_xor_sync(0xffffffffu, o[v].x, off);
-                    o[v].y += __shfl_xor_sync(0xffffffffu, o[v].y, off);
+                for (int off = Gm::TPR; off < 32; off <<= 1) {
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        o[g][v].x += __shfl_xor_sync(0xffffffffu, o[g][v].x, off);
+                        o[g][v].y += __shfl_xor_sync(0xffffffffu, o[g][v].y, off);
+                    }
                 }
             }
             if (piece_first == 0 && last_tile) {
-                if (lane < G::TPR) {
-                    const float inv = 1.f / lt;
-                    float2* op = reinterpret_cast<float2*>(p.out + lane_id * D + col);
+                if (lane < Gm::TPR) {
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) op[v] = make_float2(o[v].x * inv, o[v].y * inv);
+                    for (int g = 0; g < G; ++g) {
+                        const float inv = 1.f / lt[g];
+                        float2* op = reinterpret_cast<float2*>(p.out + (lane_id * G + g) * D + col);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v)
+                            op[v] = make_float2(o[g][v].x * inv, o[g][v].y * inv);
+                    }
                 }
             } else {
                 // deposit the partial; the last of the lane's workers to arrive merges
                 const int64_t slot = lane_id + w;
-                if (lane < G::TPR) {
-                    float2* op = reinterpret_cast<float2*>(p.part_o + slot * D + col);
+                if (lane < Gm::TPR) {
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) op[v] = o[v];
+                    for (int g = 0; g < G; ++g) {
+                        float2* op = reinterpret_cast<float2*>(p.part_o + (slot * G + g) * D + col);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) op[v] = o[g][v];
+                    }
                 }
-                if (lane == 0) p.part_ml[slot] = make_float2(m, lt);
+                if (lane == 0) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) p.part_ml[slot * G + g] = make_float2(m[g], lt[g]);
+                }
                 __threadfence();
                 __syncwarp();
                 const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // lane's first tile
@@ -738,7 +778,9 @@ split_decode_kernel(const KParams p) {
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
                     __threadfence();
-                    merge_lane<D, G::DPL>(p, lane_id, w_lo, w_hi, T_all, lane);
+#pragma unroll 1
+                    for (int g = 0; g < G; ++g)
+                        merge_query<D, Gm::DPL, G>(p, lane_id, g, w_lo, w_hi, T_all, lane);
                 }
                 __syncwarp();
             }
@@ -751,7 +793,7 @@ split_decode_kernel(const KParams p) {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WorkspaceLayout workspace_layout(int B, int H, int D, int workers) {
+WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G) {
     WorkspaceLayout L{};
     size_t off = 0;
     // lane counters first: their place must not depend on the worker count,
@@ -762,11 +804,11 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers) {
     off = align_up(off + sizeof(int64_t) * ((size_t)B + 1), 256);
     L.worker_req = off;
     off = align_up(off + sizeof(int32_t) * (size_t)workers, 256);
-    const size_t slots = (size_t)B * H + (size_t)workers;
+    const size_t slots = (size_t)B * H + (size_t)workers;   // per KV lane and worker
     L.part_ml = off;
-    off = align_up(off + sizeof(float2) * slots, 256);
+    off = align_up(off + sizeof(float2) * slots * (size_t)G, 256);
     L.part_o = off;
-    off = align_up(off + sizeof(float) * slots * (size_t)D, 256);
+    off = align_up(off + sizeof(float) * slots * (size_t)G * (size_t)D, 256);
     L.total = off;
     return L;
 }
@@ -781,32 +823,32 @@ int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len) {
     return (int)(want < pool_workers ? (want < 1 ? 1 : want) : pool_workers);
 }
 
-template <typename T, int D>
+template <typename T, int D, int G>
 static cudaError_t prepare_split() {
     static bool done = false;   // per instantiation
     if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<T, D>,
+    cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<T, D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Geo<T, D>::CTA_SMEM);
     if (e == cudaSuccess) done = true;
     return e;
 }
 
-template <typename T, int D>
+template <typename T, int D, int G>
 static int resident_workers_t(int num_sms) {
-    if (prepare_split<T, D>() != cudaSuccess) return 0;
+    if (prepare_split<T, D, G>() != cudaSuccess) return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_kernel<T, D>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_kernel<T, D, G>,
                                                       Geo<T, D>::WARPS * 32, Geo<T, D>::CTA_SMEM) !=
         cudaSuccess)
         return 0;
     return blocks * num_sms * Geo<T, D>::WARPS;
 }
 
-template <typename T, int D>
+template <typename T, int D, int G>
 static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream) {
-    using G = Geo<T, D>;
-    cudaError_t e = prepare_split<T, D>();
+    using Gm = Geo<T, D>;
+    cudaError_t e = prepare_split<T, D, G>();
     if (e != cudaSuccess) return e;
     if (p.epoch == 0) {   // a single request with epoch counters needs no plan
         plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
@@ -814,9 +856,9 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     }
     if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)((p.W + G::WARPS - 1) / G::WARPS));
-    cfg.blockDim = dim3(G::WARPS * 32);
-    cfg.dynamicSmemBytes = G::CTA_SMEM;
+    cfg.gridDim = dim3((unsigned)((p.W + Gm::WARPS - 1) / Gm::WARPS));
+    cfg.blockDim = dim3(Gm::WARPS * 32);
+    cfg.dynamicSmemBytes = Gm::CTA_SMEM;
     cfg.stream = stream;
     // dependent launch only behind this call's own plan kernel; with epoch
     // counters the kernel follows whatever came before in plain stream order
@@ -825,28 +867,32 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.epoch == 0 ? 1 : 0;
-    if ((e = cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D>, p)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G>, p)) != cudaSuccess) return e;
     if (a.ev_after && (e = cudaEventRecord(a.ev_after, stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
-#define PKV_FOR_EACH_D(X, T) X(T, 2) X(T, 4) X(T, 8) X(T, 16) X(T, 32) X(T, 64) X(T, 128)
+// Instantiated geometries: every head width for multi-head attention; groups
+// of 2, 4 and 8 query heads per KV head at head widths 64 and 128.
+#define PKV_FOR_EACH_D(X, T) X(T, 2, 1) X(T, 4, 1) X(T, 8, 1) X(T, 16, 1) X(T, 32, 1) \
+    X(T, 64, 1) X(T, 128, 1) X(T, 64, 2) X(T, 64, 4) X(T, 64, 8) X(T, 128, 2) X(T, 128, 4) X(T, 128, 8)
 
-bool decode_supported(int dtype, int D) {
+bool decode_supported(int dtype, int D, int G) {
     if (D < 2 || D > 256 || (D & (D - 1)) != 0) return false;
-    if (dtype == PKV_F32) return D <= 128;
-    if (dtype == PKV_BF16) return D <= 256;
-    return false;
+    if (dtype != PKV_F32 && dtype != PKV_BF16) return false;
+    if (dtype == PKV_F32 && D > 128) return false;
+    if (G == 1) return true;
+    return (G == 2 || G == 4 || G == 8) && (D == 64 || D == 128);
 }
 
-int resident_workers(int dtype, int D, int num_sms) {
-#define PKV_RW(T, DD) \
-    if (D == DD) return resident_workers_t<T, DD>(num_sms);
+int resident_workers(int dtype, int D, int G, int num_sms) {
+#define PKV_RW(T, DD, GG) \
+    if (D == DD && G == GG) return resident_workers_t<T, DD, GG>(num_sms);
     if (dtype == PKV_F32) {
         PKV_FOR_EACH_D(PKV_RW, float)
     } else if (dtype == PKV_BF16) {
         PKV_FOR_EACH_D(PKV_RW, __nv_bfloat16)
-        PKV_RW(__nv_bfloat16, 256)
+        PKV_RW(__nv_bfloat16, 256, 1)
     }
 #undef PKV_RW
     return 0;
@@ -871,7 +917,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.tiles_per_page = a.P / kTile;
     p.qscale = 1.4426950408889634f / sqrtf((float)a.D);
     p.out = a.out;
-    const WorkspaceLayout L = workspace_layout(a.B, a.H, a.D, a.workers);
+    const WorkspaceLayout L = workspace_layout(a.B, a.H, a.D, a.workers, a.G);
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     p.req_prefix = reinterpret_cast<int64_t*>(ws + L.req_prefix);
     p.worker_req = reinterpret_cast<int32_t*>(ws + L.worker_req);
@@ -881,13 +927,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.part_o = reinterpret_cast<float*>(ws + L.part_o);
     p.W = a.workers;
     p.err = a.dev_error;
-#define PKV_LAUNCH(T, DD) \
-    if (a.D == DD) return launch_t<T, DD>(a, p, stream);
+#define PKV_LAUNCH(T, DD, GG) \
+    if (a.D == DD && a.G == GG) return launch_t<T, DD, GG>(a, p, stream);
     if (a.dtype == PKV_F32) {
         PKV_FOR_EACH_D(PKV_LAUNCH, float)
     } else if (a.dtype == PKV_BF16) {
         PKV_FOR_EACH_D(PKV_LAUNCH, __nv_bfloat16)
-        PKV_LAUNCH(__nv_bfloat16, 256)
+        PKV_LAUNCH(__nv_bfloat16, 256, 1)
     }
 #undef PKV_LAUNCH
     return cudaErrorInvalidValue;

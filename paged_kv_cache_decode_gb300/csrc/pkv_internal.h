@@ -22,8 +22,9 @@ constexpr int kSplitWarps = PKV_SPLIT_WARPS;
 // One launch of the decode path for one layer.
 struct DecodeArgs {
     int dtype;               // PKV_F32 / PKV_BF16
-    int B, H, D, P;          // requests, heads, head width, page size (multiple of kTile)
-    const float* q;          // [B][H][D]
+    int B, H, D, P;          // requests, KV heads, head width, page size (multiple of kTile)
+    int G;                   // query heads per KV head (1: multi-head attention)
+    const float* q;          // [B][H*G][D]
     const void* k_new;       // [B][H][D] storage dtype
     const void* v_new;
     void* k_pages;           // this layer's pools, [pages][H][P][D]
@@ -34,7 +35,7 @@ struct DecodeArgs {
     const int32_t* seq_lens; // [B] device; nullptr => single request of length single_t
     int64_t single_t;
     int64_t max_seq_len;
-    float* out;              // [B][H][D]
+    float* out;              // [B][H*G][D]
     void* workspace;
     size_t workspace_bytes;
     int workers;             // workers of this launch (split-kernel warps)
@@ -50,12 +51,12 @@ struct WorkspaceLayout {
     size_t req_prefix;   // int64 [B + 1]: tiles-per-lane prefix over requests
     size_t worker_req;   // int32 [workers]: request holding each worker's first tile
     size_t lane_cnt;     // uint64 [B*H]: partials deposited per lane (plan-zeroed or epoch-tagged)
-    size_t part_ml;      // float2 [B*H + workers]: (running max in log2 units, sum)
-    size_t part_o;       // float [B*H + workers][D]: unnormalised partial outputs
+    size_t part_ml;      // float2 [B*H + workers][G]: (running max in log2 units, sum)
+    size_t part_o;       // float [B*H + workers][G][D]: unnormalised partial outputs
     size_t total;
 };
 
-WorkspaceLayout workspace_layout(int B, int H, int D, int workers);
+WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G);
 
 // Workers one launch uses: the pool's resident worker count, capped by the
 // number of tiles the launch can hold (B * H * ceil(max_seq_len / kTile)).
@@ -63,10 +64,10 @@ int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len);
 
 // Resident split-kernel warps per SM x SMs for this geometry on the current
 // device; 0 if the geometry is not implemented.
-int resident_workers(int dtype, int D, int num_sms);
+int resident_workers(int dtype, int D, int G, int num_sms);
 
-// True if the kernels implement (dtype, D).
-bool decode_supported(int dtype, int D);
+// True if the kernels implement (dtype, D, G).
+bool decode_supported(int dtype, int D, int G);
 
 // Enqueue the plan and split kernels on `stream`.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

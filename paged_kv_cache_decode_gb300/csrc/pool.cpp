@@ -61,6 +61,7 @@ struct SplitMix64 {
 
 struct pkv_pool {
     int layers = 0, heads = 0, head_dim = 0, page_size = 0, dtype = 0;
+    int query_heads = 0, group = 1;    // query heads = group x KV heads (grouped-query attention)
     int64_t pages = 0, max_context = 0, max_pages_per_request = 0;
     bool host_only = false;
     std::deque<int32_t> free_list;     // front = next page to lease
@@ -135,10 +136,51 @@ const char* pkv_status_string(int status) {
     }
 }
 
+int pkv_pool_options_init(pkv_pool_options* o) {
+    if (!o) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL options");
+    *o = pkv_pool_options{};
+    o->layers = 1;
+    o->pages = 0;
+    o->kv_heads = 1;
+    o->query_heads = 0;
+    o->head_dim = 128;
+    o->page_size = 16;
+    o->dtype = PKV_BF16;
+    o->max_context = 4096;
+    o->seed = 0;
+    o->flags = 0;
+    return ok();
+}
+
 int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page_size, int dtype,
                     int64_t max_context, uint64_t seed, unsigned flags, pkv_pool** out) {
-    if (!out) return fail(PKV_ERR_INVALID_ARGUMENT, "out is NULL");
+    pkv_pool_options o{};
+    o.layers = layers;
+    o.pages = pages;
+    o.kv_heads = heads;
+    o.query_heads = heads;
+    o.head_dim = head_dim;
+    o.page_size = page_size;
+    o.dtype = dtype;
+    o.max_context = max_context;
+    o.seed = seed;
+    o.flags = flags;
+    return pkv_pool_create_ex(&o, out);
+}
+
+int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
+    if (!out || !opts) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
     *out = nullptr;
+    const int layers = opts->layers, heads = opts->kv_heads, head_dim = opts->head_dim;
+    const int page_size = opts->page_size, dtype = opts->dtype;
+    int64_t pages = opts->pages;
+    const int64_t max_context = opts->max_context;
+    const uint64_t seed = opts->seed;
+    const unsigned flags = opts->flags;
+    const int query_heads = opts->query_heads == 0 ? heads : opts->query_heads;
+    if (heads >= 1 && (query_heads < heads || query_heads % heads != 0))
+        return fail(PKV_ERR_INVALID_ARGUMENT, "query_heads %d is not a multiple of kv_heads %d",
+                    query_heads, heads);
     if (layers < 1 || heads < 1 || head_dim < 1 || page_size < 1 || max_context < 1 || pages < 0)
         return fail(PKV_ERR_INVALID_ARGUMENT,
                     "bad geometry: layers=%d heads=%d head_dim=%d page_size=%d max_context=%lld "
@@ -156,16 +198,19 @@ int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page
         if (page_size % pkv::kTile != 0)
             return fail(PKV_ERR_UNSUPPORTED, "page_size %d is not a multiple of %d", page_size,
                         pkv::kTile);
-        if (!pkv::decode_supported(dtype, head_dim))
+        if (!pkv::decode_supported(dtype, head_dim, query_heads / heads))
             return fail(PKV_ERR_UNSUPPORTED,
-                        "head_dim %d not implemented (powers of two, 2..128 fp32, 2..256 bf16)",
-                        head_dim);
+                        "head_dim %d with %d query heads per KV head not implemented (powers of "
+                        "two, 2..128 fp32, 2..256 bf16; groups of 2, 4, 8 at head_dim 64, 128)",
+                        head_dim, query_heads / heads);
     }
 
     pkv_pool* p = new (std::nothrow) pkv_pool;
     if (!p) return fail(PKV_ERR_OUT_OF_MEMORY, "host allocation failed");
     p->layers = layers;
     p->heads = heads;
+    p->query_heads = query_heads;
+    p->group = query_heads / heads;
     p->head_dim = head_dim;
     p->page_size = page_size;
     p->dtype = dtype;
@@ -192,7 +237,7 @@ int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page
             delete p;
             return cuda_fail(e, "device query");
         }
-        p->workers = pkv::resident_workers(dtype, head_dim, sms);
+        p->workers = pkv::resident_workers(dtype, head_dim, p->group, sms);
         if (p->workers <= 0) {
             delete p;
             return fail(PKV_ERR_CUDA, "split kernel cannot be resident on this device");
@@ -249,6 +294,13 @@ int pkv_pool_kv_ptr(const pkv_pool* p, int layer, void** k_pages, void** v_pages
     return ok();
 }
 
+int pkv_pool_heads(const pkv_pool* p, int* kv_heads, int* query_heads) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if (kv_heads) *kv_heads = p->heads;
+    if (query_heads) *query_heads = p->query_heads;
+    return ok();
+}
+
 int pkv_pool_bytes(const pkv_pool* p, uint64_t* bytes) {
     if (!p || !bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
     *bytes = 2ull * (uint64_t)p->layers * (uint64_t)p->pages * (uint64_t)p->page_size *
@@ -289,7 +341,7 @@ int pkv_request_create(pkv_pool* p, pkv_request** out) {
         r->workspace_workers =
             pkv::launch_workers(p->workers, 1, p->heads, p->max_context);
         r->workspace_bytes =
-            pkv::workspace_layout(1, p->heads, p->head_dim, r->workspace_workers).total;
+            pkv::workspace_layout(1, p->heads, p->head_dim, r->workspace_workers, p->group).total;
         cudaError_t e = cudaMalloc(&r->dev_table, sizeof(int32_t) * (size_t)p->max_pages_per_request);
         if (e == cudaSuccess) e = cudaMalloc(&r->dev_workspace, r->workspace_bytes);
         if (e == cudaSuccess) e = cudaMemset(r->dev_workspace, 0, r->workspace_bytes);
@@ -421,6 +473,7 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.dtype = p->dtype;
     a.B = 1;
     a.H = p->heads;
+    a.G = p->group;
     a.D = p->head_dim;
     a.P = p->page_size;
     a.q = q;
@@ -468,7 +521,7 @@ int pkv_commit_token(pkv_request* r) {
     r->length = t;
     r->counters.committed_tokens += 1;
     r->counters.cache_appends += p->layers;
-    r->counters.score_cells += (int64_t)p->layers * p->heads * t;
+    r->counters.score_cells += (int64_t)p->layers * p->query_heads * t;
     r->pending = false;
     r->leased_by_begin = false;
     return ok();
@@ -492,7 +545,7 @@ int pkv_workspace_size(const pkv_pool* p, int batch, int64_t max_seq_len, size_t
     if (batch < 0 || max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "bad batch or length");
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     const int w = pkv::launch_workers(p->workers, batch, p->heads, max_seq_len);
-    *bytes = pkv::workspace_layout(batch, p->heads, p->head_dim, w).total;
+    *bytes = pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
     return ok();
 }
 
@@ -513,7 +566,7 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
     const int w = pkv::launch_workers(p->workers, batch, p->heads, max_seq_len);
-    const size_t need = pkv::workspace_layout(batch, p->heads, p->head_dim, w).total;
+    const size_t need = pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
                     need);
@@ -523,6 +576,7 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     a.dtype = p->dtype;
     a.B = batch;
     a.H = p->heads;
+    a.G = p->group;
     a.D = p->head_dim;
     a.P = p->page_size;
     a.q = q;
@@ -610,10 +664,11 @@ int prepare_batched(pkv_pool* p, int layer, int batch, const float* q, const voi
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
     const int w = launch_workers(p->workers, batch, p->heads, max_seq_len);
-    *workspace_bytes = workspace_layout(batch, p->heads, p->head_dim, w).total;
+    *workspace_bytes = workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
     a->dtype = p->dtype;
     a->B = batch;
     a->H = p->heads;
+    a->G = p->group;
     a->D = p->head_dim;
     a->P = p->page_size;
     a->q = q;

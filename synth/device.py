@@ -17,17 +17,20 @@ TORCH_STORAGE = {F32: torch.float32, 1: torch.bfloat16}
 
 
 def step_inputs(w: Workload, layer: int = 0):
-    """Host arrays of one batched step: q [B,H,D] fp32, k_new / v_new [B,H,D] storage
-    dtype (token t_b - 1 of each request's key / value sequence)."""
+    """Host arrays of one batched step: q [B,HQ,D] fp32 (HQ = H x group query heads),
+    k_new / v_new [B,H,D] storage dtype (token t_b - 1 of each request's key / value
+    sequence)."""
     B, H, D = w.B, w.H, w.D
+    HQ = H * getattr(w, "group", 1)
     sd = np.float32 if w.dtype == F32 else np.uint16
-    q = np.empty((B, H, D), np.float32)
+    q = np.empty((B, HQ, D), np.float32)
     k = np.empty((B, H, D), sd)
     v = np.empty((B, H, D), sd)
     for b in range(B):
         t = int(w.seq_lens[b])
+        for qh in range(HQ):
+            q[b, qh] = rows(w.seed, Q, layer, b, qh, t - 1, 1, D, F32)[0]
         for h in range(H):
-            q[b, h] = rows(w.seed, Q, layer, b, h, t - 1, 1, D, F32)[0]
             k[b, h] = rows(w.seed, KHIST, layer, b, h, t - 1, 1, D, w.dtype)[0]
             v[b, h] = rows(w.seed, VHIST, layer, b, h, t - 1, 1, D, w.dtype)[0]
     return q, k, v

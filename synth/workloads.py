@@ -30,6 +30,11 @@ class Workload:
     seed: int
     seq_lens: np.ndarray   # [B] int32, retained length t_b including the new token
     churn_cycles: int = 0  # seeded lease/release cycles before the final tables are leased
+    group: int = 1         # query heads per KV head (H is the number of KV heads)
+
+    @property
+    def HQ(self) -> int:
+        return self.H * self.group
 
     @property
     def n_pages(self) -> np.ndarray:
@@ -92,6 +97,15 @@ def churn_ops(w: Workload, max_count: int = 64):
     return [(int(r), int(o), int(c) if o == LEASE else 0) for r, o, c in zip(req, op, cnt)]
 
 
+def gqa(group: int = 8, dtype: int = BF16, seed: int = 5, B: int = 64, t_max: int = 8192) -> Workload:
+    """Grouped-query decode: 64 requests, 8 KV heads x `group` query heads, d_h=128,
+    t ~ U{1..8192}, pool of 32768 shuffled pages."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, t_max + 1, size=B).astype(np.int32)
+    name = f"gqa{group}_" + ("f32" if dtype == F32 else "bf16")
+    return Workload(name, B, 1, 8, 128, 16, dtype, 32768, t_max, seed, lens, group=group)
+
+
 REGISTRY = {
     "tiny": tiny,
     "single_t128": lambda: single(128),
@@ -101,4 +115,7 @@ REGISTRY = {
     "batched_bf16": lambda: batched(BF16),
     "ragged": ragged,
     "long": long_context,
+    "gqa8_bf16": lambda: gqa(8, BF16),
+    "gqa4_bf16": lambda: gqa(4, BF16),
+    "gqa8_f32": lambda: gqa(8, F32),
 }

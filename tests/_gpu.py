@@ -45,9 +45,10 @@ class BatchedRun:
         self.w = w
         self.layer = layer
         self.pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dtype_name(w.dtype),
-                             w.max_context, w.seed)
+                             w.max_context, w.seed, query_heads=w.HQ)
         self.opool = OraclePool(w.layers, w.pool_pages, w.H, w.D, w.P, w.dtype,
-                                max_context=w.max_context, seed=w.seed, storage=False)
+                                max_context=w.max_context, seed=w.seed, storage=False,
+                                query_heads=w.HQ)
         self.reqs = [self.pool.request() for _ in range(w.B)]
         self.oreqs = [self.opool.request() for _ in range(w.B)]
         for r_i, kind, cnt in churn_ops(w) if w.churn_cycles else []:
@@ -79,7 +80,7 @@ class BatchedRun:
         self.dev = dict(q=to_device(self.q), k=to_device(self.k_new), v=to_device(self.v_new),
                         tables=torch.from_numpy(self.tables).cuda(),
                         lens=torch.from_numpy(w.seq_lens.astype(np.int32)).cuda())
-        self.out = torch.full((w.B, w.H, w.D), float("nan"), device="cuda")
+        self.out = torch.full((w.B, w.HQ, w.D), float("nan"), device="cuda")
         self.ws = self.pool.workspace(w.B, self.max_seq_len)
         self.stream = stream
 
@@ -95,7 +96,7 @@ class BatchedRun:
         holding only their pages; tables are the oracle model's own."""
         w = self.w
         requests = list(range(w.B)) if requests is None else list(requests)
-        heads = list(range(w.H)) if heads is None else list(heads)
+        heads = list(range(w.HQ)) if heads is None else list(heads)   # query heads
         npg = [int(w.n_pages[b]) for b in requests]
         compact = {}
         for b, n in zip(requests, npg):
@@ -111,11 +112,11 @@ class BatchedRun:
             t = int(w.seq_lens[b])
             kp[ids] = synth.history_pages(w.seed, KHIST, self.layer, b, n, w.H, w.P, w.D, t - 1, w.dtype)
             vp[ids] = synth.history_pages(w.seed, VHIST, self.layer, b, n, w.H, w.P, w.D, t - 1, w.dtype)
-        lanes = [i * w.H + h for i in range(len(requests)) for h in heads]
+        lanes = [i * w.HQ + h for i in range(len(requests)) for h in heads]
         ref = oracle.paged_decode_attention(kp, vp, self.q[requests], self.k_new[requests],
                                             self.v_new[requests], ctab,
                                             w.seq_lens[requests].astype(np.int32), w.dtype,
-                                            lanes=lanes)
+                                            lanes=lanes, group=w.group)
         return {(b, h): ref[i, h] for i, b in enumerate(requests) for h in heads}
 
     def appended_rows(self, b: int):
@@ -136,7 +137,7 @@ class BatchedRun:
 
 
 def make_workload(name, seq_lens, H, D, P=16, dtype=F32, pool_pages=None, seed=0, layers=1,
-                  max_context=None, churn=0) -> Workload:
+                  max_context=None, churn=0, group=1) -> Workload:
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     n = (seq_lens.astype(np.int64) + P - 1) // P
     if pool_pages is None:
@@ -144,4 +145,4 @@ def make_workload(name, seq_lens, H, D, P=16, dtype=F32, pool_pages=None, seed=0
     if max_context is None:
         max_context = int(max(seq_lens.max(), 1))
     return Workload(name, len(seq_lens), layers, H, D, P, dtype, int(pool_pages), int(max_context),
-                    seed, seq_lens, churn_cycles=churn)
+                    seed, seq_lens, churn_cycles=churn, group=group)

@@ -34,20 +34,22 @@ def _host(t: torch.Tensor, dtype: int) -> np.ndarray:
 
 # ------------------------------------------------------------ transactional --
 
-def _lane_tensors(seed, layer, H, pos, D, dtype, kseed=None):
+def _lane_tensors(seed, layer, H, pos, D, dtype, kseed=None, group=1):
     kseed = seed if kseed is None else kseed
-    q = synth.lane_rows(seed, Q, layer, 0, H, pos, D, F32)
+    q = synth.lane_rows(seed, Q, layer, 0, H * group, pos, D, F32)
     k = synth.lane_rows(kseed, KHIST, layer, 0, H, pos, D, dtype)
     v = synth.lane_rows(kseed, VHIST, layer, 0, H, pos, D, dtype)
     return q, k, v
 
 
 def _serial(layers, H, D, dtype, pool_pages, max_context, steps, seed, abort_at=None,
-            check_at=None, P=16):
+            check_at=None, P=16, group=1):
     """Serial begin / append x layers / commit on the library and on the oracle model."""
-    pool = pkv.Pool(layers, pool_pages, H, D, P, dtype_name(dtype), max_context, seed)
+    pool = pkv.Pool(layers, pool_pages, H, D, P, dtype_name(dtype), max_context, seed,
+                    query_heads=H * group)
     req = pool.request()
-    opool = OraclePool(layers, pool_pages, H, D, P, dtype, max_context=max_context, seed=seed)
+    opool = OraclePool(layers, pool_pages, H, D, P, dtype, max_context=max_context, seed=seed,
+                       query_heads=H * group)
     oreq = opool.request()
     errs = []
     for t in range(1, steps + 1):
@@ -55,7 +57,7 @@ def _serial(layers, H, D, dtype, pool_pages, max_context, steps, seed, abort_at=
         assert pos == oreq.begin_token() == t - 1
         if abort_at is not None and t == abort_at:
             for layer in range(layers - 1):
-                q, k, v = _lane_tensors(seed, layer, H, pos, D, dtype, kseed=seed + 99)
+                q, k, v = _lane_tensors(seed, layer, H, pos, D, dtype, kseed=seed + 99, group=group)
                 req.append_and_attend(layer, to_device(q), to_device(k),
                                       to_device(v))
                 oreq.append_and_attend(layer, q, k, v, compute=False)
@@ -67,7 +69,7 @@ def _serial(layers, H, D, dtype, pool_pages, max_context, steps, seed, abort_at=
             assert req.begin_token() == oreq.begin_token() == pos
         compute = check_at is None or t in check_at
         for layer in range(layers):
-            q, k, v = _lane_tensors(seed, layer, H, pos, D, dtype)
+            q, k, v = _lane_tensors(seed, layer, H, pos, D, dtype, group=group)
             out = req.append_and_attend(layer, to_device(q), to_device(k),
                                         to_device(v))
             ref = oreq.append_and_attend(layer, q, k, v, compute=compute)
@@ -280,3 +282,41 @@ def test_argument_errors_change_nothing():
         assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
     finally:
         run.close()
+
+
+# ------------------------------------------------------------ grouped query --
+
+@pytest.mark.parametrize("group,D,dtype", [(2, 64, F32), (4, 64, BF16), (8, 64, F32),
+                                           (2, 128, BF16), (4, 128, F32), (8, 128, BF16),
+                                           (8, 128, F32)])
+def test_gqa_batched(group, D, dtype):
+    lens = [1, 16, 17, 300, 1000, 33, 2048, 5]
+    _batched_check(make_workload(f"gqa{group}", lens, 2, D, dtype=dtype, seed=40 + group,
+                                 group=group))
+
+
+def test_gqa_full_config_every_lane():
+    """64 requests, 8 KV heads x 8 query heads, d_h=128, bf16, t ~ U{1..8192}."""
+    _batched_check(workloads.gqa(8))
+
+
+def test_gqa_serial_with_abort():
+    c, _ = _serial(2, 2, 64, BF16, 64, 200, 40, 7, abort_at=17, group=4)
+    assert c["score_cells"] == 2 * 8 * sum(range(1, 41))
+
+
+def test_gqa_more_workers_than_tiles():
+    _batched_check(make_workload("gqa_few", [40, 3], 1, 128, dtype=BF16, seed=46, group=8,
+                                 max_context=8192), max_seq_len=8192)
+
+
+def test_gqa_geometry_errors():
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.Pool(1, 8, 2, 64, 16, "bf16", 64, query_heads=6)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.Pool(1, 8, 4, 64, 16, "bf16", 64, query_heads=6)
+    assert e.value.status == pkv.PKV_ERR_INVALID_ARGUMENT
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.Pool(1, 8, 2, 32, 16, "bf16", 64, query_heads=4)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED

@@ -15,7 +15,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "attention.c")
 MUTANTS = {
     "scale_dropped": ("const double scale = 1.0 / sqrt((double)D);", "const double scale = 1.0;"),
     "scale_squared": ("const double scale = 1.0 / sqrt((double)D);", "const double scale = 1.0 / D;"),
-    "new_key_excluded": ("seq_lens[b], h, scores,", "seq_lens[b] - 1 + (seq_lens[b] == 1), h, scores,"),
+    "new_key_excluded": ("seq_lens[b], qh / group,", "seq_lens[b] - 1 + (seq_lens[b] == 1), qh / group,"),
+    "group_head_map": ("seq_lens[b], qh / group,", "seq_lens[b], qh % H,"),
     "slot_index": ("int64_t off = pool_offset(page, h, j % P, H, P, D);",
                    "int64_t off = pool_offset(page, h, (j + 1) % P, H, P, D);"),
     "page_index": ("int64_t page = table[j / P];\n        if", "int64_t page = table[j / (P + 1)];\n        if"),
@@ -34,6 +35,8 @@ MUTANTS = {
 def _pins_pass(lib) -> bool:
     """The pins of test_oracle_pins, run against one library."""
     try:
+        if not _gqa_pin_passes(lib):
+            return False
         for lens, H, D, P, dtype in [([5, 17, 33], 2, 2, 16, F32), ([31, 48, 2], 2, 8, 16, BF16),
                                      ([1], 2, 4, 16, F32)]:
             case = PagedCase(lens, H, D, P, dtype, seed=11)
@@ -53,6 +56,18 @@ def _pins_pass(lib) -> bool:
     except (ValueError, FloatingPointError):
         return False
     return True
+
+
+def _gqa_pin_passes(lib) -> bool:
+    """Grouped-query attention equals multi-head attention on KV heads repeated."""
+    from tests.test_oracle_pins import gqa_case
+    case, q, group, kp_rep, vp_rep, knew_rep, vnew_rep = gqa_case(group=2)
+    kp, vp = case.k_pool.copy(), case.v_pool.copy()
+    a = oracle.paged_decode_attention(kp, vp, q, case.k_new, case.v_new, case.tables,
+                                      case.seq_lens, case.dtype, library=lib, group=group)
+    b = oracle.paged_decode_attention(kp_rep, vp_rep, q, knew_rep, vnew_rep, case.tables,
+                                      case.seq_lens, case.dtype, library=lib)
+    return np.allclose(a, b, rtol=0, atol=1e-12)
 
 
 def _compile(tmp_path, name, text):

@@ -326,3 +326,52 @@ def test_bf16_decode_matches_torch():
     out = oracle.paged_decode_attention(kp, vp, np.zeros((1, 1, 8), np.float32), k_new, v_new,
                                         np.zeros((1, 1), np.int32), np.array([1], np.int32), BF16)
     assert np.array_equal(out[0, 0], to_f64(bits, BF16))
+
+
+# ---------------------------------------------------------------------------
+# grouped-query attention
+
+
+def gqa_case(group=2, H=2, D=8, dtype=F32, lens=(23, 5, 40), seed=14):
+    """A paged case with H KV heads plus a [B, H*group, D] query, and the same pools
+    with every KV head repeated group times (a multi-head layout of the same data)."""
+    case = PagedCase(list(lens), H, D, 16, dtype, seed=seed)
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((case.B, H * group, D)).astype(np.float32)
+    rep = lambda x, axis: np.repeat(x, group, axis=axis)       # noqa: E731
+    return (case, q, group, np.ascontiguousarray(rep(case.k_pool, 1)),
+            np.ascontiguousarray(rep(case.v_pool, 1)), np.ascontiguousarray(rep(case.k_new, 1)),
+            np.ascontiguousarray(rep(case.v_new, 1)))
+
+
+@pytest.mark.parametrize("group,dtype", [(2, F32), (4, BF16), (8, F32)])
+def test_gqa_equals_mha_on_repeated_kv_heads(group, dtype):
+    case, q, g, kp_rep, vp_rep, knew_rep, vnew_rep = gqa_case(group, dtype=dtype)
+    kp, vp = case.k_pool.copy(), case.v_pool.copy()
+    a = oracle.paged_decode_attention(kp, vp, q, case.k_new, case.v_new, case.tables,
+                                      case.seq_lens, dtype, group=g)
+    b = oracle.paged_decode_attention(kp_rep, vp_rep, q, knew_rep, vnew_rep, case.tables,
+                                      case.seq_lens, dtype)
+    assert np.array_equal(a, b)
+
+
+def test_gqa_matches_dense_causal_per_query_head():
+    group, H, D = 4, 2, 8
+    case, q, g, *_ = gqa_case(group, H=H, D=D)
+    out = oracle.paged_decode_attention(case.k_pool.copy(), case.v_pool.copy(), q, case.k_new,
+                                        case.v_new, case.tables, case.seq_lens, F32, group=group)
+    for b, t in enumerate(case.seq_lens):
+        for qh in range(H * group):
+            lane = b * H + qh // group
+            Q = np.zeros((t, D))
+            Q[-1] = q[b, qh]
+            ref, _ = dense_causal_last_row(Q, to_f64(case.K[lane], F32), to_f64(case.V[lane], F32))
+            np.testing.assert_allclose(out[b, qh], ref, rtol=0, atol=1e-12)
+
+
+def test_group_one_is_multi_head():
+    case = PagedCase([30, 7], 3, 8, 16, F32, seed=15)
+    a, _, _ = run_oracle(case)
+    b = oracle.paged_decode_attention(case.k_pool.copy(), case.v_pool.copy(), case.q, case.k_new,
+                                      case.v_new, case.tables, case.seq_lens, F32, group=1)
+    assert np.array_equal(a, b)
