@@ -216,14 +216,14 @@ def measured_traffic(workload: str):
 
 # ------------------------------------------------------------ the GPU arm --
 
-def setup_device(w, torch):
+def setup_device(w, torch, cuda_cores=False):
     """Pool, tables from the library's allocator, history in HBM, step inputs on device."""
     import paged_kv_cache_decode_gb300 as pkv
     from synth.device import fill_history, step_inputs, to_device
     from synth.workloads import churn_ops, LEASE
 
     pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "f32" if w.elem_bytes == 4 else "bf16",
-                    w.max_context, w.seed, query_heads=w.HQ)
+                    w.max_context, w.seed, query_heads=w.HQ, cuda_cores=cuda_cores)
     reqs = [pool.request() for _ in range(w.B)]
     for r_i, kind, cnt in (churn_ops(w) if w.churn_cycles else []):
         try:
@@ -257,7 +257,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     rank, world = dist_init("nccl")
     w = make_workload(args.workload, rank, args.requests)
-    pool, reqs, host, dev, ws, out, max_seq_len = setup_device(w, torch)
+    pool, reqs, host, dev, ws, out, max_seq_len = setup_device(w, torch, args.cuda_cores)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -336,6 +336,7 @@ def run_gpu(args):
         sampler.stop()
 
     alg = algorithmic_bytes(w)
+    kernel_name = pool.kernel_name()
     line = None
     if rank == 0:
         peak, peak_kind = measured_peak_hbm()
@@ -360,7 +361,7 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": measured_traffic(w.name),
-                         "kernel": f"split_decode_kernel<{'bf16' if w.elem_bytes == 2 else 'f32'},{w.D}>",
+                         "kernel": kernel_name,
                          "kernel_ms": round(kernel_ms, 5), "peak_kind": peak_kind + " (hbm_gbs copy)"},
             "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
@@ -482,6 +483,7 @@ def run_gpu_serial(args):
     if sampler:
         sampler.stop()
     alg = token_bytes(w, t)
+    kernel_name = pool.kernel_name()
     layer_alg = alg // w.layers
     h2d = sum(x.numel() * x.element_size() for layer in hin for x in layer)
     line = None
@@ -506,7 +508,7 @@ def run_gpu_serial(args):
             "tokens_per_s": round(world / (tok_ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": f"split_decode_kernel<{'bf16' if w.elem_bytes == 2 else 'f32'},{w.D},{w.group}>",
+                         "kernel": kernel_name,
                          "kernel_ms": round(kernel_ms, 5), "peak_kind": peak_kind + " (hbm_gbs copy)",
                          "note": "one layer's split kernel; latency-bound at this size"},
             "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
@@ -621,6 +623,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="long")
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="CUDA-core kernel even where the tensor-core kernel applies")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests (small profiling captures)")
     return ap.parse_args(argv)

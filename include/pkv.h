@@ -75,6 +75,10 @@ typedef enum pkv_dtype {
 #define PKV_POOL_HOST_ONLY 1u   /* bookkeeping only: free list, tables, transactions; no device
                                    storage, so append/attend entry points return PKV_ERR_NO_STORAGE */
 
+#define PKV_POOL_CUDA_CORES 2u  /* use the CUDA-core kernel even where the tensor-core kernel
+                                   applies (bf16 storage, head_dim 64 or 128, 2, 4 or 8 query
+                                   heads per KV head) */
+
 /* bits of the device error word */
 #define PKV_DEVERR_SEQ_LEN 1u   /* a seq_len < 1, > max_seq_len, or needing > max_pages pages */
 #define PKV_DEVERR_PAGE_ID 2u   /* a page-table entry outside [0, pages) */
@@ -130,7 +134,7 @@ int pkv_pool_options_init(pkv_pool_options* options);
  *   seed:        free-list order: a FIFO queue initialised to a Fisher-Yates
  *                shuffle of 0..pages-1 driven by SplitMix64(seed), swap index
  *                next() mod (i + 1) for i = pages-1 down to 1.
- *   flags:       0, or PKV_POOL_HOST_ONLY.
+ *   flags:       0, or PKV_POOL_HOST_ONLY and/or PKV_POOL_CUDA_CORES.
  * Supported by the kernels: head_dim a power of two, 2 <= head_dim <= 128 for
  * PKV_F32 and <= 256 for PKV_BF16 (else PKV_ERR_UNSUPPORTED, unless HOST_ONLY).
  * Equivalent to pkv_pool_create_ex with kv_heads = query_heads = heads.
@@ -148,6 +152,11 @@ int pkv_pool_create_ex(const pkv_pool_options* options, pkv_pool** out);
 
 /* KV heads stored per page and heads of the query (either pointer may be NULL). */
 int pkv_pool_heads(const pkv_pool* pool, int* kv_heads, int* query_heads);
+
+/* *tensor_cores = 1 if the pool's attention runs the tensor-core kernel (bf16,
+ * head_dim 64 or 128, 2, 4 or 8 query heads per KV head, not
+ * PKV_POOL_CUDA_CORES), 0 for the CUDA-core kernel. */
+int pkv_pool_kernel(const pkv_pool* pool, int* tensor_cores);
 
 /* Free the pool and its device storage.  PKV_ERR_BAD_STATE while any request
  * created from it is alive.  NULL is accepted. */

@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     PKV_OK, PKV_ERR_INVALID_ARGUMENT, PKV_ERR_OUT_OF_PAGES, PKV_ERR_CAPACITY_EXCEEDED,
     PKV_ERR_BAD_STATE, PKV_ERR_OUT_OF_MEMORY, PKV_ERR_CUDA, PKV_ERR_DEVICE_CHECK,
     PKV_ERR_NO_STORAGE, PKV_ERR_UNSUPPORTED, PKV_F32, PKV_BF16, PKV_POOL_HOST_ONLY,
+    PKV_POOL_CUDA_CORES,
     PKV_DEVERR_SEQ_LEN, PKV_DEVERR_PAGE_ID, PKV_DEVERR_TIMEOUT,
 )
 
@@ -89,7 +90,7 @@ class Pool:
 
     def __init__(self, layers: int, pages: int, heads: int, head_dim: int, page_size: int = 16,
                  dtype="f32", max_context: int = 4096, seed: int = 0, host_only: bool = False,
-                 query_heads: int = 0):
+                 query_heads: int = 0, cuda_cores: bool = False):
         self.layers, self.heads, self.head_dim, self.page_size = layers, heads, head_dim, page_size
         self.query_heads = query_heads or heads
         self.dtype = _dtype_code(dtype)
@@ -100,7 +101,8 @@ class Pool:
         check(lib.pkv_pool_options_init(ctypes.byref(o)), "pkv_pool_options_init")
         o.layers, o.pages, o.kv_heads, o.query_heads = layers, pages, heads, self.query_heads
         o.head_dim, o.page_size, o.dtype, o.max_context = head_dim, page_size, self.dtype, max_context
-        o.seed, o.flags = seed & ((1 << 64) - 1), PKV_POOL_HOST_ONLY if host_only else 0
+        o.seed = seed & ((1 << 64) - 1)
+        o.flags = (PKV_POOL_HOST_ONLY if host_only else 0) | (PKV_POOL_CUDA_CORES if cuda_cores else 0)
         h = ctypes.c_void_p()
         check(lib.pkv_pool_create_ex(ctypes.byref(o), ctypes.byref(h)), "pkv_pool_create_ex")
         self._h = h
@@ -128,6 +130,19 @@ class Pool:
             t = torch.as_tensor(_DeviceArray(ptr, shape, typestr), device="cuda")
             out.append(t if self.dtype == PKV_F32 else t.view(torch.bfloat16))
         return tuple(out)
+
+    @property
+    def tensor_cores(self) -> bool:
+        """True if this pool's attention runs the tensor-core kernel."""
+        v = ctypes.c_int()
+        check(lib.pkv_pool_kernel(self.handle, ctypes.byref(v)), "pkv_pool_kernel")
+        return bool(v.value)
+
+    def kernel_name(self) -> str:
+        if self.tensor_cores:
+            return f"split_decode_mma_kernel<{self.head_dim},{self.query_heads // self.heads}>"
+        st = "f32" if self.dtype == PKV_F32 else "bf16"
+        return f"split_decode_kernel<{st},{self.head_dim},{self.query_heads // self.heads}>"
 
     def bytes(self) -> int:
         b = ctypes.c_uint64()

@@ -28,6 +28,7 @@ PKV_ERR_UNSUPPORTED = 9
 PKV_F32 = 0
 PKV_BF16 = 1
 PKV_POOL_HOST_ONLY = 1
+PKV_POOL_CUDA_CORES = 2
 
 PKV_DEVERR_SEQ_LEN = 1
 PKV_DEVERR_PAGE_ID = 2
@@ -59,6 +60,7 @@ SIGNATURES = {
     "pkv_pool_options_init": [_P(pkv_pool_options)],
     "pkv_pool_create_ex": [_P(pkv_pool_options), _P(_vp)],
     "pkv_pool_heads": [_vp, _P(_i), _P(_i)],
+    "pkv_pool_kernel": [_vp, _P(_i)],
     "pkv_pool_destroy": [_vp],
     "pkv_pool_kv_ptr": [_vp, _i, _P(_vp), _P(_vp)],
     "pkv_pool_bytes": [_vp, _P(_u64)],

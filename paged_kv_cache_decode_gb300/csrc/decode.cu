@@ -40,10 +40,12 @@
 // Faults are not raised by trapping: bad lengths and page ids, and waits that
 // run out, set bits of a device error word and the offending work is skipped.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "pkv.h"
 #include "pkv_internal.h"
@@ -789,6 +791,389 @@ split_decode_kernel(const KParams p) {
     }
 }
 
+// ------------------------------------------------- tensor-core split kernel --
+//
+// bf16 storage, head width 64 or 128.  Same workers, partition, ring, fused
+// append, partials and merge as split_decode_kernel; what differs is how a
+// staged tile is consumed.  K and V tiles arrive by TMA tensor loads with the
+// 128-byte swizzle (each 16-row x 64-column box lands as 16 rows of 128 bytes
+// whose 16-byte chunks are XOR-permuted by row), so the ldmatrix reads below
+// hit 32 distinct banks.  Scores S = Q K^T and the mixture O += P V run on
+// mma.sync m16n8k16 (bf16 inputs, fp32 accumulation) with a 16-row A tile:
+// row g holds the bf16 rounding of query g (pre-scaled by log2(e)/sqrt(d_h))
+// and row g + 8 the bf16 rounding of its remainder, so the two partial products
+// sum to the fp32 query's product with ~2^-16 relative error.  The softmax
+// weights P are split the same way for O.  Lane l owns query g = l / 4: its
+// four scores per tile sit in the accumulator fragment, the quad of lanes
+// 4g..4g+3 reduces the tile maximum and sum, and the weights feed the P V
+// product straight from registers.
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D = A B + D, m16n8k16, bf16 x bf16 -> fp32
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// bf16 rounding of (lo, hi) and of the remainders
+__device__ __forceinline__ void split_bf16(float lo, float hi, uint32_t& big, uint32_t& rest) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    big = *reinterpret_cast<const uint32_t*>(&b);
+    rest = pack_bf16(lo - __low2float(b), hi - __high2float(b));
+}
+
+template <int D>
+struct MmaGeo {
+    static constexpr int HALVES = D / 64;                 // 128-byte swizzle boxes per row
+    static constexpr int HALF_BYTES = kTile * 128;        // one box: 16 rows x 128 bytes
+    static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int KSTEPS = D / 16;                 // k-steps of S = Q K^T
+    static constexpr int NB = D / 8;                      // n-blocks of O
+    static constexpr int WARPS = Geo<__nv_bfloat16, D>::WARPS;
+    static constexpr int STAGES = Geo<__nv_bfloat16, D>::STAGES;
+    static constexpr int WARP_SMEM = STAGES * STAGE_BYTES;
+    // stage rings (1024-byte aligned, as the swizzle requires), then mbarriers and page ids
+    static constexpr int CTA_SMEM = 1024 + WARPS * (WARP_SMEM + STAGES * 12);
+    static_assert(D == 64 || D == 128, "tensor-core path: head width 64 or 128");
+    static_assert(CTA_SMEM <= 227 * 1024, "CTA does not fit an SM");
+};
+
+// Byte offset of 16-byte chunk c (0 .. D/8 - 1) of row r in a swizzled tile.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return (uint32_t)((c >> 3) * MmaGeo<64>::HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(MmaGeo<D>::WARPS * 32, 1)
+split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv) {
+    using M = MmaGeo<D>;
+    static_assert(G >= 1 && G <= 8, "at most 8 query heads per KV head");
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t w = (int64_t)blockIdx.x * M::WARPS + warp;
+    if (w >= p.W) return;
+
+    unsigned char* ring = smem + warp * M::WARP_SMEM;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + M::WARPS * M::WARP_SMEM) + warp * M::STAGES;
+    int32_t* stage_page =
+        reinterpret_cast<int32_t*>(smem + M::WARPS * (M::WARP_SMEM + M::STAGES * 8)) +
+        warp * M::STAGES;
+    if (lane == 0) {
+        for (int s = 0; s < M::STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t policy = l2_stream_policy();
+
+    const bool batched = p.seq_lens != nullptr;
+    bool plan_seen = false;
+    if (batched) {
+        pdl_wait_primary();
+        plan_seen = true;
+    }
+
+    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
+    const int64_t begin = (w * T_all) / p.W;
+    const int64_t end = ((w + 1) * T_all) / p.W;
+    const int n_work = (int)(end - begin);
+    if (n_work <= 0) return;
+
+    Cursor cur;
+    {
+        const int b0 = batched ? __ldg(p.worker_req + w) : 0;
+        const int64_t pre = req_prefix_at(p, b0);
+        cur.b = b0;
+        cur.n = (int)(req_prefix_at(p, b0 + 1) - pre);
+        cur.first = (int64_t)p.H * pre;
+        const int64_t local = begin - cur.first;
+        cur.h = (int)(local / cur.n);
+        cur.tile = (int)(local % cur.n);
+        cur.page_idx = cur.tile / p.tiles_per_page;
+        cur.slot0 = (cur.tile - cur.page_idx * p.tiles_per_page) * kTile;
+    }
+    Cursor prod = cur;
+
+    // Producer step (lane 0): stage tile `prod` into stage s, box by box.
+    auto issue = [&](int s) {
+        if (lane != 0) return;
+        const int32_t page = __ldg(p.tables + (int64_t)prod.b * p.max_pages + prod.page_idx);
+        stage_page[s] = page;
+        if (page < 0 || page >= p.n_pages) {
+            atomicOr(p.err, PKV_DEVERR_PAGE_ID);
+            mbar_arrive(&bars[s]);
+            return;
+        }
+        const int y = (int)(((int64_t)page * p.H + prod.h) * p.P + prod.slot0);   // pool row
+        unsigned char* dst = ring + s * M::STAGE_BYTES;
+        mbar_arrive_expect_tx(&bars[s], M::STAGE_BYTES);
+#pragma unroll
+        for (int hf = 0; hf < M::HALVES; ++hf) {
+            tma_load_2d(dst + hf * M::HALF_BYTES, &tmk, hf * 64, y, &bars[s], policy);
+            tma_load_2d(dst + M::TILE_BYTES + hf * M::HALF_BYTES, &tmv, hf * 64, y, &bars[s], policy);
+        }
+    };
+
+    const int prologue = n_work < M::STAGES ? n_work : M::STAGES;
+    for (int s = 0; s < prologue; ++s) {
+        issue(s);
+        cursor_advance(prod, p);
+    }
+
+    const int g = lane >> 2, t = lane & 3;     // fragment row group and column pair
+    const bool q_ok = g < G;                    // lanes with g >= G carry zero queries
+    // ldmatrix row addresses: matrix j = lane / 8, row r = lane % 8
+    const int mj = lane >> 3, mr = lane & 7;
+
+    uint32_t qa[M::KSTEPS][4];                  // A fragments of [q_hi; q_lo]
+    float o[M::NB][4];                          // O accumulator fragments
+    float m = -INFINITY, l = 0.f;               // running max and this lane's share of the sum
+    int piece_first = 0, t_b = 0;
+    int s = 0;
+    uint32_t parity = 0;
+
+    for (int k = 0; k < n_work; ++k) {
+        const int64_t lane_id = (int64_t)cur.b * p.H + cur.h;
+
+        if (k == 0 || cur.tile == 0) {   // a new lane piece starts
+            piece_first = cur.tile;
+            t_b = (int)seq_len_at(p, cur.b);
+            const float* qp = p.q + (lane_id * G + (q_ok ? g : 0)) * D;
+#pragma unroll
+            for (int ks = 0; ks < M::KSTEPS; ++ks) {
+                const float2 lo = *reinterpret_cast<const float2*>(qp + ks * 16 + 2 * t);
+                const float2 hi = *reinterpret_cast<const float2*>(qp + ks * 16 + 8 + 2 * t);
+                uint32_t b0, r0, b1, r1;
+                split_bf16(lo.x * p.qscale, lo.y * p.qscale, b0, r0);
+                split_bf16(hi.x * p.qscale, hi.y * p.qscale, b1, r1);
+                qa[ks][0] = q_ok ? b0 : 0u;   // row g,     k = 2t, 2t+1
+                qa[ks][1] = q_ok ? r0 : 0u;   // row g + 8
+                qa[ks][2] = q_ok ? b1 : 0u;   // row g,     k = 2t+8, 2t+9
+                qa[ks][3] = q_ok ? r1 : 0u;   // row g + 8
+            }
+#pragma unroll
+            for (int nb = 0; nb < M::NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+            m = -INFINITY;
+            l = 0.f;
+        }
+
+        if (!mbar_wait_bounded(&bars[s], parity, kWaitLimitNs)) {
+            if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+            const int last = (k + M::STAGES - 1 < n_work - 1) ? k + M::STAGES - 1 : n_work - 1;
+            int s2 = s;
+            uint32_t par2 = parity;
+            for (int j = k + 1; j <= last; ++j) {
+                if (++s2 == M::STAGES) {
+                    s2 = 0;
+                    par2 ^= 1u;
+                }
+                mbar_wait_bounded(&bars[s2], par2, kWaitLimitNs);
+            }
+            return;
+        }
+
+        unsigned char* Ks = ring + s * M::STAGE_BYTES;
+        unsigned char* Vs = Ks + M::TILE_BYTES;
+        const int32_t page = stage_page[s];
+        const bool page_ok = page >= 0 && page < p.n_pages;
+        const bool last_tile = cur.tile == cur.n - 1;
+        const int rem = t_b - cur.tile * kTile;
+        const int rows = !page_ok ? 0 : (rem < kTile ? rem : kTile);
+
+        if (last_tile && page_ok) {
+            // fused append: row t_b - 1 from k_new / v_new into the tile and the page;
+            // rows past it (stale bytes, possibly not finite) are cleared in V
+            const int r = rows - 1;
+            if (lane < D / 8) {
+                const int64_t src = lane_id * D + lane * 8;
+                const uint4 kb = *reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.k_new) + src);
+                const uint4 vb = *reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.v_new) + src);
+                *reinterpret_cast<uint4*>(Ks + swz(r, lane)) = kb;
+                *reinterpret_cast<uint4*>(Vs + swz(r, lane)) = vb;
+                const int64_t dst = (((int64_t)page * p.H + cur.h) * p.P + cur.slot0 + r) * D + lane * 8;
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.k_pages) + dst) = kb;
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.v_pages) + dst) = vb;
+            }
+            for (int i = lane; i < (kTile - rows) * (D / 8); i += 32) {
+                const int rr = rows + i / (D / 8), c = i % (D / 8);
+                *reinterpret_cast<uint4*>(Vs + swz(rr, c)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        if (rows > 0) {
+            // S = [q_hi; q_lo] K^T : two 16 x 8 blocks (keys 0-7, 8-15)
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kbase = smem_u32(Ks);
+#pragma unroll
+            for (int ks = 0; ks < M::KSTEPS; ++ks) {
+                // matrices: (keys 0-7, chunk 2ks), (keys 0-7, 2ks+1), (keys 8-15, 2ks), (keys 8-15, 2ks+1)
+                const int key = ((mj >> 1) << 3) + mr;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kbase + swz(key, 2 * ks + (mj & 1)), b0, b1, b2, b3);
+                mma_bf16(sa, qa[ks], b0, b1);
+                mma_bf16(sb, qa[ks], b2, b3);
+            }
+            // scores of query g at keys 2t, 2t+1 (block a) and 8+2t, 9+2t (block b)
+            float sc[4] = {sa[0] + sa[2], sa[1] + sa[3], sb[0] + sb[2], sb[1] + sb[3]};
+            const int keys[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (!q_ok || keys[i] >= rows) sc[i] = -INFINITY;
+                tmax = fmaxf(tmax, sc[i]);
+            }
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+            const float m_new = q_ok ? fmaxf(m, tmax) : 0.f;
+            const float alpha = q_ok ? exp2f(m - m_new) : 1.f;
+            float pw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pw[i] = q_ok ? exp2f(sc[i] - m_new) : 0.f;
+            l = fmaf(l, alpha, (pw[0] + pw[1]) + (pw[2] + pw[3]));
+            m = q_ok ? m_new : m;
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int nb = 0; nb < M::NB; ++nb) {
+                    o[nb][0] *= alpha;
+                    o[nb][1] *= alpha;
+                    o[nb][2] *= alpha;
+                    o[nb][3] *= alpha;
+                }
+            }
+            // A fragment of [P_hi; P_lo] over the 16 keys
+            uint32_t pa[4];
+            split_bf16(pw[0], pw[1], pa[0], pa[1]);
+            split_bf16(pw[2], pw[3], pa[2], pa[3]);
+            // O += [P_hi; P_lo] V : V[key][dim] as the k x n operand, transposed on load
+            const uint32_t vbase = smem_u32(Vs);
+#pragma unroll
+            for (int np = 0; np < M::NB / 2; ++np) {
+                // matrices: (keys 0-7, chunk 2np), (keys 8-15, 2np), (keys 0-7, 2np+1), (keys 8-15, 2np+1)
+                const int key = ((mj & 1) << 3) + mr;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(vbase + swz(key, 2 * np + (mj >> 1)), b0, b1, b2, b3);
+                mma_bf16(o[2 * np], pa, b0, b1);
+                mma_bf16(o[2 * np + 1], pa, b2, b3);
+            }
+        }
+
+        // the stage is free again: hand it to the copy engine for tile k + STAGES
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (k + M::STAGES < n_work) {
+            issue(s);
+            cursor_advance(prod, p);
+        }
+        if (++s == M::STAGES) {
+            s = 0;
+            parity ^= 1u;
+        }
+
+        if (last_tile || k == n_work - 1) {
+            // close the lane piece: quad sum of l; rows g and g + 8 of O add up
+            float lt = l;
+            lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+            lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+            if (piece_first == 0 && last_tile) {
+                if (q_ok) {
+                    const float inv = 1.f / lt;
+                    float* op = p.out + (lane_id * G + g) * D + 2 * t;
+#pragma unroll
+                    for (int nb = 0; nb < M::NB; ++nb)
+                        *reinterpret_cast<float2*>(op + nb * 8) =
+                            make_float2((o[nb][0] + o[nb][2]) * inv, (o[nb][1] + o[nb][3]) * inv);
+                }
+            } else {
+                const int64_t slot = lane_id + w;
+                if (q_ok) {
+                    float* op = p.part_o + (slot * G + g) * D + 2 * t;
+#pragma unroll
+                    for (int nb = 0; nb < M::NB; ++nb)
+                        *reinterpret_cast<float2*>(op + nb * 8) =
+                            make_float2(o[nb][0] + o[nb][2], o[nb][1] + o[nb][3]);
+                    if (t == 0) p.part_ml[slot * G + g] = make_float2(m, lt);
+                }
+                __threadfence();
+                __syncwarp();
+                const int64_t A = cur.first + (int64_t)cur.h * cur.n;
+                const int64_t w_lo = worker_of(A, T_all, p.W);
+                const int64_t w_hi = worker_of(A + cur.n - 1, T_all, p.W);
+                int need;
+                if (T_all >= p.W) {
+                    need = (int)(w_hi - w_lo + 1);
+                } else {
+                    int c = 0;
+                    for (int64_t x = w_lo + lane; x <= w_hi; x += 32)
+                        c += (x * T_all) / p.W != ((x + 1) * T_all) / p.W;
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                    need = c;
+                }
+                int arrived = 0;
+                if (p.epoch == 0) {
+                    if (!plan_seen) {
+                        pdl_wait_primary();
+                        plan_seen = true;
+                    }
+                    if (lane == 0) arrived = (int)atomicAdd(&p.lane_cnt[lane_id], 1ull) + 1;
+                } else if (lane == 0) {
+                    unsigned long long* c = &p.lane_cnt[lane_id];
+                    atomicMax(c, (unsigned long long)p.epoch << 32);
+                    arrived = (int)((atomicAdd(c, 1ull) & 0xffffffffull) + 1);
+                }
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == need) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int gg = 0; gg < G; ++gg)
+                        merge_query<D, Geo<__nv_bfloat16, D>::DPL, G>(p, lane_id, gg, w_lo, w_hi,
+                                                                      T_all, lane);
+                }
+                __syncwarp();
+            }
+        }
+        cursor_advance(cur, p);
+    }
+}
+
 // ------------------------------------------------------------------ host --
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -872,6 +1257,65 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     return cudaSuccess;
 }
 
+template <int D, int G>
+static cudaError_t prepare_mma() {
+    static bool done = false;   // per instantiation
+    if (done) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(split_decode_mma_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         MmaGeo<D>::CTA_SMEM);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
+template <int D, int G>
+static int resident_workers_mma(int num_sms) {
+    if (prepare_mma<D, G>() != cudaSuccess) return 0;
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_mma_kernel<D, G>,
+                                                      MmaGeo<D>::WARPS * 32, MmaGeo<D>::CTA_SMEM) !=
+        cudaSuccess)
+        return 0;
+    return blocks * num_sms * MmaGeo<D>::WARPS;
+}
+
+template <int D, int G>
+static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stream) {
+    using M = MmaGeo<D>;
+    cudaError_t e = prepare_mma<D, G>();
+    if (e != cudaSuccess) return e;
+    if (p.epoch == 0) {
+        plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+    CUtensorMap tmk, tmv;
+    memcpy(&tmk, a.tmap_k, sizeof tmk);
+    memcpy(&tmv, a.tmap_v, sizeof tmv);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((p.W + M::WARPS - 1) / M::WARPS));
+    cfg.blockDim = dim3(M::WARPS * 32);
+    cfg.dynamicSmemBytes = M::CTA_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.epoch == 0 ? 1 : 0;
+    if ((e = cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<D, G>, p, tmk, tmv)) != cudaSuccess)
+        return e;
+    if (a.ev_after && (e = cudaEventRecord(a.ev_after, stream)) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+// The tensor-core kernel serves grouped-query pools; for one query head per KV
+// head the CUDA-core kernel is as fast (measured on GB300) and is kept.
+#define PKV_FOR_EACH_MMA(X) X(64, 2) X(64, 4) X(64, 8) X(128, 2) X(128, 4) X(128, 8)
+
+bool mma_supported(int dtype, int D, int G) {
+    return dtype == PKV_BF16 && (D == 64 || D == 128) && (G == 2 || G == 4 || G == 8);
+}
+
 // Instantiated geometries: every head width for multi-head attention; groups
 // of 2, 4 and 8 query heads per KV head at head widths 64 and 128.
 #define PKV_FOR_EACH_D(X, T) X(T, 2, 1) X(T, 4, 1) X(T, 8, 1) X(T, 16, 1) X(T, 32, 1) \
@@ -885,7 +1329,14 @@ bool decode_supported(int dtype, int D, int G) {
     return (G == 2 || G == 4 || G == 8) && (D == 64 || D == 128);
 }
 
-int resident_workers(int dtype, int D, int G, int num_sms) {
+int resident_workers(int dtype, int D, int G, int num_sms, bool tensor_cores) {
+    if (tensor_cores) {
+#define PKV_RWM(DD, GG) \
+        if (D == DD && G == GG) return resident_workers_mma<DD, GG>(num_sms);
+        PKV_FOR_EACH_MMA(PKV_RWM)
+#undef PKV_RWM
+        return 0;
+    }
 #define PKV_RW(T, DD, GG) \
     if (D == DD && G == GG) return resident_workers_t<T, DD, GG>(num_sms);
     if (dtype == PKV_F32) {
@@ -927,6 +1378,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.part_o = reinterpret_cast<float*>(ws + L.part_o);
     p.W = a.workers;
     p.err = a.dev_error;
+    if (a.tmap_k != nullptr && a.tmap_v != nullptr) {
+#define PKV_LAUNCH_MMA(DD, GG) \
+        if (a.D == DD && a.G == GG) return launch_mma<DD, GG>(a, p, stream);
+        PKV_FOR_EACH_MMA(PKV_LAUNCH_MMA)
+#undef PKV_LAUNCH_MMA
+        return cudaErrorInvalidValue;
+    }
 #define PKV_LAUNCH(T, DD, GG) \
     if (a.D == DD && a.G == GG) return launch_t<T, DD, GG>(a, p, stream);
     if (a.dtype == PKV_F32) {

@@ -44,7 +44,15 @@ struct DecodeArgs {
     cudaEvent_t ev_after;
     uint32_t epoch;          // single request only: nonzero call epoch of the lane counters
                              // (no plan kernel; the workspace's counters started at zero)
+    const void* tmap_k;      // CUtensorMap of this layer's K / V pools (host memory), or
+    const void* tmap_v;      // nullptr: selects the tensor-core kernel when non-null
 };
+
+// Bytes of a CUtensorMap (the driver's TMA descriptor).
+constexpr int kTensorMapBytes = 128;
+
+// True if the tensor-core kernel implements (dtype, D, G).
+bool mma_supported(int dtype, int D, int G);
 
 // Byte offsets of the scratch areas inside a workspace.
 struct WorkspaceLayout {
@@ -64,7 +72,7 @@ int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len);
 
 // Resident split-kernel warps per SM x SMs for this geometry on the current
 // device; 0 if the geometry is not implemented.
-int resident_workers(int dtype, int D, int G, int num_sms);
+int resident_workers(int dtype, int D, int G, int num_sms, bool tensor_cores);
 
 // True if the kernels implement (dtype, D, G).
 bool decode_supported(int dtype, int D, int G);

@@ -10,6 +10,8 @@
 // together, counters advance on commit, reset zeroes them, rejected operations
 // change nothing).
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -74,6 +76,9 @@ struct pkv_pool {
     int64_t live_requests = 0;
     cudaEvent_t ev_before = nullptr;   // optional split-kernel timing events
     cudaEvent_t ev_after = nullptr;
+    bool tensor_cores = false;         // K/V tiles by TMA tensor loads, scores and mixture by MMA
+    std::vector<CUtensorMap> tmap_k;   // per layer, when tensor_cores
+    std::vector<CUtensorMap> tmap_v;
 };
 
 struct pkv_request {
@@ -97,6 +102,39 @@ struct pkv_request {
 namespace {
 
 int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+// The driver's tensor-map encoder, fetched through the runtime (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// One layer's K or V pool as a 2-D bf16 tensor [pages*H*P rows][D columns],
+// read in boxes of 16 rows x 64 columns (one 128-byte row each) with the
+// 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, void* base, int64_t rows, int D) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)pkv::kTile};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 void mark_dirty(pkv_request* r, int64_t from) {
     if (from < r->dev_dirty_from) r->dev_dirty_from = from;
@@ -188,7 +226,8 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
                     layers, heads, head_dim, page_size, (long long)max_context, (long long)pages);
     if (dtype != PKV_F32 && dtype != PKV_BF16)
         return fail(PKV_ERR_INVALID_ARGUMENT, "dtype %d is neither PKV_F32 nor PKV_BF16", dtype);
-    if (flags & ~PKV_POOL_HOST_ONLY) return fail(PKV_ERR_INVALID_ARGUMENT, "unknown flags");
+    if (flags & ~(PKV_POOL_HOST_ONLY | PKV_POOL_CUDA_CORES))
+        return fail(PKV_ERR_INVALID_ARGUMENT, "unknown flags");
     const bool host_only = (flags & PKV_POOL_HOST_ONLY) != 0;
     const int64_t per_request = (max_context + page_size - 1) / page_size;
     if (pages == 0) pages = per_request;
@@ -237,7 +276,11 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
             delete p;
             return cuda_fail(e, "device query");
         }
-        p->workers = pkv::resident_workers(dtype, head_dim, p->group, sms);
+        const int64_t rows = pages * page_size * heads;   // pool rows of one layer
+        p->tensor_cores = !(flags & PKV_POOL_CUDA_CORES) &&
+                          pkv::mma_supported(dtype, head_dim, p->group) && rows < INT32_MAX &&
+                          tensor_map_encoder() != nullptr;
+        p->workers = pkv::resident_workers(dtype, head_dim, p->group, sms, p->tensor_cores);
         if (p->workers <= 0) {
             delete p;
             return fail(PKV_ERR_CUDA, "split kernel cannot be resident on this device");
@@ -254,6 +297,22 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
             cudaGetLastError();
             return fail(PKV_ERR_OUT_OF_MEMORY, "cudaMalloc of 2 x %zu bytes: %s", total,
                         cudaGetErrorString(e));
+        }
+        if (p->tensor_cores) {
+            p->tmap_k.resize((size_t)layers);
+            p->tmap_v.resize((size_t)layers);
+            for (int l = 0; l < layers && p->tensor_cores; ++l) {
+                char* kb = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)l;
+                char* vb = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)l;
+                if (!encode_pool_map(&p->tmap_k[(size_t)l], kb, rows, head_dim) ||
+                    !encode_pool_map(&p->tmap_v[(size_t)l], vb, rows, head_dim)) {
+                    cudaFree(p->k_base);
+                    cudaFree(p->v_base);
+                    cudaFree(p->dev_error);
+                    delete p;
+                    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed for layer %d", l);
+                }
+            }
         }
         if ((e = cudaMemset(p->k_base, 0, total)) != cudaSuccess ||
             (e = cudaMemset(p->v_base, 0, total)) != cudaSuccess ||
@@ -298,6 +357,12 @@ int pkv_pool_heads(const pkv_pool* p, int* kv_heads, int* query_heads) {
     if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
     if (kv_heads) *kv_heads = p->heads;
     if (query_heads) *query_heads = p->query_heads;
+    return ok();
+}
+
+int pkv_pool_kernel(const pkv_pool* p, int* tensor_cores) {
+    if (!p || !tensor_cores) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    *tensor_cores = p->tensor_cores ? 1 : 0;
     return ok();
 }
 
@@ -474,6 +539,8 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.B = 1;
     a.H = p->heads;
     a.G = p->group;
+    a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
+    a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
     a.D = p->head_dim;
     a.P = p->page_size;
     a.q = q;
@@ -577,6 +644,8 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     a.B = batch;
     a.H = p->heads;
     a.G = p->group;
+    a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
+    a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
     a.D = p->head_dim;
     a.P = p->page_size;
     a.q = q;
@@ -669,6 +738,8 @@ int prepare_batched(pkv_pool* p, int layer, int batch, const float* q, const voi
     a->B = batch;
     a->H = p->heads;
     a->G = p->group;
+    a->tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
+    a->tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
     a->D = p->head_dim;
     a->P = p->page_size;
     a->q = q;

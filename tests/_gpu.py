@@ -41,11 +41,11 @@ class BatchedRun:
     history written into the pages, one batched step run on the device."""
 
     def __init__(self, w: Workload, layer: int = 0, max_seq_len=None, page_table_pad=0,
-                 stream=None):
+                 stream=None, cuda_cores=False):
         self.w = w
         self.layer = layer
         self.pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dtype_name(w.dtype),
-                             w.max_context, w.seed, query_heads=w.HQ)
+                             w.max_context, w.seed, query_heads=w.HQ, cuda_cores=cuda_cores)
         self.opool = OraclePool(w.layers, w.pool_pages, w.H, w.D, w.P, w.dtype,
                                 max_context=w.max_context, seed=w.seed, storage=False,
                                 query_heads=w.HQ)

@@ -43,10 +43,10 @@ def _lane_tensors(seed, layer, H, pos, D, dtype, kseed=None, group=1):
 
 
 def _serial(layers, H, D, dtype, pool_pages, max_context, steps, seed, abort_at=None,
-            check_at=None, P=16, group=1):
+            check_at=None, P=16, group=1, cuda_cores=False):
     """Serial begin / append x layers / commit on the library and on the oracle model."""
     pool = pkv.Pool(layers, pool_pages, H, D, P, dtype_name(dtype), max_context, seed,
-                    query_heads=H * group)
+                    query_heads=H * group, cuda_cores=cuda_cores)
     req = pool.request()
     opool = OraclePool(layers, pool_pages, H, D, P, dtype, max_context=max_context, seed=seed,
                        query_heads=H * group)
@@ -320,3 +320,47 @@ def test_gqa_geometry_errors():
     with pytest.raises(pkv.PkvError) as e:
         pkv.Pool(1, 8, 2, 32, 16, "bf16", 64, query_heads=4)
     assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+
+
+# ---------------------------------------- tensor-core and CUDA-core kernels --
+# bf16 grouped-query pools at head width 64 or 128 run the tensor-core kernel by
+# default; PKV_POOL_CUDA_CORES selects the CUDA-core kernel for the same geometry.
+
+def test_kernel_selection():
+    def pool(**kw):
+        return pkv.Pool(1, 8, 2, kw.pop("D", 128), 16, kw.pop("dtype", "bf16"), 64, **kw)
+    with pool(query_heads=16) as p:
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<128,8>"
+    with pool(query_heads=16, cuda_cores=True) as p:
+        assert not p.tensor_cores
+    with pool() as p:
+        assert not p.tensor_cores
+    with pool(query_heads=4, dtype="f32") as p:
+        assert not p.tensor_cores
+
+
+@pytest.mark.parametrize("group,D", [(2, 64), (4, 128), (8, 128)])
+def test_gqa_cuda_core_kernel(group, D):
+    lens = [1, 16, 17, 300, 1000, 33, 2048, 5]
+    _batched_check(make_workload(f"cc{group}", lens, 2, D, dtype=BF16, seed=50 + group,
+                                 group=group), cuda_cores=True)
+
+
+def test_serial_bf16_gqa_cuda_core_kernel_with_abort():
+    _serial(3, 4, 128, BF16, 64, 200, 70, 5, abort_at=33, P=32, group=2, cuda_cores=True)
+
+
+def test_serial_bf16_tensor_core_gqa_page_size_64():
+    _serial(2, 2, 128, BF16, 64, 300, 90, 9, abort_at=65, P=64, group=8)
+
+
+def test_tensor_core_and_cuda_core_kernels_agree():
+    w = make_workload("agree", [1, 15, 16, 17, 500, 4096, 33], 4, 128, dtype=BF16, seed=60, group=4)
+    a, b = BatchedRun(w), BatchedRun(w, cuda_cores=True)
+    try:
+        oa, ob = a.run().cpu().numpy(), b.run().cpu().numpy()
+        rel = np.abs(oa - ob).max(axis=-1) / np.maximum(np.abs(ob).max(axis=-1), 1e-6)
+        assert rel.max() < 1e-4
+    finally:
+        a.close()
+        b.close()
