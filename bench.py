@@ -65,6 +65,10 @@ def describe(w) -> str:
     if w.name.startswith("batched"):
         return (f"batched decode: {w.B} requests, t ~ U[1,4096], H={w.H}, d_h={w.D}, {st}, "
                 f"pool of {w.pool_pages} shuffled pages")
+    if w.name.startswith("window"):
+        return (f"sliding-window decode: {w.B} requests, t ~ U[1,{w.max_context}], window "
+                f"{w.window}, {w.H} KV heads x {w.group} query heads each, d_h={w.D}, {st}, "
+                f"pool of {w.pool_pages} shuffled pages")
     if w.name.startswith("gqa"):
         return (f"grouped-query decode: {w.B} requests, t ~ U[1,{w.max_context}], {w.H} KV heads x "
                 f"{w.group} query heads each, d_h={w.D}, {st}, pool of {w.pool_pages} shuffled pages")
@@ -78,6 +82,8 @@ def algorithmic_bytes(w) -> int:
     """Bytes one step must move: retained history K and V rows, the new rows read
     and written, q and out, page-table entries and lengths."""
     lens = w.seq_lens.astype(np.int64)
+    if getattr(w, "window", 0):
+        lens = np.minimum(lens, w.window)                        # rows a query attends to
     es = w.elem_bytes
     hist = int((lens - 1).sum()) * w.H * w.D * 2 * es          # H = KV heads
     new_rows = w.B * w.H * w.D * es * 2 * 2
@@ -223,7 +229,8 @@ def setup_device(w, torch, cuda_cores=False):
     from synth.workloads import churn_ops, LEASE
 
     pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "f32" if w.elem_bytes == 4 else "bf16",
-                    w.max_context, w.seed, query_heads=w.HQ, cuda_cores=cuda_cores)
+                    w.max_context, w.seed, query_heads=w.HQ, cuda_cores=cuda_cores,
+                    window=w.window)
     reqs = [pool.request() for _ in range(w.B)]
     for r_i, kind, cnt in (churn_ops(w) if w.churn_cycles else []):
         try:
@@ -549,8 +556,10 @@ def oracle_sample(w, requests, threads=0):
 
     def run():
         return oracle.paged_decode_attention(kp, vp, q[requests], k_new[requests], v_new[requests],
-                                             tab, lens, dt, threads=threads, group=w.group)
-    sample_bytes = int((lens.astype(np.int64) - 1).sum()) * w.H * w.D * 2 * w.elem_bytes
+                                             tab, lens, dt, threads=threads, group=w.group,
+                                             window=w.window)
+    attended = np.minimum(lens.astype(np.int64), w.window) if w.window else lens.astype(np.int64)
+    sample_bytes = int((attended - 1).sum()) * w.H * w.D * 2 * w.elem_bytes
     return run, sample_bytes, lens
 
 

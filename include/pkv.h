@@ -89,7 +89,8 @@ typedef enum pkv_dtype {
 typedef struct pkv_counters {
     int64_t committed_tokens;   /* tokens made visible by pkv_commit_token */
     int64_t cache_appends;      /* layers x committed tokens */
-    int64_t score_cells;        /* sum over committed tokens of layers x query_heads x t */
+    int64_t score_cells;        /* sum over committed tokens of layers x query_heads x
+                                   min(t, window) (t without a window) */
 } pkv_counters;
 
 /* ---------------------------------------------------------------- pool -- */
@@ -103,6 +104,10 @@ typedef struct pkv_counters {
  *                multiple of kv_heads: query head q reads KV head
  *                q / (query_heads / kv_heads) (grouped-query attention,
  *                [ROLLOUT-KV]; kv_heads == 1 is multi-query attention).
+ *   window:      sliding window ([ROLLOUT-KV]'s fixed window of W positions):
+ *                > 0 makes every query attend only to the last `window`
+ *                positions (itself included); 0 (default) attends to the whole
+ *                prefix.  Pages before the window stay leased.
  * The other fields are those of pkv_pool_create.
  */
 typedef struct pkv_pool_options {
@@ -116,6 +121,7 @@ typedef struct pkv_pool_options {
     int64_t max_context;
     uint64_t seed;
     unsigned flags;
+    int64_t window;
 } pkv_pool_options;
 
 int pkv_pool_options_init(pkv_pool_options* options);

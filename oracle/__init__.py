@@ -62,6 +62,9 @@ def load(path: str):
     L.orc_paged_decode_attention.restype = i32
     L.orc_paged_decode_attention.argtypes = [i32, i32, i32, i32, i32, vp, vp, i64, vp, vp,
                                              vp, vp, i32, vp, vp, vp, i64, i32]
+    L.orc_paged_decode_attention_ex.restype = i32
+    L.orc_paged_decode_attention_ex.argtypes = [i32, i32, i32, i64, i32, i32, i32, vp, vp, i64, vp,
+                                                vp, vp, vp, i32, vp, vp, vp, i64, i32]
     L.orc_paged_decode_attention_gqa.restype = i32
     L.orc_paged_decode_attention_gqa.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, i64, vp, vp,
                                                  vp, vp, i32, vp, vp, vp, i64, i32]
@@ -88,13 +91,15 @@ def _check_pool(pool: np.ndarray, dtype: int):
 def paged_decode_attention(k_pool: np.ndarray, v_pool: np.ndarray, q: np.ndarray,
                            k_new: np.ndarray, v_new: np.ndarray, tables: np.ndarray,
                            seq_lens: np.ndarray, dtype: int = F32, lanes=None,
-                           threads: int = 0, library=None, group: int = 1) -> np.ndarray:
+                           threads: int = 0, library=None, group: int = 1,
+                           window: int = 0) -> np.ndarray:
     """Append the new rows, then fp64 attention of each lane's newest query.
 
     k_pool, v_pool: one layer, [pages, H, P, D] storage dtype (fp32 or bf16 bits as
     uint16); modified in place by the append.  q [B, H*group, D] fp32; k_new, v_new
     [B, H, D] storage dtype; tables [B, max_pages] int32; seq_lens [B] int32 (t_b,
-    new token included).  Query head qh reads KV head qh // group.  Returns out
+    new token included).  Query head qh reads KV head qh // group.  With window W > 0
+    only the last W positions are attended.  Returns out
     [B, H*group, D] fp64 (query lanes b*H*group + qh not listed in ``lanes`` are
     left zero).  ``library``: an alternative loaded oracle library (tests only).
     """
@@ -119,10 +124,13 @@ def paged_decode_attention(k_pool: np.ndarray, v_pool: np.ndarray, q: np.ndarray
         lane_arr = np.ascontiguousarray(lanes, dtype=np.int64)
         n_lanes = lane_arr.size
     L = library or lib()
-    if group == 1:
+    if group == 1 and window == 0:
         call = lambda *a: L.orc_paged_decode_attention(*a)           # noqa: E731
-    else:
+    elif window == 0:
         call = lambda B_, H_, *a: L.orc_paged_decode_attention_gqa(B_, H_, group, *a)  # noqa: E731
+    else:
+        call = lambda B_, H_, *a: L.orc_paged_decode_attention_ex(B_, H_, group, window,  # noqa
+                                                                  *a)
     rc = call(
         B, H, D, P, dtype, k_pool.ctypes.data, v_pool.ctypes.data, n_pages, q.ctypes.data,
         k_new.ctypes.data, v_new.ctypes.data, tables.ctypes.data, tables.shape[1],

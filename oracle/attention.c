@@ -38,6 +38,10 @@
  * than query heads): with `group` query heads per KV head, query head qh reads
  * the keys and values of KV head qh / group.  group = 1 is ordinary multi-head
  * attention.
+ *
+ * Sliding window (same page: a fixed window of W positions gives O(TW)
+ * attention arithmetic): with window W > 0 the newest query attends to the
+ * keys at positions max(0, t - W) .. t - 1 only; W = 0 means the whole prefix.
  */
 #include <stdint.h>
 #include <string.h>
@@ -90,9 +94,10 @@ int orc_append(int B, int H, int D, int P, int dtype, void* k_pool, void* v_pool
  */
 static int lane_attention(int H, int D, int P, int dtype, const void* k_pool, const void* v_pool,
                           int64_t n_pages, const float* q, const int32_t* table, int64_t t, int h,
-                          double* scores, double* out) {
+                          int64_t window, double* scores, double* out) {
     const double scale = 1.0 / sqrt((double)D);
-    for (int64_t j = 0; j < t; ++j) {
+    const int64_t j0 = (window > 0 && t > window) ? t - window : 0;   /* first key attended */
+    for (int64_t j = j0; j < t; ++j) {
         int64_t page = table[j / P];
         if (page < 0 || page >= n_pages) return -1;
         int64_t off = pool_offset(page, h, j % P, H, P, D);
@@ -101,13 +106,13 @@ static int lane_attention(int H, int D, int P, int dtype, const void* k_pool, co
         scores[j] = dot * scale;
     }
     double m = -INFINITY;
-    for (int64_t j = 0; j < t; ++j) if (scores[j] > m) m = scores[j];
+    for (int64_t j = j0; j < t; ++j) if (scores[j] > m) m = scores[j];
     double sum = 0.0;
-    for (int64_t j = 0; j < t; ++j) { scores[j] = exp(scores[j] - m); sum += scores[j]; }
-    for (int64_t j = 0; j < t; ++j) scores[j] /= sum;          /* softmax weights */
+    for (int64_t j = j0; j < t; ++j) { scores[j] = exp(scores[j] - m); sum += scores[j]; }
+    for (int64_t j = j0; j < t; ++j) scores[j] /= sum;          /* softmax weights */
     for (int d = 0; d < D; ++d) {
         double mix = 0.0;
-        for (int64_t j = 0; j < t; ++j) {
+        for (int64_t j = j0; j < t; ++j) {
             int64_t page = table[j / P];
             mix += scores[j] * load_elem(v_pool, pool_offset(page, h, j % P, H, P, D) + d, dtype);
         }
@@ -130,12 +135,12 @@ static int lane_attention(int H, int D, int P, int dtype, const void* k_pool, co
  *   threads  OpenMP threads for the lane loop (<= 0: library default)
  * Returns 0 on success, -1 on an out-of-range length or page id.
  */
-int orc_paged_decode_attention_gqa(int B, int H, int group, int D, int P, int dtype, void* k_pool,
-                                   void* v_pool, int64_t n_pages, const float* q,
-                                   const void* k_new, const void* v_new, const int32_t* tables,
-                                   int max_pages, const int32_t* seq_lens, double* out,
-                                   const int64_t* lanes, int64_t n_lanes, int threads) {
-    if (group < 1) return -1;
+int orc_paged_decode_attention_ex(int B, int H, int group, int64_t window, int D, int P,
+                                  int dtype, void* k_pool, void* v_pool, int64_t n_pages,
+                                  const float* q, const void* k_new, const void* v_new,
+                                  const int32_t* tables, int max_pages, const int32_t* seq_lens,
+                                  double* out, const int64_t* lanes, int64_t n_lanes, int threads) {
+    if (group < 1 || window < 0) return -1;
     int rc = orc_append(B, H, D, P, dtype, k_pool, v_pool, n_pages, k_new, v_new, tables,
                         max_pages, seq_lens);
     if (rc != 0) return rc;
@@ -161,12 +166,23 @@ int orc_paged_decode_attention_gqa(int B, int H, int group, int D, int P, int dt
             int b = (int)(lane / HQ), qh = (int)(lane % HQ);
             if (lane_attention(H, D, P, dtype, k_pool, v_pool, n_pages, q + lane * D,
                                tables + (int64_t)b * max_pages, seq_lens[b], qh / group,
-                               scores, out + lane * D) != 0)
+                               window, scores, out + lane * D) != 0)
                 bad = 1;
         }
         free(scores);
     }
     return bad ? -1 : 0;
+}
+
+/* Grouped-query attention over the whole prefix. */
+int orc_paged_decode_attention_gqa(int B, int H, int group, int D, int P, int dtype, void* k_pool,
+                                   void* v_pool, int64_t n_pages, const float* q,
+                                   const void* k_new, const void* v_new, const int32_t* tables,
+                                   int max_pages, const int32_t* seq_lens, double* out,
+                                   const int64_t* lanes, int64_t n_lanes, int threads) {
+    return orc_paged_decode_attention_ex(B, H, group, 0, D, P, dtype, k_pool, v_pool, n_pages, q,
+                                         k_new, v_new, tables, max_pages, seq_lens, out, lanes,
+                                         n_lanes, threads);
 }
 
 /* Multi-head attention: one query head per KV head. */

@@ -89,15 +89,17 @@ class OraclePool:
 
     def __init__(self, layers: int, pages: int, heads: int, head_dim: int, page_size: int = 16,
                  dtype: int = F32, max_context: int = 0, seed: int = 0, storage: bool = True,
-                 query_heads: int = 0):
+                 query_heads: int = 0, window: int = 0):
         """heads: KV heads stored per page; query_heads: heads of the query (0 = heads),
-        a multiple of heads (grouped-query attention)."""
+        a multiple of heads (grouped-query attention); window: attend to the last
+        `window` positions only (0 = the whole prefix)."""
         if layers < 1 or heads < 1 or head_dim < 1 or page_size < 1 or max_context < 1 or pages < 0:
             raise OracleError(Status.INVALID_ARGUMENT, "bad pool geometry")
         query_heads = query_heads or heads
         if query_heads % heads:
             raise OracleError(Status.INVALID_ARGUMENT, "query heads not a multiple of KV heads")
         self.HQ, self.group = query_heads, query_heads // heads
+        self.window = window
         if pages == 0:
             pages = -(-max_context // page_size)       # one maximum-length context
         self.layers, self.pages, self.H, self.D, self.P = layers, pages, heads, head_dim, page_size
@@ -196,7 +198,7 @@ class OracleRequest:
         kp, vp = p.k[layer], p.v[layer]
         if compute:
             out = paged_decode_attention(kp, vp, q[None], k[None], v[None], tables, lens, p.dtype,
-                                         group=p.group)[0]
+                                         group=p.group, window=p.window)[0]
         else:
             _append(kp, vp, k[None], v[None], tables, lens, p.dtype)
             out = None
@@ -213,7 +215,7 @@ class OracleRequest:
         self.length = t
         self.committed_tokens += 1
         self.cache_appends += p.layers
-        self.score_cells += p.layers * p.HQ * t
+        self.score_cells += p.layers * p.HQ * (min(t, p.window) if p.window else t)
         self.pending = None
 
     def abort_token(self) -> None:

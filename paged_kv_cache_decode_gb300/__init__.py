@@ -86,13 +86,15 @@ class Pool:
 
     ``heads`` is the number of KV heads stored per page; ``query_heads`` (default:
     ``heads``) the heads of the query and output, a multiple of ``heads``
-    (grouped-query attention)."""
+    (grouped-query attention); ``window`` > 0 limits every query to the last
+    ``window`` positions (sliding window)."""
 
     def __init__(self, layers: int, pages: int, heads: int, head_dim: int, page_size: int = 16,
                  dtype="f32", max_context: int = 4096, seed: int = 0, host_only: bool = False,
-                 query_heads: int = 0, cuda_cores: bool = False):
+                 query_heads: int = 0, cuda_cores: bool = False, window: int = 0):
         self.layers, self.heads, self.head_dim, self.page_size = layers, heads, head_dim, page_size
         self.query_heads = query_heads or heads
+        self.window = window
         self.dtype = _dtype_code(dtype)
         self.torch_dtype = _TORCH_DTYPE[self.dtype]
         self.max_context = max_context
@@ -102,6 +104,7 @@ class Pool:
         o.layers, o.pages, o.kv_heads, o.query_heads = layers, pages, heads, self.query_heads
         o.head_dim, o.page_size, o.dtype, o.max_context = head_dim, page_size, self.dtype, max_context
         o.seed = seed & ((1 << 64) - 1)
+        o.window = window
         o.flags = (PKV_POOL_HOST_ONLY if host_only else 0) | (PKV_POOL_CUDA_CORES if cuda_cores else 0)
         h = ctypes.c_void_p()
         check(lib.pkv_pool_create_ex(ctypes.byref(o), ctypes.byref(h)), "pkv_pool_create_ex")
@@ -331,9 +334,9 @@ class Request:
 # --------------------------------------------------------- C-ABI names --
 
 def pool_create(layers, pages, heads, head_dim, page_size=16, dtype="f32", max_context=4096,
-                seed=0, host_only=False, query_heads=0) -> Pool:
+                seed=0, host_only=False, query_heads=0, cuda_cores=False, window=0) -> Pool:
     return Pool(layers, pages, heads, head_dim, page_size, dtype, max_context, seed, host_only,
-                query_heads)
+                query_heads, cuda_cores, window)
 
 
 def pool_destroy(pool: Pool) -> None:

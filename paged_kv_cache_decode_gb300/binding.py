@@ -42,7 +42,7 @@ class pkv_pool_options(ctypes.Structure):
                 ("query_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("max_context", ctypes.c_int64), ("seed", ctypes.c_uint64),
-                ("flags", ctypes.c_uint)]
+                ("flags", ctypes.c_uint), ("window", ctypes.c_int64)]
 
 
 class pkv_counters(ctypes.Structure):

@@ -255,6 +255,7 @@ struct KParams {
     int64_t single_t;
     int64_t max_seq_len;
     int B, H, P, tiles_per_page;
+    int64_t window;             // attend to the last `window` positions (0: all)
     float qscale;               // log2(e) / sqrt(D)
     float* out;
     int64_t* req_prefix;        // [B + 1] tiles-per-lane prefix (plan kernel)
@@ -271,10 +272,21 @@ __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
 }
 
+// First position a query at retained length t attends to (sliding window).
+__device__ __forceinline__ int64_t window_start(const KParams& p, int64_t t) {
+    return (p.window > 0 && t > p.window) ? t - p.window : 0;
+}
+
+// Tiles a lane of retained length t reads: from the tile holding the window's
+// first position to the tile holding position t - 1.
+__device__ __forceinline__ int64_t lane_tiles(const KParams& p, int64_t t) {
+    return (t + kTile - 1) / kTile - window_start(p, t) / kTile;
+}
+
 // Tiles-per-lane prefix over requests: closed form for a single request (no
 // dependence on the plan kernel), else the plan kernel's table.
 __device__ __forceinline__ int64_t req_prefix_at(const KParams& p, int b) {
-    if (p.seq_lens == nullptr) return b == 0 ? 0 : (p.single_t + kTile - 1) / kTile;
+    if (p.seq_lens == nullptr) return b == 0 ? 0 : lane_tiles(p, p.single_t);
     return __ldg(p.req_prefix + b);
 }
 
@@ -304,7 +316,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
             if (t < 1 || t > p.max_seq_len || pages > p.max_pages) {
                 atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
             } else {
-                n = (t + kTile - 1) / kTile;
+                n = lane_tiles(p, t);
             }
         }
         int64_t incl = n;
@@ -360,12 +372,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
 // with the tile's page-table index and first slot tracked incrementally.
 struct Cursor {
     int b, h;
-    int tile;          // tile within the lane
+    int tile;          // tile within the lane (0 .. n-1)
     int n;             // tiles of this lane
+    int tile0;         // position / 16 of the lane's tile 0 (the window's first tile)
     int page_idx;      // logical page of the tile
     int slot0;         // first slot of the tile within its page
     int64_t first;     // flattened index of tile 0 of head 0 of request b
 };
+
+// Page index and slot of the lane's tile `tile`.
+__device__ __forceinline__ void cursor_place(Cursor& c, const KParams& p) {
+    const int abs = c.tile0 + c.tile;
+    c.page_idx = abs / p.tiles_per_page;
+    c.slot0 = (abs - c.page_idx * p.tiles_per_page) * kTile;
+}
 
 __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
     ++c.tile;
@@ -376,9 +396,10 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
     }
     if (c.tile < c.n) return;
     c.tile = 0;
-    c.page_idx = 0;
-    c.slot0 = 0;
-    if (++c.h < p.H) return;
+    if (++c.h < p.H) {
+        cursor_place(c, p);
+        return;
+    }
     c.h = 0;
     // next request with at least one tile
     int64_t pre = req_prefix_at(p, c.b + 1);
@@ -388,6 +409,8 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
         if (nxt > pre) {
             c.n = (int)(nxt - pre);
             c.first = (int64_t)p.H * pre;
+            c.tile0 = (int)(window_start(p, seq_len_at(p, c.b)) / kTile);
+            cursor_place(c, p);
             return;
         }
         pre = nxt;
@@ -508,8 +531,8 @@ split_decode_kernel(const KParams p) {
         const int64_t local = begin - cur.first;
         cur.h = (int)(local / cur.n);
         cur.tile = (int)(local % cur.n);
-        cur.page_idx = cur.tile / p.tiles_per_page;
-        cur.slot0 = (cur.tile - cur.page_idx * p.tiles_per_page) * kTile;
+        cur.tile0 = (int)(window_start(p, seq_len_at(p, b0)) / kTile);
+        cursor_place(cur, p);
     }
     Cursor prod = cur;
 
@@ -545,7 +568,7 @@ split_decode_kernel(const KParams p) {
     float2 qv[G][NV];
     float2 o[G][NV];
     float m[G], l[G];
-    int piece_first = 0, t_b = 0;
+    int piece_first = 0, t_b = 0, w_start = 0;
     int s = 0;
     uint32_t parity = 0;
 
@@ -555,6 +578,7 @@ split_decode_kernel(const KParams p) {
         if (k == 0 || cur.tile == 0) {   // a new lane piece starts
             piece_first = cur.tile;
             t_b = (int)seq_len_at(p, cur.b);
+            w_start = (int)window_start(p, t_b);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float2* qp = reinterpret_cast<const float2*>(p.q + (lane_id * G + g) * D + col);
@@ -590,8 +614,11 @@ split_decode_kernel(const KParams p) {
         const int32_t page = stage_page[s];
         const bool page_ok = page >= 0 && page < p.n_pages;
         const bool last_tile = cur.tile == cur.n - 1;
-        const int rem = t_b - cur.tile * kTile;
+        const int base = (cur.tile0 + cur.tile) * kTile;          // position of the tile's row 0
+        const int rem = t_b - base;
         const int rows = !page_ok ? 0 : (rem < kTile ? rem : kTile);
+        const int lo = w_start > base ? w_start - base : 0;       // rows before the window
+
 
         if (last_tile && page_ok) {
             // fused append: row t_b - 1 comes from k_new / v_new, into the tile and the page
@@ -652,7 +679,7 @@ split_decode_kernel(const KParams p) {
             float p_own[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float s_own = row_own < rows ? sc[g][0] : -INFINITY;
+                const float s_own = (row_own >= lo && row_own < rows) ? sc[g][0] : -INFINITY;
                 float tmax = s_own;
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1)
@@ -675,7 +702,7 @@ split_decode_kernel(const KParams p) {
                     pw[g] = Gm::TPR >= 2
                         ? __shfl_sync(0xffffffffu, p_own[g], (lane & ~(Gm::TPR - 1)) | (it << 1))
                         : p_own[g];
-                if (row < rows) {
+                if (row >= lo && row < rows) {
                     float2 vf[NV];
                     const VT vb = *reinterpret_cast<const VT*>(Vs + row * D + col);
                     Storage<T>::template to_float2<Gm::VEC>(&vb, vf);
@@ -924,8 +951,8 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         const int64_t local = begin - cur.first;
         cur.h = (int)(local / cur.n);
         cur.tile = (int)(local % cur.n);
-        cur.page_idx = cur.tile / p.tiles_per_page;
-        cur.slot0 = (cur.tile - cur.page_idx * p.tiles_per_page) * kTile;
+        cur.tile0 = (int)(window_start(p, seq_len_at(p, b0)) / kTile);
+        cursor_place(cur, p);
     }
     Cursor prod = cur;
 
@@ -963,7 +990,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     uint32_t qa[M::KSTEPS][4];                  // A fragments of [q_hi; q_lo]
     float o[M::NB][4];                          // O accumulator fragments
     float m = -INFINITY, l = 0.f;               // running max and this lane's share of the sum
-    int piece_first = 0, t_b = 0;
+    int piece_first = 0, t_b = 0, w_start = 0;
     int s = 0;
     uint32_t parity = 0;
 
@@ -973,6 +1000,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         if (k == 0 || cur.tile == 0) {   // a new lane piece starts
             piece_first = cur.tile;
             t_b = (int)seq_len_at(p, cur.b);
+            w_start = (int)window_start(p, t_b);
             const float* qp = p.q + (lane_id * G + (q_ok ? g : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < M::KSTEPS; ++ks) {
@@ -1012,8 +1040,11 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         const int32_t page = stage_page[s];
         const bool page_ok = page >= 0 && page < p.n_pages;
         const bool last_tile = cur.tile == cur.n - 1;
-        const int rem = t_b - cur.tile * kTile;
+        const int base = (cur.tile0 + cur.tile) * kTile;          // position of the tile's row 0
+        const int rem = t_b - base;
         const int rows = !page_ok ? 0 : (rem < kTile ? rem : kTile);
+        const int lo = w_start > base ? w_start - base : 0;       // rows before the window
+
 
         if (last_tile && page_ok) {
             // fused append: row t_b - 1 from k_new / v_new into the tile and the page;
@@ -1057,7 +1088,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             float tmax = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if (!q_ok || keys[i] >= rows) sc[i] = -INFINITY;
+                if (!q_ok || keys[i] < lo || keys[i] >= rows) sc[i] = -INFINITY;
                 tmax = fmaxf(tmax, sc[i]);
             }
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
@@ -1366,6 +1397,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.H = a.H;
     p.P = a.P;
     p.tiles_per_page = a.P / kTile;
+    p.window = a.window;
     p.qscale = 1.4426950408889634f / sqrtf((float)a.D);
     p.out = a.out;
     const WorkspaceLayout L = workspace_layout(a.B, a.H, a.D, a.workers, a.G);

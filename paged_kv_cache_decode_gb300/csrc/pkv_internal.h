@@ -24,6 +24,7 @@ struct DecodeArgs {
     int dtype;               // PKV_F32 / PKV_BF16
     int B, H, D, P;          // requests, KV heads, head width, page size (multiple of kTile)
     int G;                   // query heads per KV head (1: multi-head attention)
+    int64_t window;          // attend to the last `window` positions (0: the whole prefix)
     const float* q;          // [B][H*G][D]
     const void* k_new;       // [B][H][D] storage dtype
     const void* v_new;
@@ -69,6 +70,12 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G);
 // Workers one launch uses: the pool's resident worker count, capped by the
 // number of tiles the launch can hold (B * H * ceil(max_seq_len / kTile)).
 int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len);
+
+// Longest stretch of positions one query reads: max_seq_len, or with a
+// sliding window the window plus one partial tile.
+inline int64_t attended_len(int64_t max_seq_len, int64_t window) {
+    return (window > 0 && window + kTile < max_seq_len) ? window + kTile : max_seq_len;
+}
 
 // Resident split-kernel warps per SM x SMs for this geometry on the current
 // device; 0 if the geometry is not implemented.

@@ -64,6 +64,7 @@ struct SplitMix64 {
 struct pkv_pool {
     int layers = 0, heads = 0, head_dim = 0, page_size = 0, dtype = 0;
     int query_heads = 0, group = 1;    // query heads = group x KV heads (grouped-query attention)
+    int64_t window = 0;                // sliding window in positions (0: whole prefix)
     int64_t pages = 0, max_context = 0, max_pages_per_request = 0;
     bool host_only = false;
     std::deque<int32_t> free_list;     // front = next page to lease
@@ -187,6 +188,7 @@ int pkv_pool_options_init(pkv_pool_options* o) {
     o->max_context = 4096;
     o->seed = 0;
     o->flags = 0;
+    o->window = 0;
     return ok();
 }
 
@@ -203,6 +205,7 @@ int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page
     o.max_context = max_context;
     o.seed = seed;
     o.flags = flags;
+    o.window = 0;
     return pkv_pool_create_ex(&o, out);
 }
 
@@ -216,6 +219,7 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
     const uint64_t seed = opts->seed;
     const unsigned flags = opts->flags;
     const int query_heads = opts->query_heads == 0 ? heads : opts->query_heads;
+    if (opts->window < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "negative window");
     if (heads >= 1 && (query_heads < heads || query_heads % heads != 0))
         return fail(PKV_ERR_INVALID_ARGUMENT, "query_heads %d is not a multiple of kv_heads %d",
                     query_heads, heads);
@@ -250,6 +254,7 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
     p->heads = heads;
     p->query_heads = query_heads;
     p->group = query_heads / heads;
+    p->window = opts->window;
     p->head_dim = head_dim;
     p->page_size = page_size;
     p->dtype = dtype;
@@ -404,7 +409,7 @@ int pkv_request_create(pkv_pool* p, pkv_request** out) {
             return rc;
         }
         r->workspace_workers =
-            pkv::launch_workers(p->workers, 1, p->heads, p->max_context);
+            pkv::launch_workers(p->workers, 1, p->heads, pkv::attended_len(p->max_context, p->window));
         r->workspace_bytes =
             pkv::workspace_layout(1, p->heads, p->head_dim, r->workspace_workers, p->group).total;
         cudaError_t e = cudaMalloc(&r->dev_table, sizeof(int32_t) * (size_t)p->max_pages_per_request);
@@ -539,6 +544,7 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.B = 1;
     a.H = p->heads;
     a.G = p->group;
+    a.window = p->window;
     a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
     a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
     a.D = p->head_dim;
@@ -559,7 +565,7 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.out = out;
     a.workspace = r->dev_workspace;
     a.workspace_bytes = r->workspace_bytes;
-    a.workers = pkv::launch_workers(r->workspace_workers, 1, p->heads, r->position + 1);
+    a.workers = pkv::launch_workers(r->workspace_workers, 1, p->heads, pkv::attended_len(r->position + 1, p->window));
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
@@ -588,7 +594,8 @@ int pkv_commit_token(pkv_request* r) {
     r->length = t;
     r->counters.committed_tokens += 1;
     r->counters.cache_appends += p->layers;
-    r->counters.score_cells += (int64_t)p->layers * p->query_heads * t;
+    r->counters.score_cells +=
+        (int64_t)p->layers * p->query_heads * (p->window > 0 && p->window < t ? p->window : t);
     r->pending = false;
     r->leased_by_begin = false;
     return ok();
@@ -611,7 +618,7 @@ int pkv_workspace_size(const pkv_pool* p, int batch, int64_t max_seq_len, size_t
     if (!p || !bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
     if (batch < 0 || max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "bad batch or length");
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
-    const int w = pkv::launch_workers(p->workers, batch, p->heads, max_seq_len);
+    const int w = pkv::launch_workers(p->workers, batch, p->heads, pkv::attended_len(max_seq_len, p->window));
     *bytes = pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
     return ok();
 }
@@ -632,7 +639,7 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
         return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
-    const int w = pkv::launch_workers(p->workers, batch, p->heads, max_seq_len);
+    const int w = pkv::launch_workers(p->workers, batch, p->heads, pkv::attended_len(max_seq_len, p->window));
     const size_t need = pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
@@ -644,6 +651,7 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     a.B = batch;
     a.H = p->heads;
     a.G = p->group;
+    a.window = p->window;
     a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
     a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
     a.D = p->head_dim;
@@ -732,12 +740,13 @@ int prepare_batched(pkv_pool* p, int layer, int batch, const float* q, const voi
         return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
-    const int w = launch_workers(p->workers, batch, p->heads, max_seq_len);
+    const int w = launch_workers(p->workers, batch, p->heads, attended_len(max_seq_len, p->window));
     *workspace_bytes = workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
     a->dtype = p->dtype;
     a->B = batch;
     a->H = p->heads;
     a->G = p->group;
+    a->window = p->window;
     a->tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
     a->tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
     a->D = p->head_dim;

@@ -31,6 +31,7 @@ class Workload:
     seq_lens: np.ndarray   # [B] int32, retained length t_b including the new token
     churn_cycles: int = 0  # seeded lease/release cycles before the final tables are leased
     group: int = 1         # query heads per KV head (H is the number of KV heads)
+    window: int = 0        # sliding window in positions (0: whole prefix)
 
     @property
     def HQ(self) -> int:
@@ -106,6 +107,15 @@ def gqa(group: int = 8, dtype: int = BF16, seed: int = 5, B: int = 64, t_max: in
     return Workload(name, B, 1, 8, 128, 16, dtype, 32768, t_max, seed, lens, group=group)
 
 
+def sliding_window(seed: int = 6, B: int = 64, t_max: int = 32768, window: int = 4096) -> Workload:
+    """Sliding-window grouped-query decode: 64 requests, t ~ U{1..32768}, window 4096,
+    8 KV heads x 4 query heads, d_h=128, bf16, pool of 140000 shuffled pages."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, t_max + 1, size=B).astype(np.int32)
+    return Workload("window_bf16", B, 1, 8, 128, 16, BF16, 140000, t_max, seed, lens, group=4,
+                    window=window)
+
+
 REGISTRY = {
     "tiny": tiny,
     "single_t128": lambda: single(128),
@@ -118,4 +128,5 @@ REGISTRY = {
     "gqa8_bf16": lambda: gqa(8, BF16),
     "gqa4_bf16": lambda: gqa(4, BF16),
     "gqa8_f32": lambda: gqa(8, F32),
+    "window_bf16": sliding_window,
 }

@@ -45,10 +45,11 @@ class BatchedRun:
         self.w = w
         self.layer = layer
         self.pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dtype_name(w.dtype),
-                             w.max_context, w.seed, query_heads=w.HQ, cuda_cores=cuda_cores)
+                             w.max_context, w.seed, query_heads=w.HQ, cuda_cores=cuda_cores,
+                             window=w.window)
         self.opool = OraclePool(w.layers, w.pool_pages, w.H, w.D, w.P, w.dtype,
                                 max_context=w.max_context, seed=w.seed, storage=False,
-                                query_heads=w.HQ)
+                                query_heads=w.HQ, window=w.window)
         self.reqs = [self.pool.request() for _ in range(w.B)]
         self.oreqs = [self.opool.request() for _ in range(w.B)]
         for r_i, kind, cnt in churn_ops(w) if w.churn_cycles else []:
@@ -116,7 +117,7 @@ class BatchedRun:
         ref = oracle.paged_decode_attention(kp, vp, self.q[requests], self.k_new[requests],
                                             self.v_new[requests], ctab,
                                             w.seq_lens[requests].astype(np.int32), w.dtype,
-                                            lanes=lanes, group=w.group)
+                                            lanes=lanes, group=w.group, window=w.window)
         return {(b, h): ref[i, h] for i, b in enumerate(requests) for h in heads}
 
     def appended_rows(self, b: int):
@@ -137,7 +138,7 @@ class BatchedRun:
 
 
 def make_workload(name, seq_lens, H, D, P=16, dtype=F32, pool_pages=None, seed=0, layers=1,
-                  max_context=None, churn=0, group=1) -> Workload:
+                  max_context=None, churn=0, group=1, window=0) -> Workload:
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
     n = (seq_lens.astype(np.int64) + P - 1) // P
     if pool_pages is None:
@@ -145,4 +146,4 @@ def make_workload(name, seq_lens, H, D, P=16, dtype=F32, pool_pages=None, seed=0
     if max_context is None:
         max_context = int(max(seq_lens.max(), 1))
     return Workload(name, len(seq_lens), layers, H, D, P, dtype, int(pool_pages), int(max_context),
-                    seed, seq_lens, churn_cycles=churn, group=group)
+                    seed, seq_lens, churn_cycles=churn, group=group, window=window)

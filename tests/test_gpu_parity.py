@@ -43,13 +43,13 @@ def _lane_tensors(seed, layer, H, pos, D, dtype, kseed=None, group=1):
 
 
 def _serial(layers, H, D, dtype, pool_pages, max_context, steps, seed, abort_at=None,
-            check_at=None, P=16, group=1, cuda_cores=False):
+            check_at=None, P=16, group=1, cuda_cores=False, window=0):
     """Serial begin / append x layers / commit on the library and on the oracle model."""
     pool = pkv.Pool(layers, pool_pages, H, D, P, dtype_name(dtype), max_context, seed,
-                    query_heads=H * group, cuda_cores=cuda_cores)
+                    query_heads=H * group, cuda_cores=cuda_cores, window=window)
     req = pool.request()
     opool = OraclePool(layers, pool_pages, H, D, P, dtype, max_context=max_context, seed=seed,
-                       query_heads=H * group)
+                       query_heads=H * group, window=window)
     oreq = opool.request()
     errs = []
     for t in range(1, steps + 1):
@@ -364,3 +364,35 @@ def test_tensor_core_and_cuda_core_kernels_agree():
     finally:
         a.close()
         b.close()
+
+
+# ----------------------------------------------------------- sliding window --
+
+@pytest.mark.parametrize("window,dtype,group", [(1, F32, 1), (16, BF16, 1), (17, F32, 1),
+                                                (100, BF16, 1), (64, BF16, 4), (333, BF16, 8),
+                                                (5000, BF16, 2)])
+def test_window_batched(window, dtype, group):
+    lens = [1, 2, 16, 17, 33, 100, 101, 300, 1000, 4097]
+    D = 128 if group > 1 else 64
+    _batched_check(make_workload(f"win{window}", lens, 2, D, dtype=dtype, seed=70 + window,
+                                 group=group, window=window))
+
+
+def test_window_cuda_core_kernel_gqa():
+    lens = [5, 16, 17, 300, 1000, 2049]
+    _batched_check(make_workload("wincc", lens, 2, 128, dtype=BF16, seed=77, group=4, window=129),
+                   cuda_cores=True)
+
+
+def test_window_full_config_every_lane():
+    """64 requests, t ~ U{1..32768}, window 4096, 8 KV heads x 4 query heads."""
+    _batched_check(workloads.sliding_window())
+
+
+def test_window_serial_with_abort():
+    c, _ = _serial(2, 2, 64, F32, 64, 300, 60, 8, abort_at=40, window=20)
+    assert c["score_cells"] == 2 * 2 * sum(min(t, 20) for t in range(1, 61))
+
+
+def test_window_serial_gqa_tensor_cores():
+    _serial(2, 2, 128, BF16, 64, 300, 50, 9, group=8, window=33)

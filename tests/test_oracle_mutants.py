@@ -17,6 +17,8 @@ MUTANTS = {
     "scale_squared": ("const double scale = 1.0 / sqrt((double)D);", "const double scale = 1.0 / D;"),
     "new_key_excluded": ("seq_lens[b], qh / group,", "seq_lens[b] - 1 + (seq_lens[b] == 1), qh / group,"),
     "group_head_map": ("seq_lens[b], qh / group,", "seq_lens[b], qh % H,"),
+    "window_start": ("const int64_t j0 = (window > 0 && t > window) ? t - window : 0;",
+                     "const int64_t j0 = (window > 0 && t > window) ? t - window + 1 : 0;"),
     "slot_index": ("int64_t off = pool_offset(page, h, j % P, H, P, D);",
                    "int64_t off = pool_offset(page, h, (j + 1) % P, H, P, D);"),
     "page_index": ("int64_t page = table[j / P];\n        if", "int64_t page = table[j / (P + 1)];\n        if"),
@@ -35,7 +37,7 @@ MUTANTS = {
 def _pins_pass(lib) -> bool:
     """The pins of test_oracle_pins, run against one library."""
     try:
-        if not _gqa_pin_passes(lib):
+        if not _gqa_pin_passes(lib) or not _window_pin_passes(lib):
             return False
         for lens, H, D, P, dtype in [([5, 17, 33], 2, 2, 16, F32), ([31, 48, 2], 2, 8, 16, BF16),
                                      ([1], 2, 4, 16, F32)]:
@@ -68,6 +70,22 @@ def _gqa_pin_passes(lib) -> bool:
     b = oracle.paged_decode_attention(kp_rep, vp_rep, q, knew_rep, vnew_rep, case.tables,
                                       case.seq_lens, case.dtype, library=lib)
     return np.allclose(a, b, rtol=0, atol=1e-12)
+
+
+def _window_pin_passes(lib) -> bool:
+    from tests.test_oracle_pins import banded_last_row
+    case = PagedCase([3, 17, 50], 2, 8, 16, F32, seed=21)
+    out = oracle.paged_decode_attention(case.k_pool.copy(), case.v_pool.copy(), case.q, case.k_new,
+                                        case.v_new, case.tables, case.seq_lens, F32, library=lib,
+                                        window=17)
+    for b in range(case.B):
+        for h in range(2):
+            lane = b * 2 + h
+            ref = banded_last_row(case.query_rows(b, h), to_f64(case.K[lane], F32),
+                                  to_f64(case.V[lane], F32), 17)
+            if not np.allclose(out[b, h], ref, rtol=0, atol=1e-12):
+                return False
+    return True
 
 
 def _compile(tmp_path, name, text):

@@ -375,3 +375,58 @@ def test_group_one_is_multi_head():
     b = oracle.paged_decode_attention(case.k_pool.copy(), case.v_pool.copy(), case.q, case.k_new,
                                       case.v_new, case.tables, case.seq_lens, F32, group=1)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# sliding window
+
+
+def banded_last_row(Qrows, K, V, window):
+    """Dense causal attention with each row limited to its last `window` keys."""
+    Qd = np.asarray(Qrows, dtype=np.float64)
+    t, D = Qd.shape
+    S = Qd @ K.T / np.sqrt(D)
+    i, j = np.indices((t, t))
+    S = np.where((j <= i) & (j > i - window), S, -np.inf)
+    S = S - S.max(axis=1, keepdims=True)
+    W = np.exp(S)
+    W /= W.sum(axis=1, keepdims=True)
+    return (W @ V)[-1]
+
+
+@pytest.mark.parametrize("window", [1, 5, 16, 17, 40])
+def test_window_matches_banded_dense_reference(window):
+    case = PagedCase([3, 17, 50, 33], 2, 8, 16, BF16, seed=21)
+    out = oracle.paged_decode_attention(case.k_pool.copy(), case.v_pool.copy(), case.q,
+                                        case.k_new, case.v_new, case.tables, case.seq_lens,
+                                        BF16, window=window)
+    for b, t in enumerate(case.seq_lens):
+        for h in range(2):
+            lane = b * 2 + h
+            ref = banded_last_row(case.query_rows(b, h), to_f64(case.K[lane], BF16),
+                                  to_f64(case.V[lane], BF16), window)
+            np.testing.assert_allclose(out[b, h], ref, rtol=0, atol=1e-12)
+
+
+def test_window_one_is_the_new_value_and_wide_window_is_full():
+    case = PagedCase([9, 30], 2, 4, 16, F32, seed=22)
+    one = oracle.paged_decode_attention(case.k_pool.copy(), case.v_pool.copy(), case.q, case.k_new,
+                                        case.v_new, case.tables, case.seq_lens, F32, window=1)
+    assert np.array_equal(one, to_f64(case.v_new, F32))
+    full, _, _ = run_oracle(case)
+    wide = oracle.paged_decode_attention(case.k_pool.copy(), case.v_pool.copy(), case.q, case.k_new,
+                                         case.v_new, case.tables, case.seq_lens, F32, window=30)
+    assert np.array_equal(full, wide)
+
+
+def test_window_score_cells_are_lanes_times_min_t_w():
+    pool = OraclePool(2, 4, 2, 2, 16, F32, max_context=64, seed=0, window=2)
+    req = pool.request()
+    for pos in range(4):
+        req.begin_token()
+        for layer in range(2):
+            req.append_and_attend(layer, synth.lane_rows(0, Q, layer, 0, 2, pos, 2),
+                                  synth.lane_rows(0, KHIST, layer, 0, 2, pos, 2),
+                                  synth.lane_rows(0, VHIST, layer, 0, 2, pos, 2))
+        req.commit_token()
+    assert req.score_cells == 4 * (1 + 2 + 2 + 2)
