@@ -7,6 +7,7 @@
  *   [SERVE-FLOW]   "Incremental Serving", section "Request flow".
  *   [SERVE-PAGED]  "Incremental Serving", section "Paged KV-cache layout".
  *   [SERVE-CABI]   "Incremental Serving", section "Stable C and Python sessions".
+ *   [SERVE-SCOPE]  "Incremental Serving", section "Current scope".
  *   [CACHED-MIX]   "38 · Cached generation", section "Prepare every block, then
  *                  commit every cache together" (function incremental_mixture,
  *                  and the prepared-ticket commit).
@@ -187,9 +188,26 @@ int pkv_pool_free_list(const pkv_pool* pool, int32_t* host_out, int64_t cap, int
 /* New empty request (length 0, no pages) drawing pages from `pool`. */
 int pkv_request_create(pkv_pool* pool, pkv_request** out);
 
-/* Abort a pending token if any, return every page to the pool, free the
- * request ([SERVE-PAGED]: pages go back when a request is destroyed).  NULL ok. */
+/* Abort a pending token if any, drop the request's reference to every page it
+ * holds (pages nobody else references go back to the pool), free the request
+ * ([SERVE-PAGED]: pages go back when a request is destroyed).  NULL ok. */
 int pkv_request_destroy(pkv_request* req);
+
+/*
+ * Prefix sharing ([SERVE-SCOPE]: page sharing between matching prompts and
+ * copy-on-write prefix management, listed there as future work).  Create a
+ * request that shares every page of `parent` at the parent's visible length:
+ * nothing is copied, each shared page gains a reference.  Either request may
+ * then decode on its own: a token that would be written into a page another
+ * request still references first moves the writer to a private copy
+ * (pkv_begin_token leases it, each layer's pkv_append_and_attend copies that
+ * layer's page before its kernel).  Full shared pages are never written.
+ * BAD_STATE if the parent has a token pending.
+ */
+int pkv_request_fork(const pkv_request* parent, pkv_request** child);
+
+/* Number of requests referencing physical page `page` (0: free). */
+int pkv_pool_page_refs(const pkv_pool* pool, int32_t page, int* refs);
 
 /*
  * Lease n more pages now, appended to the request's logical page table in the
@@ -200,9 +218,10 @@ int pkv_request_destroy(pkv_request* req);
  */
 int pkv_lease_pages(pkv_request* req, int64_t n);
 
-/* Reset: push every page to the back of the free list in logical order, set
- * the visible length to 0 and zero the counters ([SERVE-PAGED]; [CACHED-BIND]
- * reset).  BAD_STATE while a token is pending. */
+/* Reset: drop the request's reference to every page in logical order (a page
+ * nobody else references goes to the back of the free list), set the visible
+ * length to 0 and zero the counters ([SERVE-PAGED]; [CACHED-BIND] reset).
+ * BAD_STATE while a token is pending. */
 int pkv_release_pages(pkv_request* req);
 
 /* Visible (committed) length. */
@@ -221,7 +240,9 @@ int pkv_request_counters(const pkv_request* req, pkv_counters* out);
 /*
  * Reserve the next logical position ([SERVE-FLOW] step 1).  *position receives
  * it (= the visible length).  If that position starts a page the request does
- * not hold yet, one page is leased from the free list's front.
+ * not hold yet, one page is leased from the free list's front; if it falls in a
+ * page another request also references (after pkv_request_fork), a private
+ * page is leased from the front to replace it (copy-on-write).
  * BAD_STATE if a token is already pending; CAPACITY_EXCEEDED at max_context;
  * OUT_OF_PAGES if a page is needed and none is free.
  */
@@ -253,10 +274,11 @@ int pkv_append_and_attend(pkv_request* req, int layer, const float* q, const voi
 int pkv_commit_token(pkv_request* req);
 
 /* Drop the pending token ([SERVE-FLOW] step 4): the visible length stays, and a
- * page leased by its pkv_begin_token goes back to the front of the free list,
- * so table and free list are exactly as before pkv_begin_token.  Rows already
- * written for it stay in the page, unreachable, and are overwritten by the
- * retry.  BAD_STATE if no token is pending. */
+ * page leased by its pkv_begin_token (new or copy-on-write) goes back to the
+ * front of the free list while a shared page gets its place back, so table,
+ * page references and free list are exactly as before pkv_begin_token.  Rows
+ * already written for it stay in the page, unreachable, and are overwritten by
+ * the retry.  BAD_STATE if no token is pending. */
 int pkv_abort_token(pkv_request* req);
 
 /* -------------------------------------------------------------- batched -- */

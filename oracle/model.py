@@ -31,6 +31,19 @@ Readings where the sources are silent (each also listed in the design notes):
 * the new row is written into its slot by ``append_and_attend``; it is visible
   only once committed because readers stop at the visible length;
 * ``begin_token`` at ``max_context`` reports capacity exhaustion.
+
+Prefix sharing ("Incremental Serving", section "Current scope", names page
+sharing between matching prompts and copy-on-write prefix management as
+future work; this is the plainest reading):
+
+* ``fork`` makes a request that shares every page of its parent (each page
+  counts its references); a page returns to the free list when its last
+  reference is released;
+* writing a token into a page that another request also references first
+  moves the writer to a private copy: ``begin_token`` leases a fresh page for
+  that logical page (from the free list's front), and the page's K/V bytes are
+  copied into it before the token's row is written; ``abort_token`` restores
+  the shared page and returns the fresh one to the front.
 """
 from __future__ import annotations
 
@@ -106,6 +119,7 @@ class OraclePool:
         self.dtype, self.max_context = dtype, max_context
         self.max_pages_per_request = -(-max_context // page_size)
         self.free = collections.deque(shuffled_pages(pages, seed))
+        self.refs = [0] * pages                       # references per physical page
         sd = np.float32 if dtype == F32 else np.uint16
         if storage:
             self.k = np.zeros((layers, pages, heads, page_size, head_dim), dtype=sd)
@@ -123,6 +137,16 @@ class OraclePool:
         r = OracleRequest(self)
         self.requests.append(r)
         return r
+
+    def _lease(self) -> int:
+        page = self.free.popleft()
+        self.refs[page] = 1
+        return page
+
+    def _drop(self, page: int, front: bool = False) -> None:
+        self.refs[page] -= 1
+        if self.refs[page] == 0:
+            (self.free.appendleft if front else self.free.append)(page)
 
 
 class OracleRequest:
@@ -149,13 +173,14 @@ class OracleRequest:
         if n > len(p.free):
             raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
         for _ in range(n):
-            self.table.append(p.free.popleft())
+            self.table.append(p._lease())
 
     def release_pages(self) -> None:
         """Reset: every page back to the pool (logical order), length and work zeroed."""
         if self.pending is not None:
             raise OracleError(Status.BAD_STATE, "token pending")
-        self.pool.free.extend(self.table)
+        for page in self.table:
+            self.pool._drop(page)
         self.table = []
         self.length = 0
         self.committed_tokens = self.cache_appends = self.score_cells = 0
@@ -166,6 +191,17 @@ class OracleRequest:
         self.release_pages()
         self.pool.requests.remove(self)
 
+    def fork(self) -> "OracleRequest":
+        """A new request sharing every page of this one, at the same visible length."""
+        if self.pending is not None:
+            raise OracleError(Status.BAD_STATE, "token pending")
+        child = self.pool.request()
+        child.table = list(self.table)
+        child.length = self.length
+        for page in self.table:
+            self.pool.refs[page] += 1
+        return child
+
     # -- the transaction ------------------------------------------------------
     def begin_token(self) -> int:
         p = self.pool
@@ -174,12 +210,26 @@ class OracleRequest:
         if self.length >= p.max_context:
             raise OracleError(Status.CAPACITY_EXCEEDED, "maximum context reached")
         leased = None
-        if self.length // p.P >= len(self.table):
+        cow = None
+        idx = self.length // p.P
+        if idx >= len(self.table):
             if not p.free:
                 raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
-            leased = p.free.popleft()
+            leased = p._lease()
             self.table.append(leased)
-        self.pending = dict(pos=self.length, leased=leased, appended=set())
+        elif p.refs[self.table[idx]] > 1:
+            # the page is shared: write into a private copy
+            if not p.free:
+                raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
+            old = self.table[idx]
+            new = p._lease()
+            p.refs[old] -= 1
+            self.table[idx] = new
+            if p.k is not None:
+                p.k[:, new] = p.k[:, old]
+                p.v[:, new] = p.v[:, old]
+            cow = (idx, old, new)
+        self.pending = dict(pos=self.length, leased=leased, cow=cow, appended=set())
         return self.length
 
     def append_and_attend(self, layer: int, q: np.ndarray, k: np.ndarray, v: np.ndarray,
@@ -221,10 +271,16 @@ class OracleRequest:
     def abort_token(self) -> None:
         if self.pending is None:
             raise OracleError(Status.BAD_STATE, "no token pending")
+        p = self.pool
         if self.pending["leased"] is not None:
             page = self.table.pop()
             assert page == self.pending["leased"]
-            self.pool.free.appendleft(page)
+            p._drop(page, front=True)
+        if self.pending["cow"] is not None:
+            idx, old, new = self.pending["cow"]
+            self.table[idx] = old
+            p.refs[old] += 1
+            p._drop(new, front=True)
         self.pending = None
 
 

@@ -35,7 +35,7 @@ from .binding import (  # noqa: F401
 
 __all__ = [
     "Pool", "Request", "PkvError", "pool_create", "pool_destroy", "request_create",
-    "request_destroy", "lease_pages", "release_pages", "begin_token", "append_and_attend",
+    "request_destroy", "request_fork", "lease_pages", "release_pages", "begin_token", "append_and_attend",
     "commit_token", "abort_token", "paged_decode_attention", "workspace_size",
     "check_device_status", "PKV_F32", "PKV_BF16",
 ]
@@ -175,6 +175,12 @@ class Pool:
         self._requests.append(r)
         return r
 
+    def page_refs(self, page: int) -> int:
+        """Requests referencing physical page `page` (0: free)."""
+        n = ctypes.c_int()
+        check(lib.pkv_pool_page_refs(self.handle, page, ctypes.byref(n)), "pkv_pool_page_refs")
+        return n.value
+
     # -- batched ----------------------------------------------------------
     def workspace_size(self, batch: int, max_seq_len: int) -> int:
         b = ctypes.c_size_t()
@@ -259,11 +265,20 @@ class Pool:
 class Request:
     """One request's logical page table, visible length and pending token."""
 
-    def __init__(self, pool: Pool):
+    def __init__(self, pool: Pool, handle=None):
         self.pool = pool
+        if handle is None:
+            handle = ctypes.c_void_p()
+            check(lib.pkv_request_create(pool.handle, ctypes.byref(handle)), "pkv_request_create")
+        self._h = handle
+
+    def fork(self) -> "Request":
+        """A request sharing every page of this one (copy-on-write on later writes)."""
         h = ctypes.c_void_p()
-        check(lib.pkv_request_create(pool.handle, ctypes.byref(h)), "pkv_request_create")
-        self._h = h
+        check(lib.pkv_request_fork(self.handle, ctypes.byref(h)), "pkv_request_fork")
+        child = Request(self.pool, h)
+        self.pool._requests.append(child)
+        return child
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -349,6 +364,10 @@ def request_create(pool: Pool) -> Request:
 
 def request_destroy(req: Request) -> None:
     req.close()
+
+
+def request_fork(parent: Request) -> Request:
+    return parent.fork()
 
 
 def lease_pages(req: Request, n: int) -> None:

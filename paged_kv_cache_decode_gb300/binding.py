@@ -68,6 +68,8 @@ SIGNATURES = {
     "pkv_pool_free_list": [_vp, _vp, _i64, _P(_i64)],
     "pkv_request_create": [_vp, _P(_vp)],
     "pkv_request_destroy": [_vp],
+    "pkv_request_fork": [_vp, _P(_vp)],
+    "pkv_pool_page_refs": [_vp, ctypes.c_int32, _P(_i)],
     "pkv_lease_pages": [_vp, _i64],
     "pkv_release_pages": [_vp],
     "pkv_request_length": [_vp, _P(_i64)],

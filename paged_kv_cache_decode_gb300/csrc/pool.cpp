@@ -68,6 +68,7 @@ struct pkv_pool {
     int64_t pages = 0, max_context = 0, max_pages_per_request = 0;
     bool host_only = false;
     std::deque<int32_t> free_list;     // front = next page to lease
+    std::vector<int32_t> refs;         // requests referencing each physical page (0: free)
     void* k_base = nullptr;            // [layers][pages][H][P][D]
     void* v_base = nullptr;
     size_t layer_bytes = 0;
@@ -98,6 +99,13 @@ struct pkv_request {
     size_t workspace_bytes = 0;
     int workspace_workers = 0;
     uint32_t epoch = 0;                // calls made on dev_workspace (lane-counter epochs)
+    // copy-on-write of the pending token: logical page cow_idx moved from the
+    // shared page cow_old to the private page cow_new; each layer's bytes are
+    // copied by that layer's append
+    bool cow = false;
+    int64_t cow_idx = 0;
+    int32_t cow_old = -1, cow_new = -1;
+    std::vector<uint8_t> cow_copied;
 };
 
 namespace {
@@ -139,6 +147,22 @@ bool encode_pool_map(CUtensorMap* map, void* base, int64_t rows, int D) {
 
 void mark_dirty(pkv_request* r, int64_t from) {
     if (from < r->dev_dirty_from) r->dev_dirty_from = from;
+}
+
+// Take the free list's front page with one reference.
+int32_t lease_front(pkv_pool* p) {
+    const int32_t page = p->free_list.front();
+    p->free_list.pop_front();
+    p->refs[(size_t)page] = 1;
+    return page;
+}
+
+// Drop one reference; a page nobody references goes back to the free list.
+void drop_page(pkv_pool* p, int32_t page, bool front) {
+    if (--p->refs[(size_t)page] == 0) {
+        if (front) p->free_list.push_front(page);
+        else p->free_list.push_back(page);
+    }
 }
 
 int check_device(const pkv_pool* p) {
@@ -272,6 +296,7 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
         std::swap(order[(size_t)i], order[(size_t)j]);
     }
     p->free_list.assign(order.begin(), order.end());
+    p->refs.assign((size_t)pages, 0);
 
     if (!host_only) {
         cudaError_t e = cudaGetDevice(&p->device);
@@ -401,6 +426,7 @@ int pkv_request_create(pkv_pool* p, pkv_request** out) {
     if (!r) return fail(PKV_ERR_OUT_OF_MEMORY, "host allocation failed");
     r->pool = p;
     r->appended.assign((size_t)p->layers, 0);
+    r->cow_copied.assign((size_t)p->layers, 0);
     r->table.reserve((size_t)p->max_pages_per_request);
     if (!p->host_only) {
         int rc = check_device(p);
@@ -432,7 +458,7 @@ int pkv_request_destroy(pkv_request* r) {
     if (!r) return ok();
     pkv_pool* p = r->pool;
     if (r->pending) pkv_abort_token(r);
-    for (int32_t pg : r->table) p->free_list.push_back(pg);
+    for (int32_t pg : r->table) drop_page(p, pg, false);
     if (!p->host_only) {
         cudaFree(r->dev_table);
         cudaFree(r->dev_workspace);
@@ -455,17 +481,14 @@ int pkv_lease_pages(pkv_request* r, int64_t n) {
         return fail(PKV_ERR_OUT_OF_PAGES, "%lld pages requested, %lld free", (long long)n,
                     (long long)p->free_list.size());
     mark_dirty(r, (int64_t)r->table.size());
-    for (int64_t i = 0; i < n; ++i) {
-        r->table.push_back(p->free_list.front());
-        p->free_list.pop_front();
-    }
+    for (int64_t i = 0; i < n; ++i) r->table.push_back(lease_front(p));
     return ok();
 }
 
 int pkv_release_pages(pkv_request* r) {
     if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
     if (r->pending) return fail(PKV_ERR_BAD_STATE, "a token is pending");
-    for (int32_t pg : r->table) r->pool->free_list.push_back(pg);
+    for (int32_t pg : r->table) drop_page(r->pool, pg, false);
     r->table.clear();
     r->length = 0;
     r->counters = pkv_counters{};
@@ -501,12 +524,24 @@ int pkv_begin_token(pkv_request* r, int64_t* position) {
     if (r->length >= p->max_context)
         return fail(PKV_ERR_CAPACITY_EXCEEDED, "request is at its maximum context %lld",
                     (long long)p->max_context);
-    bool lease = r->length / p->page_size >= (int64_t)r->table.size();
-    if (lease && p->free_list.empty()) return fail(PKV_ERR_OUT_OF_PAGES, "no free page");
+    const int64_t idx = r->length / p->page_size;
+    const bool lease = idx >= (int64_t)r->table.size();
+    const bool cow = !lease && p->refs[(size_t)r->table[(size_t)idx]] > 1;
+    if ((lease || cow) && p->free_list.empty()) return fail(PKV_ERR_OUT_OF_PAGES, "no free page");
     if (lease) {
         mark_dirty(r, (int64_t)r->table.size());
-        r->table.push_back(p->free_list.front());
-        p->free_list.pop_front();
+        r->table.push_back(lease_front(p));
+    }
+    r->cow = cow;
+    if (cow) {
+        // the page is shared with another request: write into a private copy
+        r->cow_idx = idx;
+        r->cow_old = r->table[(size_t)idx];
+        r->cow_new = lease_front(p);
+        --p->refs[(size_t)r->cow_old];
+        r->table[(size_t)idx] = r->cow_new;
+        mark_dirty(r, idx);
+        std::fill(r->cow_copied.begin(), r->cow_copied.end(), 0);
     }
     r->pending = true;
     r->position = r->length;
@@ -538,6 +573,21 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
                                         cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e, "page-table upload");
         r->dev_dirty_from = n;
+    }
+    if (r->cow && !r->cow_copied[(size_t)layer]) {
+        // this layer's bytes of the shared page go to the private page first
+        const size_t page_bytes = (size_t)p->page_size * p->heads * p->head_dim * elem_bytes(p->dtype);
+        char* kb = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)layer;
+        char* vb = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)layer;
+        cudaError_t e = cudaMemcpyAsync(kb + page_bytes * (size_t)r->cow_new,
+                                        kb + page_bytes * (size_t)r->cow_old, page_bytes,
+                                        cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(vb + page_bytes * (size_t)r->cow_new,
+                                vb + page_bytes * (size_t)r->cow_old, page_bytes,
+                                cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "copy-on-write page copy");
+        r->cow_copied[(size_t)layer] = 1;
     }
     pkv::DecodeArgs a{};
     a.dtype = p->dtype;
@@ -598,19 +648,51 @@ int pkv_commit_token(pkv_request* r) {
         (int64_t)p->layers * p->query_heads * (p->window > 0 && p->window < t ? p->window : t);
     r->pending = false;
     r->leased_by_begin = false;
+    r->cow = false;
     return ok();
 }
 
 int pkv_abort_token(pkv_request* r) {
     if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
     if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
+    pkv_pool* p = r->pool;
     if (r->leased_by_begin) {
-        r->pool->free_list.push_front(r->table.back());
+        const int32_t pg = r->table.back();
         r->table.pop_back();
+        drop_page(p, pg, true);
         mark_dirty(r, (int64_t)r->table.size());
+    }
+    if (r->cow) {
+        r->table[(size_t)r->cow_idx] = r->cow_old;
+        ++p->refs[(size_t)r->cow_old];
+        drop_page(p, r->cow_new, true);
+        mark_dirty(r, r->cow_idx);
     }
     r->pending = false;
     r->leased_by_begin = false;
+    r->cow = false;
+    return ok();
+}
+
+int pkv_request_fork(const pkv_request* parent, pkv_request** out) {
+    if (!parent || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    *out = nullptr;
+    if (parent->pending) return fail(PKV_ERR_BAD_STATE, "the parent has a token pending");
+    pkv_request* child = nullptr;
+    int rc = pkv_request_create(parent->pool, &child);
+    if (rc != PKV_OK) return rc;
+    child->table = parent->table;
+    child->length = parent->length;
+    child->dev_dirty_from = 0;
+    for (int32_t pg : child->table) ++parent->pool->refs[(size_t)pg];
+    *out = child;
+    return ok();
+}
+
+int pkv_pool_page_refs(const pkv_pool* p, int32_t page, int* refs) {
+    if (!p || !refs) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    if (page < 0 || page >= p->pages) return fail(PKV_ERR_INVALID_ARGUMENT, "page outside the pool");
+    *refs = p->refs[(size_t)page];
     return ok();
 }
 

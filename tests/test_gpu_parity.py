@@ -396,3 +396,56 @@ def test_window_serial_with_abort():
 
 def test_window_serial_gqa_tensor_cores():
     _serial(2, 2, 128, BF16, 64, 300, 50, 9, group=8, window=33)
+
+
+# ----------------------------------------------------------- prefix sharing --
+
+def _token(seed, layers, H, pos, D, dtype, group=1):
+    return [_lane_tensors(seed, layer, H, pos, D, dtype, group=group) for layer in range(layers)]
+
+
+@pytest.mark.parametrize("dtype,group,fork_at", [(F32, 1, 37), (BF16, 4, 48), (BF16, 1, 20)])
+def test_fork_then_divergent_decodes(dtype, group, fork_at):
+    """Parent and child share the prefix; each then decodes its own tokens.  The
+    partially filled shared page is copied on the first write; outputs, tables,
+    references and every used page's bytes match the oracle model."""
+    layers, H, D, P = 2, 2, 128 if group > 1 else 64, 16
+    pool = pkv.Pool(layers, 64, H, D, P, dtype_name(dtype), 512, 3, query_heads=H * group)
+    opool = OraclePool(layers, 64, H, D, P, dtype, max_context=512, seed=3, query_heads=H * group)
+    parent, oparent = pool.request(), opool.request()
+
+    def step(req, oreq, seed, check=True):
+        pos = req.begin_token()
+        assert oreq.begin_token() == pos
+        for layer, (q, k, v) in enumerate(_token(seed, layers, H, pos, D, dtype, group)):
+            out = req.append_and_attend(layer, to_device(q), to_device(k), to_device(v))
+            ref = oreq.append_and_attend(layer, q, k, v)
+            if check:
+                check_close(out.cpu().numpy(), ref, dtype, f"pos={pos} layer={layer}")
+        req.commit_token()
+        oreq.commit_token()
+
+    for _ in range(fork_at):
+        step(parent, oparent, 1, check=False)
+    child, ochild = parent.fork(), oparent.fork()
+    assert child.length == parent.length == fork_at
+    for i in range(20):
+        step(parent, oparent, 100)
+        step(child, ochild, 200)
+        if i == 3:   # abort a token of the child, then go on
+            child.begin_token()
+            ochild.begin_token()
+            child.abort_token()
+            ochild.abort_token()
+    for r, o in ((parent, oparent), (child, ochild)):
+        assert r.page_table() == o.table and r.length == o.length
+    assert pool.free_list() == list(opool.free)
+    assert [pool.page_refs(i) for i in range(64)] == opool.refs
+    used = sorted(set(parent.page_table()) | set(child.page_table()))
+    idx = torch.tensor(used, dtype=torch.int64)
+    for layer in range(layers):
+        kd, vd = pool.kv_pages(layer)
+        assert _host(kd[idx.cuda()], dtype).tobytes() == opool.k[layer][used].tobytes()
+        assert _host(vd[idx.cuda()], dtype).tobytes() == opool.v[layer][used].tobytes()
+    assert pool.check_device_status() == 0
+    pool.close()

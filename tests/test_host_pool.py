@@ -162,3 +162,77 @@ def test_ragged_churn_tables_match_oracle():
         assert p.free_list() == list(op_.free)
         used = sorted(x for r in reqs for x in r.page_table())
         assert len(used) == len(set(used)) == int(w.n_pages.sum())
+
+
+# ------------------------------------------------------------ prefix sharing --
+
+def _refs(pool, n):
+    return [pool.page_refs(i) for i in range(n)]
+
+
+def test_fork_shares_pages_and_copy_on_write_leases_a_private_page():
+    P, pages = 16, 12
+    with host_pool(pages=pages, max_context=16 * 8, seed=3) as p:
+        op_ = OraclePool(1, pages, 2, 4, P, F32, max_context=16 * 8, seed=3, storage=False)
+        r, o = p.request(), op_.request()
+        r.lease_pages(3)
+        o.lease_pages(3)
+        # a mid-page length cannot be reached on a host-only pool, so share three pages
+        c, oc = r.fork(), o.fork()
+        assert c.page_table() == r.page_table() == oc.table
+        assert _refs(p, pages) == op_.refs and sorted(set(op_.refs)) == [0, 2]
+        # begin at position 0 of page 0, which is shared: copy-on-write
+        assert c.begin_token() == oc.begin_token() == 0
+        assert c.page_table() == oc.table and c.page_table()[0] != r.page_table()[0]
+        assert _refs(p, pages) == op_.refs and p.free_list() == list(op_.free)
+        c.abort_token()
+        oc.abort_token()
+        assert c.page_table() == r.page_table() == oc.table
+        assert _refs(p, pages) == op_.refs and p.free_list() == list(op_.free)
+        # releasing the parent keeps the pages the child still references
+        r.release_pages()
+        o.release_pages()
+        assert p.free_pages == len(op_.free) == pages - 3
+        c.release_pages()
+        oc.release_pages()
+        assert p.free_list() == list(op_.free) and p.free_pages == pages
+
+
+def test_random_sequences_with_forks_match_oracle():
+    rng = np.random.default_rng(11)
+    P, pages, maxc = 16, 30, 16 * 10
+    with host_pool(pages=pages, max_context=maxc, seed=5) as p:
+        op_ = OraclePool(1, pages, 2, 4, P, F32, max_context=maxc, seed=5, storage=False)
+        reqs, oreqs = [p.request()], [op_.request()]
+        for step in range(3000):
+            i = int(rng.integers(0, len(reqs)))
+            r, o = reqs[i], oreqs[i]
+            kind = int(rng.integers(0, 7))
+            if kind == 5 and len(reqs) < 8:
+                a = b = 0
+                try:
+                    c = r.fork()
+                except pkv.PkvError as e:
+                    a = e.status
+                try:
+                    oc = o.fork()
+                except OracleError as e:
+                    b = e.status
+                assert a == b
+                if a == 0:
+                    reqs.append(c)
+                    oreqs.append(oc)
+                continue
+            if kind == 6 and len(reqs) > 1:
+                r.close()
+                o.destroy()
+                reqs.pop(i)
+                oreqs.pop(i)
+                continue
+            op = [("lease_pages", (int(rng.integers(0, 4)),)), ("release_pages", ()),
+                  ("begin_token", ()), ("abort_token", ()), ("begin_token", ())][kind % 5]
+            a, b = _apply(op, r, o)
+            assert a == b, (step, op, a, b)
+            assert r.page_table() == o.table
+        assert p.free_list() == list(op_.free)
+        assert _refs(p, pages) == op_.refs
