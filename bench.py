@@ -65,6 +65,11 @@ def describe(w) -> str:
     if w.name.startswith("batched"):
         return (f"batched decode: {w.B} requests, t ~ U[1,4096], H={w.H}, d_h={w.D}, {st}, "
                 f"pool of {w.pool_pages} shuffled pages")
+    if w.name.startswith("prefix"):
+        return (f"shared-prompt decode: {w.B} requests forked from one {w.shared_prefix}-token "
+                f"prompt, each with its own suffix (t ~ {w.shared_prefix} + U[1,"
+                f"{w.max_context - w.shared_prefix}]), {w.H} KV heads x {w.group} query heads, "
+                f"d_h={w.D}, {st}")
     if w.name.startswith("window"):
         return (f"sliding-window decode: {w.B} requests, t ~ U[1,{w.max_context}], window "
                 f"{w.window}, {w.H} KV heads x {w.group} query heads each, d_h={w.D}, {st}, "
@@ -81,15 +86,23 @@ def describe(w) -> str:
 def algorithmic_bytes(w) -> int:
     """Bytes one step must move: retained history K and V rows, the new rows read
     and written, q and out, page-table entries and lengths."""
-    lens = w.seq_lens.astype(np.int64)
-    if getattr(w, "window", 0):
-        lens = np.minimum(lens, w.window)                        # rows a query attends to
+    from synth.workloads import unique_rows
     es = w.elem_bytes
-    hist = int((lens - 1).sum()) * w.H * w.D * 2 * es          # H = KV heads
+    # history rows read once (a window limits them; a shared prefix counts once);
+    # the new row of each lane is read from k_new / v_new instead
+    hist = (unique_rows(w) - w.B) * w.H * w.D * 2 * es
     new_rows = w.B * w.H * w.D * es * 2 * 2
     q_out = w.B * w.HQ * w.D * 4 * 2                             # query heads
     tables = int(w.n_pages.sum()) * 4 + w.B * 4
     return hist + new_rows + q_out + tables
+
+
+def logical_bytes(w) -> int:
+    """K/V bytes the attention reads counting every request's rows, shared or not."""
+    lens = w.seq_lens.astype(np.int64)
+    if w.window:
+        lens = np.minimum(lens, w.window)
+    return int((lens - 1).sum()) * w.H * w.D * 2 * w.elem_bytes
 
 
 # ---------------------------------------------------------------- ranks --
@@ -237,9 +250,19 @@ def setup_device(w, torch, cuda_cores=False):
             reqs[r_i].lease_pages(cnt) if kind == LEASE else reqs[r_i].release_pages()
         except pkv.PkvError:
             pass
-    for b, r in enumerate(reqs):
-        r.release_pages()
-        r.lease_pages(int(w.n_pages[b]))
+    if w.shared_prefix:
+        # every request forks from request 0's prompt pages, then leases its own suffix
+        sp = w.shared_prefix // w.P
+        reqs[0].lease_pages(sp)
+        for b in range(1, w.B):
+            reqs[b].close()
+            reqs[b] = reqs[0].fork()
+        for b, r in enumerate(reqs):
+            r.lease_pages(int(w.n_pages[b]) - sp)
+    else:
+        for b, r in enumerate(reqs):
+            r.release_pages()
+            r.lease_pages(int(w.n_pages[b]))
     max_pages = int(w.n_pages.max())
     tables = np.full((w.B, max_pages), -1, dtype=np.int32)
     for b, r in enumerate(reqs):
@@ -360,10 +383,12 @@ def run_gpu(args):
                        "seq_len_max": int(w.seq_lens.max()), "tokens_retained": int(w.seq_lens.sum()),
                        "storage": "bf16" if w.elem_bytes == 2 else "fp32", "accumulate": "fp32",
                        "alg_bytes_per_step": alg,
+                       "logical_kv_bytes_per_step": logical_bytes(w),
                        "l2": f"inputs larger than L2 ({alg / 1e9:.2f} GB per step, no flush)"
                              if alg > 129e6 else "inputs smaller than L2 (cache-warm)",
                        "parallelism": f"replicas x{world}"},
             "pct_of_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "logical_GBps": round(world * logical_bytes(w) / (step_ms_max * 1e-3) / 1e9, 2),
             "tokens_per_s": round(world * w.B / (step_ms_max * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -65,6 +65,9 @@ def lib():
             L.synth_rows.argtypes = [u64, u64, i64, i64, i64, i64, ctypes.c_int, vp]
             L.synth_history_pages.restype = None
             L.synth_history_pages.argtypes = [u64, u64, i64, i64, i64, i64, i64, ctypes.c_int, vp]
+            L.synth_history_pages_from.restype = None
+            L.synth_history_pages_from.argtypes = [u64, u64, i64, i64, i64, i64, i64, i64,
+                                                   ctypes.c_int, vp]
             L.synth_f32_to_bf16_array.restype = None
             L.synth_f32_to_bf16_array.argtypes = [vp, i64, vp]
             L.synth_max_threads.restype = ctypes.c_int
@@ -102,15 +105,34 @@ def lane_rows(seed: int, kind: int, layer: int, request: int, H: int, token: int
 
 
 def history_pages(seed: int, kind: int, layer: int, request: int, n_pages: int, H: int, P: int,
-                  D: int, n_tokens: int, dtype: int, out: np.ndarray | None = None) -> np.ndarray:
-    """Physical-layout pages [n_pages, H, P, D] holding tokens ``0 .. n_tokens-1`` (rest zero)."""
+                  D: int, n_tokens: int, dtype: int, out: np.ndarray | None = None,
+                  first_page: int = 0) -> np.ndarray:
+    """Physical-layout pages [n_pages, H, P, D] holding logical pages first_page ..
+    first_page + n_pages - 1 of tokens ``0 .. n_tokens-1`` (rest zero)."""
     if out is None:
         out = np.empty((n_pages, H, P, D), dtype=_np_dtype(dtype))
     assert out.shape == (n_pages, H, P, D) and out.dtype == _np_dtype(dtype)
     assert out.flags["C_CONTIGUOUS"]
     if n_pages > 0:
-        lib().synth_history_pages(seed & MASK64, stream_id(kind, layer, request), n_pages, H, P, D,
-                                  n_tokens, dtype, out.ctypes.data)
+        lib().synth_history_pages_from(seed & MASK64, stream_id(kind, layer, request), first_page,
+                                       n_pages, H, P, D, n_tokens, dtype, out.ctypes.data)
+    return out
+
+
+def request_history_pages(w, kind: int, layer: int, request: int, n_pages: int, n_tokens: int,
+                          out: np.ndarray | None = None) -> np.ndarray:
+    """History pages of one request of workload w.  With a shared prefix of S tokens
+    (w.shared_prefix, a multiple of the page size), tokens j < S are request 0's: every
+    request decodes after the same prompt."""
+    S = getattr(w, "shared_prefix", 0)
+    if out is None:
+        out = np.empty((n_pages, w.H, w.P, w.D), dtype=_np_dtype(w.dtype))
+    sp = min(S // w.P, n_pages) if request != 0 else 0
+    if sp:
+        history_pages(w.seed, kind, layer, 0, sp, w.H, w.P, w.D, n_tokens, w.dtype, out[:sp])
+    if n_pages > sp:
+        history_pages(w.seed, kind, layer, request, n_pages - sp, w.H, w.P, w.D, n_tokens, w.dtype,
+                      out[sp:], first_page=sp)
     return out
 
 

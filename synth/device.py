@@ -10,7 +10,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import F32, KHIST, VHIST, Q, rows, history_pages
+from . import F32, KHIST, VHIST, Q, rows, request_history_pages
 from .workloads import Workload
 
 TORCH_STORAGE = {F32: torch.float32, 1: torch.bfloat16}
@@ -48,17 +48,21 @@ def fill_history(k_pages: torch.Tensor, v_pages: torch.Tensor, w: Workload, tabl
                  layer: int = 0, requests=None) -> int:
     """Write tokens 0 .. t_b - 2 of every request into its pages (slot t_b - 1 is left
     for the step's own append).  k_pages / v_pages: [pages, H, P, D] device views of
-    one layer.  Returns the bytes written."""
-    P, H, D = w.P, w.H, w.D
+    one layer.  Pages of a shared prefix are written once, by request 0.  Returns the
+    bytes written."""
+    P = w.P
+    S = getattr(w, "shared_prefix", 0)
     written = 0
     reqs = range(w.B) if requests is None else requests
     for b in reqs:
         t = int(w.seq_lens[b])
         n = (t + P - 1) // P
-        idx = torch.from_numpy(np.ascontiguousarray(tables[b, :n], dtype=np.int64)).to(k_pages.device)
+        skip = S // P if (b != 0 and S) else 0           # request 0 owns the shared pages
+        idx = torch.from_numpy(np.ascontiguousarray(tables[b, skip:n], dtype=np.int64)).to(
+            k_pages.device)
         for kind, dst in ((KHIST, k_pages), (VHIST, v_pages)):
-            host = history_pages(w.seed, kind, layer, b, n, H, P, D, t - 1, w.dtype)
-            dev = to_device(host, w.dtype, k_pages.device)
+            host = request_history_pages(w, kind, layer, b, n, t - 1)[skip:]
+            dev = to_device(np.ascontiguousarray(host), w.dtype, k_pages.device)
             dst.index_copy_(0, idx, dev)
             written += host.nbytes
     return written

@@ -92,19 +92,21 @@ void synth_rows(uint64_t seed, uint64_t stream, int64_t head, int64_t token0,
 
 /*
  * Fill history pages of one request in physical layout.
- * out has shape [n_pages][H][P][D] in the storage dtype.  Logical token j of
- * head h goes to page j / P, slot j % P.  Tokens j < n_tokens get the value of
- * (stream, head h, token j); all other slots are zero.
+ * out has shape [n_pages][H][P][D] in the storage dtype and holds logical pages
+ * first_page .. first_page + n_pages - 1.  Logical token j of head h goes to
+ * page j / P, slot j % P.  Tokens j < n_tokens get the value of (stream, head h,
+ * token j); all other slots are zero.
  */
-void synth_history_pages(uint64_t seed, uint64_t stream, int64_t n_pages, int64_t H,
-                         int64_t P, int64_t D, int64_t n_tokens, int dtype, void* out) {
+void synth_history_pages_from(uint64_t seed, uint64_t stream, int64_t first_page, int64_t n_pages,
+                              int64_t H, int64_t P, int64_t D, int64_t n_tokens, int dtype,
+                              void* out) {
     uint64_t s = synth_stream_seed(seed, stream);
     int64_t es = dtype == 0 ? 4 : 2;
     #pragma omp parallel for schedule(static) collapse(2)
     for (int64_t pg = 0; pg < n_pages; ++pg) {
         for (int64_t h = 0; h < H; ++h) {
             for (int64_t slot = 0; slot < P; ++slot) {
-                int64_t j = pg * P + slot;
+                int64_t j = (first_page + pg) * P + slot;
                 int64_t base = ((pg * H + h) * P + slot) * D;
                 if (j >= n_tokens) {
                     memset((char*)out + base * es, 0, (size_t)(D * es));
@@ -118,6 +120,11 @@ void synth_history_pages(uint64_t seed, uint64_t stream, int64_t n_pages, int64_
             }
         }
     }
+}
+
+void synth_history_pages(uint64_t seed, uint64_t stream, int64_t n_pages, int64_t H,
+                         int64_t P, int64_t D, int64_t n_tokens, int dtype, void* out) {
+    synth_history_pages_from(seed, stream, 0, n_pages, H, P, D, n_tokens, dtype, out);
 }
 
 /* n fp32 -> bf16 bits, round to nearest even. */

@@ -32,6 +32,7 @@ class Workload:
     churn_cycles: int = 0  # seeded lease/release cycles before the final tables are leased
     group: int = 1         # query heads per KV head (H is the number of KV heads)
     window: int = 0        # sliding window in positions (0: whole prefix)
+    shared_prefix: int = 0  # tokens every request shares with request 0 (a prompt), pages shared
 
     @property
     def HQ(self) -> int:
@@ -116,6 +117,27 @@ def sliding_window(seed: int = 6, B: int = 64, t_max: int = 32768, window: int =
                     window=window)
 
 
+def shared_prompt(seed: int = 7, B: int = 64, prefix: int = 8192, suffix_max: int = 1024) -> Workload:
+    """Prefix-shared decode: 64 requests forked from one 8192-token prompt, each with its
+    own suffix of U{1..1024} tokens (the new token included); 8 KV heads x 4 query heads,
+    d_h=128, bf16, pool of 8192 shuffled pages."""
+    rng = np.random.default_rng(seed)
+    lens = (prefix + rng.integers(1, suffix_max + 1, size=B)).astype(np.int32)
+    return Workload("prefix_bf16", B, 1, 8, 128, 16, BF16, 8192, prefix + suffix_max, seed, lens,
+                    group=4, shared_prefix=prefix)
+
+
+def unique_rows(w: Workload) -> int:
+    """Retained (KV lane, token) rows stored once: a shared prefix counts once."""
+    lens = w.seq_lens.astype(np.int64)
+    if w.window:
+        lens = np.minimum(lens, w.window)
+    rows = int(lens.sum())
+    if w.shared_prefix:
+        rows -= (w.B - 1) * w.shared_prefix
+    return rows
+
+
 REGISTRY = {
     "tiny": tiny,
     "single_t128": lambda: single(128),
@@ -129,4 +151,5 @@ REGISTRY = {
     "gqa4_bf16": lambda: gqa(4, BF16),
     "gqa8_f32": lambda: gqa(8, F32),
     "window_bf16": sliding_window,
+    "prefix_bf16": shared_prompt,
 }

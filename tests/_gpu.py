@@ -61,12 +61,26 @@ class BatchedRun:
                         reqs[r_i].release_pages()
                 except (pkv.PkvError, oracle.OracleError):
                     pass
-        for b in range(w.B):
-            n = int(w.n_pages[b])
-            self.reqs[b].release_pages()
-            self.reqs[b].lease_pages(n)
-            self.oreqs[b].release_pages()
-            self.oreqs[b].lease_pages(n)
+        if w.shared_prefix:
+            # every request forks from request 0's prompt pages, then leases its suffix
+            sp = w.shared_prefix // w.P
+            self.reqs[0].lease_pages(sp)
+            self.oreqs[0].lease_pages(sp)
+            for b in range(1, w.B):
+                self.reqs[b].close()
+                self.oreqs[b].destroy()
+                self.reqs[b] = self.reqs[0].fork()
+                self.oreqs[b] = self.oreqs[0].fork()
+            for b in range(w.B):
+                self.reqs[b].lease_pages(int(w.n_pages[b]) - sp)
+                self.oreqs[b].lease_pages(int(w.n_pages[b]) - sp)
+        else:
+            for b in range(w.B):
+                n = int(w.n_pages[b])
+                self.reqs[b].release_pages()
+                self.reqs[b].lease_pages(n)
+                self.oreqs[b].release_pages()
+                self.oreqs[b].lease_pages(n)
         self.max_pages = int(w.n_pages.max()) + page_table_pad
         self.tables = np.full((w.B, self.max_pages), -1, dtype=np.int32)
         self.otables = np.full((w.B, self.max_pages), -1, dtype=np.int32)
@@ -111,8 +125,8 @@ class BatchedRun:
             ids = np.array([compact[int(pg)] for pg in self.otables[b, :n]], dtype=np.int64)
             ctab[i, :n] = ids
             t = int(w.seq_lens[b])
-            kp[ids] = synth.history_pages(w.seed, KHIST, self.layer, b, n, w.H, w.P, w.D, t - 1, w.dtype)
-            vp[ids] = synth.history_pages(w.seed, VHIST, self.layer, b, n, w.H, w.P, w.D, t - 1, w.dtype)
+            kp[ids] = synth.request_history_pages(w, KHIST, self.layer, b, n, t - 1)
+            vp[ids] = synth.request_history_pages(w, VHIST, self.layer, b, n, t - 1)
         lanes = [i * w.HQ + h for i in range(len(requests)) for h in heads]
         ref = oracle.paged_decode_attention(kp, vp, self.q[requests], self.k_new[requests],
                                             self.v_new[requests], ctab,

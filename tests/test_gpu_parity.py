@@ -449,3 +449,15 @@ def test_fork_then_divergent_decodes(dtype, group, fork_at):
         assert _host(vd[idx.cuda()], dtype).tobytes() == opool.v[layer][used].tobytes()
     assert pool.check_device_status() == 0
     pool.close()
+
+
+
+def test_shared_prompt_batched_every_lane():
+    """64 requests forked from one 8192-token prompt (shared pages), each with its own
+    suffix, decoded in one batched call: every lane against the oracle."""
+    run, _ = _batched_check(workloads.shared_prompt())
+
+
+def test_shared_prompt_small_mixed():
+    w = workloads.shared_prompt(seed=8, B=5, prefix=64, suffix_max=40)
+    _batched_check(w)
