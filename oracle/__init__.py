@@ -68,6 +68,9 @@ def load(path: str):
     L.orc_paged_decode_attention_gqa.restype = i32
     L.orc_paged_decode_attention_gqa.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, i64, vp, vp,
                                                  vp, vp, i32, vp, vp, vp, i64, i32]
+    L.orc_paged_prefill.restype = i32
+    L.orc_paged_prefill.argtypes = [i32, i32, i32, i64, i32, i32, i32, vp, vp, i64, vp, vp, vp, vp,
+                                    vp, i32, vp, vp, i32]
     L.orc_max_threads.restype = i32
     return L
 
@@ -141,6 +144,38 @@ def paged_decode_attention(k_pool: np.ndarray, v_pool: np.ndarray, q: np.ndarray
     return out
 
 
+def paged_prefill(k_pool: np.ndarray, v_pool: np.ndarray, q: np.ndarray, k_new: np.ndarray,
+                  v_new: np.ndarray, cu_new: np.ndarray, tables: np.ndarray, seq_lens: np.ndarray,
+                  dtype: int = F32, group: int = 1, window: int = 0, threads: int = 0,
+                  library=None) -> np.ndarray:
+    """Chunked prefill: request b appends cu_new[b+1]-cu_new[b] tokens after its
+    seq_lens[b] - n_b cached ones; each new token attends causally.  q [N, H*group, D]
+    fp32, k_new / v_new [N, H, D] storage dtype, N = cu_new[-1].  Pools are modified in
+    place.  Returns out [N, H*group, D] fp64."""
+    _check_pool(k_pool, dtype)
+    _check_pool(v_pool, dtype)
+    n_pages, H, P, D = k_pool.shape
+    cu_new = np.ascontiguousarray(cu_new, dtype=np.int32)
+    B = cu_new.size - 1
+    N = int(cu_new[-1])
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    assert q.shape == (N, H * group, D)
+    k_new = np.ascontiguousarray(k_new, dtype=_storage_dtype(dtype))
+    v_new = np.ascontiguousarray(v_new, dtype=_storage_dtype(dtype))
+    assert k_new.shape == (N, H, D) and v_new.shape == (N, H, D)
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    assert tables.shape[0] == B and seq_lens.shape == (B,)
+    out = np.zeros((N, H * group, D), dtype=np.float64)
+    rc = (library or lib()).orc_paged_prefill(
+        B, H, group, window, D, P, dtype, k_pool.ctypes.data, v_pool.ctypes.data, n_pages,
+        q.ctypes.data, k_new.ctypes.data, v_new.ctypes.data, cu_new.ctypes.data,
+        tables.ctypes.data, tables.shape[1], seq_lens.ctypes.data, out.ctypes.data, threads)
+    if rc != 0:
+        raise ValueError("oracle: sequence length or page id out of range")
+    return out
+
+
 def append(k_pool: np.ndarray, v_pool: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
            tables: np.ndarray, seq_lens: np.ndarray, dtype: int = F32) -> None:
     """Only the append step: write the new rows into slot t_b - 1."""
@@ -167,5 +202,6 @@ from .model import (  # noqa: E402
     Status, OraclePool, OracleRequest, OracleError, cached_score_cells,
 )
 
-__all__ = ["F32", "BF16", "build", "paged_decode_attention", "append", "max_threads", "Status",
+__all__ = ["F32", "BF16", "build", "paged_decode_attention", "paged_prefill", "append",
+           "max_threads", "Status",
            "OraclePool", "OracleRequest", "OracleError", "cached_score_cells"]

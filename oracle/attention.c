@@ -196,6 +196,45 @@ int orc_paged_decode_attention(int B, int H, int D, int P, int dtype, void* k_po
                                           threads);
 }
 
+/*
+ * Batched prefill writing the paged cache ("Incremental Serving", section
+ * "Paged KV-cache layout": a future batched prefill may use FlashAttention
+ * while writing the same paged cache that paged decode attention reads).
+ * Request b holds L0_b = seq_lens[b] - n_b cached tokens and appends
+ * n_b = cu_new[b+1] - cu_new[b] new ones.  Token i of the chunk goes to
+ * position L0_b + i: its key/value rows are stored there, and its output is the
+ * attention of its query over positions 0 .. L0_b + i (the window's last W
+ * positions if window > 0) — exactly steps 1-5 of one decode step at
+ * t = L0_b + i + 1, taken for i = 0 .. n_b - 1 in order.
+ *   q      [total_new][H*group][D] fp32; k_new, v_new [total_new][H][D] storage dtype
+ *   out    [total_new][H*group][D] fp64
+ * Returns 0, or -1 on an out-of-range length or page id.
+ */
+int orc_paged_prefill(int B, int H, int group, int64_t window, int D, int P, int dtype,
+                      void* k_pool, void* v_pool, int64_t n_pages, const float* q,
+                      const void* k_new, const void* v_new, const int32_t* cu_new,
+                      const int32_t* tables, int max_pages, const int32_t* seq_lens, double* out,
+                      int threads) {
+    const int HQ = H * group;
+    const int es = dtype == ORC_F32 ? 4 : 2;
+    for (int b = 0; b < B; ++b) {
+        const int n = cu_new[b + 1] - cu_new[b];
+        const int64_t L0 = (int64_t)seq_lens[b] - n;
+        if (n < 0 || L0 < 0) return -1;
+        for (int i = 0; i < n; ++i) {
+            const int64_t x = cu_new[b] + i;   /* row of this token in q / k_new / out */
+            const int32_t t = (int32_t)(L0 + i + 1);
+            int rc = orc_paged_decode_attention_ex(
+                1, H, group, window, D, P, dtype, k_pool, v_pool, n_pages, q + x * HQ * D,
+                (const char*)k_new + x * H * D * es, (const char*)v_new + x * H * D * es,
+                tables + (int64_t)b * max_pages, max_pages, &t, out + x * HQ * D, NULL, 0,
+                threads);
+            if (rc != 0) return rc;
+        }
+    }
+    return 0;
+}
+
 /* Threads the lane loop would use by default. */
 int orc_max_threads(void) {
 #ifdef _OPENMP

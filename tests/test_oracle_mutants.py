@@ -31,6 +31,9 @@ MUTANTS = {
                           "return ((page * P + slot) * H + head) * (int64_t)D;"),
     "bf16_shift": ("<< 16;   /* bf16", "<< 15;   /* bf16"),
     "head_of_query": ("q + lane * D,", "q + (int64_t)b * H * D,"),
+    "prefill_position": ("const int32_t t = (int32_t)(L0 + i + 1);",
+                         "const int32_t t = (int32_t)(L0 + n);"),
+    "prefill_row": ("const int64_t x = cu_new[b] + i;", "const int64_t x = cu_new[b] + (i > 0 ? i - 1 : 0);"),
 }
 
 
@@ -38,6 +41,8 @@ def _pins_pass(lib) -> bool:
     """The pins of test_oracle_pins, run against one library."""
     try:
         if not _gqa_pin_passes(lib) or not _window_pin_passes(lib):
+            return False
+        if not _prefill_pins_pass(lib):
             return False
         for lens, H, D, P, dtype in [([5, 17, 33], 2, 2, 16, F32), ([31, 48, 2], 2, 8, 16, BF16),
                                      ([1], 2, 4, 16, F32)]:
@@ -85,6 +90,16 @@ def _window_pin_passes(lib) -> bool:
                                   to_f64(case.V[lane], F32), 17)
             if not np.allclose(out[b, h], ref, rtol=0, atol=1e-12):
                 return False
+    return True
+
+
+def _prefill_pins_pass(lib) -> bool:
+    from tests.test_oracle_pins import PREFILL_PINS, check_prefill_pin
+    try:
+        for args in PREFILL_PINS:
+            check_prefill_pin(*args, library=lib)
+    except AssertionError:
+        return False
     return True
 
 

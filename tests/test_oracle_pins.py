@@ -430,3 +430,73 @@ def test_window_score_cells_are_lanes_times_min_t_w():
                                   synth.lane_rows(0, VHIST, layer, 0, 2, pos, 2))
         req.commit_token()
     assert req.score_cells == 4 * (1 + 2 + 2 + 2)
+
+
+# ---------------------------------------------------------------------------
+# batched prefill
+
+
+def prefill_case(L0s, ns, H, D, group=1, dtype=BF16, seed=30, P=16):
+    """Requests with L0 cached tokens (in the pool) appending n new ones."""
+    lens = [l0 + n for l0, n in zip(L0s, ns)]
+    case = PagedCase(lens, H, D, P, dtype, seed=seed)
+    # rows L0 .. L0+n-1 of every lane become the chunk's new rows; clear them from the pool
+    cu = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    N = int(cu[-1])
+    sd = np.float32 if dtype == F32 else np.uint16
+    k_new = np.empty((N, H, D), sd)
+    v_new = np.empty((N, H, D), sd)
+    q = np.empty((N, H * group, D), np.float32)
+    for b, (l0, n) in enumerate(zip(L0s, ns)):
+        for i in range(n):
+            pos = l0 + i
+            pg, slot = case.tables[b, pos // P], pos % P
+            for h in range(H):
+                k_new[cu[b] + i, h] = case.K[b * H + h][pos]
+                v_new[cu[b] + i, h] = case.V[b * H + h][pos]
+                case.k_pool[pg, h, slot] = 0
+                case.v_pool[pg, h, slot] = 0
+            for qh in range(H * group):
+                q[cu[b] + i, qh] = synth.rows(seed, Q, 0, b, qh, pos, 1, D, F32)[0]
+    return case, q, k_new, v_new, cu
+
+
+PREFILL_PINS = [([0, 0], [20, 33], 1, 0), ([5, 40], [12, 1], 2, 0), ([0, 17], [48, 16], 1, 20)]
+
+
+@pytest.mark.parametrize("L0s,ns,group,window", PREFILL_PINS)
+def test_prefill_matches_dense_causal_rows(L0s, ns, group, window):
+    check_prefill_pin(L0s, ns, group, window)
+
+
+def check_prefill_pin(L0s, ns, group, window, library=None):
+    """Chunk outputs are rows L0..L0+n-1 of dense causal (banded) softmax attention."""
+    H, D = 2, 8
+    case, q, k_new, v_new, cu = prefill_case(L0s, ns, H, D, group)
+    out = oracle.paged_prefill(case.k_pool, case.v_pool, q, k_new, v_new, cu, case.tables,
+                               case.seq_lens, BF16, group=group, window=window, library=library)
+    for b, (l0, n) in enumerate(zip(L0s, ns)):
+        t = l0 + n
+        for qh in range(H * group):
+            lane = b * H + qh // group
+            K, V = to_f64(case.K[lane], BF16), to_f64(case.V[lane], BF16)
+            Qrows = np.zeros((t, D))
+            for i in range(n):
+                Qrows[l0 + i] = q[cu[b] + i, qh]
+            S = Qrows @ K.T / np.sqrt(D)
+            ii, jj = np.indices((t, t))
+            keep = jj <= ii
+            if window:
+                keep &= jj > ii - window
+            S = np.where(keep, S, -np.inf)
+            S -= S.max(axis=1, keepdims=True)
+            W = np.exp(S)
+            W /= W.sum(axis=1, keepdims=True)
+            ref = W @ V
+            np.testing.assert_allclose(out[cu[b]:cu[b + 1], qh], ref[l0:t], rtol=0, atol=1e-12)
+    # every new row landed in its slot
+    for b, (l0, n) in enumerate(zip(L0s, ns)):
+        for i in range(n):
+            pos = l0 + i
+            pg, slot = case.tables[b, pos // 16], pos % 16
+            assert np.array_equal(case.k_pool[pg, :, slot], k_new[cu[b] + i])
