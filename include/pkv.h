@@ -351,13 +351,60 @@ int pkv_paged_decode_attention_static(pkv_pool* pool, int layer, int batch, cons
                                       const int32_t* seq_lens, int64_t max_seq_len, float* out,
                                       void* stream);
 
+/* ------------------------------------------------------------- prefill -- */
+
+/*
+ * Device scratch bytes that pkv_paged_prefill needs for `batch` requests and
+ * total_new new tokens (0 when either is 0).
+ */
+int pkv_prefill_workspace_size(const pkv_pool* pool, int batch, int64_t total_new, size_t* bytes);
+
+/*
+ * Batched prefill for one layer, writing the paged cache that decode reads
+ * ([SERVE-PAGED]: a batched prefill may use a tiled, FlashAttention-style
+ * computation while it writes the same paged cache; [SERVE-SCOPE] lists it as
+ * not yet present there).  Request b appends n_b = cu_new[b+1] - cu_new[b] tokens
+ * after its L0_b = seq_lens[b] - n_b cached ones.  For chunk token i of request
+ * b (batch row x = cu_new[b] + i, position L0_b + i):
+ *   1. store k_new[x], v_new[x] at that position, i.e. physical page
+ *      page_tables[b][(L0_b + i) / page_size], slot (L0_b + i) % page_size;
+ *   2. for each query head q (KV head h = q / (query_heads / kv_heads)):
+ *      out[x][q] = sum_j softmax_j(q[x][q] . K_j / sqrt(head_dim)) V_j over the
+ *      positions j = 0 .. L0_b + i (the pool's window, if any, keeps the last
+ *      `window` of them) -- the outputs n_b successive decode steps would give.
+ *   q            [total_new][query_heads][head_dim] bf16, device
+ *   k_new, v_new [total_new][kv_heads][head_dim] bf16, device
+ *   cu_new       [batch + 1] int32, device: row offsets, cu_new[0] = 0,
+ *                non-decreasing, cu_new[batch] <= total_new
+ *   page_tables  [batch][max_pages] int32, device (entries past
+ *                ceil(seq_lens[b] / page_size) unread)
+ *   seq_lens     [batch] int32, device: lengths after the chunk (>= n_b)
+ *   out          [total_new][query_heads][head_dim] fp32, device
+ *   workspace    device scratch of >= pkv_prefill_workspace_size bytes
+ *                (caller owned, 16-byte aligned, no initialisation needed)
+ * Pools: bf16 storage, head_dim 64 or 128, query_heads / kv_heads dividing 128
+ * (else PKV_ERR_UNSUPPORTED); batch <= 1024.  The products run on the tensor
+ * cores in bf16 with fp32 accumulation: the weights are rounded to bf16 before
+ * they multiply V.  Stateless over bookkeeping: the caller owns lengths and
+ * tables.  Bad lengths or page ids found on the device set the pool's error
+ * word (a bad page reads as zeros); the affected rows of `out` are then
+ * unspecified.  Once a wait has run out (PKV_DEVERR_TIMEOUT), later prefill
+ * calls skip their attention work until pkv_check_device_status clears the
+ * word.  Enqueues three kernels on `stream` and returns without waiting; calls
+ * whose device work can overlap must use different workspaces.
+ */
+int pkv_paged_prefill(pkv_pool* pool, int layer, int batch, int64_t total_new, const void* q,
+                      const void* k_new, const void* v_new, const int32_t* cu_new,
+                      const int32_t* page_tables, int max_pages, const int32_t* seq_lens,
+                      float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------- tracing -- */
 
 /*
  * Kernel timing hook.  When `before` and `after` are non-NULL cudaEvent_t
- * handles, every later pkv_append_and_attend / pkv_paged_decode_attention on
- * this pool records `before` on its stream immediately before the split
- * (attention) kernel and `after` immediately after it, so
+ * handles, every later pkv_append_and_attend / pkv_paged_decode_attention /
+ * pkv_paged_prefill on this pool records `before` on its stream immediately
+ * before the attention kernel and `after` immediately after it, so
  * cudaEventElapsedTime(before, after) is that kernel's device time.  NULL,
  * NULL turns the hook off.  The events stay owned by the caller.
  */

@@ -36,7 +36,7 @@ from .binding import (  # noqa: F401
 __all__ = [
     "Pool", "Request", "PkvError", "pool_create", "pool_destroy", "request_create",
     "request_destroy", "request_fork", "lease_pages", "release_pages", "begin_token", "append_and_attend",
-    "commit_token", "abort_token", "paged_decode_attention", "workspace_size",
+    "commit_token", "abort_token", "paged_decode_attention", "paged_prefill", "workspace_size",
     "check_device_status", "PKV_F32", "PKV_BF16",
 ]
 
@@ -216,6 +216,43 @@ class Pool:
             _dev(out, "out", torch.float32, (B, HQ, D)),
             _dev(workspace, "workspace", torch.uint8, None), workspace.numel(),
             _stream_ptr(stream)), "pkv_paged_decode_attention")
+        return out
+
+    def prefill_workspace_size(self, batch: int, total_new: int) -> int:
+        n = ctypes.c_size_t()
+        check(lib.pkv_prefill_workspace_size(self.handle, batch, total_new, ctypes.byref(n)),
+              "pkv_prefill_workspace_size")
+        return n.value
+
+    def paged_prefill(self, layer: int, q, k_new, v_new, cu_new, page_tables, seq_lens, out=None,
+                      workspace=None, stream=None):
+        """Batched prefill of one layer: request b appends rows cu_new[b] .. cu_new[b+1]-1
+        of q / k_new / v_new (bf16) after its seq_lens[b] - n_b cached tokens; returns
+        out [N, query_heads, head_dim] fp32."""
+        N = q.shape[0]
+        B = cu_new.shape[0] - 1
+        H, HQ, D = self.heads, self.query_heads, self.head_dim
+        if out is None:
+            out = torch.empty((N, HQ, D), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            key = ("prefill", B, N)
+            if key not in self._ws:
+                n = self.prefill_workspace_size(B, N)
+                self._ws[key] = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+            workspace = self._ws[key]
+        if page_tables.dim() != 2 or page_tables.shape[0] != B:
+            raise ValueError("page_tables must be [batch, max_pages]")
+        check(lib.pkv_paged_prefill(
+            self.handle, layer, B, N,
+            _dev(q, "q", torch.bfloat16, (N, HQ, D)),
+            _dev(k_new, "k_new", torch.bfloat16, (N, H, D)),
+            _dev(v_new, "v_new", torch.bfloat16, (N, H, D)),
+            _dev(cu_new, "cu_new", torch.int32, (B + 1,)),
+            _dev(page_tables, "page_tables", torch.int32, None), page_tables.shape[1],
+            _dev(seq_lens, "seq_lens", torch.int32, (B,)),
+            _dev(out, "out", torch.float32, (N, HQ, D)),
+            _dev(workspace, "workspace", torch.uint8, None), workspace.numel(),
+            _stream_ptr(stream)), "pkv_paged_prefill")
         return out
 
     def set_timing_events(self, before, after) -> None:
@@ -402,6 +439,12 @@ def paged_decode_attention(pool: Pool, layer, q, k_new, v_new, page_tables, seq_
                            out=None, workspace=None, stream=None):
     return pool.paged_decode_attention(layer, q, k_new, v_new, page_tables, seq_lens, max_seq_len,
                                        out, workspace, stream)
+
+
+def paged_prefill(pool: Pool, layer, q, k_new, v_new, cu_new, page_tables, seq_lens, out=None,
+                  workspace=None, stream=None):
+    return pool.paged_prefill(layer, q, k_new, v_new, cu_new, page_tables, seq_lens, out,
+                              workspace, stream)
 
 
 def check_device_status(pool: Pool) -> int:

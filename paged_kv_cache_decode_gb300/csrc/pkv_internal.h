@@ -98,4 +98,45 @@ int prepare_batched(pkv_pool* pool, int layer, int batch, const float* q, const 
                     const int32_t* seq_lens, int64_t max_seq_len, float* out, DecodeArgs* a,
                     size_t* workspace_bytes);
 
+// ---------------------------------------------------------------- prefill --
+
+// One launch of the batched prefill for one layer (bf16 pools, D 64 or 128).
+struct PrefillArgs {
+    int B, H, G, D, P;
+    int64_t window;
+    const void* q;           // [N][H*G][D] bf16
+    const void* k_new;       // [N][H][D] bf16
+    const void* v_new;
+    void* k_pages;           // this layer's pools, [pages][H][P][D]
+    void* v_pages;
+    int64_t n_pages;
+    const int32_t* cu_new;   // [B + 1] device
+    const int32_t* seq_lens; // [B] device, lengths after the chunk
+    const int32_t* tables;   // [B][max_pages] device
+    int max_pages;
+    int64_t total_new;       // N, rows of q / k_new / v_new / out
+    float* out;              // [N][H*G][D] fp32
+    void* workspace;
+    unsigned* dev_error;
+    cudaEvent_t ev_before;   // optional: recorded around the attention kernel
+    cudaEvent_t ev_after;
+    const void* tmap_k;      // CUtensorMap of this layer's K / V pools (host memory)
+    const void* tmap_v;
+};
+
+// Upper bound on the query tiles of a call (sum over requests of ceil(n_b / (128 / G))).
+int64_t prefill_max_tiles(int B, int G, int64_t total_new);
+
+// Scratch bytes of one call.
+size_t prefill_workspace_bytes(int B, int G, int64_t total_new);
+
+// True if the prefill kernels implement (dtype, D, G).
+bool prefill_supported(int dtype, int D, int G);
+
+// Largest batch one call takes.
+int prefill_max_batch();
+
+// Enqueue the plan, append and attention kernels on `stream`.
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
 }  // namespace pkv

@@ -78,8 +78,9 @@ struct pkv_pool {
     int64_t live_requests = 0;
     cudaEvent_t ev_before = nullptr;   // optional split-kernel timing events
     cudaEvent_t ev_after = nullptr;
-    bool tensor_cores = false;         // K/V tiles by TMA tensor loads, scores and mixture by MMA
-    std::vector<CUtensorMap> tmap_k;   // per layer, when tensor_cores
+    bool tensor_cores = false;         // decode: K/V tiles by TMA tensor loads, products by MMA
+    bool tmaps = false;                // tensor maps built (bf16, head_dim 64 or 128)
+    std::vector<CUtensorMap> tmap_k;   // per layer, when tmaps
     std::vector<CUtensorMap> tmap_v;
 };
 
@@ -307,9 +308,10 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
             return cuda_fail(e, "device query");
         }
         const int64_t rows = pages * page_size * heads;   // pool rows of one layer
-        p->tensor_cores = !(flags & PKV_POOL_CUDA_CORES) &&
-                          pkv::mma_supported(dtype, head_dim, p->group) && rows < INT32_MAX &&
-                          tensor_map_encoder() != nullptr;
+        p->tmaps = dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) && rows < INT32_MAX &&
+                   tensor_map_encoder() != nullptr;
+        p->tensor_cores = p->tmaps && !(flags & PKV_POOL_CUDA_CORES) &&
+                          pkv::mma_supported(dtype, head_dim, p->group);
         p->workers = pkv::resident_workers(dtype, head_dim, p->group, sms, p->tensor_cores);
         if (p->workers <= 0) {
             delete p;
@@ -328,10 +330,10 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
             return fail(PKV_ERR_OUT_OF_MEMORY, "cudaMalloc of 2 x %zu bytes: %s", total,
                         cudaGetErrorString(e));
         }
-        if (p->tensor_cores) {
+        if (p->tmaps) {
             p->tmap_k.resize((size_t)layers);
             p->tmap_v.resize((size_t)layers);
-            for (int l = 0; l < layers && p->tensor_cores; ++l) {
+            for (int l = 0; l < layers; ++l) {
                 char* kb = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)l;
                 char* vb = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)l;
                 if (!encode_pool_map(&p->tmap_k[(size_t)l], kb, rows, head_dim) ||
@@ -760,6 +762,79 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     a.ev_after = p->ev_after;
     cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ok();
+}
+
+int pkv_prefill_workspace_size(const pkv_pool* p, int batch, int64_t total_new, size_t* bytes) {
+    if (!p || !bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    if (batch < 0 || total_new < 0)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch or token count");
+    *bytes = (batch == 0 || total_new == 0) ? 0
+                                            : pkv::prefill_workspace_bytes(batch, p->group, total_new);
+    return ok();
+}
+
+int pkv_paged_prefill(pkv_pool* p, int layer, int batch, int64_t total_new, const void* q,
+                      const void* k_new, const void* v_new, const int32_t* cu_new,
+                      const int32_t* page_tables, int max_pages, const int32_t* seq_lens,
+                      float* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    if (layer < 0 || layer >= p->layers)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (batch < 0 || total_new < 0)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch or token count");
+    if (batch > pkv::prefill_max_batch())
+        return fail(PKV_ERR_INVALID_ARGUMENT, "batch %d above %d", batch, pkv::prefill_max_batch());
+    if (total_new > INT32_MAX) return fail(PKV_ERR_INVALID_ARGUMENT, "more than 2^31 - 1 tokens");
+    if (!pkv::prefill_supported(p->dtype, p->head_dim, p->group) || !p->tmaps)
+        return fail(PKV_ERR_UNSUPPORTED,
+                    "prefill needs bf16 pools of head_dim 64 or 128 (%d query heads per KV head)",
+                    p->group);
+    if (batch == 0 || total_new == 0) return ok();
+    if (!q || !k_new || !v_new || !cu_new || !page_tables || !seq_lens || !out || !workspace)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
+    if (max_pages < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages must be >= 1");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+    if (pkv::prefill_max_tiles(batch, p->group, total_new) * p->heads > INT32_MAX)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "%lld tokens need more CTAs than one launch holds",
+                    (long long)total_new);
+    const size_t need = pkv::prefill_workspace_bytes(batch, p->group, total_new);
+    if (workspace_bytes < need)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need);
+    int rc = check_device(p);
+    if (rc != PKV_OK) return rc;
+    pkv::PrefillArgs a{};
+    a.B = batch;
+    a.H = p->heads;
+    a.G = p->group;
+    a.D = p->head_dim;
+    a.P = p->page_size;
+    a.window = p->window;
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    void *kp, *vp;
+    pkv_pool_kv_ptr(p, layer, &kp, &vp);
+    a.k_pages = kp;
+    a.v_pages = vp;
+    a.n_pages = p->pages;
+    a.cu_new = cu_new;
+    a.seq_lens = seq_lens;
+    a.tables = page_tables;
+    a.max_pages = max_pages;
+    a.total_new = total_new;
+    a.out = out;
+    a.workspace = workspace;
+    a.dev_error = p->dev_error;
+    a.ev_before = p->ev_before;
+    a.ev_after = p->ev_after;
+    a.tmap_k = &p->tmap_k[(size_t)layer];
+    a.tmap_v = &p->tmap_v[(size_t)layer];
+    cudaError_t e = pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return ok();
 }
 

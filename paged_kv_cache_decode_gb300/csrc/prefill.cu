@@ -1,0 +1,725 @@
+// Batched prefill into the paged KV cache, on the sm_103a tensor cores.
+//
+// What is computed ("Incremental Serving", section "Paged KV-cache layout": a
+// batched prefill may run a FlashAttention-style tiled computation while it
+// writes the same paged cache that paged decode attention reads).  Request b
+// holds L0 = seq_lens[b] - n_b cached tokens and appends the n_b rows
+// cu_new[b] .. cu_new[b+1]-1 of the batch.  Chunk token i sits at position
+// L0 + i: its key and value rows are stored there, and its output is the
+// softmax attention of its query over positions 0 .. L0 + i (the last `window`
+// of them with a sliding window) -- what n_b successive decode steps give.
+//
+// Three launches per call:
+//   1. plan (one CTA): validates lengths and lists the query tiles request by
+//      request, the heaviest (last) tile of each request first;
+//   2. append: copies every new key / value row into its page;
+//   3. attention: one CTA per (query tile, KV head).
+//
+// Attention CTA.  A query tile is 128 rows: 128/G consecutive tokens times the
+// G query heads that share one KV head, so every key tile serves all of them.
+// Key tiles are 128 positions, loaded as 8 groups of 16 rows (a group never
+// straddles a page) by TMA tensor copies with the 128-byte swizzle.  Per key tile
+//     S  = Q K^T               tcgen05.mma, M=128 N=128 K=d_h, fp32 in TMEM
+//     P  = 2^(c S - c m)       softmax warps: TMEM -> registers -> bf16 in smem
+//     O += P V                 tcgen05.mma, M=128 N=d_h K=128, fp32 in TMEM
+// with c = log2(e) / sqrt(d_h).  Warp roles (192 threads):
+//   warps 0-3  softmax: warp w reads TMEM lanes 32w..32w+31, one query row per
+//              thread; it stages Q, writes P, rescales O and stores the output;
+//   warp 4     producer: one thread issues the K / V tile copies into a ring;
+//   warp 5     MMA: allocates TMEM, one thread issues the MMAs and commits.
+// S is double-buffered in TMEM, so S of key tile j+1 runs on the tensor cores
+// while the softmax warps work on tile j.
+//
+// Exponent base.  Row m only moves when the row's maximum grows by more than 8
+// in log2 units; O and the row sum l are then scaled by 2^(c (m_old - m_new)).
+// Until then every weight is at most 2^8, which bf16 and the fp32 accumulators
+// hold as well as any other; O / l uses the same m in both, so the result is the
+// softmax whatever m is.
+//
+// Faults are not raised by trapping: bad lengths and page ids set bits of the
+// device error word (a bad page reads as zeros), and a wait that runs out sets
+// the timeout bit and ends the CTA's work; later CTAs of a pool whose error word
+// holds the timeout bit return at once.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kRows = 128;                  // query rows per tile = TMEM lanes
+constexpr int kKeys = 128;                  // key positions per key tile
+constexpr int kPfThreads = 192;
+constexpr int kPlanThreads = 1024;          // one request per plan thread
+constexpr uint64_t kPfWaitLimitNs = 4000000000ull;
+
+template <int D>
+struct PfGeo {
+    static constexpr int CHUNKS = D / 64;                    // 128-byte swizzle columns of Q, K, V
+    static constexpr int COL_BYTES = kRows * 128;            // one such column of a 128-row tile
+    static constexpr int Q_BYTES = CHUNKS * COL_BYTES;
+    static constexpr int P_BYTES = (kKeys / 64) * COL_BYTES;
+    static constexpr int KV_BYTES = CHUNKS * kKeys * 128;    // one K or V tile
+    static constexpr int STAGES = D == 64 ? 4 : 2;
+    static constexpr int RING_BYTES = STAGES * 2 * KV_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 + Q_BYTES + P_BYTES + RING_BYTES + BAR_BYTES;
+    static constexpr uint32_t S_COL = 0;                     // S buffers at columns 0 and 128
+    static constexpr uint32_t O_COL = 256;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(D == 64 || D == 128, "prefill: head width 64 or 128");
+    static_assert(SMEM <= 227 * 1024, "prefill CTA does not fit an SM");
+    static_assert(3 * STAGES * 8 + 6 * 8 + 8 <= BAR_BYTES, "barrier area");
+};
+
+struct PfParams {
+    int B, H, G, P, max_pages;
+    int64_t window;
+    int64_t n_pages;
+    int pool_rows;                 // rows of one layer's 2-D pool view (pages * H * P)
+    const __nv_bfloat16* q;        // [N][H*G][D]
+    const __nv_bfloat16* k_new;    // [N][H][D]
+    const __nv_bfloat16* v_new;
+    __nv_bfloat16* k_pages;        // [pages][H][P][D]
+    __nv_bfloat16* v_pages;
+    const int32_t* cu_new;         // [B + 1]
+    const int32_t* seq_lens;       // [B]
+    const int32_t* tables;         // [B][max_pages]
+    float* out;                    // [N][H*G][D]
+    int2* items;                   // query tiles (request, tile), in launch order
+    int* n_items;
+    int max_items;                 // capacity of items (the launch's CTAs / H)
+    int64_t total_new;             // N
+    float scale_log2;              // log2(e) / sqrt(D)
+    unsigned* dev_error;
+};
+
+// ----------------------------------------------------------- tcgen05 PTX --
+
+// Shared-memory matrix descriptor: 128-byte swizzle, start / leading / stride
+// byte offsets (16-byte units), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, M = 128, A K-major,
+// B K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int N, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint64_t l2_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bounded wait; gives up early once another role of the CTA has given up.
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        unsigned* dev_error) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - start > kPfWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(dev_error, PKV_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// The same, taken by a whole warp: true only if every lane saw the phase.
+__device__ __forceinline__ bool pf_warp_wait(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, unsigned* dev_error) {
+    const bool ok = pf_wait(bar, parity, abort_flag, dev_error);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of 16-byte piece u of row r in a K-major operand of 128 rows
+// stored as 128-byte swizzled columns of 64 bf16 (the layout TMA writes).
+__device__ __forceinline__ uint32_t sw_off(int r, int u) {
+    return (uint32_t)((u >> 3) * (kRows * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ plan --
+
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfParams p) {
+    __shared__ int warp_sum[kPlanThreads / 32];
+    const int b = threadIdx.x;
+    const int T = kRows / p.G;
+    int tiles = 0;
+    if (b < p.B) {
+        const int c0 = p.cu_new[b], c1 = p.cu_new[b + 1];
+        const int64_t n = (int64_t)c1 - c0;
+        const int64_t t = p.seq_lens[b];
+        const bool ok = c0 >= 0 && n >= 0 && c1 <= p.total_new && t - n >= 0 &&
+                        t <= (int64_t)p.max_pages * p.P;
+        if (!ok) atomicOr(p.dev_error, PKV_DEVERR_SEQ_LEN);
+        else tiles = (int)((n + T - 1) / T);
+    }
+    // exclusive prefix of tiles over requests
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
+        }
+        warp_sum[lane] = w;               // inclusive over warps
+    }
+    __syncthreads();
+    const int first = (warp > 0 ? warp_sum[warp - 1] : 0) + incl - tiles;
+    // requests whose row ranges overlap can hold more tiles than the launch has CTAs for
+    const int total = warp_sum[kPlanThreads / 32 - 1];
+    if (total > p.max_items && threadIdx.x == 0) atomicOr(p.dev_error, PKV_DEVERR_SEQ_LEN);
+    for (int k = 0; k < tiles && first + k < p.max_items; ++k)
+        p.items[first + k] = make_int2(b, tiles - 1 - k);
+    if (threadIdx.x == 0) *p.n_items = total < p.max_items ? total : p.max_items;
+}
+
+// ---------------------------------------------------------------- append --
+
+// Every new key / value row into its page: one thread per 16-byte piece.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_append_kernel(const PfParams p) {
+    constexpr int U = D / 8;
+    const int64_t total = p.total_new * p.H * U;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t x = idx / (p.H * U);
+        const int rem = (int)(idx - x * p.H * U);
+        const int h = rem / U, u = rem - (rem / U) * U;
+        int lo = 0, hi = p.B;                       // last request with cu_new[b] <= x
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.cu_new[mid] <= x) lo = mid;
+            else hi = mid;
+        }
+        const int b = lo;
+        const int c0 = p.cu_new[b], c1 = p.cu_new[b + 1];
+        if (x < c0 || x >= c1) continue;
+        const int64_t t = p.seq_lens[b];
+        const int64_t L0 = t - (c1 - c0);
+        if (L0 < 0 || t > (int64_t)p.max_pages * p.P) continue;      // the plan reports it
+        const int64_t pos = L0 + (x - c0);
+        const int32_t page = p.tables[(int64_t)b * p.max_pages + pos / p.P];
+        if (page < 0 || page >= p.n_pages) {
+            atomicOr(p.dev_error, PKV_DEVERR_PAGE_ID);
+            continue;
+        }
+        const int64_t dst = (((int64_t)page * p.H + h) * p.P + pos % p.P) * D + u * 8;
+        const int64_t src = (x * p.H + h) * D + u * 8;
+        *reinterpret_cast<uint4*>(p.k_pages + dst) = *reinterpret_cast<const uint4*>(p.k_new + src);
+        *reinterpret_cast<uint4*>(p.v_pages + dst) = *reinterpret_cast<const uint4*>(p.v_new + src);
+    }
+}
+
+// ------------------------------------------------------------- attention --
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1)
+prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv) {
+    using M = PfGeo<D>;
+    const int item = blockIdx.x / p.H;
+    const int h = blockIdx.x - item * p.H;
+    if (item >= *p.n_items) return;
+    if (*reinterpret_cast<volatile unsigned*>(p.dev_error) & PKV_DEVERR_TIMEOUT) return;
+
+    const int2 it = p.items[item];
+    const int b = it.x, tile = it.y;
+    const int G = p.G, T = kRows / G;
+    const int c0 = p.cu_new[b];
+    const int n = p.cu_new[b + 1] - c0;
+    const int64_t t_b = p.seq_lens[b];
+    const int64_t L0 = t_b - n;
+    const int i0 = tile * T;
+    const int i_end = min(n, i0 + T);                         // tokens i0 .. i_end-1
+    const int64_t pos_last = L0 + i_end - 1;
+    const int64_t lo_first =
+        p.window > 0 ? (L0 + i0 - p.window + 1 > 0 ? L0 + i0 - p.window + 1 : 0) : 0;
+    const int64_t kt0 = lo_first / kKeys;
+    const int ntiles = (int)(pos_last / kKeys - kt0 + 1);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* Qs = sm;
+    unsigned char* Ps = Qs + M::Q_BYTES;
+    unsigned char* ring = Ps + M::P_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + M::RING_BYTES);
+    uint64_t* k_full = bars;
+    uint64_t* v_full = bars + M::STAGES;
+    uint64_t* kv_empty = bars + 2 * M::STAGES;
+    uint64_t* s_full = bars + 3 * M::STAGES;     // two
+    uint64_t* p_full = s_full + 2;
+    uint64_t* o_done = p_full + 1;
+    uint64_t* q_ready = o_done + 1;
+    uint64_t* drain = q_ready + 1;               // MMA completion on the abort path
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < M::STAGES; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        mbar_init(q_ready, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(tmem_slot, M::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        // ------------------------------------------------------ softmax --
+        const int r = threadIdx.x;                            // query row = TMEM lane
+        const int g = r % G;
+        const int i = i0 + r / G;
+        const bool valid = i < i_end;
+        const int HQ = p.H * G;
+        const int64_t row_x = (int64_t)c0 + i;
+        const int qh = h * G + g;
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + (row_x * HQ + qh) * D);
+#pragma unroll
+            for (int u = 0; u < D / 8; ++u) {
+                const uint4 v = valid ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(Qs + sw_off(r, u)) = v;
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(q_ready);
+
+        const int64_t pos = L0 + i;
+        const int64_t hi = valid ? pos : -1;                  // keys lo .. hi
+        const int64_t lo = p.window > 0 ? (pos - p.window + 1 > 0 ? pos - p.window + 1 : 0) : 0;
+        const float c = p.scale_log2;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            if (!pf_warp_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.dev_error)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[kKeys];
+#pragma unroll
+            for (int cc = 0; cc < kKeys / 32; ++cc)
+                tmem_ld32(tmem + lane_base + M::S_COL + (j & 1) * kKeys + cc * 32, sv + cc * 32);
+            tmem_wait_ld();
+            const int64_t k0 = (kt0 + j) * kKeys;
+            const bool full = k0 >= lo && k0 + kKeys - 1 <= hi;
+            // keys e_lo .. e_hi of the tile are this row's (none when e_lo > e_hi)
+            const int e_lo = full ? 0 : (int)(lo - k0 > 0 ? (lo - k0 < kKeys ? lo - k0 : kKeys) : 0);
+            const int e_hi = full ? kKeys - 1
+                                  : (int)(hi - k0 < kKeys - 1 ? (hi - k0 > -1 ? hi - k0 : -1)
+                                                              : kKeys - 1);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < kKeys; ++e)
+                if (full || (e >= e_lo && e <= e_hi)) mx = fmaxf(mx, __uint_as_float(sv[e]));
+            float alpha = 1.f;
+            if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f)) {
+                alpha = m_used == -INFINITY ? 0.f : ex2((m_used - mx) * c);
+                m_used = mx;
+                l *= alpha;
+            }
+            // the previous P V must be complete before O is rescaled or P rewritten
+            if (j > 0) {
+                if (!pf_warp_wait(o_done, (j - 1) & 1, abort_flag, p.dev_error)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t ov[32];
+                        tmem_ld32(tmem + lane_base + M::O_COL + cc * 32, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(tmem + lane_base + M::O_COL + cc * 32, ov);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            const float mb = m_used == -INFINITY ? 0.f : m_used * c;
+            float lsum = 0.f;
+#pragma unroll
+            for (int u = 0; u < kKeys / 8; ++u) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = u * 8 + 2 * k;
+                    const bool a0 = full || (e >= e_lo && e <= e_hi);
+                    const bool a1 = full || (e + 1 >= e_lo && e + 1 <= e_hi);
+                    const float p0 = a0 ? ex2(fmaf(__uint_as_float(sv[e]), c, -mb)) : 0.f;
+                    const float p1 = a1 ? ex2(fmaf(__uint_as_float(sv[e + 1]), c, -mb)) : 0.f;
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                    lsum += __low2float(pb) + __high2float(pb);
+                    w[k] = *reinterpret_cast<const uint32_t*>(&pb);
+                }
+                *reinterpret_cast<uint4*>(Ps + sw_off(r, u)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l += lsum;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (ok && pf_warp_wait(o_done, (ntiles - 1) & 1, abort_flag, p.dev_error)) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float4* dst = reinterpret_cast<float4*>(p.out + (row_x * HQ + qh) * D);
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t ov[32];
+                tmem_ld32(tmem + lane_base + M::O_COL + cc * 32, ov);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        dst[(cc * 32 + e) / 4] = make_float4(
+                            __uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                            __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+                }
+            }
+        }
+    } else if (warp == 4) {
+        // ----------------------------------------------------- producer --
+        if (lane == 0) {
+            const uint64_t pol = l2_normal_policy();
+            const int32_t* table = p.tables + (int64_t)b * p.max_pages;
+            int issued = 0;
+            bool aborted = false;
+            for (int j = 0; j < ntiles; ++j) {
+                const int s = j % M::STAGES;
+                if (j >= M::STAGES &&
+                    !pf_wait(&kv_empty[s], ((j / M::STAGES) - 1) & 1, abort_flag, p.dev_error)) {
+                    aborted = true;
+                    break;
+                }
+                const int64_t k0 = (kt0 + j) * kKeys;
+                int y[kKeys / 16];
+#pragma unroll
+                for (int gi = 0; gi < kKeys / 16; ++gi) {
+                    const int64_t key = k0 + 16 * gi;
+                    y[gi] = p.pool_rows;                            // past the pool: reads zeros
+                    if (key <= pos_last) {
+                        const int32_t page = table[key / p.P];
+                        if (page >= 0 && page < p.n_pages)
+                            y[gi] = (int)(((int64_t)page * p.H + h) * p.P + key % p.P);
+                        else
+                            atomicOr(p.dev_error, PKV_DEVERR_PAGE_ID);
+                    }
+                }
+                unsigned char* Ks = ring + s * 2 * M::KV_BYTES;
+                unsigned char* Vs = Ks + M::KV_BYTES;
+                mbar_arrive_expect_tx(&k_full[s], M::KV_BYTES);
+#pragma unroll
+                for (int gi = 0; gi < kKeys / 16; ++gi)
+#pragma unroll
+                    for (int cc = 0; cc < M::CHUNKS; ++cc)
+                        tma_load_2d(Ks + cc * kKeys * 128 + gi * 2048, &tmk, cc * 64, y[gi],
+                                    &k_full[s], pol);
+                mbar_arrive_expect_tx(&v_full[s], M::KV_BYTES);
+#pragma unroll
+                for (int gi = 0; gi < kKeys / 16; ++gi)
+#pragma unroll
+                    for (int cc = 0; cc < M::CHUNKS; ++cc)
+                        tma_load_2d(Vs + cc * kKeys * 128 + gi * 2048, &tmv, cc * 64, y[gi],
+                                    &v_full[s], pol);
+                ++issued;
+            }
+            if (aborted || *abort_flag) {
+                // let the copies in flight land before the CTA's shared memory goes away
+                for (int j = issued - M::STAGES > 0 ? issued - M::STAGES : 0; j < issued; ++j) {
+                    const int s = j % M::STAGES;
+                    mbar_wait_bounded(&k_full[s], (j / M::STAGES) & 1, kPfWaitLimitNs);
+                    mbar_wait_bounded(&v_full[s], (j / M::STAGES) & 1, kPfWaitLimitNs);
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- MMA --
+        constexpr uint32_t idS = idesc_bf16(kKeys, false);
+        constexpr uint32_t idO = idesc_bf16(D, true);
+        // V is MN-major: 64-column swizzle atoms kKeys * 128 bytes apart, 8-row groups
+        // 1024 bytes apart.  With D = 64 there is a single atom column, and the atom
+        // stride is set equal to the group stride.
+        constexpr uint32_t kVLbo = D == 64 ? 1024u : (uint32_t)(kKeys * 128);
+        const uint32_t q_addr = smem_u32(Qs), p_addr = smem_u32(Ps);
+        bool ok = pf_warp_wait(q_ready, 0, abort_flag, p.dev_error);
+        bool issued_any = false;
+        for (int j = 0; ok && j <= ntiles; ++j) {
+            if (j < ntiles) {
+                const int s = j % M::STAGES;
+                if (!pf_warp_wait(&k_full[s], (j / M::STAGES) & 1, abort_flag, p.dev_error)) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t k_addr = smem_u32(ring + s * 2 * M::KV_BYTES);
+                    const uint32_t d = tmem + M::S_COL + (j & 1) * kKeys;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+                        umma_bf16(d, sw128_desc(q_addr + off, 16, 1024),
+                                  sw128_desc(k_addr + off, 16, 1024), idS, k > 0);
+                    }
+                    umma_commit(&s_full[j & 1]);
+                }
+                issued_any = true;
+                __syncwarp();
+            }
+            if (j > 0) {
+                const int jj = j - 1, s = jj % M::STAGES;
+                if (!pf_warp_wait(p_full, jj & 1, abort_flag, p.dev_error)) break;
+                if (!pf_warp_wait(&v_full[s], (jj / M::STAGES) & 1, abort_flag, p.dev_error)) break;
+                unsigned char* Vs = ring + s * 2 * M::KV_BYTES + M::KV_BYTES;
+                if (jj == ntiles - 1) {
+                    // rows at positions >= t_b of the last loaded group hold stale
+                    // bytes, possibly not finite: clear them in V (their weights are 0)
+                    const int64_t k0 = (kt0 + jj) * kKeys;
+                    const int r0 = (int)(t_b - k0);
+                    const int r1 = (int)(((pos_last - k0) / 16 + 1) * 16);
+                    for (int idx = lane; idx < (r1 - r0) * M::CHUNKS * 8; idx += 32) {
+                        const int row = r0 + idx / (M::CHUNKS * 8);
+                        const int piece = idx % (M::CHUNKS * 8);
+                        *reinterpret_cast<uint4*>(Vs + (piece >> 3) * kKeys * 128 + row * 128 +
+                                                  (piece & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t v_addr = smem_u32(Vs);
+#pragma unroll
+                    for (int k = 0; k < kKeys / 16; ++k) {
+                        const uint32_t a_off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+                        umma_bf16(tmem + M::O_COL, sw128_desc(p_addr + a_off, 16, 1024),
+                                  sw128_desc(v_addr + k * 16 * 128, kVLbo, 1024), idO,
+                                  (jj > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&kv_empty[s]);
+                    umma_commit(o_done);
+                }
+                __syncwarp();
+            }
+        }
+        if (issued_any && *abort_flag) {
+            // MMAs still in flight read shared memory and write TMEM: let them finish
+            if (lane == 0) {
+                umma_commit(drain);
+                mbar_wait_bounded(drain, 0, kPfWaitLimitNs);
+            }
+            __syncwarp();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, M::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host --
+
+template <int D>
+cudaError_t launch_prefill_t(const PrefillArgs& a, const PfParams& p, cudaStream_t stream) {
+    using M = PfGeo<D>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_attention_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+    const int64_t pieces = a.total_new * a.H * (D / 8);
+    int sms = 148;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (pieces + 255) / 256;
+    const int append_blocks = (int)(want < (int64_t)sms * 8 ? (want > 0 ? want : 1) : (int64_t)sms * 8);
+    prefill_append_kernel<D><<<append_blocks, 256, 0, stream>>>(p);
+    const int64_t blocks = prefill_max_tiles(a.B, a.G, a.total_new) * a.H;
+    CUtensorMap tmk, tmv;
+    std::memcpy(&tmk, a.tmap_k, sizeof tmk);
+    std::memcpy(&tmv, a.tmap_v, sizeof tmv);
+    if (a.ev_before) cudaEventRecord(a.ev_before, stream);
+    prefill_attention_kernel<D><<<(unsigned)blocks, kPfThreads, M::SMEM, stream>>>(p, tmk, tmv);
+    if (a.ev_after) cudaEventRecord(a.ev_after, stream);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t prefill_max_tiles(int B, int G, int64_t total_new) {
+    return total_new / (kRows / G) + B;
+}
+
+size_t prefill_workspace_bytes(int B, int G, int64_t total_new) {
+    return 256 + (size_t)prefill_max_tiles(B, G, total_new) * sizeof(int2);
+}
+
+bool prefill_supported(int dtype, int D, int G) {
+    return dtype == PKV_BF16 && (D == 64 || D == 128) && G >= 1 && G <= kRows && kRows % G == 0;
+}
+
+int prefill_max_batch() { return kPlanThreads; }
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+    PfParams p{};
+    p.B = a.B;
+    p.H = a.H;
+    p.G = a.G;
+    p.P = a.P;
+    p.max_pages = a.max_pages;
+    p.window = a.window;
+    p.n_pages = a.n_pages;
+    p.pool_rows = (int)(a.n_pages * a.H * a.P);
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
+    p.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+    p.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+    p.k_pages = static_cast<__nv_bfloat16*>(a.k_pages);
+    p.v_pages = static_cast<__nv_bfloat16*>(a.v_pages);
+    p.cu_new = a.cu_new;
+    p.seq_lens = a.seq_lens;
+    p.tables = a.tables;
+    p.out = a.out;
+    p.n_items = static_cast<int*>(a.workspace);
+    p.max_items = (int)prefill_max_tiles(a.B, a.G, a.total_new);
+    p.items = reinterpret_cast<int2*>(static_cast<char*>(a.workspace) + 256);
+    p.total_new = a.total_new;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a.D));
+    p.dev_error = a.dev_error;
+    switch (a.D) {
+        case 64: return launch_prefill_t<64>(a, p, stream);
+        case 128: return launch_prefill_t<128>(a, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pkv

@@ -36,6 +36,30 @@ def step_inputs(w: Workload, layer: int = 0):
     return q, k, v
 
 
+def prefill_inputs(w: Workload, layer: int = 0):
+    """Host arrays of one batched prefill: q [N,HQ,D] and k_new / v_new [N,H,D] as bf16
+    bits (tokens t_b - n_b .. t_b - 1 of each request's streams, requests in order) and
+    the row offsets cu [B+1] int32."""
+    H, D, HQ = w.H, w.D, w.HQ
+    n = w.new_tokens.astype(np.int64)
+    cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    N = int(cu[-1])
+    q = np.empty((N, HQ, D), np.uint16)
+    k = np.empty((N, H, D), np.uint16)
+    v = np.empty((N, H, D), np.uint16)
+    for b in range(w.B):
+        t, nb = int(w.seq_lens[b]), int(n[b])
+        if nb == 0:
+            continue
+        rows_ = slice(int(cu[b]), int(cu[b + 1]))
+        for qh in range(HQ):
+            q[rows_, qh] = rows(w.seed, Q, layer, b, qh, t - nb, nb, D, 1)
+        for h in range(H):
+            k[rows_, h] = rows(w.seed, KHIST, layer, b, h, t - nb, nb, D, 1)
+            v[rows_, h] = rows(w.seed, VHIST, layer, b, h, t - nb, nb, D, 1)
+    return q, k, v, cu
+
+
 def to_device(x: np.ndarray, dtype: int | None = None, device="cuda") -> torch.Tensor:
     """numpy -> torch on the device; uint16 arrays are bf16 bit patterns."""
     t = torch.from_numpy(np.ascontiguousarray(x))
@@ -47,8 +71,9 @@ def to_device(x: np.ndarray, dtype: int | None = None, device="cuda") -> torch.T
 def fill_history(k_pages: torch.Tensor, v_pages: torch.Tensor, w: Workload, tables: np.ndarray,
                  layer: int = 0, requests=None) -> int:
     """Write tokens 0 .. t_b - 2 of every request into its pages (slot t_b - 1 is left
-    for the step's own append).  k_pages / v_pages: [pages, H, P, D] device views of
-    one layer.  Pages of a shared prefix are written once, by request 0.  Returns the
+    for the step's own append; with w.new_tokens, tokens 0 .. t_b - n_b - 1, the chunk
+    being the prefill's).  k_pages / v_pages: [pages, H, P, D] device views of one
+    layer.  Pages of a shared prefix are written once, by request 0.  Returns the
     bytes written."""
     P = w.P
     S = getattr(w, "shared_prefix", 0)
@@ -56,12 +81,13 @@ def fill_history(k_pages: torch.Tensor, v_pages: torch.Tensor, w: Workload, tabl
     reqs = range(w.B) if requests is None else requests
     for b in reqs:
         t = int(w.seq_lens[b])
+        cached = t - (int(w.new_tokens[b]) if w.new_tokens is not None else 1)
         n = (t + P - 1) // P
         skip = S // P if (b != 0 and S) else 0           # request 0 owns the shared pages
         idx = torch.from_numpy(np.ascontiguousarray(tables[b, skip:n], dtype=np.int64)).to(
             k_pages.device)
         for kind, dst in ((KHIST, k_pages), (VHIST, v_pages)):
-            host = request_history_pages(w, kind, layer, b, n, t - 1)[skip:]
+            host = request_history_pages(w, kind, layer, b, n, cached)[skip:]
             dev = to_device(np.ascontiguousarray(host), w.dtype, k_pages.device)
             dst.index_copy_(0, idx, dev)
             written += host.nbytes

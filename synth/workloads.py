@@ -33,6 +33,7 @@ class Workload:
     group: int = 1         # query heads per KV head (H is the number of KV heads)
     window: int = 0        # sliding window in positions (0: whole prefix)
     shared_prefix: int = 0  # tokens every request shares with request 0 (a prompt), pages shared
+    new_tokens: np.ndarray | None = None  # prefill: [B] chunk tokens appended (the last of seq_lens)
 
     @property
     def HQ(self) -> int:
@@ -127,6 +128,30 @@ def shared_prompt(seed: int = 7, B: int = 64, prefix: int = 8192, suffix_max: in
                     group=4, shared_prefix=prefix)
 
 
+def chunked_prefill(seed: int = 8, B: int = 8, chunk: int = 4096, cached_max: int = 4096) -> Workload:
+    """Chunked prefill: 8 requests each append a chunk of 4096 tokens after U{0..4096}
+    cached ones; 8 KV heads x 4 query heads, d_h=128, bf16, pool of 8192 shuffled pages."""
+    rng = np.random.default_rng(seed)
+    cached = rng.integers(0, cached_max + 1, size=B)
+    new = np.full(B, chunk, dtype=np.int32)
+    lens = (cached + new).astype(np.int32)
+    return Workload("prefill_bf16", B, 1, 8, 128, 16, BF16, 8192, cached_max + chunk, seed, lens,
+                    group=4, new_tokens=new)
+
+
+def attended_pairs(w: Workload) -> int:
+    """(query row, key) pairs of a prefill: sum over chunk tokens of the keys each attends,
+    times the query heads."""
+    total = 0
+    for t, n in zip(w.seq_lens.astype(np.int64), w.new_tokens.astype(np.int64)):
+        pos = np.arange(t - n, t, dtype=np.int64)          # positions of the chunk tokens
+        keys = pos + 1
+        if w.window:
+            keys = np.minimum(keys, w.window)
+        total += int(keys.sum())
+    return total * w.HQ
+
+
 def unique_rows(w: Workload) -> int:
     """Retained (KV lane, token) rows stored once: a shared prefix counts once."""
     lens = w.seq_lens.astype(np.int64)
@@ -152,4 +177,5 @@ REGISTRY = {
     "gqa8_f32": lambda: gqa(8, F32),
     "window_bf16": sliding_window,
     "prefix_bf16": shared_prompt,
+    "prefill_bf16": chunked_prefill,
 }

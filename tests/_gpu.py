@@ -161,3 +161,116 @@ def make_workload(name, seq_lens, H, D, P=16, dtype=F32, pool_pages=None, seed=0
         max_context = int(max(seq_lens.max(), 1))
     return Workload(name, len(seq_lens), layers, H, D, P, dtype, int(pool_pages), int(max_context),
                     seed, seq_lens, churn_cycles=churn, group=group, window=window)
+
+
+class PrefillRun:
+    """A bf16 pool whose requests hold their cached tokens, and one batched prefill of
+    the workload's chunks through the C ABI.  Slots at and after each request's
+    cached length start as NaN, so a row the prefill fails to write, or a stale row
+    it reads, shows up in the output."""
+
+    def __init__(self, w: Workload, poison: bool = True):
+        from synth.device import prefill_inputs
+        self.w = w
+        self.pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "bf16", w.max_context, w.seed,
+                             query_heads=w.HQ, window=w.window)
+        self.reqs = [self.pool.request() for _ in range(w.B)]
+        for r, n in zip(self.reqs, w.n_pages):
+            r.lease_pages(int(n))
+        self.max_pages = max(int(w.n_pages.max()), 1)
+        self.tables = np.full((w.B, self.max_pages), -1, dtype=np.int32)
+        for b, r in enumerate(self.reqs):
+            t = r.page_table()
+            self.tables[b, :len(t)] = t
+        self.k_pages, self.v_pages = self.pool.kv_pages(0)
+        self.cached = (w.seq_lens - w.new_tokens).astype(np.int64)
+        if poison:
+            self.k_pages.fill_(float("nan"))
+            self.v_pages.fill_(float("nan"))
+        fill_history(self.k_pages, self.v_pages, w, self.tables, 0)
+        if poison:
+            pg, sl = [], []
+            for b in range(w.B):
+                pos = np.arange(self.cached[b], int(w.n_pages[b]) * w.P)
+                pg.append(self.tables[b, pos // w.P])
+                sl.append(pos % w.P)
+            pg = torch.from_numpy(np.concatenate(pg).astype(np.int64)).cuda()
+            sl = torch.from_numpy(np.concatenate(sl).astype(np.int64)).cuda()
+            self.k_pages[pg, :, sl] = float("nan")
+            self.v_pages[pg, :, sl] = float("nan")
+        self.q, self.k_new, self.v_new, self.cu = prefill_inputs(w, 0)
+        self.N = int(self.cu[-1])
+        self.dev = dict(q=to_device(self.q), k=to_device(self.k_new), v=to_device(self.v_new),
+                        cu=torch.from_numpy(self.cu).cuda(),
+                        tables=torch.from_numpy(self.tables).cuda(),
+                        lens=torch.from_numpy(w.seq_lens.astype(np.int32)).cuda())
+        self.out = torch.full((self.N, w.HQ, w.D), float("nan"), device="cuda")
+
+    def run(self, stream=None):
+        d = self.dev
+        self.pool.paged_prefill(0, d["q"], d["k"], d["v"], d["cu"], d["tables"], d["lens"],
+                                out=self.out, stream=stream)
+        return self.out
+
+    def _host_pages(self, b: int, n_tokens: int):
+        """Request b's pages holding its tokens 0 .. n_tokens - 1 (rest zero)."""
+        w = self.w
+        n = max((n_tokens + w.P - 1) // w.P, 1)
+        kp = synth.request_history_pages(w, KHIST, 0, b, n, n_tokens)
+        vp = synth.request_history_pages(w, VHIST, 0, b, n, n_tokens)
+        return kp, vp, np.arange(n, dtype=np.int32)[None, :]
+
+    def oracle_out(self, b: int) -> np.ndarray:
+        """Oracle prefill of request b alone: [n_b, HQ, D] fp64."""
+        w = self.w
+        nb = int(w.new_tokens[b])
+        kp, vp, table = self._host_pages(b, int(self.cached[b]))
+        tail = (int(w.seq_lens[b]) + w.P - 1) // w.P
+        if tail > kp.shape[0]:
+            pad = np.zeros((tail - kp.shape[0],) + kp.shape[1:], dtype=kp.dtype)
+            kp, vp = np.concatenate([kp, pad]), np.concatenate([vp, pad])
+            table = np.arange(tail, dtype=np.int32)[None, :]
+        rows = slice(int(self.cu[b]), int(self.cu[b + 1]))
+        cu = np.array([0, nb], dtype=np.int32)
+        return oracle.paged_prefill(kp, vp, synth.bf16_to_f32(self.q[rows]), self.k_new[rows],
+                                    self.v_new[rows], cu, table,
+                                    np.array([w.seq_lens[b]], dtype=np.int32), BF16,
+                                    group=w.group, window=w.window)
+
+    def oracle_row(self, b: int, i: int) -> np.ndarray:
+        """Oracle output of chunk token i of request b, as the decode step at position
+        cached + i: [HQ, D] fp64."""
+        w = self.w
+        pos = int(self.cached[b]) + i
+        kp, vp, table = self._host_pages(b, pos + 1)
+        x = int(self.cu[b]) + i
+        out = oracle.paged_decode_attention(kp, vp, synth.bf16_to_f32(self.q[x:x + 1]),
+                                            self.k_new[x:x + 1], self.v_new[x:x + 1], table,
+                                            np.array([pos + 1], dtype=np.int32), BF16,
+                                            group=w.group, window=w.window)
+        return out[0]
+
+    def chunk_rows(self, b: int, i: int):
+        """Device K and V bytes at chunk token i of request b (all heads)."""
+        pos = int(self.cached[b]) + i
+        pg = int(self.tables[b, pos // self.w.P])
+        slot = pos % self.w.P
+        k = self.k_pages[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
+        v = self.v_pages[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
+        return k, v
+
+    def close(self):
+        for r in self.reqs:
+            r.close()
+        self.pool.close()
+
+
+def make_prefill(name, cached, new, H, D, group=1, P=16, window=0, seed=0, pool_pages=None):
+    cached = np.asarray(cached, dtype=np.int64)
+    new = np.asarray(new, dtype=np.int32)
+    lens = (cached + new).astype(np.int32)
+    n = (lens.astype(np.int64) + P - 1) // P
+    if pool_pages is None:
+        pool_pages = int(n.sum()) + 13
+    return Workload(name, len(lens), 1, H, D, P, BF16, int(pool_pages), int(max(lens.max(), 1)),
+                    seed, lens, group=group, window=window, new_tokens=new)

@@ -1,0 +1,182 @@
+"""Batched prefill on the device vs the fp64 oracle, through the C ABI.
+
+Bar: bit-exact K/V rows written into the pages; normwise relative error per
+(token, query head) row <= PREFILL_RTOL.  The tensor cores multiply V by the
+softmax weights rounded to bf16 (relative rounding error <= 2^-9 each), so a row
+of the output moves by at most 2^-8 x sum_j w_j |v_j| in exact arithmetic; for
+the N(0,1) rows of these workloads that is a few 1e-3 of the row's largest
+element at the worst of thousands of rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_decode_gb300 as pkv
+from synth import workloads
+from tests._gpu import PrefillRun, make_prefill
+
+pytestmark = pytest.mark.gpu
+
+PREFILL_RTOL = 1e-2
+
+
+@pytest.fixture(autouse=True)
+def _need_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _normwise(out: np.ndarray, ref: np.ndarray) -> float:
+    num = np.abs(out - ref).max(axis=-1)
+    den = np.maximum(np.abs(ref).max(axis=-1), 1e-6)
+    return float((num / den).max()) if out.size else 0.0
+
+
+CASES = {
+    # name: (cached, new, H, D, group, P, window)
+    "d128_mha": ([0, 37, 300], [1, 50, 200], 2, 128, 1, 16, 0),
+    "d64_gqa4": ([0, 129, 1000], [100, 33, 64], 2, 64, 4, 16, 0),
+    "d128_gqa8_window": ([50, 400], [300, 16], 1, 128, 8, 16, 100),
+    "d128_gqa2_page32": ([17], [259], 2, 128, 2, 32, 0),
+    "d64_mha_long": ([2000], [130], 1, 64, 1, 16, 0),
+    "empty_request": ([10, 5, 0], [0, 20, 0], 2, 128, 2, 16, 0),
+    "d64_gqa8_window_ragged": ([0, 3, 700], [129, 255, 1], 2, 64, 8, 64, 33),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_prefill_matches_oracle(name):
+    cached, new, H, D, G, P, W = CASES[name]
+    w = make_prefill(name, cached, new, H, D, group=G, P=P, window=W, seed=41)
+    run = PrefillRun(w)
+    try:
+        out = run.run().cpu().numpy()
+        torch.cuda.synchronize()
+        assert run.pool.check_device_status() == 0
+        worst = 0.0
+        for b in range(w.B):
+            nb = int(w.new_tokens[b])
+            if nb == 0:
+                continue
+            got = out[run.cu[b]:run.cu[b + 1]]
+            assert np.isfinite(got).all(), f"request {b}: non-finite output"
+            err = _normwise(got, run.oracle_out(b))
+            worst = max(worst, err)
+            for i in range(nb):
+                k, v = run.chunk_rows(b, i)
+                x = int(run.cu[b]) + i
+                assert np.array_equal(k, run.k_new[x]) and np.array_equal(v, run.v_new[x])
+        print(f"{name}: worst normwise error {worst:.2e}")
+        assert worst <= PREFILL_RTOL
+    finally:
+        run.close()
+
+
+def test_prefill_is_batch_invariant():
+    """A request's outputs do not depend on the other requests of the batch: request 0
+    alone and request 0 beside two others give the same bits."""
+    outs = []
+    for cached, new in (([100, 0, 513], [200, 77, 140]), ([100], [200])):
+        w = make_prefill("batch", cached, new, 2, 128, group=4, seed=42)
+        run = PrefillRun(w)
+        try:
+            outs.append(run.run()[:200].cpu().numpy())
+        finally:
+            run.close()
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_prefill_full_workload_sampled_rows():
+    """The benchmarked workload at full size: sampled chunk tokens against the oracle's
+    decode step at their position, every output finite, sampled rows in the pages."""
+    w = workloads.chunked_prefill()
+    run = PrefillRun(w, poison=False)
+    try:
+        out = run.run()
+        torch.cuda.synchronize()
+        assert run.pool.check_device_status() == 0
+        assert torch.isfinite(out).all()
+        out = out.cpu().numpy()
+        rng = np.random.default_rng(5)
+        worst = 0.0
+        for b in range(w.B):
+            nb = int(w.new_tokens[b])
+            for i in sorted({0, nb - 1, *rng.integers(0, nb, size=2).tolist()}):
+                x = int(run.cu[b]) + i
+                worst = max(worst, _normwise(out[x], run.oracle_row(b, i)))
+                k, v = run.chunk_rows(b, i)
+                assert np.array_equal(k, run.k_new[x]) and np.array_equal(v, run.v_new[x])
+        print(f"prefill_bf16 sampled: worst normwise error {worst:.2e}")
+        assert worst <= PREFILL_RTOL
+    finally:
+        run.close()
+
+
+def test_prefill_then_decode_reads_the_chunk():
+    """A decode step after the prefill attends over the rows the prefill wrote."""
+    import oracle
+    import synth
+    from synth import KHIST, VHIST, Q, F32, BF16
+    w = make_prefill("then_decode", [40, 0], [90, 33], 2, 128, group=2, seed=43)
+    run = PrefillRun(w)
+    try:
+        run.run()
+        # next token of every request: position t_b, leased page if needed
+        B, H, HQ, D, P = w.B, w.H, w.HQ, w.D, w.P
+        for b, r in enumerate(run.reqs):
+            need = (int(w.seq_lens[b]) + 1 + P - 1) // P
+            if need > len(r.page_table()):
+                r.lease_pages(need - len(r.page_table()))
+        max_pages = max(len(r.page_table()) for r in run.reqs)
+        tables = np.full((B, max_pages), -1, dtype=np.int32)
+        for b, r in enumerate(run.reqs):
+            tables[b, :len(r.page_table())] = r.page_table()
+        lens = (w.seq_lens + 1).astype(np.int32)
+        q = np.stack([synth.lane_rows(w.seed, Q, 0, b, HQ, int(lens[b]) - 1, D, F32) for b in range(B)])
+        k = np.stack([synth.lane_rows(w.seed, KHIST, 0, b, H, int(lens[b]) - 1, D, BF16) for b in range(B)])
+        v = np.stack([synth.lane_rows(w.seed, VHIST, 0, b, H, int(lens[b]) - 1, D, BF16) for b in range(B)])
+        from synth.device import to_device
+        out = run.pool.paged_decode_attention(0, to_device(q), to_device(k), to_device(v),
+                                              torch.from_numpy(tables).cuda(),
+                                              torch.from_numpy(lens).cuda(), int(lens.max()))
+        out = out.cpu().numpy()
+        for b in range(B):
+            t = int(lens[b])
+            n = (t + P - 1) // P
+            kp = synth.request_history_pages(w, KHIST, 0, b, n, t - 1)
+            vp = synth.request_history_pages(w, VHIST, 0, b, n, t - 1)
+            ref = oracle.paged_decode_attention(kp, vp, q[b:b + 1], k[b:b + 1], v[b:b + 1],
+                                                np.arange(n, dtype=np.int32)[None, :],
+                                                np.array([t], dtype=np.int32), BF16, group=2)
+            assert _normwise(out[b], ref[0]) <= 5e-3
+    finally:
+        run.close()
+
+
+def test_prefill_bad_lengths_and_pages_set_error_bits():
+    w = make_prefill("bad", [5, 20], [10, 10], 1, 64, seed=44)
+    run = PrefillRun(w)
+    try:
+        lens = run.dev["lens"].clone()
+        lens[0] = 3                                   # shorter than its chunk
+        run.pool.paged_prefill(0, run.dev["q"], run.dev["k"], run.dev["v"], run.dev["cu"],
+                               run.dev["tables"], lens, out=run.out)
+        with pytest.raises(pkv.PkvError):
+            run.pool.check_device_status()
+        assert run.pool.check_device_status() == 0   # cleared
+        tables = run.dev["tables"].clone()
+        tables[1, 0] = w.pool_pages + 5               # page id past the pool
+        run.pool.paged_prefill(0, run.dev["q"], run.dev["k"], run.dev["v"], run.dev["cu"],
+                               tables, run.dev["lens"], out=run.out)
+        torch.cuda.synchronize()
+        bits = 0
+        try:
+            run.pool.check_device_status()
+        except pkv.PkvError as e:
+            bits = str(e)
+        assert "0x2" in str(bits)
+        # request 0 unaffected by request 1's bad page
+        got = run.out[run.cu[0]:run.cu[1]].cpu().numpy()
+        assert _normwise(got, run.oracle_out(0)) <= PREFILL_RTOL
+    finally:
+        run.close()
