@@ -38,6 +38,7 @@ DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "decode.c
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------- workload --
@@ -51,6 +52,8 @@ def make_workload(name: str, rank: int = 0, requests: int = 0):
     if 0 < requests < w.B:
         w.B = requests
         w.seq_lens = w.seq_lens[:requests].copy()
+        if w.new_tokens is not None:
+            w.new_tokens = w.new_tokens[:requests].copy()
         if w.name == "long":
             w.pool_pages = int(w.n_pages.sum())
         w.name += f"_first{requests}"
@@ -77,6 +80,12 @@ def describe(w) -> str:
     if w.name.startswith("gqa"):
         return (f"grouped-query decode: {w.B} requests, t ~ U[1,{w.max_context}], {w.H} KV heads x "
                 f"{w.group} query heads each, d_h={w.D}, {st}, pool of {w.pool_pages} shuffled pages")
+    if w.name.startswith("prefill"):
+        cached = w.seq_lens - w.new_tokens
+        return (f"chunked prefill: {w.B} requests each appending {int(w.new_tokens[0])} tokens "
+                f"after U[0,{int(w.max_context - w.new_tokens.max())}] cached ones (mean "
+                f"{float(cached.mean()):.0f}), {w.H} KV heads x {w.group} query heads, d_h={w.D}, "
+                f"bf16 pages of {w.P}, causal")
     if w.name == "ragged":
         return (f"ragged fragmented pool: {w.B} requests, lognormal(ln 512, 1) lengths, H={w.H}, "
                 f"d_h={w.D}, {st}, {w.pool_pages}-page pool after {w.churn_cycles} lease/release cycles")
@@ -553,6 +562,210 @@ def run_gpu_serial(args):
     return line, w
 
 
+# ------------------------------------------------- the GPU arm, prefill --
+
+def prefill_flops(w) -> int:
+    """Algorithmic FLOPs of one batched prefill: S = Q K^T and O = P V over every
+    (query row, attended key) pair, 2 x d_h each."""
+    from synth.workloads import attended_pairs
+    return attended_pairs(w) * 4 * w.D
+
+
+def measured_peak_bf16():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def setup_prefill(w, torch):
+    """Pool, tables from the library's allocator, cached tokens in HBM, chunk inputs on device."""
+    import paged_kv_cache_decode_gb300 as pkv
+    from synth.device import fill_history, prefill_inputs, to_device
+    pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "bf16", w.max_context, w.seed,
+                    query_heads=w.HQ, window=w.window)
+    reqs = [pool.request() for _ in range(w.B)]
+    for b, r in enumerate(reqs):
+        r.lease_pages(int(w.n_pages[b]))
+    tables = np.full((w.B, int(w.n_pages.max())), -1, dtype=np.int32)
+    for b, r in enumerate(reqs):
+        t = r.page_table()
+        tables[b, :len(t)] = t
+    k_pages, v_pages = pool.kv_pages(0)
+    fill_history(k_pages, v_pages, w, tables, 0)
+    q, k_new, v_new, cu = prefill_inputs(w, 0)
+    host = dict(q=q, k=k_new, v=v_new, cu=cu, tables=tables, lens=w.seq_lens.astype(np.int32))
+    dev = {k: (to_device(v) if v.dtype == np.uint16 else torch.from_numpy(v).cuda())
+           for k, v in host.items()}
+    N = int(cu[-1])
+    out = torch.empty((N, w.HQ, w.D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(pool.prefill_workspace_size(w.B, N), 16), dtype=torch.uint8,
+                     device="cuda")
+    torch.cuda.synchronize()
+    return pool, reqs, host, dev, ws, out
+
+
+def run_gpu_prefill(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    rank, world = dist_init("nccl")
+    w = make_workload(args.workload, rank, args.requests)
+    pool, reqs, host, dev, ws, out = setup_prefill(w, torch)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pool.paged_prefill(0, dev["q"], dev["k"], dev["v"], dev["cu"], dev["tables"], dev["lens"],
+                           out=out, workspace=ws)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pool.check_device_status() == 0
+
+    K = args.steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(K):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    step_ms_max = max_over_ranks(start.elapsed_time(end) / K, "cuda")
+
+    # the attention kernel alone, events recorded around its launch
+    evb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    eva = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        pool.set_timing_events(evb[i], eva[i])
+        step()
+    torch.cuda.synchronize()
+    pool.set_timing_events(None, None)
+    kernel_ms = float(np.mean([b.elapsed_time(a) for b, a in zip(evb, eva)]))
+
+    # end to end: pinned host inputs copied in, the output copied out, every step
+    hp = {}
+    for k, v in host.items():
+        t = torch.from_numpy(np.ascontiguousarray(v))
+        hp[k] = (t.view(torch.int16) if v.dtype == np.uint16 else t).pin_memory()
+    dv = {k: (d.view(torch.int16) if d.dtype == torch.bfloat16 else d) for k, d in dev.items()}
+    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in hp.values())
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for k in hp:
+            dv[k].copy_(hp[k], non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, "cuda")
+    assert pool.check_device_status() == 0
+    if sampler:
+        sampler.stop()
+
+    flops = prefill_flops(w)
+    N = int(host["cu"][-1])
+    kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.H * w.D * 2 * 2
+    line = None
+    if rank == 0:
+        peak, peak_kind = measured_peak_bf16()
+        achieved = flops / (kernel_ms * 1e-3) / 1e12
+        value = world * flops / (step_ms_max * 1e-3) / 1e12
+        line = {
+            "metric": "batched prefill attention into the paged cache: TFLOP/s (causal, "
+                      "algorithmic FLOPs) and new tokens/s",
+            "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
+                       "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P,
+                       "pool_pages": w.pool_pages, "new_tokens": N,
+                       "cached_tokens": int((w.seq_lens - w.new_tokens).sum()),
+                       "storage": "bf16", "accumulate": "fp32", "flops_per_step": flops,
+                       "l2": f"K/V of the step {kv_bytes / 1e9:.2f} GB, re-read across query "
+                             f"tiles through L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "tokens_per_s": round(world * N / (step_ms_max * 1e-3), 1),
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "prefill_attention_kernel<%d>" % w.D,
+                         "kernel_ms": round(kernel_ms, 5),
+                         "peak_kind": peak_kind + " (bf16_tflops burst, cuBLAS)"},
+            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": K * 3,
+            "clocks": sampler.summary(t0, t1) if sampler else None,
+        }
+    for r in reqs:
+        r.close()
+    pool.close()
+    return line, w
+
+
+def oracle_prefill_sample(w, target_flops: float = 5e10, threads=0):
+    """The first chunk tokens of request 0, as many as make about target_flops of
+    oracle work, with the request's cached pages; a callable runs the oracle once."""
+    import oracle
+    import synth
+    from synth import KHIST, VHIST
+    from synth.device import prefill_inputs
+    q, k_new, v_new, cu = prefill_inputs(w, 0)
+    t, nb = int(w.seq_lens[0]), int(w.new_tokens[0])
+    L0 = t - nb
+    m = 0
+    work = 0.0
+    while m < nb and work < target_flops:
+        keys = L0 + m + 1
+        work += (min(keys, w.window) if w.window else keys) * w.HQ * 4 * w.D
+        m += 1
+    n = (L0 + m + w.P - 1) // w.P
+    kp = synth.history_pages(w.seed, KHIST, 0, 0, n, w.H, w.P, w.D, L0, w.dtype)
+    vp = synth.history_pages(w.seed, VHIST, 0, 0, n, w.H, w.P, w.D, L0, w.dtype)
+    table = np.arange(n, dtype=np.int32)[None, :]
+    qf = synth.bf16_to_f32(q[:m])
+    cu1 = np.array([0, m], dtype=np.int32)
+    lens = np.array([L0 + m], dtype=np.int32)
+
+    def run():
+        return oracle.paged_prefill(kp.copy(), vp.copy(), qf, k_new[:m], v_new[:m], cu1, table, lens,
+                                    w.dtype, group=w.group, window=w.window, threads=threads)
+    return run, work, m, L0
+
+
+def cpu_baseline_prefill(w):
+    import oracle
+    run, work, m, L0 = oracle_prefill_sample(w)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": round(work / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"request 0: the first {m} of its {int(w.new_tokens[0])} chunk tokens after "
+                      f"{L0} cached ({work / 1e9:.1f} GFLOP), fp64 C oracle, one pass, {dt:.2f} s",
+            "tokens_per_s": round(m / dt, 3)}
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(w, requests, threads=0):
@@ -615,12 +828,43 @@ def cpu_baseline(w, lane_tokens=1 << 24):
             "tokens_per_s": round(len(reqs) / dt, 3)}
 
 
+def run_reference_prefill(args, w):
+    import oracle
+    run, work, m, L0 = oracle_prefill_sample(w, target_flops=1e9)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = round(work / dt / 1e12, 6)
+    sample = (f"each step: request 0's first {m} chunk tokens after {L0} cached "
+              f"({work / 1e9:.1f} GFLOP), fp64 C oracle on the host cores")
+    return {
+        "impl": "reference",
+        "metric": "batched prefill attention into the paged cache: TFLOP/s (causal, "
+                  "algorithmic FLOPs) and new tokens/s",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
+                   "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P},
+        "tokens_per_s": round(m / dt, 3),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }, w
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return None, None
     import oracle
     w = make_workload(args.workload, 0, args.requests)
+    if w.new_tokens is not None:
+        return run_reference_prefill(args, w)
     reqs = sample_requests(w, 1)                       # one request per step
     run, sbytes, lens = oracle_sample(w, reqs)
     for _ in range(args.warmup):
@@ -673,10 +917,17 @@ def main(argv=None):
     if args.impl == "reference":
         line, _ = run_reference(args)
     else:
-        line, w = (run_gpu_serial if args.workload.startswith("single") else run_gpu)(args)
+        if args.workload.startswith("single"):
+            runner = run_gpu_serial
+        elif args.workload.startswith("prefill"):
+            runner = run_gpu_prefill
+        else:
+            runner = run_gpu
+        line, w = runner(args)
         rank, world, _ = dist_env()
         if line is not None and world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w)
+            line["cpu_baseline"] = (cpu_baseline_prefill(w) if w.new_tokens is not None
+                                    else cpu_baseline(w))
     if line is not None:
         print(json.dumps(line), flush=True)
 

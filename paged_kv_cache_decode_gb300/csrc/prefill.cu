@@ -10,26 +10,32 @@
 // of them with a sliding window) -- what n_b successive decode steps give.
 //
 // Three launches per call:
-//   1. plan (one CTA): validates lengths and lists the query tiles request by
-//      request, the heaviest (last) tile of each request first;
+//   1. plan (one CTA): validates lengths and lists the work units request by
+//      request, the heaviest (last) unit of each request first;
 //   2. append: copies every new key / value row into its page;
-//   3. attention: one CTA per (query tile, KV head).
+//   3. attention: one CTA per (work unit, KV head).
 //
 // Attention CTA.  A query tile is 128 rows: 128/G consecutive tokens times the
 // G query heads that share one KV head, so every key tile serves all of them.
-// Key tiles are 128 positions, loaded as 8 groups of 16 rows (a group never
-// straddles a page) by TMA tensor copies with the 128-byte swizzle.  Per key tile
+// A work unit is two consecutive query tiles, A and B, which share every K / V
+// tile the CTA loads.  Key tiles are 128 positions, loaded as 8 groups of 16
+// rows (a group never straddles a page) by TMA tensor copies with the 128-byte
+// swizzle into a ring of slots, K and V of a tile in consecutive slots.  Per key
+// tile and query tile:
 //     S  = Q K^T               tcgen05.mma, M=128 N=128 K=d_h, fp32 in TMEM
 //     P  = 2^(c S - c m)       softmax warps: TMEM -> registers -> bf16 in smem
 //     O += P V                 tcgen05.mma, M=128 N=d_h K=128, fp32 in TMEM
-// with c = log2(e) / sqrt(d_h).  Warp roles (192 threads):
-//   warps 0-3  softmax: warp w reads TMEM lanes 32w..32w+31, one query row per
-//              thread; it stages Q, writes P, rescales O and stores the output;
-//   warp 4     producer: one thread issues the K / V tile copies into a ring;
-//   warp 5     MMA: allocates TMEM, one thread issues the MMAs and commits.
-// S is double-buffered in TMEM, so S of key tile j+1 runs on the tensor cores
-// while the softmax warps work on tile j.
-//
+// with c = log2(e) / sqrt(d_h).  Warp roles (320 threads):
+//   warps 0-3, 4-7  softmax of tiles A, B: warp w reads TMEM lanes 32(w%4) ..
+//              32(w%4)+31, one query row per thread; they stage Q, write P,
+//              rescale O and store the output;
+//   warp 8     producer: one thread issues the K / V tile copies;
+//   warp 9     MMA: allocates TMEM, one thread issues the MMAs and commits.
+// The MMA order S_A(j+1), P V_B(j), S_B(j+1), P V_A(j+1) ... keeps the tensor cores
+// on one tile while the other tile's softmax runs.  A commit after S_A(j+1) also
+// covers P V_A(j), so when tile A's softmax sees S it may overwrite P_A and
+// rescale O_A.
+
 // Exponent base.  Row m only moves when the row's maximum grows by more than 8
 // in log2 units; O and the row sum l are then scaled by 2^(c (m_old - m_new)).
 // Until then every weight is at most 2^8, which bf16 and the fp32 accumulators
@@ -59,7 +65,7 @@ namespace {
 
 constexpr int kRows = 128;                  // query rows per tile = TMEM lanes
 constexpr int kKeys = 128;                  // key positions per key tile
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 320;             // 8 softmax warps, producer, MMA
 constexpr int kPlanThreads = 1024;          // one request per plan thread
 constexpr uint64_t kPfWaitLimitNs = 4000000000ull;
 
@@ -67,19 +73,21 @@ template <int D>
 struct PfGeo {
     static constexpr int CHUNKS = D / 64;                    // 128-byte swizzle columns of Q, K, V
     static constexpr int COL_BYTES = kRows * 128;            // one such column of a 128-row tile
-    static constexpr int Q_BYTES = CHUNKS * COL_BYTES;
-    static constexpr int P_BYTES = (kKeys / 64) * COL_BYTES;
-    static constexpr int KV_BYTES = CHUNKS * kKeys * 128;    // one K or V tile
-    static constexpr int STAGES = D == 64 ? 4 : 2;
-    static constexpr int RING_BYTES = STAGES * 2 * KV_BYTES;
+    static constexpr int Q_BYTES = CHUNKS * COL_BYTES;       // one query tile
+    static constexpr int P_BYTES = (kKeys / 64) * COL_BYTES; // one tile of weights
+    static constexpr int KV_BYTES = CHUNKS * kKeys * 128;    // one K or V tile = one ring slot
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + Q_BYTES + P_BYTES + RING_BYTES + BAR_BYTES;
-    static constexpr uint32_t S_COL = 0;                     // S buffers at columns 0 and 128
-    static constexpr uint32_t O_COL = 256;
+    static constexpr int FIXED = 1024 + 2 * Q_BYTES + 2 * P_BYTES + BAR_BYTES;
+    static constexpr int SLOTS_FIT = (227 * 1024 - FIXED) / KV_BYTES;
+    static constexpr int SLOTS = SLOTS_FIT < 8 ? SLOTS_FIT : 8;
+    static constexpr int SMEM = FIXED + SLOTS * KV_BYTES;
+    static constexpr uint32_t S_COL = 0;                     // S of tiles A and B: columns 0, 128
+    static constexpr uint32_t O_COL = 256;                   // O of tiles A and B: 256, 256 + D
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(D == 64 || D == 128, "prefill: head width 64 or 128");
+    static_assert(SLOTS >= 3, "ring too small");
     static_assert(SMEM <= 227 * 1024, "prefill CTA does not fit an SM");
-    static_assert(3 * STAGES * 8 + 6 * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(2 * SLOTS * 8 + 7 * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
 struct PfParams {
@@ -243,7 +251,7 @@ __device__ __forceinline__ uint32_t sw_off(int r, int u) {
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfParams p) {
     __shared__ int warp_sum[kPlanThreads / 32];
     const int b = threadIdx.x;
-    const int T = kRows / p.G;
+    const int T = 2 * kRows / p.G;                // tokens of one work unit (two query tiles)
     int tiles = 0;
     if (b < p.B) {
         const int c0 = p.cu_new[b], c1 = p.cu_new[b + 1];
@@ -333,14 +341,14 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
     if (*reinterpret_cast<volatile unsigned*>(p.dev_error) & PKV_DEVERR_TIMEOUT) return;
 
     const int2 it = p.items[item];
-    const int b = it.x, tile = it.y;
-    const int G = p.G, T = kRows / G;
+    const int b = it.x, unit = it.y;
+    const int G = p.G, T = kRows / G;                         // tokens per query tile
     const int c0 = p.cu_new[b];
     const int n = p.cu_new[b + 1] - c0;
     const int64_t t_b = p.seq_lens[b];
     const int64_t L0 = t_b - n;
-    const int i0 = tile * T;
-    const int i_end = min(n, i0 + T);                         // tokens i0 .. i_end-1
+    const int i0 = unit * 2 * T;                              // tile A: tokens i0 .. i0+T-1
+    const int i_end = min(n, i0 + 2 * T);                     // the unit's tokens end here
     const int64_t pos_last = L0 + i_end - 1;
     const int64_t lo_first =
         p.window > 0 ? (L0 + i0 - p.window + 1 > 0 ? L0 + i0 - p.window + 1 : 0) : 0;
@@ -350,16 +358,15 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char* Qs = sm;
-    unsigned char* Ps = Qs + M::Q_BYTES;
-    unsigned char* ring = Ps + M::P_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + M::RING_BYTES);
-    uint64_t* k_full = bars;
-    uint64_t* v_full = bars + M::STAGES;
-    uint64_t* kv_empty = bars + 2 * M::STAGES;
-    uint64_t* s_full = bars + 3 * M::STAGES;     // two
-    uint64_t* p_full = s_full + 2;
-    uint64_t* o_done = p_full + 1;
+    unsigned char* Qs = sm;                                   // tiles A, B
+    unsigned char* Ps = Qs + 2 * M::Q_BYTES;                  // tiles A, B
+    unsigned char* ring = Ps + 2 * M::P_BYTES;                // SLOTS K or V tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + M::SLOTS * M::KV_BYTES);
+    uint64_t* slot_full = bars;                  // per slot: copy landed
+    uint64_t* slot_empty = bars + M::SLOTS;      //           MMAs reading it done
+    uint64_t* s_full = bars + 2 * M::SLOTS;      // per tile A, B: S computed
+    uint64_t* p_full = s_full + 2;               //                P written
+    uint64_t* o_done = p_full + 2;               // last P V of both tiles done
     uint64_t* q_ready = o_done + 1;
     uint64_t* drain = q_ready + 1;               // MMA completion on the abort path
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -367,41 +374,44 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < M::STAGES; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < M::SLOTS; ++s) {
+            mbar_init(&slot_full[s], 1);
+            mbar_init(&slot_empty[s], 1);
         }
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(p_full, 128);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 128);
+        }
         mbar_init(o_done, 1);
-        mbar_init(q_ready, 128);
+        mbar_init(q_ready, 256);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(tmem_slot, M::TMEM_COLS);
+    if (warp == 9) tmem_alloc(tmem_slot, M::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp < 4) {
+    if (warp < 8) {
         // ------------------------------------------------------ softmax --
-        const int r = threadIdx.x;                            // query row = TMEM lane
+        const int x = warp >> 2;                              // query tile A (0) or B (1)
+        const int r = threadIdx.x & 127;                      // row of the tile = TMEM lane
         const int g = r % G;
-        const int i = i0 + r / G;
+        const int i = i0 + x * T + r / G;
         const bool valid = i < i_end;
         const int HQ = p.H * G;
         const int64_t row_x = (int64_t)c0 + i;
         const int qh = h * G + g;
+        unsigned char* Qx = Qs + x * M::Q_BYTES;
+        unsigned char* Px = Ps + x * M::P_BYTES;
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.q + (row_x * HQ + qh) * D);
 #pragma unroll
             for (int u = 0; u < D / 8; ++u) {
                 const uint4 v = valid ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(Qs + sw_off(r, u)) = v;
+                *reinterpret_cast<uint4*>(Qx + sw_off(r, u)) = v;
             }
         }
         fence_proxy_async_smem();
@@ -411,89 +421,114 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
         const int64_t hi = valid ? pos : -1;                  // keys lo .. hi
         const int64_t lo = p.window > 0 ? (pos - p.window + 1 > 0 ? pos - p.window + 1 : 0) : 0;
         const float c = p.scale_log2;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t t_s = tmem + ((uint32_t)((warp & 3) * 32) << 16) + M::S_COL + x * kKeys;
+        const uint32_t t_o = tmem + ((uint32_t)((warp & 3) * 32) << 16) + M::O_COL + x * D;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            if (!pf_warp_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.dev_error)) {
+            if (!pf_warp_wait(&s_full[x], j & 1, abort_flag, p.dev_error)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sv[kKeys];
-#pragma unroll
-            for (int cc = 0; cc < kKeys / 32; ++cc)
-                tmem_ld32(tmem + lane_base + M::S_COL + (j & 1) * kKeys + cc * 32, sv + cc * 32);
-            tmem_wait_ld();
+            // keys e_lo .. e_hi of the tile are this row's (none when e_lo > e_hi)
             const int64_t k0 = (kt0 + j) * kKeys;
             const bool full = k0 >= lo && k0 + kKeys - 1 <= hi;
-            // keys e_lo .. e_hi of the tile are this row's (none when e_lo > e_hi)
             const int e_lo = full ? 0 : (int)(lo - k0 > 0 ? (lo - k0 < kKeys ? lo - k0 : kKeys) : 0);
             const int e_hi = full ? kKeys - 1
                                   : (int)(hi - k0 < kKeys - 1 ? (hi - k0 > -1 ? hi - k0 : -1)
                                                               : kKeys - 1);
-            float mx = -INFINITY;
+            // pass 1: row maximum, eight independent chains, 64 columns at a time
+            float m8[8];
 #pragma unroll
-            for (int e = 0; e < kKeys; ++e)
-                if (full || (e >= e_lo && e <= e_hi)) mx = fmaxf(mx, __uint_as_float(sv[e]));
+            for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t sv[64];
+                tmem_ld32(t_s + hh * 64, sv);
+                tmem_ld32(t_s + hh * 64 + 32, sv + 32);
+                tmem_wait_ld();
+                if (!full) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
+                }
+#pragma unroll
+                for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sv[e]));
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             float alpha = 1.f;
             if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f)) {
                 alpha = m_used == -INFINITY ? 0.f : ex2((m_used - mx) * c);
                 m_used = mx;
                 l *= alpha;
             }
-            // the previous P V must be complete before O is rescaled or P rewritten
-            if (j > 0) {
-                if (!pf_warp_wait(o_done, (j - 1) & 1, abort_flag, p.dev_error)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            // S of this tile was committed after P V of the previous one, so that P V is
+            // complete: O may be rescaled and P overwritten
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t ov[32];
-                        tmem_ld32(tmem + lane_base + M::O_COL + cc * 32, ov);
-                        tmem_wait_ld();
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    tmem_ld32(t_o + cc * 32, ov);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(tmem + lane_base + M::O_COL + cc * 32, ov);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e)
+                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(t_o + cc * 32, ov);
                 }
+                tmem_wait_st();
             }
+            // pass 2: weights 2^(c s - c m), packed FMA for the exponents, the row sum in
+            // four chains of packed adds, bf16 pairs to shared memory
             const float mb = m_used == -INFINITY ? 0.f : m_used * c;
-            float lsum = 0.f;
+            const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
+            float2 acc[4];
 #pragma unroll
-            for (int u = 0; u < kKeys / 8; ++u) {
-                uint32_t w[4];
+            for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = u * 8 + 2 * k;
-                    const bool a0 = full || (e >= e_lo && e <= e_hi);
-                    const bool a1 = full || (e + 1 >= e_lo && e + 1 <= e_hi);
-                    const float p0 = a0 ? ex2(fmaf(__uint_as_float(sv[e]), c, -mb)) : 0.f;
-                    const float p1 = a1 ? ex2(fmaf(__uint_as_float(sv[e + 1]), c, -mb)) : 0.f;
-                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                    lsum += __low2float(pb) + __high2float(pb);
-                    w[k] = *reinterpret_cast<const uint32_t*>(&pb);
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t sv[64];
+                tmem_ld32(t_s + hh * 64, sv);
+                tmem_ld32(t_s + hh * 64 + 32, sv + 32);
+                tmem_wait_ld();
+                if (!full) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
                 }
-                *reinterpret_cast<uint4*>(Ps + sw_off(r, u)) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = u * 8 + 2 * k;
+                        const float2 xe = __ffma2_rn(
+                            make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
+                        const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
+                        acc[k] = __fadd2_rn(acc[k], pr);
+                        const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
+                        w[k] = *reinterpret_cast<const uint32_t*>(&pb);
+                    }
+                    *reinterpret_cast<uint4*>(Px + sw_off(r, hh * 8 + u)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
             }
-            l += lsum;
+            const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+            const float2 a = __fadd2_rn(a01, a23);
+            l += a.x + a.y;
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[x]);
         }
-        if (ok && pf_warp_wait(o_done, (ntiles - 1) & 1, abort_flag, p.dev_error)) {
+        if (ok && pf_warp_wait(o_done, 0, abort_flag, p.dev_error)) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             float4* dst = reinterpret_cast<float4*>(p.out + (row_x * HQ + qh) * D);
 #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t ov[32];
-                tmem_ld32(tmem + lane_base + M::O_COL + cc * 32, ov);
+                tmem_ld32(t_o + cc * 32, ov);
                 tmem_wait_ld();
                 if (valid) {
 #pragma unroll
@@ -504,20 +539,16 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
                 }
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == 8) {
         // ----------------------------------------------------- producer --
+        // loads in order: K of tile j is load 2j, V of tile j load 2j+1, into slot
+        // load % SLOTS once the MMAs that read the slot's previous tile are done
         if (lane == 0) {
             const uint64_t pol = l2_normal_policy();
             const int32_t* table = p.tables + (int64_t)b * p.max_pages;
             int issued = 0;
             bool aborted = false;
-            for (int j = 0; j < ntiles; ++j) {
-                const int s = j % M::STAGES;
-                if (j >= M::STAGES &&
-                    !pf_wait(&kv_empty[s], ((j / M::STAGES) - 1) & 1, abort_flag, p.dev_error)) {
-                    aborted = true;
-                    break;
-                }
+            for (int j = 0; j < ntiles && !aborted; ++j) {
                 const int64_t k0 = (kt0 + j) * kKeys;
                 int y[kKeys / 16];
 #pragma unroll
@@ -532,98 +563,131 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
                             atomicOr(p.dev_error, PKV_DEVERR_PAGE_ID);
                     }
                 }
-                unsigned char* Ks = ring + s * 2 * M::KV_BYTES;
-                unsigned char* Vs = Ks + M::KV_BYTES;
-                mbar_arrive_expect_tx(&k_full[s], M::KV_BYTES);
 #pragma unroll
-                for (int gi = 0; gi < kKeys / 16; ++gi)
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int ld = 2 * j + kv, s = ld % M::SLOTS;
+                    if (ld >= M::SLOTS &&
+                        !pf_wait(&slot_empty[s], ((ld / M::SLOTS) - 1) & 1, abort_flag, p.dev_error)) {
+                        aborted = true;
+                        break;
+                    }
+                    unsigned char* dst = ring + s * M::KV_BYTES;
+                    const CUtensorMap* map = kv ? &tmv : &tmk;
+                    mbar_arrive_expect_tx(&slot_full[s], M::KV_BYTES);
 #pragma unroll
-                    for (int cc = 0; cc < M::CHUNKS; ++cc)
-                        tma_load_2d(Ks + cc * kKeys * 128 + gi * 2048, &tmk, cc * 64, y[gi],
-                                    &k_full[s], pol);
-                mbar_arrive_expect_tx(&v_full[s], M::KV_BYTES);
+                    for (int gi = 0; gi < kKeys / 16; ++gi)
 #pragma unroll
-                for (int gi = 0; gi < kKeys / 16; ++gi)
-#pragma unroll
-                    for (int cc = 0; cc < M::CHUNKS; ++cc)
-                        tma_load_2d(Vs + cc * kKeys * 128 + gi * 2048, &tmv, cc * 64, y[gi],
-                                    &v_full[s], pol);
-                ++issued;
+                        for (int cc = 0; cc < M::CHUNKS; ++cc)
+                            tma_load_2d(dst + cc * kKeys * 128 + gi * 2048, map, cc * 64, y[gi],
+                                        &slot_full[s], pol);
+                    ++issued;
+                }
             }
             if (aborted || *abort_flag) {
                 // let the copies in flight land before the CTA's shared memory goes away
-                for (int j = issued - M::STAGES > 0 ? issued - M::STAGES : 0; j < issued; ++j) {
-                    const int s = j % M::STAGES;
-                    mbar_wait_bounded(&k_full[s], (j / M::STAGES) & 1, kPfWaitLimitNs);
-                    mbar_wait_bounded(&v_full[s], (j / M::STAGES) & 1, kPfWaitLimitNs);
-                }
+                for (int ld = issued - M::SLOTS > 0 ? issued - M::SLOTS : 0; ld < issued; ++ld)
+                    mbar_wait_bounded(&slot_full[ld % M::SLOTS], (ld / M::SLOTS) & 1, kPfWaitLimitNs);
             }
         }
     } else {
         // ---------------------------------------------------------- MMA --
+        // S_A(0) S_B(0) | P V_A(j) S_A(j+1) P V_B(j) S_B(j+1) | ... : while one
+        // tile's softmax runs, the tensor cores work on the other tile
         constexpr uint32_t idS = idesc_bf16(kKeys, false);
         constexpr uint32_t idO = idesc_bf16(D, true);
         // V is MN-major: 64-column swizzle atoms kKeys * 128 bytes apart, 8-row groups
         // 1024 bytes apart.  With D = 64 there is a single atom column, and the atom
         // stride is set equal to the group stride.
         constexpr uint32_t kVLbo = D == 64 ? 1024u : (uint32_t)(kKeys * 128);
-        const uint32_t q_addr = smem_u32(Qs), p_addr = smem_u32(Ps);
-        bool ok = pf_warp_wait(q_ready, 0, abort_flag, p.dev_error);
-        bool issued_any = false;
-        for (int j = 0; ok && j <= ntiles; ++j) {
-            if (j < ntiles) {
-                const int s = j % M::STAGES;
-                if (!pf_warp_wait(&k_full[s], (j / M::STAGES) & 1, abort_flag, p.dev_error)) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t k_addr = smem_u32(ring + s * 2 * M::KV_BYTES);
-                    const uint32_t d = tmem + M::S_COL + (j & 1) * kKeys;
+        const uint32_t q_addr = smem_u32(Qs), p_addr = smem_u32(Ps), ring_addr = smem_u32(ring);
+        auto wait_slot = [&](int ld) {
+            return pf_warp_wait(&slot_full[ld % M::SLOTS], (ld / M::SLOTS) & 1, abort_flag,
+                                p.dev_error);
+        };
+        auto issue_s = [&](int j, int x) {
+            const uint32_t k_addr = ring_addr + ((2 * j) % M::SLOTS) * M::KV_BYTES;
+            const uint32_t qa = q_addr + x * M::Q_BYTES;
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-                        umma_bf16(d, sw128_desc(q_addr + off, 16, 1024),
-                                  sw128_desc(k_addr + off, 16, 1024), idS, k > 0);
-                    }
-                    umma_commit(&s_full[j & 1]);
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+                umma_bf16(tmem + M::S_COL + x * kKeys, sw128_desc(qa + off, 16, 1024),
+                          sw128_desc(k_addr + off, 16, 1024), idS, k > 0);
+            }
+            umma_commit(&s_full[x]);
+        };
+        auto issue_pv = [&](int j, int x) {
+            const uint32_t v_addr = ring_addr + ((2 * j + 1) % M::SLOTS) * M::KV_BYTES;
+            const uint32_t pa = p_addr + x * M::P_BYTES;
+#pragma unroll
+            for (int k = 0; k < kKeys / 16; ++k) {
+                const uint32_t a_off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+                umma_bf16(tmem + M::O_COL + x * D, sw128_desc(pa + a_off, 16, 1024),
+                          sw128_desc(v_addr + k * 16 * 128, kVLbo, 1024), idO,
+                          (j > 0 || k > 0) ? 1u : 0u);
+            }
+        };
+        bool ok = pf_warp_wait(q_ready, 0, abort_flag, p.dev_error) && wait_slot(0);
+        bool issued_any = false;
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0) {
+                issue_s(0, 0);
+                issue_s(0, 1);
+                umma_commit(&slot_empty[0]);
+            }
+            issued_any = true;
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+            const bool more = j + 1 < ntiles;
+            if (!pf_warp_wait(&p_full[0], j & 1, abort_flag, p.dev_error) || !wait_slot(2 * j + 1)) {
+                ok = false;
+                break;
+            }
+            if (j == ntiles - 1) {
+                // rows at positions >= t_b of the last loaded group hold stale bytes,
+                // possibly not finite: clear them in V (their weights are 0)
+                unsigned char* Vs = ring + ((2 * j + 1) % M::SLOTS) * M::KV_BYTES;
+                const int64_t k0 = (kt0 + j) * kKeys;
+                const int r0 = (int)(t_b - k0);
+                const int r1 = (int)(((pos_last - k0) / 16 + 1) * 16);
+                for (int idx = lane; idx < (r1 - r0) * M::CHUNKS * 8; idx += 32) {
+                    const int row = r0 + idx / (M::CHUNKS * 8);
+                    const int piece = idx % (M::CHUNKS * 8);
+                    *reinterpret_cast<uint4*>(Vs + (piece >> 3) * kKeys * 128 + row * 128 +
+                                              (piece & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
-                issued_any = true;
+                fence_proxy_async_smem();
                 __syncwarp();
             }
-            if (j > 0) {
-                const int jj = j - 1, s = jj % M::STAGES;
-                if (!pf_warp_wait(p_full, jj & 1, abort_flag, p.dev_error)) break;
-                if (!pf_warp_wait(&v_full[s], (jj / M::STAGES) & 1, abort_flag, p.dev_error)) break;
-                unsigned char* Vs = ring + s * 2 * M::KV_BYTES + M::KV_BYTES;
-                if (jj == ntiles - 1) {
-                    // rows at positions >= t_b of the last loaded group hold stale
-                    // bytes, possibly not finite: clear them in V (their weights are 0)
-                    const int64_t k0 = (kt0 + jj) * kKeys;
-                    const int r0 = (int)(t_b - k0);
-                    const int r1 = (int)(((pos_last - k0) / 16 + 1) * 16);
-                    for (int idx = lane; idx < (r1 - r0) * M::CHUNKS * 8; idx += 32) {
-                        const int row = r0 + idx / (M::CHUNKS * 8);
-                        const int piece = idx % (M::CHUNKS * 8);
-                        *reinterpret_cast<uint4*>(Vs + (piece >> 3) * kKeys * 128 + row * 128 +
-                                                  (piece & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+            tc_fence_after();
+            if (lane == 0) issue_pv(j, 0);
+            __syncwarp();
+            if (more) {
+                if (!wait_slot(2 * j + 2)) {
+                    ok = false;
+                    break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t v_addr = smem_u32(Vs);
-#pragma unroll
-                    for (int k = 0; k < kKeys / 16; ++k) {
-                        const uint32_t a_off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-                        umma_bf16(tmem + M::O_COL, sw128_desc(p_addr + a_off, 16, 1024),
-                                  sw128_desc(v_addr + k * 16 * 128, kVLbo, 1024), idO,
-                                  (jj > 0 || k > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&kv_empty[s]);
+                if (lane == 0) issue_s(j + 1, 0);
+                __syncwarp();
+            }
+            if (!pf_warp_wait(&p_full[1], j & 1, abort_flag, p.dev_error)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                issue_pv(j, 1);
+                umma_commit(&slot_empty[(2 * j + 1) % M::SLOTS]);
+                if (more) {
+                    issue_s(j + 1, 1);
+                    umma_commit(&slot_empty[(2 * j + 2) % M::SLOTS]);
+                } else {
                     umma_commit(o_done);
                 }
-                __syncwarp();
             }
+            __syncwarp();
         }
         if (issued_any && *abort_flag) {
             // MMAs still in flight read shared memory and write TMEM: let them finish
@@ -637,7 +701,7 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, M::TMEM_COLS);
     }
@@ -677,7 +741,7 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const PfParams& p, cudaStream
 }  // namespace
 
 int64_t prefill_max_tiles(int B, int G, int64_t total_new) {
-    return total_new / (kRows / G) + B;
+    return total_new / (2 * kRows / G) + B;
 }
 
 size_t prefill_workspace_bytes(int B, int G, int64_t total_new) {
