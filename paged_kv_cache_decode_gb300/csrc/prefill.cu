@@ -23,18 +23,21 @@
 // swizzle into a ring of slots, K and V of a tile in consecutive slots.  Per key
 // tile and query tile:
 //     S  = Q K^T               tcgen05.mma, M=128 N=128 K=d_h, fp32 in TMEM
-//     P  = 2^(c S - c m)       softmax warps: TMEM -> registers -> bf16 in smem
-//     O += P V                 tcgen05.mma, M=128 N=d_h K=128, fp32 in TMEM
+//     P  = 2^(c S - c m)       softmax warps: TMEM -> registers -> bf16 back into
+//                              TMEM over the S columns already read
+//     O += P V                 tcgen05.mma with A = P from TMEM, M=128 N=d_h K=128
 // with c = log2(e) / sqrt(d_h).  Warp roles (320 threads):
 //   warps 0-3, 4-7  softmax of tiles A, B: warp w reads TMEM lanes 32(w%4) ..
 //              32(w%4)+31, one query row per thread; they stage Q, write P,
 //              rescale O and store the output;
-//   warp 8     producer: one thread issues the K / V tile copies;
+//   warp 8     producer: eight lanes issue the K / V tile copies, one 16-row
+//              group each;
 //   warp 9     MMA: allocates TMEM, one thread issues the MMAs and commits.
-// The MMA order S_A(j+1), P V_B(j), S_B(j+1), P V_A(j+1) ... keeps the tensor cores
-// on one tile while the other tile's softmax runs.  A commit after S_A(j+1) also
-// covers P V_A(j), so when tile A's softmax sees S it may overwrite P_A and
-// rescale O_A.
+// The MMA order P V_A(j), S_A(j+1), P V_B(j), S_B(j+1) ... keeps the tensor cores
+// on one tile while the other tile's softmax runs.  MMAs of one thread run in
+// issue order, so S_A(j+1) overwrites P_A(j) only after P V_A(j) has read it, and
+// a commit after S_A(j+1) also covers P V_A(j): when tile A's softmax sees S it
+// may rescale O_A.
 
 // Exponent base.  Row m only moves when the row's maximum grows by more than 8
 // in log2 units; O and the row sum l are then scaled by 2^(c (m_old - m_new)).
@@ -74,15 +77,15 @@ struct PfGeo {
     static constexpr int CHUNKS = D / 64;                    // 128-byte swizzle columns of Q, K, V
     static constexpr int COL_BYTES = kRows * 128;            // one such column of a 128-row tile
     static constexpr int Q_BYTES = CHUNKS * COL_BYTES;       // one query tile
-    static constexpr int P_BYTES = (kKeys / 64) * COL_BYTES; // one tile of weights
     static constexpr int KV_BYTES = CHUNKS * kKeys * 128;    // one K or V tile = one ring slot
     static constexpr int BAR_BYTES = 256;
-    static constexpr int FIXED = 1024 + 2 * Q_BYTES + 2 * P_BYTES + BAR_BYTES;
+    static constexpr int FIXED = 1024 + 2 * Q_BYTES + BAR_BYTES;
     static constexpr int SLOTS_FIT = (227 * 1024 - FIXED) / KV_BYTES;
     static constexpr int SLOTS = SLOTS_FIT < 8 ? SLOTS_FIT : 8;
     static constexpr int SMEM = FIXED + SLOTS * KV_BYTES;
     static constexpr uint32_t S_COL = 0;                     // S of tiles A and B: columns 0, 128
     static constexpr uint32_t O_COL = 256;                   // O of tiles A and B: 256, 256 + D
+    // P (bf16 pairs, 64 columns) overwrites the first half of its tile's S columns
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(D == 64 || D == 128, "prefill: head width 64 or 128");
     static_assert(SLOTS >= 3, "ring too small");
@@ -135,6 +138,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with A read from TMEM (M rows on lanes, bf16 pairs along columns).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -359,8 +373,7 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* Qs = sm;                                   // tiles A, B
-    unsigned char* Ps = Qs + 2 * M::Q_BYTES;                  // tiles A, B
-    unsigned char* ring = Ps + 2 * M::P_BYTES;                // SLOTS K or V tiles
+    unsigned char* ring = Qs + 2 * M::Q_BYTES;                // SLOTS K or V tiles
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + M::SLOTS * M::KV_BYTES);
     uint64_t* slot_full = bars;                  // per slot: copy landed
     uint64_t* slot_empty = bars + M::SLOTS;      //           MMAs reading it done
@@ -405,7 +418,6 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
         const int64_t row_x = (int64_t)c0 + i;
         const int qh = h * G + g;
         unsigned char* Qx = Qs + x * M::Q_BYTES;
-        unsigned char* Px = Ps + x * M::P_BYTES;
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.q + (row_x * HQ + qh) * D);
 #pragma unroll
@@ -465,7 +477,7 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
                 l *= alpha;
             }
             // S of this tile was committed after P V of the previous one, so that P V is
-            // complete: O may be rescaled and P overwritten
+            // complete: O may be rescaled
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
@@ -480,7 +492,8 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
                 tmem_wait_st();
             }
             // pass 2: weights 2^(c s - c m), packed FMA for the exponents, the row sum in
-            // four chains of packed adds, bf16 pairs to shared memory
+            // four chains of packed adds; bf16 pairs into TMEM over the S columns already
+            // read (keys 2i, 2i+1 -> column i)
             const float mb = m_used == -INFINITY ? 0.f : m_used * c;
             const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
             float2 acc[4];
@@ -497,27 +510,22 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
                     for (int e = 0; e < 64; ++e)
                         if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
                 }
+                uint32_t w[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = u * 8 + 2 * k;
-                        const float2 xe = __ffma2_rn(
-                            make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
-                        const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
-                        acc[k] = __fadd2_rn(acc[k], pr);
-                        const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
-                        w[k] = *reinterpret_cast<const uint32_t*>(&pb);
-                    }
-                    *reinterpret_cast<uint4*>(Px + sw_off(r, hh * 8 + u)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 xe = __ffma2_rn(
+                        make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
+                    const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
+                    acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], pr);
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
+                    w[e >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
                 }
+                tmem_st32(t_s + hh * 32, w);
             }
+            tmem_wait_st();
             const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
             const float2 a = __fadd2_rn(a01, a23);
             l += a.x + a.y;
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&p_full[x]);
         }
@@ -542,52 +550,48 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
     } else if (warp == 8) {
         // ----------------------------------------------------- producer --
         // loads in order: K of tile j is load 2j, V of tile j load 2j+1, into slot
-        // load % SLOTS once the MMAs that read the slot's previous tile are done
-        if (lane == 0) {
-            const uint64_t pol = l2_normal_policy();
-            const int32_t* table = p.tables + (int64_t)b * p.max_pages;
-            int issued = 0;
-            bool aborted = false;
-            for (int j = 0; j < ntiles && !aborted; ++j) {
-                const int64_t k0 = (kt0 + j) * kKeys;
-                int y[kKeys / 16];
+        // load % SLOTS once the MMAs that read the slot's previous tile are done.
+        // Lane gi < 8 looks up the page of the tile's 16-row group gi and issues its
+        // boxes; lane 0 arms the slot's barrier first.
+        const uint64_t pol = l2_normal_policy();
+        const int32_t* table = p.tables + (int64_t)b * p.max_pages;
+        const int gi = lane & 7;
+        int issued = 0;
+        bool aborted = false;
+        for (int j = 0; j < ntiles && !aborted; ++j) {
+            const int64_t key = (kt0 + j) * kKeys + 16 * gi;
+            int y = p.pool_rows;                                    // past the pool: reads zeros
+            if (lane < 8 && key <= pos_last) {
+                const int32_t page = table[key / p.P];
+                if (page >= 0 && page < p.n_pages)
+                    y = (int)(((int64_t)page * p.H + h) * p.P + key % p.P);
+                else
+                    atomicOr(p.dev_error, PKV_DEVERR_PAGE_ID);
+            }
 #pragma unroll
-                for (int gi = 0; gi < kKeys / 16; ++gi) {
-                    const int64_t key = k0 + 16 * gi;
-                    y[gi] = p.pool_rows;                            // past the pool: reads zeros
-                    if (key <= pos_last) {
-                        const int32_t page = table[key / p.P];
-                        if (page >= 0 && page < p.n_pages)
-                            y[gi] = (int)(((int64_t)page * p.H + h) * p.P + key % p.P);
-                        else
-                            atomicOr(p.dev_error, PKV_DEVERR_PAGE_ID);
-                    }
+            for (int kv = 0; kv < 2; ++kv) {
+                const int ld = 2 * j + kv, s = ld % M::SLOTS;
+                if (ld >= M::SLOTS && !pf_warp_wait(&slot_empty[s], ((ld / M::SLOTS) - 1) & 1,
+                                                    abort_flag, p.dev_error)) {
+                    aborted = true;
+                    break;
                 }
-#pragma unroll
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int ld = 2 * j + kv, s = ld % M::SLOTS;
-                    if (ld >= M::SLOTS &&
-                        !pf_wait(&slot_empty[s], ((ld / M::SLOTS) - 1) & 1, abort_flag, p.dev_error)) {
-                        aborted = true;
-                        break;
-                    }
-                    unsigned char* dst = ring + s * M::KV_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(&slot_full[s], M::KV_BYTES);
+                __syncwarp();
+                if (lane < 8) {
+                    unsigned char* dst = ring + s * M::KV_BYTES + gi * 2048;
                     const CUtensorMap* map = kv ? &tmv : &tmk;
-                    mbar_arrive_expect_tx(&slot_full[s], M::KV_BYTES);
 #pragma unroll
-                    for (int gi = 0; gi < kKeys / 16; ++gi)
-#pragma unroll
-                        for (int cc = 0; cc < M::CHUNKS; ++cc)
-                            tma_load_2d(dst + cc * kKeys * 128 + gi * 2048, map, cc * 64, y[gi],
-                                        &slot_full[s], pol);
-                    ++issued;
+                    for (int cc = 0; cc < M::CHUNKS; ++cc)
+                        tma_load_2d(dst + cc * kKeys * 128, map, cc * 64, y, &slot_full[s], pol);
                 }
+                ++issued;
             }
-            if (aborted || *abort_flag) {
-                // let the copies in flight land before the CTA's shared memory goes away
-                for (int ld = issued - M::SLOTS > 0 ? issued - M::SLOTS : 0; ld < issued; ++ld)
-                    mbar_wait_bounded(&slot_full[ld % M::SLOTS], (ld / M::SLOTS) & 1, kPfWaitLimitNs);
-            }
+        }
+        if (lane == 0 && (aborted || *abort_flag)) {
+            // let the copies in flight land before the CTA's shared memory goes away
+            for (int ld = issued - M::SLOTS > 0 ? issued - M::SLOTS : 0; ld < issued; ++ld)
+                mbar_wait_bounded(&slot_full[ld % M::SLOTS], (ld / M::SLOTS) & 1, kPfWaitLimitNs);
         }
     } else {
         // ---------------------------------------------------------- MMA --
@@ -599,7 +603,7 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
         // 1024 bytes apart.  With D = 64 there is a single atom column, and the atom
         // stride is set equal to the group stride.
         constexpr uint32_t kVLbo = D == 64 ? 1024u : (uint32_t)(kKeys * 128);
-        const uint32_t q_addr = smem_u32(Qs), p_addr = smem_u32(Ps), ring_addr = smem_u32(ring);
+        const uint32_t q_addr = smem_u32(Qs), ring_addr = smem_u32(ring);
         auto wait_slot = [&](int ld) {
             return pf_warp_wait(&slot_full[ld % M::SLOTS], (ld / M::SLOTS) & 1, abort_flag,
                                 p.dev_error);
@@ -617,14 +621,12 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
         };
         auto issue_pv = [&](int j, int x) {
             const uint32_t v_addr = ring_addr + ((2 * j + 1) % M::SLOTS) * M::KV_BYTES;
-            const uint32_t pa = p_addr + x * M::P_BYTES;
+            const uint32_t pa = tmem + M::S_COL + x * kKeys;        // P in TMEM, 8 columns per k-step
 #pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k) {
-                const uint32_t a_off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-                umma_bf16(tmem + M::O_COL + x * D, sw128_desc(pa + a_off, 16, 1024),
-                          sw128_desc(v_addr + k * 16 * 128, kVLbo, 1024), idO,
-                          (j > 0 || k > 0) ? 1u : 0u);
-            }
+            for (int k = 0; k < kKeys / 16; ++k)
+                umma_bf16_tmem_a(tmem + M::O_COL + x * D, pa + k * 8,
+                                 sw128_desc(v_addr + k * 16 * 128, kVLbo, 1024), idO,
+                                 (j > 0 || k > 0) ? 1u : 0u);
         };
         bool ok = pf_warp_wait(q_ready, 0, abort_flag, p.dev_error) && wait_slot(0);
         bool issued_any = false;
