@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention: achieved HBM GB/s (% of 8 TB/s) and decode tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "decode.cu")
+PREFILL_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "prefill.cu")
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -219,25 +220,25 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_hash() -> str:
-    with open(DECODE_SRC, "rb") as f:
+def source_hash(path: str) -> str:
+    with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per launch of the split kernel from the committed ncu summary
-    profiles/traffic_split_decode_<workload>.txt, or None when there is none or
-    the kernel source changed since the counters were taken."""
+def measured_traffic(workload: str, kernel: str = "split_decode", source: str = DECODE_SRC):
+    """DRAM bytes per launch of a kernel from the committed ncu summary
+    profiles/traffic_<kernel>_<workload>.txt, or None when there is none or the
+    kernel source changed since the counters were taken."""
     rec = {}
     try:
-        with open(os.path.join(TRAFFIC_DIR, f"traffic_split_decode_{workload}.txt")) as f:
+        with open(os.path.join(TRAFFIC_DIR, f"traffic_{kernel}_{workload}.txt")) as f:
             for line in f:
                 line = line.split("#", 1)[0].split()
                 if len(line) == 2:
                     rec[line[0]] = line[1]
     except OSError:
         return None
-    if rec.get("source_sha256") != decode_source_hash() or "dram_bytes_per_launch" not in rec:
+    if rec.get("source_sha256") != source_hash(source) or "dram_bytes_per_launch" not in rec:
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -707,7 +708,8 @@ def run_gpu_prefill(args):
                        "parallelism": f"replicas x{world}"},
             "tokens_per_s": round(world * N / (step_ms_max * 1e-3), 1),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "traffic": measured_traffic(w.name, "prefill_attention", PREFILL_SRC),
                          "kernel": "prefill_attention_kernel<%d>" % w.D,
                          "kernel_ms": round(kernel_ms, 5),
                          "peak_kind": peak_kind + " (bf16_tflops burst, cuBLAS)"},
