@@ -242,7 +242,9 @@ int pkv_request_counters(const pkv_request* req, pkv_counters* out);
  * it (= the visible length).  If that position starts a page the request does
  * not hold yet, one page is leased from the free list's front; if it falls in a
  * page another request also references (after pkv_request_fork), a private
- * page is leased from the front to replace it (copy-on-write).
+ * page is leased from the front to replace it (copy-on-write); the request
+ * keeps its reference to the shared page until pkv_commit_token drops it (to
+ * the free list's back if it was the last one), so an abort can restore it.
  * BAD_STATE if a token is already pending; CAPACITY_EXCEEDED at max_context;
  * OUT_OF_PAGES if a page is needed and none is free.
  */
@@ -267,18 +269,54 @@ int pkv_begin_token(pkv_request* req, int64_t* position);
 int pkv_append_and_attend(pkv_request* req, int layer, const float* q, const void* k,
                           const void* v, float* out, void* stream);
 
-/* Make the pending position visible ([SERVE-FLOW] step 3).  BAD_STATE unless a
- * token is pending and every layer ran pkv_append_and_attend for it exactly
- * once ([CACHED-BIND]: all layers advance together).  Counters advance by
- * layers (appends) and layers x query_heads x t (score cells). */
+/*
+ * Open a chunk of n >= 1 positions at the visible length, the batched prefill
+ * of one request taken through the same transaction ([SERVE-PAGED]: a batched
+ * prefill writing the same paged cache; [SERVE-FLOW] steps 1-4 for n positions
+ * at once).  *position receives the first.  Pages for all n positions are
+ * leased now from the free list's front: first a private copy for every page
+ * another request also references among those the chunk writes (ascending
+ * logical index; copy-on-write), then the pages the request does not hold yet.
+ * All or nothing: BAD_STATE if a token or chunk is pending; CAPACITY_EXCEEDED
+ * if length + n passes max_context; OUT_OF_PAGES if too few pages are free;
+ * UNSUPPORTED on a device pool that pkv_paged_prefill does not take (host-only
+ * pools keep the bookkeeping).  Then pkv_prefill_chunk once per layer and
+ * pkv_commit_token or pkv_abort_token.
+ */
+int pkv_begin_chunk(pkv_request* req, int64_t n, int64_t* position);
+
+/*
+ * One layer's step for the pending chunk: store its n key/value rows at
+ * positions position .. position+n-1 of `layer`'s pools and attend each of its
+ * queries causally, as pkv_paged_prefill does for one request (chunk token i
+ * over positions 0 .. position+i, the window applied).
+ *   q   [n][query_heads][head_dim] bf16, device
+ *   k,v [n][kv_heads][head_dim] bf16, device
+ *   out [n][query_heads][head_dim] fp32, device
+ * Call once per layer per pending chunk; BAD_STATE if no chunk is pending (a
+ * pending single token takes pkv_append_and_attend) or the layer already ran.
+ * The rows are written at once but are visible to later tokens only after
+ * pkv_commit_token.  Enqueues a page-table upload of the changed entries, one
+ * device-to-device copy per copy-on-write page and the three prefill kernels on
+ * `stream`; returns without waiting.
+ */
+int pkv_prefill_chunk(pkv_request* req, int layer, const void* q, const void* k, const void* v,
+                      float* out, void* stream);
+
+/* Make the pending position, or every position of the pending chunk, visible
+ * ([SERVE-FLOW] step 3).  BAD_STATE unless a token or chunk is pending and
+ * every layer ran pkv_append_and_attend (pkv_prefill_chunk) for it exactly
+ * once ([CACHED-BIND]: all layers advance together).  Counters count each
+ * position as one committed token: appends advance by layers, score cells by
+ * layers x query_heads x min(t, window) for each new retained length t. */
 int pkv_commit_token(pkv_request* req);
 
-/* Drop the pending token ([SERVE-FLOW] step 4): the visible length stays, and a
- * page leased by its pkv_begin_token (new or copy-on-write) goes back to the
- * front of the free list while a shared page gets its place back, so table,
- * page references and free list are exactly as before pkv_begin_token.  Rows
- * already written for it stay in the page, unreachable, and are overwritten by
- * the retry.  BAD_STATE if no token is pending. */
+/* Drop the pending token or chunk ([SERVE-FLOW] step 4): the visible length
+ * stays, the pages its begin leased (new or copy-on-write) go back to the
+ * front of the free list, last leased first, and shared pages get their places
+ * back, so table, page references and free list are exactly as before the
+ * begin.  Rows already written stay in the pages, unreachable, and are
+ * overwritten by the retry.  BAD_STATE if nothing is pending. */
 int pkv_abort_token(pkv_request* req);
 
 /* -------------------------------------------------------------- batched -- */

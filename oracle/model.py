@@ -42,8 +42,22 @@ future work; this is the plainest reading):
 * writing a token into a page that another request also references first
   moves the writer to a private copy: ``begin_token`` leases a fresh page for
   that logical page (from the free list's front), and the page's K/V bytes are
-  copied into it before the token's row is written; ``abort_token`` restores
-  the shared page and returns the fresh one to the front.
+  copied into it before the token's row is written.  The writer keeps its
+  reference to the shared page while the token is pending: ``commit_token``
+  drops it (the page goes to the back of the free list if that was its last
+  reference), ``abort_token`` puts the shared page back in the table and
+  returns the fresh one to the front.  So a sharer that leaves while the
+  token is pending cannot free a page the abort would restore.
+
+Chunks (the batched prefill of "Incremental Serving", section "Paged KV-cache
+layout", taken through the same transaction): ``begin_chunk(n)`` opens n
+positions at the visible length at once.  Pages for all of them are leased
+now, the shared pages among those the chunk writes are replaced by private
+copies first (ascending logical index), then pages for logical indices the
+request does not hold yet; ``prefill_chunk`` runs once per layer; commit makes
+all n visible and counts each as a committed token; abort returns the leased
+pages to the free list's front, last leased first, so the pool is exactly as
+before ``begin_chunk``.
 """
 from __future__ import annotations
 
@@ -51,7 +65,7 @@ import collections
 
 import numpy as np
 
-from . import F32, paged_decode_attention, append as _append
+from . import F32, paged_decode_attention, paged_prefill, append as _append
 
 MASK64 = (1 << 64) - 1
 
@@ -204,39 +218,47 @@ class OracleRequest:
 
     # -- the transaction ------------------------------------------------------
     def begin_token(self) -> int:
+        return self._begin(1, chunk=False)
+
+    def begin_chunk(self, n: int) -> int:
+        """Open a chunk of n tokens at the visible length (batched prefill)."""
+        if n < 1:
+            raise OracleError(Status.INVALID_ARGUMENT, "a chunk holds at least one token")
+        return self._begin(n, chunk=True)
+
+    def _begin(self, n: int, chunk: bool) -> int:
         p = self.pool
         if self.pending is not None:
             raise OracleError(Status.BAD_STATE, "token already pending")
-        if self.length >= p.max_context:
+        if self.length + n > p.max_context:
             raise OracleError(Status.CAPACITY_EXCEEDED, "maximum context reached")
-        leased = None
-        cow = None
-        idx = self.length // p.P
-        if idx >= len(self.table):
-            if not p.free:
-                raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
-            leased = p._lease()
-            self.table.append(leased)
-        elif p.refs[self.table[idx]] > 1:
+        first, last = self.length // p.P, (self.length + n - 1) // p.P
+        held = len(self.table)
+        shared = [i for i in range(first, min(last, held - 1) + 1) if p.refs[self.table[i]] > 1]
+        new = max(0, last + 1 - held)
+        if len(shared) + new > len(p.free):
+            raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
+        cow = []
+        for idx in shared:
             # the page is shared: write into a private copy
-            if not p.free:
-                raise OracleError(Status.OUT_OF_PAGES, "pool exhausted")
             old = self.table[idx]
-            new = p._lease()
-            p.refs[old] -= 1
-            self.table[idx] = new
+            page = p._lease()
+            self.table[idx] = page
             if p.k is not None:
-                p.k[:, new] = p.k[:, old]
-                p.v[:, new] = p.v[:, old]
-            cow = (idx, old, new)
-        self.pending = dict(pos=self.length, leased=leased, cow=cow, appended=set())
+                p.k[:, page] = p.k[:, old]
+                p.v[:, page] = p.v[:, old]
+            cow.append((idx, old, page))
+        leased = [p._lease() for _ in range(new)]
+        self.table.extend(leased)
+        self.pending = dict(pos=self.length, n=n, chunk=chunk, leased=leased, cow=cow,
+                            appended=set())
         return self.length
 
     def append_and_attend(self, layer: int, q: np.ndarray, k: np.ndarray, v: np.ndarray,
                           compute: bool = True):
         """q [HQ, D] fp32; k, v [H, D] storage dtype.  Returns out [HQ, D] fp64 (or None)."""
         p = self.pool
-        if self.pending is None:
+        if self.pending is None or self.pending["chunk"]:
             raise OracleError(Status.BAD_STATE, "no token pending")
         if not 0 <= layer < p.layers:
             raise OracleError(Status.INVALID_ARGUMENT, "layer out of range")
@@ -255,31 +277,59 @@ class OracleRequest:
         self.pending["appended"].add(layer)
         return out
 
+    def prefill_chunk(self, layer: int, q: np.ndarray, k: np.ndarray, v: np.ndarray,
+                      compute: bool = True):
+        """One layer of the pending chunk: q [n, HQ, D] fp32; k, v [n, H, D] storage dtype.
+        Returns out [n, HQ, D] fp64 (or None)."""
+        p = self.pool
+        if self.pending is None or not self.pending["chunk"]:
+            raise OracleError(Status.BAD_STATE, "no chunk pending")
+        if not 0 <= layer < p.layers:
+            raise OracleError(Status.INVALID_ARGUMENT, "layer out of range")
+        if layer in self.pending["appended"]:
+            raise OracleError(Status.BAD_STATE, "layer already ran for this chunk")
+        pos, n = self.pending["pos"], self.pending["n"]
+        tables = np.asarray(self.table, dtype=np.int32)[None, :]
+        kp, vp = p.k[layer], p.v[layer]
+        if compute:
+            out = paged_prefill(kp, vp, q, k, v, np.array([0, n], dtype=np.int32), tables,
+                                np.array([pos + n], dtype=np.int32), p.dtype, group=p.group,
+                                window=p.window)
+        else:
+            for i in range(n):
+                _append(kp, vp, k[i:i + 1], v[i:i + 1], tables,
+                        np.array([pos + i + 1], dtype=np.int32), p.dtype)
+            out = None
+        self.pending["appended"].add(layer)
+        return out
+
     def commit_token(self) -> None:
+        """Commit the pending token or chunk: every position becomes visible; the
+        counters count each position as one committed token."""
         p = self.pool
         if self.pending is None:
             raise OracleError(Status.BAD_STATE, "no token pending")
         if len(self.pending["appended"]) != p.layers:
             raise OracleError(Status.BAD_STATE, "not every layer appended")
-        t = self.pending["pos"] + 1
-        self.length = t
-        self.committed_tokens += 1
-        self.cache_appends += p.layers
-        self.score_cells += p.layers * p.HQ * (min(t, p.window) if p.window else t)
+        pos, n = self.pending["pos"], self.pending["n"]
+        for _, old, _ in self.pending["cow"]:
+            p._drop(old)
+        self.length = pos + n
+        self.committed_tokens += n
+        self.cache_appends += p.layers * n
+        for t in range(pos + 1, pos + n + 1):
+            self.score_cells += p.layers * p.HQ * (min(t, p.window) if p.window else t)
         self.pending = None
 
     def abort_token(self) -> None:
         if self.pending is None:
             raise OracleError(Status.BAD_STATE, "no token pending")
         p = self.pool
-        if self.pending["leased"] is not None:
-            page = self.table.pop()
-            assert page == self.pending["leased"]
+        for page in reversed(self.pending["leased"]):
+            assert self.table.pop() == page
             p._drop(page, front=True)
-        if self.pending["cow"] is not None:
-            idx, old, new = self.pending["cow"]
+        for idx, old, new in reversed(self.pending["cow"]):
             self.table[idx] = old
-            p.refs[old] += 1
             p._drop(new, front=True)
         self.pending = None
 

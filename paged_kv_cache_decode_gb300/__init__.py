@@ -36,7 +36,8 @@ from .binding import (  # noqa: F401
 __all__ = [
     "Pool", "Request", "PkvError", "pool_create", "pool_destroy", "request_create",
     "request_destroy", "request_fork", "lease_pages", "release_pages", "begin_token", "append_and_attend",
-    "commit_token", "abort_token", "paged_decode_attention", "paged_prefill", "workspace_size",
+    "commit_token", "abort_token", "begin_chunk", "prefill_chunk", "paged_decode_attention",
+    "paged_prefill", "workspace_size",
     "check_device_status", "PKV_F32", "PKV_BF16",
 ]
 
@@ -369,6 +370,27 @@ class Request:
             _dev(out, "out", torch.float32, qshape), _stream_ptr(stream)), "pkv_append_and_attend")
         return out
 
+    def begin_chunk(self, n: int) -> int:
+        """Open a chunk of n positions at the visible length; returns the first."""
+        pos = ctypes.c_int64()
+        check(lib.pkv_begin_chunk(self.handle, n, ctypes.byref(pos)), "pkv_begin_chunk")
+        return pos.value
+
+    def prefill_chunk(self, layer: int, q, k, v, out=None, stream=None):
+        """One layer of the pending chunk: q [n, query_heads, d_h], k, v [n, heads, d_h]
+        bf16; returns out [n, query_heads, d_h] fp32."""
+        p = self.pool
+        n = q.shape[0]
+        qshape = (n, p.query_heads, p.head_dim)
+        kshape = (n, p.heads, p.head_dim)
+        if out is None:
+            out = torch.empty(qshape, dtype=torch.float32, device=q.device)
+        check(lib.pkv_prefill_chunk(
+            self.handle, layer, _dev(q, "q", torch.bfloat16, qshape),
+            _dev(k, "k", torch.bfloat16, kshape), _dev(v, "v", torch.bfloat16, kshape),
+            _dev(out, "out", torch.float32, qshape), _stream_ptr(stream)), "pkv_prefill_chunk")
+        return out
+
     def commit_token(self) -> None:
         check(lib.pkv_commit_token(self.handle), "pkv_commit_token")
 
@@ -421,6 +443,14 @@ def begin_token(req: Request) -> int:
 
 def append_and_attend(req: Request, layer, q, k, v, out=None, stream=None):
     return req.append_and_attend(layer, q, k, v, out, stream)
+
+
+def begin_chunk(req: Request, n: int) -> int:
+    return req.begin_chunk(n)
+
+
+def prefill_chunk(req: Request, layer, q, k, v, out=None, stream=None):
+    return req.prefill_chunk(layer, q, k, v, out, stream)
 
 
 def commit_token(req: Request) -> None:

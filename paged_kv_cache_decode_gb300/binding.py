@@ -86,6 +86,8 @@ SIGNATURES = {
                                           _vp],
     "pkv_prefill_workspace_size": [_vp, _i, _i64, _P(_sz)],
     "pkv_paged_prefill": [_vp, _i, _i, _i64, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp],
+    "pkv_begin_chunk": [_vp, _i64, _P(_i64)],
+    "pkv_prefill_chunk": [_vp, _i, _vp, _vp, _vp, _vp, _vp],
     "pkv_pool_set_timing_events": [_vp, _vp, _vp],
     "pkv_check_device_status": [_vp, _P(_u32)],
     "pkv_last_error": [],

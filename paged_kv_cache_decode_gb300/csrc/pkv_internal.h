@@ -110,8 +110,10 @@ struct PrefillArgs {
     void* k_pages;           // this layer's pools, [pages][H][P][D]
     void* v_pages;
     int64_t n_pages;
-    const int32_t* cu_new;   // [B + 1] device
-    const int32_t* seq_lens; // [B] device, lengths after the chunk
+    const int32_t* cu_new;   // [B + 1] device; nullptr: one request, values below
+    const int32_t* seq_lens; // [B] device, lengths after the chunk; nullptr: single_t
+    int64_t single_n;        // one request without device arrays: its chunk length
+    int64_t single_t;        //   and its length after the chunk
     const int32_t* tables;   // [B][max_pages] device
     int max_pages;
     int64_t total_new;       // N, rows of q / k_new / v_new / out

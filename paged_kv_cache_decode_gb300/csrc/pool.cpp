@@ -89,9 +89,11 @@ struct pkv_request {
     std::vector<int32_t> table;        // logical page -> physical page
     int64_t length = 0;                // visible (committed) length
     bool pending = false;
-    int64_t position = 0;              // pending position
-    bool leased_by_begin = false;
-    std::vector<uint8_t> appended;     // per layer, for the pending token
+    int64_t position = 0;              // pending position (the first of a pending chunk)
+    int64_t pending_n = 0;             // positions pending: 1 (begin_token) or n (begin_chunk)
+    bool chunk = false;                // pending positions are a chunk (pkv_prefill_chunk)
+    int64_t leased_count = 0;          // pages the begin appended to the table (leased last)
+    std::vector<uint8_t> appended;     // per layer, for the pending token or chunk
     int appended_count = 0;
     pkv_counters counters{};
     int32_t* dev_table = nullptr;      // device copy, max_pages_per_request entries
@@ -100,13 +102,18 @@ struct pkv_request {
     size_t workspace_bytes = 0;
     int workspace_workers = 0;
     uint32_t epoch = 0;                // calls made on dev_workspace (lane-counter epochs)
-    // copy-on-write of the pending token: logical page cow_idx moved from the
-    // shared page cow_old to the private page cow_new; each layer's bytes are
-    // copied by that layer's append
-    bool cow = false;
-    int64_t cow_idx = 0;
-    int32_t cow_old = -1, cow_new = -1;
+    // copy-on-write of the pending positions: logical page idx moved from the
+    // shared page old_page to the private page new_page (leased in ascending
+    // idx, before any appended page); each layer's bytes are copied by that
+    // layer's append or prefill
+    struct CowPage {
+        int64_t idx;
+        int32_t old_page, new_page;
+    };
+    std::vector<CowPage> cow;
     std::vector<uint8_t> cow_copied;
+    void* dev_prefill_ws = nullptr;    // prefill scratch for one request's chunks
+    size_t prefill_ws_bytes = 0;
 };
 
 namespace {
@@ -440,12 +447,17 @@ int pkv_request_create(pkv_pool* p, pkv_request** out) {
             pkv::launch_workers(p->workers, 1, p->heads, pkv::attended_len(p->max_context, p->window));
         r->workspace_bytes =
             pkv::workspace_layout(1, p->heads, p->head_dim, r->workspace_workers, p->group).total;
+        if (p->tmaps && pkv::prefill_supported(p->dtype, p->head_dim, p->group))
+            r->prefill_ws_bytes = pkv::prefill_workspace_bytes(1, p->group, p->max_context);
         cudaError_t e = cudaMalloc(&r->dev_table, sizeof(int32_t) * (size_t)p->max_pages_per_request);
         if (e == cudaSuccess) e = cudaMalloc(&r->dev_workspace, r->workspace_bytes);
         if (e == cudaSuccess) e = cudaMemset(r->dev_workspace, 0, r->workspace_bytes);
+        if (e == cudaSuccess && r->prefill_ws_bytes)
+            e = cudaMalloc(&r->dev_prefill_ws, r->prefill_ws_bytes);
         if (e != cudaSuccess) {
             cudaFree(r->dev_table);
             cudaFree(r->dev_workspace);
+            cudaFree(r->dev_prefill_ws);
             delete r;
             cudaGetLastError();
             return fail(PKV_ERR_OUT_OF_MEMORY, "cudaMalloc for request: %s", cudaGetErrorString(e));
@@ -464,6 +476,7 @@ int pkv_request_destroy(pkv_request* r) {
     if (!p->host_only) {
         cudaFree(r->dev_table);
         cudaFree(r->dev_workspace);
+        cudaFree(r->dev_prefill_ws);
     }
     --p->live_requests;
     delete r;
@@ -519,39 +532,112 @@ int pkv_request_counters(const pkv_request* r, pkv_counters* out) {
     return ok();
 }
 
-int pkv_begin_token(pkv_request* r, int64_t* position) {
-    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+}  // extern "C"
+
+namespace {
+
+// Open n pending positions at the visible length: copy-on-write replacements
+// for the shared pages among those the positions write (ascending logical
+// index), then pages for logical indices the request does not hold yet, all
+// from the free list's front.  All or nothing.
+int begin_pending(pkv_request* r, int64_t n, bool chunk, int64_t* position) {
     pkv_pool* p = r->pool;
     if (r->pending) return fail(PKV_ERR_BAD_STATE, "a token is already pending");
-    if (r->length >= p->max_context)
-        return fail(PKV_ERR_CAPACITY_EXCEEDED, "request is at its maximum context %lld",
-                    (long long)p->max_context);
-    const int64_t idx = r->length / p->page_size;
-    const bool lease = idx >= (int64_t)r->table.size();
-    const bool cow = !lease && p->refs[(size_t)r->table[(size_t)idx]] > 1;
-    if ((lease || cow) && p->free_list.empty()) return fail(PKV_ERR_OUT_OF_PAGES, "no free page");
-    if (lease) {
-        mark_dirty(r, (int64_t)r->table.size());
-        r->table.push_back(lease_front(p));
-    }
-    r->cow = cow;
-    if (cow) {
-        // the page is shared with another request: write into a private copy
-        r->cow_idx = idx;
-        r->cow_old = r->table[(size_t)idx];
-        r->cow_new = lease_front(p);
-        --p->refs[(size_t)r->cow_old];
-        r->table[(size_t)idx] = r->cow_new;
+    if (r->length + n > p->max_context)
+        return fail(PKV_ERR_CAPACITY_EXCEEDED, "%lld + %lld positions pass the maximum context %lld",
+                    (long long)r->length, (long long)n, (long long)p->max_context);
+    const int64_t first = r->length / p->page_size;
+    const int64_t last = (r->length + n - 1) / p->page_size;
+    const int64_t held = (int64_t)r->table.size();
+    int64_t shared = 0;
+    for (int64_t idx = first; idx <= last && idx < held; ++idx)
+        if (p->refs[(size_t)r->table[(size_t)idx]] > 1) ++shared;
+    const int64_t fresh = last + 1 > held ? last + 1 - held : 0;
+    if (shared + fresh > (int64_t)p->free_list.size())
+        return fail(PKV_ERR_OUT_OF_PAGES, "%lld pages needed, %lld free", (long long)(shared + fresh),
+                    (long long)p->free_list.size());
+    r->cow.clear();
+    for (int64_t idx = first; idx <= last && idx < held; ++idx) {
+        const int32_t old = r->table[(size_t)idx];
+        if (p->refs[(size_t)old] <= 1) continue;
+        // the page is shared with another request: write into a private copy;
+        // the reference to the shared page is kept until commit
+        const int32_t page = lease_front(p);
+        r->table[(size_t)idx] = page;
+        r->cow.push_back({idx, old, page});
         mark_dirty(r, idx);
-        std::fill(r->cow_copied.begin(), r->cow_copied.end(), 0);
     }
+    if (fresh) mark_dirty(r, held);
+    for (int64_t i = 0; i < fresh; ++i) r->table.push_back(lease_front(p));
+    r->leased_count = fresh;
+    std::fill(r->cow_copied.begin(), r->cow_copied.end(), 0);
     r->pending = true;
     r->position = r->length;
-    r->leased_by_begin = lease;
+    r->pending_n = n;
+    r->chunk = chunk;
     std::fill(r->appended.begin(), r->appended.end(), 0);
     r->appended_count = 0;
     if (position) *position = r->position;
     return ok();
+}
+
+// Before a layer's first write for the pending positions: upload the changed
+// page-table entries and copy this layer's bytes of every shared page into its
+// private replacement.
+int prepare_layer_write(pkv_request* r, int layer, cudaStream_t s) {
+    pkv_pool* p = r->pool;
+    const int64_t n = (int64_t)r->table.size();
+    if (r->dev_dirty_from < n) {
+        cudaError_t e = cudaMemcpyAsync(r->dev_table + r->dev_dirty_from,
+                                        r->table.data() + r->dev_dirty_from,
+                                        sizeof(int32_t) * (size_t)(n - r->dev_dirty_from),
+                                        cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "page-table upload");
+        r->dev_dirty_from = n;
+    }
+    if (!r->cow.empty() && !r->cow_copied[(size_t)layer]) {
+        const size_t page_bytes = (size_t)p->page_size * p->heads * p->head_dim * elem_bytes(p->dtype);
+        char* kb = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)layer;
+        char* vb = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)layer;
+        for (const auto& c : r->cow) {
+            cudaError_t e = cudaMemcpyAsync(kb + page_bytes * (size_t)c.new_page,
+                                            kb + page_bytes * (size_t)c.old_page, page_bytes,
+                                            cudaMemcpyDeviceToDevice, s);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(vb + page_bytes * (size_t)c.new_page,
+                                    vb + page_bytes * (size_t)c.old_page, page_bytes,
+                                    cudaMemcpyDeviceToDevice, s);
+            if (e != cudaSuccess) return cuda_fail(e, "copy-on-write page copy");
+        }
+        r->cow_copied[(size_t)layer] = 1;
+    }
+    return PKV_OK;
+}
+
+// Sum over t = t0+1 .. t0+n of min(t, window) (window 0: of t).
+int64_t attended_sum(int64_t t0, int64_t n, int64_t window) {
+    const int64_t a = t0 + 1, b = t0 + n;
+    if (window <= 0 || b <= window) return (a + b) * n / 2;
+    if (a > window) return window * n;
+    return (a + window) * (window - a + 1) / 2 + window * (b - window);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_begin_token(pkv_request* r, int64_t* position) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    return begin_pending(r, 1, false, position);
+}
+
+int pkv_begin_chunk(pkv_request* r, int64_t n, int64_t* position) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    if (n < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "a chunk holds at least one token");
+    pkv_pool* p = r->pool;
+    if (!p->host_only && !(p->tmaps && pkv::prefill_supported(p->dtype, p->head_dim, p->group)))
+        return fail(PKV_ERR_UNSUPPORTED, "prefill needs bf16 pools of head_dim 64 or 128");
+    return begin_pending(r, n, true, position);
 }
 
 int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void* k, const void* v,
@@ -563,34 +649,13 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
         return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
+    if (r->chunk) return fail(PKV_ERR_BAD_STATE, "a chunk is pending (pkv_prefill_chunk)");
     if (r->appended[(size_t)layer]) return fail(PKV_ERR_BAD_STATE, "layer %d already ran", layer);
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t n = (int64_t)r->table.size();
-    if (r->dev_dirty_from < n) {
-        cudaError_t e = cudaMemcpyAsync(r->dev_table + r->dev_dirty_from,
-                                        r->table.data() + r->dev_dirty_from,
-                                        sizeof(int32_t) * (size_t)(n - r->dev_dirty_from),
-                                        cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "page-table upload");
-        r->dev_dirty_from = n;
-    }
-    if (r->cow && !r->cow_copied[(size_t)layer]) {
-        // this layer's bytes of the shared page go to the private page first
-        const size_t page_bytes = (size_t)p->page_size * p->heads * p->head_dim * elem_bytes(p->dtype);
-        char* kb = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)layer;
-        char* vb = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)layer;
-        cudaError_t e = cudaMemcpyAsync(kb + page_bytes * (size_t)r->cow_new,
-                                        kb + page_bytes * (size_t)r->cow_old, page_bytes,
-                                        cudaMemcpyDeviceToDevice, s);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(vb + page_bytes * (size_t)r->cow_new,
-                                vb + page_bytes * (size_t)r->cow_old, page_bytes,
-                                cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "copy-on-write page copy");
-        r->cow_copied[(size_t)layer] = 1;
-    }
+    rc = prepare_layer_write(r, layer, s);
+    if (rc != PKV_OK) return rc;
     pkv::DecodeArgs a{};
     a.dtype = p->dtype;
     a.B = 1;
@@ -636,21 +701,74 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     return ok();
 }
 
+int pkv_prefill_chunk(pkv_request* r, int layer, const void* q, const void* k, const void* v,
+                      float* out, void* stream) {
+    if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
+    pkv_pool* p = r->pool;
+    if (!q || !k || !v || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL tensor pointer");
+    if (layer < 0 || layer >= p->layers)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    if (!r->pending || !r->chunk) return fail(PKV_ERR_BAD_STATE, "no chunk pending");
+    if (r->appended[(size_t)layer]) return fail(PKV_ERR_BAD_STATE, "layer %d already ran", layer);
+    int rc = check_device(p);
+    if (rc != PKV_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = prepare_layer_write(r, layer, s);
+    if (rc != PKV_OK) return rc;
+    pkv::PrefillArgs a{};
+    a.B = 1;
+    a.H = p->heads;
+    a.G = p->group;
+    a.D = p->head_dim;
+    a.P = p->page_size;
+    a.window = p->window;
+    a.q = q;
+    a.k_new = k;
+    a.v_new = v;
+    void *kp, *vp;
+    pkv_pool_kv_ptr(p, layer, &kp, &vp);
+    a.k_pages = kp;
+    a.v_pages = vp;
+    a.n_pages = p->pages;
+    a.cu_new = nullptr;
+    a.seq_lens = nullptr;
+    a.single_n = r->pending_n;
+    a.single_t = r->position + r->pending_n;
+    a.tables = r->dev_table;
+    a.max_pages = (int)p->max_pages_per_request;
+    a.total_new = r->pending_n;
+    a.out = out;
+    a.workspace = r->dev_prefill_ws;
+    a.dev_error = p->dev_error;
+    a.ev_before = p->ev_before;
+    a.ev_after = p->ev_after;
+    a.tmap_k = &p->tmap_k[(size_t)layer];
+    a.tmap_v = &p->tmap_v[(size_t)layer];
+    cudaError_t e = pkv::launch_prefill(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    r->appended[(size_t)layer] = 1;
+    ++r->appended_count;
+    return ok();
+}
+
 int pkv_commit_token(pkv_request* r) {
     if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
     pkv_pool* p = r->pool;
     if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
     if (r->appended_count != p->layers)
         return fail(PKV_ERR_BAD_STATE, "%d of %d layers appended", r->appended_count, p->layers);
-    const int64_t t = r->position + 1;
-    r->length = t;
-    r->counters.committed_tokens += 1;
-    r->counters.cache_appends += p->layers;
+    const int64_t n = r->pending_n;
+    for (const auto& c : r->cow) drop_page(p, c.old_page, false);
+    r->counters.committed_tokens += n;
+    r->counters.cache_appends += (int64_t)p->layers * n;
     r->counters.score_cells +=
-        (int64_t)p->layers * p->query_heads * (p->window > 0 && p->window < t ? p->window : t);
+        (int64_t)p->layers * p->query_heads * attended_sum(r->position, n, p->window);
+    r->length = r->position + n;
     r->pending = false;
-    r->leased_by_begin = false;
-    r->cow = false;
+    r->chunk = false;
+    r->leased_count = 0;
+    r->cow.clear();
     return ok();
 }
 
@@ -658,21 +776,23 @@ int pkv_abort_token(pkv_request* r) {
     if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
     if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
     pkv_pool* p = r->pool;
-    if (r->leased_by_begin) {
+    // back to the free list's front, last leased first, so the pool is exactly
+    // as before the begin
+    for (int64_t i = 0; i < r->leased_count; ++i) {
         const int32_t pg = r->table.back();
         r->table.pop_back();
         drop_page(p, pg, true);
-        mark_dirty(r, (int64_t)r->table.size());
     }
-    if (r->cow) {
-        r->table[(size_t)r->cow_idx] = r->cow_old;
-        ++p->refs[(size_t)r->cow_old];
-        drop_page(p, r->cow_new, true);
-        mark_dirty(r, r->cow_idx);
+    if (r->leased_count) mark_dirty(r, (int64_t)r->table.size());
+    for (auto it = r->cow.rbegin(); it != r->cow.rend(); ++it) {
+        r->table[(size_t)it->idx] = it->old_page;
+        drop_page(p, it->new_page, true);
+        mark_dirty(r, it->idx);
     }
     r->pending = false;
-    r->leased_by_begin = false;
-    r->cow = false;
+    r->chunk = false;
+    r->leased_count = 0;
+    r->cow.clear();
     return ok();
 }
 

@@ -103,8 +103,10 @@ struct PfParams {
     const __nv_bfloat16* v_new;
     __nv_bfloat16* k_pages;        // [pages][H][P][D]
     __nv_bfloat16* v_pages;
-    const int32_t* cu_new;         // [B + 1]
-    const int32_t* seq_lens;       // [B]
+    const int32_t* cu_new;         // [B + 1]; nullptr: one request of single_n rows
+    const int32_t* seq_lens;       // [B]; nullptr: single_t
+    int single_n;
+    int64_t single_t;
     const int32_t* tables;         // [B][max_pages]
     float* out;                    // [N][H*G][D]
     int2* items;                   // query tiles (request, tile), in launch order
@@ -260,6 +262,15 @@ __device__ __forceinline__ uint32_t sw_off(int r, int u) {
     return (uint32_t)((u >> 3) * (kRows * 128) + r * 128 + (((u & 7) ^ (r & 7)) << 4));
 }
 
+// Row offset of request b's chunk and its length after the chunk.
+__device__ __forceinline__ int cu_at(const PfParams& p, int b) {
+    return p.cu_new ? p.cu_new[b] : (b == 0 ? 0 : p.single_n);
+}
+
+__device__ __forceinline__ int64_t seq_len_at(const PfParams& p, int b) {
+    return p.seq_lens ? (int64_t)p.seq_lens[b] : p.single_t;
+}
+
 // ------------------------------------------------------------------ plan --
 
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfParams p) {
@@ -268,9 +279,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPara
     const int T = 2 * kRows / p.G;                // tokens of one work unit (two query tiles)
     int tiles = 0;
     if (b < p.B) {
-        const int c0 = p.cu_new[b], c1 = p.cu_new[b + 1];
+        const int c0 = cu_at(p, b), c1 = cu_at(p, b + 1);
         const int64_t n = (int64_t)c1 - c0;
-        const int64_t t = p.seq_lens[b];
+        const int64_t t = seq_len_at(p, b);
         const bool ok = c0 >= 0 && n >= 0 && c1 <= p.total_new && t - n >= 0 &&
                         t <= (int64_t)p.max_pages * p.P;
         if (!ok) atomicOr(p.dev_error, PKV_DEVERR_SEQ_LEN);
@@ -320,13 +331,13 @@ __global__ void __launch_bounds__(256) prefill_append_kernel(const PfParams p) {
         int lo = 0, hi = p.B;                       // last request with cu_new[b] <= x
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (p.cu_new[mid] <= x) lo = mid;
+            if (cu_at(p, mid) <= x) lo = mid;
             else hi = mid;
         }
         const int b = lo;
-        const int c0 = p.cu_new[b], c1 = p.cu_new[b + 1];
+        const int c0 = cu_at(p, b), c1 = cu_at(p, b + 1);
         if (x < c0 || x >= c1) continue;
-        const int64_t t = p.seq_lens[b];
+        const int64_t t = seq_len_at(p, b);
         const int64_t L0 = t - (c1 - c0);
         if (L0 < 0 || t > (int64_t)p.max_pages * p.P) continue;      // the plan reports it
         const int64_t pos = L0 + (x - c0);
@@ -357,9 +368,9 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
     const int2 it = p.items[item];
     const int b = it.x, unit = it.y;
     const int G = p.G, T = kRows / G;                         // tokens per query tile
-    const int c0 = p.cu_new[b];
-    const int n = p.cu_new[b + 1] - c0;
-    const int64_t t_b = p.seq_lens[b];
+    const int c0 = cu_at(p, b);
+    const int n = cu_at(p, b + 1) - c0;
+    const int64_t t_b = seq_len_at(p, b);
     const int64_t L0 = t_b - n;
     const int i0 = unit * 2 * T;                              // tile A: tokens i0 .. i0+T-1
     const int i_end = min(n, i0 + 2 * T);                     // the unit's tokens end here
@@ -773,6 +784,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     p.v_pages = static_cast<__nv_bfloat16*>(a.v_pages);
     p.cu_new = a.cu_new;
     p.seq_lens = a.seq_lens;
+    p.single_n = (int)a.single_n;
+    p.single_t = a.single_t;
     p.tables = a.tables;
     p.out = a.out;
     p.n_items = static_cast<int*>(a.workspace);

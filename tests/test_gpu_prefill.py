@@ -180,3 +180,148 @@ def test_prefill_bad_lengths_and_pages_set_error_bits():
         assert _normwise(got, run.oracle_out(0)) <= PREFILL_RTOL
     finally:
         run.close()
+
+
+# ------------------------------------------------------ request chunks --
+
+def _chunk_inputs(seed, layer, HQ, H, D, pos, n, req=0):
+    """Chunk rows pos .. pos+n-1 of one request's streams: q [n,HQ,D], k, v [n,H,D] (bf16 bits)."""
+    import synth
+    from synth import KHIST, VHIST, Q, BF16
+    q = np.stack([synth.rows(seed, Q, layer, req, qh, pos, n, D, BF16) for qh in range(HQ)], axis=1)
+    k = np.stack([synth.rows(seed, KHIST, layer, req, h, pos, n, D, BF16) for h in range(H)], axis=1)
+    v = np.stack([synth.rows(seed, VHIST, layer, req, h, pos, n, D, BF16) for h in range(H)], axis=1)
+    return q, k, v
+
+
+def _run_chunk(req, oreq, seed, layers, HQ, H, D, n, rid=0, only_layers=None):
+    import synth
+    from synth.device import to_device
+    pos = req.begin_chunk(n)
+    assert pos == oreq.begin_chunk(n)
+    outs = []
+    for layer in (range(layers) if only_layers is None else only_layers):
+        q, k, v = _chunk_inputs(seed, layer, HQ, H, D, pos, n, rid)
+        out = req.prefill_chunk(layer, to_device(q), to_device(k), to_device(v)).cpu().numpy()
+        ref = oreq.prefill_chunk(layer, synth.bf16_to_f32(q), k, v)
+        assert _normwise(out, ref) <= PREFILL_RTOL
+        outs.append(out)
+    return outs
+
+
+def _pages_equal(pool, opool, pages, layers):
+    for layer in range(layers):
+        kp, vp = pool.kv_pages(layer)
+        for pg in pages:
+            k = kp[pg].cpu().view(torch.int16).numpy().view(np.uint16)
+            v = vp[pg].cpu().view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(k, opool.k[layer, pg]) and np.array_equal(v, opool.v[layer, pg])
+
+
+def test_request_chunks_then_a_token_match_the_oracle_model():
+    import synth
+    from oracle.model import OraclePool
+    from synth import KHIST, VHIST, Q, F32, BF16
+    from synth.device import to_device
+    layers, H, HQ, D, seed = 2, 2, 4, 128, 5
+    pool = pkv.Pool(layers, 64, H, D, 16, "bf16", 1024, seed, query_heads=HQ)
+    opool = OraclePool(layers, 64, H, D, 16, BF16, max_context=1024, seed=seed, query_heads=HQ)
+    req, oreq = pool.request(), opool.request()
+    try:
+        for n in (70, 45, 1, 130):
+            _run_chunk(req, oreq, seed, layers, HQ, H, D, n)
+            req.commit_token()
+            oreq.commit_token()
+            assert req.page_table() == oreq.table and req.length == oreq.length
+        c = req.counters()
+        assert (c["committed_tokens"], c["cache_appends"], c["score_cells"]) == (
+            oreq.committed_tokens, oreq.cache_appends, oreq.score_cells)
+        # a decode token after the chunks reads their rows
+        pos = req.begin_token()
+        assert pos == oreq.begin_token() == 246
+        for layer in range(layers):
+            q = synth.lane_rows(seed, Q, layer, 0, HQ, pos, D, F32)
+            k = synth.lane_rows(seed, KHIST, layer, 0, H, pos, D, BF16)
+            v = synth.lane_rows(seed, VHIST, layer, 0, H, pos, D, BF16)
+            out = req.append_and_attend(layer, to_device(q), to_device(k), to_device(v)).cpu().numpy()
+            ref = oreq.append_and_attend(layer, q, k, v)
+            assert _normwise(out, ref) <= 5e-3
+        req.commit_token()
+        oreq.commit_token()
+        c = req.counters()
+        assert (c["committed_tokens"], c["cache_appends"], c["score_cells"]) == (
+            oreq.committed_tokens, oreq.cache_appends, oreq.score_cells)
+        torch.cuda.synchronize()
+        assert pool.check_device_status() == 0
+        _pages_equal(pool, opool, req.page_table(), layers)
+    finally:
+        req.close()
+        pool.close()
+
+
+def test_chunk_abort_then_retry_matches_no_abort():
+    from oracle.model import OraclePool
+    from synth import BF16
+    layers, H, HQ, D, seed = 2, 1, 8, 64, 9
+    results = []
+    for abort in (False, True):
+        pool = pkv.Pool(layers, 32, H, D, 16, "bf16", 512, seed, query_heads=HQ)
+        opool = OraclePool(layers, 32, H, D, 16, BF16, max_context=512, seed=seed, query_heads=HQ)
+        req, oreq = pool.request(), opool.request()
+        try:
+            _run_chunk(req, oreq, seed, layers, HQ, H, D, 50)
+            req.commit_token()
+            oreq.commit_token()
+            if abort:
+                free0, table0 = pool.free_list(), req.page_table()
+                _run_chunk(req, oreq, seed, layers, HQ, H, D, 40, only_layers=[0])
+                req.abort_token()
+                oreq.abort_token()
+                assert pool.free_list() == free0 and req.page_table() == table0 and req.length == 50
+            outs = _run_chunk(req, oreq, seed, layers, HQ, H, D, 40)
+            req.commit_token()
+            oreq.commit_token()
+            results.append((outs, req.page_table(), pool.free_list()))
+        finally:
+            req.close()
+            pool.close()
+    (o0, t0, f0), (o1, t1, f1) = results
+    assert t0 == t1 and f0 == f1
+    assert all(np.array_equal(a, b) for a, b in zip(o0, o1))
+
+
+def test_chunks_over_forked_pages_copy_on_write():
+    from oracle.model import OraclePool
+    from synth import BF16
+    layers, H, HQ, D, seed = 1, 2, 4, 128, 12
+    pool = pkv.Pool(layers, 40, H, D, 16, "bf16", 640, seed, query_heads=HQ)
+    opool = OraclePool(layers, 40, H, D, 16, BF16, max_context=640, seed=seed, query_heads=HQ)
+    parent, oparent = pool.request(), opool.request()
+    child = ochild = None
+    try:
+        _run_chunk(parent, oparent, seed, layers, HQ, H, D, 40)          # pages 0, 1, 2 (partial)
+        parent.commit_token()
+        oparent.commit_token()
+        child, ochild = parent.fork(), oparent.fork()
+        shared = parent.page_table()
+        # the child continues in the shared partial page: it gets a private copy of page 2
+        _run_chunk(child, ochild, seed, layers, HQ, H, D, 30, rid=1)
+        child.commit_token()
+        ochild.commit_token()
+        assert child.page_table()[:2] == shared[:2] and child.page_table()[2] != shared[2]
+        # the parent writes page 2 in place now that only it holds it
+        _run_chunk(parent, oparent, seed, layers, HQ, H, D, 20)
+        parent.commit_token()
+        oparent.commit_token()
+        assert parent.page_table()[2] == shared[2]
+        for r, o in ((parent, oparent), (child, ochild)):
+            assert r.page_table() == o.table and r.length == o.length
+        assert pool.free_list() == list(opool.free)
+        assert [pool.page_refs(i) for i in range(40)] == opool.refs
+        torch.cuda.synchronize()
+        _pages_equal(pool, opool, sorted(set(parent.page_table() + child.page_table())), layers)
+    finally:
+        if child is not None:
+            child.close()
+        parent.close()
+        pool.close()

@@ -236,3 +236,117 @@ def test_random_sequences_with_forks_match_oracle():
             assert r.page_table() == o.table
         assert p.free_list() == list(op_.free)
         assert _refs(p, pages) == op_.refs
+
+
+# ------------------------------------------------------------------ chunks --
+
+def test_chunk_over_shared_pages_copies_each_and_abort_restores():
+    P, pages = 16, 24
+    with host_pool(pages=pages, max_context=16 * 10, seed=8) as p:
+        op_ = OraclePool(1, pages, 2, 4, P, F32, max_context=16 * 10, seed=8, storage=False)
+        r, o = p.request(), op_.request()
+        r.lease_pages(4)
+        o.lease_pages(4)
+        c, oc = r.fork(), o.fork()
+        # the child writes positions 0..40: pages 0, 1, 2 are shared -> three private copies
+        assert c.begin_chunk(41) == oc.begin_chunk(41) == 0
+        assert c.page_table() == oc.table
+        assert sum(a != b for a, b in zip(c.page_table(), r.page_table())) == 3
+        assert _refs(p, pages) == op_.refs and p.free_list() == list(op_.free)
+        c.abort_token()
+        oc.abort_token()
+        assert c.page_table() == r.page_table() == oc.table
+        assert _refs(p, pages) == op_.refs and p.free_list() == list(op_.free)
+        # a chunk past the held pages leases the rest, in logical order
+        assert c.begin_chunk(16 * 6) == oc.begin_chunk(16 * 6) == 0
+        assert c.page_table() == oc.table and len(c.page_table()) == 6
+        assert p.free_list() == list(op_.free)
+
+
+def test_chunk_rejections_change_nothing():
+    with host_pool(pages=5, max_context=64, seed=2) as p:
+        r = p.request()
+        snap = lambda: (r.page_table(), r.length, p.free_list())
+        s0 = snap()
+        for n, st in [(0, pkv.PKV_ERR_INVALID_ARGUMENT), (65, pkv.PKV_ERR_CAPACITY_EXCEEDED)]:
+            with pytest.raises(pkv.PkvError) as e:
+                r.begin_chunk(n)
+            assert e.value.status == st and snap() == s0
+        other = p.request()
+        other.lease_pages(3)
+        with pytest.raises(pkv.PkvError) as e:          # 3 pages needed, 2 free
+            r.begin_chunk(40)
+        assert e.value.status == pkv.PKV_ERR_OUT_OF_PAGES and r.page_table() == []
+        assert r.begin_chunk(20) == 0
+        for fn in (r.begin_token, lambda: r.begin_chunk(1), r.release_pages, r.fork):
+            with pytest.raises(pkv.PkvError) as e:
+                fn()
+            assert e.value.status == pkv.PKV_ERR_BAD_STATE
+        import torch
+        z = torch.zeros(2, 4)
+        with pytest.raises(ValueError):
+            r.append_and_attend(0, z, z, z)
+        r.abort_token()
+        assert r.page_table() == [] and r.length == 0
+
+
+def test_random_sequences_with_chunks_match_oracle():
+    rng = np.random.default_rng(13)
+    P, pages, maxc = 16, 40, 16 * 12
+    with host_pool(pages=pages, max_context=maxc, seed=6) as p:
+        op_ = OraclePool(1, pages, 2, 4, P, F32, max_context=maxc, seed=6, storage=False)
+        reqs, oreqs = [p.request()], [op_.request()]
+        for step in range(3000):
+            i = int(rng.integers(0, len(reqs)))
+            r, o = reqs[i], oreqs[i]
+            kind = int(rng.integers(0, 8))
+            if kind == 6 and len(reqs) < 8:
+                a = b = 0
+                try:
+                    c = r.fork()
+                except pkv.PkvError as e:
+                    a = e.status
+                try:
+                    oc = o.fork()
+                except OracleError as e:
+                    b = e.status
+                assert a == b
+                if a == 0:
+                    reqs.append(c)
+                    oreqs.append(oc)
+                continue
+            if kind == 7 and len(reqs) > 1:
+                r.close()
+                o.destroy()
+                reqs.pop(i)
+                oreqs.pop(i)
+                continue
+            op = [("lease_pages", (int(rng.integers(0, 4)),)), ("release_pages", ()),
+                  ("begin_token", ()), ("abort_token", ()), ("begin_chunk", (int(rng.integers(1, 70)),)),
+                  ("abort_token", ()), ("begin_chunk", (int(rng.integers(1, 5)),))][kind % 7]
+            a, b = _apply(op, r, o)
+            assert a == b, (step, op, a, b)
+            assert r.page_table() == o.table
+        assert p.free_list() == list(op_.free)
+        assert _refs(p, pages) == op_.refs
+
+
+def test_sharer_leaving_during_a_pending_copy_on_write_frees_nothing_held():
+    """The child writes into a shared page (copy-on-write) and the parent is destroyed
+    while that token is pending: the shared page stays held by the child, and the
+    abort puts it back in the child's table (commit, which frees it, runs on the GPU)."""
+    with host_pool(pages=6, max_context=64, seed=3) as p:
+        op_ = OraclePool(1, 6, 2, 4, 16, F32, max_context=64, seed=3, storage=False)
+        r, o = p.request(), op_.request()
+        r.lease_pages(2)
+        o.lease_pages(2)
+        c, oc = r.fork(), o.fork()
+        shared = c.page_table()[0]
+        assert c.begin_token() == oc.begin_token() == 0
+        r.close()
+        o.destroy()
+        assert shared not in p.free_list() and p.page_refs(shared) == op_.refs[shared] == 1
+        c.abort_token()
+        oc.abort_token()
+        assert c.page_table()[0] == oc.table[0] == shared and shared not in p.free_list()
+        assert p.free_list() == list(op_.free) and _refs(p, 6) == op_.refs
