@@ -299,10 +299,23 @@ def run_gpu(args):
     w = make_workload(args.workload, rank, args.requests)
     pool, reqs, host, dev, ws, out, max_seq_len = setup_device(w, torch, args.cuda_cores)
     stream = torch.cuda.current_stream()
+    shared = 0 if args.plain else int(w.shared_prefix)
+    if shared:
+        import ctypes
+        import paged_kv_cache_decode_gb300 as pkv
+        n = ctypes.c_size_t()
+        pkv.check(pkv.lib.pkv_workspace_size_shared(pool.handle, w.B, max_seq_len, shared,
+                                                    ctypes.byref(n)), "pkv_workspace_size_shared")
+        ws = torch.empty(max(n.value, 16), dtype=torch.uint8, device="cuda")
 
     def step():
-        pool.paged_decode_attention(0, dev["q"], dev["k"], dev["v"], dev["tables"], dev["lens"],
-                                    max_seq_len, out=out, workspace=ws)
+        if shared:
+            pool.paged_decode_attention_shared(0, dev["q"], dev["k"], dev["v"], dev["tables"],
+                                               dev["lens"], max_seq_len, shared, out=out,
+                                               workspace=ws)
+        else:
+            pool.paged_decode_attention(0, dev["q"], dev["k"], dev["v"], dev["tables"], dev["lens"],
+                                        max_seq_len, out=out, workspace=ws)
 
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3)
@@ -377,6 +390,8 @@ def run_gpu(args):
 
     alg = algorithmic_bytes(w)
     kernel_name = pool.kernel_name()
+    if shared:
+        kernel_name = f"shared_prefix_kernel<{w.D}> + {kernel_name} + combine_kernel"
     line = None
     if rank == 0:
         peak, peak_kind = measured_peak_hbm()
@@ -408,9 +423,13 @@ def run_gpu(args):
             "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": K * 2,
+            "gpu_launches": K * (4 if shared else 2),
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
+        if shared:
+            line["config"]["path"] = (f"shared-prefix call: the {shared}-token prompt once per KV "
+                                      "head on the tensor cores, each request's own positions by "
+                                      "the split kernel, partials merged")
     pool.close()
     return line, w
 
@@ -905,6 +924,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="CUDA-core kernel even where the tensor-core kernel applies")
+    ap.add_argument("--plain", action="store_true",
+                    help="shared-prompt workload through the plain batched call")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests (small profiling captures)")
     return ap.parse_args(argv)

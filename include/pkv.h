@@ -84,6 +84,8 @@ typedef enum pkv_dtype {
 #define PKV_DEVERR_SEQ_LEN 1u   /* a seq_len < 1, > max_seq_len, or needing > max_pages pages */
 #define PKV_DEVERR_PAGE_ID 2u   /* a page-table entry outside [0, pages) */
 #define PKV_DEVERR_TIMEOUT 4u   /* a bounded wait for an async copy ran out */
+#define PKV_DEVERR_SHARED 8u    /* a request's page table differs from request 0's within the
+                                   declared shared prefix (pkv_paged_decode_attention_shared) */
 
 /* Work counters of one request ([CACHED-BIND] work counters; [CACHED-CELLS]).
  * They advance only when a token commits; reset (release) zeroes them. */
@@ -355,6 +357,44 @@ int pkv_paged_decode_attention(pkv_pool* pool, int layer, int batch, const float
                                const void* k_new, const void* v_new, const int32_t* page_tables,
                                int max_pages, const int32_t* seq_lens, int64_t max_seq_len,
                                float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Device scratch bytes that pkv_paged_decode_attention_shared needs (see there);
+ * equal to pkv_workspace_size when shared_len is 0.
+ */
+int pkv_workspace_size_shared(const pkv_pool* pool, int batch, int64_t max_seq_len,
+                              int64_t shared_len, size_t* bytes);
+
+/*
+ * pkv_paged_decode_attention for a batch whose requests share a prefix: the
+ * first shared_len positions of every request map to the same physical pages
+ * (request 0's table entries 0 .. shared_len/page_size - 1), as after
+ * pkv_request_fork of one prompt ([SERVE-SCOPE]: page sharing between
+ * requests).  Same arguments, layout and results as pkv_paged_decode_attention;
+ * the shared pages are read once per KV head instead of once per request.
+ * The softmax over all t_b keys splits exactly into the shared keys and the
+ * request's own keys and is merged back:
+ *   out = (2^(m1-M) o1 + 2^(m2-M) o2) / (2^(m1-M) l1 + 2^(m2-M) l2),
+ * (m, l, o) being each part's maximum, sum and unnormalised output.  The shared
+ * part runs on the tensor cores with q and the weights split into bf16 hi + lo
+ * (fp32-level products); the rest is the batched decode path.
+ *   shared_len  multiple of page_size, 0 <= shared_len < max_seq_len; every
+ *               request needs t_b > shared_len (its new row is its own); 0 is
+ *               pkv_paged_decode_attention
+ *   workspace   >= pkv_workspace_size_shared bytes
+ * Pools: bf16, head_dim 64 or 128, query_heads / kv_heads dividing 128 (else
+ * PKV_ERR_UNSUPPORTED).  A table that differs from request 0's within the
+ * prefix sets PKV_DEVERR_SHARED, a t_b <= shared_len sets PKV_DEVERR_SEQ_LEN
+ * (rows of the affected requests unspecified).  Enqueues four kernels on
+ * `stream` (plan, prefix, split over each request's own positions, and a merge
+ * of the partials) and returns without waiting.
+ */
+int pkv_paged_decode_attention_shared(pkv_pool* pool, int layer, int batch, const float* q,
+                                      const void* k_new, const void* v_new,
+                                      const int32_t* page_tables, int max_pages,
+                                      const int32_t* seq_lens, int64_t max_seq_len,
+                                      int64_t shared_len, float* out, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of the fixed device array that pkv_paged_decode_attention_static uses

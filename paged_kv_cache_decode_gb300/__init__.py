@@ -30,13 +30,14 @@ from .binding import (  # noqa: F401
     PKV_ERR_BAD_STATE, PKV_ERR_OUT_OF_MEMORY, PKV_ERR_CUDA, PKV_ERR_DEVICE_CHECK,
     PKV_ERR_NO_STORAGE, PKV_ERR_UNSUPPORTED, PKV_F32, PKV_BF16, PKV_POOL_HOST_ONLY,
     PKV_POOL_CUDA_CORES,
-    PKV_DEVERR_SEQ_LEN, PKV_DEVERR_PAGE_ID, PKV_DEVERR_TIMEOUT,
+    PKV_DEVERR_SEQ_LEN, PKV_DEVERR_PAGE_ID, PKV_DEVERR_TIMEOUT, PKV_DEVERR_SHARED,
 )
 
 __all__ = [
     "Pool", "Request", "PkvError", "pool_create", "pool_destroy", "request_create",
     "request_destroy", "request_fork", "lease_pages", "release_pages", "begin_token", "append_and_attend",
     "commit_token", "abort_token", "begin_chunk", "prefill_chunk", "paged_decode_attention",
+    "paged_decode_attention_shared",
     "paged_prefill", "workspace_size",
     "check_device_status", "PKV_F32", "PKV_BF16",
 ]
@@ -217,6 +218,37 @@ class Pool:
             _dev(out, "out", torch.float32, (B, HQ, D)),
             _dev(workspace, "workspace", torch.uint8, None), workspace.numel(),
             _stream_ptr(stream)), "pkv_paged_decode_attention")
+        return out
+
+    def paged_decode_attention_shared(self, layer: int, q, k_new, v_new, page_tables, seq_lens,
+                                      max_seq_len: int, shared_len: int, out=None, workspace=None,
+                                      stream=None):
+        """paged_decode_attention for a batch whose first shared_len positions share
+        request 0's pages (read once per KV head)."""
+        B = q.shape[0]
+        H, HQ, D = self.heads, self.query_heads, self.head_dim
+        if out is None:
+            out = torch.empty((B, HQ, D), dtype=torch.float32, device=q.device)
+        if workspace is None:
+            key = ("shared", B, max_seq_len, shared_len)
+            if key not in self._ws:
+                n = ctypes.c_size_t()
+                check(lib.pkv_workspace_size_shared(self.handle, B, int(max_seq_len), int(shared_len),
+                                                    ctypes.byref(n)), "pkv_workspace_size_shared")
+                self._ws[key] = torch.empty(max(n.value, 16), dtype=torch.uint8, device=q.device)
+            workspace = self._ws[key]
+        if page_tables.dim() != 2 or page_tables.shape[0] != B:
+            raise ValueError("page_tables must be [batch, max_pages]")
+        check(lib.pkv_paged_decode_attention_shared(
+            self.handle, layer, B,
+            _dev(q, "q", torch.float32, (B, HQ, D)),
+            _dev(k_new, "k_new", self.torch_dtype, (B, H, D)),
+            _dev(v_new, "v_new", self.torch_dtype, (B, H, D)),
+            _dev(page_tables, "page_tables", torch.int32, None), page_tables.shape[1],
+            _dev(seq_lens, "seq_lens", torch.int32, (B,)), int(max_seq_len), int(shared_len),
+            _dev(out, "out", torch.float32, (B, HQ, D)),
+            _dev(workspace, "workspace", torch.uint8, None), workspace.numel(),
+            _stream_ptr(stream)), "pkv_paged_decode_attention_shared")
         return out
 
     def prefill_workspace_size(self, batch: int, total_new: int) -> int:
@@ -469,6 +501,12 @@ def paged_decode_attention(pool: Pool, layer, q, k_new, v_new, page_tables, seq_
                            out=None, workspace=None, stream=None):
     return pool.paged_decode_attention(layer, q, k_new, v_new, page_tables, seq_lens, max_seq_len,
                                        out, workspace, stream)
+
+
+def paged_decode_attention_shared(pool: Pool, layer, q, k_new, v_new, page_tables, seq_lens,
+                                  max_seq_len, shared_len, out=None, workspace=None, stream=None):
+    return pool.paged_decode_attention_shared(layer, q, k_new, v_new, page_tables, seq_lens,
+                                              max_seq_len, shared_len, out, workspace, stream)
 
 
 def paged_prefill(pool: Pool, layer, q, k_new, v_new, cu_new, page_tables, seq_lens, out=None,

@@ -33,6 +33,7 @@ PKV_POOL_CUDA_CORES = 2
 PKV_DEVERR_SEQ_LEN = 1
 PKV_DEVERR_PAGE_ID = 2
 PKV_DEVERR_TIMEOUT = 4
+PKV_DEVERR_SHARED = 8
 
 LIB_PATH = _build.LIB
 
@@ -88,6 +89,9 @@ SIGNATURES = {
     "pkv_paged_prefill": [_vp, _i, _i, _i64, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp],
     "pkv_begin_chunk": [_vp, _i64, _P(_i64)],
     "pkv_prefill_chunk": [_vp, _i, _vp, _vp, _vp, _vp, _vp],
+    "pkv_workspace_size_shared": [_vp, _i, _i64, _i64, _P(_sz)],
+    "pkv_paged_decode_attention_shared": [_vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i64, _i64,
+                                          _vp, _vp, _sz, _vp],
     "pkv_pool_set_timing_events": [_vp, _vp, _vp],
     "pkv_check_device_status": [_vp, _P(_u32)],
     "pkv_last_error": [],

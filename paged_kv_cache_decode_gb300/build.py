@@ -19,8 +19,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 
-SOURCES = ["decode.cu", "prefill.cu", "pool.cpp", "static_scratch.cu"]
+SOURCES = ["decode.cu", "prefill.cu", "shared_prefix.cu", "pool.cpp", "static_scratch.cu"]
 HEADERS = [os.path.join(CSRC, "pkv_internal.h"), os.path.join(CSRC, "ptx.cuh"),
+           os.path.join(CSRC, "tc05.cuh"),
            os.path.join(INCLUDE, "pkv.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -158,15 +158,25 @@ struct KParams {
     float* part_o;
     int W;
     unsigned* err;
+    // shared prefix: positions below key_start were attended by the prefix kernel,
+    // whose pre_splits partials per query row (stride pre_stride rows) join the merge
+    int64_t key_start;
+    const float2* pre_ml;
+    const float* pre_o;
+    int pre_splits;
+    int64_t pre_stride;
 };
 
 __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
 }
 
-// First position a query at retained length t attends to (sliding window).
+// First position this kernel reads for a query at retained length t: the
+// window's first position, or the first position after a shared prefix that
+// the prefix kernel attends.
 __device__ __forceinline__ int64_t window_start(const KParams& p, int64_t t) {
-    return (p.window > 0 && t > p.window) ? t - p.window : 0;
+    const int64_t w = (p.window > 0 && t > p.window) ? t - p.window : 0;
+    return w > p.key_start ? w : p.key_start;
 }
 
 // Tiles a lane of retained length t reads: from the tile holding the window's
@@ -205,7 +215,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
         if (i < p.B) {
             const int64_t t = seq_len_at(p, i);
             const int64_t pages = (t + p.P - 1) / p.P;
-            if (t < 1 || t > p.max_seq_len || pages > p.max_pages) {
+            if (t < 1 || t > p.max_seq_len || pages > p.max_pages || t <= p.key_start) {
                 atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
             } else {
                 n = lane_tiles(p, t);
@@ -328,9 +338,14 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
     auto owns_tiles = [&](int64_t w) { return (w * T_all) / p.W != ((w + 1) * T_all) / p.W; };
     const int cnt = (int)(w_hi - w_lo + 1);
     const int64_t slot0 = lane_id + w_lo;
+    const int64_t row = lane_id * G + g;                  // query row (request, query head)
     float M = -INFINITY;
     for (int j = lane; j < cnt; j += 32)
         if (owns_tiles(w_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + j) * G + g]).x);
+    for (int s = lane; s < p.pre_splits; s += 32) {
+        const float2 ml = __ldcg(&p.pre_ml[s * p.pre_stride + row]);
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
@@ -360,6 +375,30 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
             }
         }
     }
+    // the shared prefix's partials, weighted the same way
+    for (int base = 0; base < p.pre_splits; base += 32) {
+        float wgt = 0.f;
+        if (base + lane < p.pre_splits) {
+            const float2 ml = __ldcg(&p.pre_ml[(base + lane) * p.pre_stride + row]);
+            if (ml.y > 0.f) {
+                wgt = exp2f(ml.x - M);
+                L = fmaf(ml.y, wgt, L);
+            }
+        }
+        const int nj = p.pre_splits - base < 32 ? p.pre_splits - base : 32;
+#pragma unroll 8
+        for (int j = 0; j < nj; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wgt, j);
+            if (has_features) {
+                const float* op = p.pre_o + ((base + j) * p.pre_stride + row) * D + lane * DPL;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) {
+                    const float v = __ldcg(op + i);
+                    acc[i] = wj != 0.f ? fmaf(wj, v, acc[i]) : acc[i];
+                }
+            }
+        }
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     if (!has_features) return;
@@ -367,6 +406,26 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
     float* out = p.out + (lane_id * G + g) * D + lane * DPL;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
+}
+
+// Shared-prefix calls: one warp per query row merges the row's worker partials
+// and the prefix kernel's partials (after the split kernel, in stream order).
+template <int D, int G>
+__global__ void __launch_bounds__(256) combine_kernel(const KParams p) {
+    constexpr int DPL = D >= 32 ? D / 32 : 1;
+    const int64_t qrow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (qrow >= (int64_t)p.B * p.H * G) return;
+    const int64_t lane_id = qrow / G;
+    const int g = (int)(qrow - lane_id * G);
+    const int b = (int)(lane_id / p.H), h = (int)(lane_id - (int64_t)b * p.H);
+    const int64_t pre_b = req_prefix_at(p, b);
+    const int64_t n = req_prefix_at(p, b + 1) - pre_b;    // 0 for a request the plan rejected
+    if (n <= 0) return;
+    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
+    const int64_t A = (int64_t)p.H * pre_b + (int64_t)h * n;
+    merge_query<D, DPL, G>(p, lane_id, g, worker_of(A, T_all, p.W), worker_of(A + n - 1, T_all, p.W),
+                           T_all, lane);
 }
 
 // One worker (warp) of the split kernel.  A lane here is a (request, KV head)
@@ -638,7 +697,7 @@ split_decode_kernel(const KParams p) {
                     }
                 }
             }
-            if (piece_first == 0 && last_tile) {
+            if (piece_first == 0 && last_tile && p.pre_ml == nullptr) {
                 if (lane < Gm::TPR) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -666,6 +725,10 @@ split_decode_kernel(const KParams p) {
                 }
                 __threadfence();
                 __syncwarp();
+                if (p.pre_ml != nullptr) {       // the combine kernel merges every lane
+                    cursor_advance(cur, p);
+                    continue;
+                }
                 const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // lane's first tile
                 const int64_t w_lo = worker_of(A, T_all, p.W);
                 const int64_t w_hi = worker_of(A + cur.n - 1, T_all, p.W);
@@ -1027,7 +1090,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             float lt = l;
             lt += __shfl_xor_sync(0xffffffffu, lt, 1);
             lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-            if (piece_first == 0 && last_tile) {
+            if (piece_first == 0 && last_tile && p.pre_ml == nullptr) {
                 if (q_ok) {
                     const float inv = 1.f / lt;
                     float* op = p.out + (lane_id * G + g) * D + 2 * t;
@@ -1048,6 +1111,10 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 }
                 __threadfence();
                 __syncwarp();
+                if (p.pre_ml != nullptr) {       // the combine kernel merges every lane
+                    cursor_advance(cur, p);
+                    continue;
+                }
                 const int64_t A = cur.first + (int64_t)cur.h * cur.n;
                 const int64_t w_lo = worker_of(A, T_all, p.W);
                 const int64_t w_hi = worker_of(A + cur.n - 1, T_all, p.W);
@@ -1154,7 +1221,9 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
         plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    // the timing events bracket the attention: the prefix kernel, if any, and the split kernel
     if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+    if (a.before_split && (e = a.before_split(a.before_split_ctx, stream)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)((p.W + Gm::WARPS - 1) / Gm::WARPS));
     cfg.blockDim = dim3(Gm::WARPS * 32);
@@ -1168,6 +1237,11 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     cfg.attrs = attr;
     cfg.numAttrs = p.epoch == 0 ? 1 : 0;
     if ((e = cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G>, p)) != cudaSuccess) return e;
+    if (p.pre_ml != nullptr) {
+        const int64_t rows = (int64_t)p.B * p.H * G;
+        combine_kernel<D, G><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (a.ev_after && (e = cudaEventRecord(a.ev_after, stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }
@@ -1203,7 +1277,9 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
         plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    // the timing events bracket the attention: the prefix kernel, if any, and the split kernel
     if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+    if (a.before_split && (e = a.before_split(a.before_split_ctx, stream)) != cudaSuccess) return e;
     CUtensorMap tmk, tmv;
     memcpy(&tmk, a.tmap_k, sizeof tmk);
     memcpy(&tmv, a.tmap_v, sizeof tmv);
@@ -1219,6 +1295,11 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
     cfg.numAttrs = p.epoch == 0 ? 1 : 0;
     if ((e = cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<D, G>, p, tmk, tmv)) != cudaSuccess)
         return e;
+    if (p.pre_ml != nullptr) {
+        const int64_t rows = (int64_t)p.B * p.H * G;
+        combine_kernel<D, G><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (a.ev_after && (e = cudaEventRecord(a.ev_after, stream)) != cudaSuccess) return e;
     return cudaSuccess;
 }
@@ -1294,6 +1375,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.part_o = reinterpret_cast<float*>(ws + L.part_o);
     p.W = a.workers;
     p.err = a.dev_error;
+    p.key_start = a.key_start;
+    p.pre_ml = static_cast<const float2*>(a.pre_ml);
+    p.pre_o = a.pre_o;
+    p.pre_splits = a.pre_splits;
+    p.pre_stride = a.pre_stride;
     if (a.tmap_k != nullptr && a.tmap_v != nullptr) {
 #define PKV_LAUNCH_MMA(DD, GG) \
         if (a.D == DD && a.G == GG) return launch_mma<DD, GG>(a, p, stream);

@@ -47,6 +47,16 @@ struct DecodeArgs {
                              // (no plan kernel; the workspace's counters started at zero)
     const void* tmap_k;      // CUtensorMap of this layer's K / V pools (host memory), or
     const void* tmap_v;      // nullptr: selects the tensor-core kernel when non-null
+    // shared prefix (batched calls): the split kernel reads positions >= key_start and
+    // merges pre_splits partials per query row from the prefix kernel, which
+    // before_split(before_split_ctx, stream) enqueues between the plan and split kernels
+    int64_t key_start;
+    const void* pre_ml;      // float2 [pre_splits][pre_stride]: (max in log2 units, sum)
+    const float* pre_o;      // float [pre_splits][pre_stride][D]: unnormalised outputs
+    int pre_splits;
+    int64_t pre_stride;      // query rows per split (B * query heads)
+    cudaError_t (*before_split)(const void* ctx, cudaStream_t stream);
+    const void* before_split_ctx;
 };
 
 // Bytes of a CUtensorMap (the driver's TMA descriptor).
@@ -140,5 +150,42 @@ int prefill_max_batch();
 
 // Enqueue the plan, append and attention kernels on `stream`.
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------- shared prefix --
+
+// How the prefix kernel cuts its work: 128-row tiles of (request, query head)
+// rows per KV head, and key splits of split_len positions (whole 128-key tiles).
+struct SharedPrefixPlan {
+    int row_tiles;
+    int64_t split_len;
+    int splits;
+};
+
+SharedPrefixPlan shared_prefix_plan(int B, int H, int G, int64_t shared_len, int num_sms);
+
+// True if the prefix kernel implements (dtype, D, G).
+bool shared_prefix_supported(int dtype, int D, int G);
+
+// One launch of the prefix kernel (the shared part of a batch's decode attention).
+struct SharedPrefixArgs {
+    int B, H, G, D, P, max_pages;
+    int64_t window;
+    int64_t n_pages;
+    const float* q;          // [B][H*G][D] fp32
+    const int32_t* tables;   // [B][max_pages]; request 0's first shared_len / P entries
+    const int32_t* seq_lens; // [B]
+    int64_t shared_len;
+    SharedPrefixPlan plan;
+    float2* pre_ml;          // [splits][B*H*G]
+    float* pre_o;            // [splits][B*H*G][D]
+    unsigned* dev_error;
+    const void* tmap_k;      // CUtensorMap of this layer's K / V pools (host memory)
+    const void* tmap_v;
+};
+
+cudaError_t launch_shared_prefix(const SharedPrefixArgs& a, cudaStream_t stream);
+
+// DecodeArgs::before_split for a shared prefix: ctx is a SharedPrefixArgs.
+cudaError_t launch_shared_prefix_hook(const void* ctx, cudaStream_t stream);
 
 }  // namespace pkv

@@ -74,6 +74,7 @@ struct pkv_pool {
     size_t layer_bytes = 0;
     unsigned* dev_error = nullptr;
     int device = -1;
+    int sms = 0;                       // streaming multiprocessors of the device
     int workers = 0;                   // resident split-kernel warps on the device
     int64_t live_requests = 0;
     cudaEvent_t ev_before = nullptr;   // optional split-kernel timing events
@@ -314,6 +315,7 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
             delete p;
             return cuda_fail(e, "device query");
         }
+        p->sms = sms;
         const int64_t rows = pages * page_size * heads;   // pool rows of one layer
         p->tmaps = dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) && rows < INT32_MAX &&
                    tensor_map_encoder() != nullptr;
@@ -955,6 +957,121 @@ int pkv_paged_prefill(pkv_pool* p, int layer, int batch, int64_t total_new, cons
     a.tmap_v = &p->tmap_v[(size_t)layer];
     cudaError_t e = pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return ok();
+}
+
+}  // extern "C"
+
+namespace {
+
+// Scratch of a shared-prefix call: the decode workspace, then the prefix partials.
+struct SharedLayout {
+    size_t decode, pre_ml, pre_o, total;
+    pkv::SharedPrefixPlan plan;
+};
+
+SharedLayout shared_layout(const pkv_pool* p, int batch, int64_t max_seq_len, int64_t shared_len) {
+    SharedLayout L{};
+    const int w = pkv::launch_workers(p->workers, batch, p->heads,
+                                      pkv::attended_len(max_seq_len, p->window));
+    L.decode = (pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total + 255) /
+               256 * 256;
+    L.plan = pkv::shared_prefix_plan(batch, p->heads, p->group, shared_len, p->sms);
+    const size_t rows = (size_t)L.plan.splits * batch * p->query_heads;
+    L.pre_ml = L.decode;
+    L.pre_o = L.pre_ml + (rows * sizeof(float2) + 255) / 256 * 256;
+    L.total = L.pre_o + rows * p->head_dim * sizeof(float);
+    return L;
+}
+
+int check_shared(const pkv_pool* p, int64_t max_seq_len, int64_t shared_len) {
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+    if (shared_len < 0 || shared_len % p->page_size != 0)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "shared_len %lld is not a multiple of page_size %d",
+                    (long long)shared_len, p->page_size);
+    if (shared_len > 0 && shared_len >= max_seq_len)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "shared_len %lld leaves no position of a request's own",
+                    (long long)shared_len);
+    if (shared_len > 0 && !(p->tmaps && pkv::shared_prefix_supported(p->dtype, p->head_dim, p->group)))
+        return fail(PKV_ERR_UNSUPPORTED, "shared prefixes need bf16 pools of head_dim 64 or 128");
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_workspace_size_shared(const pkv_pool* p, int batch, int64_t max_seq_len, int64_t shared_len,
+                              size_t* bytes) {
+    if (!p || !bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
+    if (batch < 0 || max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "bad batch or length");
+    int rc = check_shared(p, max_seq_len, shared_len);
+    if (rc != PKV_OK) return rc;
+    if (shared_len == 0) return pkv_workspace_size(p, batch, max_seq_len, bytes);
+    *bytes = batch == 0 ? 0 : shared_layout(p, batch, max_seq_len, shared_len).total;
+    return ok();
+}
+
+int pkv_paged_decode_attention_shared(pkv_pool* p, int layer, int batch, const float* q,
+                                      const void* k_new, const void* v_new,
+                                      const int32_t* page_tables, int max_pages,
+                                      const int32_t* seq_lens, int64_t max_seq_len,
+                                      int64_t shared_len, float* out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    if (max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "max_seq_len must be >= 1");
+    int rc = check_shared(p, max_seq_len, shared_len);
+    if (rc != PKV_OK) return rc;
+    if (shared_len == 0)
+        return pkv_paged_decode_attention(p, layer, batch, q, k_new, v_new, page_tables, max_pages,
+                                          seq_lens, max_seq_len, out, workspace, workspace_bytes,
+                                          stream);
+    if (shared_len / p->page_size > max_pages)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "shared_len %lld needs more than max_pages pages",
+                    (long long)shared_len);
+    pkv::DecodeArgs a{};
+    size_t need = 0;
+    rc = pkv::prepare_batched(p, layer, batch, q, k_new, v_new, page_tables, max_pages, seq_lens,
+                              max_seq_len, out, &a, &need);
+    if (rc != PKV_OK || a.B == 0) return rc;
+    if (!workspace) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL workspace");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+    const SharedLayout L = shared_layout(p, batch, max_seq_len, shared_len);
+    if (workspace_bytes < L.total)
+        return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    L.total);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    pkv::SharedPrefixArgs sp{};
+    sp.B = batch;
+    sp.H = p->heads;
+    sp.G = p->group;
+    sp.D = p->head_dim;
+    sp.P = p->page_size;
+    sp.max_pages = max_pages;
+    sp.window = p->window;
+    sp.n_pages = p->pages;
+    sp.q = q;
+    sp.tables = page_tables;
+    sp.seq_lens = seq_lens;
+    sp.shared_len = shared_len;
+    sp.plan = L.plan;
+    sp.pre_ml = reinterpret_cast<float2*>(ws + L.pre_ml);
+    sp.pre_o = reinterpret_cast<float*>(ws + L.pre_o);
+    sp.dev_error = p->dev_error;
+    sp.tmap_k = &p->tmap_k[(size_t)layer];
+    sp.tmap_v = &p->tmap_v[(size_t)layer];
+    a.workspace = workspace;
+    a.workspace_bytes = L.decode;
+    a.key_start = shared_len;
+    a.pre_ml = sp.pre_ml;
+    a.pre_o = sp.pre_o;
+    a.pre_splits = L.plan.splits;
+    a.pre_stride = (int64_t)batch * p->query_heads;
+    a.before_split = pkv::launch_shared_prefix_hook;
+    a.before_split_ctx = &sp;
+    cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix decode launch");
     return ok();
 }
 
