@@ -835,8 +835,13 @@ struct MmaGeo {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int KSTEPS = D / 16;                 // k-steps of S = Q K^T
     static constexpr int NB = D / 8;                      // n-blocks of O
+#if defined(PKV_MMA_WARPS) && defined(PKV_MMA_STAGES)
+    static constexpr int WARPS = PKV_MMA_WARPS;
+    static constexpr int STAGES = PKV_MMA_STAGES;
+#else
     static constexpr int WARPS = Geo<__nv_bfloat16, D>::WARPS;
     static constexpr int STAGES = Geo<__nv_bfloat16, D>::STAGES;
+#endif
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES;
     // stage rings (1024-byte aligned, as the swizzle requires), then mbarriers and page ids
     static constexpr int CTA_SMEM = 1024 + WARPS * (WARP_SMEM + STAGES * 12);
