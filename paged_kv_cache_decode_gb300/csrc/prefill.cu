@@ -475,24 +475,28 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
             return pf_warp_wait(&slot_full[ld % M::SLOTS], (ld / M::SLOTS) & 1, abort_flag,
                                 p.dev_error);
         };
+        // descriptors are built once per group: a k-step only moves the start address,
+        // by a constant (shared-memory addresses stay below 2^18, so no field overflows)
         auto issue_s = [&](int j, int x) {
             const uint32_t k_addr = ring_addr + ((2 * j) % M::SLOTS) * M::KV_BYTES;
-            const uint32_t qa = q_addr + x * M::Q_BYTES;
+            const uint64_t da = sw128_desc(q_addr + x * M::Q_BYTES, 16, 1024);
+            const uint64_t db = sw128_desc(k_addr, 16, 1024);
+            const uint32_t d = tmem + M::S_COL + x * kKeys;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-                umma_bf16(tmem + M::S_COL + x * kKeys, sw128_desc(qa + off, 16, 1024),
-                          sw128_desc(k_addr + off, 16, 1024), idS, k > 0);
+                const uint64_t dk = (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4);
+                umma_bf16(d, da + dk, db + dk, idS, k > 0);
             }
             umma_commit(&s_full[x]);
         };
         auto issue_pv = [&](int j, int x) {
             const uint32_t v_addr = ring_addr + ((2 * j + 1) % M::SLOTS) * M::KV_BYTES;
+            const uint64_t dv = sw128_desc(v_addr, kVLbo, 1024);
             const uint32_t pa = tmem + M::S_COL + x * kKeys;        // P in TMEM, 8 columns per k-step
+            const uint32_t o = tmem + M::O_COL + x * D;
 #pragma unroll
             for (int k = 0; k < kKeys / 16; ++k)
-                umma_bf16_tmem_a(tmem + M::O_COL + x * D, pa + k * 8,
-                                 sw128_desc(v_addr + k * 16 * 128, kVLbo, 1024), idO,
+                umma_bf16_tmem_a(o, pa + k * 8, dv + (uint64_t)((k * 16 * 128) >> 4), idO,
                                  (j > 0 || k > 0) ? 1u : 0u);
         };
         bool ok = pf_warp_wait(q_ready, 0, abort_flag, p.dev_error) && wait_slot(0);

@@ -383,17 +383,18 @@ shared_prefix_kernel(const __grid_constant__ SpParams p, const __grid_constant__
             return pf_warp_wait(&slot_full[ld % M::SLOTS], (ld / M::SLOTS) & 1, abort_flag,
                                 p.dev_error);
         };
+        // descriptors are built once per group; a k-step only moves the start address
         auto issue_s = [&](int j) {
             const uint32_t k_addr = ring_addr + ((2 * j) % M::SLOTS) * M::KV_BYTES;
             const uint32_t d = tmem + M::S_COL + (j & 1) * kSpKeys;
+            const uint64_t db = sw128_desc(k_addr, 16, 1024);
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
-                const uint32_t qa = part ? qlo_addr : qhi_addr;
+                const uint64_t da = sw128_desc(part ? qlo_addr : qhi_addr, 16, 1024);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * (kSpRows * 128) + (k & 3) * 32;
-                    umma_bf16(d, sw128_desc(qa + off, 16, 1024), sw128_desc(k_addr + off, 16, 1024),
-                              idS, (part > 0 || k > 0) ? 1u : 0u);
+                    const uint64_t dk = (uint64_t)(((k >> 2) * (kSpRows * 128) + (k & 3) * 32) >> 4);
+                    umma_bf16(d, da + dk, db + dk, idS, (part > 0 || k > 0) ? 1u : 0u);
                 }
             }
             umma_commit(&s_full[j & 1]);
@@ -402,12 +403,13 @@ shared_prefix_kernel(const __grid_constant__ SpParams p, const __grid_constant__
         auto issue_pv = [&](int j) {
             const uint32_t v_addr = ring_addr + ((2 * j + 1) % M::SLOTS) * M::KV_BYTES;
             const uint32_t pa = tmem + M::S_COL + (j & 1) * kSpKeys;
+            const uint64_t dv = sw128_desc(v_addr, kVLbo, 1024);
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
                 for (int k = 0; k < kSpKeys / 16; ++k)
                     umma_bf16_tmem_a(tmem + M::O_COL, pa + part * 64 + k * 8,
-                                     sw128_desc(v_addr + k * 16 * 128, kVLbo, 1024), idO,
+                                     dv + (uint64_t)((k * 16 * 128) >> 4), idO,
                                      (j > 0 || part > 0 || k > 0) ? 1u : 0u);
             umma_commit(&slot_empty[(2 * j + 1) % M::SLOTS]);
             umma_commit(&pv_done[j & 1]);
