@@ -36,6 +36,7 @@ METRIC = "paged decode attention: achieved HBM GB/s (% of 8 TB/s) and decode tok
 NOMINAL_HBM_GBS = 8000.0
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "decode.cu")
 PREFILL_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "prefill.cu")
+SHARED_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "shared_prefix.cu")
 TRAFFIC_DIR = os.path.join(ROOT, "profiles")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -225,10 +226,11 @@ def source_hash(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def measured_traffic(workload: str, kernel: str = "split_decode", source: str = DECODE_SRC):
+def measured_traffic(workload: str, kernel: str = "split_decode", source=DECODE_SRC):
     """DRAM bytes per launch of a kernel from the committed ncu summary
     profiles/traffic_<kernel>_<workload>.txt, or None when there is none or the
-    kernel source changed since the counters were taken."""
+    kernel source changed since the counters were taken.  Several sources hash
+    as the sha256 of their sha256 hex digests, in order."""
     rec = {}
     try:
         with open(os.path.join(TRAFFIC_DIR, f"traffic_{kernel}_{workload}.txt")) as f:
@@ -238,7 +240,11 @@ def measured_traffic(workload: str, kernel: str = "split_decode", source: str = 
                     rec[line[0]] = line[1]
     except OSError:
         return None
-    if rec.get("source_sha256") != source_hash(source) or "dram_bytes_per_launch" not in rec:
+    if isinstance(source, (list, tuple)):
+        want = hashlib.sha256("".join(source_hash(x) for x in source).encode()).hexdigest()
+    else:
+        want = source_hash(source)
+    if rec.get("source_sha256") != want or "dram_bytes_per_launch" not in rec:
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -417,7 +423,9 @@ def run_gpu(args):
             "tokens_per_s": round(world * w.B / (step_ms_max * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": measured_traffic(w.name),
+                         "traffic": (measured_traffic(w.name, "shared_prefix",
+                                                      [DECODE_SRC, SHARED_SRC]) if shared
+                                     else measured_traffic(w.name)),
                          "kernel": kernel_name,
                          "kernel_ms": round(kernel_ms, 5), "peak_kind": peak_kind + " (hbm_gbs copy)"},
             "e2e": {"value": round(world * alg / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
