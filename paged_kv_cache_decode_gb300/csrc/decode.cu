@@ -488,9 +488,20 @@ split_decode_kernel(const KParams p) {
     Cursor prod = cur;
 
     // Producer step (lane 0): stage tile `prod` into stage s.
+    // page-table entries by warp: lane i holds entry tab_base + i of request tab_b, so
+    // a tile's page id is a shuffle and the table is read once per 32 pages
+    int tab_b = -1;
+    int64_t tab_base = 0;
+    int32_t tab_val = -1;
     auto issue = [&](int s) {
+        if (prod.b != tab_b || prod.page_idx < tab_base || prod.page_idx >= tab_base + 32) {
+            tab_b = prod.b;
+            tab_base = prod.page_idx;
+            const int64_t e = tab_base + lane;
+            tab_val = e < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages + e) : -1;
+        }
+        const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(prod.page_idx - tab_base));
         if (lane != 0) return;
-        const int32_t page = __ldg(p.tables + (int64_t)prod.b * p.max_pages + prod.page_idx);
         stage_page[s] = page;
         if (page < 0 || page >= p.n_pages) {
             atomicOr(p.err, PKV_DEVERR_PAGE_ID);
@@ -909,9 +920,20 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     Cursor prod = cur;
 
     // Producer step (lane 0): stage tile `prod` into stage s, box by box.
+    // page-table entries by warp: lane i holds entry tab_base + i of request tab_b, so
+    // a tile's page id is a shuffle and the table is read once per 32 pages
+    int tab_b = -1;
+    int64_t tab_base = 0;
+    int32_t tab_val = -1;
     auto issue = [&](int s) {
+        if (prod.b != tab_b || prod.page_idx < tab_base || prod.page_idx >= tab_base + 32) {
+            tab_b = prod.b;
+            tab_base = prod.page_idx;
+            const int64_t e = tab_base + lane;
+            tab_val = e < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages + e) : -1;
+        }
+        const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(prod.page_idx - tab_base));
         if (lane != 0) return;
-        const int32_t page = __ldg(p.tables + (int64_t)prod.b * p.max_pages + prod.page_idx);
         stage_page[s] = page;
         if (page < 0 || page >= p.n_pages) {
             atomicOr(p.err, PKV_DEVERR_PAGE_ID);
