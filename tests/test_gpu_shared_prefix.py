@@ -107,3 +107,66 @@ def test_shared_prefix_full_workload_sampled():
         print(f"prefix_bf16 shared sampled: {err:.2e}")
     finally:
         run.close()
+
+
+def test_shared_prefix_edge_lengths_and_page_size():
+    """A request whose only own position is its new token, page size 32, a window that
+    cuts into the prefix for some requests, G = 1 (CUDA-core suffix kernel)."""
+    rng_lens = [1, 2, 40, 97]                       # own positions (the new token included)
+    prefix = 96
+    lens = np.array([prefix + n for n in rng_lens], dtype=np.int32)
+    pages = int(((lens.astype(np.int64) + 31) // 32).sum()) + 8
+    w = Workload("edge", len(lens), 1, 2, 64, 32, BF16, pages, int(lens.max()), 17, lens, group=1,
+                 window=60, shared_prefix=prefix)
+    run = BatchedRun(w)
+    try:
+        out = _shared(run, prefix).cpu().numpy()
+        torch.cuda.synchronize()
+        assert run.pool.check_device_status() == 0
+        ref = run.oracle_out()
+        check_close(np.stack([out[k] for k in ref]), np.stack(list(ref.values())), BF16, "edge")
+    finally:
+        run.close()
+
+
+def test_shared_prefix_request_without_own_positions_sets_error_bit():
+    w = _workload("short", 3, 64, 10, 2, 128, 4, seed=8)
+    run = BatchedRun(w)
+    try:
+        lens = run.dev["lens"].clone()
+        lens[1] = 64                                    # t_b == shared_len: its new row would be shared
+        d = run.dev
+        run.pool.paged_decode_attention_shared(0, d["q"], d["k"], d["v"], d["tables"], lens,
+                                               run.max_seq_len, 64)
+        torch.cuda.synchronize()
+        with pytest.raises(pkv.PkvError) as e:
+            run.pool.check_device_status()
+        assert "0x1" in str(e.value)
+    finally:
+        run.close()
+
+
+def test_shared_prefix_argument_errors():
+    w = _workload("args", 2, 32, 5, 2, 128, 4, seed=9)
+    run = BatchedRun(w)
+    try:
+        d = run.dev
+        for shared, st in [(17, pkv.PKV_ERR_INVALID_ARGUMENT), (run.max_seq_len, pkv.PKV_ERR_INVALID_ARGUMENT)]:
+            with pytest.raises(pkv.PkvError) as e:
+                run.pool.paged_decode_attention_shared(0, d["q"], d["k"], d["v"], d["tables"], d["lens"],
+                                                       run.max_seq_len, shared)
+            assert e.value.status == st
+    finally:
+        run.close()
+    # fp32 pools have no shared-prefix kernel
+    w32 = Workload("f32", 2, 1, 2, 64, 16, 0, 64, 256, 1, np.array([40, 50], dtype=np.int32),
+                   shared_prefix=32)
+    run = BatchedRun(w32)
+    try:
+        d = run.dev
+        with pytest.raises(pkv.PkvError) as e:
+            run.pool.paged_decode_attention_shared(0, d["q"], d["k"], d["v"], d["tables"], d["lens"],
+                                                   run.max_seq_len, 32)
+        assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+    finally:
+        run.close()
