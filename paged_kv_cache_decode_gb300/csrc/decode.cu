@@ -93,6 +93,12 @@ struct Storage<__nv_bfloat16> {
 #ifndef PKV_SM_SMEM_BUDGET
 #define PKV_SM_SMEM_BUDGET 131072  // stage-ring bytes of one split CTA (one CTA per SM)
 #endif
+#ifndef PKV_SM_SMEM_BUDGET_GROUPED
+// fp32 with several query heads per KV head: each tile carries G times the
+// arithmetic, and a larger ring buys more warps to hide it (bf16 tiles are half
+// the size and already get eight warps)
+#define PKV_SM_SMEM_BUDGET_GROUPED 196608
+#endif
 
 // Warp geometry of one 16-row tile for storage type T and head width D, and
 // the CTA shape.  TPR lanes share one row (VEC elements each, one 16-byte
@@ -101,8 +107,10 @@ struct Storage<__nv_bfloat16> {
 // ((l % TPR) >> 1) * RPI + l / TPR (lanes l and l ^ 1 hold the same row when
 // TPR >= 2), so each lane takes one exp2 per tile.  One CTA per SM: WARPS
 // workers, each with STAGES tiles in flight, within the shared-memory budget.
-template <typename T, int D>
+template <typename T, int D, int G = 1>
 struct Geo {
+    static constexpr int BUDGET =
+        (G > 1 && sizeof(T) == 4) ? PKV_SM_SMEM_BUDGET_GROUPED : PKV_SM_SMEM_BUDGET;
     static constexpr int ES = sizeof(T);
     static constexpr int VEC = (16 / ES) < D ? (16 / ES) : D;  // elements per lane vector
     static constexpr int VBYTES = VEC * ES;                    // 16, 8 or 4
@@ -114,10 +122,10 @@ struct Geo {
                                         : ITERS == 2 ? 1 : 0;  // log2(ITERS)
     static constexpr int TILE_BYTES = kTile * D * ES;          // K (or V) rows of one tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int STAGES_AT_WARPS = PKV_SM_SMEM_BUDGET / (kSplitWarps * STAGE_BYTES);
+    static constexpr int STAGES_AT_WARPS = BUDGET / (kSplitWarps * STAGE_BYTES);
     static constexpr int WARPS = STAGES_AT_WARPS >= 2
-        ? kSplitWarps : (PKV_SM_SMEM_BUDGET / (2 * STAGE_BYTES) > 0 ? PKV_SM_SMEM_BUDGET / (2 * STAGE_BYTES) : 1);
-    static constexpr int STAGES_RAW = PKV_SM_SMEM_BUDGET / (WARPS * STAGE_BYTES);
+        ? kSplitWarps : (BUDGET / (2 * STAGE_BYTES) > 0 ? BUDGET / (2 * STAGE_BYTES) : 1);
+    static constexpr int STAGES_RAW = BUDGET / (WARPS * STAGE_BYTES);
     static constexpr int STAGES = STAGES_RAW < 2 ? 2 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES;
     // per warp: stage buffers, then per stage an mbarrier (8 B) and the staged page id (4 B)
@@ -432,9 +440,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const KParams p) {
 // pair; its G query heads (grouped-query attention, G = 1 for multi-head) share
 // every staged K/V tile: query head h*G + g of request b reads KV head h.
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(Geo<T, D>::WARPS * 32, 1)
+__global__ void __launch_bounds__(Geo<T, D, G>::WARPS * 32, 1)
 split_decode_kernel(const KParams p) {
-    using Gm = Geo<T, D>;
+    using Gm = Geo<T, D, G>;
     using VT = typename VecBits<Gm::VBYTES>::type;
     constexpr int NV = Gm::VEC / 2;   // float pairs per lane vector
     extern __shared__ __align__(128) unsigned char smem[];
@@ -1223,7 +1231,7 @@ static cudaError_t prepare_split() {
     if (done) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<T, D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Geo<T, D>::CTA_SMEM);
+                                         Geo<T, D, G>::CTA_SMEM);
     if (e == cudaSuccess) done = true;
     return e;
 }
@@ -1233,15 +1241,15 @@ static int resident_workers_t(int num_sms) {
     if (prepare_split<T, D, G>() != cudaSuccess) return 0;
     int blocks = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_kernel<T, D, G>,
-                                                      Geo<T, D>::WARPS * 32, Geo<T, D>::CTA_SMEM) !=
+                                                      Geo<T, D, G>::WARPS * 32, Geo<T, D, G>::CTA_SMEM) !=
         cudaSuccess)
         return 0;
-    return blocks * num_sms * Geo<T, D>::WARPS;
+    return blocks * num_sms * Geo<T, D, G>::WARPS;
 }
 
 template <typename T, int D, int G>
 static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream) {
-    using Gm = Geo<T, D>;
+    using Gm = Geo<T, D, G>;
     cudaError_t e = prepare_split<T, D, G>();
     if (e != cudaSuccess) return e;
     if (p.epoch == 0) {   // a single request with epoch counters needs no plan
