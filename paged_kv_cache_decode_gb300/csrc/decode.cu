@@ -416,6 +416,82 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
     for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
 
+// Combine the partials of all G query rows of KV lane `lane_id` at once (G >= 2
+// dividing 32), deposited by workers w_lo..w_hi in slots lane_id + w, into out.
+// For the maxima, sums and weights lane j takes worker slot j / G of a chunk of
+// 32 / G slots and query row j % G, so every row's max and sum reduce over the
+// lanes of one residue class mod G; for the o vectors lane j takes features
+// j * D/32 .. of every row, each weight broadcast by shuffle.  The loads of the
+// whole group go out together: a few L2 round trips per lane instead of a few
+// per query row, which matters because the merging warp's ring waits meanwhile.
+template <int D, int G>
+__device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, int64_t w_lo,
+                                           int64_t w_hi, int64_t T_all, int lane) {
+    static_assert(G >= 2 && 32 % G == 0 && D % 64 == 0, "grouped merge: G divides 32, D 64 or 128");
+    constexpr int SPC = 32 / G;          // worker slots per chunk
+    constexpr int DPL = D / 32;          // features per lane (2 or 4)
+    auto owns_tiles = [&](int64_t w) { return (w * T_all) / p.W != ((w + 1) * T_all) / p.W; };
+    const int cnt = (int)(w_hi - w_lo + 1);
+    const int64_t slot0 = lane_id + w_lo;
+    const int r = lane % G;              // the query row this lane weighs
+    float M = -INFINITY;
+    for (int j = lane / G; j < cnt; j += SPC)
+        if (owns_tiles(w_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + j) * G + r]).x);
+#pragma unroll
+    for (int off = 16; off >= G; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    float acc[G][DPL];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[g][i] = 0.f;
+    for (int base = 0; base < cnt; base += SPC) {
+        const int j = base + lane / G;
+        float wgt = 0.f;
+        if (j < cnt && owns_tiles(w_lo + j)) {
+            const float2 ml = __ldcg(&p.part_ml[(slot0 + j) * G + r]);
+            wgt = exp2f(ml.x - M);
+            L = fmaf(ml.y, wgt, L);
+        }
+        const int nj = cnt - base < SPC ? cnt - base : SPC;
+#pragma unroll 1
+        for (int jj = 0; jj < nj; ++jj) {
+            const float* op = p.part_o + (slot0 + base + jj) * G * D + lane * DPL;
+            float v[G][DPL];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                if constexpr (DPL == 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(op + g * D));
+                    v[g][0] = x.x, v[g][1] = x.y, v[g][2] = x.z, v[g][3] = x.w;
+                } else {
+                    const float2 x = __ldcg(reinterpret_cast<const float2*>(op + g * D));
+                    v[g][0] = x.x, v[g][1] = x.y;
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                // slots of workers that own no tile hold stale data: weight 0, value dropped
+                const float wj = __shfl_sync(0xffffffffu, wgt, jj * G + g);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc[g][i] = wj != 0.f ? fmaf(wj, v[g][i], acc[g][i]) : acc[g][i];
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= G; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    float* out = p.out + lane_id * G * D + lane * DPL;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float inv = 1.f / __shfl_sync(0xffffffffu, L, g);
+        if constexpr (DPL == 4) {
+            *reinterpret_cast<float4*>(out + g * D) =
+                make_float4(acc[g][0] * inv, acc[g][1] * inv, acc[g][2] * inv, acc[g][3] * inv);
+        } else {
+            *reinterpret_cast<float2*>(out + g * D) = make_float2(acc[g][0] * inv, acc[g][1] * inv);
+        }
+    }
+}
+
 // Shared-prefix calls: one warp per query row merges the row's worker partials
 // and the prefix kernel's partials (after the split kernel, in stream order).
 template <int D, int G>
@@ -781,9 +857,10 @@ split_decode_kernel(const KParams p) {
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
                     __threadfence();
-#pragma unroll 1
-                    for (int g = 0; g < G; ++g)
-                        merge_query<D, Gm::DPL, G>(p, lane_id, g, w_lo, w_hi, T_all, lane);
+                    if constexpr (G == 1)
+                        merge_query<D, Gm::DPL, G>(p, lane_id, 0, w_lo, w_hi, T_all, lane);
+                    else
+                        merge_lane<D, G>(p, lane_id, w_lo, w_hi, T_all, lane);
                 }
                 __syncwarp();
             }
@@ -1179,10 +1256,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
                     __threadfence();
-#pragma unroll 1
-                    for (int gg = 0; gg < G; ++gg)
-                        merge_query<D, Geo<__nv_bfloat16, D>::DPL, G>(p, lane_id, gg, w_lo, w_hi,
-                                                                      T_all, lane);
+                    merge_lane<D, G>(p, lane_id, w_lo, w_hi, T_all, lane);
                 }
                 __syncwarp();
             }
