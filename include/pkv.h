@@ -32,6 +32,10 @@
  *     as void*; NULL is the legacy default stream).  No entry point
  *     synchronises except pkv_check_device_status.  The caller's current CUDA
  *     device must be the device the pool was created on.
+ *   - The q, k, v and out tensors of every attention call must each start on a
+ *     multiple of min(16, bytes of one head row) (head_dim x element size);
+ *     others are rejected with PKV_ERR_INVALID_ARGUMENT.  Workspaces start on a
+ *     multiple of 16 bytes.
  *   - Device-side faults are never raised by trapping: a kernel that meets an
  *     out-of-range length or page id, or a wait that runs out, sets a bit in the
  *     pool's device error word, skips the bad access and returns;

@@ -48,6 +48,7 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+
 // SplitMix64 (Steele, Lea & Flood 2014).
 struct SplitMix64 {
     uint64_t state;
@@ -118,6 +119,22 @@ struct pkv_request {
 };
 
 namespace {
+
+// The kernels move head rows of q, k, v and out in vectors of up to 16 bytes:
+// each tensor must start on a multiple of min(16, bytes of one head row).
+int check_rows_aligned(const pkv_pool* p, const void* q, int q_es, const void* k, const void* v,
+                       const void* out) {
+    auto ok_at = [&](const void* x, int es) {
+        const int64_t row = (int64_t)p->head_dim * es;
+        const int64_t a = row < 16 ? row : 16;
+        return reinterpret_cast<uintptr_t>(x) % (uintptr_t)a == 0;
+    };
+    const int kv_es = p->dtype == PKV_BF16 ? 2 : 4;
+    if (!ok_at(q, q_es) || !ok_at(k, kv_es) || !ok_at(v, kv_es) || !ok_at(out, 4))
+        return fail(PKV_ERR_INVALID_ARGUMENT,
+                    "q, k, v and out must each start on a multiple of min(16, one head row's bytes)");
+    return PKV_OK;
+}
 
 int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
 
@@ -649,6 +666,7 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     if (!q || !k || !v || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL tensor pointer");
     if (layer < 0 || layer >= p->layers)
         return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (int rc = check_rows_aligned(p, q, 4, k, v, out); rc != PKV_OK) return rc;
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (!r->pending) return fail(PKV_ERR_BAD_STATE, "no token pending");
     if (r->chunk) return fail(PKV_ERR_BAD_STATE, "a chunk is pending (pkv_prefill_chunk)");
@@ -710,6 +728,7 @@ int pkv_prefill_chunk(pkv_request* r, int layer, const void* q, const void* k, c
     if (!q || !k || !v || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL tensor pointer");
     if (layer < 0 || layer >= p->layers)
         return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
+    if (int rc = check_rows_aligned(p, q, 2, k, v, out); rc != PKV_OK) return rc;
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (!r->pending || !r->chunk) return fail(PKV_ERR_BAD_STATE, "no chunk pending");
     if (r->appended[(size_t)layer]) return fail(PKV_ERR_BAD_STATE, "layer %d already ran", layer);
@@ -834,17 +853,20 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
                                int max_pages, const int32_t* seq_lens, int64_t max_seq_len,
                                float* out, void* workspace, size_t workspace_bytes, void* stream) {
     if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
-    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (layer < 0 || layer >= p->layers)
         return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
     if (batch < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch");
+    if (batch > 0) {
+        if (!q || !k_new || !v_new || !page_tables || !seq_lens || !out || !workspace)
+            return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
+        if (max_pages < 1 || max_seq_len < 1)
+            return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
+        if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+            return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+        if (int rc = check_rows_aligned(p, q, 4, k_new, v_new, out); rc != PKV_OK) return rc;
+    }
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (batch == 0) return ok();
-    if (!q || !k_new || !v_new || !page_tables || !seq_lens || !out || !workspace)
-        return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
-    if (max_pages < 1 || max_seq_len < 1)
-        return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
-    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
-        return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
     const int w = pkv::launch_workers(p->workers, batch, p->heads, pkv::attended_len(max_seq_len, p->window));
     const size_t need = pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
     if (workspace_bytes < need)
@@ -919,6 +941,7 @@ int pkv_paged_prefill(pkv_pool* p, int layer, int batch, int64_t total_new, cons
     if (max_pages < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages must be >= 1");
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+    if (int rc = check_rows_aligned(p, q, 2, k_new, v_new, out); rc != PKV_OK) return rc;
     if (pkv::prefill_max_tiles(batch, p->group, total_new) * p->heads > INT32_MAX)
         return fail(PKV_ERR_INVALID_ARGUMENT, "%lld tokens need more CTAs than one launch holds",
                     (long long)total_new);
@@ -1121,17 +1144,21 @@ int prepare_batched(pkv_pool* p, int layer, int batch, const float* q, const voi
                     const int32_t* seq_lens, int64_t max_seq_len, float* out, DecodeArgs* a,
                     size_t* workspace_bytes) {
     if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
-    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (layer < 0 || layer >= p->layers)
         return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
     if (batch < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch");
     *a = DecodeArgs{};
     *workspace_bytes = 0;
+    if (batch > 0) {
+        if (!q || !k_new || !v_new || !page_tables || !seq_lens || !out)
+            return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
+        if (max_pages < 1 || max_seq_len < 1)
+            return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
+        const int rc = check_rows_aligned(p, q, 4, k_new, v_new, out);
+        if (rc != PKV_OK) return rc;
+    }
+    if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (batch == 0) return ok();
-    if (!q || !k_new || !v_new || !page_tables || !seq_lens || !out)
-        return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
-    if (max_pages < 1 || max_seq_len < 1)
-        return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages and max_seq_len must be >= 1");
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
     const int w = launch_workers(p->workers, batch, p->heads, attended_len(max_seq_len, p->window));

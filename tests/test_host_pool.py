@@ -121,6 +121,46 @@ def test_append_on_host_only_pool_reports_no_storage():
         assert st == pkv.PKV_ERR_NO_STORAGE
 
 
+def test_misaligned_tensors_rejected_before_device_work():
+    """q, k, v and out must start on a multiple of min(16, one head row's bytes):
+    the check runs on the host before anything else touches the pointers (fake
+    addresses here), and a rejected call leaves the pending token as it was."""
+    import ctypes
+    A = ctypes.c_void_p
+    with host_pool(head_dim=64, dtype="bf16") as p:       # rows: q/out 256 B, k/v 128 B
+        r = p.request()
+        r.begin_token()
+        aligned = [0x10000, 0x20000, 0x30000, 0x40000]
+        for i, off in [(0, 4), (1, 8), (2, 2), (3, 12)]:
+            ptrs = list(aligned)
+            ptrs[i] += off
+            st = pkv.lib.pkv_append_and_attend(r.handle, 0, *map(A, ptrs), None)
+            assert st == pkv.PKV_ERR_INVALID_ARGUMENT, (i, off)
+            assert b"multiple of min(16" in pkv.lib.pkv_last_error()
+        st = pkv.lib.pkv_append_and_attend(r.handle, 0, *map(A, aligned), None)
+        assert st == pkv.PKV_ERR_NO_STORAGE
+        r.abort_token()
+        assert r.length == 0
+        for off_q, off_out, want in [(4, 0, pkv.PKV_ERR_INVALID_ARGUMENT),
+                                     (0, 8, pkv.PKV_ERR_INVALID_ARGUMENT),
+                                     (0, 0, pkv.PKV_ERR_NO_STORAGE)]:
+            st = pkv.lib.pkv_paged_decode_attention(
+                p.handle, 0, 2, A(0x10000 + off_q), A(0x20000), A(0x30000), A(0x40000), 4,
+                A(0x50000), 20, A(0x60000 + off_out), A(0x70000), 1 << 20, None)
+            assert st == want, (off_q, off_out)
+    # 4-byte rows (fp32, head_dim 1 is not a pool shape; head_dim 2 -> 8-byte rows)
+    with host_pool(head_dim=2, dtype="f32") as p:
+        r = p.request()
+        r.begin_token()
+        st = pkv.lib.pkv_append_and_attend(r.handle, 0, A(0x10008), A(0x20008), A(0x30008),
+                                           A(0x40008), None)
+        assert st == pkv.PKV_ERR_NO_STORAGE                 # 8-byte rows need 8-byte alignment
+        st = pkv.lib.pkv_append_and_attend(r.handle, 0, A(0x10004), A(0x20000), A(0x30000),
+                                           A(0x40000), None)
+        assert st == pkv.PKV_ERR_INVALID_ARGUMENT
+        r.abort_token()
+
+
 def test_pool_destroy_refused_while_requests_live():
     p = host_pool()
     r = p.request()
