@@ -317,82 +317,134 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
             const int e_hi = full ? kKeys - 1
                                   : (int)(hi - k0 < kKeys - 1 ? (hi - k0 > -1 ? hi - k0 : -1)
                                                               : kKeys - 1);
-            // pass 1: row maximum, eight independent chains, 64 columns at a time
-            float m8[8];
+            // After a row block's first tile one pass usually does: the weights 2^(c s - c m)
+            // with the running m (packed FMA for the exponents, the row sum in two chains
+            // of packed adds, bf16 pairs for keys 2i, 2i+1 -> P column i), and the
+            // tile's row maximum in four chains.  They are kept when no row of the warp
+            // must raise m; else (and on the first tile) the warp takes the maximum, then
+            // the weights with the new m.
+            const float2 c2 = make_float2(c, c);
+            float mx = -INFINITY;
+            bool done = false;
+            if (j > 0) {
+                const float mb0 = m_used == -INFINITY ? 0.f : m_used * c;
+                const float2 nmb2 = make_float2(-mb0, -mb0);
+                float m4[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+                for (int k = 0; k < 4; ++k) m4[k] = -INFINITY;
+                float2 acc[2];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t sv[64];
-                tmem_ld32(t_s + hh * 64, sv);
-                tmem_ld32(t_s + hh * 64 + 32, sv + 32);
-                tmem_wait_ld();
-                if (!full) {
+                for (int k = 0; k < 2; ++k) acc[k] = make_float2(0.f, 0.f);
+                uint32_t w[64];
 #pragma unroll
-                    for (int e = 0; e < 64; ++e)
-                        if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
-                }
-#pragma unroll
-                for (int e = 0; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], __uint_as_float(sv[e]));
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            float alpha = 1.f;
-            if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f)) {
-                alpha = m_used == -INFINITY ? 0.f : ex2((m_used - mx) * c);
-                m_used = mx;
-                l *= alpha;
-            }
-            // S of this tile was committed after P V of the previous one, so that P V is
-            // complete: O may be rescaled
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t ov[32];
-                    tmem_ld32(t_o + cc * 32, ov);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t sv[64];
+                    tmem_ld32(t_s + hh * 64, sv);
+                    tmem_ld32(t_s + hh * 64 + 32, sv + 32);
                     tmem_wait_ld();
+                    if (!full) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    tmem_st32(t_o + cc * 32, ov);
+                        for (int e = 0; e < 64; ++e)
+                            if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[e]));
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        const float2 xe = __ffma2_rn(
+                            make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
+                        const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
+                        acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], pr);
+                        const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
+                        w[hh * 32 + (e >> 1)] = *reinterpret_cast<const uint32_t*>(&pb);
+                    }
+                }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                const bool raise = mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f);
+                if (!__any_sync(0xffffffffu, raise)) {
+                    tmem_st32(t_s, w);
+                    tmem_st32(t_s + 32, w + 32);
+                    tmem_wait_st();
+                    const float2 a = __fadd2_rn(acc[0], acc[1]);
+                    l += a.x + a.y;
+                    done = true;
+                }
+            } else {
+                // row maximum, four independent chains, 64 columns at a time
+                float m4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) m4[k] = -INFINITY;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t sv[64];
+                    tmem_ld32(t_s + hh * 64, sv);
+                    tmem_ld32(t_s + hh * 64 + 32, sv + 32);
+                    tmem_wait_ld();
+                    if (!full) {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e)
+                            if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[e]));
+                }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            }
+            if (!done) {
+                float alpha = 1.f;
+                if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f)) {
+                    alpha = m_used == -INFINITY ? 0.f : ex2((m_used - mx) * c);
+                    m_used = mx;
+                    l *= alpha;
+                }
+                // S of this tile was committed after P V of the previous one, so that P V
+                // is complete: O may be rescaled
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t ov[32];
+                        tmem_ld32(t_o + cc * 32, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(t_o + cc * 32, ov);
+                    }
+                    tmem_wait_st();
+                }
+                // the weights with the new m, P over the S columns already read
+                const float mb = m_used == -INFINITY ? 0.f : m_used * c;
+                const float2 nmb2 = make_float2(-mb, -mb);
+                float2 acc[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) acc[k] = make_float2(0.f, 0.f);
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t sv[64];
+                    tmem_ld32(t_s + hh * 64, sv);
+                    tmem_ld32(t_s + hh * 64 + 32, sv + 32);
+                    tmem_wait_ld();
+                    if (!full) {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e)
+                            if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
+                    }
+                    uint32_t w2[32];
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) {
+                        const float2 xe = __ffma2_rn(
+                            make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
+                        const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
+                        acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], pr);
+                        const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
+                        w2[e >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+                    }
+                    tmem_st32(t_s + hh * 32, w2);
                 }
                 tmem_wait_st();
+                const float2 a = __fadd2_rn(acc[0], acc[1]);
+                l += a.x + a.y;
             }
-            // pass 2: weights 2^(c s - c m), packed FMA for the exponents, the row sum in
-            // four chains of packed adds; bf16 pairs into TMEM over the S columns already
-            // read (keys 2i, 2i+1 -> column i)
-            const float mb = m_used == -INFINITY ? 0.f : m_used * c;
-            const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
-            float2 acc[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t sv[64];
-                tmem_ld32(t_s + hh * 64, sv);
-                tmem_ld32(t_s + hh * 64 + 32, sv + 32);
-                tmem_wait_ld();
-                if (!full) {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e)
-                        if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
-                }
-                uint32_t w[32];
-#pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const float2 xe = __ffma2_rn(
-                        make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
-                    const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
-                    acc[(e >> 1) & 3] = __fadd2_rn(acc[(e >> 1) & 3], pr);
-                    const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
-                    w[e >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-                }
-                tmem_st32(t_s + hh * 32, w);
-            }
-            tmem_wait_st();
-            const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
-            const float2 a = __fadd2_rn(a01, a23);
-            l += a.x + a.y;
             tc_fence_before();
             mbar_arrive(&p_full[x]);
         }
