@@ -81,7 +81,7 @@ typedef enum pkv_dtype {
                                    storage, so append/attend entry points return PKV_ERR_NO_STORAGE */
 
 #define PKV_POOL_CUDA_CORES 2u  /* use the CUDA-core kernel even where the tensor-core kernel
-                                   applies (bf16 storage, head_dim 64 or 128, 2, 4 or 8 query
+                                   applies (bf16 storage, head_dim 64 or 128, 2 or more query
                                    heads per KV head) */
 
 /* bits of the device error word */
@@ -158,16 +158,18 @@ int pkv_pool_options_init(pkv_pool_options* options);
 int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page_size, int dtype,
                     int64_t max_context, uint64_t seed, unsigned flags, pkv_pool** out);
 
-/* Create a pool from options (see pkv_pool_options).  Grouped-query pools
- * (query_heads = G x kv_heads) are implemented for G in {2, 4, 8} at head_dim 64
- * and 128 (else PKV_ERR_UNSUPPORTED, unless HOST_ONLY). */
+/* Create a pool from options (see pkv_pool_options).  Grouped-query and
+ * multi-query pools (query_heads = G x kv_heads) are implemented for G in
+ * {2, 4, 8, 16, 32, 64, 128} at head_dim 64 and 128 (else PKV_ERR_UNSUPPORTED,
+ * unless HOST_ONLY).  Decode runs a group above 8 as G / 8 lanes of 8 query heads
+ * per KV head, each lane reading the KV head's pages (the repeats mostly from L2). */
 int pkv_pool_create_ex(const pkv_pool_options* options, pkv_pool** out);
 
 /* KV heads stored per page and heads of the query (either pointer may be NULL). */
 int pkv_pool_heads(const pkv_pool* pool, int* kv_heads, int* query_heads);
 
 /* *tensor_cores = 1 if the pool's attention runs the tensor-core kernel (bf16,
- * head_dim 64 or 128, 2, 4 or 8 query heads per KV head, not
+ * head_dim 64 or 128, 2 or more query heads per KV head, not
  * PKV_POOL_CUDA_CORES), 0 for the CUDA-core kernel. */
 int pkv_pool_kernel(const pkv_pool* pool, int* tensor_cores);
 

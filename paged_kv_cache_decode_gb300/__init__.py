@@ -144,10 +144,13 @@ class Pool:
         return bool(v.value)
 
     def kernel_name(self) -> str:
+        """The decode split kernel this pool launches (groups above 8 query heads per KV
+        head run as lanes of 8)."""
+        g = min(self.query_heads // self.heads, 8)
         if self.tensor_cores:
-            return f"split_decode_mma_kernel<{self.head_dim},{self.query_heads // self.heads}>"
+            return f"split_decode_mma_kernel<{self.head_dim},{g}>"
         st = "f32" if self.dtype == PKV_F32 else "bf16"
-        return f"split_decode_kernel<{st},{self.head_dim},{self.query_heads // self.heads}>"
+        return f"split_decode_kernel<{st},{self.head_dim},{g}>"
 
     def bytes(self) -> int:
         b = ctypes.c_uint64()

@@ -155,6 +155,9 @@ struct KParams {
     int64_t single_t;
     int64_t max_seq_len;
     int B, H, P, tiles_per_page;
+    // lane head h reads KV head h >> kv_shift of the pool's H >> kv_shift: a pool with
+    // more than 8 query heads per KV head runs as 2^kv_shift lanes of 8 per KV head
+    int kv_shift;
     int64_t window;             // attend to the last `window` positions (0: all)
     float qscale;               // log2(e) / sqrt(D)
     float* out;
@@ -177,6 +180,16 @@ struct KParams {
 
 __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
+}
+
+// Row block [page][KV head hk] of the K / V pools, and row of k_new / v_new for KV
+// head hk of request b.  Lane head h of a request reads KV head h >> kv_shift.
+__device__ __forceinline__ int64_t kv_block(const KParams& p, int64_t page, int hk) {
+    return page * (p.H >> p.kv_shift) + hk;
+}
+
+__device__ __forceinline__ int64_t kv_new_row(const KParams& p, int b, int hk) {
+    return (int64_t)b * (p.H >> p.kv_shift) + hk;
 }
 
 // First position this kernel reads for a query at retained length t: the
@@ -263,14 +276,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
         if (in_smem) pre_s[p.B] = total;
     }
     __syncthreads();
-    const int64_t T = (int64_t)p.H * total;
+    // ranges partition the KV lanes' tiles; worker w takes range w >> kv_shift
+    const int Hk = p.H >> p.kv_shift, R = p.W >> p.kv_shift;
+    const int64_t T = (int64_t)Hk * total;
     const int64_t* pre = in_smem ? pre_s : p.req_prefix;
     for (int w = tid; w < p.W; w += kPlanThreads) {
-        const int64_t x = ((int64_t)w * T) / p.W;
-        int lo = 0, hi = p.B - 1;   // largest b with H * prefix[b] <= x
+        const int64_t x = ((int64_t)(w >> p.kv_shift) * T) / R;
+        int lo = 0, hi = p.B - 1;   // largest b with Hk * prefix[b] <= x
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)p.H * pre[mid] <= x) lo = mid; else hi = mid - 1;
+            if ((int64_t)Hk * pre[mid] <= x) lo = mid; else hi = mid - 1;
         }
         p.worker_req[w] = lo;
     }
@@ -278,16 +293,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
 
 // ---------------------------------------------------------- split kernel --
 
-// Position of a worker inside the flattened (request, head, tile) sequence,
+// Position of a worker inside the flattened (request, KV head, tile) sequence,
 // with the tile's page-table index and first slot tracked incrementally.
 struct Cursor {
-    int b, h;
+    int b, h;          // request, KV head
     int tile;          // tile within the lane (0 .. n-1)
     int n;             // tiles of this lane
     int tile0;         // position / 16 of the lane's tile 0 (the window's first tile)
     int page_idx;      // logical page of the tile
     int slot0;         // first slot of the tile within its page
-    int64_t first;     // flattened index of tile 0 of head 0 of request b
+    int64_t first;     // flattened index of tile 0 of KV head 0 of request b
 };
 
 // Page index and slot of the lane's tile `tile`.
@@ -306,7 +321,7 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
     }
     if (c.tile < c.n) return;
     c.tile = 0;
-    if (++c.h < p.H) {
+    if (++c.h < (p.H >> p.kv_shift)) {
         cursor_place(c, p);
         return;
     }
@@ -318,7 +333,7 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
         const int64_t nxt = req_prefix_at(p, c.b + 1);
         if (nxt > pre) {
             c.n = (int)(nxt - pre);
-            c.first = (int64_t)p.H * pre;
+            c.first = (int64_t)(p.H >> p.kv_shift) * pre;
             c.tile0 = (int)(window_start(p, seq_len_at(p, c.b)) / kTile);
             cursor_place(c, p);
             return;
@@ -333,23 +348,27 @@ __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t T, int W) {
     return ((x + 1) * W - 1) / T;
 }
 
-// Combine the partials of query g of KV lane `lane_id`, deposited by workers
-// w_lo..w_hi (those owning at least one tile) in slots lane_id + w, into out.
+// Combine the partials of query g of lane `lane_id` into out.  The lane's KV lane
+// K (request b, KV head hk: K = b * (H >> kv_shift) + hk) has its tiles in ranges
+// r_lo..r_hi (those owning at least one tile); sub-lane `sub` of range r wrote its
+// partial to slot ((K + r) << kv_shift) | sub.
 // One warp: lane j takes partials j, j + 32, ... for the maximum and the
 // weights 2^(m_w - M); the weighted sum of the o vectors then runs 32 partials
 // at a time with each weight broadcast by shuffle, so the loads of consecutive
 // partials are independent.  Partials are read from L2 (other SMs wrote them
 // during this kernel).
 template <int D, int DPL, int G>
-__device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, int g, int64_t w_lo,
-                                            int64_t w_hi, int64_t T_all, int lane) {
-    auto owns_tiles = [&](int64_t w) { return (w * T_all) / p.W != ((w + 1) * T_all) / p.W; };
-    const int cnt = (int)(w_hi - w_lo + 1);
-    const int64_t slot0 = lane_id + w_lo;
+__device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, int g, int64_t K,
+                                            int sub, int64_t r_lo, int64_t r_hi, int64_t T_all,
+                                            int lane) {
+    const int R = p.W >> p.kv_shift;
+    auto owns_tiles = [&](int64_t r) { return (r * T_all) / R != ((r + 1) * T_all) / R; };
+    auto slot_of = [&](int64_t r) { return ((K + r) << p.kv_shift) | sub; };
+    const int cnt = (int)(r_hi - r_lo + 1);
     const int64_t row = lane_id * G + g;                  // query row (request, query head)
     float M = -INFINITY;
     for (int j = lane; j < cnt; j += 32)
-        if (owns_tiles(w_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + j) * G + g]).x);
+        if (owns_tiles(r_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[slot_of(r_lo + j) * G + g]).x);
     for (int s = lane; s < p.pre_splits; s += 32) {
         const float2 ml = __ldcg(&p.pre_ml[s * p.pre_stride + row]);
         if (ml.y > 0.f) M = fmaxf(M, ml.x);
@@ -363,8 +382,8 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
     const bool has_features = lane * DPL < D;
     for (int base = 0; base < cnt; base += 32) {
         float wgt = 0.f;
-        if (base + lane < cnt && owns_tiles(w_lo + base + lane)) {
-            const float2 ml = __ldcg(&p.part_ml[(slot0 + base + lane) * G + g]);
+        if (base + lane < cnt && owns_tiles(r_lo + base + lane)) {
+            const float2 ml = __ldcg(&p.part_ml[slot_of(r_lo + base + lane) * G + g]);
             wgt = exp2f(ml.x - M);
             L = fmaf(ml.y, wgt, L);
         }
@@ -374,7 +393,7 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
             const float wj = __shfl_sync(0xffffffffu, wgt, j);
             if (has_features) {
                 // slots of workers that own no tile hold stale data: weight 0, value dropped
-                const float* op = p.part_o + ((slot0 + base + j) * G + g) * D + lane * DPL;
+                const float* op = p.part_o + (slot_of(r_lo + base + j) * G + g) * D + lane * DPL;
 #pragma unroll
                 for (int i = 0; i < DPL; ++i) {
                     const float v = __ldcg(op + i);
@@ -416,8 +435,8 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
     for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
 
-// Combine the partials of all G query rows of KV lane `lane_id` at once (G >= 2
-// dividing 32), deposited by workers w_lo..w_hi in slots lane_id + w, into out.
+// Combine the partials of all G query rows of lane `lane_id` at once (G >= 2
+// dividing 32) into out; slots as for merge_query.
 // For the maxima, sums and weights lane j takes worker slot j / G of a chunk of
 // 32 / G slots and query row j % G, so every row's max and sum reduce over the
 // lanes of one residue class mod G; for the o vectors lane j takes features
@@ -425,18 +444,19 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
 // whole group go out together: a few L2 round trips per lane instead of a few
 // per query row, which matters because the merging warp's ring waits meanwhile.
 template <int D, int G>
-__device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, int64_t w_lo,
-                                           int64_t w_hi, int64_t T_all, int lane) {
+__device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, int64_t K, int sub,
+                                           int64_t r_lo, int64_t r_hi, int64_t T_all, int lane) {
     static_assert(G >= 2 && 32 % G == 0 && D % 64 == 0, "grouped merge: G divides 32, D 64 or 128");
     constexpr int SPC = 32 / G;          // worker slots per chunk
     constexpr int DPL = D / 32;          // features per lane (2 or 4)
-    auto owns_tiles = [&](int64_t w) { return (w * T_all) / p.W != ((w + 1) * T_all) / p.W; };
-    const int cnt = (int)(w_hi - w_lo + 1);
-    const int64_t slot0 = lane_id + w_lo;
+    const int R = p.W >> p.kv_shift;
+    auto owns_tiles = [&](int64_t x) { return (x * T_all) / R != ((x + 1) * T_all) / R; };
+    auto slot_of = [&](int64_t x) { return ((K + x) << p.kv_shift) | sub; };
+    const int cnt = (int)(r_hi - r_lo + 1);
     const int r = lane % G;              // the query row this lane weighs
     float M = -INFINITY;
     for (int j = lane / G; j < cnt; j += SPC)
-        if (owns_tiles(w_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[(slot0 + j) * G + r]).x);
+        if (owns_tiles(r_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[slot_of(r_lo + j) * G + r]).x);
 #pragma unroll
     for (int off = 16; off >= G; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
@@ -448,15 +468,15 @@ __device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, in
     for (int base = 0; base < cnt; base += SPC) {
         const int j = base + lane / G;
         float wgt = 0.f;
-        if (j < cnt && owns_tiles(w_lo + j)) {
-            const float2 ml = __ldcg(&p.part_ml[(slot0 + j) * G + r]);
+        if (j < cnt && owns_tiles(r_lo + j)) {
+            const float2 ml = __ldcg(&p.part_ml[slot_of(r_lo + j) * G + r]);
             wgt = exp2f(ml.x - M);
             L = fmaf(ml.y, wgt, L);
         }
         const int nj = cnt - base < SPC ? cnt - base : SPC;
 #pragma unroll 1
         for (int jj = 0; jj < nj; ++jj) {
-            const float* op = p.part_o + (slot0 + base + jj) * G * D + lane * DPL;
+            const float* op = p.part_o + slot_of(r_lo + base + jj) * G * D + lane * DPL;
             float v[G][DPL];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -503,13 +523,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const KParams p) {
     const int64_t lane_id = qrow / G;
     const int g = (int)(qrow - lane_id * G);
     const int b = (int)(lane_id / p.H), h = (int)(lane_id - (int64_t)b * p.H);
+    const int hk = h >> p.kv_shift, sub = h & ((1 << p.kv_shift) - 1);
+    const int Hk = p.H >> p.kv_shift, R = p.W >> p.kv_shift;
     const int64_t pre_b = req_prefix_at(p, b);
     const int64_t n = req_prefix_at(p, b + 1) - pre_b;    // 0 for a request the plan rejected
     if (n <= 0) return;
-    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
-    const int64_t A = (int64_t)p.H * pre_b + (int64_t)h * n;
-    merge_query<D, DPL, G>(p, lane_id, g, worker_of(A, T_all, p.W), worker_of(A + n - 1, T_all, p.W),
-                           T_all, lane);
+    const int64_t T_all = (int64_t)Hk * req_prefix_at(p, p.B);
+    const int64_t A = (int64_t)Hk * pre_b + (int64_t)hk * n;
+    merge_query<D, DPL, G>(p, lane_id, g, (int64_t)b * Hk + hk, sub, worker_of(A, T_all, R),
+                           worker_of(A + n - 1, T_all, R), T_all, lane);
 }
 
 // One worker (warp) of the split kernel.  A lane here is a (request, KV head)
@@ -549,10 +571,13 @@ split_decode_kernel(const KParams p) {
         plan_seen = true;
     }
 
-    // this worker's tiles: [begin, end) of the flattened sequence
-    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
-    const int64_t begin = (w * T_all) / p.W;
-    const int64_t end = ((w + 1) * T_all) / p.W;
+    // this worker's tiles: range w >> kv_shift, [begin, end) of the flattened (request,
+    // KV head, tile) sequence, for sub-lane w & (2^kv_shift - 1) of every KV head in it
+    const int sub = (int)(w & ((1 << p.kv_shift) - 1));
+    const int Hk = p.H >> p.kv_shift, R = p.W >> p.kv_shift;
+    const int64_t T_all = (int64_t)Hk * req_prefix_at(p, p.B);
+    const int64_t begin = ((w >> p.kv_shift) * T_all) / R;
+    const int64_t end = (((w >> p.kv_shift) + 1) * T_all) / R;
     const int n_work = (int)(end - begin);
     if (n_work <= 0) return;
 
@@ -562,7 +587,7 @@ split_decode_kernel(const KParams p) {
         const int64_t pre = req_prefix_at(p, b0);
         cur.b = b0;
         cur.n = (int)(req_prefix_at(p, b0 + 1) - pre);
-        cur.first = (int64_t)p.H * pre;
+        cur.first = (int64_t)Hk * pre;
         const int64_t local = begin - cur.first;
         cur.h = (int)(local / cur.n);
         cur.tile = (int)(local % cur.n);
@@ -592,7 +617,7 @@ split_decode_kernel(const KParams p) {
             mbar_arrive(&bars[s]);
             return;
         }
-        const int64_t off = (((int64_t)page * p.H + prod.h) * p.P + prod.slot0) * D;
+        const int64_t off = (kv_block(p, page, prod.h) * p.P + prod.slot0) * D;
         unsigned char* dst = ring + s * Gm::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[s], Gm::STAGE_BYTES);
         bulk_copy_g2s(dst, static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES, &bars[s], policy);
@@ -619,7 +644,7 @@ split_decode_kernel(const KParams p) {
     uint32_t parity = 0;
 
     for (int k = 0; k < n_work; ++k) {
-        const int64_t lane_id = (int64_t)cur.b * p.H + cur.h;
+        const int64_t lane_id = (int64_t)cur.b * p.H + ((cur.h << p.kv_shift) | sub);
 
         if (k == 0 || cur.tile == 0) {   // a new lane piece starts
             piece_first = cur.tile;
@@ -670,13 +695,12 @@ split_decode_kernel(const KParams p) {
             // fused append: row t_b - 1 comes from k_new / v_new, into the tile and the page
             const int r = rows - 1;
             if (lane < Gm::TPR) {
-                const int64_t src = lane_id * D + col;
+                const int64_t src = kv_new_row(p, cur.b, cur.h) * D + col;
                 const VT kb = *reinterpret_cast<const VT*>(static_cast<const T*>(p.k_new) + src);
                 const VT vb = *reinterpret_cast<const VT*>(static_cast<const T*>(p.v_new) + src);
                 *reinterpret_cast<VT*>(Ks + r * D + col) = kb;
                 *reinterpret_cast<VT*>(Vs + r * D + col) = vb;
-                const int64_t dst =
-                    (((int64_t)page * p.H + cur.h) * p.P + cur.slot0 + r) * D + col;
+                const int64_t dst = (kv_block(p, page, cur.h) * p.P + cur.slot0 + r) * D + col;
                 *reinterpret_cast<VT*>(static_cast<T*>(p.k_pages) + dst) = kb;
                 *reinterpret_cast<VT*>(static_cast<T*>(p.v_pages) + dst) = vb;
             }
@@ -805,7 +829,8 @@ split_decode_kernel(const KParams p) {
                 }
             } else {
                 // deposit the partial; the last of the lane's workers to arrive merges
-                const int64_t slot = lane_id + w;
+                const int64_t slot =      // partial of KV lane K from range r, this sub-lane
+                    ((((int64_t)cur.b * Hk + cur.h) + (w >> p.kv_shift)) << p.kv_shift) | sub;
                 if (lane < Gm::TPR) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -824,16 +849,16 @@ split_decode_kernel(const KParams p) {
                     cursor_advance(cur, p);
                     continue;
                 }
-                const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // lane's first tile
-                const int64_t w_lo = worker_of(A, T_all, p.W);
-                const int64_t w_hi = worker_of(A + cur.n - 1, T_all, p.W);
+                const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // KV lane's first tile
+                const int64_t r_lo = worker_of(A, T_all, R);
+                const int64_t r_hi = worker_of(A + cur.n - 1, T_all, R);
                 int need;
-                if (T_all >= p.W) {
-                    need = (int)(w_hi - w_lo + 1);   // no worker is empty
+                if (T_all >= R) {
+                    need = (int)(r_hi - r_lo + 1);   // no range is empty
                 } else {
                     int c = 0;
-                    for (int64_t x = w_lo + lane; x <= w_hi; x += 32)
-                        c += (x * T_all) / p.W != ((x + 1) * T_all) / p.W;
+                    for (int64_t x = r_lo + lane; x <= r_hi; x += 32)
+                        c += (x * T_all) / R != ((x + 1) * T_all) / R;
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
                     need = c;
@@ -857,10 +882,11 @@ split_decode_kernel(const KParams p) {
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
                     __threadfence();
+                    const int64_t K = (int64_t)cur.b * Hk + cur.h;
                     if constexpr (G == 1)
-                        merge_query<D, Gm::DPL, G>(p, lane_id, 0, w_lo, w_hi, T_all, lane);
+                        merge_query<D, Gm::DPL, G>(p, lane_id, 0, K, sub, r_lo, r_hi, T_all, lane);
                     else
-                        merge_lane<D, G>(p, lane_id, w_lo, w_hi, T_all, lane);
+                        merge_lane<D, G>(p, lane_id, K, sub, r_lo, r_hi, T_all, lane);
                 }
                 __syncwarp();
             }
@@ -983,9 +1009,13 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         plan_seen = true;
     }
 
-    const int64_t T_all = (int64_t)p.H * req_prefix_at(p, p.B);
-    const int64_t begin = (w * T_all) / p.W;
-    const int64_t end = ((w + 1) * T_all) / p.W;
+    // this worker's tiles: range w >> kv_shift, [begin, end) of the flattened (request,
+    // KV head, tile) sequence, for sub-lane w & (2^kv_shift - 1) of every KV head in it
+    const int sub = (int)(w & ((1 << p.kv_shift) - 1));
+    const int Hk = p.H >> p.kv_shift, R = p.W >> p.kv_shift;
+    const int64_t T_all = (int64_t)Hk * req_prefix_at(p, p.B);
+    const int64_t begin = ((w >> p.kv_shift) * T_all) / R;
+    const int64_t end = (((w >> p.kv_shift) + 1) * T_all) / R;
     const int n_work = (int)(end - begin);
     if (n_work <= 0) return;
 
@@ -995,7 +1025,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         const int64_t pre = req_prefix_at(p, b0);
         cur.b = b0;
         cur.n = (int)(req_prefix_at(p, b0 + 1) - pre);
-        cur.first = (int64_t)p.H * pre;
+        cur.first = (int64_t)Hk * pre;
         const int64_t local = begin - cur.first;
         cur.h = (int)(local / cur.n);
         cur.tile = (int)(local % cur.n);
@@ -1025,7 +1055,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             mbar_arrive(&bars[s]);
             return;
         }
-        const int y = (int)(((int64_t)page * p.H + prod.h) * p.P + prod.slot0);   // pool row
+        const int y = (int)(kv_block(p, page, prod.h) * p.P + prod.slot0);   // pool row
         unsigned char* dst = ring + s * M::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[s], M::STAGE_BYTES);
 #pragma unroll
@@ -1054,7 +1084,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     uint32_t parity = 0;
 
     for (int k = 0; k < n_work; ++k) {
-        const int64_t lane_id = (int64_t)cur.b * p.H + cur.h;
+        const int64_t lane_id = (int64_t)cur.b * p.H + ((cur.h << p.kv_shift) | sub);
 
         if (k == 0 || cur.tile == 0) {   // a new lane piece starts
             piece_first = cur.tile;
@@ -1110,14 +1140,14 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             // rows past it (stale bytes, possibly not finite) are cleared in V
             const int r = rows - 1;
             if (lane < D / 8) {
-                const int64_t src = lane_id * D + lane * 8;
+                const int64_t src = kv_new_row(p, cur.b, cur.h) * D + lane * 8;
                 const uint4 kb = *reinterpret_cast<const uint4*>(
                     static_cast<const __nv_bfloat16*>(p.k_new) + src);
                 const uint4 vb = *reinterpret_cast<const uint4*>(
                     static_cast<const __nv_bfloat16*>(p.v_new) + src);
                 *reinterpret_cast<uint4*>(Ks + swz(r, lane)) = kb;
                 *reinterpret_cast<uint4*>(Vs + swz(r, lane)) = vb;
-                const int64_t dst = (((int64_t)page * p.H + cur.h) * p.P + cur.slot0 + r) * D + lane * 8;
+                const int64_t dst = (kv_block(p, page, cur.h) * p.P + cur.slot0 + r) * D + lane * 8;
                 *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.k_pages) + dst) = kb;
                 *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.v_pages) + dst) = vb;
             }
@@ -1212,7 +1242,8 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                             make_float2((o[nb][0] + o[nb][2]) * inv, (o[nb][1] + o[nb][3]) * inv);
                 }
             } else {
-                const int64_t slot = lane_id + w;
+                const int64_t slot =      // partial of KV lane K from range r, this sub-lane
+                    ((((int64_t)cur.b * Hk + cur.h) + (w >> p.kv_shift)) << p.kv_shift) | sub;
                 if (q_ok) {
                     float* op = p.part_o + (slot * G + g) * D + 2 * t;
 #pragma unroll
@@ -1227,16 +1258,16 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                     cursor_advance(cur, p);
                     continue;
                 }
-                const int64_t A = cur.first + (int64_t)cur.h * cur.n;
-                const int64_t w_lo = worker_of(A, T_all, p.W);
-                const int64_t w_hi = worker_of(A + cur.n - 1, T_all, p.W);
+                const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // KV lane's first tile
+                const int64_t r_lo = worker_of(A, T_all, R);
+                const int64_t r_hi = worker_of(A + cur.n - 1, T_all, R);
                 int need;
-                if (T_all >= p.W) {
-                    need = (int)(w_hi - w_lo + 1);
+                if (T_all >= R) {
+                    need = (int)(r_hi - r_lo + 1);   // no range is empty
                 } else {
                     int c = 0;
-                    for (int64_t x = w_lo + lane; x <= w_hi; x += 32)
-                        c += (x * T_all) / p.W != ((x + 1) * T_all) / p.W;
+                    for (int64_t x = r_lo + lane; x <= r_hi; x += 32)
+                        c += (x * T_all) / R != ((x + 1) * T_all) / R;
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
                     need = c;
@@ -1256,7 +1287,8 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
                     __threadfence();
-                    merge_lane<D, G>(p, lane_id, w_lo, w_hi, T_all, lane);
+                    merge_lane<D, G>(p, lane_id, (int64_t)cur.b * Hk + cur.h, sub, r_lo, r_hi,
+                                     T_all, lane);
                 }
                 __syncwarp();
             }
@@ -1293,10 +1325,13 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G) {
 #define PKV_MIN_TILES_PER_WORKER 4   // below this much work a worker's fixed costs dominate
 #endif
 
-int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len) {
+int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len, int kv_shift) {
     const int64_t tiles = (int64_t)B * H * ((max_seq_len + kTile - 1) / kTile);
     const int64_t want = (tiles + PKV_MIN_TILES_PER_WORKER - 1) / PKV_MIN_TILES_PER_WORKER;
-    return (int)(want < pool_workers ? (want < 1 ? 1 : want) : pool_workers);
+    const int w = (int)(want < pool_workers ? (want < 1 ? 1 : want) : pool_workers);
+    // one worker per sub-lane of each range: a multiple of 2^kv_shift
+    const int ns = 1 << kv_shift;
+    return w < ns ? ns : w / ns * ns;
 }
 
 template <typename T, int D, int G>
@@ -1469,6 +1504,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.max_seq_len = a.max_seq_len;
     p.B = a.B;
     p.H = a.H;
+    p.kv_shift = a.kv_shift;
     p.P = a.P;
     p.tiles_per_page = a.P / kTile;
     p.window = a.window;

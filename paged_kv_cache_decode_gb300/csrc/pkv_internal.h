@@ -22,8 +22,10 @@ constexpr int kSplitWarps = PKV_SPLIT_WARPS;
 // One launch of the decode path for one layer.
 struct DecodeArgs {
     int dtype;               // PKV_F32 / PKV_BF16
-    int B, H, D, P;          // requests, KV heads, head width, page size (multiple of kTile)
-    int G;                   // query heads per KV head (1: multi-head attention)
+    int B, H, D, P;          // requests, lane heads (KV heads << kv_shift), head width, page size
+    int G;                   // query heads per lane (1: multi-head attention; at most 8)
+    int kv_shift;            // lane head h reads KV head h >> kv_shift; H counts lanes, so
+                             // more than 8 query heads per KV head run as 2^kv_shift lanes
     int64_t window;          // attend to the last `window` positions (0: the whole prefix)
     const float* q;          // [B][H*G][D]
     const void* k_new;       // [B][H][D] storage dtype
@@ -79,7 +81,7 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G);
 
 // Workers one launch uses: the pool's resident worker count, capped by the
 // number of tiles the launch can hold (B * H * ceil(max_seq_len / kTile)).
-int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len);
+int launch_workers(int pool_workers, int B, int H, int64_t max_seq_len, int kv_shift);
 
 // Longest stretch of positions one query reads: max_seq_len, or with a
 // sliding window the window plus one partial tile.

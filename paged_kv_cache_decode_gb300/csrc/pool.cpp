@@ -65,6 +65,9 @@ struct SplitMix64 {
 struct pkv_pool {
     int layers = 0, heads = 0, head_dim = 0, page_size = 0, dtype = 0;
     int query_heads = 0, group = 1;    // query heads = group x KV heads (grouped-query attention)
+    // decode runs on lanes of at most 8 query heads: a group of 16 .. 128 (multi-query
+    // layouts) is 2^kv_shift lanes of 8 per KV head, dec_heads = heads << kv_shift
+    int dec_heads = 0, dec_group = 1, kv_shift = 0;
     int64_t window = 0;                // sliding window in positions (0: whole prefix)
     int64_t pages = 0, max_context = 0, max_pages_per_request = 0;
     bool host_only = false;
@@ -291,11 +294,14 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
         if (page_size % pkv::kTile != 0)
             return fail(PKV_ERR_UNSUPPORTED, "page_size %d is not a multiple of %d", page_size,
                         pkv::kTile);
-        if (!pkv::decode_supported(dtype, head_dim, query_heads / heads))
+        const int g = query_heads / heads;
+        const bool group_ok = g <= 8 || (g <= 128 && (g & (g - 1)) == 0);
+        if (!group_ok || !pkv::decode_supported(dtype, head_dim, g <= 8 ? g : 8))
             return fail(PKV_ERR_UNSUPPORTED,
                         "head_dim %d with %d query heads per KV head not implemented (powers of "
-                        "two, 2..128 fp32, 2..256 bf16; groups of 2, 4, 8 at head_dim 64, 128)",
-                        head_dim, query_heads / heads);
+                        "two, 2..128 fp32, 2..256 bf16; groups of 2, 4, ..., 128 at head_dim 64, "
+                        "128)",
+                        head_dim, g);
     }
 
     pkv_pool* p = new (std::nothrow) pkv_pool;
@@ -304,6 +310,9 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
     p->heads = heads;
     p->query_heads = query_heads;
     p->group = query_heads / heads;
+    p->dec_group = p->group <= 8 ? p->group : 8;
+    while ((p->dec_group << p->kv_shift) < p->group) ++p->kv_shift;
+    p->dec_heads = heads << p->kv_shift;
     p->window = opts->window;
     p->head_dim = head_dim;
     p->page_size = page_size;
@@ -337,8 +346,8 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
         p->tmaps = dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) && rows < INT32_MAX &&
                    tensor_map_encoder() != nullptr;
         p->tensor_cores = p->tmaps && !(flags & PKV_POOL_CUDA_CORES) &&
-                          pkv::mma_supported(dtype, head_dim, p->group);
-        p->workers = pkv::resident_workers(dtype, head_dim, p->group, sms, p->tensor_cores);
+                          pkv::mma_supported(dtype, head_dim, p->dec_group);
+        p->workers = pkv::resident_workers(dtype, head_dim, p->dec_group, sms, p->tensor_cores);
         if (p->workers <= 0) {
             delete p;
             return fail(PKV_ERR_CUDA, "split kernel cannot be resident on this device");
@@ -463,9 +472,9 @@ int pkv_request_create(pkv_pool* p, pkv_request** out) {
             return rc;
         }
         r->workspace_workers =
-            pkv::launch_workers(p->workers, 1, p->heads, pkv::attended_len(p->max_context, p->window));
+            pkv::launch_workers(p->workers, 1, p->dec_heads, pkv::attended_len(p->max_context, p->window), p->kv_shift);
         r->workspace_bytes =
-            pkv::workspace_layout(1, p->heads, p->head_dim, r->workspace_workers, p->group).total;
+            pkv::workspace_layout(1, p->dec_heads, p->head_dim, r->workspace_workers, p->dec_group).total;
         if (p->tmaps && pkv::prefill_supported(p->dtype, p->head_dim, p->group))
             r->prefill_ws_bytes = pkv::prefill_workspace_bytes(1, p->group, p->max_context);
         cudaError_t e = cudaMalloc(&r->dev_table, sizeof(int32_t) * (size_t)p->max_pages_per_request);
@@ -679,8 +688,9 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     pkv::DecodeArgs a{};
     a.dtype = p->dtype;
     a.B = 1;
-    a.H = p->heads;
-    a.G = p->group;
+    a.H = p->dec_heads;
+    a.G = p->dec_group;
+    a.kv_shift = p->kv_shift;
     a.window = p->window;
     a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
     a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
@@ -702,7 +712,7 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.out = out;
     a.workspace = r->dev_workspace;
     a.workspace_bytes = r->workspace_bytes;
-    a.workers = pkv::launch_workers(r->workspace_workers, 1, p->heads, pkv::attended_len(r->position + 1, p->window));
+    a.workers = pkv::launch_workers(r->workspace_workers, 1, p->dec_heads, pkv::attended_len(r->position + 1, p->window), p->kv_shift);
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
@@ -843,8 +853,8 @@ int pkv_workspace_size(const pkv_pool* p, int batch, int64_t max_seq_len, size_t
     if (!p || !bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL argument");
     if (batch < 0 || max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "bad batch or length");
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
-    const int w = pkv::launch_workers(p->workers, batch, p->heads, pkv::attended_len(max_seq_len, p->window));
-    *bytes = pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
+    const int w = pkv::launch_workers(p->workers, batch, p->dec_heads, pkv::attended_len(max_seq_len, p->window), p->kv_shift);
+    *bytes = pkv::workspace_layout(batch, p->dec_heads, p->head_dim, w, p->dec_group).total;
     return ok();
 }
 
@@ -867,8 +877,8 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     }
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (batch == 0) return ok();
-    const int w = pkv::launch_workers(p->workers, batch, p->heads, pkv::attended_len(max_seq_len, p->window));
-    const size_t need = pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
+    const int w = pkv::launch_workers(p->workers, batch, p->dec_heads, pkv::attended_len(max_seq_len, p->window), p->kv_shift);
+    const size_t need = pkv::workspace_layout(batch, p->dec_heads, p->head_dim, w, p->dec_group).total;
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
                     need);
@@ -877,8 +887,9 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     pkv::DecodeArgs a{};
     a.dtype = p->dtype;
     a.B = batch;
-    a.H = p->heads;
-    a.G = p->group;
+    a.H = p->dec_heads;
+    a.G = p->dec_group;
+    a.kv_shift = p->kv_shift;
     a.window = p->window;
     a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
     a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
@@ -995,9 +1006,9 @@ struct SharedLayout {
 
 SharedLayout shared_layout(const pkv_pool* p, int batch, int64_t max_seq_len, int64_t shared_len) {
     SharedLayout L{};
-    const int w = pkv::launch_workers(p->workers, batch, p->heads,
-                                      pkv::attended_len(max_seq_len, p->window));
-    L.decode = (pkv::workspace_layout(batch, p->heads, p->head_dim, w, p->group).total + 255) /
+    const int w = pkv::launch_workers(p->workers, batch, p->dec_heads,
+                                      pkv::attended_len(max_seq_len, p->window), p->kv_shift);
+    L.decode = (pkv::workspace_layout(batch, p->dec_heads, p->head_dim, w, p->dec_group).total + 255) /
                256 * 256;
     L.plan = pkv::shared_prefix_plan(batch, p->heads, p->group, shared_len, p->sms);
     const size_t rows = (size_t)L.plan.splits * batch * p->query_heads;
@@ -1161,12 +1172,13 @@ int prepare_batched(pkv_pool* p, int layer, int batch, const float* q, const voi
     if (batch == 0) return ok();
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
-    const int w = launch_workers(p->workers, batch, p->heads, attended_len(max_seq_len, p->window));
-    *workspace_bytes = workspace_layout(batch, p->heads, p->head_dim, w, p->group).total;
+    const int w = launch_workers(p->workers, batch, p->dec_heads, attended_len(max_seq_len, p->window), p->kv_shift);
+    *workspace_bytes = workspace_layout(batch, p->dec_heads, p->head_dim, w, p->dec_group).total;
     a->dtype = p->dtype;
     a->B = batch;
-    a->H = p->heads;
-    a->G = p->group;
+    a->H = p->dec_heads;
+    a->G = p->dec_group;
+    a->kv_shift = p->kv_shift;
     a->window = p->window;
     a->tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
     a->tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;

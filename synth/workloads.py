@@ -175,6 +175,7 @@ REGISTRY = {
     "gqa8_bf16": lambda: gqa(8, BF16),
     "gqa4_bf16": lambda: gqa(4, BF16),
     "gqa8_f32": lambda: gqa(8, F32),
+    "gqa16_bf16": lambda: gqa(16, BF16),
     "window_bf16": sliding_window,
     "prefix_bf16": shared_prompt,
     "prefill_bf16": chunked_prefill,

@@ -322,6 +322,43 @@ def test_gqa_geometry_errors():
     assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
 
 
+# --------------------------------------------------------------- multi-query --
+# 16 .. 128 query heads per KV head (down to a single KV head): decode runs them as
+# lanes of 8 query heads, 2^s lanes per KV head, each reading the KV head's pages.
+
+@pytest.mark.parametrize("group,H,D,dtype,cc", [(16, 2, 128, BF16, False), (32, 1, 128, BF16, False),
+                                                (64, 1, 64, BF16, False), (128, 1, 128, BF16, False),
+                                                (16, 2, 64, F32, False), (32, 2, 128, F32, False),
+                                                (16, 2, 128, BF16, True)])
+def test_mqa_batched(group, H, D, dtype, cc):
+    lens = [1, 16, 17, 300, 1000, 33, 2048, 5]
+    _batched_check(make_workload(f"mqa{group}", lens, H, D, dtype=dtype, seed=80 + group,
+                                 group=group), cuda_cores=cc)
+
+
+def test_mqa_window_and_few_tiles():
+    _batched_check(make_workload("mqawin", [1, 2, 40, 129, 700, 3000], 2, 128, dtype=BF16,
+                                 seed=93, group=16, window=200))
+    _batched_check(make_workload("mqa_few", [40, 3], 1, 128, dtype=BF16, seed=94, group=32,
+                                 max_context=8192), max_seq_len=8192)
+
+
+def test_mqa_serial_with_abort():
+    c, _ = _serial(2, 2, 128, BF16, 64, 200, 40, 7, abort_at=17, group=16)
+    assert c["score_cells"] == 2 * 32 * sum(range(1, 41))
+    _serial(2, 1, 64, F32, 64, 200, 30, 8, abort_at=9, group=32)
+
+
+def test_mqa_geometry():
+    for g in (16, 32, 64, 128):
+        with pkv.Pool(1, 8, 1, 128, 16, "bf16", 64, query_heads=g) as p:
+            assert p.query_heads == g and p.tensor_cores
+    for g in (12, 24, 256):
+        with pytest.raises(pkv.PkvError) as e:
+            pkv.Pool(1, 8, 1, 128, 16, "bf16", 64, query_heads=g)
+        assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+
+
 # ---------------------------------------- tensor-core and CUDA-core kernels --
 # bf16 grouped-query pools at head width 64 or 128 run the tensor-core kernel by
 # default; PKV_POOL_CUDA_CORES selects the CUDA-core kernel for the same geometry.

@@ -41,6 +41,10 @@ CASES = {
     "d64_mha_long": ([2000], [130], 1, 64, 1, 16, 0),
     "empty_request": ([10, 5, 0], [0, 20, 0], 2, 128, 2, 16, 0),
     "d64_gqa8_window_ragged": ([0, 3, 700], [129, 255, 1], 2, 64, 8, 64, 33),
+    # multi-query: a query tile is 128/G tokens x G heads
+    "d128_mqa16": ([0, 45, 333], [70, 9, 130], 2, 128, 16, 16, 0),
+    "d128_mqa32_window": ([100, 7], [41, 64], 1, 128, 32, 16, 50),
+    "d64_mqa64": ([20], [23], 1, 64, 64, 16, 0),
 }
 
 

@@ -45,6 +45,8 @@ CASES = {
     "g8_d128_many_rows": (40, 144, 300, 1, 128, 8, 0),
     "g2_d64_window": (7, 512, 90, 2, 64, 2, 200),
     "g4_d128_short_prefix": (3, 16, 17, 2, 128, 4, 0),
+    "g16_d128_mqa": (9, 192, 60, 2, 128, 16, 0),
+    "g32_d64_mqa_window": (5, 128, 70, 1, 64, 32, 90),
 }
 
 
