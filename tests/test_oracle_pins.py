@@ -344,7 +344,7 @@ def gqa_case(group=2, H=2, D=8, dtype=F32, lens=(23, 5, 40), seed=14):
             np.ascontiguousarray(rep(case.v_new, 1)))
 
 
-@pytest.mark.parametrize("group,dtype", [(2, F32), (4, BF16), (8, F32)])
+@pytest.mark.parametrize("group,dtype", [(2, F32), (4, BF16), (8, F32), (16, BF16), (32, F32)])
 def test_gqa_equals_mha_on_repeated_kv_heads(group, dtype):
     case, q, g, kp_rep, vp_rep, knew_rep, vnew_rep = gqa_case(group, dtype=dtype)
     kp, vp = case.k_pool.copy(), case.v_pool.copy()
