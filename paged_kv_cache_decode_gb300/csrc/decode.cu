@@ -563,13 +563,13 @@ split_decode_kernel(const KParams p) {
 
     // The plan kernel's prefix and worker table are needed now for a batch.  A
     // single request's partition is closed-form and its lane counters carry an
-    // epoch, so it runs without a plan kernel.
+    // epoch, so it runs without a plan kernel; it is launched as a dependent of
+    // whatever came before (the previous layer's call) and lets the next call's
+    // kernel launch at once.  Either way nothing global is read before the
+    // previous grid is complete, so every earlier write is visible.
     const bool batched = p.seq_lens != nullptr;
-    bool plan_seen = false;
-    if (batched) {
-        pdl_wait_primary();
-        plan_seen = true;
-    }
+    if (!batched) pdl_launch_dependents();
+    pdl_wait_primary();
 
     // this worker's tiles: range w >> kv_shift, [begin, end) of the flattened (request,
     // KV head, tile) sequence, for sub-lane w & (2^kv_shift - 1) of every KV head in it
@@ -866,10 +866,6 @@ split_decode_kernel(const KParams p) {
                 int arrived = 0;
                 if (p.epoch == 0) {
                     // counters zeroed by the plan kernel of this call
-                    if (!plan_seen) {
-                        pdl_wait_primary();
-                        plan_seen = true;
-                    }
                     if (lane == 0) arrived = (int)atomicAdd(&p.lane_cnt[lane_id], 1ull) + 1;
                 } else if (lane == 0) {
                     // counter = epoch << 32 | count, epochs increasing from call to
@@ -1002,12 +998,9 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     __syncwarp();
     const uint64_t policy = l2_stream_policy();
 
-    const bool batched = p.seq_lens != nullptr;
-    bool plan_seen = false;
-    if (batched) {
-        pdl_wait_primary();
-        plan_seen = true;
-    }
+    const bool batched = p.seq_lens != nullptr;   // as in the CUDA-core kernel
+    if (!batched) pdl_launch_dependents();
+    pdl_wait_primary();
 
     // this worker's tiles: range w >> kv_shift, [begin, end) of the flattened (request,
     // KV head, tile) sequence, for sub-lane w & (2^kv_shift - 1) of every KV head in it
@@ -1274,10 +1267,6 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 }
                 int arrived = 0;
                 if (p.epoch == 0) {
-                    if (!plan_seen) {
-                        pdl_wait_primary();
-                        plan_seen = true;
-                    }
                     if (lane == 0) arrived = (int)atomicAdd(&p.lane_cnt[lane_id], 1ull) + 1;
                 } else if (lane == 0) {
                     unsigned long long* c = &p.lane_cnt[lane_id];
@@ -1373,13 +1362,13 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     cfg.blockDim = dim3(Gm::WARPS * 32);
     cfg.dynamicSmemBytes = Gm::CTA_SMEM;
     cfg.stream = stream;
-    // dependent launch only behind this call's own plan kernel; with epoch
-    // counters the kernel follows whatever came before in plain stream order
+    // dependent launch: behind this call's own plan kernel, or (a single request)
+    // behind whatever came before; the kernel waits for it before reading anything
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = p.epoch == 0 ? 1 : 0;
+    cfg.numAttrs = 1;
     if ((e = cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G>, p)) != cudaSuccess) return e;
     if (p.pre_ml != nullptr) {
         const int64_t rows = (int64_t)p.B * p.H * G;
@@ -1436,7 +1425,7 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = p.epoch == 0 ? 1 : 0;
+    cfg.numAttrs = 1;
     if ((e = cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<D, G>, p, tmk, tmv)) != cudaSuccess)
         return e;
     if (p.pre_ml != nullptr) {
