@@ -286,10 +286,9 @@ int pkv_append_and_attend(pkv_request* req, int layer, const float* q, const voi
  * another request also references among those the chunk writes (ascending
  * logical index; copy-on-write), then the pages the request does not hold yet.
  * All or nothing: BAD_STATE if a token or chunk is pending; CAPACITY_EXCEEDED
- * if length + n passes max_context; OUT_OF_PAGES if too few pages are free;
- * UNSUPPORTED on a device pool that pkv_paged_prefill does not take (host-only
- * pools keep the bookkeeping).  Then pkv_prefill_chunk once per layer and
- * pkv_commit_token or pkv_abort_token.
+ * if length + n passes max_context; OUT_OF_PAGES if too few pages are free.
+ * Then pkv_prefill_chunk once per layer and pkv_commit_token or
+ * pkv_abort_token.
  */
 int pkv_begin_chunk(pkv_request* req, int64_t n, int64_t* position);
 
@@ -298,15 +297,18 @@ int pkv_begin_chunk(pkv_request* req, int64_t n, int64_t* position);
  * positions position .. position+n-1 of `layer`'s pools and attend each of its
  * queries causally, as pkv_paged_prefill does for one request (chunk token i
  * over positions 0 .. position+i, the window applied).
- *   q   [n][query_heads][head_dim] bf16, device
- *   k,v [n][kv_heads][head_dim] bf16, device
+ *   q   [n][query_heads][head_dim] storage dtype, device
+ *   k,v [n][kv_heads][head_dim] storage dtype, device
  *   out [n][query_heads][head_dim] fp32, device
  * Call once per layer per pending chunk; BAD_STATE if no chunk is pending (a
  * pending single token takes pkv_append_and_attend) or the layer already ran.
  * The rows are written at once but are visible to later tokens only after
  * pkv_commit_token.  Enqueues a page-table upload of the changed entries, one
- * device-to-device copy per copy-on-write page and the three prefill kernels on
- * `stream`; returns without waiting.
+ * device-to-device copy per copy-on-write page and the prefill kernels on
+ * `stream`; returns without waiting.  Pools pkv_paged_prefill serves through
+ * decode lanes keep a per-request scratch that grows to the largest chunk: a
+ * chunk larger than any before frees and reallocates it, which waits for the
+ * device (OUT_OF_MEMORY, nothing changed, if the allocation fails).
  */
 int pkv_prefill_chunk(pkv_request* req, int layer, const void* q, const void* k, const void* v,
                       float* out, void* stream);
@@ -456,8 +458,8 @@ int pkv_prefill_workspace_size(const pkv_pool* pool, int batch, int64_t total_ne
  *      out[x][q] = sum_j softmax_j(q[x][q] . K_j / sqrt(head_dim)) V_j over the
  *      positions j = 0 .. L0_b + i (the pool's window, if any, keeps the last
  *      `window` of them) -- the outputs n_b successive decode steps would give.
- *   q            [total_new][query_heads][head_dim] bf16, device
- *   k_new, v_new [total_new][kv_heads][head_dim] bf16, device
+ *   q            [total_new][query_heads][head_dim] storage dtype, device
+ *   k_new, v_new [total_new][kv_heads][head_dim] storage dtype, device
  *   cu_new       [batch + 1] int32, device: row offsets, cu_new[0] = 0,
  *                non-decreasing, cu_new[batch] <= total_new
  *   page_tables  [batch][max_pages] int32, device (entries past
@@ -466,16 +468,20 @@ int pkv_prefill_workspace_size(const pkv_pool* pool, int batch, int64_t total_ne
  *   out          [total_new][query_heads][head_dim] fp32, device
  *   workspace    device scratch of >= pkv_prefill_workspace_size bytes
  *                (caller owned, 16-byte aligned, no initialisation needed)
- * Pools: bf16 storage, head_dim 64 or 128, query_heads / kv_heads dividing 128
- * (else PKV_ERR_UNSUPPORTED); batch <= 1024.  The products run on the tensor
- * cores in bf16 with fp32 accumulation: the weights are rounded to bf16 before
- * they multiply V.  Stateless over bookkeeping: the caller owns lengths and
+ * Two implementations, chosen by the pool.  bf16 pools of head_dim 64 or 128:
+ * the tcgen05 tensor cores, bf16 products with fp32 accumulation, the weights
+ * rounded to bf16 before they multiply V; batch <= 1024.  Every other pool (fp32
+ * storage, other head widths): decode lanes -- every chunk row is stored first,
+ * then chunk token i of request b runs as one decode request of retained length
+ * L0_b + i + 1 over request b's pages, all in one decode launch, with the decode
+ * kernels' precision (fp32 weights; a bf16 q widened exactly to fp32).  Stateless over bookkeeping: the caller owns lengths and
  * tables.  Bad lengths or page ids found on the device set the pool's error
  * word (a bad page reads as zeros); the affected rows of `out` are then
  * unspecified.  Once a wait has run out (PKV_DEVERR_TIMEOUT), later prefill
  * calls skip their attention work until pkv_check_device_status clears the
- * word.  Enqueues three kernels on `stream` and returns without waiting; calls
- * whose device work can overlap must use different workspaces.
+ * word.  Enqueues three kernels on `stream` (plan, append, attention; or rows,
+ * decode plan, decode split) and returns without waiting; calls whose device
+ * work can overlap must use different workspaces.
  */
 int pkv_paged_prefill(pkv_pool* pool, int layer, int batch, int64_t total_new, const void* q,
                       const void* k_new, const void* v_new, const int32_t* cu_new,

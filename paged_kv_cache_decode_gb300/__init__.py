@@ -263,8 +263,8 @@ class Pool:
     def paged_prefill(self, layer: int, q, k_new, v_new, cu_new, page_tables, seq_lens, out=None,
                       workspace=None, stream=None):
         """Batched prefill of one layer: request b appends rows cu_new[b] .. cu_new[b+1]-1
-        of q / k_new / v_new (bf16) after its seq_lens[b] - n_b cached tokens; returns
-        out [N, query_heads, head_dim] fp32."""
+        of q / k_new / v_new (the pool's storage dtype) after its seq_lens[b] - n_b cached
+        tokens; returns out [N, query_heads, head_dim] fp32."""
         N = q.shape[0]
         B = cu_new.shape[0] - 1
         H, HQ, D = self.heads, self.query_heads, self.head_dim
@@ -280,9 +280,9 @@ class Pool:
             raise ValueError("page_tables must be [batch, max_pages]")
         check(lib.pkv_paged_prefill(
             self.handle, layer, B, N,
-            _dev(q, "q", torch.bfloat16, (N, HQ, D)),
-            _dev(k_new, "k_new", torch.bfloat16, (N, H, D)),
-            _dev(v_new, "v_new", torch.bfloat16, (N, H, D)),
+            _dev(q, "q", self.torch_dtype, (N, HQ, D)),
+            _dev(k_new, "k_new", self.torch_dtype, (N, H, D)),
+            _dev(v_new, "v_new", self.torch_dtype, (N, H, D)),
             _dev(cu_new, "cu_new", torch.int32, (B + 1,)),
             _dev(page_tables, "page_tables", torch.int32, None), page_tables.shape[1],
             _dev(seq_lens, "seq_lens", torch.int32, (B,)),
@@ -413,7 +413,7 @@ class Request:
 
     def prefill_chunk(self, layer: int, q, k, v, out=None, stream=None):
         """One layer of the pending chunk: q [n, query_heads, d_h], k, v [n, heads, d_h]
-        bf16; returns out [n, query_heads, d_h] fp32."""
+        in the pool's storage dtype; returns out [n, query_heads, d_h] fp32."""
         p = self.pool
         n = q.shape[0]
         qshape = (n, p.query_heads, p.head_dim)
@@ -421,8 +421,8 @@ class Request:
         if out is None:
             out = torch.empty(qshape, dtype=torch.float32, device=q.device)
         check(lib.pkv_prefill_chunk(
-            self.handle, layer, _dev(q, "q", torch.bfloat16, qshape),
-            _dev(k, "k", torch.bfloat16, kshape), _dev(v, "v", torch.bfloat16, kshape),
+            self.handle, layer, _dev(q, "q", p.torch_dtype, qshape),
+            _dev(k, "k", p.torch_dtype, kshape), _dev(v, "v", p.torch_dtype, kshape),
             _dev(out, "out", torch.float32, qshape), _stream_ptr(stream)), "pkv_prefill_chunk")
         return out
 

@@ -151,6 +151,8 @@ struct KParams {
     int64_t n_pages;
     const int32_t* tables;
     int max_pages;
+    const int32_t* table_rows;  // nullptr: request b reads table row b; else row table_rows[b]
+    bool allow_empty;           // seq_len 0: a request with no work, not an error
     const int32_t* seq_lens;    // nullptr: one request of length single_t
     int64_t single_t;
     int64_t max_seq_len;
@@ -180,6 +182,11 @@ struct KParams {
 
 __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
+}
+
+// Page-table row of request b.
+__device__ __forceinline__ int64_t table_row(const KParams& p, int b) {
+    return p.table_rows == nullptr ? (int64_t)b : (int64_t)__ldg(p.table_rows + b);
 }
 
 // Row block [page][KV head hk] of the K / V pools, and row of k_new / v_new for KV
@@ -236,7 +243,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
         if (i < p.B) {
             const int64_t t = seq_len_at(p, i);
             const int64_t pages = (t + p.P - 1) / p.P;
-            if (t < 1 || t > p.max_seq_len || pages > p.max_pages || t <= p.key_start) {
+            if (t == 0 && p.allow_empty) {
+                // no work for this request
+            } else if (t < 1 || t > p.max_seq_len || pages > p.max_pages || t <= p.key_start) {
                 atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
             } else {
                 n = lane_tiles(p, t);
@@ -607,7 +616,7 @@ split_decode_kernel(const KParams p) {
             tab_b = prod.b;
             tab_base = prod.page_idx;
             const int64_t e = tab_base + lane;
-            tab_val = e < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages + e) : -1;
+            tab_val = e < p.max_pages ? __ldg(p.tables + table_row(p, tab_b) * p.max_pages + e) : -1;
         }
         const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(prod.page_idx - tab_base));
         if (lane != 0) return;
@@ -1038,7 +1047,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             tab_b = prod.b;
             tab_base = prod.page_idx;
             const int64_t e = tab_base + lane;
-            tab_val = e < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages + e) : -1;
+            tab_val = e < p.max_pages ? __ldg(p.tables + table_row(p, tab_b) * p.max_pages + e) : -1;
         }
         const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(prod.page_idx - tab_base));
         if (lane != 0) return;
@@ -1487,6 +1496,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.v_pages = a.v_pages;
     p.n_pages = a.n_pages;
     p.tables = a.tables;
+    p.table_rows = a.table_rows;
+    p.allow_empty = a.allow_empty;
     p.max_pages = a.max_pages;
     p.seq_lens = a.seq_lens;
     p.single_t = a.single_t;
@@ -1531,6 +1542,168 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     }
 #undef PKV_LAUNCH
     return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------ prefill through decode lanes --
+
+namespace {
+
+struct LaneRowsParams {
+    int B;
+    int64_t N;
+    int H, HQ, D, P, words;       // words: 32-bit words of one K or V head row
+    const int32_t* cu_new;        // nullptr: one request of single_n rows
+    const int32_t* seq_lens;
+    int single_n;
+    int64_t single_t;
+    const int32_t* tables;
+    int max_pages;
+    int64_t n_pages;
+    const uint32_t* k_new;
+    const uint32_t* v_new;
+    uint32_t* k_pages;
+    uint32_t* v_pages;
+    const uint16_t* q_bf16;       // non-null: widen q into q32
+    float* q32;
+    int32_t* rows;
+    int32_t* lens;
+    unsigned* err;
+};
+
+__device__ __forceinline__ int lr_cu(const LaneRowsParams& p, int b) {
+    return p.cu_new ? __ldg(p.cu_new + b) : (b == 0 ? 0 : p.single_n);
+}
+
+// One warp per chunk row x: its request b (the last with cu_new[b] <= x); its decode
+// length L0_b + i + 1, or 0 when x belongs to no request or the request's lengths
+// are bad (those set the error word); its K / V rows stored at position L0_b + i;
+// and, for bf16 pools, its query widened to fp32 (exactly).
+__global__ void __launch_bounds__(256) lane_rows_kernel(const LaneRowsParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t x = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); x < p.N;
+         x += warps) {
+        int lo = 0, hi = p.B;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (lr_cu(p, mid) <= x) lo = mid;
+            else hi = mid;
+        }
+        const int b = lo;
+        const int c0 = lr_cu(p, b), c1 = lr_cu(p, b + 1);
+        int64_t t = 0, pos = 0;
+        int32_t page = -1;
+        if (x >= c0 && x < c1) {
+            const int64_t tb = p.seq_lens ? (int64_t)__ldg(p.seq_lens + b) : p.single_t;
+            const int64_t L0 = tb - (c1 - c0);
+            pos = L0 + (x - c0);
+            if (L0 < 0 || tb > (int64_t)p.max_pages * p.P) {
+                if (lane == 0) atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
+            } else {
+                t = pos + 1;
+                page = __ldg(p.tables + (int64_t)b * p.max_pages + pos / p.P);
+                if (page < 0 || page >= p.n_pages) page = -1;   // the decode kernel reports it
+            }
+        }
+        if (lane == 0) {
+            p.rows[x] = b;
+            p.lens[x] = (int32_t)t;
+        }
+        if (page >= 0) {
+            for (int h = 0; h < p.H; ++h) {
+                const int64_t dst = (((int64_t)page * p.H + h) * p.P + pos % p.P) * p.words;
+                const int64_t src = (x * p.H + h) * p.words;
+                for (int u = lane; u < p.words; u += 32) {
+                    p.k_pages[dst + u] = __ldg(p.k_new + src + u);
+                    p.v_pages[dst + u] = __ldg(p.v_new + src + u);
+                }
+            }
+        }
+        if (p.q_bf16 != nullptr) {
+            const int64_t n = (int64_t)p.HQ * p.D;
+            for (int64_t e = lane; e < n; e += 32)
+                p.q32[x * n + e] = __uint_as_float((uint32_t)__ldg(p.q_bf16 + x * n + e) << 16);
+        }
+    }
+}
+
+}  // namespace
+
+PrefillLanesLayout prefill_lanes_layout(int64_t N, int lane_heads, int D, int workers,
+                                        int lane_group, int query_heads, bool widen_q) {
+    PrefillLanesLayout L{};
+    L.decode = align_up(workspace_layout((int)N, lane_heads, D, workers, lane_group).total, 256);
+    L.rows = L.decode;
+    L.lens = align_up(L.rows + sizeof(int32_t) * (size_t)N, 256);
+    L.q32 = align_up(L.lens + sizeof(int32_t) * (size_t)N, 256);
+    L.total = widen_q ? L.q32 + sizeof(float) * (size_t)N * query_heads * D : L.q32;
+    return L;
+}
+
+cudaError_t launch_prefill_lanes(const PrefillLanesArgs& a, cudaStream_t stream) {
+    const bool widen = a.dtype == PKV_BF16;
+    const PrefillLanesLayout L = prefill_lanes_layout(a.total_new, a.lane_heads, a.D, a.workers,
+                                                      a.lane_group, a.query_heads, widen);
+    unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+    LaneRowsParams r{};
+    r.B = a.cu_new ? a.batch : 1;
+    r.N = a.total_new;
+    r.H = a.kv_heads;
+    r.HQ = a.query_heads;
+    r.D = a.D;
+    r.P = a.P;
+    r.words = a.D * (a.dtype == PKV_F32 ? 4 : 2) / 4;
+    r.cu_new = a.cu_new;
+    r.seq_lens = a.seq_lens;
+    r.single_n = a.single_n;
+    r.single_t = a.single_t;
+    r.tables = a.tables;
+    r.max_pages = a.max_pages;
+    r.n_pages = a.n_pages;
+    r.k_new = static_cast<const uint32_t*>(a.k_new);
+    r.v_new = static_cast<const uint32_t*>(a.v_new);
+    r.k_pages = static_cast<uint32_t*>(a.k_pages);
+    r.v_pages = static_cast<uint32_t*>(a.v_pages);
+    r.q_bf16 = widen ? static_cast<const uint16_t*>(a.q) : nullptr;
+    r.q32 = widen ? reinterpret_cast<float*>(ws + L.q32) : nullptr;
+    r.rows = reinterpret_cast<int32_t*>(ws + L.rows);
+    r.lens = reinterpret_cast<int32_t*>(ws + L.lens);
+    r.err = a.dev_error;
+    const int64_t want = (a.total_new + 7) / 8;
+    lane_rows_kernel<<<(unsigned)(want < 4096 ? (want < 1 ? 1 : want) : 4096), 256, 0, stream>>>(r);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    DecodeArgs d{};
+    d.dtype = a.dtype;
+    d.B = (int)a.total_new;
+    d.H = a.lane_heads;
+    d.D = a.D;
+    d.P = a.P;
+    d.G = a.lane_group;
+    d.kv_shift = a.kv_shift;
+    d.window = a.window;
+    d.q = widen ? reinterpret_cast<const float*>(ws + L.q32) : static_cast<const float*>(a.q);
+    d.k_new = a.k_new;    // stored again by the decode kernel's append: the same bytes
+    d.v_new = a.v_new;
+    d.k_pages = a.k_pages;
+    d.v_pages = a.v_pages;
+    d.n_pages = a.n_pages;
+    d.tables = a.tables;
+    d.max_pages = a.max_pages;
+    d.table_rows = r.rows;
+    d.seq_lens = r.lens;
+    d.max_seq_len = (int64_t)a.max_pages * a.P;
+    d.out = a.out;
+    d.workspace = a.workspace;
+    d.workspace_bytes = L.decode;
+    d.workers = a.workers;
+    d.dev_error = a.dev_error;
+    d.ev_before = a.ev_before;
+    d.ev_after = a.ev_after;
+    d.tmap_k = a.tmap_k;
+    d.tmap_v = a.tmap_v;
+    d.allow_empty = true;
+    return launch_decode(d, stream);
 }
 
 }  // namespace pkv

@@ -33,8 +33,9 @@ struct DecodeArgs {
     void* k_pages;           // this layer's pools, [pages][H][P][D]
     void* v_pages;
     int64_t n_pages;
-    const int32_t* tables;   // [B][max_pages]
+    const int32_t* tables;   // [B][max_pages], or rows chosen by table_rows
     int max_pages;
+    const int32_t* table_rows;  // nullptr, or [B] device: the table row request b reads
     const int32_t* seq_lens; // [B] device; nullptr => single request of length single_t
     int64_t single_t;
     int64_t max_seq_len;
@@ -59,6 +60,7 @@ struct DecodeArgs {
     int64_t pre_stride;      // query rows per split (B * query heads)
     cudaError_t (*before_split)(const void* ctx, cudaStream_t stream);
     const void* before_split_ctx;
+    bool allow_empty;        // a seq_len of 0 is a request with no work (not an error)
 };
 
 // Bytes of a CUtensorMap (the driver's TMA descriptor).
@@ -152,6 +154,49 @@ int prefill_max_batch();
 
 // Enqueue the plan, append and attention kernels on `stream`.
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// Batched prefill through decode lanes, for pools the tensor-core prefill does not
+// serve (fp32 storage, other head widths): every chunk row is first stored in its
+// page, then chunk token x of request b runs as decode request x of retained
+// length L0_b + i + 1 over request b's table row -- the n_b successive decode
+// steps the prefill stands for, at the decode kernels' precision.
+struct PrefillLanesArgs {
+    int dtype, D, P, kv_heads, query_heads;
+    int lane_heads, lane_group, kv_shift;   // the pool's decode lanes
+    int64_t window;
+    int batch;
+    int64_t total_new;
+    const void* q;                // [N][query_heads][D] storage dtype
+    const void* k_new;            // [N][kv_heads][D] storage dtype
+    const void* v_new;
+    void* k_pages;
+    void* v_pages;
+    int64_t n_pages;
+    const int32_t* cu_new;        // [batch + 1] device; nullptr: one request (single_n, single_t)
+    const int32_t* seq_lens;      // [batch] device
+    int single_n;
+    int64_t single_t;
+    const int32_t* tables;        // [batch][max_pages]
+    int max_pages;
+    float* out;                   // [N][query_heads][D]
+    void* workspace;
+    size_t workspace_bytes;
+    int workers;                  // decode workers of the launch
+    unsigned* dev_error;
+    const void* tmap_k;           // tensor-core decode kernel when non-null
+    const void* tmap_v;
+    cudaEvent_t ev_before;
+    cudaEvent_t ev_after;
+};
+
+struct PrefillLanesLayout {
+    size_t decode;                // the decode workspace of N lanes, at offset 0
+    size_t rows, lens, q32;       // int32 [N] table rows, int32 [N] lengths, fp32 widened q
+    size_t total;
+};
+PrefillLanesLayout prefill_lanes_layout(int64_t N, int lane_heads, int D, int workers,
+                                        int lane_group, int query_heads, bool widen_q);
+cudaError_t launch_prefill_lanes(const PrefillLanesArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------- shared prefix --
 

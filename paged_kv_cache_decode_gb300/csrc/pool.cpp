@@ -141,6 +141,48 @@ int check_rows_aligned(const pkv_pool* p, const void* q, int q_es, const void* k
 
 int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
 
+// Which batched prefill serves a pool: the tensor-core kernel (bf16, head_dim 64
+// or 128), or decode lanes (every other pool): chunk token by chunk token as
+// decode requests in one launch.
+bool tensor_prefill(const pkv_pool* p) {
+    return p->tmaps && pkv::prefill_supported(p->dtype, p->head_dim, p->group);
+}
+
+int lanes_workers(const pkv_pool* p, int64_t n) {
+    return pkv::launch_workers(p->workers, (int)n, p->dec_heads,
+                               pkv::attended_len(p->max_context, p->window), p->kv_shift);
+}
+
+size_t lanes_bytes(const pkv_pool* p, int64_t n) {
+    return pkv::prefill_lanes_layout(n, p->dec_heads, p->head_dim, lanes_workers(p, n),
+                                     p->dec_group, p->query_heads, p->dtype == PKV_BF16)
+        .total;
+}
+
+pkv::PrefillLanesArgs lanes_args(pkv_pool* p, int layer, int64_t n) {
+    pkv::PrefillLanesArgs a{};
+    a.dtype = p->dtype;
+    a.D = p->head_dim;
+    a.P = p->page_size;
+    a.kv_heads = p->heads;
+    a.query_heads = p->query_heads;
+    a.lane_heads = p->dec_heads;
+    a.lane_group = p->dec_group;
+    a.kv_shift = p->kv_shift;
+    a.window = p->window;
+    a.total_new = n;
+    a.k_pages = static_cast<unsigned char*>(p->k_base) + (size_t)layer * p->layer_bytes;
+    a.v_pages = static_cast<unsigned char*>(p->v_base) + (size_t)layer * p->layer_bytes;
+    a.n_pages = p->pages;
+    a.workers = lanes_workers(p, n);
+    a.dev_error = p->dev_error;
+    a.ev_before = p->ev_before;
+    a.ev_after = p->ev_after;
+    a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
+    a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
+    return a;
+}
+
 // The driver's tensor-map encoder, fetched through the runtime (no libcuda link).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -662,9 +704,6 @@ int pkv_begin_token(pkv_request* r, int64_t* position) {
 int pkv_begin_chunk(pkv_request* r, int64_t n, int64_t* position) {
     if (!r) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL request");
     if (n < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "a chunk holds at least one token");
-    pkv_pool* p = r->pool;
-    if (!p->host_only && !(p->tmaps && pkv::prefill_supported(p->dtype, p->head_dim, p->group)))
-        return fail(PKV_ERR_UNSUPPORTED, "prefill needs bf16 pools of head_dim 64 or 128");
     return begin_pending(r, n, true, position);
 }
 
@@ -738,13 +777,50 @@ int pkv_prefill_chunk(pkv_request* r, int layer, const void* q, const void* k, c
     if (!q || !k || !v || !out) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL tensor pointer");
     if (layer < 0 || layer >= p->layers)
         return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
-    if (int rc = check_rows_aligned(p, q, 2, k, v, out); rc != PKV_OK) return rc;
+    if (int rc = check_rows_aligned(p, q, elem_bytes(p->dtype), k, v, out); rc != PKV_OK) return rc;
     if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
     if (!r->pending || !r->chunk) return fail(PKV_ERR_BAD_STATE, "no chunk pending");
     if (r->appended[(size_t)layer]) return fail(PKV_ERR_BAD_STATE, "layer %d already ran", layer);
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!tensor_prefill(p)) {
+        // decode lanes: the request's scratch grows to the chunk (freeing the old
+        // one waits for the device)
+        const size_t need = lanes_bytes(p, r->pending_n);
+        if (r->prefill_ws_bytes < need) {
+            void* ws = nullptr;
+            cudaError_t e = cudaMalloc(&ws, need);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return fail(PKV_ERR_OUT_OF_MEMORY, "prefill scratch of %zu bytes", need);
+            }
+            if (r->dev_prefill_ws) cudaFree(r->dev_prefill_ws);
+            r->dev_prefill_ws = ws;
+            r->prefill_ws_bytes = need;
+        }
+        rc = prepare_layer_write(r, layer, s);
+        if (rc != PKV_OK) return rc;
+        pkv::PrefillLanesArgs a = lanes_args(p, layer, r->pending_n);
+        a.batch = 1;
+        a.q = q;
+        a.k_new = k;
+        a.v_new = v;
+        a.cu_new = nullptr;
+        a.seq_lens = nullptr;
+        a.single_n = (int)r->pending_n;
+        a.single_t = r->position + r->pending_n;
+        a.tables = r->dev_table;
+        a.max_pages = (int)p->max_pages_per_request;
+        a.out = out;
+        a.workspace = r->dev_prefill_ws;
+        a.workspace_bytes = r->prefill_ws_bytes;
+        cudaError_t e = pkv::launch_prefill_lanes(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+        r->appended[(size_t)layer] = 1;
+        ++r->appended_count;
+        return ok();
+    }
     rc = prepare_layer_write(r, layer, s);
     if (rc != PKV_OK) return rc;
     pkv::PrefillArgs a{};
@@ -925,7 +1001,8 @@ int pkv_prefill_workspace_size(const pkv_pool* p, int batch, int64_t total_new, 
     if (batch < 0 || total_new < 0)
         return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch or token count");
     *bytes = (batch == 0 || total_new == 0) ? 0
-                                            : pkv::prefill_workspace_bytes(batch, p->group, total_new);
+             : tensor_prefill(p)            ? pkv::prefill_workspace_bytes(batch, p->group, total_new)
+                                            : lanes_bytes(p, total_new);
     return ok();
 }
 
@@ -939,29 +1016,45 @@ int pkv_paged_prefill(pkv_pool* p, int layer, int batch, int64_t total_new, cons
         return fail(PKV_ERR_INVALID_ARGUMENT, "layer %d outside [0, %d)", layer, p->layers);
     if (batch < 0 || total_new < 0)
         return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch or token count");
-    if (batch > pkv::prefill_max_batch())
+    const bool tc = tensor_prefill(p);
+    if (tc && batch > pkv::prefill_max_batch())
         return fail(PKV_ERR_INVALID_ARGUMENT, "batch %d above %d", batch, pkv::prefill_max_batch());
     if (total_new > INT32_MAX) return fail(PKV_ERR_INVALID_ARGUMENT, "more than 2^31 - 1 tokens");
-    if (!pkv::prefill_supported(p->dtype, p->head_dim, p->group) || !p->tmaps)
-        return fail(PKV_ERR_UNSUPPORTED,
-                    "prefill needs bf16 pools of head_dim 64 or 128 (%d query heads per KV head)",
-                    p->group);
     if (batch == 0 || total_new == 0) return ok();
     if (!q || !k_new || !v_new || !cu_new || !page_tables || !seq_lens || !out || !workspace)
         return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pointer");
     if (max_pages < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "max_pages must be >= 1");
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
-    if (int rc = check_rows_aligned(p, q, 2, k_new, v_new, out); rc != PKV_OK) return rc;
-    if (pkv::prefill_max_tiles(batch, p->group, total_new) * p->heads > INT32_MAX)
+    if (int rc = check_rows_aligned(p, q, elem_bytes(p->dtype), k_new, v_new, out); rc != PKV_OK)
+        return rc;
+    if (tc && pkv::prefill_max_tiles(batch, p->group, total_new) * p->heads > INT32_MAX)
         return fail(PKV_ERR_INVALID_ARGUMENT, "%lld tokens need more CTAs than one launch holds",
                     (long long)total_new);
-    const size_t need = pkv::prefill_workspace_bytes(batch, p->group, total_new);
+    const size_t need =
+        tc ? pkv::prefill_workspace_bytes(batch, p->group, total_new) : lanes_bytes(p, total_new);
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
                     need);
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
+    if (!tc) {
+        pkv::PrefillLanesArgs a = lanes_args(p, layer, total_new);
+        a.batch = batch;
+        a.q = q;
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.cu_new = cu_new;
+        a.seq_lens = seq_lens;
+        a.tables = page_tables;
+        a.max_pages = max_pages;
+        a.out = out;
+        a.workspace = workspace;
+        a.workspace_bytes = workspace_bytes;
+        cudaError_t e = pkv::launch_prefill_lanes(a, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+        return ok();
+    }
     pkv::PrefillArgs a{};
     a.B = batch;
     a.H = p->heads;

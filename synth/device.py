@@ -37,26 +37,27 @@ def step_inputs(w: Workload, layer: int = 0):
 
 
 def prefill_inputs(w: Workload, layer: int = 0):
-    """Host arrays of one batched prefill: q [N,HQ,D] and k_new / v_new [N,H,D] as bf16
-    bits (tokens t_b - n_b .. t_b - 1 of each request's streams, requests in order) and
-    the row offsets cu [B+1] int32."""
+    """Host arrays of one batched prefill: q [N,HQ,D] and k_new / v_new [N,H,D] in the
+    storage dtype (bf16 bits or fp32; tokens t_b - n_b .. t_b - 1 of each request's
+    streams, requests in order) and the row offsets cu [B+1] int32."""
     H, D, HQ = w.H, w.D, w.HQ
     n = w.new_tokens.astype(np.int64)
     cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
     N = int(cu[-1])
-    q = np.empty((N, HQ, D), np.uint16)
-    k = np.empty((N, H, D), np.uint16)
-    v = np.empty((N, H, D), np.uint16)
+    sd = np.float32 if w.dtype == F32 else np.uint16
+    q = np.empty((N, HQ, D), sd)
+    k = np.empty((N, H, D), sd)
+    v = np.empty((N, H, D), sd)
     for b in range(w.B):
         t, nb = int(w.seq_lens[b]), int(n[b])
         if nb == 0:
             continue
         rows_ = slice(int(cu[b]), int(cu[b + 1]))
         for qh in range(HQ):
-            q[rows_, qh] = rows(w.seed, Q, layer, b, qh, t - nb, nb, D, 1)
+            q[rows_, qh] = rows(w.seed, Q, layer, b, qh, t - nb, nb, D, w.dtype)
         for h in range(H):
-            k[rows_, h] = rows(w.seed, KHIST, layer, b, h, t - nb, nb, D, 1)
-            v[rows_, h] = rows(w.seed, VHIST, layer, b, h, t - nb, nb, D, 1)
+            k[rows_, h] = rows(w.seed, KHIST, layer, b, h, t - nb, nb, D, w.dtype)
+            v[rows_, h] = rows(w.seed, VHIST, layer, b, h, t - nb, nb, D, w.dtype)
     return q, k, v, cu
 
 

@@ -164,16 +164,16 @@ def make_workload(name, seq_lens, H, D, P=16, dtype=F32, pool_pages=None, seed=0
 
 
 class PrefillRun:
-    """A bf16 pool whose requests hold their cached tokens, and one batched prefill of
-    the workload's chunks through the C ABI.  Slots at and after each request's
+    """A pool (the workload's storage dtype) whose requests hold their cached tokens,
+    and one batched prefill of the workload's chunks through the C ABI.  Slots at and after each request's
     cached length start as NaN, so a row the prefill fails to write, or a stale row
     it reads, shows up in the output."""
 
     def __init__(self, w: Workload, poison: bool = True):
         from synth.device import prefill_inputs
         self.w = w
-        self.pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "bf16", w.max_context, w.seed,
-                             query_heads=w.HQ, window=w.window)
+        self.pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dtype_name(w.dtype),
+                             w.max_context, w.seed, query_heads=w.HQ, window=w.window)
         self.reqs = [self.pool.request() for _ in range(w.B)]
         for r, n in zip(self.reqs, w.n_pages):
             r.lease_pages(int(n))
@@ -232,10 +232,13 @@ class PrefillRun:
             table = np.arange(tail, dtype=np.int32)[None, :]
         rows = slice(int(self.cu[b]), int(self.cu[b + 1]))
         cu = np.array([0, nb], dtype=np.int32)
-        return oracle.paged_prefill(kp, vp, synth.bf16_to_f32(self.q[rows]), self.k_new[rows],
+        return oracle.paged_prefill(kp, vp, self._q32(self.q[rows]), self.k_new[rows],
                                     self.v_new[rows], cu, table,
-                                    np.array([w.seq_lens[b]], dtype=np.int32), BF16,
+                                    np.array([w.seq_lens[b]], dtype=np.int32), w.dtype,
                                     group=w.group, window=w.window)
+
+    def _q32(self, q: np.ndarray) -> np.ndarray:
+        return synth.bf16_to_f32(q) if q.dtype == np.uint16 else q
 
     def oracle_row(self, b: int, i: int) -> np.ndarray:
         """Oracle output of chunk token i of request b, as the decode step at position
@@ -244,9 +247,9 @@ class PrefillRun:
         pos = int(self.cached[b]) + i
         kp, vp, table = self._host_pages(b, pos + 1)
         x = int(self.cu[b]) + i
-        out = oracle.paged_decode_attention(kp, vp, synth.bf16_to_f32(self.q[x:x + 1]),
+        out = oracle.paged_decode_attention(kp, vp, self._q32(self.q[x:x + 1]),
                                             self.k_new[x:x + 1], self.v_new[x:x + 1], table,
-                                            np.array([pos + 1], dtype=np.int32), BF16,
+                                            np.array([pos + 1], dtype=np.int32), w.dtype,
                                             group=w.group, window=w.window)
         return out[0]
 
@@ -255,6 +258,8 @@ class PrefillRun:
         pos = int(self.cached[b]) + i
         pg = int(self.tables[b, pos // self.w.P])
         slot = pos % self.w.P
+        if self.w.dtype == F32:
+            return self.k_pages[pg, :, slot].cpu().numpy(), self.v_pages[pg, :, slot].cpu().numpy()
         k = self.k_pages[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
         v = self.v_pages[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
         return k, v
@@ -265,12 +270,13 @@ class PrefillRun:
         self.pool.close()
 
 
-def make_prefill(name, cached, new, H, D, group=1, P=16, window=0, seed=0, pool_pages=None):
+def make_prefill(name, cached, new, H, D, group=1, P=16, window=0, seed=0, pool_pages=None,
+                 dtype=BF16):
     cached = np.asarray(cached, dtype=np.int64)
     new = np.asarray(new, dtype=np.int32)
     lens = (cached + new).astype(np.int32)
     n = (lens.astype(np.int64) + P - 1) // P
     if pool_pages is None:
         pool_pages = int(n.sum()) + 13
-    return Workload(name, len(lens), 1, H, D, P, BF16, int(pool_pages), int(max(lens.max(), 1)),
+    return Workload(name, len(lens), 1, H, D, P, dtype, int(pool_pages), int(max(lens.max(), 1)),
                     seed, lens, group=group, window=window, new_tokens=new)
