@@ -390,12 +390,14 @@ int pkv_workspace_size_shared(const pkv_pool* pool, int batch, int64_t max_seq_l
  *               request needs t_b > shared_len (its new row is its own); 0 is
  *               pkv_paged_decode_attention
  *   workspace   >= pkv_workspace_size_shared bytes
- * Pools: bf16, head_dim 64 or 128, query_heads / kv_heads dividing 128 (else
- * PKV_ERR_UNSUPPORTED).  A table that differs from request 0's within the
- * prefix sets PKV_DEVERR_SHARED, a t_b <= shared_len sets PKV_DEVERR_SEQ_LEN
- * (rows of the affected requests unspecified).  Enqueues four kernels on
- * `stream` (plan, prefix, split over each request's own positions, and a merge
- * of the partials) and returns without waiting.
+ * bf16 pools of head_dim 64 or 128: a table that differs from request 0's
+ * within the prefix sets PKV_DEVERR_SHARED, a t_b <= shared_len sets
+ * PKV_DEVERR_SEQ_LEN (rows of the affected requests unspecified); enqueues four
+ * kernels on `stream` (plan, prefix, split over each request's own positions,
+ * and a merge of the partials) and returns without waiting.  Other pools (fp32,
+ * other head widths) run pkv_paged_decode_attention with the same arguments:
+ * each request over its own pages, the same results, no shared reading and no
+ * PKV_DEVERR_SHARED check.
  */
 int pkv_paged_decode_attention_shared(pkv_pool* pool, int layer, int batch, const float* q,
                                       const void* k_new, const void* v_new,

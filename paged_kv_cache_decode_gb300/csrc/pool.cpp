@@ -1119,9 +1119,13 @@ int check_shared(const pkv_pool* p, int64_t max_seq_len, int64_t shared_len) {
     if (shared_len > 0 && shared_len >= max_seq_len)
         return fail(PKV_ERR_INVALID_ARGUMENT, "shared_len %lld leaves no position of a request's own",
                     (long long)shared_len);
-    if (shared_len > 0 && !(p->tmaps && pkv::shared_prefix_supported(p->dtype, p->head_dim, p->group)))
-        return fail(PKV_ERR_UNSUPPORTED, "shared prefixes need bf16 pools of head_dim 64 or 128");
     return PKV_OK;
+}
+
+// The pool has the shared-prefix kernel (bf16, head_dim 64 or 128); other pools take
+// the plain batched call, each request over its own pages.
+bool shared_kernel(const pkv_pool* p) {
+    return p->tmaps && pkv::shared_prefix_supported(p->dtype, p->head_dim, p->group);
 }
 
 }  // namespace
@@ -1134,7 +1138,7 @@ int pkv_workspace_size_shared(const pkv_pool* p, int batch, int64_t max_seq_len,
     if (batch < 0 || max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "bad batch or length");
     int rc = check_shared(p, max_seq_len, shared_len);
     if (rc != PKV_OK) return rc;
-    if (shared_len == 0) return pkv_workspace_size(p, batch, max_seq_len, bytes);
+    if (shared_len == 0 || !shared_kernel(p)) return pkv_workspace_size(p, batch, max_seq_len, bytes);
     *bytes = batch == 0 ? 0 : shared_layout(p, batch, max_seq_len, shared_len).total;
     return ok();
 }
@@ -1149,7 +1153,7 @@ int pkv_paged_decode_attention_shared(pkv_pool* p, int layer, int batch, const f
     if (max_seq_len < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "max_seq_len must be >= 1");
     int rc = check_shared(p, max_seq_len, shared_len);
     if (rc != PKV_OK) return rc;
-    if (shared_len == 0)
+    if (shared_len == 0 || !shared_kernel(p))
         return pkv_paged_decode_attention(p, layer, batch, q, k_new, v_new, page_tables, max_pages,
                                           seq_lens, max_seq_len, out, workspace, workspace_bytes,
                                           stream);

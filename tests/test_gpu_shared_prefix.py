@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import paged_kv_cache_decode_gb300 as pkv
-from synth import BF16, workloads
+from synth import BF16, F32, workloads
 from synth.workloads import Workload
 from tests._gpu import BatchedRun, check_close
 
@@ -160,15 +160,18 @@ def test_shared_prefix_argument_errors():
             assert e.value.status == st
     finally:
         run.close()
-    # fp32 pools have no shared-prefix kernel
+    # fp32 pools have no shared-prefix kernel: the call is the plain batched one
     w32 = Workload("f32", 2, 1, 2, 64, 16, 0, 64, 256, 1, np.array([40, 50], dtype=np.int32),
                    shared_prefix=32)
     run = BatchedRun(w32)
     try:
         d = run.dev
-        with pytest.raises(pkv.PkvError) as e:
-            run.pool.paged_decode_attention_shared(0, d["q"], d["k"], d["v"], d["tables"], d["lens"],
-                                                   run.max_seq_len, 32)
-        assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+        out = run.pool.paged_decode_attention_shared(0, d["q"], d["k"], d["v"], d["tables"],
+                                                     d["lens"], run.max_seq_len, 32)
+        torch.cuda.synchronize()
+        assert run.pool.check_device_status() == 0
+        ref = run.oracle_out()
+        check_close(np.stack([out.cpu().numpy()[k] for k in ref]), np.stack(list(ref.values())),
+                    F32, "fp32 shared call")
     finally:
         run.close()
