@@ -1,13 +1,16 @@
 """Random sequences of request operations on the GPU against the oracle model.
 
-Several requests share one bf16 grouped-query pool; each step applies one
+Several requests share one grouped-query pool (bf16 at head width 64, whose chunks
+take the tensor-core prefill; fp32, and bf16 at head width 32, whose chunks run
+through decode lanes); each step applies one
 seeded random operation to the library and to the oracle model alike — a
 token (every layer, then commit), a token aborted after some layers, a chunk
 (prefill, every layer, then commit), a chunk aborted after some layers, a fork,
 a destroy, a release.  After every step the tables, lengths, page references,
-free list and counters agree exactly; every committed output agrees within the
-bf16 bars (decode 5e-3, prefill 1e-2 normwise); at the end every page a live
-request holds has the same K/V bytes on both sides.
+free list and counters agree exactly; every output agrees within the bars
+(fp32: max abs 1e-5; bf16: decode 5e-3 and tensor-core prefill 1e-2 normwise,
+decode-lane prefill 5e-3); at the end every page a live request holds has the
+same K/V bytes on both sides.
 """
 import numpy as np
 import pytest
@@ -16,13 +19,13 @@ import torch
 import paged_kv_cache_decode_gb300 as pkv
 import synth
 from oracle.model import OraclePool, OracleError
-from synth import BF16
+from synth import BF16, F32
 from synth.device import to_device
+from tests._gpu import FP32_ATOL
 
 pytestmark = pytest.mark.gpu
 
-LAYERS, H, G, D, P = 2, 2, 2, 64, 16
-HQ = H * G
+LAYERS, H, P = 2, 2, 16
 PAGES, MAXC = 48, 192
 
 
@@ -38,8 +41,17 @@ def _normwise(out, ref):
     return float((num / den).max())
 
 
-def _rows(rng, shape):
-    return synth.f32_to_bf16(rng.standard_normal(shape).astype(np.float32))
+def _rows(rng, shape, dtype):
+    x = rng.standard_normal(shape).astype(np.float32)
+    return x if dtype == F32 else synth.f32_to_bf16(x)
+
+
+def _q32(x):
+    return synth.bf16_to_f32(x) if x.dtype == np.uint16 else x
+
+
+def _err(out, ref, dtype):
+    return float(np.abs(out - ref).max()) if dtype == F32 else _normwise(out, ref)
 
 
 def _status(fn):
@@ -50,11 +62,15 @@ def _status(fn):
         return e.status
 
 
-@pytest.mark.parametrize("seed", [1, 2])
-def test_random_request_operations_match_oracle_model(seed):
+@pytest.mark.parametrize("seed,dtype,D,G", [(1, BF16, 64, 2), (2, BF16, 64, 2), (3, F32, 64, 2),
+                                            (4, BF16, 32, 1)])
+def test_random_request_operations_match_oracle_model(seed, dtype, D, G):
+    HQ = H * G
     rng = np.random.default_rng(seed)
-    pool = pkv.Pool(LAYERS, PAGES, H, D, P, "bf16", MAXC, seed, query_heads=HQ)
-    opool = OraclePool(LAYERS, PAGES, H, D, P, BF16, max_context=MAXC, seed=seed, query_heads=HQ)
+    pool = pkv.Pool(LAYERS, PAGES, H, D, P, "f32" if dtype == F32 else "bf16", MAXC, seed,
+                    query_heads=HQ)
+    opool = OraclePool(LAYERS, PAGES, H, D, P, dtype, max_context=MAXC, seed=seed, query_heads=HQ)
+    lanes = dtype == F32 or D not in (64, 128)      # chunks through decode lanes
     reqs, oreqs = [pool.request()], [opool.request()]
     worst = {"decode": 0.0, "prefill": 0.0}
     try:
@@ -81,10 +97,10 @@ def test_random_request_operations_match_oracle_model(seed):
                     done = LAYERS if kind != 5 else int(rng.integers(0, LAYERS))
                     for layer in range(done):
                         q = rng.standard_normal((HQ, D)).astype(np.float32)
-                        k, v = _rows(rng, (H, D)), _rows(rng, (H, D))
+                        k, v = _rows(rng, (H, D), dtype), _rows(rng, (H, D), dtype)
                         out = r.append_and_attend(layer, to_device(q), to_device(k), to_device(v))
                         ref = o.append_and_attend(layer, q, k, v)
-                        worst["decode"] = max(worst["decode"], _normwise(out.cpu().numpy(), ref))
+                        worst["decode"] = max(worst["decode"], _err(out.cpu().numpy(), ref, dtype))
                     if kind == 5:
                         r.abort_token()
                         o.abort_token()
@@ -101,11 +117,11 @@ def test_random_request_operations_match_oracle_model(seed):
                 if a == 0:
                     done = LAYERS if kind != 8 else int(rng.integers(0, LAYERS))
                     for layer in range(done):
-                        q = _rows(rng, (n, HQ, D))
-                        k, v = _rows(rng, (n, H, D)), _rows(rng, (n, H, D))
+                        q = _rows(rng, (n, HQ, D), dtype)
+                        k, v = _rows(rng, (n, H, D), dtype), _rows(rng, (n, H, D), dtype)
                         out = r.prefill_chunk(layer, to_device(q), to_device(k), to_device(v))
-                        ref = o.prefill_chunk(layer, synth.bf16_to_f32(q), k, v)
-                        worst["prefill"] = max(worst["prefill"], _normwise(out.cpu().numpy(), ref))
+                        ref = o.prefill_chunk(layer, _q32(q), k, v)
+                        worst["prefill"] = max(worst["prefill"], _err(out.cpu().numpy(), ref, dtype))
                     if kind == 8:
                         r.abort_token()
                         o.abort_token()
@@ -122,15 +138,21 @@ def test_random_request_operations_match_oracle_model(seed):
         torch.cuda.synchronize()
         assert pool.check_device_status() == 0
         print(f"seed {seed}: worst decode {worst['decode']:.2e}, prefill {worst['prefill']:.2e}")
-        assert worst["decode"] <= 5e-3 and worst["prefill"] <= 1e-2
+        if dtype == F32:
+            assert worst["decode"] <= FP32_ATOL and worst["prefill"] <= FP32_ATOL
+        else:
+            assert worst["decode"] <= 5e-3 and worst["prefill"] <= (5e-3 if lanes else 1e-2)
         # every page a live request holds: the visible rows agree byte for byte
         for layer in range(LAYERS):
             kp, vp = pool.kv_pages(layer)
             for oo in oreqs:
                 for j in range(oo.length):
                     pg, slot = oo.table[j // P], j % P
-                    k = kp[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
-                    v = vp[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
+                    if dtype == F32:
+                        k, v = kp[pg, :, slot].cpu().numpy(), vp[pg, :, slot].cpu().numpy()
+                    else:
+                        k = kp[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
+                        v = vp[pg, :, slot].cpu().view(torch.int16).numpy().view(np.uint16)
                     assert np.array_equal(k, opool.k[layer, pg, :, slot])
                     assert np.array_equal(v, opool.v[layer, pg, :, slot])
     finally:
