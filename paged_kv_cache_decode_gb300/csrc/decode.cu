@@ -152,6 +152,7 @@ struct KParams {
     const int32_t* tables;
     int max_pages;
     const int32_t* table_rows;  // nullptr: request b reads table row b; else row table_rows[b]
+                                // (CUDA-core kernel only)
     bool allow_empty;           // seq_len 0: a request with no work, not an error
     const int32_t* seq_lens;    // nullptr: one request of length single_t
     int64_t single_t;
@@ -184,10 +185,6 @@ __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
 }
 
-// Page-table row of request b.
-__device__ __forceinline__ int64_t table_row(const KParams& p, int b) {
-    return p.table_rows == nullptr ? (int64_t)b : (int64_t)__ldg(p.table_rows + b);
-}
 
 // Row block [page][KV head hk] of the K / V pools, and row of k_new / v_new for KV
 // head hk of request b.  Lane head h of a request reads KV head h >> kv_shift.
@@ -545,8 +542,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const KParams p) {
 
 // One worker (warp) of the split kernel.  A lane here is a (request, KV head)
 // pair; its G query heads (grouped-query attention, G = 1 for multi-head) share
-// every staged K/V tile: query head h*G + g of request b reads KV head h.
-template <typename T, int D, int G>
+// every staged K/V tile: query head h*G + g of request b reads KV head h.  ROWS:
+// request b reads page-table row p.table_rows[b] (the prefill through decode lanes);
+// a separate instantiation, so the plain decode carries no extra live state.
+template <typename T, int D, int G, bool ROWS = false>
 __global__ void __launch_bounds__(Geo<T, D, G>::WARPS * 32, 1)
 split_decode_kernel(const KParams p) {
     using Gm = Geo<T, D, G>;
@@ -616,7 +615,8 @@ split_decode_kernel(const KParams p) {
             tab_b = prod.b;
             tab_base = prod.page_idx;
             const int64_t e = tab_base + lane;
-            tab_val = e < p.max_pages ? __ldg(p.tables + table_row(p, tab_b) * p.max_pages + e) : -1;
+            const int64_t row = ROWS ? (int64_t)__ldg(p.table_rows + tab_b) : (int64_t)tab_b;
+            tab_val = e < p.max_pages ? __ldg(p.tables + row * p.max_pages + e) : -1;
         }
         const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(prod.page_idx - tab_base));
         if (lane != 0) return;
@@ -1047,7 +1047,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             tab_b = prod.b;
             tab_base = prod.page_idx;
             const int64_t e = tab_base + lane;
-            tab_val = e < p.max_pages ? __ldg(p.tables + table_row(p, tab_b) * p.max_pages + e) : -1;
+            tab_val = e < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages + e) : -1;
         }
         const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(prod.page_idx - tab_base));
         if (lane != 0) return;
@@ -1336,9 +1336,12 @@ template <typename T, int D, int G>
 static cudaError_t prepare_split() {
     static bool done = false;   // per instantiation
     if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<T, D, G>,
+    cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<T, D, G, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Geo<T, D, G>::CTA_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(split_decode_kernel<T, D, G, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<T, D, G>::CTA_SMEM);
     if (e == cudaSuccess) done = true;
     return e;
 }
@@ -1378,7 +1381,9 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G>, p)) != cudaSuccess) return e;
+    e = p.table_rows != nullptr ? cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G, true>, p)
+                                : cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G, false>, p);
+    if (e != cudaSuccess) return e;
     if (p.pre_ml != nullptr) {
         const int64_t rows = (int64_t)p.B * p.H * G;
         combine_kernel<D, G><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
@@ -1526,6 +1531,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.pre_splits = a.pre_splits;
     p.pre_stride = a.pre_stride;
     if (a.tmap_k != nullptr && a.tmap_v != nullptr) {
+        if (a.table_rows != nullptr) return cudaErrorInvalidValue;   // CUDA-core kernel only
 #define PKV_LAUNCH_MMA(DD, GG) \
         if (a.D == DD && a.G == GG) return launch_mma<DD, GG>(a, p, stream);
         PKV_FOR_EACH_MMA(PKV_LAUNCH_MMA)

@@ -178,8 +178,8 @@ pkv::PrefillLanesArgs lanes_args(pkv_pool* p, int layer, int64_t n) {
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
-    a.tmap_k = p->tensor_cores ? &p->tmap_k[(size_t)layer] : nullptr;
-    a.tmap_v = p->tensor_cores ? &p->tmap_v[(size_t)layer] : nullptr;
+    a.tmap_k = nullptr;   // decode lanes read table rows: the CUDA-core kernel
+    a.tmap_v = nullptr;
     return a;
 }
 
