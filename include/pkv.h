@@ -161,8 +161,10 @@ int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page
 /* Create a pool from options (see pkv_pool_options).  Grouped-query and
  * multi-query pools (query_heads = G x kv_heads) are implemented for G in
  * {2, 4, 8, 16, 32, 64, 128} at head_dim 64 and 128 (else PKV_ERR_UNSUPPORTED,
- * unless HOST_ONLY).  Decode runs a group above 8 as G / 8 lanes of 8 query heads
- * per KV head, each lane reading the KV head's pages (the repeats mostly from L2). */
+ * unless HOST_ONLY).  Decode on the tensor-core kernel runs a group above 16 as
+ * G / 16 lanes of 16 query heads per KV head, the CUDA-core kernel a group above 8
+ * as G / 8 lanes of 8, each lane reading the KV head's pages (the repeats mostly
+ * from L2). */
 int pkv_pool_create_ex(const pkv_pool_options* options, pkv_pool** out);
 
 /* KV heads stored per page and heads of the query (either pointer may be NULL). */

@@ -144,11 +144,12 @@ class Pool:
         return bool(v.value)
 
     def kernel_name(self) -> str:
-        """The decode split kernel this pool launches (groups above 8 query heads per KV
-        head run as lanes of 8)."""
-        g = min(self.query_heads // self.heads, 8)
+        """The decode split kernel this pool launches (larger groups of query heads per
+        KV head run as lanes of 16 on the tensor-core kernel, of 8 on the CUDA-core one)."""
+        g = self.query_heads // self.heads
         if self.tensor_cores:
-            return f"split_decode_mma_kernel<{self.head_dim},{g}>"
+            return f"split_decode_mma_kernel<{self.head_dim},{min(g, 16)}>"
+        g = min(g, 8)
         st = "f32" if self.dtype == PKV_F32 else "bf16"
         return f"split_decode_kernel<{st},{self.head_dim},{g}>"
 

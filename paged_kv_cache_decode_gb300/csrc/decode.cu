@@ -159,7 +159,8 @@ struct KParams {
     int64_t max_seq_len;
     int B, H, P, tiles_per_page;
     // lane head h reads KV head h >> kv_shift of the pool's H >> kv_shift: a pool with
-    // more than 8 query heads per KV head runs as 2^kv_shift lanes of 8 per KV head
+    // more query heads per KV head than a lane takes (8; 16 on the tensor-core kernel)
+    // runs as 2^kv_shift lanes per KV head
     int kv_shift;
     int64_t window;             // attend to the last `window` positions (0: all)
     float qscale;               // log2(e) / sqrt(D)
@@ -441,79 +442,85 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
     for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
 
-// Combine the partials of all G query rows of lane `lane_id` at once (G >= 2
-// dividing 32) into out; slots as for merge_query.
-// For the maxima, sums and weights lane j takes worker slot j / G of a chunk of
-// 32 / G slots and query row j % G, so every row's max and sum reduce over the
-// lanes of one residue class mod G; for the o vectors lane j takes features
-// j * D/32 .. of every row, each weight broadcast by shuffle.  The loads of the
-// whole group go out together: a few L2 round trips per lane instead of a few
-// per query row, which matters because the merging warp's ring waits meanwhile.
+// Combine the partials of the G query rows of lane `lane_id` (G >= 2) into out,
+// GB = min(G, 8) rows at a time; slots as for merge_query.
+// For the maxima, sums and weights lane j takes worker slot j / GB of a chunk of
+// 32 / GB slots and query row j % GB, so every row's max and sum reduce over the
+// lanes of one residue class mod GB; for the o vectors lane j takes features
+// j * D/32 .. of every row, each weight broadcast by shuffle.  The loads of a
+// row block go out together: a few L2 round trips per lane instead of a few per
+// query row, which matters because the merging warp's ring waits meanwhile.
 template <int D, int G>
 __device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, int64_t K, int sub,
                                            int64_t r_lo, int64_t r_hi, int64_t T_all, int lane) {
-    static_assert(G >= 2 && 32 % G == 0 && D % 64 == 0, "grouped merge: G divides 32, D 64 or 128");
-    constexpr int SPC = 32 / G;          // worker slots per chunk
+    constexpr int GB = G < 8 ? G : 8;    // rows merged together
+    static_assert(GB >= 2 && 32 % GB == 0 && G % GB == 0 && D % 64 == 0,
+                  "grouped merge: G a power of two, D 64 or 128");
+    constexpr int SPC = 32 / GB;         // worker slots per chunk
     constexpr int DPL = D / 32;          // features per lane (2 or 4)
     const int R = p.W >> p.kv_shift;
     auto owns_tiles = [&](int64_t x) { return (x * T_all) / R != ((x + 1) * T_all) / R; };
     auto slot_of = [&](int64_t x) { return ((K + x) << p.kv_shift) | sub; };
     const int cnt = (int)(r_hi - r_lo + 1);
-    const int r = lane % G;              // the query row this lane weighs
-    float M = -INFINITY;
-    for (int j = lane / G; j < cnt; j += SPC)
-        if (owns_tiles(r_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[slot_of(r_lo + j) * G + r]).x);
-#pragma unroll
-    for (int off = 16; off >= G; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    float acc[G][DPL];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[g][i] = 0.f;
-    for (int base = 0; base < cnt; base += SPC) {
-        const int j = base + lane / G;
-        float wgt = 0.f;
-        if (j < cnt && owns_tiles(r_lo + j)) {
-            const float2 ml = __ldcg(&p.part_ml[slot_of(r_lo + j) * G + r]);
-            wgt = exp2f(ml.x - M);
-            L = fmaf(ml.y, wgt, L);
-        }
-        const int nj = cnt - base < SPC ? cnt - base : SPC;
+    const int r = lane % GB;             // the query row (within the block) this lane weighs
 #pragma unroll 1
-        for (int jj = 0; jj < nj; ++jj) {
-            const float* op = p.part_o + slot_of(r_lo + base + jj) * G * D + lane * DPL;
-            float v[G][DPL];
+    for (int g0 = 0; g0 < G; g0 += GB) {
+        float M = -INFINITY;
+        for (int j = lane / GB; j < cnt; j += SPC)
+            if (owns_tiles(r_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[slot_of(r_lo + j) * G + g0 + r]).x);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                if constexpr (DPL == 4) {
-                    const float4 x = __ldcg(reinterpret_cast<const float4*>(op + g * D));
-                    v[g][0] = x.x, v[g][1] = x.y, v[g][2] = x.z, v[g][3] = x.w;
-                } else {
-                    const float2 x = __ldcg(reinterpret_cast<const float2*>(op + g * D));
-                    v[g][0] = x.x, v[g][1] = x.y;
+        for (int off = 16; off >= GB; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        float acc[GB][DPL];
+#pragma unroll
+        for (int g = 0; g < GB; ++g)
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[g][i] = 0.f;
+        for (int base = 0; base < cnt; base += SPC) {
+            const int j = base + lane / GB;
+            float wgt = 0.f;
+            if (j < cnt && owns_tiles(r_lo + j)) {
+                const float2 ml = __ldcg(&p.part_ml[slot_of(r_lo + j) * G + g0 + r]);
+                wgt = exp2f(ml.x - M);
+                L = fmaf(ml.y, wgt, L);
+            }
+            const int nj = cnt - base < SPC ? cnt - base : SPC;
+#pragma unroll 1
+            for (int jj = 0; jj < nj; ++jj) {
+                const float* op = p.part_o + (slot_of(r_lo + base + jj) * G + g0) * D + lane * DPL;
+                float v[GB][DPL];
+#pragma unroll
+                for (int g = 0; g < GB; ++g) {
+                    if constexpr (DPL == 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4*>(op + g * D));
+                        v[g][0] = x.x, v[g][1] = x.y, v[g][2] = x.z, v[g][3] = x.w;
+                    } else {
+                        const float2 x = __ldcg(reinterpret_cast<const float2*>(op + g * D));
+                        v[g][0] = x.x, v[g][1] = x.y;
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < GB; ++g) {
+                    // slots of workers that own no tile hold stale data: weight 0, value dropped
+                    const float wj = __shfl_sync(0xffffffffu, wgt, jj * GB + g);
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i)
+                        acc[g][i] = wj != 0.f ? fmaf(wj, v[g][i], acc[g][i]) : acc[g][i];
                 }
             }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                // slots of workers that own no tile hold stale data: weight 0, value dropped
-                const float wj = __shfl_sync(0xffffffffu, wgt, jj * G + g);
-#pragma unroll
-                for (int i = 0; i < DPL; ++i) acc[g][i] = wj != 0.f ? fmaf(wj, v[g][i], acc[g][i]) : acc[g][i];
-            }
         }
-    }
 #pragma unroll
-    for (int off = 16; off >= G; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    float* out = p.out + lane_id * G * D + lane * DPL;
+        for (int off = 16; off >= GB; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        float* out = p.out + (lane_id * G + g0) * D + lane * DPL;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float inv = 1.f / __shfl_sync(0xffffffffu, L, g);
-        if constexpr (DPL == 4) {
-            *reinterpret_cast<float4*>(out + g * D) =
-                make_float4(acc[g][0] * inv, acc[g][1] * inv, acc[g][2] * inv, acc[g][3] * inv);
-        } else {
-            *reinterpret_cast<float2*>(out + g * D) = make_float2(acc[g][0] * inv, acc[g][1] * inv);
+        for (int g = 0; g < GB; ++g) {
+            const float inv = 1.f / __shfl_sync(0xffffffffu, L, g);
+            if constexpr (DPL == 4) {
+                *reinterpret_cast<float4*>(out + g * D) =
+                    make_float4(acc[g][0] * inv, acc[g][1] * inv, acc[g][2] * inv, acc[g][3] * inv);
+            } else {
+                *reinterpret_cast<float2*>(out + g * D) = make_float2(acc[g][0] * inv, acc[g][1] * inv);
+            }
         }
     }
 }
@@ -986,7 +993,14 @@ __global__ void __launch_bounds__(MmaGeo<D>::WARPS * 32, 1)
 split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using M = MmaGeo<D>;
-    static_assert(G >= 1 && G <= 8, "at most 8 query heads per KV head");
+    static_assert((G >= 1 && G <= 8) || G == 16, "1 to 8, or 16, query heads per KV head");
+    // WIDE (G = 16): lane l owns queries l / 4 and l / 4 + 8, the A operands are
+    // [q_hi rows 0-15] and [q_lo rows 0-15] (two MMAs per product), and each MMA row
+    // is a query of its own.  Otherwise rows g and g + 8 of one A operand hold the
+    // two bf16 parts of query g.
+    constexpr bool WIDE = G == 16;
+    constexpr int NQ = WIDE ? 2 : 1;            // queries per lane
+    constexpr int NA = WIDE ? 2 : 1;            // A operands per product
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1078,9 +1092,9 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     // ldmatrix row addresses: matrix j = lane / 8, row r = lane % 8
     const int mj = lane >> 3, mr = lane & 7;
 
-    uint32_t qa[M::KSTEPS][4];                  // A fragments of [q_hi; q_lo]
+    uint32_t qa[NA][M::KSTEPS][4];              // A fragments of [q_hi; q_lo] (WIDE: q_hi, q_lo)
     float o[M::NB][4];                          // O accumulator fragments
-    float m = -INFINITY, l = 0.f;               // running max and this lane's share of the sum
+    float m[NQ], l[NQ];                         // running max and this lane's share of the sum
     int piece_first = 0, t_b = 0, w_start = 0;
     int s = 0;
     uint32_t parity = 0;
@@ -1100,15 +1114,29 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 uint32_t b0, r0, b1, r1;
                 split_bf16(lo.x * p.qscale, lo.y * p.qscale, b0, r0);
                 split_bf16(hi.x * p.qscale, hi.y * p.qscale, b1, r1);
-                qa[ks][0] = q_ok ? b0 : 0u;   // row g,     k = 2t, 2t+1
-                qa[ks][1] = q_ok ? r0 : 0u;   // row g + 8
-                qa[ks][2] = q_ok ? b1 : 0u;   // row g,     k = 2t+8, 2t+9
-                qa[ks][3] = q_ok ? r1 : 0u;   // row g + 8
+                if constexpr (WIDE) {
+                    // query g + 8 sits 8 rows further on
+                    const float2 lo8 = *reinterpret_cast<const float2*>(qp + 8 * D + ks * 16 + 2 * t);
+                    const float2 hi8 = *reinterpret_cast<const float2*>(qp + 8 * D + ks * 16 + 8 + 2 * t);
+                    uint32_t b2, r2, b3, r3;
+                    split_bf16(lo8.x * p.qscale, lo8.y * p.qscale, b2, r2);
+                    split_bf16(hi8.x * p.qscale, hi8.y * p.qscale, b3, r3);
+                    qa[0][ks][0] = b0, qa[0][ks][1] = b2, qa[0][ks][2] = b1, qa[0][ks][3] = b3;
+                    qa[1][ks][0] = r0, qa[1][ks][1] = r2, qa[1][ks][2] = r1, qa[1][ks][3] = r3;
+                } else {
+                    qa[0][ks][0] = q_ok ? b0 : 0u;   // row g,     k = 2t, 2t+1
+                    qa[0][ks][1] = q_ok ? r0 : 0u;   // row g + 8
+                    qa[0][ks][2] = q_ok ? b1 : 0u;   // row g,     k = 2t+8, 2t+9
+                    qa[0][ks][3] = q_ok ? r1 : 0u;   // row g + 8
+                }
             }
 #pragma unroll
             for (int nb = 0; nb < M::NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
-            m = -INFINITY;
-            l = 0.f;
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                m[qi] = -INFINITY;
+                l[qi] = 0.f;
+            }
         }
 
         if (!mbar_wait_bounded(&bars[s], parity, kWaitLimitNs)) {
@@ -1161,8 +1189,12 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         }
 
         if (rows > 0) {
-            // S = [q_hi; q_lo] K^T : two 16 x 8 blocks (keys 0-7, 8-15)
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            // S = [q_hi; q_lo] K^T (WIDE: q_hi K^T and q_lo K^T): 16 x 8 blocks for keys
+            // 0-7 (sa) and 8-15 (sb)
+            float sa[NA][4], sb[NA][4];
+#pragma unroll
+            for (int a = 0; a < NA; ++a)
+                sa[a][0] = sa[a][1] = sa[a][2] = sa[a][3] = sb[a][0] = sb[a][1] = sb[a][2] = sb[a][3] = 0.f;
             const uint32_t kbase = smem_u32(Ks);
 #pragma unroll
             for (int ks = 0; ks < M::KSTEPS; ++ks) {
@@ -1170,40 +1202,71 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 const int key = ((mj >> 1) << 3) + mr;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kbase + swz(key, 2 * ks + (mj & 1)), b0, b1, b2, b3);
-                mma_bf16(sa, qa[ks], b0, b1);
-                mma_bf16(sb, qa[ks], b2, b3);
-            }
-            // scores of query g at keys 2t, 2t+1 (block a) and 8+2t, 9+2t (block b)
-            float sc[4] = {sa[0] + sa[2], sa[1] + sa[3], sb[0] + sb[2], sb[1] + sb[3]};
-            const int keys[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-            float tmax = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (!q_ok || keys[i] < lo || keys[i] >= rows) sc[i] = -INFINITY;
-                tmax = fmaxf(tmax, sc[i]);
-            }
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-            const float m_new = q_ok ? fmaxf(m, tmax) : 0.f;
-            const float alpha = q_ok ? exp2f(m - m_new) : 1.f;
-            float pw[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pw[i] = q_ok ? exp2f(sc[i] - m_new) : 0.f;
-            l = fmaf(l, alpha, (pw[0] + pw[1]) + (pw[2] + pw[3]));
-            m = q_ok ? m_new : m;
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                for (int nb = 0; nb < M::NB; ++nb) {
-                    o[nb][0] *= alpha;
-                    o[nb][1] *= alpha;
-                    o[nb][2] *= alpha;
-                    o[nb][3] *= alpha;
+                for (int a = 0; a < NA; ++a) {
+                    mma_bf16(sa[a], qa[a][ks], b0, b1);
+                    mma_bf16(sb[a], qa[a][ks], b2, b3);
                 }
             }
-            // A fragment of [P_hi; P_lo] over the 16 keys
-            uint32_t pa[4];
-            split_bf16(pw[0], pw[1], pa[0], pa[1]);
-            split_bf16(pw[2], pw[3], pa[2], pa[3]);
+            // scores of query g (WIDE: and g + 8) at keys 2t, 2t+1 (block a) and 8+2t, 9+2t (block b)
+            float sc[NQ][4];
+            if constexpr (WIDE) {
+#pragma unroll
+                for (int qi = 0; qi < 2; ++qi) {
+                    sc[qi][0] = sa[0][2 * qi] + sa[1][2 * qi];
+                    sc[qi][1] = sa[0][2 * qi + 1] + sa[1][2 * qi + 1];
+                    sc[qi][2] = sb[0][2 * qi] + sb[1][2 * qi];
+                    sc[qi][3] = sb[0][2 * qi + 1] + sb[1][2 * qi + 1];
+                }
+            } else {
+                sc[0][0] = sa[0][0] + sa[0][2];
+                sc[0][1] = sa[0][1] + sa[0][3];
+                sc[0][2] = sb[0][0] + sb[0][2];
+                sc[0][3] = sb[0][1] + sb[0][3];
+            }
+            const int keys[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+            float alpha[NQ], pw[NQ][4];
+            bool rescale = false;
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (!q_ok || keys[i] < lo || keys[i] >= rows) sc[qi][i] = -INFINITY;
+                    tmax = fmaxf(tmax, sc[qi][i]);
+                }
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+                const float m_new = q_ok ? fmaxf(m[qi], tmax) : 0.f;
+                alpha[qi] = q_ok ? exp2f(m[qi] - m_new) : 1.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pw[qi][i] = q_ok ? exp2f(sc[qi][i] - m_new) : 0.f;
+                l[qi] = fmaf(l[qi], alpha[qi], (pw[qi][0] + pw[qi][1]) + (pw[qi][2] + pw[qi][3]));
+                m[qi] = q_ok ? m_new : m[qi];
+                rescale = rescale || alpha[qi] != 1.f;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                // accumulator rows g and g + 8: query g's two parts, or (WIDE) queries g, g + 8
+                const float a_g = alpha[0], a_g8 = alpha[NQ - 1];
+#pragma unroll
+                for (int nb = 0; nb < M::NB; ++nb) {
+                    o[nb][0] *= a_g;
+                    o[nb][1] *= a_g;
+                    o[nb][2] *= a_g8;
+                    o[nb][3] *= a_g8;
+                }
+            }
+            // A fragments of [P_hi; P_lo] over the 16 keys (WIDE: P_hi and P_lo of both queries)
+            uint32_t pa[NA][4];
+            if constexpr (WIDE) {
+                split_bf16(pw[0][0], pw[0][1], pa[0][0], pa[1][0]);   // row g,     keys 2t, 2t+1
+                split_bf16(pw[1][0], pw[1][1], pa[0][1], pa[1][1]);   // row g + 8
+                split_bf16(pw[0][2], pw[0][3], pa[0][2], pa[1][2]);   // row g,     keys 8+2t, 9+2t
+                split_bf16(pw[1][2], pw[1][3], pa[0][3], pa[1][3]);   // row g + 8
+            } else {
+                split_bf16(pw[0][0], pw[0][1], pa[0][0], pa[0][1]);
+                split_bf16(pw[0][2], pw[0][3], pa[0][2], pa[0][3]);
+            }
             // O += [P_hi; P_lo] V : V[key][dim] as the k x n operand, transposed on load
             const uint32_t vbase = smem_u32(Vs);
 #pragma unroll
@@ -1212,8 +1275,11 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 const int key = ((mj & 1) << 3) + mr;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_trans(vbase + swz(key, 2 * np + (mj >> 1)), b0, b1, b2, b3);
-                mma_bf16(o[2 * np], pa, b0, b1);
-                mma_bf16(o[2 * np + 1], pa, b2, b3);
+#pragma unroll
+                for (int a = 0; a < NA; ++a) {
+                    mma_bf16(o[2 * np], pa[a], b0, b1);
+                    mma_bf16(o[2 * np + 1], pa[a], b2, b3);
+                }
             }
         }
 
@@ -1230,29 +1296,44 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         }
 
         if (last_tile || k == n_work - 1) {
-            // close the lane piece: quad sum of l; rows g and g + 8 of O add up
-            float lt = l;
-            lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-            lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+            // close the lane piece: quad sums of l; rows g and g + 8 of O add up (WIDE:
+            // they are queries g and g + 8)
+            float lt[NQ];
+#pragma unroll
+            for (int qi = 0; qi < NQ; ++qi) {
+                lt[qi] = l[qi];
+                lt[qi] += __shfl_xor_sync(0xffffffffu, lt[qi], 1);
+                lt[qi] += __shfl_xor_sync(0xffffffffu, lt[qi], 2);
+            }
+            auto o_pair = [&](int nb, int qi) {
+                return WIDE ? make_float2(o[nb][2 * qi], o[nb][2 * qi + 1])
+                            : make_float2(o[nb][0] + o[nb][2], o[nb][1] + o[nb][3]);
+            };
             if (piece_first == 0 && last_tile && p.pre_ml == nullptr) {
                 if (q_ok) {
-                    const float inv = 1.f / lt;
-                    float* op = p.out + (lane_id * G + g) * D + 2 * t;
 #pragma unroll
-                    for (int nb = 0; nb < M::NB; ++nb)
-                        *reinterpret_cast<float2*>(op + nb * 8) =
-                            make_float2((o[nb][0] + o[nb][2]) * inv, (o[nb][1] + o[nb][3]) * inv);
+                    for (int qi = 0; qi < NQ; ++qi) {
+                        const float inv = 1.f / lt[qi];
+                        float* op = p.out + (lane_id * G + g + 8 * qi) * D + 2 * t;
+#pragma unroll
+                        for (int nb = 0; nb < M::NB; ++nb) {
+                            const float2 x = o_pair(nb, qi);
+                            *reinterpret_cast<float2*>(op + nb * 8) = make_float2(x.x * inv, x.y * inv);
+                        }
+                    }
                 }
             } else {
                 const int64_t slot =      // partial of KV lane K from range r, this sub-lane
                     ((((int64_t)cur.b * Hk + cur.h) + (w >> p.kv_shift)) << p.kv_shift) | sub;
                 if (q_ok) {
-                    float* op = p.part_o + (slot * G + g) * D + 2 * t;
 #pragma unroll
-                    for (int nb = 0; nb < M::NB; ++nb)
-                        *reinterpret_cast<float2*>(op + nb * 8) =
-                            make_float2(o[nb][0] + o[nb][2], o[nb][1] + o[nb][3]);
-                    if (t == 0) p.part_ml[slot * G + g] = make_float2(m, lt);
+                    for (int qi = 0; qi < NQ; ++qi) {
+                        float* op = p.part_o + (slot * G + g + 8 * qi) * D + 2 * t;
+#pragma unroll
+                        for (int nb = 0; nb < M::NB; ++nb)
+                            *reinterpret_cast<float2*>(op + nb * 8) = o_pair(nb, qi);
+                        if (t == 0) p.part_ml[slot * G + g + 8 * qi] = make_float2(m[qi], lt[qi]);
+                    }
                 }
                 __threadfence();
                 __syncwarp();
@@ -1453,10 +1534,11 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
 
 // The tensor-core kernel serves grouped-query pools; for one query head per KV
 // head the CUDA-core kernel is as fast (measured on GB300) and is kept.
-#define PKV_FOR_EACH_MMA(X) X(64, 2) X(64, 4) X(64, 8) X(128, 2) X(128, 4) X(128, 8)
+#define PKV_FOR_EACH_MMA(X) X(64, 2) X(64, 4) X(64, 8) X(64, 16) X(128, 2) X(128, 4) X(128, 8) \
+    X(128, 16)
 
 bool mma_supported(int dtype, int D, int G) {
-    return dtype == PKV_BF16 && (D == 64 || D == 128) && (G == 2 || G == 4 || G == 8);
+    return dtype == PKV_BF16 && (D == 64 || D == 128) && (G == 2 || G == 4 || G == 8 || G == 16);
 }
 
 // Instantiated geometries: every head width for multi-head attention; groups

@@ -65,8 +65,9 @@ struct SplitMix64 {
 struct pkv_pool {
     int layers = 0, heads = 0, head_dim = 0, page_size = 0, dtype = 0;
     int query_heads = 0, group = 1;    // query heads = group x KV heads (grouped-query attention)
-    // decode runs on lanes of at most 8 query heads: a group of 16 .. 128 (multi-query
-    // layouts) is 2^kv_shift lanes of 8 per KV head, dec_heads = heads << kv_shift
+    // decode runs on lanes of at most 8 query heads (16 on the tensor-core kernel): a
+    // larger group (multi-query layouts, up to 128) is 2^kv_shift lanes of dec_group
+    // per KV head, dec_heads = heads << kv_shift
     int dec_heads = 0, dec_group = 1, kv_shift = 0;
     int64_t window = 0;                // sliding window in positions (0: whole prefix)
     int64_t pages = 0, max_context = 0, max_pages_per_request = 0;
@@ -389,6 +390,12 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
                    tensor_map_encoder() != nullptr;
         p->tensor_cores = p->tmaps && !(flags & PKV_POOL_CUDA_CORES) &&
                           pkv::mma_supported(dtype, head_dim, p->dec_group);
+        if (p->tensor_cores && p->group >= 16) {   // lanes of 16 query heads
+            p->dec_group = 16;
+            p->kv_shift = 0;
+            while ((p->dec_group << p->kv_shift) < p->group) ++p->kv_shift;
+            p->dec_heads = heads << p->kv_shift;
+        }
         p->workers = pkv::resident_workers(dtype, head_dim, p->dec_group, sms, p->tensor_cores);
         if (p->workers <= 0) {
             delete p;

@@ -368,6 +368,10 @@ def test_kernel_selection():
         return pkv.Pool(1, 8, 2, kw.pop("D", 128), 16, kw.pop("dtype", "bf16"), 64, **kw)
     with pool(query_heads=16) as p:
         assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<128,8>"
+    with pool(query_heads=32) as p:
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<128,16>"
+    with pool(query_heads=64, D=64) as p:
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<64,16>"
     with pool(query_heads=16, cuda_cores=True) as p:
         assert not p.tensor_cores
     with pool() as p:
