@@ -407,6 +407,37 @@ def test_tensor_core_and_cuda_core_kernels_agree():
         b.close()
 
 
+
+# 16-query lanes: groups of 16 and more run on the tensor-core kernel as lanes of 16
+# query heads (two MMA rows per fragment lane); the CUDA-core kernel runs them as
+# lanes of 8.  Page sizes 32 and 64 put several tiles in a page.
+
+@pytest.mark.parametrize("group,H,D,P,window", [(16, 2, 128, 32, 0), (16, 1, 64, 64, 0),
+                                                (32, 2, 64, 16, 77), (16, 3, 128, 64, 300)])
+def test_wide_lanes_page_sizes(group, H, D, P, window):
+    lens = [1, 15, 16, 17, 64, 65, 500, 1999, 4096]
+    _batched_check(make_workload(f"wide{group}_{P}", lens, H, D, P=P, dtype=BF16,
+                                 seed=110 + group + P, group=group, window=window))
+
+
+def test_wide_lanes_agree_with_cuda_core_lanes_of_8():
+    w = make_workload("wide_agree", [1, 15, 16, 17, 500, 4096, 33], 2, 128, dtype=BF16, seed=61,
+                      group=32)
+    a, b = BatchedRun(w), BatchedRun(w, cuda_cores=True)
+    try:
+        assert a.pool.kernel_name() == "split_decode_mma_kernel<128,16>"
+        assert b.pool.kernel_name() == "split_decode_kernel<bf16,128,8>"
+        oa, ob = a.run().cpu().numpy(), b.run().cpu().numpy()
+        rel = np.abs(oa - ob).max(axis=-1) / np.maximum(np.abs(ob).max(axis=-1), 1e-6)
+        assert rel.max() < 1e-4
+    finally:
+        a.close()
+        b.close()
+
+
+def test_wide_lanes_serial_page_size_32_with_abort():
+    _serial(2, 1, 64, BF16, 64, 300, 70, 12, abort_at=33, P=32, group=16)
+
 # ----------------------------------------------------------- sliding window --
 
 @pytest.mark.parametrize("window,dtype,group", [(1, F32, 1), (16, BF16, 1), (17, F32, 1),
