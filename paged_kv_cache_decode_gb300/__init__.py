@@ -145,13 +145,12 @@ class Pool:
 
     def kernel_name(self) -> str:
         """The decode split kernel this pool launches (larger groups of query heads per
-        KV head run as lanes of 16 on the tensor-core kernel, of 8 on the CUDA-core one)."""
+        KV head run as lanes of 16 on the bf16 tensor-core kernel, of 8 otherwise)."""
         g = self.query_heads // self.heads
-        if self.tensor_cores:
-            return f"split_decode_mma_kernel<{self.head_dim},{min(g, 16)}>"
-        g = min(g, 8)
         st = "f32" if self.dtype == PKV_F32 else "bf16"
-        return f"split_decode_kernel<{st},{self.head_dim},{g}>"
+        if self.tensor_cores:
+            return f"split_decode_mma_kernel<{st},{self.head_dim},{min(g, 16 if st == 'bf16' else 8)}>"
+        return f"split_decode_kernel<{st},{self.head_dim},{min(g, 8)}>"
 
     def bytes(self) -> int:
         b = ctypes.c_uint64()

@@ -909,12 +909,13 @@ split_decode_kernel(const KParams p) {
 
 // ------------------------------------------------- tensor-core split kernel --
 //
-// bf16 storage, head width 64 or 128.  Same workers, partition, ring, fused
-// append, partials and merge as split_decode_kernel; what differs is how a
+// bf16 or fp32 storage, head width 64 or 128.  Same workers, partition, ring,
+// fused append, partials and merge as split_decode_kernel; what differs is how a
 // staged tile is consumed.  K and V tiles arrive by TMA tensor loads with the
-// 128-byte swizzle (each 16-row x 64-column box lands as 16 rows of 128 bytes
+// 128-byte swizzle (each 16-row x 128-byte box lands as 16 rows of 128 bytes
 // whose 16-byte chunks are XOR-permuted by row), so the ldmatrix reads below
-// hit 32 distinct banks.  Scores S = Q K^T and the mixture O += P V run on
+// hit 32 distinct banks.  The bf16 form follows; the fp32 form (tf32 MMAs on
+// split operands) is described in the kernel.  Scores S = Q K^T and the mixture O += P V run on
 // mma.sync m16n8k16 (bf16 inputs, fp32 accumulation) with a 16-row A tile:
 // row g holds the bf16 rounding of query g (pre-scaled by log2(e)/sqrt(d_h))
 // and row g + 8 the bf16 rounding of its remainder, so the two partial products
@@ -961,20 +962,50 @@ __device__ __forceinline__ void split_bf16(float lo, float hi, uint32_t& big, ui
     rest = pack_bf16(lo - __low2float(b), hi - __high2float(b));
 }
 
-template <int D>
+// D = A B + D, m16n8k8, tf32 x tf32 -> fp32
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// tf32 rounding of x and of the remainder: x = big + rest to ~2^-22 relative
+__device__ __forceinline__ void split_tf32(float x, uint32_t& big, uint32_t& rest) {
+    big = to_tf32(x);
+    rest = to_tf32(x - __uint_as_float(big));
+}
+
+// Shared-memory tile geometry of the tensor-core kernel for storage type T:
+// every 16-row tile of K (and of V) is BOXES boxes of 16 rows x 128 bytes, each
+// written by one TMA tensor load with the 128-byte swizzle.
+template <typename T, int D>
 struct MmaGeo {
-    static constexpr int HALVES = D / 64;                 // 128-byte swizzle boxes per row
-    static constexpr int HALF_BYTES = kTile * 128;        // one box: 16 rows x 128 bytes
-    static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+    static constexpr int ES = sizeof(T);
+    static constexpr int ROW_BYTES = D * ES;
+    static constexpr int CHUNKS = ROW_BYTES / 16;         // 16-byte chunks per row
+    static constexpr int BOXES = ROW_BYTES / 128;         // 128-byte swizzle boxes per row
+    static constexpr int BOX_ELEMS = 128 / ES;            // elements per box row
+    static constexpr int BOX_BYTES = kTile * 128;         // one box: 16 rows x 128 bytes
+    static constexpr int TILE_BYTES = BOXES * BOX_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int KSTEPS = D / 16;                 // k-steps of S = Q K^T
+    static constexpr int KSTEPS = ROW_BYTES / 32;         // k-steps of S = Q K^T (16 bf16 / 8 fp32)
     static constexpr int NB = D / 8;                      // n-blocks of O
 #if defined(PKV_MMA_WARPS) && defined(PKV_MMA_STAGES)
     static constexpr int WARPS = PKV_MMA_WARPS;
     static constexpr int STAGES = PKV_MMA_STAGES;
 #else
-    static constexpr int WARPS = Geo<__nv_bfloat16, D>::WARPS;
-    static constexpr int STAGES = Geo<__nv_bfloat16, D>::STAGES;
+    // the CUDA-core kernel's grouped geometry for the same bytes per tile
+    static constexpr int WARPS = Geo<T, D, sizeof(T) == 4 ? 2 : 1>::WARPS;
+    static constexpr int STAGES = Geo<T, D, sizeof(T) == 4 ? 2 : 1>::STAGES;
 #endif
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES;
     // stage rings (1024-byte aligned, as the swizzle requires), then mbarriers and page ids
@@ -983,17 +1014,22 @@ struct MmaGeo {
     static_assert(CTA_SMEM <= 227 * 1024, "CTA does not fit an SM");
 };
 
-// Byte offset of 16-byte chunk c (0 .. D/8 - 1) of row r in a swizzled tile.
+// Byte offset of 16-byte chunk c of row r in a swizzled tile.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
-    return (uint32_t)((c >> 3) * MmaGeo<64>::HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    return (uint32_t)((c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(MmaGeo<D>::WARPS * 32, 1)
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(MmaGeo<T, D>::WARPS * 32, 1)
 split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
-    using M = MmaGeo<D>;
-    static_assert((G >= 1 && G <= 8) || G == 16, "1 to 8, or 16, query heads per KV head");
+    using M = MmaGeo<T, D>;
+    // F32: fp32 storage on tf32 MMAs (m16n8k8).  Every fp32 operand is split into its
+    // tf32 rounding and the tf32 rounding of the remainder (together ~2^-22 relative);
+    // [big; rest] rows of q (or P) times the big and the rest parts of K (or V) give all
+    // four cross products, each exact in fp32, so S and O keep fp32 accuracy.
+    constexpr bool F32 = sizeof(T) == 4;
+    static_assert((G >= 1 && G <= 8) || (G == 16 && !F32), "1 to 8 (bf16: or 16) query heads per KV head");
     // WIDE (G = 16): lane l owns queries l / 4 and l / 4 + 8, the A operands are
     // [q_hi rows 0-15] and [q_lo rows 0-15] (two MMAs per product), and each MMA row
     // is a query of its own.  Otherwise rows g and g + 8 of one A operand hold the
@@ -1001,6 +1037,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     constexpr bool WIDE = G == 16;
     constexpr int NQ = WIDE ? 2 : 1;            // queries per lane
     constexpr int NA = WIDE ? 2 : 1;            // A operands per product
+    constexpr int NS = WIDE || F32 ? 2 : 1;     // accumulator sets per S block (A or B parts)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1075,9 +1112,10 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         unsigned char* dst = ring + s * M::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[s], M::STAGE_BYTES);
 #pragma unroll
-        for (int hf = 0; hf < M::HALVES; ++hf) {
-            tma_load_2d(dst + hf * M::HALF_BYTES, &tmk, hf * 64, y, &bars[s], policy);
-            tma_load_2d(dst + M::TILE_BYTES + hf * M::HALF_BYTES, &tmv, hf * 64, y, &bars[s], policy);
+        for (int bx = 0; bx < M::BOXES; ++bx) {
+            tma_load_2d(dst + bx * M::BOX_BYTES, &tmk, bx * M::BOX_ELEMS, y, &bars[s], policy);
+            tma_load_2d(dst + M::TILE_BYTES + bx * M::BOX_BYTES, &tmv, bx * M::BOX_ELEMS, y, &bars[s],
+                        policy);
         }
     };
 
@@ -1092,7 +1130,8 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     // ldmatrix row addresses: matrix j = lane / 8, row r = lane % 8
     const int mj = lane >> 3, mr = lane & 7;
 
-    uint32_t qa[NA][M::KSTEPS][4];              // A fragments of [q_hi; q_lo] (WIDE: q_hi, q_lo)
+    uint32_t qa[NA][M::KSTEPS][4];              // A fragments of [q_hi; q_lo] (WIDE: q_hi, q_lo;
+                                                // F32: [q_big; q_rest] over 8 features a step)
     float o[M::NB][4];                          // O accumulator fragments
     float m[NQ], l[NQ];                         // running max and this lane's share of the sum
     int piece_first = 0, t_b = 0, w_start = 0;
@@ -1109,6 +1148,17 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             const float* qp = p.q + (lane_id * G + (q_ok ? g : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < M::KSTEPS; ++ks) {
+                if constexpr (F32) {
+                    // row g: k = t and t + 4 of features 8ks .. 8ks+7; row g + 8: their rests
+                    uint32_t b0, r0, b1, r1;
+                    split_tf32(qp[ks * 8 + t] * p.qscale, b0, r0);
+                    split_tf32(qp[ks * 8 + 4 + t] * p.qscale, b1, r1);
+                    qa[0][ks][0] = q_ok ? b0 : 0u;
+                    qa[0][ks][1] = q_ok ? r0 : 0u;
+                    qa[0][ks][2] = q_ok ? b1 : 0u;
+                    qa[0][ks][3] = q_ok ? r1 : 0u;
+                    continue;
+                }
                 const float2 lo = *reinterpret_cast<const float2*>(qp + ks * 16 + 2 * t);
                 const float2 hi = *reinterpret_cast<const float2*>(qp + ks * 16 + 8 + 2 * t);
                 uint32_t b0, r0, b1, r1;
@@ -1169,48 +1219,66 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             // fused append: row t_b - 1 from k_new / v_new into the tile and the page;
             // rows past it (stale bytes, possibly not finite) are cleared in V
             const int r = rows - 1;
-            if (lane < D / 8) {
-                const int64_t src = kv_new_row(p, cur.b, cur.h) * D + lane * 8;
-                const uint4 kb = *reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(p.k_new) + src);
-                const uint4 vb = *reinterpret_cast<const uint4*>(
-                    static_cast<const __nv_bfloat16*>(p.v_new) + src);
+            constexpr int EPC = 16 / M::ES;               // elements per 16-byte chunk
+            if (lane < M::CHUNKS) {
+                const int64_t src = kv_new_row(p, cur.b, cur.h) * D + lane * EPC;
+                const uint4 kb = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src);
+                const uint4 vb = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src);
                 *reinterpret_cast<uint4*>(Ks + swz(r, lane)) = kb;
                 *reinterpret_cast<uint4*>(Vs + swz(r, lane)) = vb;
-                const int64_t dst = (kv_block(p, page, cur.h) * p.P + cur.slot0 + r) * D + lane * 8;
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.k_pages) + dst) = kb;
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.v_pages) + dst) = vb;
+                const int64_t dst = (kv_block(p, page, cur.h) * p.P + cur.slot0 + r) * D + lane * EPC;
+                *reinterpret_cast<uint4*>(static_cast<T*>(p.k_pages) + dst) = kb;
+                *reinterpret_cast<uint4*>(static_cast<T*>(p.v_pages) + dst) = vb;
             }
-            for (int i = lane; i < (kTile - rows) * (D / 8); i += 32) {
-                const int rr = rows + i / (D / 8), c = i % (D / 8);
+            for (int i = lane; i < (kTile - rows) * M::CHUNKS; i += 32) {
+                const int rr = rows + i / M::CHUNKS, c = i % M::CHUNKS;
                 *reinterpret_cast<uint4*>(Vs + swz(rr, c)) = make_uint4(0u, 0u, 0u, 0u);
             }
             __syncwarp();
         }
 
         if (rows > 0) {
-            // S = [q_hi; q_lo] K^T (WIDE: q_hi K^T and q_lo K^T): 16 x 8 blocks for keys
-            // 0-7 (sa) and 8-15 (sb)
-            float sa[NA][4], sb[NA][4];
+            // S = [q_hi; q_lo] K^T (WIDE: q_hi K^T and q_lo K^T; F32: [q_big; q_rest] times
+            // K_big^T and K_rest^T): 16 x 8 blocks for keys 0-7 (sa) and 8-15 (sb), one
+            // accumulator set per A or B part
+            float sa[NS][4], sb[NS][4];
 #pragma unroll
-            for (int a = 0; a < NA; ++a)
+            for (int a = 0; a < NS; ++a)
                 sa[a][0] = sa[a][1] = sa[a][2] = sa[a][3] = sb[a][0] = sb[a][1] = sb[a][2] = sb[a][3] = 0.f;
             const uint32_t kbase = smem_u32(Ks);
 #pragma unroll
             for (int ks = 0; ks < M::KSTEPS; ++ks) {
                 // matrices: (keys 0-7, chunk 2ks), (keys 0-7, 2ks+1), (keys 8-15, 2ks), (keys 8-15, 2ks+1)
+                // (F32: lane 4g+t receives feature 8ks+t, then 8ks+4+t, of key g: B of m16n8k8)
                 const int key = ((mj >> 1) << 3) + mr;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kbase + swz(key, 2 * ks + (mj & 1)), b0, b1, b2, b3);
+                if constexpr (F32) {
+                    uint32_t g0, r0, g1, r1, g2, r2, g3, r3;
+                    split_tf32(__uint_as_float(b0), g0, r0);
+                    split_tf32(__uint_as_float(b1), g1, r1);
+                    split_tf32(__uint_as_float(b2), g2, r2);
+                    split_tf32(__uint_as_float(b3), g3, r3);
+                    mma_tf32(sa[0], qa[0][ks], g0, g1);
+                    mma_tf32(sb[0], qa[0][ks], g2, g3);
+                    mma_tf32(sa[1], qa[0][ks], r0, r1);
+                    mma_tf32(sb[1], qa[0][ks], r2, r3);
+                } else {
 #pragma unroll
-                for (int a = 0; a < NA; ++a) {
-                    mma_bf16(sa[a], qa[a][ks], b0, b1);
-                    mma_bf16(sb[a], qa[a][ks], b2, b3);
+                    for (int a = 0; a < NA; ++a) {
+                        mma_bf16(sa[a], qa[a][ks], b0, b1);
+                        mma_bf16(sb[a], qa[a][ks], b2, b3);
+                    }
                 }
             }
             // scores of query g (WIDE: and g + 8) at keys 2t, 2t+1 (block a) and 8+2t, 9+2t (block b)
             float sc[NQ][4];
-            if constexpr (WIDE) {
+            if constexpr (F32) {
+                sc[0][0] = (sa[0][0] + sa[1][0]) + (sa[0][2] + sa[1][2]);
+                sc[0][1] = (sa[0][1] + sa[1][1]) + (sa[0][3] + sa[1][3]);
+                sc[0][2] = (sb[0][0] + sb[1][0]) + (sb[0][2] + sb[1][2]);
+                sc[0][3] = (sb[0][1] + sb[1][1]) + (sb[0][3] + sb[1][3]);
+            } else if constexpr (WIDE) {
 #pragma unroll
                 for (int qi = 0; qi < 2; ++qi) {
                     sc[qi][0] = sa[0][2 * qi] + sa[1][2 * qi];
@@ -1256,29 +1324,62 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                     o[nb][3] *= a_g8;
                 }
             }
-            // A fragments of [P_hi; P_lo] over the 16 keys (WIDE: P_hi and P_lo of both queries)
-            uint32_t pa[NA][4];
-            if constexpr (WIDE) {
-                split_bf16(pw[0][0], pw[0][1], pa[0][0], pa[1][0]);   // row g,     keys 2t, 2t+1
-                split_bf16(pw[1][0], pw[1][1], pa[0][1], pa[1][1]);   // row g + 8
-                split_bf16(pw[0][2], pw[0][3], pa[0][2], pa[1][2]);   // row g,     keys 8+2t, 9+2t
-                split_bf16(pw[1][2], pw[1][3], pa[0][3], pa[1][3]);   // row g + 8
+            if constexpr (F32) {
+                // O += [P_big; P_rest] V over two k-steps of 8 keys.  In step kk, k index t
+                // stands for key 8kk + 2t and k index t + 4 for key 8kk + 2t + 1 (the keys
+                // whose weights this lane holds); V's rows are read in the same order, at
+                // feature 8nb + g (the 128-byte swizzle keeps the 32 lanes on 32 banks).
+                uint32_t pa[2][4];
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    split_tf32(pw[0][2 * kk], pa[kk][0], pa[kk][1]);
+                    split_tf32(pw[0][2 * kk + 1], pa[kk][2], pa[kk][3]);
+                }
+                const unsigned char* vcol = Vs + ((g & 3) << 2);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int r0 = 8 * kk + 2 * t;
+#pragma unroll
+                    for (int n0 = 0; n0 < M::NB; n0 += 4) {   // 4 n-blocks: independent MMAs in a row
+                        uint32_t vg[4][2], vr[4][2];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int c = 2 * (n0 + j) + (g >> 2);   // chunk of feature 8(n0+j) + g
+                            split_tf32(*reinterpret_cast<const float*>(vcol + swz(r0, c)), vg[j][0], vr[j][0]);
+                            split_tf32(*reinterpret_cast<const float*>(vcol + swz(r0 + 1, c)), vg[j][1],
+                                       vr[j][1]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) mma_tf32(o[n0 + j], pa[kk], vg[j][0], vg[j][1]);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) mma_tf32(o[n0 + j], pa[kk], vr[j][0], vr[j][1]);
+                    }
+                }
             } else {
-                split_bf16(pw[0][0], pw[0][1], pa[0][0], pa[0][1]);
-                split_bf16(pw[0][2], pw[0][3], pa[0][2], pa[0][3]);
-            }
-            // O += [P_hi; P_lo] V : V[key][dim] as the k x n operand, transposed on load
-            const uint32_t vbase = smem_u32(Vs);
+                // A fragments of [P_hi; P_lo] over the 16 keys (WIDE: P_hi and P_lo of both queries)
+                uint32_t pa[NA][4];
+                if constexpr (WIDE) {
+                    split_bf16(pw[0][0], pw[0][1], pa[0][0], pa[1][0]);   // row g,     keys 2t, 2t+1
+                    split_bf16(pw[1][0], pw[1][1], pa[0][1], pa[1][1]);   // row g + 8
+                    split_bf16(pw[0][2], pw[0][3], pa[0][2], pa[1][2]);   // row g,     keys 8+2t, 9+2t
+                    split_bf16(pw[1][2], pw[1][3], pa[0][3], pa[1][3]);   // row g + 8
+                } else {
+                    split_bf16(pw[0][0], pw[0][1], pa[0][0], pa[0][1]);
+                    split_bf16(pw[0][2], pw[0][3], pa[0][2], pa[0][3]);
+                }
+                // O += [P_hi; P_lo] V : V[key][dim] as the k x n operand, transposed on load
+                const uint32_t vbase = smem_u32(Vs);
 #pragma unroll
-            for (int np = 0; np < M::NB / 2; ++np) {
-                // matrices: (keys 0-7, chunk 2np), (keys 8-15, 2np), (keys 0-7, 2np+1), (keys 8-15, 2np+1)
-                const int key = ((mj & 1) << 3) + mr;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vbase + swz(key, 2 * np + (mj >> 1)), b0, b1, b2, b3);
+                for (int np = 0; np < M::NB / 2; ++np) {
+                    // matrices: (keys 0-7, chunk 2np), (keys 8-15, 2np), (keys 0-7, 2np+1), (keys 8-15, 2np+1)
+                    const int key = ((mj & 1) << 3) + mr;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(vbase + swz(key, 2 * np + (mj >> 1)), b0, b1, b2, b3);
 #pragma unroll
-                for (int a = 0; a < NA; ++a) {
-                    mma_bf16(o[2 * np], pa[a], b0, b1);
-                    mma_bf16(o[2 * np + 1], pa[a], b2, b3);
+                    for (int a = 0; a < NA; ++a) {
+                        mma_bf16(o[2 * np], pa[a], b0, b1);
+                        mma_bf16(o[2 * np + 1], pa[a], b2, b3);
+                    }
                 }
             }
         }
@@ -1474,32 +1575,32 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     return cudaSuccess;
 }
 
-template <int D, int G>
+template <typename T, int D, int G>
 static cudaError_t prepare_mma() {
     static bool done = false;   // per instantiation
     if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(split_decode_mma_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(split_decode_mma_kernel<T, D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MmaGeo<D>::CTA_SMEM);
+                                         MmaGeo<T, D>::CTA_SMEM);
     if (e == cudaSuccess) done = true;
     return e;
 }
 
-template <int D, int G>
+template <typename T, int D, int G>
 static int resident_workers_mma(int num_sms) {
-    if (prepare_mma<D, G>() != cudaSuccess) return 0;
+    if (prepare_mma<T, D, G>() != cudaSuccess) return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_mma_kernel<D, G>,
-                                                      MmaGeo<D>::WARPS * 32, MmaGeo<D>::CTA_SMEM) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_mma_kernel<T, D, G>,
+                                                      MmaGeo<T, D>::WARPS * 32,
+                                                      MmaGeo<T, D>::CTA_SMEM) != cudaSuccess)
         return 0;
-    return blocks * num_sms * MmaGeo<D>::WARPS;
+    return blocks * num_sms * MmaGeo<T, D>::WARPS;
 }
 
-template <int D, int G>
+template <typename T, int D, int G>
 static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stream) {
-    using M = MmaGeo<D>;
-    cudaError_t e = prepare_mma<D, G>();
+    using M = MmaGeo<T, D>;
+    cudaError_t e = prepare_mma<T, D, G>();
     if (e != cudaSuccess) return e;
     if (p.epoch == 0) {
         plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
@@ -1521,7 +1622,7 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<D, G>, p, tmk, tmv)) != cudaSuccess)
+    if ((e = cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<T, D, G>, p, tmk, tmv)) != cudaSuccess)
         return e;
     if (p.pre_ml != nullptr) {
         const int64_t rows = (int64_t)p.B * p.H * G;
@@ -1532,13 +1633,18 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
     return cudaSuccess;
 }
 
-// The tensor-core kernel serves grouped-query pools; for one query head per KV
-// head the CUDA-core kernel is as fast (measured on GB300) and is kept.
-#define PKV_FOR_EACH_MMA(X) X(64, 2) X(64, 4) X(64, 8) X(64, 16) X(128, 2) X(128, 4) X(128, 8) \
-    X(128, 16)
+// The tensor-core kernel serves grouped-query pools (bf16 on bf16 MMAs, fp32 on
+// split tf32 MMAs); for one query head per KV head the CUDA-core kernel is as fast
+// (measured on GB300) and is kept.
+#define PKV_FOR_EACH_MMA(X) X(__nv_bfloat16, 64, 2) X(__nv_bfloat16, 64, 4) X(__nv_bfloat16, 64, 8) \
+    X(__nv_bfloat16, 64, 16) X(__nv_bfloat16, 128, 2) X(__nv_bfloat16, 128, 4)                    \
+    X(__nv_bfloat16, 128, 8) X(__nv_bfloat16, 128, 16) X(float, 64, 2) X(float, 64, 4)           \
+    X(float, 64, 8) X(float, 128, 2) X(float, 128, 4) X(float, 128, 8)
 
 bool mma_supported(int dtype, int D, int G) {
-    return dtype == PKV_BF16 && (D == 64 || D == 128) && (G == 2 || G == 4 || G == 8 || G == 16);
+    if (D != 64 && D != 128) return false;
+    if (dtype == PKV_BF16) return G == 2 || G == 4 || G == 8 || G == 16;
+    return dtype == PKV_F32 && (G == 2 || G == 4 || G == 8);
 }
 
 // Instantiated geometries: every head width for multi-head attention; groups
@@ -1556,8 +1662,9 @@ bool decode_supported(int dtype, int D, int G) {
 
 int resident_workers(int dtype, int D, int G, int num_sms, bool tensor_cores) {
     if (tensor_cores) {
-#define PKV_RWM(DD, GG) \
-        if (D == DD && G == GG) return resident_workers_mma<DD, GG>(num_sms);
+#define PKV_RWM(TT, DD, GG)                                             \
+        if (dtype == (sizeof(TT) == 4 ? PKV_F32 : PKV_BF16) && D == DD && G == GG) \
+            return resident_workers_mma<TT, DD, GG>(num_sms);
         PKV_FOR_EACH_MMA(PKV_RWM)
 #undef PKV_RWM
         return 0;
@@ -1614,8 +1721,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.pre_stride = a.pre_stride;
     if (a.tmap_k != nullptr && a.tmap_v != nullptr) {
         if (a.table_rows != nullptr) return cudaErrorInvalidValue;   // CUDA-core kernel only
-#define PKV_LAUNCH_MMA(DD, GG) \
-        if (a.D == DD && a.G == GG) return launch_mma<DD, GG>(a, p, stream);
+#define PKV_LAUNCH_MMA(TT, DD, GG)                                                   \
+        if (a.dtype == (sizeof(TT) == 4 ? PKV_F32 : PKV_BF16) && a.D == DD && a.G == GG) \
+            return launch_mma<TT, DD, GG>(a, p, stream);
         PKV_FOR_EACH_MMA(PKV_LAUNCH_MMA)
 #undef PKV_LAUNCH_MMA
         return cudaErrorInvalidValue;

@@ -85,7 +85,7 @@ struct pkv_pool {
     cudaEvent_t ev_before = nullptr;   // optional split-kernel timing events
     cudaEvent_t ev_after = nullptr;
     bool tensor_cores = false;         // decode: K/V tiles by TMA tensor loads, products by MMA
-    bool tmaps = false;                // tensor maps built (bf16, head_dim 64 or 128)
+    bool tmaps = false;                // tensor maps built (head_dim 64 or 128)
     std::vector<CUtensorMap> tmap_k;   // per layer, when tmaps
     std::vector<CUtensorMap> tmap_v;
 };
@@ -202,17 +202,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// One layer's K or V pool as a 2-D bf16 tensor [pages*H*P rows][D columns],
-// read in boxes of 16 rows x 64 columns (one 128-byte row each) with the
-// 128-byte swizzle.
-bool encode_pool_map(CUtensorMap* map, void* base, int64_t rows, int D) {
+// One layer's K or V pool as a 2-D tensor [pages*H*P rows][D columns] of the
+// storage type, read in boxes of 16 rows x 128 bytes (64 bf16 or 32 fp32 columns)
+// with the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, void* base, int64_t rows, int D, int dtype) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
+    const int es = dtype == PKV_F32 ? 4 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)pkv::kTile};
+    cuuint64_t strides[1] = {(cuuint64_t)D * es};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)pkv::kTile};
     cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+    return fn(map, dtype == PKV_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              2, base, dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -386,11 +388,12 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
         }
         p->sms = sms;
         const int64_t rows = pages * page_size * heads;   // pool rows of one layer
-        p->tmaps = dtype == PKV_BF16 && (head_dim == 64 || head_dim == 128) && rows < INT32_MAX &&
+        p->tmaps = (head_dim == 64 || head_dim == 128) && rows < INT32_MAX &&
                    tensor_map_encoder() != nullptr;
         p->tensor_cores = p->tmaps && !(flags & PKV_POOL_CUDA_CORES) &&
                           pkv::mma_supported(dtype, head_dim, p->dec_group);
-        if (p->tensor_cores && p->group >= 16) {   // lanes of 16 query heads
+        if (p->tensor_cores && p->group >= 16 && pkv::mma_supported(dtype, head_dim, 16)) {
+            // lanes of 16 query heads
             p->dec_group = 16;
             p->kv_shift = 0;
             while ((p->dec_group << p->kv_shift) < p->group) ++p->kv_shift;
@@ -420,8 +423,8 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
             for (int l = 0; l < layers; ++l) {
                 char* kb = static_cast<char*>(p->k_base) + p->layer_bytes * (size_t)l;
                 char* vb = static_cast<char*>(p->v_base) + p->layer_bytes * (size_t)l;
-                if (!encode_pool_map(&p->tmap_k[(size_t)l], kb, rows, head_dim) ||
-                    !encode_pool_map(&p->tmap_v[(size_t)l], vb, rows, head_dim)) {
+                if (!encode_pool_map(&p->tmap_k[(size_t)l], kb, rows, head_dim, dtype) ||
+                    !encode_pool_map(&p->tmap_v[(size_t)l], vb, rows, head_dim, dtype)) {
                     cudaFree(p->k_base);
                     cudaFree(p->v_base);
                     cudaFree(p->dev_error);

@@ -295,6 +295,45 @@ def test_gqa_batched(group, D, dtype):
                                  group=group))
 
 
+# fp32 pools with several query heads per KV head run the tensor-core kernel on
+# split tf32 products (each operand as its tf32 rounding plus the rounding of the
+# rest; all four cross products), held to the fp32 bar; PKV_POOL_CUDA_CORES keeps
+# the CUDA-core kernel for the same geometry.
+
+@pytest.mark.parametrize("group,D", [(2, 64), (8, 128)])
+def test_gqa_fp32_cuda_core_kernel(group, D):
+    lens = [1, 16, 17, 300, 1000, 33, 2048, 5]
+    _batched_check(make_workload(f"cc32_{group}", lens, 2, D, dtype=F32, seed=140 + group,
+                                 group=group), cuda_cores=True)
+
+
+def test_fp32_tensor_core_and_cuda_core_kernels_agree():
+    w = make_workload("agree32", [1, 15, 16, 17, 500, 4096, 33], 2, 128, dtype=F32, seed=62,
+                      group=8)
+    a, b = BatchedRun(w), BatchedRun(w, cuda_cores=True)
+    try:
+        assert a.pool.kernel_name() == "split_decode_mma_kernel<f32,128,8>"
+        assert b.pool.kernel_name() == "split_decode_kernel<f32,128,8>"
+        oa, ob = a.run().cpu().numpy(), b.run().cpu().numpy()
+        assert np.abs(oa - ob).max() < 4e-6
+    finally:
+        a.close()
+        b.close()
+
+
+@pytest.mark.parametrize("group,D,P,window", [(4, 128, 32, 0), (8, 64, 64, 0), (2, 128, 16, 100),
+                                              (8, 128, 16, 4000)])
+def test_gqa_fp32_tensor_core_pages_and_windows(group, D, P, window):
+    lens = [1, 15, 16, 17, 64, 65, 500, 1999, 4096]
+    _batched_check(make_workload(f"tc32_{group}_{P}_{window}", lens, 2, D, P=P, dtype=F32,
+                                 seed=150 + group + P, group=group, window=window))
+
+
+def test_gqa_fp32_tensor_core_serial_with_abort():
+    c, _ = _serial(2, 2, 128, F32, 64, 300, 70, 14, abort_at=33, P=32, group=4)
+    assert c["score_cells"] == 2 * 8 * sum(range(1, 71))
+
+
 def test_gqa_full_config_every_lane():
     """64 requests, 8 KV heads x 8 query heads, d_h=128, bf16, t ~ U{1..8192}."""
     _batched_check(workloads.gqa(8))
@@ -367,17 +406,23 @@ def test_kernel_selection():
     def pool(**kw):
         return pkv.Pool(1, 8, 2, kw.pop("D", 128), 16, kw.pop("dtype", "bf16"), 64, **kw)
     with pool(query_heads=16) as p:
-        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<128,8>"
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<bf16,128,8>"
     with pool(query_heads=32) as p:
-        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<128,16>"
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<bf16,128,16>"
     with pool(query_heads=64, D=64) as p:
-        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<64,16>"
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<bf16,64,16>"
     with pool(query_heads=16, cuda_cores=True) as p:
         assert not p.tensor_cores
     with pool() as p:
         assert not p.tensor_cores
     with pool(query_heads=4, dtype="f32") as p:
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<f32,128,2>"
+    with pool(query_heads=64, dtype="f32", D=64) as p:
+        assert p.tensor_cores and p.kernel_name() == "split_decode_mma_kernel<f32,64,8>"
+    with pool(dtype="f32") as p:
         assert not p.tensor_cores
+    with pool(query_heads=4, dtype="f32", cuda_cores=True) as p:
+        assert not p.tensor_cores and p.kernel_name() == "split_decode_kernel<f32,128,2>"
 
 
 @pytest.mark.parametrize("group,D", [(2, 64), (4, 128), (8, 128)])
@@ -425,7 +470,7 @@ def test_wide_lanes_agree_with_cuda_core_lanes_of_8():
                       group=32)
     a, b = BatchedRun(w), BatchedRun(w, cuda_cores=True)
     try:
-        assert a.pool.kernel_name() == "split_decode_mma_kernel<128,16>"
+        assert a.pool.kernel_name() == "split_decode_mma_kernel<bf16,128,16>"
         assert b.pool.kernel_name() == "split_decode_kernel<bf16,128,8>"
         oa, ob = a.run().cpu().numpy(), b.run().cpu().numpy()
         rel = np.abs(oa - ob).max(axis=-1) / np.maximum(np.abs(ob).max(axis=-1), 1e-6)
