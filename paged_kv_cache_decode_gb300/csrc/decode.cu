@@ -972,16 +972,12 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// tf32 rounding of x and of the remainder: x = big + rest to ~2^-22 relative
+// x as big + rest, both tf32 values: big is x with its 13 low mantissa bits
+// cleared, rest the cleared part (exact in fp32) with its own 13 low bits cleared,
+// so |x - big - rest| < 2^-20 |x|.  Two logic operations and one subtraction.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& big, uint32_t& rest) {
-    big = to_tf32(x);
-    rest = to_tf32(x - __uint_as_float(big));
+    big = __float_as_uint(x) & 0xffffe000u;
+    rest = __float_as_uint(x - __uint_as_float(big)) & 0xffffe000u;
 }
 
 // Shared-memory tile geometry of the tensor-core kernel for storage type T:
@@ -1003,9 +999,16 @@ struct MmaGeo {
     static constexpr int WARPS = PKV_MMA_WARPS;
     static constexpr int STAGES = PKV_MMA_STAGES;
 #else
-    // the CUDA-core kernel's grouped geometry for the same bytes per tile
-    static constexpr int WARPS = Geo<T, D, sizeof(T) == 4 ? 2 : 1>::WARPS;
-    static constexpr int STAGES = Geo<T, D, sizeof(T) == 4 ? 2 : 1>::STAGES;
+    // bf16: the CUDA-core kernel's geometry for the same bytes per tile.  fp32: as many
+    // warps (up to 8) as fit with two stages each (7 at head width 128: the kernel is
+    // latency-bound, so warps beat stages), then as many stages as fit (up to 4).
+    static constexpr int SMEM_MAX = 227 * 1024 - 1024;   // less the swizzle alignment
+    static constexpr int F32_WARPS = SMEM_MAX / (2 * (STAGE_BYTES + 12)) < 8
+                                         ? SMEM_MAX / (2 * (STAGE_BYTES + 12)) : 8;
+    static constexpr int F32_STAGES = SMEM_MAX / (F32_WARPS * (STAGE_BYTES + 12)) < 4
+                                          ? SMEM_MAX / (F32_WARPS * (STAGE_BYTES + 12)) : 4;
+    static constexpr int WARPS = ES == 4 ? F32_WARPS : Geo<T, D>::WARPS;
+    static constexpr int STAGES = ES == 4 ? F32_STAGES : Geo<T, D>::STAGES;
 #endif
     static constexpr int WARP_SMEM = STAGES * STAGE_BYTES;
     // stage rings (1024-byte aligned, as the swizzle requires), then mbarriers and page ids
@@ -1024,10 +1027,10 @@ __global__ void __launch_bounds__(MmaGeo<T, D>::WARPS * 32, 1)
 split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
     using M = MmaGeo<T, D>;
-    // F32: fp32 storage on tf32 MMAs (m16n8k8).  Every fp32 operand is split into its
-    // tf32 rounding and the tf32 rounding of the remainder (together ~2^-22 relative);
-    // [big; rest] rows of q (or P) times the big and the rest parts of K (or V) give all
-    // four cross products, each exact in fp32, so S and O keep fp32 accuracy.
+    // F32: fp32 storage on tf32 MMAs (m16n8k8).  Every fp32 operand is split into two
+    // tf32 parts (big + rest, within 2^-20 relative); [big; rest] rows of q (or P) times
+    // the big and the rest parts of K (or V) give all four cross products, each exact in
+    // fp32, so S and O keep fp32-level accuracy.
     constexpr bool F32 = sizeof(T) == 4;
     static_assert((G >= 1 && G <= 8) || (G == 16 && !F32), "1 to 8 (bf16: or 16) query heads per KV head");
     // WIDE (G = 16): lane l owns queries l / 4 and l / 4 + 8, the A operands are
