@@ -81,8 +81,8 @@ typedef enum pkv_dtype {
                                    storage, so append/attend entry points return PKV_ERR_NO_STORAGE */
 
 #define PKV_POOL_CUDA_CORES 2u  /* use the CUDA-core kernel even where the tensor-core kernel
-                                   applies (bf16 storage, head_dim 64 or 128, 2 or more query
-                                   heads per KV head) */
+                                   applies (bf16 or fp32 storage, head_dim 64 or 128, 2 or
+                                   more query heads per KV head) */
 
 /* bits of the device error word */
 #define PKV_DEVERR_SEQ_LEN 1u   /* a seq_len < 1, > max_seq_len, or needing > max_pages pages */
@@ -161,8 +161,8 @@ int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page
 /* Create a pool from options (see pkv_pool_options).  Grouped-query and
  * multi-query pools (query_heads = G x kv_heads) are implemented for G in
  * {2, 4, 8, 16, 32, 64, 128} at head_dim 64 and 128 (else PKV_ERR_UNSUPPORTED,
- * unless HOST_ONLY).  Decode on the tensor-core kernel runs a group above 16 as
- * G / 16 lanes of 16 query heads per KV head, the CUDA-core kernel a group above 8
+ * unless HOST_ONLY).  Decode on the bf16 tensor-core kernel runs a group above 16
+ * as G / 16 lanes of 16 query heads per KV head, the other kernels a group above 8
  * as G / 8 lanes of 8, each lane reading the KV head's pages (the repeats mostly
  * from L2). */
 int pkv_pool_create_ex(const pkv_pool_options* options, pkv_pool** out);
@@ -170,9 +170,11 @@ int pkv_pool_create_ex(const pkv_pool_options* options, pkv_pool** out);
 /* KV heads stored per page and heads of the query (either pointer may be NULL). */
 int pkv_pool_heads(const pkv_pool* pool, int* kv_heads, int* query_heads);
 
-/* *tensor_cores = 1 if the pool's attention runs the tensor-core kernel (bf16,
- * head_dim 64 or 128, 2 or more query heads per KV head, not
- * PKV_POOL_CUDA_CORES), 0 for the CUDA-core kernel. */
+/* *tensor_cores = 1 if the pool's decode attention runs the tensor-core kernel
+ * (head_dim 64 or 128, 2 or more query heads per KV head, not
+ * PKV_POOL_CUDA_CORES; bf16 products with fp32 accumulation for bf16 pools, and
+ * for fp32 pools tf32 products of each operand's two tf32 parts, which keep fp32
+ * accuracy), 0 for the CUDA-core kernel. */
 int pkv_pool_kernel(const pkv_pool* pool, int* tensor_cores);
 
 /* Free the pool and its device storage.  PKV_ERR_BAD_STATE while any request
