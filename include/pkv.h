@@ -485,9 +485,9 @@ int pkv_prefill_workspace_size(const pkv_pool* pool, int batch, int64_t total_ne
  * then chunk token i of request b runs as one decode request of retained length
  * L0_b + i + 1 over request b's pages, all in one decode launch, with the decode
  * kernels' precision (fp32 weights; a bf16 q widened exactly to fp32).
- * Stateless over bookkeeping: the caller owns lengths and tables.  Bad lengths or page ids found on the device set the pool's error
- * word (a bad page reads as zeros); the affected rows of `out` are then
- * unspecified.  Once a wait has run out (PKV_DEVERR_TIMEOUT), later prefill
+ * Stateless over bookkeeping: the caller owns lengths and tables.  Bad lengths
+ * or page ids found on the device set the pool's error word (a bad page reads as
+ * zeros); the affected rows of `out` are then unspecified.  Once a wait has run out (PKV_DEVERR_TIMEOUT), later prefill
  * calls skip their attention work until pkv_check_device_status clears the
  * word.  Enqueues three kernels on `stream` (plan, append, attention; or rows,
  * decode plan, decode split) and returns without waiting; calls whose device

@@ -1022,10 +1022,11 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)((c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool ROWS = false>
 __global__ void __launch_bounds__(MmaGeo<T, D>::WARPS * 32, 1)
 split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
+    // ROWS: request b reads page-table row p.table_rows[b], as in split_decode_kernel
     using M = MmaGeo<T, D>;
     // F32: fp32 storage on tf32 MMAs (m16n8k8).  Every fp32 operand is split into two
     // tf32 parts (big + rest, within 2^-20 relative); [big; rest] rows of q (or P) times
@@ -1101,7 +1102,8 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             tab_b = prod.b;
             tab_base = prod.page_idx;
             const int64_t e = tab_base + lane;
-            tab_val = e < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages + e) : -1;
+            const int64_t row = ROWS ? (int64_t)__ldg(p.table_rows + tab_b) : (int64_t)tab_b;
+            tab_val = e < p.max_pages ? __ldg(p.tables + row * p.max_pages + e) : -1;
         }
         const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(prod.page_idx - tab_base));
         if (lane != 0) return;
@@ -1582,9 +1584,12 @@ template <typename T, int D, int G>
 static cudaError_t prepare_mma() {
     static bool done = false;   // per instantiation
     if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(split_decode_mma_kernel<T, D, G>,
+    cudaError_t e = cudaFuncSetAttribute(split_decode_mma_kernel<T, D, G, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          MmaGeo<T, D>::CTA_SMEM);
+    if (e == cudaSuccess && sizeof(T) == 4)   // table rows: fp32 only (the decode-lane prefill)
+        e = cudaFuncSetAttribute(split_decode_mma_kernel<T, D, G, sizeof(T) == 4>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, MmaGeo<T, D>::CTA_SMEM);
     if (e == cudaSuccess) done = true;
     return e;
 }
@@ -1593,7 +1598,7 @@ template <typename T, int D, int G>
 static int resident_workers_mma(int num_sms) {
     if (prepare_mma<T, D, G>() != cudaSuccess) return 0;
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_mma_kernel<T, D, G>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, split_decode_mma_kernel<T, D, G, false>,
                                                       MmaGeo<T, D>::WARPS * 32,
                                                       MmaGeo<T, D>::CTA_SMEM) != cudaSuccess)
         return 0;
@@ -1625,8 +1630,11 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<T, D, G>, p, tmk, tmv)) != cudaSuccess)
-        return e;
+    if (p.table_rows != nullptr && sizeof(T) != 4) return cudaErrorInvalidValue;
+    e = p.table_rows != nullptr
+            ? cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<T, D, G, sizeof(T) == 4>, p, tmk, tmv)
+            : cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<T, D, G, false>, p, tmk, tmv);
+    if (e != cudaSuccess) return e;
     if (p.pre_ml != nullptr) {
         const int64_t rows = (int64_t)p.B * p.H * G;
         combine_kernel<D, G><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
@@ -1723,7 +1731,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.pre_splits = a.pre_splits;
     p.pre_stride = a.pre_stride;
     if (a.tmap_k != nullptr && a.tmap_v != nullptr) {
-        if (a.table_rows != nullptr) return cudaErrorInvalidValue;   // CUDA-core kernel only
+        // table rows on the tensor-core kernel: fp32 pools only (the bf16 pools it
+        // serves prefill on the tcgen05 kernel, not through decode lanes)
+        if (a.table_rows != nullptr && a.dtype != PKV_F32) return cudaErrorInvalidValue;
 #define PKV_LAUNCH_MMA(TT, DD, GG)                                                   \
         if (a.dtype == (sizeof(TT) == 4 ? PKV_F32 : PKV_BF16) && a.D == DD && a.G == GG) \
             return launch_mma<TT, DD, GG>(a, p, stream);

@@ -179,8 +179,11 @@ pkv::PrefillLanesArgs lanes_args(pkv_pool* p, int layer, int64_t n) {
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
-    a.tmap_k = nullptr;   // decode lanes read table rows: the CUDA-core kernel
-    a.tmap_v = nullptr;
+    // decode lanes read table rows: on the tensor-core kernel for fp32 pools that use
+    // it (the bf16 pools it serves prefill on the tcgen05 kernel, not through lanes)
+    const bool tc = p->tensor_cores && p->dtype == PKV_F32;
+    a.tmap_k = tc ? &p->tmap_k[(size_t)layer] : nullptr;
+    a.tmap_v = tc ? &p->tmap_v[(size_t)layer] : nullptr;
     return a;
 }
 
