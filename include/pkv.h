@@ -153,7 +153,10 @@ int pkv_pool_options_init(pkv_pool_options* options);
  * Equivalent to pkv_pool_create_ex with kv_heads = query_heads = heads.
  * Device storage is 2 * layers * pages * page_size * heads * head_dim * element
  * size bytes ([ROLLOUT-KV]), zero-filled; the pool also allocates a 4-byte
- * device error word.  On success *out receives the handle.
+ * device error word.  A device pool also makes sure that the library's fixed
+ * scratch array of pkv_paged_decode_attention_static (PKV_STATIC_SCRATCH_BYTES)
+ * is loaded on the current device, once per context.  On success *out receives
+ * the handle.
  */
 int pkv_pool_create(int layers, int64_t pages, int heads, int head_dim, int page_size, int dtype,
                     int64_t max_context, uint64_t seed, unsigned flags, pkv_pool** out);
@@ -412,7 +415,10 @@ int pkv_paged_decode_attention_shared(pkv_pool* pool, int layer, int batch, cons
 
 /*
  * Bytes of the fixed device array that pkv_paged_decode_attention_static uses
- * as scratch (8 MiB).  Every GPU that loads libpkv.so holds it until exit.
+ * as scratch (8 MiB).  The CUDA runtime loads the array lazily, in each context
+ * the first time its address is asked for; pkv_pool_create does so on the
+ * pool's device, so the array is in place once a device pool exists, and it
+ * stays until the context is destroyed (normally at process exit).
  */
 #define PKV_STATIC_SCRATCH_BYTES (8u << 20)
 
@@ -427,14 +433,19 @@ int pkv_paged_decode_attention_shared(pkv_pool* pool, int layer, int batch, cons
  * pkv_paged_decode_attention.
  *
  * Scratch is a file-scope device array of PKV_STATIC_SCRATCH_BYTES inside the
- * library.  The call makes no cudaMalloc, cudaFree or other allocating call.
- * The first call on a device (with that device current) looks up the array's
- * device address with cudaGetSymbolAddress; make that first call before any
- * stream capture.  A batch whose scratch need (pkv_workspace_size) exceeds
+ * library.  The call makes no cudaMalloc, cudaFree or other allocating call: it
+ * asks the runtime for the array's device address in the current context
+ * (cudaGetSymbolAddress) on every call, a lookup once the array is loaded.  The
+ * array is loaded when the pool is created (see PKV_STATIC_SCRATCH_BYTES); in a
+ * context where no pool was created, for instance after a device reset, the
+ * first call loads it and so allocates it, and should come before the
+ * application reserves the rest of the device's memory and before any stream
+ * capture.  A batch whose scratch need (pkv_workspace_size) exceeds
  * PKV_STATIC_SCRATCH_BYTES is rejected with PKV_ERR_INVALID_ARGUMENT and
  * changes nothing.  All calls on a device share the array and it keeps the last
- * call's contents (no part of it needs to start at zero); calls whose device
- * work can overlap race on it and must be serialised by the caller, for
+ * call's contents: the per-lane arrival counters, the only part that must start
+ * at zero, are cleared by each call's own plan kernel.  Calls whose device work
+ * can overlap race on the array and must be serialised by the caller, for
  * instance by issuing them on one stream.
  */
 int pkv_paged_decode_attention_static(pkv_pool* pool, int layer, int batch, const float* q,
@@ -480,7 +491,8 @@ int pkv_prefill_workspace_size(const pkv_pool* pool, int batch, int64_t total_ne
  *                (caller owned, 16-byte aligned, no initialisation needed)
  * Two implementations, chosen by the pool.  bf16 pools of head_dim 64 or 128:
  * the tcgen05 tensor cores, bf16 products with fp32 accumulation, the weights
- * rounded to bf16 before they multiply V; batch <= 1024.  Every other pool (fp32
+ * split into bf16 hi + lo before they multiply V (each weight carried
+ * to about 2^-16); batch <= 1024.  Every other pool (fp32
  * storage, other head widths): decode lanes -- every chunk row is stored first,
  * then chunk token i of request b runs as one decode request of retained length
  * L0_b + i + 1 over request b's pages, all in one decode launch, with the decode

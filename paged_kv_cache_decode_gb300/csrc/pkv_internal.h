@@ -101,6 +101,10 @@ bool decode_supported(int dtype, int D, int G);
 // Enqueue the plan and split kernels on `stream`.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// Device address, in the current context, of the fixed scratch array of
+// pkv_paged_decode_attention_static; the first call in a context loads it.
+cudaError_t static_scratch_address(void** ptr);
+
 // Record a failed call in the thread's last-error message; returns `status`.
 int record_error(int status, const char* fmt, ...);
 

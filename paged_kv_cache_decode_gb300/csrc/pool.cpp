@@ -436,6 +436,17 @@ int pkv_pool_create_ex(const pkv_pool_options* opts, pkv_pool** out) {
                 }
             }
         }
+        // load the fixed scratch array of pkv_paged_decode_attention_static on this
+        // device now, while memory is available, rather than in that call
+        void* static_scratch = nullptr;
+        if ((e = pkv::static_scratch_address(&static_scratch)) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(p->k_base);
+            cudaFree(p->v_base);
+            cudaFree(p->dev_error);
+            delete p;
+            return cuda_fail(e, "loading the static scratch array");
+        }
         if ((e = cudaMemset(p->k_base, 0, total)) != cudaSuccess ||
             (e = cudaMemset(p->v_base, 0, total)) != cudaSuccess ||
             (e = cudaMemset(p->dev_error, 0, sizeof(unsigned))) != cudaSuccess ||

@@ -23,9 +23,10 @@
 // swizzle into a ring of slots, K and V of a tile in consecutive slots.  Per key
 // tile and query tile:
 //     S  = Q K^T               tcgen05.mma, M=128 N=128 K=d_h, fp32 in TMEM
-//     P  = 2^(c S - c m)       softmax warps: TMEM -> registers -> bf16 back into
-//                              TMEM over the S columns already read
-//     O += P V                 tcgen05.mma with A = P from TMEM, M=128 N=d_h K=128
+//     P  = 2^(c S - c m)       softmax warps: TMEM -> registers -> bf16 hi + lo
+//                              back into TMEM over the S columns already read
+//     O += P_hi V + P_lo V     tcgen05.mma with A = P from TMEM, M=128 N=d_h K=128,
+//                              twice: each weight carried to ~2^-16, not bf16's 2^-9
 // with c = log2(e) / sqrt(d_h).  Warp roles (320 threads):
 //   warps 0-3, 4-7  softmax of tiles A, B: warp w reads TMEM lanes 32(w%4) ..
 //              32(w%4)+31, one query row per thread; they stage Q, write P,
@@ -86,7 +87,7 @@ struct PfGeo {
     static constexpr int SMEM = FIXED + SLOTS * KV_BYTES;
     static constexpr uint32_t S_COL = 0;                     // S of tiles A and B: columns 0, 128
     static constexpr uint32_t O_COL = 256;                   // O of tiles A and B: 256, 256 + D
-    // P (bf16 pairs, 64 columns) overwrites the first half of its tile's S columns
+    // P_hi and P_lo (bf16 pairs, 64 columns each) overwrite their tile's S columns
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(D == 64 || D == 128, "prefill: head width 64 or 128");
     static_assert(SLOTS >= 3, "ring too small");
@@ -317,134 +318,103 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
             const int e_hi = full ? kKeys - 1
                                   : (int)(hi - k0 < kKeys - 1 ? (hi - k0 > -1 ? hi - k0 : -1)
                                                               : kKeys - 1);
-            // After a row block's first tile one pass usually does: the weights 2^(c s - c m)
-            // with the running m (packed FMA for the exponents, the row sum in two chains
-            // of packed adds, bf16 pairs for keys 2i, 2i+1 -> P column i), and the
-            // tile's row maximum in four chains.  They are kept when no row of the warp
-            // must raise m; else (and on the first tile) the warp takes the maximum, then
-            // the weights with the new m.
+            // The tile's row maximum first, from 1.5 reads of S: keys 64..127 for their
+            // maximum only, then keys 0..63 kept in registers.  With m settled (and O
+            // rescaled if it moved), the weights 2^(c s - c m) of keys 0..63 from those
+            // registers, then of keys 64..127 from a second read.  Each weight w is
+            // split into bf16 hi = rn(w) and lo = rn(w - hi) (w - hi is exact in fp32),
+            // so P_hi V + P_lo V carries w to about 2^-16 instead of bf16's 2^-9.  The
+            // pairs go back over the S columns of their own half, already read: keys
+            // 64hh + 2i, 2i+1 -> P_hi column 64hh + i, P_lo column 64hh + 32 + i.
             const float2 c2 = make_float2(c, c);
-            float mx = -INFINITY;
-            bool done = false;
-            if (j > 0) {
-                const float mb0 = m_used == -INFINITY ? 0.f : m_used * c;
-                const float2 nmb2 = make_float2(-mb0, -mb0);
-                float m4[4];
+            float m4[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) m4[k] = -INFINITY;
-                float2 acc[2];
+            for (int k = 0; k < 4; ++k) m4[k] = -INFINITY;
+            {
+                uint32_t sv[64];
+                tmem_ld32(t_s + 64, sv);
+                tmem_ld32(t_s + 96, sv + 32);
+                tmem_wait_ld();
+                if (!full) {
 #pragma unroll
-                for (int k = 0; k < 2; ++k) acc[k] = make_float2(0.f, 0.f);
-                uint32_t w[64];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t sv[64];
-                    tmem_ld32(t_s + hh * 64, sv);
-                    tmem_ld32(t_s + hh * 64 + 32, sv + 32);
-                    tmem_wait_ld();
-                    if (!full) {
-#pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[e]));
-#pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
-                        const float2 xe = __ffma2_rn(
-                            make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
-                        const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
-                        acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], pr);
-                        const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
-                        w[hh * 32 + (e >> 1)] = *reinterpret_cast<const uint32_t*>(&pb);
-                    }
+                    for (int e = 0; e < 64; ++e)
+                        if (64 + e < e_lo || 64 + e > e_hi) sv[e] = 0xff800000u;
                 }
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                const bool raise = mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f);
-                if (!__any_sync(0xffffffffu, raise)) {
-                    tmem_st32(t_s, w);
-                    tmem_st32(t_s + 32, w + 32);
-                    tmem_wait_st();
-                    const float2 a = __fadd2_rn(acc[0], acc[1]);
-                    l += a.x + a.y;
-                    done = true;
-                }
-            } else {
-                // row maximum, four independent chains, 64 columns at a time
-                float m4[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) m4[k] = -INFINITY;
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t sv[64];
-                    tmem_ld32(t_s + hh * 64, sv);
-                    tmem_ld32(t_s + hh * 64 + 32, sv + 32);
-                    tmem_wait_ld();
-                    if (!full) {
-#pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[e]));
-                }
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[e]));
             }
-            if (!done) {
-                float alpha = 1.f;
-                if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f)) {
-                    alpha = m_used == -INFINITY ? 0.f : ex2((m_used - mx) * c);
-                    m_used = mx;
-                    l *= alpha;
-                }
-                // S of this tile was committed after P V of the previous one, so that P V
-                // is complete: O may be rescaled
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t ov[32];
-                        tmem_ld32(t_o + cc * 32, ov);
-                        tmem_wait_ld();
+            uint32_t s0[64];                                  // S of keys 0..63
+            tmem_ld32(t_s, s0);
+            tmem_ld32(t_s + 32, s0 + 32);
+            tmem_wait_ld();
+            if (!full) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(t_o + cc * 32, ov);
-                    }
-                    tmem_wait_st();
-                }
-                // the weights with the new m, P over the S columns already read
-                const float mb = m_used == -INFINITY ? 0.f : m_used * c;
-                const float2 nmb2 = make_float2(-mb, -mb);
-                float2 acc[2];
+                for (int e = 0; e < 64; ++e)
+                    if (e < e_lo || e > e_hi) s0[e] = 0xff800000u;
+            }
 #pragma unroll
-                for (int k = 0; k < 2; ++k) acc[k] = make_float2(0.f, 0.f);
+            for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(s0[e]));
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            float alpha = 1.f;
+            if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f)) {
+                alpha = m_used == -INFINITY ? 0.f : ex2((m_used - mx) * c);
+                m_used = mx;
+                l *= alpha;
+            }
+            // S of this tile was committed after P V of the previous one, so that P V
+            // is complete: O may be rescaled
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t sv[64];
-                    tmem_ld32(t_s + hh * 64, sv);
-                    tmem_ld32(t_s + hh * 64 + 32, sv + 32);
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    tmem_ld32(t_o + cc * 32, ov);
                     tmem_wait_ld();
-                    if (!full) {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            if (hh * 64 + e < e_lo || hh * 64 + e > e_hi) sv[e] = 0xff800000u;
-                    }
-                    uint32_t w2[32];
-#pragma unroll
-                    for (int e = 0; e < 64; e += 2) {
-                        const float2 xe = __ffma2_rn(
-                            make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
-                        const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
-                        acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], pr);
-                        const __nv_bfloat162 pb = __floats2bfloat162_rn(pr.x, pr.y);
-                        w2[e >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-                    }
-                    tmem_st32(t_s + hh * 32, w2);
+                    for (int e = 0; e < 32; ++e)
+                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(t_o + cc * 32, ov);
                 }
                 tmem_wait_st();
-                const float2 a = __fadd2_rn(acc[0], acc[1]);
-                l += a.x + a.y;
             }
+            const float mb = m_used == -INFINITY ? 0.f : m_used * c;
+            const float2 nmb2 = make_float2(-mb, -mb);
+            float2 acc[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) acc[k] = make_float2(0.f, 0.f);
+            // weights of 64 keys -> 32 P_hi pairs at column `col`, 32 P_lo pairs at col + 32
+            auto weights = [&](const uint32_t* sv, uint32_t col) {
+                uint32_t phi[32], plo[32];
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 xe = __ffma2_rn(
+                        make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nmb2);
+                    const float2 pr = make_float2(ex2(xe.x), ex2(xe.y));
+                    acc[(e >> 1) & 1] = __fadd2_rn(acc[(e >> 1) & 1], pr);
+                    const __nv_bfloat162 hb = __floats2bfloat162_rn(pr.x, pr.y);
+                    const __nv_bfloat162 lb =
+                        __floats2bfloat162_rn(pr.x - __low2float(hb), pr.y - __high2float(hb));
+                    phi[e >> 1] = *reinterpret_cast<const uint32_t*>(&hb);
+                    plo[e >> 1] = *reinterpret_cast<const uint32_t*>(&lb);
+                }
+                tmem_st32(t_s + col, phi);
+                tmem_st32(t_s + col + 32, plo);
+            };
+            weights(s0, 0);
+            {
+                uint32_t sv[64];
+                tmem_ld32(t_s + 64, sv);
+                tmem_ld32(t_s + 96, sv + 32);
+                tmem_wait_ld();
+                if (!full) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (64 + e < e_lo || 64 + e > e_hi) sv[e] = 0xff800000u;
+                }
+                weights(sv, 64);
+            }
+            tmem_wait_st();
+            const float2 a = __fadd2_rn(acc[0], acc[1]);
+            l += a.x + a.y;
             tc_fence_before();
             mbar_arrive(&p_full[x]);
         }
@@ -544,12 +514,17 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
         auto issue_pv = [&](int j, int x) {
             const uint32_t v_addr = ring_addr + ((2 * j + 1) % M::SLOTS) * M::KV_BYTES;
             const uint64_t dv = sw128_desc(v_addr, kVLbo, 1024);
-            const uint32_t pa = tmem + M::S_COL + x * kKeys;        // P in TMEM, 8 columns per k-step
+            // P in TMEM: keys 16k .. 16k+15 are P_hi columns 64(k/4) + 8(k%4) .. +7 and the
+            // P_lo columns 32 further on
+            const uint32_t pa = tmem + M::S_COL + x * kKeys;
             const uint32_t o = tmem + M::O_COL + x * D;
 #pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k)
-                umma_bf16_tmem_a(o, pa + k * 8, dv + (uint64_t)((k * 16 * 128) >> 4), idO,
-                                 (j > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kKeys / 16; ++k) {
+                const uint64_t dvk = dv + (uint64_t)((k * 16 * 128) >> 4);
+                const uint32_t ph = pa + (k >> 2) * 64 + (k & 3) * 8;
+                umma_bf16_tmem_a(o, ph, dvk, idO, (j > 0 || k > 0) ? 1u : 0u);
+                umma_bf16_tmem_a(o, ph + 32, dvk, idO, 1u);
+            }
         };
         bool ok = pf_warp_wait(q_ready, 0, abort_flag, p.dev_error) && wait_slot(0);
         bool issued_any = false;

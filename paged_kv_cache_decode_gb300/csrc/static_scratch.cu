@@ -7,15 +7,26 @@
 // fragment it) and has no allocator to lend, or code on a latency-critical path
 // that must not call cudaMalloc / cudaFree because those can synchronise the
 // device and take milliseconds.  This entry point serves them: its scratch is a
-// fixed array in this library's device memory, sized PKV_STATIC_SCRATCH_BYTES,
-// which every GPU that loads the library holds until the process exits.
+// fixed array in this library's device memory, sized PKV_STATIC_SCRATCH_BYTES.
+//
+// When the array comes into being.  This file holds no kernel, so it is a module
+// of its own, and under the CUDA runtime's lazy module loading (the default) the
+// module -- and with it the array's 8 MiB -- is loaded in a context only when
+// something first asks for the array's address.  pkv_pool_create does that, on
+// the pool's device (static_scratch_address below), so the array is in place
+// before the caller's decode loop and before an application reserves the rest of
+// the GPU's memory; from then on it stays until the context is destroyed.
 //
 // The array is shared by every call on a device and keeps the previous call's
-// contents.  Nothing in it needs to start at zero: the plan kernel writes the
-// tile prefix and the worker table before any reader, and every partial slot the
-// merge kernel reads is written by the split kernel of the same call.  Calls
-// whose device work can overlap (different streams, or different host threads)
-// race on the array; serialise them, e.g. on one stream.
+// contents.  What must start at zero is cleared on every call: the per-lane
+// arrival counters at the start of the scratch, which the last arriving worker
+// of a lane relies on, are zeroed by the plan kernel of each batched call (a
+// batched call always runs its plan kernel; epoch-tagged counters are used only
+// by the single-request path, which never comes here).  The plan kernel also
+// writes the tile prefix and the worker table before any reader, and every
+// partial slot the merge reads is written by the split kernel of the same call.
+// Calls whose device work can overlap (different streams, or different host
+// threads) race on the array; serialise them, e.g. on one stream.
 
 #include <cuda_runtime.h>
 
@@ -28,11 +39,21 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 256;
-// Device address of g_static_scratch per device, looked up once per device.
-void* g_scratch_addr[kMaxDevices] = {};
-
 }  // namespace
+
+namespace pkv {
+
+// Device address of the array in the current context.  The name g_static_scratch
+// in host code is a host-side stand-in, not a device address; this asks the
+// runtime for the real one.  The first request in a context loads this file's
+// module (and so the array); later ones are a lookup.  Not cached: after a
+// device reset, or in another context of the same device, the address differs.
+cudaError_t static_scratch_address(void** ptr) {
+    *ptr = nullptr;
+    return cudaGetSymbolAddress(ptr, g_static_scratch);
+}
+
+}  // namespace pkv
 
 extern "C" int pkv_paged_decode_attention_static(pkv_pool* pool, int layer, int batch,
                                                  const float* q, const void* k_new,
@@ -50,22 +71,15 @@ extern "C" int pkv_paged_decode_attention_static(pkv_pool* pool, int layer, int 
             "batch %d x max_seq_len %lld needs %zu bytes of scratch, more than the %zu-byte "
             "static array; use pkv_paged_decode_attention with a workspace",
             batch, (long long)max_seq_len, need, (size_t)PKV_STATIC_SCRATCH_BYTES);
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return pkv::record_error(PKV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return pkv::record_error(PKV_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
-    if (g_scratch_addr[dev] == nullptr) {
-        // first call on this device (which is current): find the array's device address
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-        if (e != cudaSuccess || ptr == nullptr)
-            return pkv::record_error(PKV_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s",
-                                     cudaGetErrorString(e));
-        g_scratch_addr[dev] = ptr;
-    }
-    a.workspace = g_scratch_addr[dev];
+    // the lane counters in the array are zeroed by this call's plan kernel only
+    if (a.epoch != 0)
+        return pkv::record_error(PKV_ERR_BAD_STATE, "batched call with epoch-tagged counters");
+    void* ptr = nullptr;
+    cudaError_t e = pkv::static_scratch_address(&ptr);
+    if (e != cudaSuccess || ptr == nullptr)
+        return pkv::record_error(PKV_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s",
+                                 cudaGetErrorString(e));
+    a.workspace = ptr;
     a.workspace_bytes = PKV_STATIC_SCRATCH_BYTES;
     e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

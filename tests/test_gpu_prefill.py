@@ -1,11 +1,11 @@
 """Batched prefill on the device vs the fp64 oracle, through the C ABI.
 
 Bar: bit-exact K/V rows written into the pages; normwise relative error per
-(token, query head) row <= PREFILL_RTOL.  The tensor cores multiply V by the
-softmax weights rounded to bf16 (relative rounding error <= 2^-9 each), so a row
-of the output moves by at most 2^-8 x sum_j w_j |v_j| in exact arithmetic; for
-the N(0,1) rows of these workloads that is a few 1e-3 of the row's largest
-element at the worst of thousands of rows.
+(token, query head) row <= PREFILL_RTOL, the bf16-storage bar of decode.  q, k
+and v are the pool's bf16 values (the oracle reads the same bits); the tensor
+cores multiply V by the softmax weights split into bf16 hi + lo, which carries
+each weight to about 2^-16 relative, so the error left is that of fp32
+accumulation and the exp2 approximation, far inside the bar.
 """
 import numpy as np
 import pytest
@@ -17,7 +17,7 @@ from tests._gpu import PrefillRun, make_prefill
 
 pytestmark = pytest.mark.gpu
 
-PREFILL_RTOL = 1e-2
+PREFILL_RTOL = 5e-3
 
 
 @pytest.fixture(autouse=True)
