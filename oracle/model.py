@@ -20,7 +20,7 @@ Sources restated here:
   values = lanes x retained length per token); reset clears length and work;
   a rejected operation leaves the state unchanged.
 
-Readings where the sources are silent (each also listed in the design notes):
+Readings where the sources are silent:
 
 * free list: FIFO queue initialised to a Fisher-Yates shuffle of 0..pages-1
   driven by SplitMix64(seed), swap index ``next() mod (i + 1)`` for i from
