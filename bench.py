@@ -33,6 +33,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: achieved HBM GB/s (% of 8 TB/s) and decode tokens/s"
+PREFILL_METRIC = ("batched prefill attention into the paged cache: TFLOP/s (causal, algorithmic "
+                  "FLOPs) and new tokens/s")
+# further decode workloads measured in the default (long-context) run, each a short record
+EXTRA_WORKLOADS = ("batched_bf16", "batched_f32", "ragged")
 NOMINAL_HBM_GBS = 8000.0
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "decode.cu")
 PREFILL_SRC = os.path.join(ROOT, "paged_kv_cache_decode_gb300", "csrc", "prefill.cu")
@@ -106,6 +110,55 @@ def algorithmic_bytes(w) -> int:
     q_out = w.B * w.HQ * w.D * 4 * 2                             # query heads
     tables = int(w.n_pages.sum()) * 4 + w.B * 4
     return hist + new_rows + q_out + tables
+
+
+def decode_config(w, world: int, shared: int = 0) -> dict:
+    """The ``config`` object of a decode line; both arms print the same one."""
+    alg = algorithmic_bytes(w)
+    cfg = {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
+           "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P,
+           "pool_pages": w.pool_pages,
+           "seq_len_max": int(w.seq_lens.max()), "tokens_retained": int(w.seq_lens.sum()),
+           "storage": "bf16" if w.elem_bytes == 2 else "fp32", "accumulate": "fp32",
+           "alg_bytes_per_step": alg,
+           "logical_kv_bytes_per_step": logical_bytes(w),
+           "l2": f"inputs larger than L2 ({alg / 1e9:.2f} GB per step, no flush)"
+                 if alg > 129e6 else "inputs smaller than L2 (cache-warm)",
+           "parallelism": f"replicas x{world}"}
+    if shared:
+        cfg["path"] = (f"shared-prefix call: the {shared}-token prompt once per KV head on the "
+                       "tensor cores, each request's own positions by the split kernel, partials "
+                       "merged")
+    return cfg
+
+
+def prefill_config(w, world: int) -> dict:
+    """The ``config`` object of a prefill line; both arms print the same one."""
+    kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.H * w.D * 2 * 2
+    return {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
+            "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P,
+            "pool_pages": w.pool_pages, "new_tokens": int(w.new_tokens.sum()),
+            "cached_tokens": int((w.seq_lens - w.new_tokens).sum()),
+            "storage": "bf16", "accumulate": "fp32", "flops_per_step": prefill_flops(w),
+            "l2": f"K/V of the step {kv_bytes / 1e9:.2f} GB, re-read across query "
+                  f"tiles through L2 (no flush)",
+            "parallelism": f"replicas x{world}"}
+
+
+def serial_config(w, world: int) -> dict:
+    """The ``config`` object of a single-request line; both arms print the same one."""
+    t = int(w.seq_lens[0])
+    alg = token_bytes(w, t)
+    layer_alg = alg // w.layers
+    return {"workload": (f"single request: {w.layers} layers, H={w.H}, d_h={w.D}, "
+                         f"retained length t={t}, pool of {w.pool_pages} shuffled pages; "
+                         "a step is one token through every layer (transactional API)"),
+            "name": w.name, "layers": w.layers, "heads": w.H, "head_dim": w.D,
+            "page_size": w.P, "seq_len": t, "alg_bytes_per_step": alg,
+            "l2": f"{layer_alg / 1e6:.1f} MB per layer, {alg / 1e6:.0f} MB per token, no flush: "
+                  + ("every layer's history fits in the 129 MB L2 between tokens"
+                     if alg <= 129e6 else "larger than the 129 MB L2"),
+            "parallelism": f"replicas x{world}"}
 
 
 def logical_bytes(w) -> int:
@@ -297,7 +350,9 @@ def setup_device(w, torch, cuda_cores=False):
     return pool, reqs, host, dev, ws, out, max_seq_len
 
 
-def run_gpu(args):
+def run_gpu(args, compact=False):
+    """The decode step of args.workload; with compact=True (a further workload measured
+    in the same run) a short record without the end-to-end leg."""
     import torch
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -356,6 +411,26 @@ def run_gpu(args):
     torch.cuda.synchronize()
     pool.set_timing_events(None, None)
     kernel_ms = float(np.mean([b.elapsed_time(a) for b, a in zip(evb, eva)]))
+    assert pool.check_device_status() == 0
+    if compact:
+        if sampler:
+            sampler.stop()
+        alg = algorithmic_bytes(w)
+        peak, peak_kind = measured_peak_hbm()
+        achieved = alg / (kernel_ms * 1e-3) / 1e9
+        rec = {"workload": describe(w), "value": round(alg / (step_ms_max * 1e-3) / 1e9, 2),
+               "unit": "GB/s", "steps": K, "warmup": args.warmup,
+               "ms_per_step": round(step_ms_max, 5), "alg_bytes_per_step": alg,
+               "tokens_per_s": round(w.B / (step_ms_max * 1e-3), 1),
+               "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                            "unit": "GB/s", "frac": round(achieved / peak, 4),
+                            "traffic": measured_traffic(w.name), "kernel": pool.kernel_name(),
+                            "kernel_ms": round(kernel_ms, 5),
+                            "peak_kind": peak_kind + " (hbm_gbs copy)"},
+               "gpu_launches": 2 * K,
+               "clocks": sampler.summary(t0, t1) if sampler else None}
+        pool.close()
+        return rec, w
 
     # end to end: host buffers in pinned memory, copies inside the timed region
     hp = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()
@@ -408,16 +483,7 @@ def run_gpu(args):
             "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.elem_bytes == 2 else "f32", "data": "synthetic",
-            "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
-                       "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P,
-                       "pool_pages": w.pool_pages,
-                       "seq_len_max": int(w.seq_lens.max()), "tokens_retained": int(w.seq_lens.sum()),
-                       "storage": "bf16" if w.elem_bytes == 2 else "fp32", "accumulate": "fp32",
-                       "alg_bytes_per_step": alg,
-                       "logical_kv_bytes_per_step": logical_bytes(w),
-                       "l2": f"inputs larger than L2 ({alg / 1e9:.2f} GB per step, no flush)"
-                             if alg > 129e6 else "inputs smaller than L2 (cache-warm)",
-                       "parallelism": f"replicas x{world}"},
+            "config": decode_config(w, world, shared),
             "pct_of_8TBps": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "logical_GBps": round(world * logical_bytes(w) / (step_ms_max * 1e-3) / 1e9, 2),
             "tokens_per_s": round(world * w.B / (step_ms_max * 1e-3), 1),
@@ -434,10 +500,6 @@ def run_gpu(args):
             "gpu_launches": K * (4 if shared else 2),
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
-        if shared:
-            line["config"]["path"] = (f"shared-prefix call: the {shared}-token prompt once per KV "
-                                      "head on the tensor cores, each request's own positions by "
-                                      "the split kernel, partials merged")
     pool.close()
     return line, w
 
@@ -564,15 +626,7 @@ def run_gpu_serial(args):
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(tok_ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.elem_bytes == 2 else "f32", "data": "synthetic",
-            "config": {"workload": (f"single request: {w.layers} layers, H={w.H}, d_h={w.D}, "
-                                    f"retained length t={t}, pool of {w.pool_pages} shuffled pages; "
-                                    "a step is one token through every layer (transactional API)"),
-                       "name": w.name, "layers": w.layers, "heads": w.H, "head_dim": w.D,
-                       "page_size": w.P, "seq_len": t, "alg_bytes_per_step": alg,
-                       "l2": f"{layer_alg / 1e6:.1f} MB per layer, {alg / 1e6:.0f} MB per token, no flush: "
-                             + ("every layer's history fits in the 129 MB L2 between tokens"
-                                if alg <= 129e6 else "larger than the 129 MB L2"),
-                       "parallelism": f"replicas x{world}"},
+            "config": serial_config(w, world),
             "us_per_token": round(tok_ms * 1e3, 2),
             "tokens_per_s": round(world / (tok_ms * 1e-3), 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -712,27 +766,18 @@ def run_gpu_prefill(args):
 
     flops = prefill_flops(w)
     N = int(host["cu"][-1])
-    kv_bytes = int(w.seq_lens.astype(np.int64).sum()) * w.H * w.D * 2 * 2
     line = None
     if rank == 0:
         peak, peak_kind = measured_peak_bf16()
         achieved = flops / (kernel_ms * 1e-3) / 1e12
         value = world * flops / (step_ms_max * 1e-3) / 1e12
         line = {
-            "metric": "batched prefill attention into the paged cache: TFLOP/s (causal, "
-                      "algorithmic FLOPs) and new tokens/s",
+            "metric": PREFILL_METRIC,
             "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
-                       "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P,
-                       "pool_pages": w.pool_pages, "new_tokens": N,
-                       "cached_tokens": int((w.seq_lens - w.new_tokens).sum()),
-                       "storage": "bf16", "accumulate": "fp32", "flops_per_step": flops,
-                       "l2": f"K/V of the step {kv_bytes / 1e9:.2f} GB, re-read across query "
-                             f"tiles through L2 (no flush)",
-                       "parallelism": f"replicas x{world}"},
+            "config": prefill_config(w, world),
             "tokens_per_s": round(world * N / (step_ms_max * 1e-3), 1),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -841,23 +886,55 @@ def sample_requests(w, target_tokens: int):
     return out
 
 
+def sample_lanes(w, lanes: int):
+    """Requests 0, 1, ... until they hold at least `lanes` (request, KV head) lanes."""
+    return list(range(min(w.B, max(1, -(-lanes // w.H)))))
+
+
+def attended_tokens(w, requests=None) -> int:
+    lens = w.seq_lens.astype(np.int64)
+    if requests is not None:
+        lens = lens[list(requests)]
+    if w.window:
+        lens = np.minimum(lens, w.window)
+    return int(lens.sum())
+
+
+def oracle_decode_rate(w, requests, threads=0, passes=1):
+    """The oracle on the given requests' lanes: the metric's value for the whole step
+    (the step's algorithmic bytes over the time the sample's share of its work takes),
+    the seconds of one pass, and the fraction of the step the sample is."""
+    run, _, lens = oracle_sample(w, requests, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(passes):
+        run()
+    dt = (time.perf_counter() - t0) / passes
+    frac = attended_tokens(w, requests) / attended_tokens(w)
+    return algorithmic_bytes(w) * frac / dt / 1e9, dt, frac, lens
+
+
 def cpu_baseline(w, lane_tokens=1 << 24):
     """The oracle on the whole step, or on its first requests up to ``lane_tokens``
-    retained (lane, token) pairs (~10-30 s of CPU work on 16 cores)."""
+    retained (lane, token) pairs (~10-30 s of CPU work on 16 cores); also one
+    request on a single thread."""
     import oracle
     reqs = sample_requests(w, max(1, lane_tokens // w.H))
-    run, sbytes, lens = oracle_sample(w, reqs)
-    t0 = time.perf_counter()
-    run()
-    dt = time.perf_counter() - t0
-    return {"value": round(sbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+    value, dt, frac, lens = oracle_decode_rate(w, reqs)
+    one = sample_lanes(w, 1)
+    v1, dt1, _, lens1 = oracle_decode_rate(w, one, threads=1)
+    return {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
             "kind": "oracle",
             "sample": f"{len(reqs)} of {w.B} requests ({len(reqs) * w.H} lanes, "
-                      f"{int(lens.sum())} tokens), fp64 C oracle, one pass, {dt:.2f} s",
-            "tokens_per_s": round(len(reqs) / dt, 3)}
+                      f"{int(lens.sum())} tokens, {100 * frac:.1f} % of the step's work), fp64 C "
+                      f"oracle, one pass, {dt:.2f} s; value = the step's algorithmic bytes over "
+                      "the time of the whole step at that rate",
+            "tokens_per_s": round(len(reqs) / dt, 3),
+            "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"request 0 ({w.H} lanes, {int(lens1.sum())} tokens), "
+                                        f"one thread, one pass, {dt1:.2f} s"}}
 
 
-def run_reference_prefill(args, w):
+def run_reference_prefill(args, w, world):
     import oracle
     run, work, m, L0 = oracle_prefill_sample(w, target_flops=1e9)
     for _ in range(args.warmup):
@@ -868,16 +945,15 @@ def run_reference_prefill(args, w):
     dt = (time.perf_counter() - t0) / args.steps
     value = round(work / dt / 1e12, 6)
     sample = (f"each step: request 0's first {m} chunk tokens after {L0} cached "
-              f"({work / 1e9:.1f} GFLOP), fp64 C oracle on the host cores")
+              f"({work / 1e9:.1f} GFLOP), fp64 C oracle on the host cores; value = FLOPs of "
+              "the sample over its time")
     return {
         "impl": "reference",
-        "metric": "batched prefill attention into the paged cache: TFLOP/s (causal, "
-                  "algorithmic FLOPs) and new tokens/s",
-        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "metric": PREFILL_METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
-                   "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P},
+        "config": prefill_config(w, world),
         "tokens_per_s": round(m / dt, 3),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": sample},
@@ -886,34 +962,57 @@ def run_reference_prefill(args, w):
     }, w
 
 
+REFERENCE_BUDGET_S = 120.0      # host time the reference arm's timed and warm-up steps may take
+
+
 def run_reference(args):
+    """The oracle as it stands, on the host cores, on this arm's workload, metric and
+    config.  Each step runs it over the step's first requests: at least as many lanes
+    as the oracle has threads, more while the --steps + --warmup passes stay within
+    REFERENCE_BUDGET_S (by a timed pass of the smallest sample), the whole step when
+    that fits."""
     rank, world, _ = dist_env()
     if rank != 0:
         return None, None
     import oracle
     w = make_workload(args.workload, 0, args.requests)
     if w.new_tokens is not None:
-        return run_reference_prefill(args, w)
-    reqs = sample_requests(w, 1)                       # one request per step
-    run, sbytes, lens = oracle_sample(w, reqs)
+        return run_reference_prefill(args, w, world)
+    cores = oracle.max_threads()
+    reqs = sample_lanes(w, cores)
+    run, _, _ = oracle_sample(w, reqs)
+    t0 = time.perf_counter()
+    run()
+    per_token = (time.perf_counter() - t0) / attended_tokens(w, reqs)
+    budget = REFERENCE_BUDGET_S / (args.steps + args.warmup)
+    while len(reqs) < w.B and per_token * attended_tokens(w, reqs + [len(reqs)]) <= budget:
+        reqs.append(len(reqs))
+    if args.workload.startswith("single"):
+        cfg = serial_config(w, world)
+        alg = token_bytes(w, int(w.seq_lens[0]))
+    else:
+        cfg = decode_config(w, world, 0 if args.plain else int(w.shared_prefix))
+        alg = algorithmic_bytes(w)
+    run, _, lens = oracle_sample(w, reqs)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run()
     dt = (time.perf_counter() - t0) / args.steps
-    value = round(sbytes / dt / 1e9, 4)
-    sample = (f"each step: request 0 of {w.B} ({w.H} lanes x {int(lens[0])} tokens), "
-              f"fp64 C oracle on the host cores")
+    frac = attended_tokens(w, reqs) / attended_tokens(w) / w.layers
+    value = round(alg * frac / dt / 1e9, 4)
+    sample = (f"each step: requests 0..{len(reqs) - 1} of {w.B} ({len(reqs) * w.H} lanes, "
+              f"{int(lens.sum())} tokens, one layer: {100 * frac:.1f} % of the step's work), "
+              f"fp64 C oracle on {cores} host threads; value = the step's algorithmic bytes over "
+              "the time of the whole step at that rate")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(w), "name": w.name, "requests": w.B, "heads": w.H,
-                   "head_dim": w.D, "page_size": w.P},
-        "tokens_per_s": round(len(reqs) / dt, 3),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(),
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / frac * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "tokens_per_s": round(w.B * frac / dt, 3),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -936,6 +1035,8 @@ def parse_args(argv=None):
                     help="shared-prompt workload through the plain batched call")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests (small profiling captures)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="long-context run without the batched and ragged records")
     return ap.parse_args(argv)
 
 
@@ -943,11 +1044,16 @@ def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    import __graft_entry__
-    __graft_entry__.build()
     if args.impl == "reference":
+        # the oracle and the input generator only; the library is neither built nor loaded
+        import oracle
+        import synth
+        synth.build()
+        oracle.build()
         line, _ = run_reference(args)
     else:
+        import __graft_entry__
+        __graft_entry__.build()
         if args.workload.startswith("single"):
             runner = run_gpu_serial
         elif args.workload.startswith("prefill"):
@@ -959,6 +1065,15 @@ def main(argv=None):
         if line is not None and world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = (cpu_baseline_prefill(w) if w.new_tokens is not None
                                     else cpu_baseline(w))
+        if (line is not None and world == 1 and args.workload == "long" and not args.requests
+                and not args.no_extras):
+            extra = {}
+            for name in EXTRA_WORKLOADS:
+                sub = argparse.Namespace(**vars(args))
+                sub.workload, sub.steps = name, min(args.steps, 100)
+                extra[name], _ = run_gpu(sub, compact=True)
+            line["also_measured"] = extra
+            line["gpu_launches"] += sum(r["gpu_launches"] for r in extra.values())
     if line is not None:
         print(json.dumps(line), flush=True)
 
