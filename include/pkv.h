@@ -522,6 +522,44 @@ int pkv_paged_prefill(pkv_pool* pool, int layer, int batch, int64_t total_new, c
  */
 int pkv_pool_set_timing_events(pkv_pool* pool, void* before, void* after);
 
+/* ----------------------------------------------------- failure injection -- */
+
+/*
+ * Test hooks that make one later call fail the way a real failure would, so that
+ * the recovery the sources prescribe can be checked: after a failure,
+ * pkv_abort_token leaves the visible length unchanged ([SERVE-FLOW] step 4), and a
+ * rejected operation changes nothing ([CACHED-BIND]).  Nothing is armed unless this is
+ * called; every hook fires once and is then disarmed.  One hook of each kind at a
+ * time (arming a kind again replaces its hook).
+ *   PKV_INJECT_NONE         disarm every hook.
+ *   PKV_INJECT_LEASE        arg = n >= 1: the call that would take the n-th page
+ *                           lease from now (pkv_lease_pages, pkv_begin_token,
+ *                           pkv_begin_chunk; copy-on-write pages included) fails
+ *                           with PKV_ERR_OUT_OF_PAGES and changes nothing.
+ *   PKV_INJECT_LAYER        arg = layer: the next pkv_append_and_attend or
+ *                           pkv_prefill_chunk on that layer that passes its
+ *                           argument and state checks fails with PKV_ERR_CUDA
+ *                           before it enqueues anything; the layer stays not run.
+ *   PKV_INJECT_DEVICE_WAIT  arg = split-kernel worker (0 .. workers - 1), device
+ *                           pools: in the split kernel of the next
+ *                           pkv_append_and_attend or batched decode call
+ *                           (pkv_paged_decode_attention and its _shared and
+ *                           _static forms) on this pool, that worker arms the
+ *                           barrier of its first staged tile
+ *                           without issuing the tile's copy, and every bounded
+ *                           wait of that launch gives up after wait_limit_ns
+ *                           (1 ms .. 4 s).  The worker's wait runs out: it sets
+ *                           PKV_DEVERR_TIMEOUT, lets the copies it did issue land
+ *                           and returns; the rows its tiles feed are unspecified.
+ *                           Nothing faults or hangs, and the context stays usable.
+ * wait_limit_ns is read for PKV_INJECT_DEVICE_WAIT only.
+ */
+#define PKV_INJECT_NONE 0
+#define PKV_INJECT_LEASE 1
+#define PKV_INJECT_LAYER 2
+#define PKV_INJECT_DEVICE_WAIT 3
+int pkv_pool_inject_fault(pkv_pool* pool, int kind, int64_t arg, uint64_t wait_limit_ns);
+
 /* -------------------------------------------------------------- status -- */
 
 /* Synchronise the device, then read and clear the pool's device error word.

@@ -31,6 +31,7 @@ from .binding import (  # noqa: F401
     PKV_ERR_NO_STORAGE, PKV_ERR_UNSUPPORTED, PKV_F32, PKV_BF16, PKV_POOL_HOST_ONLY,
     PKV_POOL_CUDA_CORES,
     PKV_DEVERR_SEQ_LEN, PKV_DEVERR_PAGE_ID, PKV_DEVERR_TIMEOUT, PKV_DEVERR_SHARED,
+    PKV_INJECT_NONE, PKV_INJECT_LEASE, PKV_INJECT_LAYER, PKV_INJECT_DEVICE_WAIT,
 )
 
 __all__ = [
@@ -302,6 +303,11 @@ class Pool:
             return ctypes.c_void_p(ev.cuda_event)
         check(lib.pkv_pool_set_timing_events(self.handle, handle(before), handle(after)),
               "pkv_pool_set_timing_events")
+
+    def inject_fault(self, kind: int, arg: int = 0, wait_limit_ns: int = 0) -> None:
+        """Arm a one-shot failure hook (PKV_INJECT_*; tests of the recovery paths)."""
+        check(lib.pkv_pool_inject_fault(self.handle, kind, arg, wait_limit_ns),
+              "pkv_pool_inject_fault")
 
     def check_device_status(self) -> int:
         """Synchronise; return the device error bits (raises PkvError if any were set)."""

@@ -35,6 +35,11 @@ PKV_DEVERR_PAGE_ID = 2
 PKV_DEVERR_TIMEOUT = 4
 PKV_DEVERR_SHARED = 8
 
+PKV_INJECT_NONE = 0
+PKV_INJECT_LEASE = 1
+PKV_INJECT_LAYER = 2
+PKV_INJECT_DEVICE_WAIT = 3
+
 LIB_PATH = _build.LIB
 
 
@@ -93,6 +98,7 @@ SIGNATURES = {
     "pkv_paged_decode_attention_shared": [_vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i64, _i64,
                                           _vp, _vp, _sz, _vp],
     "pkv_pool_set_timing_events": [_vp, _vp, _vp],
+    "pkv_pool_inject_fault": [_vp, _i, _i64, ctypes.c_uint64],
     "pkv_check_device_status": [_vp, _P(_u32)],
     "pkv_last_error": [],
     "pkv_status_string": [_i],

@@ -180,6 +180,9 @@ struct KParams {
     const float* pre_o;
     int pre_splits;
     int64_t pre_stride;
+    uint64_t wait_ns;           // each bounded wait gives up after this long
+    int inject_worker;          // failure injection: 0 off; else worker inject_worker - 1 arms
+                                // its first stage without issuing the copy
 };
 
 __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
@@ -617,7 +620,9 @@ split_decode_kernel(const KParams p) {
     int tab_b = -1;
     int64_t tab_base = 0;
     int32_t tab_val = -1;
-    auto issue = [&](int s) {
+    // armed_only: failure injection -- the barrier expects the stage's bytes but no
+    // copy is issued, so the wait on this stage runs out
+    auto issue = [&](int s, bool armed_only) {
         if (prod.b != tab_b || prod.page_idx < tab_base || prod.page_idx >= tab_base + 32) {
             tab_b = prod.b;
             tab_base = prod.page_idx;
@@ -636,6 +641,7 @@ split_decode_kernel(const KParams p) {
         const int64_t off = (kv_block(p, page, prod.h) * p.P + prod.slot0) * D;
         unsigned char* dst = ring + s * Gm::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[s], Gm::STAGE_BYTES);
+        if (armed_only) return;
         bulk_copy_g2s(dst, static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES, &bars[s], policy);
         bulk_copy_g2s(dst + Gm::TILE_BYTES, static_cast<const T*>(p.v_pages) + off, Gm::TILE_BYTES,
                       &bars[s], policy);
@@ -643,7 +649,7 @@ split_decode_kernel(const KParams p) {
 
     const int prologue = n_work < Gm::STAGES ? n_work : Gm::STAGES;
     for (int s = 0; s < prologue; ++s) {
-        issue(s);
+        issue(s, s == 0 && p.inject_worker == w + 1);
         cursor_advance(prod, p);
     }
 
@@ -680,7 +686,7 @@ split_decode_kernel(const KParams p) {
             }
         }
 
-        if (!mbar_wait_bounded(&bars[s], parity, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(&bars[s], parity, p.wait_ns)) {
             if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
             // let the copies already issued land before the shared memory goes away
             const int last = (k + Gm::STAGES - 1 < n_work - 1) ? k + Gm::STAGES - 1 : n_work - 1;
@@ -691,7 +697,7 @@ split_decode_kernel(const KParams p) {
                     s2 = 0;
                     par2 ^= 1u;
                 }
-                mbar_wait_bounded(&bars[s2], par2, kWaitLimitNs);
+                mbar_wait_bounded(&bars[s2], par2, p.wait_ns);
             }
             return;
         }
@@ -806,7 +812,7 @@ split_decode_kernel(const KParams p) {
         fence_proxy_async_smem();
         __syncwarp();
         if (k + Gm::STAGES < n_work) {
-            issue(s);
+            issue(s, false);
             cursor_advance(prod, p);
         }
         if (++s == Gm::STAGES) {
@@ -1097,7 +1103,9 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     int tab_b = -1;
     int64_t tab_base = 0;
     int32_t tab_val = -1;
-    auto issue = [&](int s) {
+    // armed_only: failure injection -- the barrier expects the stage's bytes but no
+    // copy is issued, so the wait on this stage runs out
+    auto issue = [&](int s, bool armed_only) {
         if (prod.b != tab_b || prod.page_idx < tab_base || prod.page_idx >= tab_base + 32) {
             tab_b = prod.b;
             tab_base = prod.page_idx;
@@ -1116,6 +1124,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         const int y = (int)(kv_block(p, page, prod.h) * p.P + prod.slot0);   // pool row
         unsigned char* dst = ring + s * M::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars[s], M::STAGE_BYTES);
+        if (armed_only) return;
 #pragma unroll
         for (int bx = 0; bx < M::BOXES; ++bx) {
             tma_load_2d(dst + bx * M::BOX_BYTES, &tmk, bx * M::BOX_ELEMS, y, &bars[s], policy);
@@ -1126,7 +1135,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
 
     const int prologue = n_work < M::STAGES ? n_work : M::STAGES;
     for (int s = 0; s < prologue; ++s) {
-        issue(s);
+        issue(s, s == 0 && p.inject_worker == w + 1);
         cursor_advance(prod, p);
     }
 
@@ -1194,7 +1203,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             }
         }
 
-        if (!mbar_wait_bounded(&bars[s], parity, kWaitLimitNs)) {
+        if (!mbar_wait_bounded(&bars[s], parity, p.wait_ns)) {
             if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
             const int last = (k + M::STAGES - 1 < n_work - 1) ? k + M::STAGES - 1 : n_work - 1;
             int s2 = s;
@@ -1204,7 +1213,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                     s2 = 0;
                     par2 ^= 1u;
                 }
-                mbar_wait_bounded(&bars[s2], par2, kWaitLimitNs);
+                mbar_wait_bounded(&bars[s2], par2, p.wait_ns);
             }
             return;
         }
@@ -1393,7 +1402,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
         fence_proxy_async_smem();
         __syncwarp();
         if (k + M::STAGES < n_work) {
-            issue(s);
+            issue(s, false);
             cursor_advance(prod, p);
         }
         if (++s == M::STAGES) {
@@ -1730,6 +1739,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.pre_o = a.pre_o;
     p.pre_splits = a.pre_splits;
     p.pre_stride = a.pre_stride;
+    p.wait_ns = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs;
+    p.inject_worker = a.inject_worker;
     if (a.tmap_k != nullptr && a.tmap_v != nullptr) {
         // table rows on the tensor-core kernel: fp32 pools only (the bf16 pools it
         // serves prefill on the tcgen05 kernel, not through decode lanes)

@@ -61,6 +61,9 @@ struct DecodeArgs {
     cudaError_t (*before_split)(const void* ctx, cudaStream_t stream);
     const void* before_split_ctx;
     bool allow_empty;        // a seq_len of 0 is a request with no work (not an error)
+    uint64_t wait_limit_ns;  // bounded waits give up after this long (0: the default, 4 s)
+    int inject_worker;       // failure injection: 0 off; else split worker inject_worker - 1
+                             // arms its first stage's barrier without issuing the copy
 };
 
 // Bytes of a CUtensorMap (the driver's TMA descriptor).

@@ -88,6 +88,11 @@ struct pkv_pool {
     bool tmaps = false;                // tensor maps built (head_dim 64 or 128)
     std::vector<CUtensorMap> tmap_k;   // per layer, when tmaps
     std::vector<CUtensorMap> tmap_v;
+    // failure injection (pkv_pool_inject_fault), each hook one-shot
+    int64_t inject_lease = 0;          // > 0: page leases until the one that fails
+    int inject_layer = -1;             // >= 0: the next layer call on this layer fails
+    int inject_worker = -1;            // >= 0: the next decode launch's worker skips a copy
+    uint64_t inject_wait_ns = 0;       //        with this wait limit
 };
 
 struct pkv_request {
@@ -240,6 +245,33 @@ void drop_page(pkv_pool* p, int32_t page, bool front) {
         if (front) p->free_list.push_front(page);
         else p->free_list.push_back(page);
     }
+}
+
+// Failure injection: true (and the hook disarmed) when a call about to lease n
+// pages reaches the lease armed to fail; else the leases are counted.
+bool lease_fault(pkv_pool* p, int64_t n) {
+    if (p->inject_lease <= 0 || n <= 0) return false;
+    if (n >= p->inject_lease) {
+        p->inject_lease = 0;
+        return true;
+    }
+    p->inject_lease -= n;
+    return false;
+}
+
+// Failure injection: true (and the hook disarmed) for the armed layer.
+bool layer_fault(pkv_pool* p, int layer) {
+    if (p->inject_layer < 0 || p->inject_layer != layer) return false;
+    p->inject_layer = -1;
+    return true;
+}
+
+// Failure injection: hand the armed split-worker copy skip to one launch.
+void take_wait_fault(pkv_pool* p, pkv::DecodeArgs* a) {
+    if (p->inject_worker < 0) return;
+    a->inject_worker = p->inject_worker + 1;
+    a->wait_limit_ns = p->inject_wait_ns;
+    p->inject_worker = -1;
 }
 
 int check_device(const pkv_pool* p) {
@@ -589,6 +621,7 @@ int pkv_lease_pages(pkv_request* r, int64_t n) {
     if (n > (int64_t)p->free_list.size())
         return fail(PKV_ERR_OUT_OF_PAGES, "%lld pages requested, %lld free", (long long)n,
                     (long long)p->free_list.size());
+    if (lease_fault(p, n)) return fail(PKV_ERR_OUT_OF_PAGES, "injected lease failure");
     mark_dirty(r, (int64_t)r->table.size());
     for (int64_t i = 0; i < n; ++i) r->table.push_back(lease_front(p));
     return ok();
@@ -650,6 +683,7 @@ int begin_pending(pkv_request* r, int64_t n, bool chunk, int64_t* position) {
     if (shared + fresh > (int64_t)p->free_list.size())
         return fail(PKV_ERR_OUT_OF_PAGES, "%lld pages needed, %lld free", (long long)(shared + fresh),
                     (long long)p->free_list.size());
+    if (lease_fault(p, shared + fresh)) return fail(PKV_ERR_OUT_OF_PAGES, "injected lease failure");
     r->cow.clear();
     for (int64_t idx = first; idx <= last && idx < held; ++idx) {
         const int32_t old = r->table[(size_t)idx];
@@ -745,6 +779,7 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     if (r->appended[(size_t)layer]) return fail(PKV_ERR_BAD_STATE, "layer %d already ran", layer);
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
+    if (layer_fault(p, layer)) return fail(PKV_ERR_CUDA, "injected failure on layer %d", layer);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = prepare_layer_write(r, layer, s);
     if (rc != PKV_OK) return rc;
@@ -779,6 +814,7 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
+    take_wait_fault(p, &a);
     if (r->epoch == UINT32_MAX) {
         // epochs must increase: after 2^32 - 1 calls start over from zeroed counters
         cudaError_t z = cudaMemsetAsync(r->dev_workspace, 0, r->workspace_bytes, s);
@@ -807,6 +843,7 @@ int pkv_prefill_chunk(pkv_request* r, int layer, const void* q, const void* k, c
     if (r->appended[(size_t)layer]) return fail(PKV_ERR_BAD_STATE, "layer %d already ran", layer);
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
+    if (layer_fault(p, layer)) return fail(PKV_ERR_CUDA, "injected failure on layer %d", layer);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!tensor_prefill(p)) {
         // decode lanes: the request's scratch grows to the chunk (freeing the old
@@ -1015,6 +1052,7 @@ int pkv_paged_decode_attention(pkv_pool* p, int layer, int batch, const float* q
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
+    take_wait_fault(p, &a);
     cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ok();
@@ -1239,6 +1277,39 @@ int pkv_pool_set_timing_events(pkv_pool* p, void* before, void* after) {
     return ok();
 }
 
+int pkv_pool_inject_fault(pkv_pool* p, int kind, int64_t arg, uint64_t wait_limit_ns) {
+    if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
+    switch (kind) {
+        case PKV_INJECT_NONE:
+            p->inject_lease = 0;
+            p->inject_layer = -1;
+            p->inject_worker = -1;
+            return ok();
+        case PKV_INJECT_LEASE:
+            if (arg < 1) return fail(PKV_ERR_INVALID_ARGUMENT, "lease count must be >= 1");
+            p->inject_lease = arg;
+            return ok();
+        case PKV_INJECT_LAYER:
+            if (arg < 0 || arg >= p->layers)
+                return fail(PKV_ERR_INVALID_ARGUMENT, "layer %lld outside [0, %d)", (long long)arg,
+                            p->layers);
+            p->inject_layer = (int)arg;
+            return ok();
+        case PKV_INJECT_DEVICE_WAIT:
+            if (p->host_only) return fail(PKV_ERR_NO_STORAGE, "host-only pool has no device storage");
+            if (arg < 0 || arg >= p->workers)
+                return fail(PKV_ERR_INVALID_ARGUMENT, "worker %lld outside [0, %d)", (long long)arg,
+                            p->workers);
+            if (wait_limit_ns < 1000000ull || wait_limit_ns > 4000000000ull)
+                return fail(PKV_ERR_INVALID_ARGUMENT, "wait limit must be within [1 ms, 4 s]");
+            p->inject_worker = (int)arg;
+            p->inject_wait_ns = wait_limit_ns;
+            return ok();
+        default:
+            return fail(PKV_ERR_INVALID_ARGUMENT, "unknown fault kind %d", kind);
+    }
+}
+
 int pkv_check_device_status(pkv_pool* p, uint32_t* bits) {
     if (!p) return fail(PKV_ERR_INVALID_ARGUMENT, "NULL pool");
     if (bits) *bits = 0;
@@ -1320,6 +1391,7 @@ int prepare_batched(pkv_pool* p, int layer, int batch, const float* q, const voi
     a->dev_error = p->dev_error;
     a->ev_before = p->ev_before;
     a->ev_after = p->ev_after;
+    take_wait_fault(p, a);
     return ok();
 }
 

@@ -327,9 +327,7 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
             // pairs go back over the S columns of their own half, already read: keys
             // 64hh + 2i, 2i+1 -> P_hi column 64hh + i, P_lo column 64hh + 32 + i.
             const float2 c2 = make_float2(c, c);
-            float m4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) m4[k] = -INFINITY;
+            float m2[2] = {-INFINITY, -INFINITY};
             {
                 uint32_t sv[64];
                 tmem_ld32(t_s + 64, sv);
@@ -341,7 +339,10 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
                         if (64 + e < e_lo || 64 + e > e_hi) sv[e] = 0xff800000u;
                 }
 #pragma unroll
-                for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sv[e]));
+                for (int e = 0; e < 64; e += 4) {
+                    m2[0] = fmax3(m2[0], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
+                    m2[1] = fmax3(m2[1], __uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3]));
+                }
             }
             uint32_t s0[64];                                  // S of keys 0..63
             tmem_ld32(t_s, s0);
@@ -353,8 +354,11 @@ prefill_attention_kernel(const __grid_constant__ PfParams p, const __grid_consta
                     if (e < e_lo || e > e_hi) s0[e] = 0xff800000u;
             }
 #pragma unroll
-            for (int e = 0; e < 64; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(s0[e]));
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            for (int e = 0; e < 64; e += 4) {
+                m2[0] = fmax3(m2[0], __uint_as_float(s0[e]), __uint_as_float(s0[e + 1]));
+                m2[1] = fmax3(m2[1], __uint_as_float(s0[e + 2]), __uint_as_float(s0[e + 3]));
+            }
+            const float mx = fmaxf(m2[0], m2[1]);
             float alpha = 1.f;
             if (mx > m_used && (m_used == -INFINITY || (mx - m_used) * c > 8.f)) {
                 alpha = m_used == -INFINITY ? 0.f : ex2((m_used - mx) * c);

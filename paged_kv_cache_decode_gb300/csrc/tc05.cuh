@@ -129,14 +129,37 @@ __device__ __forceinline__ uint64_t l2_normal_policy() {
     return pol;
 }
 
+// One try_wait that may suspend the thread for up to kTcSuspendNs until the phase
+// completes, instead of returning at once: a waiting warp then issues nothing.
+constexpr uint32_t kTcSuspendNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kTcSuspendNs)
+        : "memory");
+    return done != 0;
+}
+
+// Largest of three (the three-input form of max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Bounded wait; gives up early once another role of the CTA has given up.
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                         unsigned* dev_error) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if ((i & 3) == 0) {
             if (*abort_flag) return false;
             if (global_timer_ns() - start > kTcWaitLimitNs) {
                 *abort_flag = 1;
