@@ -353,6 +353,13 @@ __device__ __forceinline__ void cursor_advance(Cursor& c, const KParams& p) {
     c.b = p.B;   // past the end; never dereferenced
 }
 
+// Release / acquire fence at GPU scope: with a relaxed atomic on the lane counter
+// it orders a worker's partial before its count (writer) and every counted
+// partial before the merge's reads (the last arriver).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // Worker that owns flattened tile x: the inverse of begin(w) = floor(w T / W).
 __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t T, int W) {
     return ((x + 1) * W - 1) / T;
@@ -361,78 +368,80 @@ __device__ __forceinline__ int64_t worker_of(int64_t x, int64_t T, int W) {
 // Combine the partials of query g of lane `lane_id` into out.  The lane's KV lane
 // K (request b, KV head hk: K = b * (H >> kv_shift) + hk) has its tiles in ranges
 // r_lo..r_hi (those owning at least one tile); sub-lane `sub` of range r wrote its
-// partial to slot ((K + r) << kv_shift) | sub.
-// One warp: lane j takes partials j, j + 32, ... for the maximum and the
-// weights 2^(m_w - M); the weighted sum of the o vectors then runs 32 partials
-// at a time with each weight broadcast by shuffle, so the loads of consecutive
-// partials are independent.  Partials are read from L2 (other SMs wrote them
-// during this kernel).
+// partial to slot ((K + r) << kv_shift) | sub.  In a shared-prefix call (the
+// combine kernel) the prefix kernel's pre_splits partials of the query row follow
+// as partials cnt .. cnt + pre_splits - 1.
+// One warp: lane j takes partials j, j + 32, ... for the maximum and the weights
+// 2^(m_w - M), each (max, sum) loaded once; lane l sums features l * DPL .. of
+// every partial's o vector, each weight broadcast by shuffle.  The o vectors are
+// read CJ partials at a time with every load issued before any is used, and the
+// first CJ together with the (max, sum) pairs, so a merge of up to CJ partials
+// (32 at head width 64) costs one L2 round trip.  Partials are read from L2
+// (other SMs wrote them during this kernel).
 template <int D, int DPL, int G>
 __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, int g, int64_t K,
                                             int sub, int64_t r_lo, int64_t r_hi, int64_t T_all,
                                             int lane) {
+    constexpr int CJ = 64 / DPL < 32 ? 64 / DPL : 32;    // o vectors in flight (<= 64 floats)
     const int R = p.W >> p.kv_shift;
     auto owns_tiles = [&](int64_t r) { return (r * T_all) / R != ((r + 1) * T_all) / R; };
     auto slot_of = [&](int64_t r) { return ((K + r) << p.kv_shift) | sub; };
-    const int cnt = (int)(r_hi - r_lo + 1);
+    const int cw = (int)(r_hi - r_lo + 1);
+    const int cnt = cw + p.pre_splits;
     const int64_t row = lane_id * G + g;                  // query row (request, query head)
-    float M = -INFINITY;
-    for (int j = lane; j < cnt; j += 32)
-        if (owns_tiles(r_lo + j)) M = fmaxf(M, __ldcg(&p.part_ml[slot_of(r_lo + j) * G + g]).x);
-    for (int s = lane; s < p.pre_splits; s += 32) {
-        const float2 ml = __ldcg(&p.pre_ml[s * p.pre_stride + row]);
-        if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    }
+    const bool has_features = lane * DPL < D;
+    // (max, sum) of partial j; a worker that owns no tile, or a prefix split with
+    // no key of the row, contributes nothing
+    auto load_ml = [&](int j) -> float2 {
+        if (j < cw) {
+            if (!owns_tiles(r_lo + j)) return make_float2(-INFINITY, 0.f);
+            return __ldcg(&p.part_ml[slot_of(r_lo + j) * G + g]);
+        }
+        if (j >= cnt) return make_float2(-INFINITY, 0.f);
+        const float2 ml = __ldcg(&p.pre_ml[(int64_t)(j - cw) * p.pre_stride + row]);
+        return ml.y > 0.f ? ml : make_float2(-INFINITY, 0.f);
+    };
+    auto load_o = [&](int j, float (&v)[DPL]) {
+        if (j < cnt && has_features) {
+            const float* op = (j < cw ? p.part_o + (slot_of(r_lo + j) * G + g) * D
+                                      : p.pre_o + ((int64_t)(j - cw) * p.pre_stride + row) * D) +
+                              lane * DPL;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) v[i] = __ldcg(op + i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) v[i] = 0.f;
+        }
+    };
+    const float2 ml0 = load_ml(lane);
+    float v[CJ][DPL];
+#pragma unroll
+    for (int jj = 0; jj < CJ; ++jj) load_o(jj, v[jj]);
+    float M = ml0.x;
+    for (int j = 32 + lane; j < cnt; j += 32) M = fmaxf(M, load_ml(j).x);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
     float acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    const bool has_features = lane * DPL < D;
     for (int base = 0; base < cnt; base += 32) {
-        float wgt = 0.f;
-        if (base + lane < cnt && owns_tiles(r_lo + base + lane)) {
-            const float2 ml = __ldcg(&p.part_ml[slot_of(r_lo + base + lane) * G + g]);
-            wgt = exp2f(ml.x - M);
-            L = fmaf(ml.y, wgt, L);
-        }
-        const int nj = cnt - base < 32 ? cnt - base : 32;
-#pragma unroll 8
-        for (int j = 0; j < nj; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, wgt, j);
-            if (has_features) {
-                // slots of workers that own no tile hold stale data: weight 0, value dropped
-                const float* op = p.part_o + (slot_of(r_lo + base + j) * G + g) * D + lane * DPL;
+        const float2 ml = base == 0 ? ml0 : load_ml(base + lane);
+        const float wgt = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+        L = fmaf(ml.y, wgt, L);
+        for (int c0 = 0; c0 < 32 && base + c0 < cnt; c0 += CJ) {
+            if (base + c0 > 0) {
 #pragma unroll
-                for (int i = 0; i < DPL; ++i) {
-                    const float v = __ldcg(op + i);
-                    acc[i] = wj != 0.f ? fmaf(wj, v, acc[i]) : acc[i];
-                }
+                for (int jj = 0; jj < CJ; ++jj) load_o(base + c0 + jj, v[jj]);
             }
-        }
-    }
-    // the shared prefix's partials, weighted the same way
-    for (int base = 0; base < p.pre_splits; base += 32) {
-        float wgt = 0.f;
-        if (base + lane < p.pre_splits) {
-            const float2 ml = __ldcg(&p.pre_ml[(base + lane) * p.pre_stride + row]);
-            if (ml.y > 0.f) {
-                wgt = exp2f(ml.x - M);
-                L = fmaf(ml.y, wgt, L);
-            }
-        }
-        const int nj = p.pre_splits - base < 32 ? p.pre_splits - base : 32;
-#pragma unroll 8
-        for (int j = 0; j < nj; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, wgt, j);
-            if (has_features) {
-                const float* op = p.pre_o + ((base + j) * p.pre_stride + row) * D + lane * DPL;
 #pragma unroll
-                for (int i = 0; i < DPL; ++i) {
-                    const float v = __ldcg(op + i);
-                    acc[i] = wj != 0.f ? fmaf(wj, v, acc[i]) : acc[i];
-                }
+            for (int jj = 0; jj < CJ; ++jj) {
+                // partials with weight 0 (no tile, or past the lane's last) may hold
+                // stale data: value dropped
+                const float wj = __shfl_sync(0xffffffffu, wgt, c0 + jj);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i)
+                    acc[i] = wj != 0.f ? fmaf(wj, v[jj][i], acc[i]) : acc[i];
             }
         }
     }
@@ -440,7 +449,7 @@ __device__ __forceinline__ void merge_query(const KParams& p, int64_t lane_id, i
     for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     if (!has_features) return;
     const float inv = 1.f / L;
-    float* out = p.out + (lane_id * G + g) * D + lane * DPL;
+    float* out = p.out + row * D + lane * DPL;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
 }
@@ -865,7 +874,7 @@ split_decode_kernel(const KParams p) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) p.part_ml[slot * G + g] = make_float2(m[g], lt[g]);
                 }
-                __threadfence();
+                fence_acq_rel_gpu();   // release: the partial before the counter
                 __syncwarp();
                 if (p.pre_ml != nullptr) {       // the combine kernel merges every lane
                     cursor_advance(cur, p);
@@ -899,7 +908,7 @@ split_decode_kernel(const KParams p) {
                 }
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
-                    __threadfence();
+                    fence_acq_rel_gpu();   // acquire: every counted partial is visible
                     const int64_t K = (int64_t)cur.b * Hk + cur.h;
                     if constexpr (G == 1)
                         merge_query<D, Gm::DPL, G>(p, lane_id, 0, K, sub, r_lo, r_hi, T_all, lane);
@@ -1450,7 +1459,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                         if (t == 0) p.part_ml[slot * G + g + 8 * qi] = make_float2(m[qi], lt[qi]);
                     }
                 }
-                __threadfence();
+                fence_acq_rel_gpu();   // release: the partial before the counter
                 __syncwarp();
                 if (p.pre_ml != nullptr) {       // the combine kernel merges every lane
                     cursor_advance(cur, p);
@@ -1480,7 +1489,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                 }
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == need) {
-                    __threadfence();
+                    fence_acq_rel_gpu();   // acquire: every counted partial is visible
                     merge_lane<D, G>(p, lane_id, (int64_t)cur.b * Hk + cur.h, sub, r_lo, r_hi,
                                      T_all, lane);
                 }
