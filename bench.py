@@ -91,7 +91,7 @@ def describe(w) -> str:
         return (f"chunked prefill: {w.B} requests each appending {int(w.new_tokens[0])} tokens "
                 f"after U[0,{int(w.max_context - w.new_tokens.max())}] cached ones (mean "
                 f"{float(cached.mean()):.0f}), {w.H} KV heads x {w.group} query heads, d_h={w.D}, "
-                f"bf16 pages of {w.P}, causal")
+                f"{st} pages of {w.P}, causal")
     if w.name == "ragged":
         return (f"ragged fragmented pool: {w.B} requests, lognormal(ln 512, 1) lengths, H={w.H}, "
                 f"d_h={w.D}, {st}, {w.pool_pages}-page pool after {w.churn_cycles} lease/release cycles")
@@ -139,7 +139,8 @@ def prefill_config(w, world: int) -> dict:
             "query_heads": w.HQ, "head_dim": w.D, "page_size": w.P,
             "pool_pages": w.pool_pages, "new_tokens": int(w.new_tokens.sum()),
             "cached_tokens": int((w.seq_lens - w.new_tokens).sum()),
-            "storage": "bf16", "accumulate": "fp32", "flops_per_step": prefill_flops(w),
+            "storage": "bf16" if w.elem_bytes == 2 else "fp32", "accumulate": "fp32",
+            "flops_per_step": prefill_flops(w),
             "l2": f"K/V of the step {kv_bytes / 1e9:.2f} GB, re-read across query "
                   f"tiles through L2 (no flush)",
             "parallelism": f"replicas x{world}"}
@@ -665,7 +666,8 @@ def setup_prefill(w, torch):
     """Pool, tables from the library's allocator, cached tokens in HBM, chunk inputs on device."""
     import paged_kv_cache_decode_gb300 as pkv
     from synth.device import fill_history, prefill_inputs, to_device
-    pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "bf16", w.max_context, w.seed,
+    pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, "bf16" if w.elem_bytes == 2 else "f32",
+                    w.max_context, w.seed,
                     query_heads=w.HQ, window=w.window)
     reqs = [pool.request() for _ in range(w.B)]
     for b, r in enumerate(reqs):
@@ -766,9 +768,21 @@ def run_gpu_prefill(args):
 
     flops = prefill_flops(w)
     N = int(host["cu"][-1])
+    f32 = w.elem_bytes == 4
+    if f32:
+        # decode lanes: lane rows, block plan, the decode plan and the split kernel
+        kernel = "split_decode_mma_kernel<f32,%d,8> (block lanes, table rows)" % w.D
+        launches = 4
+    else:
+        kernel = "prefill_attention_kernel<%d>" % w.D
+        launches = 3
     line = None
     if rank == 0:
         peak, peak_kind = measured_peak_bf16()
+        peak_note = " (bf16_tflops burst, cuBLAS)"
+        if f32:
+            # tf32 products: the measured bf16 peak times the nominal tf32 / bf16 ratio
+            peak, peak_note = round(peak * 1.1 / 2.25, 1), " (bf16_tflops burst x 1.1/2.25, tf32)"
         achieved = flops / (kernel_ms * 1e-3) / 1e12
         value = world * flops / (step_ms_max * 1e-3) / 1e12
         line = {
@@ -776,19 +790,20 @@ def run_gpu_prefill(args):
             "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": "f32" if f32 else "bf16", "data": "synthetic",
             "config": prefill_config(w, world),
             "tokens_per_s": round(world * N / (step_ms_max * 1e-3), 1),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "traffic": measured_traffic(w.name, "prefill_attention", PREFILL_SRC),
-                         "kernel": "prefill_attention_kernel<%d>" % w.D,
+                         "traffic": (None if f32 else
+                                     measured_traffic(w.name, "prefill_attention", PREFILL_SRC)),
+                         "kernel": kernel,
                          "kernel_ms": round(kernel_ms, 5),
-                         "peak_kind": peak_kind + " (bf16_tflops burst, cuBLAS)"},
+                         "peak_kind": peak_kind + peak_note},
             "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": K * 3,
+            "gpu_launches": K * launches,
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
     for r in reqs:
@@ -817,7 +832,7 @@ def oracle_prefill_sample(w, target_flops: float = 5e10, threads=0):
     kp = synth.history_pages(w.seed, KHIST, 0, 0, n, w.H, w.P, w.D, L0, w.dtype)
     vp = synth.history_pages(w.seed, VHIST, 0, 0, n, w.H, w.P, w.D, L0, w.dtype)
     table = np.arange(n, dtype=np.int32)[None, :]
-    qf = synth.bf16_to_f32(q[:m])
+    qf = synth.bf16_to_f32(q[:m]) if q.dtype == np.uint16 else q[:m]
     cu1 = np.array([0, m], dtype=np.int32)
     lens = np.array([L0 + m], dtype=np.int32)
 

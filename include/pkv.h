@@ -460,9 +460,9 @@ int pkv_paged_decode_attention_static(pkv_pool* pool, int layer, int batch, cons
  * Device scratch bytes that pkv_paged_prefill needs for `batch` requests and
  * total_new new tokens (0 when either is 0).  The tensor-core implementation
  * needs a few bytes per request and query tile; the decode-lane one needs the
- * decode scratch of total_new requests (per chunk row about
- * (head_dim + 2) * 4 bytes for each query head, plus the split workers'
- * partials) and, for bf16 storage, an fp32 copy of q.
+ * decode scratch of total_new requests, or of total_new / (8 / G) + batch blocks
+ * of tokens (per chunk row about (head_dim + 2) * 4 bytes for each query head,
+ * plus the split workers' partials) and, for bf16 storage, an fp32 copy of q.
  */
 int pkv_prefill_workspace_size(const pkv_pool* pool, int batch, int64_t total_new, size_t* bytes);
 
@@ -496,7 +496,10 @@ int pkv_prefill_workspace_size(const pkv_pool* pool, int batch, int64_t total_ne
  * storage, other head widths): decode lanes -- every chunk row is stored first,
  * then chunk token i of request b runs as one decode request of retained length
  * L0_b + i + 1 over request b's pages, all in one decode launch, with the decode
- * kernels' precision (fp32 weights; a bf16 q widened exactly to fp32).
+ * kernels' precision (fp32 weights; a bf16 q widened exactly to fp32).  fp32 pools
+ * of head_dim 64 or 128 with 1, 2 or 4 query heads per KV head and no window run
+ * 8 / G consecutive chunk tokens as one decode request (each token's rows masked
+ * at its own position: the same results, each K/V tile read once per block).
  * Stateless over bookkeeping: the caller owns lengths and tables.  Bad lengths
  * or page ids found on the device set the pool's error word (a bad page reads as
  * zeros); the affected rows of `out` are then unspecified.  Once a wait has run out (PKV_DEVERR_TIMEOUT), later prefill

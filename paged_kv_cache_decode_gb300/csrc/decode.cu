@@ -183,10 +183,27 @@ struct KParams {
     uint64_t wait_ns;           // each bounded wait gives up after this long
     int inject_worker;          // failure injection: 0 off; else worker inject_worker - 1 arms
                                 // its first stage without issuing the copy
+    // block lanes (prefill of fp32 pools on the tensor-core kernel's table-row form):
+    // decode request x is a block of blk_ntok[x] consecutive chunk tokens starting at
+    // chunk row blk_tok0[x]; lane row g is token g / blk_gp of the block and query
+    // head h * blk_gp + g % blk_gp of the pool, attending positions up to its own
+    // t - (ntok - 1 - g / blk_gp); nullptr: one query row per (request, query head)
+    const int32_t* blk_tok0;
+    const int32_t* blk_ntok;
+    int blk_gp;                 // the pool's query heads per KV head
+    int blk_hq;                 // the pool's query heads
 };
 
 __device__ __forceinline__ int64_t seq_len_at(const KParams& p, int b) {
     return p.seq_lens == nullptr ? p.single_t : (int64_t)__ldg(p.seq_lens + b);
+}
+
+// Block lanes: the q / out row of lane row g of decode request x, KV head h, or -1
+// for a row past the block's tokens.
+__device__ __forceinline__ int64_t block_row(const KParams& p, int x, int h, int g) {
+    const int r = g / p.blk_gp;
+    if (r >= __ldg(p.blk_ntok + x)) return -1;
+    return ((int64_t)__ldg(p.blk_tok0 + x) + r) * p.blk_hq + (int64_t)h * p.blk_gp + g % p.blk_gp;
 }
 
 
@@ -523,15 +540,20 @@ __device__ __forceinline__ void merge_lane(const KParams& p, int64_t lane_id, in
         }
 #pragma unroll
         for (int off = 16; off >= GB; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        float* out = p.out + (lane_id * G + g0) * D + lane * DPL;
 #pragma unroll
         for (int g = 0; g < GB; ++g) {
             const float inv = 1.f / __shfl_sync(0xffffffffu, L, g);
+            int64_t orow = lane_id * G + g0 + g;
+            if (p.blk_tok0 != nullptr) {   // block lanes: the row's chunk token, if any
+                orow = block_row(p, (int)(lane_id / p.H), (int)(lane_id % p.H), g0 + g);
+                if (orow < 0) continue;
+            }
+            float* out = p.out + orow * D + lane * DPL;
             if constexpr (DPL == 4) {
-                *reinterpret_cast<float4*>(out + g * D) =
+                *reinterpret_cast<float4*>(out) =
                     make_float4(acc[g][0] * inv, acc[g][1] * inv, acc[g][2] * inv, acc[g][3] * inv);
             } else {
-                *reinterpret_cast<float2*>(out + g * D) = make_float2(acc[g][0] * inv, acc[g][1] * inv);
+                *reinterpret_cast<float2*>(out) = make_float2(acc[g][0] * inv, acc[g][1] * inv);
             }
         }
     }
@@ -1149,7 +1171,12 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     }
 
     const int g = lane >> 2, t = lane & 3;     // fragment row group and column pair
-    const bool q_ok = g < G;                    // lanes with g >= G carry zero queries
+    bool q_ok = g < G;                          // lanes with g >= G carry zero queries
+    // block lanes (table-row form only): this lane's row, and how many positions
+    // before the lane's last one its token stops
+    const bool blocks = ROWS && p.blk_tok0 != nullptr;
+    int64_t q_row = 0;
+    int row_short = 0;
     // ldmatrix row addresses: matrix j = lane / 8, row r = lane % 8
     const int mj = lane >> 3, mr = lane & 7;
 
@@ -1168,7 +1195,14 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             piece_first = cur.tile;
             t_b = (int)seq_len_at(p, cur.b);
             w_start = (int)window_start(p, t_b);
-            const float* qp = p.q + (lane_id * G + (q_ok ? g : 0)) * D;
+            q_row = lane_id * G + (q_ok ? g : 0);
+            if (blocks) {
+                const int64_t br = g < G ? block_row(p, cur.b, cur.h, g) : -1;
+                q_ok = br >= 0;
+                q_row = q_ok ? br : 0;
+                row_short = q_ok ? __ldg(p.blk_ntok + cur.b) - 1 - g / p.blk_gp : 0;
+            }
+            const float* qp = p.q + q_row * D;
 #pragma unroll
             for (int ks = 0; ks < M::KSTEPS; ++ks) {
                 if constexpr (F32) {
@@ -1239,11 +1273,12 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
 
 
         if (last_tile && page_ok) {
-            // fused append: row t_b - 1 from k_new / v_new into the tile and the page;
+            // fused append: row t_b - 1 from k_new / v_new into the tile and the page
+            // (block lanes: every chunk row is already in its page and in the tile);
             // rows past it (stale bytes, possibly not finite) are cleared in V
             const int r = rows - 1;
             constexpr int EPC = 16 / M::ES;               // elements per 16-byte chunk
-            if (lane < M::CHUNKS) {
+            if (lane < M::CHUNKS && !blocks) {
                 const int64_t src = kv_new_row(p, cur.b, cur.h) * D + lane * EPC;
                 const uint4 kb = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src);
                 const uint4 vb = *reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src);
@@ -1318,20 +1353,26 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
             const int keys[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
             float alpha[NQ], pw[NQ][4];
             bool rescale = false;
+            // keys of this lane row in the tile (block lanes: its token ends row_short
+            // positions before the lane's last one)
+            const int rows_q = rows == 0 ? 0 : (rem - row_short < kTile ? rem - row_short : kTile);
 #pragma unroll
             for (int qi = 0; qi < NQ; ++qi) {
                 float tmax = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    if (!q_ok || keys[i] < lo || keys[i] >= rows) sc[qi][i] = -INFINITY;
+                    if (!q_ok || keys[i] < lo || keys[i] >= rows_q) sc[qi][i] = -INFINITY;
                     tmax = fmaxf(tmax, sc[qi][i]);
                 }
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
                 tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
                 const float m_new = q_ok ? fmaxf(m[qi], tmax) : 0.f;
-                alpha[qi] = q_ok ? exp2f(m[qi] - m_new) : 1.f;
+                // a block-lane row with no key yet (its positions end before this
+                // piece's tiles) keeps m = -inf: exponents taken from 0, weights 0
+                const float mb = m_new == -INFINITY ? 0.f : m_new;
+                alpha[qi] = q_ok ? exp2f(m[qi] - mb) : 1.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) pw[qi][i] = q_ok ? exp2f(sc[qi][i] - m_new) : 0.f;
+                for (int i = 0; i < 4; ++i) pw[qi][i] = q_ok ? exp2f(sc[qi][i] - mb) : 0.f;
                 l[qi] = fmaf(l[qi], alpha[qi], (pw[qi][0] + pw[qi][1]) + (pw[qi][2] + pw[qi][3]));
                 m[qi] = q_ok ? m_new : m[qi];
                 rescale = rescale || alpha[qi] != 1.f;
@@ -1438,7 +1479,7 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
 #pragma unroll
                     for (int qi = 0; qi < NQ; ++qi) {
                         const float inv = 1.f / lt[qi];
-                        float* op = p.out + (lane_id * G + g + 8 * qi) * D + 2 * t;
+                        float* op = p.out + (blocks ? q_row : lane_id * G + g + 8 * qi) * D + 2 * t;
 #pragma unroll
                         for (int nb = 0; nb < M::NB; ++nb) {
                             const float2 x = o_pair(nb, qi);
@@ -1750,6 +1791,14 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.pre_stride = a.pre_stride;
     p.wait_ns = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs;
     p.inject_worker = a.inject_worker;
+    p.blk_tok0 = a.blk_tok0;
+    p.blk_ntok = a.blk_ntok;
+    p.blk_gp = a.blk_gp;
+    p.blk_hq = a.blk_hq;
+    // block lanes exist only in the tensor-core kernel's table-row form (fp32)
+    if (a.blk_tok0 != nullptr &&
+        (a.table_rows == nullptr || a.tmap_k == nullptr || a.dtype != PKV_F32 || a.kv_shift != 0))
+        return cudaErrorInvalidValue;
     if (a.tmap_k != nullptr && a.tmap_v != nullptr) {
         // table rows on the tensor-core kernel: fp32 pools only (the bf16 pools it
         // serves prefill on the tcgen05 kernel, not through decode lanes)
@@ -1794,8 +1843,26 @@ struct LaneRowsParams {
     uint32_t* v_pages;
     const uint16_t* q_bf16;       // non-null: widen q into q32
     float* q32;
-    int32_t* rows;
+    int32_t* rows;                // nullptr with block lanes (the block plan writes them)
     int32_t* lens;
+    unsigned* err;
+};
+
+struct BlockPlanParams {
+    int B;
+    int64_t N;
+    int bt;                       // chunk tokens per block
+    int64_t X;                    // decode requests of the launch (blocks, then empty ones)
+    const int32_t* cu_new;        // nullptr: one request of single_n rows
+    const int32_t* seq_lens;
+    int single_n;
+    int64_t single_t;
+    int max_pages, P;
+    int32_t* first;               // [B + 1] first block of each request
+    int32_t* rows;                // [X] table row (request) of each block
+    int32_t* lens;                // [X] length at the block's last token (0: empty)
+    int32_t* tok0;                // [X] first chunk row
+    int32_t* ntok;                // [X] tokens
     unsigned* err;
 };
 
@@ -1834,7 +1901,7 @@ __global__ void __launch_bounds__(256) lane_rows_kernel(const LaneRowsParams p) 
                 if (page < 0 || page >= p.n_pages) page = -1;   // the decode kernel reports it
             }
         }
-        if (lane == 0) {
+        if (lane == 0 && p.rows != nullptr) {
             p.rows[x] = b;
             p.lens[x] = (int32_t)t;
         }
@@ -1856,23 +1923,117 @@ __global__ void __launch_bounds__(256) lane_rows_kernel(const LaneRowsParams p) 
     }
 }
 
+// Block lanes: request b's n_b chunk tokens form ceil(n_b / bt) blocks of bt
+// consecutive tokens (the last may hold fewer), numbered request by request.  One
+// CTA: block counts and their exclusive prefix over requests (first), then every
+// decode request x of the launch: its request, first chunk row, token count and
+// the length at its last token; x past the last block is empty (length 0).
+__global__ void __launch_bounds__(1024) block_plan_kernel(const BlockPlanParams p) {
+    __shared__ int warp_sum[32];
+    __shared__ int carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    auto cu = [&](int b) { return p.cu_new ? __ldg(p.cu_new + b) : (b == 0 ? 0 : p.single_n); };
+    auto seq = [&](int b) { return p.seq_lens ? (int64_t)__ldg(p.seq_lens + b) : p.single_t; };
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < p.B; base += 1024) {
+        const int b = base + tid;
+        int nb = 0;
+        if (b < p.B) {
+            const int c0 = cu(b), c1 = cu(b + 1);
+            const int64_t n = (int64_t)c1 - c0, t = seq(b);
+            const bool ok = c0 >= 0 && n >= 0 && c1 <= p.N && t - n >= 0 &&
+                            t <= (int64_t)p.max_pages * p.P;
+            if (!ok) atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
+            else nb = (int)((n + p.bt - 1) / p.bt);
+        }
+        int incl = nb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_sum[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int v = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            warp_sum[lane] = v;
+        }
+        __syncthreads();
+        const int carry = carry_s;
+        if (b < p.B) p.first[b] = carry + (wid > 0 ? warp_sum[wid - 1] : 0) + incl - nb;
+        __syncthreads();
+        if (tid == 0) carry_s = carry + warp_sum[31];
+        __syncthreads();
+    }
+    if (tid == 0) p.first[p.B] = carry_s;
+    __syncthreads();
+    const int total = carry_s;
+    for (int64_t x = tid; x < p.X; x += 1024) {
+        int32_t row = 0, len = 0, t0 = 0, nt = 0;
+        if (x < total) {
+            int lo = 0, hi = p.B;                       // last request with first[b] <= x
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (p.first[mid] <= x) lo = mid;
+                else hi = mid;
+            }
+            const int b = lo;
+            const int c0 = cu(b), n = cu(b + 1) - c0;
+            const int blk = (int)(x - p.first[b]);
+            row = b;
+            t0 = c0 + blk * p.bt;
+            nt = n - blk * p.bt < p.bt ? n - blk * p.bt : p.bt;
+            len = (int32_t)(seq(b) - n + (int64_t)blk * p.bt + nt);
+        }
+        p.rows[x] = row;
+        p.lens[x] = len;
+        p.tok0[x] = t0;
+        p.ntok[x] = nt;
+    }
+}
+
 }  // namespace
 
-PrefillLanesLayout prefill_lanes_layout(int64_t N, int lane_heads, int D, int workers,
-                                        int lane_group, int query_heads, bool widen_q) {
+int prefill_block_tokens(int dtype, int D, int G, int kv_shift, int64_t window, bool tmaps) {
+    if (dtype != PKV_F32 || !tmaps || window > 0 || kv_shift != 0 || (D != 64 && D != 128))
+        return 0;
+    return (G == 1 || G == 2 || G == 4) && mma_supported(PKV_F32, D, 8) ? 8 / G : 0;
+}
+
+PrefillLanesLayout prefill_lanes_layout(int64_t N, int batch, int block_tokens, int lane_heads,
+                                        int D, int workers, int lane_group, int query_heads,
+                                        bool widen_q) {
     PrefillLanesLayout L{};
-    L.decode = align_up(workspace_layout((int)N, lane_heads, D, workers, lane_group).total, 256);
+    const bool blocks = block_tokens > 0;
+    const int64_t X = blocks ? N / block_tokens + batch : N;
+    L.requests = X;
+    L.decode = align_up(workspace_layout((int)X, lane_heads, D, workers, blocks ? 8 : lane_group).total,
+                        256);
     L.rows = L.decode;
-    L.lens = align_up(L.rows + sizeof(int32_t) * (size_t)N, 256);
-    L.q32 = align_up(L.lens + sizeof(int32_t) * (size_t)N, 256);
+    L.lens = align_up(L.rows + sizeof(int32_t) * (size_t)X, 256);
+    L.tok0 = align_up(L.lens + sizeof(int32_t) * (size_t)X, 256);
+    L.ntok = blocks ? align_up(L.tok0 + sizeof(int32_t) * (size_t)X, 256) : L.tok0;
+    L.first = blocks ? align_up(L.ntok + sizeof(int32_t) * (size_t)X, 256) : L.ntok;
+    L.q32 = blocks ? align_up(L.first + sizeof(int32_t) * ((size_t)batch + 1), 256) : L.first;
     L.total = widen_q ? L.q32 + sizeof(float) * (size_t)N * query_heads * D : L.q32;
     return L;
 }
 
 cudaError_t launch_prefill_lanes(const PrefillLanesArgs& a, cudaStream_t stream) {
     const bool widen = a.dtype == PKV_BF16;
-    const PrefillLanesLayout L = prefill_lanes_layout(a.total_new, a.lane_heads, a.D, a.workers,
-                                                      a.lane_group, a.query_heads, widen);
+    const bool blocks = a.block_tokens > 0;
+    if (blocks && (widen || a.tmap_k == nullptr || a.kv_shift != 0 || a.window > 0))
+        return cudaErrorInvalidValue;
+    const int nreq = a.cu_new ? a.batch : 1;
+    const PrefillLanesLayout L = prefill_lanes_layout(a.total_new, nreq, a.block_tokens,
+                                                      a.lane_heads, a.D, a.workers, a.lane_group,
+                                                      a.query_heads, widen);
     unsigned char* ws = static_cast<unsigned char*>(a.workspace);
     LaneRowsParams r{};
     r.B = a.cu_new ? a.batch : 1;
@@ -1895,20 +2056,41 @@ cudaError_t launch_prefill_lanes(const PrefillLanesArgs& a, cudaStream_t stream)
     r.v_pages = static_cast<uint32_t*>(a.v_pages);
     r.q_bf16 = widen ? static_cast<const uint16_t*>(a.q) : nullptr;
     r.q32 = widen ? reinterpret_cast<float*>(ws + L.q32) : nullptr;
-    r.rows = reinterpret_cast<int32_t*>(ws + L.rows);
-    r.lens = reinterpret_cast<int32_t*>(ws + L.lens);
+    r.rows = blocks ? nullptr : reinterpret_cast<int32_t*>(ws + L.rows);
+    r.lens = blocks ? nullptr : reinterpret_cast<int32_t*>(ws + L.lens);
     r.err = a.dev_error;
     const int64_t want = (a.total_new + 7) / 8;
     lane_rows_kernel<<<(unsigned)(want < 4096 ? (want < 1 ? 1 : want) : 4096), 256, 0, stream>>>(r);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (blocks) {
+        BlockPlanParams bp{};
+        bp.B = nreq;
+        bp.N = a.total_new;
+        bp.bt = a.block_tokens;
+        bp.X = L.requests;
+        bp.cu_new = a.cu_new;
+        bp.seq_lens = a.seq_lens;
+        bp.single_n = a.single_n;
+        bp.single_t = a.single_t;
+        bp.max_pages = a.max_pages;
+        bp.P = a.P;
+        bp.first = reinterpret_cast<int32_t*>(ws + L.first);
+        bp.rows = reinterpret_cast<int32_t*>(ws + L.rows);
+        bp.lens = reinterpret_cast<int32_t*>(ws + L.lens);
+        bp.tok0 = reinterpret_cast<int32_t*>(ws + L.tok0);
+        bp.ntok = reinterpret_cast<int32_t*>(ws + L.ntok);
+        bp.err = a.dev_error;
+        block_plan_kernel<<<1, 1024, 0, stream>>>(bp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     DecodeArgs d{};
     d.dtype = a.dtype;
-    d.B = (int)a.total_new;
+    d.B = (int)L.requests;
     d.H = a.lane_heads;
     d.D = a.D;
     d.P = a.P;
-    d.G = a.lane_group;
+    d.G = blocks ? 8 : a.lane_group;
     d.kv_shift = a.kv_shift;
     d.window = a.window;
     d.q = widen ? reinterpret_cast<const float*>(ws + L.q32) : static_cast<const float*>(a.q);
@@ -1919,8 +2101,14 @@ cudaError_t launch_prefill_lanes(const PrefillLanesArgs& a, cudaStream_t stream)
     d.n_pages = a.n_pages;
     d.tables = a.tables;
     d.max_pages = a.max_pages;
-    d.table_rows = r.rows;
-    d.seq_lens = r.lens;
+    d.table_rows = reinterpret_cast<int32_t*>(ws + L.rows);
+    d.seq_lens = reinterpret_cast<int32_t*>(ws + L.lens);
+    if (blocks) {
+        d.blk_tok0 = reinterpret_cast<int32_t*>(ws + L.tok0);
+        d.blk_ntok = reinterpret_cast<int32_t*>(ws + L.ntok);
+        d.blk_gp = a.lane_group;
+        d.blk_hq = a.query_heads;
+    }
     d.max_seq_len = (int64_t)a.max_pages * a.P;
     d.out = a.out;
     d.workspace = a.workspace;

@@ -61,6 +61,9 @@ struct DecodeArgs {
     cudaError_t (*before_split)(const void* ctx, cudaStream_t stream);
     const void* before_split_ctx;
     bool allow_empty;        // a seq_len of 0 is a request with no work (not an error)
+    const int32_t* blk_tok0; // block lanes (see PrefillLanesArgs::block_tokens): [B] first
+    const int32_t* blk_ntok; //   chunk row and token count of decode request x; nullptr: off
+    int blk_gp, blk_hq;      //   the pool's query heads per KV head, and query heads
     uint64_t wait_limit_ns;  // bounded waits give up after this long (0: the default, 4 s)
     int inject_worker;       // failure injection: 0 off; else split worker inject_worker - 1
                              // arms its first stage's barrier without issuing the copy
@@ -194,15 +197,31 @@ struct PrefillLanesArgs {
     const void* tmap_v;
     cudaEvent_t ev_before;
     cudaEvent_t ev_after;
+    // > 0: block lanes -- decode request x is a block of up to block_tokens consecutive
+    // chunk tokens of one request (its last block may hold fewer), each token's query
+    // heads rows of one lane of the tensor-core kernel with its own causal end;
+    // 0: one decode request per chunk token
+    int block_tokens;
 };
 
+// Chunk tokens per decode request of the decode-lane prefill: block lanes for fp32
+// pools of head width 64 or 128 with 1, 2 or 4 query heads per KV head and no
+// sliding window (8 lane rows on the tensor-core kernel), else 0.
+int prefill_block_tokens(int dtype, int D, int G, int kv_shift, int64_t window, bool tmaps);
+
 struct PrefillLanesLayout {
-    size_t decode;                // the decode workspace of N lanes, at offset 0
-    size_t rows, lens, q32;       // int32 [N] table rows, int32 [N] lengths, fp32 widened q
+    int64_t requests;             // decode requests of the launch
+    size_t decode;                // their decode workspace, at offset 0
+    size_t rows, lens;            // int32 [requests]: table rows, lengths
+    size_t tok0, ntok, first;     // block lanes: int32 [requests] first chunk row and token
+                                  // count of each block, int32 [batch + 1] first block of
+                                  // each request
+    size_t q32;                   // fp32 widened q (bf16 pools)
     size_t total;
 };
-PrefillLanesLayout prefill_lanes_layout(int64_t N, int lane_heads, int D, int workers,
-                                        int lane_group, int query_heads, bool widen_q);
+PrefillLanesLayout prefill_lanes_layout(int64_t N, int batch, int block_tokens, int lane_heads,
+                                        int D, int workers, int lane_group, int query_heads,
+                                        bool widen_q);
 cudaError_t launch_prefill_lanes(const PrefillLanesArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------- shared prefix --

@@ -154,18 +154,33 @@ bool tensor_prefill(const pkv_pool* p) {
     return p->tmaps && pkv::prefill_supported(p->dtype, p->head_dim, p->group);
 }
 
-int lanes_workers(const pkv_pool* p, int64_t n) {
+// Chunk tokens per decode request of the decode-lane prefill (0: one per token).
+int block_tokens(const pkv_pool* p) {
+    return pkv::prefill_block_tokens(p->dtype, p->head_dim, p->dec_group, p->kv_shift, p->window,
+                                     p->tmaps);
+}
+
+// Decode workers of a decode-lane prefill of n chunk tokens over `batch` requests:
+// block lanes run on the tensor-core kernel with 8 rows a lane.
+int lanes_workers(const pkv_pool* p, int batch, int64_t n) {
+    const int bt = block_tokens(p);
+    if (bt > 0) {
+        const int resident = pkv::resident_workers(p->dtype, p->head_dim, 8, p->sms, true);
+        return pkv::launch_workers(resident, (int)(n / bt + batch), p->heads,
+                                   pkv::attended_len(p->max_context, p->window), 0);
+    }
     return pkv::launch_workers(p->workers, (int)n, p->dec_heads,
                                pkv::attended_len(p->max_context, p->window), p->kv_shift);
 }
 
-size_t lanes_bytes(const pkv_pool* p, int64_t n) {
-    return pkv::prefill_lanes_layout(n, p->dec_heads, p->head_dim, lanes_workers(p, n),
-                                     p->dec_group, p->query_heads, p->dtype == PKV_BF16)
+size_t lanes_bytes(const pkv_pool* p, int batch, int64_t n) {
+    return pkv::prefill_lanes_layout(n, batch, block_tokens(p), p->dec_heads, p->head_dim,
+                                     lanes_workers(p, batch, n), p->dec_group, p->query_heads,
+                                     p->dtype == PKV_BF16)
         .total;
 }
 
-pkv::PrefillLanesArgs lanes_args(pkv_pool* p, int layer, int64_t n) {
+pkv::PrefillLanesArgs lanes_args(pkv_pool* p, int layer, int batch, int64_t n) {
     pkv::PrefillLanesArgs a{};
     a.dtype = p->dtype;
     a.D = p->head_dim;
@@ -180,13 +195,16 @@ pkv::PrefillLanesArgs lanes_args(pkv_pool* p, int layer, int64_t n) {
     a.k_pages = static_cast<unsigned char*>(p->k_base) + (size_t)layer * p->layer_bytes;
     a.v_pages = static_cast<unsigned char*>(p->v_base) + (size_t)layer * p->layer_bytes;
     a.n_pages = p->pages;
-    a.workers = lanes_workers(p, n);
+    a.batch = batch;
+    a.workers = lanes_workers(p, batch, n);
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
     // decode lanes read table rows: on the tensor-core kernel for fp32 pools that use
-    // it (the bf16 pools it serves prefill on the tcgen05 kernel, not through lanes)
-    const bool tc = p->tensor_cores && p->dtype == PKV_F32;
+    // it or that run block lanes (the bf16 pools it serves prefill on the tcgen05
+    // kernel, not through lanes)
+    a.block_tokens = block_tokens(p);
+    const bool tc = (p->tensor_cores && p->dtype == PKV_F32) || a.block_tokens > 0;
     a.tmap_k = tc ? &p->tmap_k[(size_t)layer] : nullptr;
     a.tmap_v = tc ? &p->tmap_v[(size_t)layer] : nullptr;
     return a;
@@ -848,7 +866,7 @@ int pkv_prefill_chunk(pkv_request* r, int layer, const void* q, const void* k, c
     if (!tensor_prefill(p)) {
         // decode lanes: the request's scratch grows to the chunk (freeing the old
         // one waits for the device)
-        const size_t need = lanes_bytes(p, r->pending_n);
+        const size_t need = lanes_bytes(p, 1, r->pending_n);
         if (r->prefill_ws_bytes < need) {
             void* ws = nullptr;
             cudaError_t e = cudaMalloc(&ws, need);
@@ -862,8 +880,7 @@ int pkv_prefill_chunk(pkv_request* r, int layer, const void* q, const void* k, c
         }
         rc = prepare_layer_write(r, layer, s);
         if (rc != PKV_OK) return rc;
-        pkv::PrefillLanesArgs a = lanes_args(p, layer, r->pending_n);
-        a.batch = 1;
+        pkv::PrefillLanesArgs a = lanes_args(p, layer, 1, r->pending_n);
         a.q = q;
         a.k_new = k;
         a.v_new = v;
@@ -1064,7 +1081,7 @@ int pkv_prefill_workspace_size(const pkv_pool* p, int batch, int64_t total_new, 
         return fail(PKV_ERR_INVALID_ARGUMENT, "negative batch or token count");
     *bytes = (batch == 0 || total_new == 0) ? 0
              : tensor_prefill(p)            ? pkv::prefill_workspace_bytes(batch, p->group, total_new)
-                                            : lanes_bytes(p, total_new);
+                                            : lanes_bytes(p, batch, total_new);
     return ok();
 }
 
@@ -1094,15 +1111,14 @@ int pkv_paged_prefill(pkv_pool* p, int layer, int batch, int64_t total_new, cons
         return fail(PKV_ERR_INVALID_ARGUMENT, "%lld tokens need more CTAs than one launch holds",
                     (long long)total_new);
     const size_t need =
-        tc ? pkv::prefill_workspace_bytes(batch, p->group, total_new) : lanes_bytes(p, total_new);
+        tc ? pkv::prefill_workspace_bytes(batch, p->group, total_new) : lanes_bytes(p, batch, total_new);
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed", workspace_bytes,
                     need);
     int rc = check_device(p);
     if (rc != PKV_OK) return rc;
     if (!tc) {
-        pkv::PrefillLanesArgs a = lanes_args(p, layer, total_new);
-        a.batch = batch;
+        pkv::PrefillLanesArgs a = lanes_args(p, layer, batch, total_new);
         a.q = q;
         a.k_new = k_new;
         a.v_new = v_new;

@@ -139,6 +139,18 @@ def chunked_prefill(seed: int = 8, B: int = 8, chunk: int = 4096, cached_max: in
                     group=4, new_tokens=new)
 
 
+def chunked_prefill_f32(seed: int = 9, B: int = 8, chunk: int = 1024, cached_max: int = 1024) -> Workload:
+    """Chunked prefill of an fp32 pool: 8 requests each append a chunk of 1024 tokens
+    after U{0..1024} cached ones; 8 KV heads, one query head each, d_h=128, fp32,
+    pool of 2048 shuffled pages."""
+    rng = np.random.default_rng(seed)
+    cached = rng.integers(0, cached_max + 1, size=B)
+    new = np.full(B, chunk, dtype=np.int32)
+    lens = (cached + new).astype(np.int32)
+    return Workload("prefill_f32", B, 1, 8, 128, 16, F32, 2048, cached_max + chunk, seed, lens,
+                    group=1, new_tokens=new)
+
+
 def attended_pairs(w: Workload) -> int:
     """(query row, key) pairs of a prefill: sum over chunk tokens of the keys each attends,
     times the query heads."""
@@ -179,4 +191,5 @@ REGISTRY = {
     "window_bf16": sliding_window,
     "prefix_bf16": shared_prompt,
     "prefill_bf16": chunked_prefill,
+    "prefill_f32": chunked_prefill_f32,
 }

@@ -3,7 +3,10 @@
 Pools the tensor-core prefill does not serve (fp32 storage; bf16 head widths other
 than 64 and 128) prefill by storing every chunk row in its page and running chunk
 token i of request b as one decode request of retained length L0_b + i + 1 over
-request b's pages -- the n_b successive decode steps the prefill stands for.  The
+request b's pages -- the n_b successive decode steps the prefill stands for.  fp32
+pools of head width 64 or 128 with 1, 2 or 4 query heads per KV head and no window
+run block lanes: 8 / G consecutive chunk tokens share one decode lane of the
+tensor-core kernel, each lane row masked at its own token's position.  The
 bars are therefore the decode ones: max abs error <= 1e-5 for fp32 storage,
 normwise relative error <= 5e-3 per (token, query head) row for bf16; the K/V rows
 written into the pages bit-exact.
@@ -35,6 +38,11 @@ CASES = {
     "f32_d128_mqa16_page32": ([17, 0], [90, 33], 1, 128, 16, 32, 0, F32),
     "f32_d16_window_ragged": ([0, 3, 700], [129, 255, 1], 2, 16, 1, 16, 33, F32),
     "f32_empty_requests": ([10, 5, 0], [0, 20, 0], 2, 64, 2, 16, 0, F32),
+    # block lanes (fp32, head width 64 / 128, 1, 2 or 4 query heads per KV head, no
+    # window): 8 / G consecutive chunk tokens share one lane of the tensor-core kernel
+    "f32_d128_mha_blocks": ([0, 16, 255], [1, 17, 300], 1, 128, 1, 16, 0, F32),
+    "f32_d128_gqa2_blocks": ([0, 100, 1000], [37, 8, 129], 2, 128, 2, 16, 0, F32),
+    "f32_d64_gqa4_blocks_page32": ([5, 0], [3, 77], 2, 64, 4, 32, 0, F32),
     "bf16_d32_mha": ([0, 129, 40], [100, 33, 64], 2, 32, 1, 16, 0, BF16),
     "bf16_d256_mha": ([20], [70], 1, 256, 1, 16, 0, BF16),
 }
@@ -61,6 +69,27 @@ def test_prefill_lanes_match_oracle(name):
                 x = int(run.cu[b]) + i
                 assert np.array_equal(k, run.k_new[x]) and np.array_equal(v, run.v_new[x])
         print(f"{name}: worst error {worst:.2e}")
+    finally:
+        run.close()
+
+
+def test_block_lanes_many_requests():
+    """Over 1024 requests (the block plan's scan loops over request chunks) of
+    chunks of 0 to 9 tokens: every row against the oracle."""
+    rng = np.random.default_rng(46)
+    B = 1100
+    new = rng.integers(0, 10, size=B)
+    cached = rng.integers(0, 40, size=B)
+    w = make_prefill("many", cached, new, 1, 64, group=2, seed=47, dtype=F32)
+    run = PrefillRun(w)
+    try:
+        out = run.run().cpu().numpy()
+        torch.cuda.synchronize()
+        assert run.pool.check_device_status() == 0
+        for b in range(0, B, 7):                    # a seventh of the requests
+            if int(w.new_tokens[b]) == 0:
+                continue
+            check_close(out[run.cu[b]:run.cu[b + 1]], run.oracle_out(b), F32, f"request {b}")
     finally:
         run.close()
 
