@@ -896,12 +896,15 @@ split_decode_kernel(const KParams p) {
 #pragma unroll
                     for (int g = 0; g < G; ++g) p.part_ml[slot * G + g] = make_float2(m[g], lt[g]);
                 }
-                fence_acq_rel_gpu();   // release: the partial before the counter
-                __syncwarp();
-                if (p.pre_ml != nullptr) {       // the combine kernel merges every lane
+                if (p.pre_ml != nullptr) {
+                    // the combine kernel merges every lane, after this kernel: no counter,
+                    // and the kernel boundary orders the partials
+                    __syncwarp();
                     cursor_advance(cur, p);
                     continue;
                 }
+                fence_acq_rel_gpu();   // release: every lane's share of the partial
+                __syncwarp();          // before lane 0 counts it
                 const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // KV lane's first tile
                 const int64_t r_lo = worker_of(A, T_all, R);
                 const int64_t r_hi = worker_of(A + cur.n - 1, T_all, R);
@@ -1500,12 +1503,15 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                         if (t == 0) p.part_ml[slot * G + g + 8 * qi] = make_float2(m[qi], lt[qi]);
                     }
                 }
-                fence_acq_rel_gpu();   // release: the partial before the counter
-                __syncwarp();
-                if (p.pre_ml != nullptr) {       // the combine kernel merges every lane
+                if (p.pre_ml != nullptr) {
+                    // the combine kernel merges every lane, after this kernel: no counter,
+                    // and the kernel boundary orders the partials
+                    __syncwarp();
                     cursor_advance(cur, p);
                     continue;
                 }
+                fence_acq_rel_gpu();   // release: every lane's share of the partial
+                __syncwarp();          // before lane 0 counts it
                 const int64_t A = cur.first + (int64_t)cur.h * cur.n;   // KV lane's first tile
                 const int64_t r_lo = worker_of(A, T_all, R);
                 const int64_t r_hi = worker_of(A + cur.n - 1, T_all, R);
