@@ -131,6 +131,13 @@ struct Geo {
     // per warp: stage buffers, then per stage an mbarrier (8 B) and the staged page id (4 B)
     static constexpr int CTA_SMEM = WARPS * (WARP_SMEM + STAGES * 12);
     static constexpr int DPL = D >= 32 ? D / 32 : 1;           // features per lane when merging
+    // cluster lanes (a single request): after the rings, 8 lane mbarriers and a
+    // partial slot (max, sum, o[D]) for each worker of up to 8 CTAs
+    static constexpr int CLU_OFF = (CTA_SMEM + 15) / 16 * 16;
+    static constexpr int LANE_SLOTS = 8 * WARPS;
+    static constexpr int CLU_BYTES = 64 + LANE_SLOTS * (D + 2) * 4;
+    static constexpr bool CLUSTER_LANES =
+        (WARPS == 4 || WARPS == 8) && CLU_OFF + CLU_BYTES <= 227 * 1024;
     static_assert(D % VEC == 0 && VEC % 2 == 0, "unsupported head width");
     static_assert(TPR <= 32 && (TPR & (TPR - 1)) == 0, "unsupported head width");
     static_assert(RPI * ITERS >= kTile, "a warp step pattern must cover the tile");
@@ -183,6 +190,12 @@ struct KParams {
     uint64_t wait_ns;           // each bounded wait gives up after this long
     int inject_worker;          // failure injection: 0 off; else worker inject_worker - 1 arms
                                 // its first stage without issuing the copy
+    // cluster lanes (a single request on the CUDA-core kernel, multi-head pools):
+    // > 0: each lane's tiles are split over lane_workers consecutive workers (of this
+    // CTA when fewer than a CTA's warps, else of the lane_workers / WARPS CTAs of one
+    // cluster), which merge through the lead CTA's shared memory instead of global
+    // partials and counters; 0: off
+    int lane_workers;
     // block lanes (prefill of fp32 pools on the tensor-core kernel's table-row form):
     // decode request x is a block of blk_ntok[x] consecutive chunk tokens starting at
     // chunk row blk_tok0[x]; lane row g is token g / blk_gp of the block and query
@@ -596,6 +609,21 @@ split_decode_kernel(const KParams p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t w = (int64_t)blockIdx.x * Gm::WARPS + warp;
+    // cluster lanes: every CTA's lane barriers are initialised before any worker of
+    // the cluster can arrive on them (every thread takes part, so before any return)
+    uint64_t* lane_bar = reinterpret_cast<uint64_t*>(smem + Gm::CLU_OFF);        // [8]
+    float* lane_part = reinterpret_cast<float*>(smem + Gm::CLU_OFF + 64);        // [slots][D+2]
+    if constexpr (Gm::CLUSTER_LANES) {
+        if (p.lane_workers > 0) {
+            if (threadIdx.x < 8) mbar_init(&lane_bar[threadIdx.x], 32u * (uint32_t)p.lane_workers);
+            if (p.lane_workers > Gm::WARPS) {     // lanes span the CTAs of a cluster
+                if (threadIdx.x == 0) fence_mbar_init();
+                cluster_sync_all();
+            } else {                               // lanes inside this CTA
+                __syncthreads();
+            }
+        }
+    }
     if (w >= p.W) return;
 
     unsigned char* ring = smem + warp * Gm::WARP_SMEM;
@@ -880,6 +908,81 @@ split_decode_kernel(const KParams p) {
                             op[v] = make_float2(o[g][v].x * inv, o[g][v].y * inv);
                     }
                 }
+            } else if (Gm::CLUSTER_LANES && G == 1 && p.lane_workers > 0) {
+                // cluster lanes: worker j of the lane's kw writes its partial into slot
+                // j of the lead CTA (cluster rank 0; this CTA when kw < WARPS) and
+                // arrives on the lane's barrier there; worker 0 waits and merges
+                const int kw = p.lane_workers;
+                const bool clu = kw > Gm::WARPS;            // else the lane is inside this CTA
+                const int j = (int)(w % kw);
+                const int slot = clu ? j : warp;
+                const int bidx = clu ? 0 : warp / kw;
+                if (clu) {
+                    const uint32_t part = cluster_map(smem_u32(lane_part + slot * (D + 2)), 0);
+                    if (lane < Gm::TPR) {
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            st_cluster_f32(part + 4u * (uint32_t)(2 + col + 2 * v), o[0][v].x);
+                            st_cluster_f32(part + 4u * (uint32_t)(3 + col + 2 * v), o[0][v].y);
+                        }
+                    }
+                    if (lane == 0) {
+                        st_cluster_f32(part, m[0]);
+                        st_cluster_f32(part + 4u, lt[0]);
+                    }
+                    // each lane releases its own stores (cluster scope)
+                    mbar_arrive_cluster(cluster_map(smem_u32(&lane_bar[bidx]), 0));
+                } else {
+                    float* part = lane_part + slot * (D + 2);
+                    if (lane < Gm::TPR) {
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            part[2 + col + 2 * v] = o[0][v].x;
+                            part[3 + col + 2 * v] = o[0][v].y;
+                        }
+                    }
+                    if (lane == 0) {
+                        part[0] = m[0];
+                        part[1] = lt[0];
+                    }
+                    mbar_arrive(&lane_bar[bidx]);   // release at CTA scope
+                }
+                if (j == 0) {
+                    const bool arrived_all = clu ? mbar_wait_cluster_bounded(&lane_bar[bidx], 0, p.wait_ns)
+                                                 : mbar_wait_bounded(&lane_bar[bidx], 0, p.wait_ns);
+                    if (!arrived_all) {
+                        if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+                    } else {
+                        constexpr int DPL = Gm::DPL;
+                        const float* base = lane_part + (slot - j) * (D + 2);
+                        float M = -INFINITY;
+                        for (int s2 = lane; s2 < kw; s2 += 32) M = fmaxf(M, base[s2 * (D + 2)]);
+#pragma unroll
+                        for (int off = 16; off >= 1; off >>= 1)
+                            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                        float L = 0.f, acc[DPL];
+#pragma unroll
+                        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+                        const bool feat = lane * DPL < D;
+                        for (int s2 = 0; s2 < kw; ++s2) {
+                            const float* ps = base + s2 * (D + 2);
+                            const float ls = ps[1];
+                            const float ws = ls > 0.f ? exp2f(ps[0] - M) : 0.f;
+                            L = fmaf(ls, ws, L);
+                            if (feat) {
+#pragma unroll
+                                for (int i = 0; i < DPL; ++i) acc[i] = fmaf(ws, ps[2 + lane * DPL + i], acc[i]);
+                            }
+                        }
+                        if (feat) {
+                            const float inv = 1.f / L;
+                            float* op = p.out + lane_id * D + lane * DPL;
+#pragma unroll
+                            for (int i = 0; i < DPL; ++i) op[i] = acc[i] * inv;
+                        }
+                    }
+                }
+                __syncwarp();
             } else {
                 // deposit the partial; the last of the lane's workers to arrive merges
                 const int64_t slot =      // partial of KV lane K from range r, this sub-lane
@@ -1588,9 +1691,11 @@ template <typename T, int D, int G>
 static cudaError_t prepare_split() {
     static bool done = false;   // per instantiation
     if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(split_decode_kernel<T, D, G, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Geo<T, D, G>::CTA_SMEM);
+    using Gm = Geo<T, D, G>;
+    // room for the cluster-lane barriers and partial slots in single-request launches
+    cudaError_t e = cudaFuncSetAttribute(
+        split_decode_kernel<T, D, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        Gm::CLUSTER_LANES && G == 1 ? Gm::CLU_OFF + Gm::CLU_BYTES : Gm::CTA_SMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(split_decode_kernel<T, D, G, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<T, D, G>::CTA_SMEM);
@@ -1621,18 +1726,58 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     // the timing events bracket the attention: the prefix kernel, if any, and the split kernel
     if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
     if (a.before_split && (e = a.before_split(a.before_split_ctx, stream)) != cudaSuccess) return e;
+    // cluster lanes for a single request on a multi-head pool: kw workers per lane,
+    // a power of two below a CTA's warps (lanes inside one CTA) or a multiple of them
+    // (one cluster of kw / WARPS CTAs per lane); every lane has the same tiles
+    int kw = 0;
+    if constexpr (Gm::CLUSTER_LANES && G == 1) {
+        if (p.seq_lens == nullptr && p.kv_shift == 0 && p.table_rows == nullptr &&
+            p.pre_ml == nullptr && p.inject_worker == 0) {
+            const int64_t t = p.single_t;
+            const int64_t ws = (p.window > 0 && t > p.window) ? t - p.window : 0;
+            const int64_t n = (t + kTile - 1) / kTile - ws / kTile;    // tiles per lane
+            int64_t k0 = (n + PKV_MIN_TILES_PER_WORKER - 1) / PKV_MIN_TILES_PER_WORKER;
+            if (k0 < 1) k0 = 1;
+            int64_t k = 1;
+            if (k0 <= Gm::WARPS) {
+                while (k < k0) k <<= 1;
+            } else {
+                k = (k0 + Gm::WARPS - 1) / Gm::WARPS * Gm::WARPS;
+            }
+            static int sms = 0;
+            if (sms == 0) {
+                int dev = 0;
+                if (cudaGetDevice(&dev) != cudaSuccess ||
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                    sms = -1;
+            }
+            const int64_t ctas = ((int64_t)p.H * k + Gm::WARPS - 1) / Gm::WARPS;
+            if (k <= 8 * Gm::WARPS && k <= n && sms > 0 && ctas <= sms) kw = (int)k;
+        }
+    }
+    if (kw > 0) {
+        p.lane_workers = kw;
+        p.W = p.H * kw;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)((p.W + Gm::WARPS - 1) / Gm::WARPS));
     cfg.blockDim = dim3(Gm::WARPS * 32);
-    cfg.dynamicSmemBytes = Gm::CTA_SMEM;
+    cfg.dynamicSmemBytes = kw > 0 ? Gm::CLU_OFF + Gm::CLU_BYTES : Gm::CTA_SMEM;
     cfg.stream = stream;
     // dependent launch: behind this call's own plan kernel, or (a single request)
     // behind whatever came before; the kernel waits for it before reading anything
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (kw > Gm::WARPS) {   // a lane spans the CTAs of one cluster
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)(kw / Gm::WARPS);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     e = p.table_rows != nullptr ? cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G, true>, p)
                                 : cudaLaunchKernelEx(&cfg, split_decode_kernel<T, D, G, false>, p);
     if (e != cudaSuccess) return e;
