@@ -1674,6 +1674,11 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G) {
     return L;
 }
 
+#ifndef PKV_LANE_MIN_TILES
+// cluster lanes: tiles per worker at least (their merge through shared memory is
+// cheap, so a worker's tiles can all be in flight in its ring at once)
+#define PKV_LANE_MIN_TILES 3
+#endif
 #ifndef PKV_MIN_TILES_PER_WORKER
 #define PKV_MIN_TILES_PER_WORKER 4   // below this much work a worker's fixed costs dominate
 #endif
@@ -1736,7 +1741,7 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
             const int64_t t = p.single_t;
             const int64_t ws = (p.window > 0 && t > p.window) ? t - p.window : 0;
             const int64_t n = (t + kTile - 1) / kTile - ws / kTile;    // tiles per lane
-            int64_t k0 = (n + PKV_MIN_TILES_PER_WORKER - 1) / PKV_MIN_TILES_PER_WORKER;
+            int64_t k0 = (n + PKV_LANE_MIN_TILES - 1) / PKV_LANE_MIN_TILES;
             if (k0 < 1) k0 = 1;
             int64_t k = 1;
             if (k0 <= Gm::WARPS) {
