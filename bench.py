@@ -51,7 +51,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 def make_workload(name: str, rank: int = 0, requests: int = 0):
     """The named workload; ``requests`` > 0 keeps only its first requests (small
-    profiling captures; the long-context pool shrinks to match)."""
+    profiling captures that hold a few GB on the device).  The pool shrinks to
+    match: exactly the kept pages for the long-context workload (all its pages are
+    used), else at most twice them, so the tables still scatter over a pool."""
     from synth import workloads
     w = workloads.REGISTRY[name]()
     w.seed += 1000 * rank          # each replica draws its own values
@@ -60,8 +62,8 @@ def make_workload(name: str, rank: int = 0, requests: int = 0):
         w.seq_lens = w.seq_lens[:requests].copy()
         if w.new_tokens is not None:
             w.new_tokens = w.new_tokens[:requests].copy()
-        if w.name == "long":
-            w.pool_pages = int(w.n_pages.sum())
+        kept = int(w.n_pages.sum())
+        w.pool_pages = min(w.pool_pages, kept if w.name == "long" else 2 * kept)
         w.name += f"_first{requests}"
     return w
 
