@@ -190,6 +190,10 @@ struct KParams {
     uint64_t wait_ns;           // each bounded wait gives up after this long
     int inject_worker;          // failure injection: 0 off; else worker inject_worker - 1 arms
                                 // its first stage without issuing the copy
+    // next layer's pools, or nullptr: every staged (page, head) block of this layer
+    // is also fetched into L2 from these, for the same request's next layer call
+    const void* next_k;
+    const void* next_v;
     // cluster lanes (a single request on the CUDA-core kernel, multi-head pools):
     // > 0: each lane's tiles are split over lane_workers consecutive workers (of this
     // CTA when fewer than a CTA's warps, else of the lane_workers / WARPS CTAs of one
@@ -642,11 +646,16 @@ split_decode_kernel(const KParams p) {
     // single request's partition is closed-form and its lane counters carry an
     // epoch, so it runs without a plan kernel; it is launched as a dependent of
     // whatever came before (the previous layer's call) and lets the next call's
-    // kernel launch at once.  Either way nothing global is read before the
-    // previous grid is complete, so every earlier write is visible.
+    // kernel launch at once.  Either way nothing an earlier kernel may have written
+    // is read before the previous grid is complete, so every such write is visible.
     const bool batched = p.seq_lens != nullptr;
+    // A single request's page table is written only by copies in stream order, never
+    // by a kernel, so its first entries are read (and its first tiles fetched into
+    // L2, which changes no memory) before the wait; the copies into shared memory,
+    // q and the pages' rows are read after it.
+    const bool early = !batched && !ROWS;
     if (!batched) pdl_launch_dependents();
-    pdl_wait_primary();
+    if (!early) pdl_wait_primary();
 
     // this worker's tiles: range w >> kv_shift, [begin, end) of the flattened (request,
     // KV head, tile) sequence, for sub-lane w & (2^kv_shift - 1) of every KV head in it
@@ -656,7 +665,10 @@ split_decode_kernel(const KParams p) {
     const int64_t begin = ((w >> p.kv_shift) * T_all) / R;
     const int64_t end = (((w >> p.kv_shift) + 1) * T_all) / R;
     const int n_work = (int)(end - begin);
-    if (n_work <= 0) return;
+    if (n_work <= 0) {
+        if (early) pdl_wait_primary();
+        return;
+    }
 
     Cursor cur;
     {
@@ -704,9 +716,32 @@ split_decode_kernel(const KParams p) {
         bulk_copy_g2s(dst, static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES, &bars[s], policy);
         bulk_copy_g2s(dst + Gm::TILE_BYTES, static_cast<const T*>(p.v_pages) + off, Gm::TILE_BYTES,
                       &bars[s], policy);
+        if (p.next_k != nullptr) {
+            bulk_prefetch_l2(static_cast<const T*>(p.next_k) + off, Gm::TILE_BYTES);
+            bulk_prefetch_l2(static_cast<const T*>(p.next_v) + off, Gm::TILE_BYTES);
+        }
     };
 
     const int prologue = n_work < Gm::STAGES ? n_work : Gm::STAGES;
+    if (early) {
+        tab_b = prod.b;
+        tab_base = prod.page_idx;
+        tab_val = tab_base + lane < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages +
+                                                        tab_base + lane) : -1;
+        Cursor pf = prod;
+        for (int s = 0; s < prologue; ++s) {
+            if (pf.b == tab_b && pf.page_idx < tab_base + 32) {
+                const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(pf.page_idx - tab_base));
+                if (lane == 0 && page >= 0 && page < p.n_pages) {
+                    const int64_t off = (kv_block(p, page, pf.h) * p.P + pf.slot0) * D;
+                    bulk_prefetch_l2(static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES);
+                    bulk_prefetch_l2(static_cast<const T*>(p.v_pages) + off, Gm::TILE_BYTES);
+                }
+            }
+            cursor_advance(pf, p);
+        }
+        pdl_wait_primary();
+    }
     for (int s = 0; s < prologue; ++s) {
         issue(s, s == 0 && p.inject_worker == w + 1);
         cursor_advance(prod, p);
@@ -1947,6 +1982,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.pre_stride = a.pre_stride;
     p.wait_ns = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs;
     p.inject_worker = a.inject_worker;
+    p.next_k = a.next_k;
+    p.next_v = a.next_v;
     p.blk_tok0 = a.blk_tok0;
     p.blk_ntok = a.blk_ntok;
     p.blk_gp = a.blk_gp;

@@ -148,6 +148,12 @@ __device__ __forceinline__ uint64_t l2_stream_policy() {
     return pol;
 }
 
+// Fire-and-forget fetch of `bytes` at `src` into L2 (16-byte aligned, a multiple of
+// 16 bytes); nothing waits on it and it changes no memory.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
                                               uint64_t* bar, uint64_t policy) {
