@@ -146,6 +146,7 @@ struct Geo {
 };
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
+constexpr int kEarlyTiles = 4;    // tiles a single-request worker fetches into L2 before its wait
 
 // ----------------------------------------------------------- parameters --
 
@@ -190,10 +191,6 @@ struct KParams {
     uint64_t wait_ns;           // each bounded wait gives up after this long
     int inject_worker;          // failure injection: 0 off; else worker inject_worker - 1 arms
                                 // its first stage without issuing the copy
-    // next layer's pools, or nullptr: every staged (page, head) block of this layer
-    // is also fetched into L2 from these, for the same request's next layer call
-    const void* next_k;
-    const void* next_v;
     // cluster lanes (a single request on the CUDA-core kernel, multi-head pools):
     // > 0: each lane's tiles are split over lane_workers consecutive workers (of this
     // CTA when fewer than a CTA's warps, else of the lane_workers / WARPS CTAs of one
@@ -650,9 +647,9 @@ split_decode_kernel(const KParams p) {
     // is read before the previous grid is complete, so every such write is visible.
     const bool batched = p.seq_lens != nullptr;
     // A single request's page table is written only by copies in stream order, never
-    // by a kernel, so its first entries are read (and its first tiles fetched into
-    // L2, which changes no memory) before the wait; the copies into shared memory,
-    // q and the pages' rows are read after it.
+    // by a kernel, so its first entries are read (and this worker's tiles fetched into
+    // L2, which changes no memory: a later write by the previous grid lands in L2
+    // too) before the wait; the copies into shared memory and q come after it.
     const bool early = !batched && !ROWS;
     if (!batched) pdl_launch_dependents();
     if (!early) pdl_wait_primary();
@@ -716,10 +713,6 @@ split_decode_kernel(const KParams p) {
         bulk_copy_g2s(dst, static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES, &bars[s], policy);
         bulk_copy_g2s(dst + Gm::TILE_BYTES, static_cast<const T*>(p.v_pages) + off, Gm::TILE_BYTES,
                       &bars[s], policy);
-        if (p.next_k != nullptr) {
-            bulk_prefetch_l2(static_cast<const T*>(p.next_k) + off, Gm::TILE_BYTES);
-            bulk_prefetch_l2(static_cast<const T*>(p.next_v) + off, Gm::TILE_BYTES);
-        }
     };
 
     const int prologue = n_work < Gm::STAGES ? n_work : Gm::STAGES;
@@ -728,18 +721,21 @@ split_decode_kernel(const KParams p) {
         tab_base = prod.page_idx;
         tab_val = tab_base + lane < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages +
                                                         tab_base + lane) : -1;
+        // this worker's first tiles (inside the table window) go to L2 now: a few, so
+        // that a long call's workers do not evict one another's
         Cursor pf = prod;
-        for (int s = 0; s < prologue; ++s) {
-            if (pf.b == tab_b && pf.page_idx < tab_base + 32) {
-                const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(pf.page_idx - tab_base));
-                if (lane == 0 && page >= 0 && page < p.n_pages) {
-                    const int64_t off = (kv_block(p, page, pf.h) * p.P + pf.slot0) * D;
-                    bulk_prefetch_l2(static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES);
-                    bulk_prefetch_l2(static_cast<const T*>(p.v_pages) + off, Gm::TILE_BYTES);
-                }
+        for (int k = 0; k < n_work && k < kEarlyTiles; ++k) {
+            if (pf.b != tab_b || pf.page_idx < tab_base || pf.page_idx >= tab_base + 32) break;
+            const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(pf.page_idx - tab_base));
+            if (lane == 0 && page >= 0 && page < p.n_pages) {
+                const int64_t off = (kv_block(p, page, pf.h) * p.P + pf.slot0) * D;
+                bulk_prefetch_l2(static_cast<const T*>(p.k_pages) + off, Gm::TILE_BYTES);
+                bulk_prefetch_l2(static_cast<const T*>(p.v_pages) + off, Gm::TILE_BYTES);
             }
             cursor_advance(pf, p);
         }
+        // the entries are in registers before the wait, not loaded after it
+        asm volatile("" ::"r"(tab_val));
         pdl_wait_primary();
     }
     for (int s = 0; s < prologue; ++s) {
@@ -1982,8 +1978,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.pre_stride = a.pre_stride;
     p.wait_ns = a.wait_limit_ns ? a.wait_limit_ns : kWaitLimitNs;
     p.inject_worker = a.inject_worker;
-    p.next_k = a.next_k;
-    p.next_v = a.next_v;
     p.blk_tok0 = a.blk_tok0;
     p.blk_ntok = a.blk_ntok;
     p.blk_gp = a.blk_gp;

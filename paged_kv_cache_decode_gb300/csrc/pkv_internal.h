@@ -67,8 +67,6 @@ struct DecodeArgs {
     uint64_t wait_limit_ns;  // bounded waits give up after this long (0: the default, 4 s)
     int inject_worker;       // failure injection: 0 off; else split worker inject_worker - 1
                              // arms its first stage's barrier without issuing the copy
-    const void* next_k;      // next layer's K / V pools, or nullptr: the CUDA-core kernel also
-    const void* next_v;      //   fetches every block it stages into L2 from these
 };
 
 // Bytes of a CUtensorMap (the driver's TMA descriptor).

@@ -730,20 +730,6 @@ int begin_pending(pkv_request* r, int64_t n, bool chunk, int64_t* position) {
 // Before a layer's first write for the pending positions: upload the changed
 // page-table entries and copy this layer's bytes of every shared page into its
 // private replacement.
-// A call whose K/V rows fit well inside L2 is latency-bound: its split kernel also
-// fetches the same (page, head) blocks of the next layer into L2, so that the
-// request's next layer call (one token through the layers in order) reads them
-// from L2.  Larger calls stream at the HBM rate and would only evict their own rows.
-constexpr int64_t kNextLayerPrefetchMaxBytes = int64_t(32) << 20;
-
-void next_layer_prefetch(const pkv_pool* p, int layer, int64_t rows, pkv::DecodeArgs* a) {
-    const int64_t bytes = rows * p->heads * p->head_dim * 2 * elem_bytes(p->dtype);
-    if (layer + 1 >= p->layers || bytes > kNextLayerPrefetchMaxBytes || a->tmap_k != nullptr)
-        return;
-    a->next_k = static_cast<const char*>(p->k_base) + p->layer_bytes * (size_t)(layer + 1);
-    a->next_v = static_cast<const char*>(p->v_base) + p->layer_bytes * (size_t)(layer + 1);
-}
-
 int prepare_layer_write(pkv_request* r, int layer, cudaStream_t s) {
     pkv_pool* p = r->pool;
     const int64_t n = (int64_t)r->table.size();
@@ -846,7 +832,6 @@ int pkv_append_and_attend(pkv_request* r, int layer, const float* q, const void*
     a.dev_error = p->dev_error;
     a.ev_before = p->ev_before;
     a.ev_after = p->ev_after;
-    next_layer_prefetch(p, layer, pkv::attended_len(r->position + 1, p->window), &a);
     take_wait_fault(p, &a);
     if (r->epoch == UINT32_MAX) {
         // epochs must increase: after 2^32 - 1 calls start over from zeroed counters
