@@ -76,6 +76,38 @@ def test_prefill_matches_oracle(name):
         run.close()
 
 
+def test_prefill_v_far_from_unit_scale():
+    """V rows far from unit scale: chunk rows scaled by 2^20 in some key tiles of
+    request 0 (next to unscaled rows of the same tiles), and one request whose every
+    V row is scaled by 2^-20.  Every row stays inside the bar: the weights carry
+    their relative precision whatever V's scale.  Powers of two keep the bf16
+    values exact."""
+    import synth
+    from synth.device import to_device
+    w = make_prefill("v_range", [0, 200, 0], [300, 130, 257], 2, 128, group=4, seed=44)
+    run = PrefillRun(w)
+    try:
+        v = synth.bf16_to_f32(run.v_new).copy()
+        c = run.cu
+        v[c[0]:c[0] + 100] *= 2.0 ** 20              # key tile 0 of request 0, both halves
+        v[c[0] + 200:c[0] + 230] *= 2.0 ** 20        # part of key tile 1
+        v[c[2]:c[3]] *= 2.0 ** -20                   # request 2: all of its rows tiny
+        run.v_new = synth.f32_to_bf16(v)
+        assert np.array_equal(synth.bf16_to_f32(run.v_new), v)
+        run.dev["v"] = to_device(run.v_new, w.dtype)
+        out = run.run().cpu().numpy()
+        torch.cuda.synchronize()
+        assert run.pool.check_device_status() == 0
+        for b in range(w.B):
+            got = out[c[b]:c[b + 1]]
+            assert np.isfinite(got).all(), f"request {b}: non-finite output"
+            err = _normwise(got, run.oracle_out(b))
+            print(f"request {b}: worst normwise error {err:.2e}")
+            assert err <= PREFILL_RTOL
+    finally:
+        run.close()
+
+
 def test_prefill_is_batch_invariant():
     """A request's outputs do not depend on the other requests of the batch: request 0
     alone and request 0 beside two others give the same bits."""
