@@ -119,6 +119,70 @@ def test_serial_bf16_and_page_size_32():
     _serial(3, 4, 128, BF16, 64, 200, 70, 5, abort_at=33, P=32)
 
 
+@pytest.mark.parametrize("layers,dtype,H,t0", [(1, F32, 4, 0), (2, BF16, 4, 0), (12, F32, 12, 300)])
+def test_back_to_back_tokens_without_host_copies(layers, dtype, H, t0):
+    """Tokens issued back to back through the C ABI with every input already on the
+    device, so each call's kernel is a dependent launch of the previous call's (no
+    host copy between them breaks the chain): with one layer every kernel attends
+    over the row the kernel just before it appended.  The page table, the lengths,
+    every output and every appended byte equal the oracle model's.  t0 tokens go in
+    first through the binding; the next 40 are checked."""
+    import ctypes
+    D, P, T, seed = 64, 16, 40, 23
+    pool = pkv.Pool(layers, 128, H, D, P, dtype_name(dtype), 512, seed)
+    req = pool.request()
+    opool = OraclePool(layers, 128, H, D, P, dtype, max_context=512, seed=seed)
+    oreq = opool.request()
+    for t in range(t0):
+        pos = req.begin_token()
+        assert pos == oreq.begin_token()
+        for layer in range(layers):
+            q, k, v = _lane_tensors(seed, layer, H, pos, D, dtype)
+            req.append_and_attend(layer, to_device(q), to_device(k), to_device(v))
+            oreq.append_and_attend(layer, q, k, v, compute=False)
+        req.commit_token()
+        oreq.commit_token()
+    host = [[_lane_tensors(seed, layer, H, t0 + i, D, dtype) for layer in range(layers)]
+            for i in range(T)]
+    qd = to_device(np.stack([[x[0] for x in row] for row in host]))   # [T][layers][H][D]
+    kd = to_device(np.stack([[x[1] for x in row] for row in host]))
+    vd = to_device(np.stack([[x[2] for x in row] for row in host]))
+    out = torch.full((T, layers, H, D), float("nan"), device="cuda")
+    torch.cuda.synchronize()
+    lib, h = pkv.lib, req.handle
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    pos = ctypes.c_int64()
+
+    def at(x, i, layer):
+        return ctypes.c_void_p(x[i, layer].data_ptr())
+
+    for i in range(T):
+        assert lib.pkv_begin_token(h, ctypes.byref(pos)) == pkv.PKV_OK
+        for layer in range(layers):
+            assert lib.pkv_append_and_attend(h, layer, at(qd, i, layer), at(kd, i, layer),
+                                             at(vd, i, layer), at(out, i, layer), stream) == pkv.PKV_OK
+        assert lib.pkv_commit_token(h) == pkv.PKV_OK
+    torch.cuda.synchronize()
+    assert pool.check_device_status() == 0
+    got = out.cpu().numpy()
+    for i in range(T):
+        assert oreq.begin_token() == t0 + i
+        for layer in range(layers):
+            q, k, v = host[i][layer]
+            ref = oreq.append_and_attend(layer, q, k, v)
+            check_close(got[i, layer], ref, dtype, f"token {t0 + i} layer {layer}")
+        oreq.commit_token()
+    assert req.length == oreq.length == t0 + T
+    assert req.page_table() == oreq.table
+    used = torch.tensor(req.page_table(), dtype=torch.int64)
+    for layer in range(layers):
+        kp, vp = pool.kv_pages(layer)
+        assert _host(kp[used.cuda()], dtype).tobytes() == opool.k[layer][used.numpy()].tobytes()
+        assert _host(vp[used.cuda()], dtype).tobytes() == opool.v[layer][used.numpy()].tobytes()
+    req.close()
+    pool.close()
+
+
 # ------------------------------------------------------------------ batched --
 
 def _batched_check(w, requests=None, heads=None, **kw):
