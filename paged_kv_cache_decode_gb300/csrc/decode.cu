@@ -616,7 +616,13 @@ split_decode_kernel(const KParams p) {
     float* lane_part = reinterpret_cast<float*>(smem + Gm::CLU_OFF + 64);        // [slots][D+2]
     if constexpr (Gm::CLUSTER_LANES) {
         if (p.lane_workers > 0) {
-            if (threadIdx.x < 8) mbar_init(&lane_bar[threadIdx.x], 32u * (uint32_t)p.lane_workers);
+            // inside a CTA: one barrier per lane, every lane of its kw workers arrives.
+            // Across a cluster: barrier 0 gathers this CTA's WARPS workers, barrier 1 (of
+            // the lead CTA) the cluster's kw / WARPS CTA partials
+            const uint32_t kw = (uint32_t)p.lane_workers;
+            const uint32_t cnt = kw <= (uint32_t)Gm::WARPS ? 32u * kw
+                                 : threadIdx.x == 1 ? 32u * (kw / Gm::WARPS) : 32u * Gm::WARPS;
+            if (threadIdx.x < 8) mbar_init(&lane_bar[threadIdx.x], cnt);
             if (p.lane_workers > Gm::WARPS) {     // lanes span the CTAs of a cluster
                 if (threadIdx.x == 0) fence_mbar_init();
                 cluster_sync_all();
@@ -940,31 +946,21 @@ split_decode_kernel(const KParams p) {
                     }
                 }
             } else if (Gm::CLUSTER_LANES && G == 1 && p.lane_workers > 0) {
-                // cluster lanes: worker j of the lane's kw writes its partial into slot
-                // j of the lead CTA (cluster rank 0; this CTA when kw < WARPS) and
-                // arrives on the lane's barrier there; worker 0 waits and merges
+                // cluster lanes: the lane's kw workers merge their partials (max, sum, o)
+                // in shared memory.  Inside one CTA (kw <= WARPS) worker j writes slot warp
+                // and arrives on the lane's barrier; worker 0 waits and merges.  Across a
+                // cluster of kw / WARPS CTAs, in two levels: every CTA's warps write their
+                // slots and arrive on the CTA's barrier 0; its warp 0 merges those WARPS
+                // partials and writes the result into slot WARPS + rank of the lead CTA
+                // (cluster rank 0), arriving on the lead's barrier 1 (release, cluster
+                // scope); the lead's warp 0 waits (acquire) and merges the CTA partials.
+                constexpr int DPL = Gm::DPL;
                 const int kw = p.lane_workers;
-                const bool clu = kw > Gm::WARPS;            // else the lane is inside this CTA
+                const bool clu = kw > Gm::WARPS;
                 const int j = (int)(w % kw);
-                const int slot = clu ? j : warp;
                 const int bidx = clu ? 0 : warp / kw;
-                if (clu) {
-                    const uint32_t part = cluster_map(smem_u32(lane_part + slot * (D + 2)), 0);
-                    if (lane < Gm::TPR) {
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            st_cluster_f32(part + 4u * (uint32_t)(2 + col + 2 * v), o[0][v].x);
-                            st_cluster_f32(part + 4u * (uint32_t)(3 + col + 2 * v), o[0][v].y);
-                        }
-                    }
-                    if (lane == 0) {
-                        st_cluster_f32(part, m[0]);
-                        st_cluster_f32(part + 4u, lt[0]);
-                    }
-                    // each lane releases its own stores (cluster scope)
-                    mbar_arrive_cluster(cluster_map(smem_u32(&lane_bar[bidx]), 0));
-                } else {
-                    float* part = lane_part + slot * (D + 2);
+                {
+                    float* part = lane_part + warp * (D + 2);
                     if (lane < Gm::TPR) {
 #pragma unroll
                         for (int v = 0; v < NV; ++v) {
@@ -978,38 +974,74 @@ split_decode_kernel(const KParams p) {
                     }
                     mbar_arrive(&lane_bar[bidx]);   // release at CTA scope
                 }
-                if (j == 0) {
-                    const bool arrived_all = clu ? mbar_wait_cluster_bounded(&lane_bar[bidx], 0, p.wait_ns)
-                                                 : mbar_wait_bounded(&lane_bar[bidx], 0, p.wait_ns);
-                    if (!arrived_all) {
+                const bool feat = lane * DPL < D;
+                float M = -INFINITY, L = 0.f, acc[DPL];
+                // n partials from `base` -> their common maximum M, sum L and this
+                // lane's features of the weighted output
+                auto merge = [&](const float* base, int n) {
+                    M = -INFINITY;
+                    for (int s2 = lane; s2 < n; s2 += 32) M = fmaxf(M, base[s2 * (D + 2)]);
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                    L = 0.f;
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+                    for (int s2 = 0; s2 < n; ++s2) {
+                        const float* ps = base + s2 * (D + 2);
+                        const float ls = ps[1];
+                        const float ws = ls > 0.f ? exp2f(ps[0] - M) : 0.f;
+                        L = fmaf(ls, ws, L);
+                        if (feat) {
+#pragma unroll
+                            for (int i = 0; i < DPL; ++i) acc[i] = fmaf(ws, ps[2 + lane * DPL + i], acc[i]);
+                        }
+                    }
+                };
+                auto write_out = [&]() {
+                    if (feat) {
+                        const float inv = 1.f / L;
+                        float* op = p.out + lane_id * D + lane * DPL;
+#pragma unroll
+                        for (int i = 0; i < DPL; ++i) op[i] = acc[i] * inv;
+                    }
+                };
+                if (!clu) {
+                    if (j == 0) {
+                        if (!mbar_wait_bounded(&lane_bar[bidx], 0, p.wait_ns)) {
+                            if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+                        } else {
+                            merge(lane_part + warp * (D + 2), kw);
+                            write_out();
+                        }
+                    }
+                } else if (warp == 0) {
+                    if (!mbar_wait_bounded(&lane_bar[0], 0, p.wait_ns)) {
                         if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
                     } else {
-                        constexpr int DPL = Gm::DPL;
-                        const float* base = lane_part + (slot - j) * (D + 2);
-                        float M = -INFINITY;
-                        for (int s2 = lane; s2 < kw; s2 += 32) M = fmaxf(M, base[s2 * (D + 2)]);
-#pragma unroll
-                        for (int off = 16; off >= 1; off >>= 1)
-                            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-                        float L = 0.f, acc[DPL];
-#pragma unroll
-                        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-                        const bool feat = lane * DPL < D;
-                        for (int s2 = 0; s2 < kw; ++s2) {
-                            const float* ps = base + s2 * (D + 2);
-                            const float ls = ps[1];
-                            const float ws = ls > 0.f ? exp2f(ps[0] - M) : 0.f;
-                            L = fmaf(ls, ws, L);
-                            if (feat) {
-#pragma unroll
-                                for (int i = 0; i < DPL; ++i) acc[i] = fmaf(ws, ps[2 + lane * DPL + i], acc[i]);
-                            }
-                        }
+                        merge(lane_part, Gm::WARPS);
+                        const int ctas = kw / Gm::WARPS;
+                        const uint32_t rank = (uint32_t)(blockIdx.x % (unsigned)ctas);
+                        const uint32_t dst =
+                            cluster_map(smem_u32(lane_part + (Gm::WARPS + rank) * (D + 2)), 0);
                         if (feat) {
-                            const float inv = 1.f / L;
-                            float* op = p.out + lane_id * D + lane * DPL;
 #pragma unroll
-                            for (int i = 0; i < DPL; ++i) op[i] = acc[i] * inv;
+                            for (int i = 0; i < DPL; ++i)
+                                st_cluster_f32(dst + 4u * (uint32_t)(2 + lane * DPL + i), acc[i]);
+                        }
+                        if (lane == 0) {
+                            st_cluster_f32(dst, M);
+                            st_cluster_f32(dst + 4u, L);
+                        }
+                        // each lane releases its own stores (cluster scope)
+                        mbar_arrive_cluster(cluster_map(smem_u32(&lane_bar[1]), 0));
+                        if (rank == 0) {
+                            if (!mbar_wait_cluster_bounded(&lane_bar[1], 0, p.wait_ns)) {
+                                if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+                            } else {
+                                merge(lane_part + Gm::WARPS * (D + 2), ctas);
+                                write_out();
+                            }
                         }
                     }
                 }
