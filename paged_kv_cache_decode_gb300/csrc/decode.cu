@@ -1738,9 +1738,10 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G) {
 }
 
 #ifndef PKV_LANE_MIN_TILES
-// cluster lanes: tiles per worker at least (their merge through shared memory is
-// cheap, so a worker's tiles can all be in flight in its ring at once)
-#define PKV_LANE_MIN_TILES 3
+// cluster lanes: tiles per worker at least (their two-level merge through shared
+// memory is cheap, so a worker's tiles can all be in flight in its ring at once,
+// and more workers spread a lane's copies over more SMs)
+#define PKV_LANE_MIN_TILES 2
 #endif
 #ifndef PKV_MIN_TILES_PER_WORKER
 #define PKV_MIN_TILES_PER_WORKER 4   // below this much work a worker's fixed costs dominate
