@@ -1738,10 +1738,16 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G) {
 }
 
 #ifndef PKV_LANE_MIN_TILES
-// cluster lanes: tiles per worker at least (their two-level merge through shared
-// memory is cheap, so a worker's tiles can all be in flight in its ring at once,
-// and more workers spread a lane's copies over more SMs)
-#define PKV_LANE_MIN_TILES 2
+// cluster lanes: tiles per worker at least.  Their two-level merge through shared
+// memory is cheap, so a lane takes as many workers as fit (one tile each at most):
+// fewer tiles per worker means fewer copy round trips, and more workers spread a
+// lane's copies over more SMs
+#define PKV_LANE_MIN_TILES 1
+#endif
+#ifndef PKV_LANE_MAX_TILES
+// ... and at most this many: a longer lane streams at the HBM rate, which the
+// global merge's grid over every SM serves better than a lane's cluster of 8 CTAs
+#define PKV_LANE_MAX_TILES 4
 #endif
 #ifndef PKV_MIN_TILES_PER_WORKER
 #define PKV_MIN_TILES_PER_WORKER 4   // below this much work a worker's fixed costs dominate
@@ -1805,14 +1811,6 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
             const int64_t t = p.single_t;
             const int64_t ws = (p.window > 0 && t > p.window) ? t - p.window : 0;
             const int64_t n = (t + kTile - 1) / kTile - ws / kTile;    // tiles per lane
-            int64_t k0 = (n + PKV_LANE_MIN_TILES - 1) / PKV_LANE_MIN_TILES;
-            if (k0 < 1) k0 = 1;
-            int64_t k = 1;
-            if (k0 <= Gm::WARPS) {
-                while (k < k0) k <<= 1;
-            } else {
-                k = (k0 + Gm::WARPS - 1) / Gm::WARPS * Gm::WARPS;
-            }
             static int sms = 0;
             if (sms == 0) {
                 int dev = 0;
@@ -1820,8 +1818,20 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
                     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                     sms = -1;
             }
-            const int64_t ctas = ((int64_t)p.H * k + Gm::WARPS - 1) / Gm::WARPS;
-            if (k <= 8 * Gm::WARPS && k <= n && sms > 0 && ctas <= sms) kw = (int)k;
+            // workers per lane at most: PKV_LANE_MIN_TILES tiles each, a cluster of 8
+            // CTAs, and every lane's CTAs resident at once (one CTA per SM)
+            int64_t kmax = (n + PKV_LANE_MIN_TILES - 1) / PKV_LANE_MIN_TILES;
+            if (kmax > 8 * Gm::WARPS) kmax = 8 * Gm::WARPS;
+            if (sms > 0 && kmax > (int64_t)sms * Gm::WARPS / p.H) kmax = (int64_t)sms * Gm::WARPS / p.H;
+            // the largest count allowed: a power of two up to WARPS, then multiples of it
+            int64_t k = 0;
+            if (kmax >= Gm::WARPS) {
+                k = kmax / Gm::WARPS * Gm::WARPS;
+            } else if (kmax >= 1) {
+                k = 1;
+                while (k * 2 <= kmax) k <<= 1;
+            }
+            if (sms > 0 && k >= 1 && k <= n && (n + k - 1) / k <= PKV_LANE_MAX_TILES) kw = (int)k;
         }
     }
     if (kw > 0) {
