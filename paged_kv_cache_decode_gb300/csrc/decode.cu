@@ -330,6 +330,33 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const KParams p) {
         }
         p.worker_req[w] = lo;
     }
+    // Launched as a dependent of the shared-prefix kernel (which needs no plan), the
+    // plan runs beside it but completes only after it: whatever waits for the plan
+    // then also sees the prefix kernel's partials.  After a plain launch this returns
+    // at once.
+    pdl_wait_primary();
+}
+
+// The plan kernel, then (shared-prefix calls) the prefix kernel.  With a prefix
+// kernel the order is reversed: the prefix kernel first, and the plan as its
+// dependent, which runs beside it.
+static cudaError_t launch_plan(const DecodeArgs& a, const KParams& p, cudaStream_t stream) {
+    if (a.before_split == nullptr) {
+        plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaError_t e = a.before_split(a.before_split_ctx, stream);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_kernel, p);
 }
 
 // ---------------------------------------------------------- split kernel --
@@ -1794,13 +1821,16 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
     using Gm = Geo<T, D, G>;
     cudaError_t e = prepare_split<T, D, G>();
     if (e != cudaSuccess) return e;
-    if (p.epoch == 0) {   // a single request with epoch counters needs no plan
-        plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the plan (a single request with epoch counters needs none) and, for a
+    // shared-prefix call, the prefix kernel; the timing events bracket the attention:
+    // the prefix kernel, if any, and the split kernel
+    if (a.before_split == nullptr) {
+        if (p.epoch == 0 && (e = launch_plan(a, p, stream)) != cudaSuccess) return e;
+        if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+    } else {
+        if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+        if ((e = launch_plan(a, p, stream)) != cudaSuccess) return e;
     }
-    // the timing events bracket the attention: the prefix kernel, if any, and the split kernel
-    if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
-    if (a.before_split && (e = a.before_split(a.before_split_ctx, stream)) != cudaSuccess) return e;
     // cluster lanes for a single request on a multi-head pool: kw workers per lane,
     // a power of two below a CTA's warps (lanes inside one CTA) or a multiple of them
     // (one cluster of kw / WARPS CTAs per lane); every lane has the same tiles
@@ -1899,13 +1929,16 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
     using M = MmaGeo<T, D>;
     cudaError_t e = prepare_mma<T, D, G>();
     if (e != cudaSuccess) return e;
-    if (p.epoch == 0) {
-        plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the plan (a single request with epoch counters needs none) and, for a
+    // shared-prefix call, the prefix kernel; the timing events bracket the attention:
+    // the prefix kernel, if any, and the split kernel
+    if (a.before_split == nullptr) {
+        if (p.epoch == 0 && (e = launch_plan(a, p, stream)) != cudaSuccess) return e;
+        if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+    } else {
+        if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
+        if ((e = launch_plan(a, p, stream)) != cudaSuccess) return e;
     }
-    // the timing events bracket the attention: the prefix kernel, if any, and the split kernel
-    if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
-    if (a.before_split && (e = a.before_split(a.before_split_ctx, stream)) != cudaSuccess) return e;
     CUtensorMap tmk, tmv;
     memcpy(&tmk, a.tmap_k, sizeof tmk);
     memcpy(&tmv, a.tmap_v, sizeof tmv);
