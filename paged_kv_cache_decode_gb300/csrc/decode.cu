@@ -1250,9 +1250,106 @@ struct MmaGeo {
     static_assert(CTA_SMEM <= 227 * 1024, "CTA does not fit an SM");
 };
 
+// Cluster lanes of the tensor-core kernel (a single request, bf16): after the rings,
+// 8 lane mbarriers and a partial slot -- G rows of (max, sum, o[D]) -- for each warp
+// and for each of up to 8 CTAs of a cluster.  Offsets from the 1024-aligned base.
+template <typename T, int D, int G>
+struct MmaClu {
+    using M = MmaGeo<T, D>;
+    static constexpr int OFF = (M::WARPS * (M::WARP_SMEM + M::STAGES * 12) + 15) / 16 * 16;
+    static constexpr int SLOT = G * (D + 2);               // floats of one partial
+    static constexpr int BYTES = 64 + (M::WARPS + 8) * SLOT * 4;
+    static constexpr int SMEM = 1024 + OFF + BYTES;         // dynamic shared memory with slots
+    static constexpr bool ON = sizeof(T) == 2 && G <= 8 && (M::WARPS == 4 || M::WARPS == 8) &&
+                               SMEM <= 227 * 1024;
+};
+
 // Byte offset of 16-byte chunk c of row r in a swizzled tile.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
     return (uint32_t)((c >> 3) * (kTile * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Cluster lanes of the tensor-core kernel, after a worker has written its partial
+// into its slot and arrived: the lane's first worker (inside one CTA), or warp 0 of
+// every CTA of the lane's cluster and then the lead's, wait, merge and write `out`.
+// Kept out of line: the split kernel's registers stay those of its streaming loop.
+template <typename T, int D, int G>
+__device__ __noinline__ void mma_lane_merge(const KParams& p, float* lane_part, uint64_t* lane_bar,
+                                            int64_t lane_id, int64_t w, int warp, int lane) {
+    using M = MmaGeo<T, D>;
+    using C = MmaClu<T, D, G>;
+    const int g = lane >> 2, t = lane & 3;
+    const bool q_ok = g < G;
+    const int kw = p.lane_workers;
+    const bool clu = kw > M::WARPS;
+    const int j = (int)(w % kw);
+    const int bidx = clu ? 0 : warp / kw;
+    float Mx = -INFINITY, Lx = 0.f;
+    float2 acc[M::NB];
+    // n partials from `base` -> row g's common maximum, sum and weighted output
+    auto merge = [&](const float* base, int n) {
+        const float* rb = base + g * (D + 2);
+        Mx = -INFINITY;
+        for (int s2 = 0; s2 < n; ++s2) Mx = fmaxf(Mx, rb[s2 * C::SLOT]);
+        Lx = 0.f;
+#pragma unroll
+        for (int nb = 0; nb < M::NB; ++nb) acc[nb] = make_float2(0.f, 0.f);
+        for (int s2 = 0; s2 < n; ++s2) {
+            const float* ps = rb + s2 * C::SLOT;
+            const float ls = ps[1];
+            const float ws = ls > 0.f ? exp2f(ps[0] - Mx) : 0.f;
+            Lx = fmaf(ls, ws, Lx);
+#pragma unroll
+            for (int nb = 0; nb < M::NB; ++nb) {
+                const float2 x = *reinterpret_cast<const float2*>(ps + 2 + nb * 8 + 2 * t);
+                acc[nb] = make_float2(fmaf(ws, x.x, acc[nb].x), fmaf(ws, x.y, acc[nb].y));
+            }
+        }
+    };
+    auto write_out = [&]() {
+        const float inv = 1.f / Lx;
+        float* op = p.out + (lane_id * G + g) * D + 2 * t;
+#pragma unroll
+        for (int nb = 0; nb < M::NB; ++nb)
+            *reinterpret_cast<float2*>(op + nb * 8) =
+                make_float2(acc[nb].x * inv, acc[nb].y * inv);
+    };
+    if (!clu) {
+        if (j == 0) {
+            if (!mbar_wait_bounded(&lane_bar[bidx], 0, p.wait_ns)) {
+                if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+            } else if (q_ok) {
+                merge(lane_part + warp * C::SLOT, kw);
+                write_out();
+            }
+        }
+    } else if (warp == 0) {
+        if (!mbar_wait_bounded(&lane_bar[0], 0, p.wait_ns)) {
+            if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+        } else {
+            const int ctas = kw / M::WARPS;
+            const uint32_t rank = (uint32_t)(blockIdx.x % (unsigned)ctas);
+            if (q_ok) {
+                merge(lane_part, M::WARPS);
+                const uint32_t dst = cluster_map(
+                    smem_u32(lane_part + (M::WARPS + rank) * C::SLOT + g * (D + 2)), 0);
+#pragma unroll
+                for (int nb = 0; nb < M::NB; ++nb)
+                    st_cluster_v2f32(dst + 4u * (uint32_t)(2 + nb * 8 + 2 * t), acc[nb]);
+                if (t == 0) st_cluster_v2f32(dst, make_float2(Mx, Lx));
+            }
+            // each lane releases its own stores (cluster scope)
+            mbar_arrive_cluster(cluster_map(smem_u32(&lane_bar[1]), 0));
+            if (rank == 0) {
+                if (!mbar_wait_cluster_bounded(&lane_bar[1], 0, p.wait_ns)) {
+                    if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+                } else if (q_ok) {
+                    merge(lane_part + M::WARPS * C::SLOT, ctas);
+                    write_out();
+                }
+            }
+        }
+    }
 }
 
 template <typename T, int D, int G, bool ROWS = false>
@@ -1281,6 +1378,27 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t w = (int64_t)blockIdx.x * M::WARPS + warp;
+    // cluster lanes: every CTA's lane barriers are initialised before any worker of
+    // the cluster can arrive on them (every thread takes part, so before any return)
+    using C = MmaClu<T, D, G>;
+    uint64_t* lane_bar = reinterpret_cast<uint64_t*>(smem + C::OFF);        // [8]
+    float* lane_part = reinterpret_cast<float*>(smem + C::OFF + 64);        // [slots][G][D+2]
+    if constexpr (C::ON && !ROWS) {
+        if (p.lane_workers > 0) {
+            // as in the CUDA-core kernel: inside a CTA one barrier per lane; across a
+            // cluster barrier 0 gathers this CTA's warps, barrier 1 (lead) the CTAs
+            const uint32_t kw = (uint32_t)p.lane_workers;
+            const uint32_t cnt = kw <= (uint32_t)M::WARPS ? 32u * kw
+                                 : threadIdx.x == 1 ? 32u * (kw / M::WARPS) : 32u * M::WARPS;
+            if (threadIdx.x < 8) mbar_init(&lane_bar[threadIdx.x], cnt);
+            if (p.lane_workers > M::WARPS) {
+                if (threadIdx.x == 0) fence_mbar_init();
+                cluster_sync_all();
+            } else {
+                __syncthreads();
+            }
+        }
+    }
     if (w >= p.W) return;
 
     unsigned char* ring = smem + warp * M::WARP_SMEM;
@@ -1295,9 +1413,12 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     __syncwarp();
     const uint64_t policy = l2_stream_policy();
 
-    const bool batched = p.seq_lens != nullptr;   // as in the CUDA-core kernel
+    // as in the CUDA-core kernel: a single request reads its page-table entries (and
+    // fetches its first tiles into L2) before the wait
+    const bool batched = p.seq_lens != nullptr;
+    const bool early = !batched && !ROWS;
     if (!batched) pdl_launch_dependents();
-    pdl_wait_primary();
+    if (!early) pdl_wait_primary();
 
     // this worker's tiles: range w >> kv_shift, [begin, end) of the flattened (request,
     // KV head, tile) sequence, for sub-lane w & (2^kv_shift - 1) of every KV head in it
@@ -1307,7 +1428,10 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     const int64_t begin = ((w >> p.kv_shift) * T_all) / R;
     const int64_t end = (((w >> p.kv_shift) + 1) * T_all) / R;
     const int n_work = (int)(end - begin);
-    if (n_work <= 0) return;
+    if (n_work <= 0) {
+        if (early) pdl_wait_primary();
+        return;
+    }
 
     Cursor cur;
     {
@@ -1361,6 +1485,25 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
     };
 
     const int prologue = n_work < M::STAGES ? n_work : M::STAGES;
+    if (early) {
+        tab_b = prod.b;
+        tab_base = prod.page_idx;
+        tab_val = tab_base + lane < p.max_pages ? __ldg(p.tables + (int64_t)tab_b * p.max_pages +
+                                                        tab_base + lane) : -1;
+        Cursor pf = prod;
+        for (int k = 0; k < n_work && k < kEarlyTiles; ++k) {
+            if (pf.b != tab_b || pf.page_idx < tab_base || pf.page_idx >= tab_base + 32) break;
+            const int32_t page = __shfl_sync(0xffffffffu, tab_val, (int)(pf.page_idx - tab_base));
+            if (lane == 0 && page >= 0 && page < p.n_pages) {
+                const int64_t off = (kv_block(p, page, pf.h) * p.P + pf.slot0) * D;
+                bulk_prefetch_l2(static_cast<const T*>(p.k_pages) + off, M::TILE_BYTES);
+                bulk_prefetch_l2(static_cast<const T*>(p.v_pages) + off, M::TILE_BYTES);
+            }
+            cursor_advance(pf, p);
+        }
+        asm volatile("" ::"r"(tab_val));   // the entries are in registers before the wait
+        pdl_wait_primary();
+    }
     for (int s = 0; s < prologue; ++s) {
         issue(s, s == 0 && p.inject_worker == w + 1);
         cursor_advance(prod, p);
@@ -1683,6 +1826,26 @@ split_decode_mma_kernel(const __grid_constant__ KParams p, const __grid_constant
                         }
                     }
                 }
+            } else if (C::ON && !ROWS && p.lane_workers > 0) {
+                // cluster lanes, as in the CUDA-core kernel: the lane's kw workers merge
+                // their partials (G rows each, in the accumulator layout: this lane holds
+                // row g, features 8nb + 2t and + 1) through shared memory, inside one CTA
+                // or in two levels across a cluster of kw / WARPS CTAs
+                const int kw = p.lane_workers;
+                const int bidx = kw > M::WARPS ? 0 : warp / kw;
+                if (q_ok) {
+                    float* r = lane_part + warp * C::SLOT + g * (D + 2);
+#pragma unroll
+                    for (int nb = 0; nb < M::NB; ++nb)
+                        *reinterpret_cast<float2*>(r + 2 + nb * 8 + 2 * t) = o_pair(nb, 0);
+                    if (t == 0) {
+                        r[0] = m[0];
+                        r[1] = lt[0];
+                    }
+                }
+                mbar_arrive(&lane_bar[bidx]);   // release at CTA scope
+                mma_lane_merge<T, D, G>(p, lane_part, lane_bar, lane_id, w, warp, lane);
+                __syncwarp();
             } else {
                 const int64_t slot =      // partial of KV lane K from range r, this sub-lane
                     ((((int64_t)cur.b * Hk + cur.h) + (w >> p.kv_shift)) << p.kv_shift) | sub;
@@ -1776,6 +1939,41 @@ WorkspaceLayout workspace_layout(int B, int H, int D, int workers, int G) {
 // global merge's grid over every SM serves better than a lane's cluster of 8 CTAs
 #define PKV_LANE_MAX_TILES 4
 #endif
+
+// Cluster lanes for a single request (either split kernel): kw workers per lane, a
+// power of two below a CTA's warps (lanes inside one CTA) or a multiple of them (one
+// cluster of kw / warps CTAs per lane), the largest that fits; every lane has the
+// same tiles.  0: this call keeps the global merge.
+static int lane_worker_count(const KParams& p, int warps) {
+    if (p.seq_lens != nullptr || p.kv_shift != 0 || p.table_rows != nullptr ||
+        p.pre_ml != nullptr || p.inject_worker != 0)
+        return 0;
+    const int64_t t = p.single_t;
+    const int64_t ws = (p.window > 0 && t > p.window) ? t - p.window : 0;
+    const int64_t n = (t + kTile - 1) / kTile - ws / kTile;    // tiles per lane
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = -1;
+    }
+    if (sms <= 0) return 0;
+    // workers per lane at most: PKV_LANE_MIN_TILES tiles each, a cluster of 8 CTAs,
+    // and every lane's CTAs resident at once (one CTA per SM)
+    int64_t kmax = (n + PKV_LANE_MIN_TILES - 1) / PKV_LANE_MIN_TILES;
+    if (kmax > 8 * warps) kmax = 8 * warps;
+    if (kmax > (int64_t)sms * warps / p.H) kmax = (int64_t)sms * warps / p.H;
+    // the largest count allowed: a power of two up to warps, then multiples of it
+    int64_t k = 0;
+    if (kmax >= warps) {
+        k = kmax / warps * warps;
+    } else if (kmax >= 1) {
+        k = 1;
+        while (k * 2 <= kmax) k <<= 1;
+    }
+    return (k >= 1 && k <= n && (n + k - 1) / k <= PKV_LANE_MAX_TILES) ? (int)k : 0;
+}
 #ifndef PKV_MIN_TILES_PER_WORKER
 #define PKV_MIN_TILES_PER_WORKER 4   // below this much work a worker's fixed costs dominate
 #endif
@@ -1831,39 +2029,9 @@ static cudaError_t launch_t(const DecodeArgs& a, KParams& p, cudaStream_t stream
         if (a.ev_before && (e = cudaEventRecord(a.ev_before, stream)) != cudaSuccess) return e;
         if ((e = launch_plan(a, p, stream)) != cudaSuccess) return e;
     }
-    // cluster lanes for a single request on a multi-head pool: kw workers per lane,
-    // a power of two below a CTA's warps (lanes inside one CTA) or a multiple of them
-    // (one cluster of kw / WARPS CTAs per lane); every lane has the same tiles
+    // cluster lanes for a single request on a multi-head pool
     int kw = 0;
-    if constexpr (Gm::CLUSTER_LANES && G == 1) {
-        if (p.seq_lens == nullptr && p.kv_shift == 0 && p.table_rows == nullptr &&
-            p.pre_ml == nullptr && p.inject_worker == 0) {
-            const int64_t t = p.single_t;
-            const int64_t ws = (p.window > 0 && t > p.window) ? t - p.window : 0;
-            const int64_t n = (t + kTile - 1) / kTile - ws / kTile;    // tiles per lane
-            static int sms = 0;
-            if (sms == 0) {
-                int dev = 0;
-                if (cudaGetDevice(&dev) != cudaSuccess ||
-                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-                    sms = -1;
-            }
-            // workers per lane at most: PKV_LANE_MIN_TILES tiles each, a cluster of 8
-            // CTAs, and every lane's CTAs resident at once (one CTA per SM)
-            int64_t kmax = (n + PKV_LANE_MIN_TILES - 1) / PKV_LANE_MIN_TILES;
-            if (kmax > 8 * Gm::WARPS) kmax = 8 * Gm::WARPS;
-            if (sms > 0 && kmax > (int64_t)sms * Gm::WARPS / p.H) kmax = (int64_t)sms * Gm::WARPS / p.H;
-            // the largest count allowed: a power of two up to WARPS, then multiples of it
-            int64_t k = 0;
-            if (kmax >= Gm::WARPS) {
-                k = kmax / Gm::WARPS * Gm::WARPS;
-            } else if (kmax >= 1) {
-                k = 1;
-                while (k * 2 <= kmax) k <<= 1;
-            }
-            if (sms > 0 && k >= 1 && k <= n && (n + k - 1) / k <= PKV_LANE_MAX_TILES) kw = (int)k;
-        }
-    }
+    if constexpr (Gm::CLUSTER_LANES && G == 1) kw = lane_worker_count(p, Gm::WARPS);
     if (kw > 0) {
         p.lane_workers = kw;
         p.W = p.H * kw;
@@ -1903,9 +2071,11 @@ template <typename T, int D, int G>
 static cudaError_t prepare_mma() {
     static bool done = false;   // per instantiation
     if (done) return cudaSuccess;
+    // with cluster lanes the partial slots follow the rings
+    constexpr int smem = MmaClu<T, D, G>::ON && MmaClu<T, D, G>::SMEM > MmaGeo<T, D>::CTA_SMEM
+                             ? MmaClu<T, D, G>::SMEM : MmaGeo<T, D>::CTA_SMEM;
     cudaError_t e = cudaFuncSetAttribute(split_decode_mma_kernel<T, D, G, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MmaGeo<T, D>::CTA_SMEM);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess && sizeof(T) == 4)   // table rows: fp32 only (the decode-lane prefill)
         e = cudaFuncSetAttribute(split_decode_mma_kernel<T, D, G, sizeof(T) == 4>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, MmaGeo<T, D>::CTA_SMEM);
@@ -1942,16 +2112,31 @@ static cudaError_t launch_mma(const DecodeArgs& a, KParams& p, cudaStream_t stre
     CUtensorMap tmk, tmv;
     memcpy(&tmk, a.tmap_k, sizeof tmk);
     memcpy(&tmv, a.tmap_v, sizeof tmv);
+    // cluster lanes for a single request (bf16, up to 8 query heads per KV head)
+    using C = MmaClu<T, D, G>;
+    int kw = 0;
+    if constexpr (C::ON) kw = lane_worker_count(p, M::WARPS);
+    if (kw > 0) {
+        p.lane_workers = kw;
+        p.W = p.H * kw;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)((p.W + M::WARPS - 1) / M::WARPS));
     cfg.blockDim = dim3(M::WARPS * 32);
-    cfg.dynamicSmemBytes = M::CTA_SMEM;
+    cfg.dynamicSmemBytes = kw > 0 ? C::SMEM : M::CTA_SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (kw > M::WARPS) {   // a lane spans the CTAs of one cluster
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)(kw / M::WARPS);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     if (p.table_rows != nullptr && sizeof(T) != 4) return cudaErrorInvalidValue;
     e = p.table_rows != nullptr
             ? cudaLaunchKernelEx(&cfg, split_decode_mma_kernel<T, D, G, sizeof(T) == 4>, p, tmk, tmv)

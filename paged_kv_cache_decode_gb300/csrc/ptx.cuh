@@ -47,6 +47,11 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_v2f32(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+                 : "memory");
+}
+
 // Arrive (release at cluster scope: this thread's earlier shared::cluster stores
 // first) on an mbarrier that may sit in another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
