@@ -153,10 +153,12 @@ def serial_config(w, world: int) -> dict:
     t = int(w.seq_lens[0])
     alg = token_bytes(w, t)
     layer_alg = alg // w.layers
-    return {"workload": (f"single request: {w.layers} layers, H={w.H}, d_h={w.D}, "
+    heads = f"H={w.H}" if w.group == 1 else f"{w.H} KV heads x {w.group} query heads"
+    st = "bf16" if w.elem_bytes == 2 else "fp32"
+    return {"workload": (f"single request: {w.layers} layers, {heads}, d_h={w.D}, {st}, "
                          f"retained length t={t}, pool of {w.pool_pages} shuffled pages; "
                          "a step is one token through every layer (transactional API)"),
-            "name": w.name, "layers": w.layers, "heads": w.H, "head_dim": w.D,
+            "name": w.name, "layers": w.layers, "heads": w.H, "query_heads": w.HQ, "head_dim": w.D,
             "page_size": w.P, "seq_len": t, "alg_bytes_per_step": alg,
             "calls": "timed token through the C ABI (pointers taken once); e2e the same "
                      "calls, with the token's inputs of every layer copied in from pinned host "
@@ -515,7 +517,7 @@ def run_gpu(args, compact=False):
 def token_bytes(w, t: int) -> int:
     """Algorithmic bytes of one token at retained length t through every layer."""
     es = w.elem_bytes
-    per_layer = ((t - 1) * w.H * w.D * 2 * es + w.H * w.D * es * 2 * 2 + w.H * w.D * 4 * 2
+    per_layer = ((t - 1) * w.H * w.D * 2 * es + w.H * w.D * es * 2 * 2 + w.HQ * w.D * 4 * 2
                  + ((t + w.P - 1) // w.P) * 4)
     return w.layers * per_layer
 
@@ -536,12 +538,13 @@ def run_gpu_serial(args):
     w = make_workload(args.workload, rank)
     t = int(w.seq_lens[0])
     dt = "f32" if w.elem_bytes == 4 else "bf16"
-    pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dt, w.max_context, w.seed)
+    pool = pkv.Pool(w.layers, w.pool_pages, w.H, w.D, w.P, dt, w.max_context, w.seed,
+                    query_heads=w.HQ)
     req = pool.request()
-    out = torch.empty((w.H, w.D), dtype=torch.float32, device="cuda")
+    out = torch.empty((w.HQ, w.D), dtype=torch.float32, device="cuda")
 
     def layer_inputs(pos):
-        return [(to_device(synth.lane_rows(w.seed, Q, l, 0, w.H, pos, w.D, F32)),
+        return [(to_device(synth.lane_rows(w.seed, Q, l, 0, w.HQ, pos, w.D, F32)),
                  to_device(synth.lane_rows(w.seed, KHIST, l, 0, w.H, pos, w.D, w.dtype)),
                  to_device(synth.lane_rows(w.seed, VHIST, l, 0, w.H, pos, w.D, w.dtype)))
                 for l in range(w.layers)]
@@ -620,8 +623,8 @@ def run_gpu_serial(args):
             n = x.numel() * x.element_size()
             hin[o:o + n].copy_(x.reshape(-1).view(torch.uint8).cpu())
     din = torch.empty(pos_b, dtype=torch.uint8, device="cuda")
-    hout = torch.empty((w.layers, w.H, w.D), dtype=torch.float32).pin_memory()
-    outs = torch.empty((w.layers, w.H, w.D), dtype=torch.float32, device="cuda")
+    hout = torch.empty((w.layers, w.HQ, w.D), dtype=torch.float32).pin_memory()
+    outs = torch.empty((w.layers, w.HQ, w.D), dtype=torch.float32, device="cuda")
     eptrs = [tuple(ctypes.c_void_p(din.data_ptr() + o) for o in row) for row in offs]
     optrs = [ctypes.c_void_p(outs[l].data_ptr()) for l in range(w.layers)]
 

@@ -63,6 +63,13 @@ def single(t: int = 2048, seed: int = 1) -> Workload:
                     np.array([t], dtype=np.int32))
 
 
+def single_gqa(t: int = 2048, seed: int = 8) -> Workload:
+    """1 request, 32 layers, 8 KV heads x 4 query heads, d_h=128, bf16, pool of 4096
+    shuffled pages (a grouped-query model decoding alone)."""
+    return Workload(f"single_gqa_t{t}", 1, 32, 8, 128, 16, BF16, 4096, 4096, seed,
+                    np.array([t], dtype=np.int32), group=4)
+
+
 def batched(dtype: int = BF16, seed: int = 2, B: int = 64, t_max: int = 4096) -> Workload:
     """64 requests, 1 layer, H=32, d_h=128, t ~ U{1..4096}, pool of 32768 pages."""
     rng = np.random.default_rng(seed)
@@ -180,6 +187,7 @@ REGISTRY = {
     "single_t128": lambda: single(128),
     "single_t512": lambda: single(512),
     "single_t2048": lambda: single(2048),
+    "single_gqa_t2048": lambda: single_gqa(2048),
     "batched_f32": lambda: batched(F32),
     "batched_bf16": lambda: batched(BF16),
     "ragged": ragged,

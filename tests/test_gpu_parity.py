@@ -115,19 +115,24 @@ def test_single_request_serial(t):
     assert max(errs) <= FP32_ATOL
 
 
-@pytest.mark.parametrize("H,D,dtype,window,t", [
-    (4, 64, F32, 0, 900),       # 57 tiles per lane: 56 workers, a cluster of 7 CTAs
-    (4, 64, F32, 700, 900),     # a window of 700 positions: 44-45 tiles, clusters of 5 CTAs
-    (2, 128, BF16, 0, 520),     # bf16 rows of 128: 33 tiles, a cluster of 4 CTAs
-    (6, 64, F32, 0, 200),       # 13 tiles: 8 workers inside one CTA
+@pytest.mark.parametrize("H,D,dtype,window,t,group", [
+    (4, 64, F32, 0, 900, 1),       # 57 tiles per lane: 56 workers, a cluster of 7 CTAs
+    (4, 64, F32, 700, 900, 1),     # a window of 700 positions: 44-45 tiles, clusters of 5 CTAs
+    (2, 128, BF16, 0, 520, 1),     # bf16 rows of 128: 33 tiles, a cluster of 4 CTAs
+    (6, 64, F32, 0, 200, 1),       # 13 tiles: 8 workers inside one CTA
+    # grouped-query pools on the tensor-core kernel (bf16, partials of G rows)
+    (8, 128, BF16, 0, 520, 4),     # 33 tiles: a cluster of 4 CTAs per KV head
+    (4, 64, BF16, 300, 700, 8),    # a window: 19-20 tiles, clusters of 2 CTAs
+    (2, 128, BF16, 0, 200, 2),     # 13 tiles: 8 workers inside one CTA
 ])
-def test_single_request_lane_geometries(H, D, dtype, window, t):
+def test_single_request_lane_geometries(H, D, dtype, window, t, group):
     """Single requests whose lanes split over every worker count the launch picks:
-    inside one CTA, and clusters of 4, 5 and 7 CTAs (the two-level merge), with and
-    without a sliding window; checked against the oracle at lengths where the lane
-    geometry changes."""
+    inside one CTA, and clusters of 2 to 7 CTAs (the two-level merge), with and
+    without a sliding window, on both split kernels; checked against the oracle at
+    lengths where the lane geometry changes."""
     checks = {1, 16, 17, 129, t // 2, t - 1, t}
-    _, errs = _serial(2, H, D, dtype, 512, 1024, t, 3, check_at=checks, window=window)
+    _, errs = _serial(2, H, D, dtype, 512, 1024, t, 3, check_at=checks, window=window,
+                      group=group)
     assert errs
 
 
