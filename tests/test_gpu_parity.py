@@ -124,6 +124,8 @@ def test_single_request_serial(t):
     (8, 128, BF16, 0, 520, 4),     # 33 tiles: a cluster of 4 CTAs per KV head
     (4, 64, BF16, 300, 700, 8),    # a window: 19-20 tiles, clusters of 2 CTAs
     (2, 128, BF16, 0, 200, 2),     # 13 tiles: 8 workers inside one CTA
+    (2, 64, F32, 0, 4200, 1),      # 263 tiles: past 4 a worker, the global merge
+    (2, 64, F32, 1000, 4200, 1),   # the same length in a window of 1000: clusters again
 ])
 def test_single_request_lane_geometries(H, D, dtype, window, t, group):
     """Single requests whose lanes split over every worker count the launch picks:
@@ -131,7 +133,7 @@ def test_single_request_lane_geometries(H, D, dtype, window, t, group):
     without a sliding window, on both split kernels; checked against the oracle at
     lengths where the lane geometry changes."""
     checks = {1, 16, 17, 129, t // 2, t - 1, t}
-    _, errs = _serial(2, H, D, dtype, 512, 1024, t, 3, check_at=checks, window=window,
+    _, errs = _serial(2, H, D, dtype, 512, max(1024, t), t, 3, check_at=checks, window=window,
                       group=group)
     assert errs
 
