@@ -30,7 +30,7 @@ print(json.dumps(dict(line=line, same=line["config"] == want,
 """
 
 
-@pytest.mark.parametrize("workload", ["single_t128", "prefix_bf16"])
+@pytest.mark.parametrize("workload", ["single_t128", "single_gqa_t2048", "prefix_bf16"])
 def test_reference_arm_config_and_no_library(workload):
     r = subprocess.run([sys.executable, "-c", PROBE.format(root=ROOT, wl=workload)],
                        capture_output=True, text=True, timeout=600, cwd=ROOT)
